@@ -1,0 +1,198 @@
+/*
+ * mgemm.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts grouped GEMM.
+ *
+ * The hot path computes gmm(x, w, group_sizes): M token rows of x, stored
+ * contiguously by expert (group e owns rows [offsets[e], offsets[e+1])), are
+ * multiplied by per-expert weights w[E, K, N]; the group sizes stay in device
+ * memory and no call ever waits on the host.  Sources, cited per entry point
+ * below:
+ *   [GRB]  "Support GPU-resident batch sizes" (tgale96/grouped_gemm PR #21):
+ *          description and benchmark script; review of
+ *          csrc/fill_arguments.cuh and csrc/grouped_gemm.cu.
+ *   [SPM]  "F8I4 Grouped Gemm Optimization for Sparse M" (pytorch/FBGEMM PR
+ *          #3854), Summary.
+ *   [FP8]  "[moe training] Optimize FP8 MoE backward pass: fused colwise
+ *          kernel + AMD tuning" (pytorch/ao commit 34322b5): commit message and
+ *          bench_colwise_block_configs.py (_colwise_kernel, run_experiment).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is a DEVICE pointer owned by the caller; the
+ *     library allocates nothing, keeps no reference after the call returns and
+ *     never synchronizes: work is enqueued on `stream` (0 = legacy default).
+ *   - Return value: MGEMM_OK (0) when the work was enqueued, or a negative
+ *     MGEMM_E* code when a host-side check failed; then nothing is launched.
+ *   - Errors found on the device (bad group sizes, a wait that timed out) are
+ *     written to the int32 `status` word at the start of the args block (see
+ *     below).  Every kernel that takes an args block reads `status` first and
+ *     writes nothing when it is non-zero.  The caller reads the word whenever
+ *     it chooses to synchronize.
+ *   - Matrices are dense and row-major unless stated; "[R, C]" means R rows of
+ *     C elements with row stride C.  bf16 is IEEE bfloat16 (2 bytes), fp8 is
+ *     OCP/NVIDIA e4m3fn (1 byte, max 448, no infinities), scales are float32.
+ *   - Base pointers must be 16-byte aligned and row strides multiples of 16
+ *     bytes (the tensor-memory-accelerator rule): K and N multiples of 8 for
+ *     bf16 operands, of 16 for fp8 operands.  1 <= E <= MGEMM_MAX_EXPERTS.
+ *     M < 2^31.  Violations return MGEMM_EALIGN / MGEMM_EINVAL.
+ */
+#ifndef MGEMM_H_
+#define MGEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st *mgemm_stream_t;
+
+/* Host-side return codes. */
+#define MGEMM_OK 0
+#define MGEMM_EINVAL (-1)   /* null pointer, bad size, bad dtype/flag */
+#define MGEMM_EALIGN (-2)   /* pointer or stride breaks the 16-byte rule */
+#define MGEMM_ETOOMANY (-3) /* E > MGEMM_MAX_EXPERTS */
+#define MGEMM_ECUDA (-4)    /* a CUDA runtime/driver call failed (launch, tensor map) */
+#define MGEMM_ENOTSUP (-5)  /* combination not provided (e.g. fp8 with w stored [E,K,N] in mgemm_fwd) */
+
+/* Device-side status codes, written to args->status. */
+#define MGEMM_STATUS_OK 0
+#define MGEMM_STATUS_NEGATIVE_SIZE 1 /* some group_sizes[e] < 0 */
+#define MGEMM_STATUS_SUM_MISMATCH 2  /* sum of group_sizes != M */
+#define MGEMM_STATUS_TIMEOUT 4       /* a pipeline wait in a GEMM gave up (about 1 s) */
+
+/* Operand types for the GEMM entry points. */
+#define MGEMM_BF16 0
+#define MGEMM_FP8_E4M3 1
+
+/* One thread per expert in the single-CTA fill kernel [GRB description]. */
+#define MGEMM_MAX_EXPERTS 1024
+/* Rows per output tile; the fill kernel's tile prefix counts tiles of this height. */
+#define MGEMM_TILE_M 128
+
+/*
+ * Args block: a device buffer of mgemm_args_bytes(E) bytes, 16-byte aligned,
+ * written by mgemm_fill_args and read by every other entry point that takes
+ * `args`.  Byte layout (E = number of experts):
+ *   [0]   int32  status        MGEMM_STATUS_*
+ *   [4]   int32  n_active      number of non-empty groups (<= min(M, E))
+ *   [8]   int32  E
+ *   [12]  int32  reserved (0)
+ *   [16]  int64  M
+ *   [24]  int64  offsets[E+1]  exclusive prefix sum of group_sizes
+ *   [A]   int32  active[E]     ids of the non-empty groups, ascending (first n_active valid)
+ *   [T]   int32  mtile_start[E+1]  prefix over active groups of ceil(m_e / MGEMM_TILE_M)
+ *   [W]   int32  wgrad_order[E]    all experts by m_e descending, ties by ascending id
+ * with A = 24 + 8(E+1), T = A + 4E, W = T + 4(E+1); mgemm_args_layout returns them.
+ */
+size_t mgemm_args_bytes(int E);
+int mgemm_args_layout(int E, size_t *off_offsets, size_t *off_active, size_t *off_mtile_start,
+                      size_t *off_wgrad_order);
+
+/*
+ * mgemm_fill_args -- turn device-resident group sizes into the args block.
+ * [GRB description]: a single-threadblock kernel converts the batch sizes that
+ * live on the GPU into GEMM arguments, removing the GPU->CPU->GPU roundtrip;
+ * [GRB review, fill_arguments.cuh]: the block scan, and the sort of problems
+ * by k descending when k is dynamic (wgrad_order here); [SPM Summary]: only
+ * the min(total_M, groups) non-empty groups are scheduled (active, mtile_start).
+ *   group_sizes  int64[E], device; group_sizes[e] rows belong to expert e
+ *   E            number of experts, 1..MGEMM_MAX_EXPERTS
+ *   M            total rows the caller expects (checked on the device)
+ *   args         device buffer of mgemm_args_bytes(E) bytes (output)
+ * One launch of one CTA.  Invalid sizes set status 1 or 2 (the other fields
+ * are then unspecified).
+ */
+int mgemm_fill_args(const int64_t *group_sizes, int E, int64_t M, void *args, mgemm_stream_t stream);
+
+/*
+ * mgemm_quant_rowwise -- fused per-row absmax scale and saturating e4m3 cast.
+ * [FP8 commit message]: replaces tensor_to_scale(A, axiswise_dim=-1),
+ * A_scaled = A.to(float32) * A_scales, A_fp8 = to_fp8_saturated(A_scaled) by
+ * one launch.  Per row r: amax = max_c |in[r, c]|;
+ * s = 2^floor(log2(fp32(448 / max(amax, 1e-12)))) (the scale rule of
+ * _colwise_kernel, applied per row); out[r, c] = e4m3_rne_sat(in[r, c] * s).
+ *   in      bf16 [R, C] with row stride ld_in elements (ld_in >= C, ld_in % 8 == 0)
+ *   out     fp8  [R, C] with row stride ld_out bytes (ld_out >= C, ld_out % 16 == 0)
+ *   scales  float32 [R]
+ * C % 8 == 0.  R == 0 or C == 0 launches nothing.
+ */
+int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t ld_in, uint8_t *out, int64_t ld_out,
+                        float *scales, mgemm_stream_t stream);
+
+/*
+ * mgemm_quant_colwise_grouped -- per-group, per-column scale and e4m3 cast,
+ * column-major output; optionally two tensors in one launch (dual form).
+ * [FP8 _colwise_kernel]: for group g (rows offsets[g]..offsets[g+1]) and
+ * column c, amax over the group's rows, the same power-of-two scale rule, the
+ * scale stored at index c + C * g, the cast clamp(x * s) -> e4m3;
+ * [FP8 run_experiment]: the output is column-major (strides (1, M));
+ * [FP8 commit message]: the dual kernel quantizes grad_output and A together.
+ *   args        args block from mgemm_fill_args (group offsets, status)
+ *   E, M        experts and rows (must match the args block)
+ *   in1         bf16 [M, C1] row-major
+ *   out1        fp8 column-major: out1[c * M + r] holds row r, column c  (C1 * M bytes)
+ *   sc1         float32 [E * C1], sc1[c + C1 * g]
+ *   in2/out2/sc2/C2  the second tensor; in2 == NULL selects the single form
+ * C1, C2 % 8 == 0.  Empty groups get scale 2^48 (amax 0) and no data.
+ */
+int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, const void *in1, int64_t C1,
+                                uint8_t *out1, float *sc1, const void *in2, int64_t C2, uint8_t *out2,
+                                float *sc2, mgemm_stream_t stream);
+
+/*
+ * mgemm_fwd -- out[r, :] = x[r, :] . w[e(r)] for every row r of every non-empty group.
+ * [GRB benchmark script]: gmm(x, w, batch_sizes) with x[M, K], w[E, K, N];
+ * [GRB review, grouped_gemm.cu]: the trans_b variant (w stored [E, N, K]);
+ * [SPM Summary]: only non-empty groups are visited; [FP8 commit message]:
+ * FP8 operands are A * scale, so the product is divided by the scales.
+ *   dtype == MGEMM_BF16:
+ *     x bf16 [M, K]; w bf16 [E, K, N] (trans_b = 0) or [E, N, K] (trans_b = 1);
+ *     sx, sw ignored (may be NULL); out bf16 [M, N] (fp32 accumulation, RNE).
+ *   dtype == MGEMM_FP8_E4M3 (trans_b must be 1):
+ *     x fp8 [M, K] + sx float32 [M]; w fp8 [E, N, K] + sw float32 [E * N];
+ *     out[r, n] = bf16( sum_k x[r,k] w[e,n,k] / (sx[r] * sw[e*N + n]) ).
+ * Rows of empty groups do not exist; no other memory is written.
+ */
+int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
+              const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream);
+
+/*
+ * mgemm_dgrad -- grad_x[r, :] = grad_out[r, :] . w[e(r)]^T (the backward pass
+ * of gmm w.r.t. x).  [GRB benchmark script]: out.sum().backward();
+ * [GRB review, grouped_gemm.cu]: the trans_b template; [FP8 commit message]:
+ * grad_output is quantized rowwise for grad_A.
+ *   grad_out  bf16 [M, N] (or fp8 [M, N] + sgo float32 [M])
+ *   w         bf16 [E, K, N] (or fp8 [E, K, N] + sw float32 [E * K], one scale per (e, k))
+ *   grad_x    bf16 [M, K]
+ */
+int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,
+                const float *sw, void *grad_x, int64_t M, int K, int N, int E, mgemm_stream_t stream);
+
+/*
+ * mgemm_wgrad -- grad_w[e] = x_e^T . grad_out_e, contracting over the m_e rows
+ * of group e ("dynamic k"); grad_w[e] = 0 when m_e = 0.
+ * [GRB review, fill_arguments.cuh]: problems sorted by k descending;
+ * [GRB review, ZeroOutK0Outputs]: k = 0 problems produce zeros;
+ * [FP8 commit message]: grad_B uses per-group colwise scales of grad_output and A.
+ *   dtype == MGEMM_BF16: x bf16 [M, K], grad_out bf16 [M, N] (row-major).
+ *   dtype == MGEMM_FP8_E4M3: x fp8 column-major (x[c * M + r]) + sx float32
+ *     [E * K]; grad_out fp8 column-major + sgo float32 [E * N] (the outputs of
+ *     mgemm_quant_colwise_grouped); M % 16 == 0.
+ *   grad_w    bf16 [E, K, N]; every element is written.
+ */
+int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, const void *grad_out,
+                const float *sgo, void *grad_w, int64_t M, int K, int N, int E, mgemm_stream_t stream);
+
+/* Number of SMs of the current device (the persistent GEMM grid size), or < 0 on error. */
+int mgemm_num_sms(void);
+/* Static string naming a MGEMM_E* or MGEMM_STATUS_* code. */
+const char *mgemm_error_string(int code);
+/* Library ABI version (major * 100 + minor). */
+int mgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MGEMM_H_ */

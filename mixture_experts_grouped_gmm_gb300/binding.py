@@ -1,0 +1,148 @@
+"""Thin Python binding of libmgemm.so (the C ABI in include/mgemm.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the GPU (or None), passes their data pointers, sizes and the current
+CUDA stream to the C entry point of the same name, and raises
+``MgemmError`` on a negative return code.  No arithmetic of the path happens
+here, and there is no fallback: if the library is missing the first call
+raises.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmgemm.so")
+
+MGEMM_OK = 0
+MGEMM_BF16 = 0
+MGEMM_FP8_E4M3 = 1
+MGEMM_MAX_EXPERTS = 1024
+MGEMM_TILE_M = 128
+STATUS = {0: "ok", 1: "negative group size", 2: "group sizes do not sum to M", 4: "pipeline wait timed out"}
+
+_lib = None
+
+
+class MgemmError(RuntimeError):
+    pass
+
+
+_SIGS = {
+    "mgemm_args_bytes": (ctypes.c_size_t, [ctypes.c_int]),
+    "mgemm_args_layout": (ctypes.c_int, [ctypes.c_int] + [ctypes.POINTER(ctypes.c_size_t)] * 4),
+    "mgemm_fill_args": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                                       ctypes.c_void_p]),
+    "mgemm_quant_rowwise": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
+    "mgemm_quant_colwise_grouped": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "mgemm_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "mgemm_dgrad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "mgemm_wgrad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "mgemm_num_sms": (ctypes.c_int, []),
+    "mgemm_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mgemm_version": (ctypes.c_int, []),
+}
+
+
+def lib():
+    """Load libmgemm.so once (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MgemmError(f"{LIB_PATH} is missing; build it with mixture_experts_grouped_gmm_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t=None):
+    dev = t.device if t is not None else None
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _check(rc, what):
+    if rc != MGEMM_OK:
+        raise MgemmError(f"{what} failed: {rc} ({lib().mgemm_error_string(rc).decode()})")
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise MgemmError("mgemm kernels take device tensors only")
+
+
+def mgemm_args_bytes(E):
+    return int(lib().mgemm_args_bytes(int(E)))
+
+
+def mgemm_args_layout(E):
+    vals = [ctypes.c_size_t() for _ in range(4)]
+    _check(lib().mgemm_args_layout(int(E), *[ctypes.byref(v) for v in vals]), "mgemm_args_layout")
+    return dict(zip(("offsets", "active", "mtile_start", "wgrad_order"), (v.value for v in vals)))
+
+
+def mgemm_fill_args(group_sizes, E, M, args):
+    _cuda(group_sizes, args)
+    _check(lib().mgemm_fill_args(_p(group_sizes), int(E), int(M), _p(args), _stream(args)), "mgemm_fill_args")
+
+
+def mgemm_quant_rowwise(inp, out, scales):
+    _cuda(inp, out, scales)
+    R, C = inp.shape
+    _check(lib().mgemm_quant_rowwise(_p(inp), R, C, inp.stride(0), _p(out), out.stride(0), _p(scales),
+                                     _stream(inp)), "mgemm_quant_rowwise")
+
+
+def mgemm_quant_colwise_grouped(args, E, M, in1, out1, sc1, in2=None, out2=None, sc2=None):
+    _cuda(args, in1, out1, sc1, in2, out2, sc2)
+    C2 = in2.shape[1] if in2 is not None else 0
+    _check(lib().mgemm_quant_colwise_grouped(_p(args), int(E), int(M), _p(in1), in1.shape[1], _p(out1), _p(sc1),
+                                             _p(in2), C2, _p(out2), _p(sc2), _stream(in1)),
+           "mgemm_quant_colwise_grouped")
+
+
+def mgemm_fwd(args, dtype, trans_b, x, sx, w, sw, out, M, K, N, E):
+    _cuda(args, x, sx, w, sw, out)
+    _check(lib().mgemm_fwd(_p(args), int(dtype), int(trans_b), _p(x), _p(sx), _p(w), _p(sw), _p(out), int(M),
+                           int(K), int(N), int(E), _stream(out)), "mgemm_fwd")
+
+
+def mgemm_dgrad(args, dtype, grad_out, sgo, w, sw, grad_x, M, K, N, E):
+    _cuda(args, grad_out, sgo, w, sw, grad_x)
+    _check(lib().mgemm_dgrad(_p(args), int(dtype), _p(grad_out), _p(sgo), _p(w), _p(sw), _p(grad_x), int(M),
+                             int(K), int(N), int(E), _stream(grad_x)), "mgemm_dgrad")
+
+
+def mgemm_wgrad(args, dtype, x, sx, grad_out, sgo, grad_w, M, K, N, E):
+    _cuda(args, x, sx, grad_out, sgo, grad_w)
+    _check(lib().mgemm_wgrad(_p(args), int(dtype), _p(x), _p(sx), _p(grad_out), _p(sgo), _p(grad_w), int(M),
+                             int(K), int(N), int(E), _stream(grad_w)), "mgemm_wgrad")
+
+
+def mgemm_num_sms():
+    return int(lib().mgemm_num_sms())
+
+
+def args_status(args):
+    """Read the device status word (synchronizes the args tensor's stream)."""
+    return int(args[:4].view(torch.int32).item())

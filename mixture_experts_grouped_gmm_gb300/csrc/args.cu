@@ -1,0 +1,167 @@
+// mgemm_fill_args: device group sizes -> args block, in one CTA.
+//
+// "Support GPU-resident batch sizes" (tgale96/grouped_gemm PR #21): a
+// single-threadblock kernel replaces the host roundtrip of the batch sizes;
+// one thread per expert (<= 1024); a block scan over the sizes; problems sorted
+// by k descending when k is dynamic.  "F8I4 Grouped Gemm Optimization for
+// Sparse M" (FBGEMM PR #3854): only the non-empty groups are scheduled.
+//
+// This kernel: warp-shuffle block scans (int64 offsets, int32 compaction and
+// tile prefix), and a rank sort for the wgrad order (each thread counts the
+// experts that precede it: larger size, or equal size and smaller id), which is
+// deterministic and needs no temporary storage.  The block size is bucketed by
+// E (32, 128, 1024 threads) since the cost of a single-CTA kernel grows with
+// its thread count.
+#include <stdio.h>
+
+#include "common.cuh"
+
+namespace mgemm {
+
+template <typename T, int NT>
+__device__ __forceinline__ T block_inclusive_scan(T v, T *warp_tot) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (NW == 1) return v;
+  if (lane == 31) warp_tot[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    T s = lane < NW ? warp_tot[lane] : T(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    if (lane < NW) warp_tot[lane] = s;
+  }
+  __syncthreads();
+  if (w > 0) v += warp_tot[w - 1];
+  __syncthreads();
+  return v;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict__ sizes, int E, int64_t M,
+                                                       uint8_t *__restrict__ args) {
+  __shared__ int64_t s_size[NT];
+  __shared__ int64_t tot64[NT / 32 > 0 ? NT / 32 : 1];
+  __shared__ int tot32[NT / 32 > 0 ? NT / 32 : 1];
+  const ArgsLayout L = args_layout(E);
+  const int t = threadIdx.x;
+  const int64_t m = t < E ? sizes[t] : 0;
+  s_size[t] = m;
+  const int any_neg = __syncthreads_or(m < 0);
+
+  // exclusive offsets: offsets[t + 1] = inclusive prefix
+  const int64_t incl = block_inclusive_scan<int64_t, NT>(m, tot64);
+  int64_t *offsets = (int64_t *)(args + L.offsets);
+  if (t == 0) offsets[0] = 0;
+  if (t < E) offsets[t + 1] = incl;
+  __shared__ int64_t total_sh;
+  if (t == E - 1) total_sh = incl;
+
+  // compaction of non-empty groups and their row-tile prefix
+  const int flag = (t < E && m > 0) ? 1 : 0;
+  const int pos = block_inclusive_scan<int, NT>(flag, tot32);
+  const int tiles = flag ? (int)((m + MGEMM_TILE_M - 1) / MGEMM_TILE_M) : 0;
+  const int tile_incl = block_inclusive_scan<int, NT>(tiles, tot32);
+  int *active = (int *)(args + L.active);
+  int *mtile_start = (int *)(args + L.mtile_start);
+  if (t == 0) mtile_start[0] = 0;
+  if (flag) {
+    active[pos - 1] = t;
+    mtile_start[pos] = tile_incl;
+  }
+  __shared__ int n_active_sh;
+  if (t == E - 1) n_active_sh = pos;
+  __syncthreads();
+
+  // wgrad order: rank = #{j : m_j > m_t} + #{j < t : m_j == m_t}
+  if (t < E) {
+    int rank = 0;
+    for (int j = 0; j < E; ++j) {
+      const int64_t mj = s_size[j];
+      rank += (mj > m) || (mj == m && j < t);
+    }
+    ((int *)(args + L.wgrad_order))[rank] = t;
+  }
+  if (t == 0) {
+    int st = MGEMM_STATUS_OK;
+    if (any_neg)
+      st = MGEMM_STATUS_NEGATIVE_SIZE;
+    else if (total_sh != M)
+      st = MGEMM_STATUS_SUM_MISMATCH;
+    int *hdr = (int *)args;
+    hdr[0] = st;
+    hdr[1] = n_active_sh;
+    hdr[2] = E;
+    hdr[3] = 0;
+    *(int64_t *)(args + 16) = M;
+  }
+}
+
+}  // namespace mgemm
+
+using namespace mgemm;
+
+extern "C" size_t mgemm_args_bytes(int E) {
+  if (E < 1 || E > MGEMM_MAX_EXPERTS) return 0;
+  return args_layout(E).bytes;
+}
+
+extern "C" int mgemm_args_layout(int E, size_t *off_offsets, size_t *off_active, size_t *off_mtile_start,
+                                 size_t *off_wgrad_order) {
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  ArgsLayout L = args_layout(E);
+  if (off_offsets) *off_offsets = L.offsets;
+  if (off_active) *off_active = L.active;
+  if (off_mtile_start) *off_mtile_start = L.mtile_start;
+  if (off_wgrad_order) *off_wgrad_order = L.wgrad_order;
+  return MGEMM_OK;
+}
+
+extern "C" int mgemm_fill_args(const int64_t *group_sizes, int E, int64_t M, void *args, mgemm_stream_t stream) {
+  if (!group_sizes || !args) return MGEMM_EINVAL;
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  if (M < 0 || M >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  if (((uintptr_t)args & 15) || ((uintptr_t)group_sizes & 7)) return MGEMM_EALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (E <= 32)
+    fill_args_kernel<32><<<1, 32, 0, s>>>(group_sizes, E, M, (uint8_t *)args);
+  else if (E <= 128)
+    fill_args_kernel<128><<<1, 128, 0, s>>>(group_sizes, E, M, (uint8_t *)args);
+  else
+    fill_args_kernel<1024><<<1, 1024, 0, s>>>(group_sizes, E, M, (uint8_t *)args);
+  return cudaGetLastError() == cudaSuccess ? MGEMM_OK : MGEMM_ECUDA;
+}
+
+extern "C" int mgemm_num_sms(void) {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MGEMM_ECUDA;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MGEMM_ECUDA;
+  return n;
+}
+
+extern "C" const char *mgemm_error_string(int code) {
+  switch (code) {
+    case MGEMM_OK: return "ok";
+    case MGEMM_EINVAL: return "invalid argument";
+    case MGEMM_EALIGN: return "pointer or stride not 16-byte aligned";
+    case MGEMM_ETOOMANY: return "too many experts";
+    case MGEMM_ECUDA: return "CUDA call failed";
+    case MGEMM_ENOTSUP: return "combination not supported";
+    case MGEMM_STATUS_NEGATIVE_SIZE: return "device status: negative group size";
+    case MGEMM_STATUS_SUM_MISMATCH: return "device status: group sizes do not sum to M";
+    case MGEMM_STATUS_TIMEOUT: return "device status: pipeline wait timed out";
+    default: return "unknown code";
+  }
+}
+
+extern "C" int mgemm_version(void) { return 100; }

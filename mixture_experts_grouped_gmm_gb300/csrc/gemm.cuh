@@ -1,0 +1,403 @@
+// Persistent grouped GEMM on sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Computes, over the tile schedule that mgemm_fill_args wrote:
+//   kRows mode (forward, dgrad):   out[r, n] = sum_k A[r, k] B_e(r)[n, k]
+//       one tile = 128 token rows of one non-empty group x 256 output
+//       columns; tiles of empty groups do not exist ("F8I4 Grouped Gemm
+//       Optimization for Sparse M", Summary).
+//   kExperts mode (wgrad):         out_e[k, n] = sum_{r in group e} A[r, k] G[r, n]
+//       one tile = 128 rows of K x 256 columns of N of expert e, contracting
+//       over the rows of group e ("dynamic k"); experts are visited in the
+//       order sorted by group size, largest first, and empty experts get a
+//       zero tile with no main loop ("Support GPU-resident batch sizes",
+//       review of csrc/fill_arguments.cuh and ZeroOutK0Outputs).
+//
+// CTA layout (192 threads, one CTA per SM, grid = number of SMs, tiles
+// strided by gridDim.x):
+//   warp 0      TMA producer: one thread fills a 4-stage ring of
+//               (A 128 x 128 B, B 256 x 128 B) shared-memory tiles, 128-byte
+//               swizzled, each stage guarded by a full/empty mbarrier pair.
+//   warp 1      TMEM owner and MMA issuer: allocates 512 TMEM columns (two
+//               128 x 256 fp32 accumulators), one thread issues
+//               tcgen05.mma (M=128, N=256, K=16 bf16 / 32 e4m3) per 32-byte
+//               K step and commits stage release / accumulator-ready events.
+//               On a tile whose contraction range does not cover the whole
+//               block (wgrad group edges), the warp first zeroes the
+//               out-of-group rows in shared memory.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane =
+//               one output row per thread), optional FP8 scale division,
+//               bf16 rounding, row/column-predicated global stores.  The
+//               second accumulator lets the next tile's main loop run during
+//               this tile's epilogue.
+// Every mbarrier wait is bounded (about 1 s); on expiry the kernel records
+// MGEMM_STATUS_TIMEOUT in the args block, lets the other roles leave their
+// loops, drains its own outstanding copies and MMAs, frees TMEM and returns.
+#pragma once
+
+#include "common.cuh"
+
+namespace mgemm {
+
+enum { kModeRows = 0, kModeExperts = 1 };
+
+template <bool kFp8, bool kAMn, bool kBMn, int kMode>
+struct GemmCfg {
+  static constexpr bool Fp8 = kFp8;
+  static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
+  static constexpr bool BMn = kBMn;
+  static constexpr int Mode = kMode;
+  static constexpr int BM = 128, BN = 256;
+  static constexpr int ESIZE = kFp8 ? 1 : 2;
+  static constexpr int BK = 128 / ESIZE;  // contraction elements per stage (one 128-byte row)
+  static constexpr int UK = 32 / ESIZE;   // contraction elements per MMA
+  static constexpr int KSTEPS = BK / UK;  // 4
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGES = 4;
+  static constexpr int CHUNK = 64 * 128;  // MN-major: one 64-element x BK-row block (8 KB)
+  static constexpr uint32_t IDESC = make_idesc(kFp8 ? 0u : 1u, kAMn, kBMn, BM, BN);
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int THREADS = 192;
+  static constexpr size_t SMEM_BYTES =
+      1024 /*align slack*/ + (size_t)STAGES * (A_BYTES + B_BYTES) + 256 /*barriers, flags*/;
+};
+
+struct GemmParams {
+  const uint8_t *args;
+  int E;
+  int n_tiles;      // ceil(Nout / BN)
+  int mt_k;         // kExperts: ceil(Kout / BM)
+  int Kc;           // kRows: contraction length
+  int Nout;         // output columns
+  int Kout;         // kExperts: output rows per expert
+  __nv_bfloat16 *out;
+  const float *rscale;  // FP8: per output row (indexed by out_row0 + r)
+  const float *cscale;  // FP8: per (expert, column): cscale[e * Nout + col]
+};
+
+struct TileInfo {
+  int e, kb_count, a_row, n0, x0, lo, hi, out_row0, out_rows;
+};
+
+template <class C>
+__device__ __forceinline__ int total_tiles(const GemmParams &p, const ArgsView &av) {
+  if (C::Mode == kModeRows) {
+    const int na = *av.n_active;
+    return av.mtile_start[na] * p.n_tiles;
+  }
+  return p.E * p.mt_k * p.n_tiles;
+}
+
+template <class C>
+__device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, const ArgsView &av) {
+  TileInfo ti;
+  const int nt = t % p.n_tiles;
+  ti.n0 = nt * C::BN;
+  if (C::Mode == kModeRows) {
+    const int gm = t / p.n_tiles;
+    int lo = 0, hi = *av.n_active - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(av.mtile_start + mid) <= gm) lo = mid; else hi = mid - 1;
+    }
+    ti.e = __ldg(av.active + lo);
+    const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
+    const int row0 = (int)rs + (gm - __ldg(av.mtile_start + lo)) * C::BM;
+    ti.kb_count = (p.Kc + C::BK - 1) / C::BK;
+    ti.a_row = row0;
+    ti.out_row0 = row0;
+    ti.out_rows = (int)min((int64_t)C::BM, re - row0);
+    ti.x0 = 0; ti.lo = 0; ti.hi = 0;
+  } else {
+    const int per_e = p.mt_k * p.n_tiles;
+    const int i = t / per_e;
+    const int mk = (t % per_e) / p.n_tiles;
+    ti.e = __ldg(av.wgrad_order + i);
+    const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
+    ti.x0 = C::Fp8 ? (int)(rs & ~(int64_t)15) : (int)rs;  // fp8: TMA inner coordinate on 16 bytes
+    ti.lo = (int)(rs - ti.x0);
+    ti.hi = (int)(re - ti.x0);
+    ti.kb_count = re > rs ? (ti.hi + C::BK - 1) / C::BK : 0;
+    ti.a_row = mk * C::BM;
+    ti.out_row0 = ti.e * p.Kout + mk * C::BM;
+    ti.out_rows = min(C::BM, p.Kout - mk * C::BM);
+  }
+  return ti;
+}
+
+// Zero the contraction positions outside [lo, hi) of one stage (positions are
+// relative to the block start).  Executed by all 32 lanes of the MMA warp.
+template <class C>
+__device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int lo, int hi, int lane) {
+  if (C::AMn) {
+    // MN-major: contraction positions are rows of 128 bytes in each 64-wide chunk
+    const int nA = C::BM / 64, nB = C::BN / 64;
+    const int nrows = C::BK;
+    for (int idx = lane; idx < (nA + nB) * nrows; idx += 32) {
+      const int ch = idx / nrows, p = idx % nrows;
+      if (p >= lo && p < hi) continue;
+      uint8_t *base = ch < nA ? sa + ch * C::CHUNK : sb + (ch - nA) * C::CHUNK;
+      uint4 *row = reinterpret_cast<uint4 *>(base + p * 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) row[j] = make_uint4(0, 0, 0, 0);
+    }
+  } else {
+    // K-major, 128-byte swizzle: row r holds 8 16-byte chunks, physical chunk
+    // pc carries logical contraction chunk pc ^ (r & 7).
+    constexpr int EPC = 16 / C::ESIZE;  // elements per 16-byte chunk
+    const int rows = C::BM + C::BN;
+    for (int idx = lane; idx < rows * 8; idx += 32) {
+      const int r = idx >> 3, pc = idx & 7;
+      const int lc = pc ^ (r & 7);
+      const int p0 = lc * EPC, p1 = p0 + EPC;
+      if (p0 >= lo && p1 <= hi) continue;
+      uint8_t *rowp = r < C::BM ? sa + r * 128 : sb + (r - C::BM) * 128;
+      uint8_t *ck = rowp + pc * 16;
+      if (p1 <= lo || p0 >= hi) {
+        *reinterpret_cast<uint4 *>(ck) = make_uint4(0, 0, 0, 0);
+      } else {
+        for (int j = 0; j < EPC; ++j) {
+          const int p = p0 + j;
+          if (p < lo || p >= hi)
+            for (int b = 0; b < C::ESIZE; ++b) ck[j * C::ESIZE + b] = 0;
+        }
+      }
+    }
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    mgemm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_BYTES);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *tfull = empty + C::STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ArgsView av(p.args, p.E);
+  if (*av.status != 0) return;
+  const int total = total_tiles<C>(p, av);
+  if ((int)blockIdx.x >= total) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  volatile int *vabort = abort_flag;
+
+  // Producer bookkeeping kept for the drain after an abort.
+  uint32_t issued = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < total && !*vabort; t += gridDim.x) {
+        const TileInfo ti = decode_tile<C>(t, p, av);
+        for (int kb = 0; kb < ti.kb_count; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, vabort)) {
+            set_status(av.status, MGEMM_STATUS_TIMEOUT);
+            *vabort = 1;
+            break;
+          }
+          uint8_t *a = sA + stage * C::A_BYTES;
+          uint8_t *b = sB + stage * C::B_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
+          ++issued;
+          if (C::Mode == kModeRows) {
+            tma_load_2d(a, &tmA, &full[stage], kb * C::BK, ti.a_row);
+            if (C::BMn) {
+#pragma unroll
+              for (int j = 0; j < C::BN / 64; ++j)
+                tma_load_3d(b + j * C::CHUNK, &tmB, &full[stage], ti.n0 + 64 * j, kb * C::BK, ti.e);
+            } else {
+              tma_load_3d(b, &tmB, &full[stage], kb * C::BK, ti.n0, ti.e);
+            }
+          } else {
+            const int xr = ti.x0 + kb * C::BK;
+            if (C::AMn) {
+#pragma unroll
+              for (int j = 0; j < C::BM / 64; ++j) tma_load_2d(a + j * C::CHUNK, &tmA, &full[stage], ti.a_row + 64 * j, xr);
+#pragma unroll
+              for (int j = 0; j < C::BN / 64; ++j) tma_load_2d(b + j * C::CHUNK, &tmB, &full[stage], ti.n0 + 64 * j, xr);
+            } else {
+              tma_load_2d(a, &tmA, &full[stage], xr, ti.a_row);
+              tma_load_2d(b, &tmB, &full[stage], xr, ti.n0);
+            }
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C>(t, p, av);
+      if (ti.kb_count == 0) continue;
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1, vabort)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * C::BN;
+      for (int kb = 0; kb < ti.kb_count; ++kb) {
+        if (!mbar_wait(&full[stage], phase, vabort)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t *a = sA + stage * C::A_BYTES;
+        uint8_t *b = sB + stage * C::B_BYTES;
+        if (C::Mode == kModeExperts) {
+          const int lo = ti.lo - kb * C::BK, hi = ti.hi - kb * C::BK;
+          if (lo > 0 || hi < C::BK) {
+            mask_stage<C>(a, b, lo, hi, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          const uint32_t abase = smem_u32(a), bbase = smem_u32(b);
+#pragma unroll
+          for (int k = 0; k < C::KSTEPS; ++k) {
+            const uint64_t ad = C::AMn ? smem_desc_sw128(abase + k * C::UK * 128, C::CHUNK, 1024)
+                                       : smem_desc_sw128(abase + k * 32, 16, 1024);
+            const uint64_t bd = C::BMn ? smem_desc_sw128(bbase + k * C::UK * 128, C::CHUNK, 1024)
+                                       : smem_desc_sw128(bbase + k * 32, 16, 1024);
+            if (C::Fp8)
+              mma_f8(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+            else
+              mma_f16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+          }
+          mma_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&tfull[acc]);
+      __syncwarp();
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    if (!ok) {
+      if (lane == 0) set_status(av.status, MGEMM_STATUS_TIMEOUT);
+      *vabort = 1;
+    }
+    // all MMAs this thread issued have completed before TMEM is released
+    if (lane == 0) {
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C>(t, p, av);
+      const bool row_ok = r < ti.out_rows;
+      __nv_bfloat16 *orow = p.out + (int64_t)(ti.out_row0 + r) * p.Nout;
+      if (ti.kb_count == 0) {
+        if (row_ok) {
+          for (int c = ti.n0; c < ti.n0 + C::BN && c < p.Nout; c += 8)
+            *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      float rinv = 1.f;
+      if (C::Fp8 && row_ok) rinv = 1.f / __ldg(p.rscale + ti.out_row0 + r);
+      if (!mbar_wait(&tfull[acc], acc_phase, vabort)) {
+        set_status(av.status, MGEMM_STATUS_TIMEOUT);
+        *vabort = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::BN;
+#pragma unroll 1
+      for (int c = 0; c < C::BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, v);
+        tmem_ld_wait();
+        const int col0 = ti.n0 + c * 32;
+        float cinv = 1.f;  // lane j holds the column scale of column col0 + j
+        if (C::Fp8 && col0 + lane < p.Nout) cinv = 1.f / __ldg(p.cscale + (int64_t)ti.e * p.Nout + col0 + lane);
+        if (row_ok && col0 < p.Nout) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float f0 = __uint_as_float(v[2 * j]), f1 = __uint_as_float(v[2 * j + 1]);
+            if (C::Fp8) {
+              f0 = f0 * rinv * __shfl_sync(0xffffffffu, cinv, 2 * j);
+              f1 = f1 * rinv * __shfl_sync(0xffffffffu, cinv, 2 * j + 1);
+            }
+            __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+            pk[j] = *reinterpret_cast<uint32_t *>(&h);
+          }
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + col0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (col0 + 8 * j < p.Nout) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  // teardown: every role has left its loop
+  tc_fence_before();
+  __syncthreads();
+  if (*vabort && warp == 0 && lane == 0) {
+    // wait for the TMA copies this CTA issued, bounded
+    for (int s = 0; s < C::STAGES; ++s) {
+      const uint32_t armed = issued / C::STAGES + ((uint32_t)s < issued % C::STAGES ? 1u : 0u);
+      if (armed) mbar_wait(&full[s], (armed - 1) & 1, nullptr);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace mgemm

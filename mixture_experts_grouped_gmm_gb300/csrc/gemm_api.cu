@@ -1,0 +1,206 @@
+// Entry points mgemm_fwd / mgemm_dgrad / mgemm_wgrad: argument checks,
+// tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry
+// point, so the library needs no link-time libcuda), grid sizing and dispatch.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm_launch.cuh"
+
+using namespace mgemm;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tiled map with 128-byte swizzle and zero fill outside the tensor.
+// dims[0] is the contiguous dimension; strides are in bytes for dims 1..rank-1.
+bool make_map(CUtensorMap *m, bool fp8, int rank, const void *base, const uint64_t *dims,
+              const uint64_t *strides, const uint32_t *box) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const uint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r =
+      enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (!cached[dev]) cached[dev] = mgemm_num_sms();
+  return cached[dev];
+}
+
+int common_checks(const void *args, int dtype, int64_t M, int K, int N, int E) {
+  if (!args) return MGEMM_EINVAL;
+  if (dtype != MGEMM_BF16 && dtype != MGEMM_FP8_E4M3) return MGEMM_EINVAL;
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  if (M < 0 || M >= (int64_t(1) << 31) || K <= 0 || N <= 0) return MGEMM_EINVAL;
+  if (!aligned16(args)) return MGEMM_EALIGN;
+  const int kmul = dtype == MGEMM_FP8_E4M3 ? 16 : 8;
+  if (K % kmul || N % kmul) return MGEMM_EALIGN;
+  return MGEMM_OK;
+}
+
+int grid_for(int64_t tiles_upper) {
+  const int sms = sm_count();
+  if (sms <= 0) return -1;
+  return (int)(tiles_upper < sms ? tiles_upper : sms);
+}
+
+}  // namespace
+
+extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
+                         const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
+  int rc = common_checks(args, dtype, M, K, N, E);
+  if (rc) return rc;
+  if (!x || !w || !out) return MGEMM_EINVAL;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(out)) return MGEMM_EALIGN;
+  const bool fp8 = dtype == MGEMM_FP8_E4M3;
+  if (fp8 && !trans_b) return MGEMM_ENOTSUP;
+  if (fp8 && (!sx || !sw)) return MGEMM_EINVAL;
+  if (M == 0) return MGEMM_OK;
+  const uint64_t es = fp8 ? 1 : 2;
+  const uint32_t bk = fp8 ? 128 : 64;
+  CUtensorMap ta, tb;
+  {
+    const uint64_t d[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t st[1] = {(uint64_t)K * es};
+    const uint32_t box[2] = {bk, 128};
+    if (!make_map(&ta, fp8, 2, x, d, st, box)) return MGEMM_ECUDA;
+  }
+  if (trans_b) {  // w [E, N, K]
+    const uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
+    const uint64_t st[2] = {(uint64_t)K * es, (uint64_t)N * K * es};
+    const uint32_t box[3] = {bk, 256, 1};
+    if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
+  } else {  // w [E, K, N], loaded as 64-column MN-major chunks
+    const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
+    const uint64_t st[2] = {(uint64_t)N * es, (uint64_t)K * N * es};
+    const uint32_t box[3] = {64, bk, 1};
+    if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
+  }
+  GemmParams p{};
+  p.args = (const uint8_t *)args;
+  p.E = E;
+  p.n_tiles = (N + 255) / 256;
+  p.Kc = K;
+  p.Nout = N;
+  p.out = (__nv_bfloat16 *)out;
+  p.rscale = sx;
+  p.cscale = sw;
+  const int64_t upper = ((M + 127) / 128 + (M < E ? M : E)) * p.n_tiles;
+  const int grid = grid_for(upper);
+  if (grid < 0) return MGEMM_ECUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (fp8) return gemm_fp8_rows(ta, tb, p, grid, s);
+  return trans_b ? gemm_bf16_rows_bk(ta, tb, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, p, grid, s);
+}
+
+extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,
+                           const float *sw, void *grad_x, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
+  int rc = common_checks(args, dtype, M, K, N, E);
+  if (rc) return rc;
+  if (!grad_out || !w || !grad_x) return MGEMM_EINVAL;
+  if (!aligned16(grad_out) || !aligned16(w) || !aligned16(grad_x)) return MGEMM_EALIGN;
+  const bool fp8 = dtype == MGEMM_FP8_E4M3;
+  if (fp8 && (!sgo || !sw)) return MGEMM_EINVAL;
+  if (M == 0) return MGEMM_OK;
+  const uint64_t es = fp8 ? 1 : 2;
+  const uint32_t bk = fp8 ? 128 : 64;
+  CUtensorMap ta, tb;
+  {  // grad_out [M, N], contraction over N
+    const uint64_t d[2] = {(uint64_t)N, (uint64_t)M};
+    const uint64_t st[1] = {(uint64_t)N * es};
+    const uint32_t box[2] = {bk, 128};
+    if (!make_map(&ta, fp8, 2, grad_out, d, st, box)) return MGEMM_ECUDA;
+  }
+  {  // w [E, K, N]: output column k, contraction n contiguous
+    const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
+    const uint64_t st[2] = {(uint64_t)N * es, (uint64_t)K * N * es};
+    const uint32_t box[3] = {bk, 256, 1};
+    if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
+  }
+  GemmParams p{};
+  p.args = (const uint8_t *)args;
+  p.E = E;
+  p.n_tiles = (K + 255) / 256;
+  p.Kc = N;
+  p.Nout = K;
+  p.out = (__nv_bfloat16 *)grad_x;
+  p.rscale = sgo;
+  p.cscale = sw;
+  const int64_t upper = ((M + 127) / 128 + (M < E ? M : E)) * p.n_tiles;
+  const int grid = grid_for(upper);
+  if (grid < 0) return MGEMM_ECUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  return fp8 ? gemm_fp8_rows(ta, tb, p, grid, s) : gemm_bf16_rows_bk(ta, tb, p, grid, s);
+}
+
+extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, const void *grad_out,
+                           const float *sgo, void *grad_w, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
+  int rc = common_checks(args, dtype, M, K, N, E);
+  if (rc) return rc;
+  if (!grad_w) return MGEMM_EINVAL;
+  if (M > 0 && (!x || !grad_out)) return MGEMM_EINVAL;
+  if (!aligned16(grad_w) || (M > 0 && (!aligned16(x) || !aligned16(grad_out)))) return MGEMM_EALIGN;
+  const bool fp8 = dtype == MGEMM_FP8_E4M3;
+  if (fp8 && (!sx || !sgo)) return MGEMM_EINVAL;
+  if (fp8 && M % 16) return MGEMM_EALIGN;
+  // With M == 0 every expert is empty: the kernel only writes zeros and never
+  // loads, so the maps just need a valid description of some memory.
+  const void *xa = M > 0 ? x : grad_w;
+  const void *ga = M > 0 ? grad_out : grad_w;
+  const uint64_t Mm = M > 0 ? (uint64_t)M : 16;
+  CUtensorMap ta, tb;
+  if (fp8) {
+    // column-major operands: x^T [K, M] and grad_out^T [N, M], contraction contiguous
+    const uint64_t da[2] = {Mm, (uint64_t)K}, db[2] = {Mm, (uint64_t)N};
+    const uint64_t st[1] = {Mm};
+    const uint32_t boxa[2] = {128, 128}, boxb[2] = {128, 256};
+    if (!make_map(&ta, true, 2, xa, da, st, boxa)) return MGEMM_ECUDA;
+    if (!make_map(&tb, true, 2, ga, db, st, boxb)) return MGEMM_ECUDA;
+  } else {
+    // row-major x [M, K] and grad_out [M, N], loaded as 64-column MN-major chunks of 64 rows
+    const uint64_t da[2] = {(uint64_t)K, Mm}, db[2] = {(uint64_t)N, Mm};
+    const uint64_t sta[1] = {(uint64_t)K * 2}, stb[1] = {(uint64_t)N * 2};
+    const uint32_t box[2] = {64, 64};
+    if (!make_map(&ta, false, 2, xa, da, sta, box)) return MGEMM_ECUDA;
+    if (!make_map(&tb, false, 2, ga, db, stb, box)) return MGEMM_ECUDA;
+  }
+  GemmParams p{};
+  p.args = (const uint8_t *)args;
+  p.E = E;
+  p.n_tiles = (N + 255) / 256;
+  p.mt_k = (K + 127) / 128;
+  p.Nout = N;
+  p.Kout = K;
+  p.out = (__nv_bfloat16 *)grad_w;
+  p.rscale = sx;
+  p.cscale = sgo;
+  const int64_t upper = (int64_t)E * p.mt_k * p.n_tiles;
+  if (upper >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  const int grid = grid_for(upper);
+  if (grid < 0) return MGEMM_ECUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  return fp8 ? gemm_fp8_experts(ta, tb, p, grid, s) : gemm_bf16_experts(ta, tb, p, grid, s);
+}

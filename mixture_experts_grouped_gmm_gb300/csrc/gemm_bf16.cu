@@ -1,0 +1,16 @@
+// bf16 instantiations of the persistent grouped GEMM (kind::f16 tensor cores).
+#include "gemm_launch.cuh"
+
+namespace mgemm {
+
+int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, true, kModeRows>>(a, b, p, grid, s);
+}
+int gemm_bf16_rows_bk(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows>>(a, b, p, grid, s);
+}
+int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, true, true, kModeExperts>>(a, b, p, grid, s);
+}
+
+}  // namespace mgemm

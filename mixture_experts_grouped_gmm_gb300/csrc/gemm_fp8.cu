@@ -1,0 +1,14 @@
+// e4m3 instantiations of the persistent grouped GEMM (kind::f8f6f4 tensor
+// cores, fp32 accumulation, power-of-two scales divided out in the epilogue).
+#include "gemm_launch.cuh"
+
+namespace mgemm {
+
+int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows>>(a, b, p, grid, s);
+}
+int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeExperts>>(a, b, p, grid, s);
+}
+
+}  // namespace mgemm

@@ -1,0 +1,35 @@
+// Host-side launch of one GemmCfg instantiation (shared by the bf16 and fp8
+// translation units) and the declarations the entry points call.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace mgemm {
+
+template <class C>
+int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MGEMM_ECUDA;
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(mgemm_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM_BYTES) != cudaSuccess)
+      return MGEMM_ECUDA;
+    attr_done[dev] = true;
+  }
+  mgemm_gemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, b, p);
+  return cudaGetLastError() == cudaSuccess ? MGEMM_OK : MGEMM_ECUDA;
+}
+
+// bf16: A K-major rows, B MN-major ([E, K, N] weights)
+int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+// bf16: A K-major rows, B K-major ([E, N, K] weights, or dgrad on [E, K, N])
+int gemm_bf16_rows_bk(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+// bf16 wgrad: both operands MN-major (row-major x and grad_out)
+int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+// fp8 forward / dgrad: both K-major, scaled epilogue
+int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+// fp8 wgrad: column-major quantized operands (K-major), scaled epilogue
+int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+
+}  // namespace mgemm

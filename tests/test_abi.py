@@ -1,0 +1,109 @@
+"""CPU-only checks of the C ABI: the library builds, loads without a GPU,
+exports every entry point include/mgemm.h declares, reports the documented
+args-block layout, and rejects bad arguments on the host before any CUDA call.
+Also checks that the product package never imports the oracle."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "mgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_grouped_gmm_gb300 import binding, build
+
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mgemm_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_six_hot_path_calls():
+    names = declared_functions()
+    for n in ("mgemm_fill_args", "mgemm_quant_rowwise", "mgemm_quant_colwise_grouped", "mgemm_fwd",
+              "mgemm_dgrad", "mgemm_wgrad"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(os.path.join(ROOT, "mixture_experts_grouped_gmm_gb300", "libmgemm.so"))
+    for n in declared_functions():
+        assert hasattr(raw, n), n
+
+
+def test_args_layout_matches_header(lib):
+    from mixture_experts_grouped_gmm_gb300 import binding as B
+
+    for E in (1, 4, 8, 64, 128, 1000, 1024):
+        lay = B.mgemm_args_layout(E)
+        A = 24 + 8 * (E + 1)
+        T = A + 4 * E
+        W = T + 4 * (E + 1)
+        assert lay == dict(offsets=24, active=A, mtile_start=T, wgrad_order=W)
+        nbytes = B.mgemm_args_bytes(E)
+        assert nbytes >= W + 4 * E and nbytes % 16 == 0
+    assert B.mgemm_args_bytes(0) == 0 and B.mgemm_args_bytes(1025) == 0
+
+
+def test_version_and_error_strings(lib):
+    assert lib.mgemm_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5, 1, 2, 4):
+        assert lib.mgemm_error_string(code).decode() != "unknown code"
+
+
+P = ctypes.c_void_p
+
+
+def test_host_checks_fill_args(lib):
+    good = P(0x10000)
+    assert lib.mgemm_fill_args(None, 4, 64, good, None) == -1
+    assert lib.mgemm_fill_args(good, 0, 64, good, None) == -1
+    assert lib.mgemm_fill_args(good, 1025, 64, good, None) == -3
+    assert lib.mgemm_fill_args(good, 4, -1, good, None) == -1
+    assert lib.mgemm_fill_args(good, 4, 64, P(0x10008), None) == -2   # args must be 16-byte aligned
+
+
+def test_host_checks_gemms(lib):
+    a, x, w, o = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    s = P(0x50000)
+    assert lib.mgemm_fwd(None, 0, 0, x, None, w, None, o, 64, 128, 256, 4, None) == -1
+    assert lib.mgemm_fwd(a, 7, 0, x, None, w, None, o, 64, 128, 256, 4, None) == -1        # dtype
+    assert lib.mgemm_fwd(a, 0, 0, x, None, w, None, o, 64, 130, 256, 4, None) == -2        # K % 8
+    assert lib.mgemm_fwd(a, 1, 1, x, s, w, s, o, 64, 136, 256, 4, None) == -2              # fp8 K % 16
+    assert lib.mgemm_fwd(a, 1, 0, x, s, w, s, o, 64, 128, 256, 4, None) == -5              # fp8 needs [E,N,K]
+    assert lib.mgemm_fwd(a, 1, 1, x, None, w, s, o, 64, 128, 256, 4, None) == -1           # scales required
+    assert lib.mgemm_fwd(a, 0, 0, P(0x20008), None, w, None, o, 64, 128, 256, 4, None) == -2
+    assert lib.mgemm_fwd(a, 0, 0, x, None, w, None, o, 64, 128, 256, 2000, None) == -3
+    assert lib.mgemm_fwd(a, 0, 0, x, None, w, None, o, 0, 128, 256, 4, None) == 0          # M = 0: nothing to do
+    assert lib.mgemm_dgrad(a, 0, x, None, w, None, None, 64, 128, 256, 4, None) == -1
+    assert lib.mgemm_wgrad(a, 1, x, s, w, s, o, 72, 128, 256, 4, None) == -2               # fp8 wgrad M % 16
+    assert lib.mgemm_wgrad(a, 0, x, None, w, None, None, 64, 128, 256, 4, None) == -1
+
+
+def test_host_checks_quant(lib):
+    i, o, s = P(0x10000), P(0x20000), P(0x30000)
+    assert lib.mgemm_quant_rowwise(i, 4, 12, 12, o, 16, s, None) == -1                    # C % 8
+    assert lib.mgemm_quant_rowwise(i, 4, 16, 16, o, 24, s, None) == -2                    # ld_out % 16
+    assert lib.mgemm_quant_rowwise(i, 0, 16, 16, o, 16, s, None) == 0                     # empty: no launch
+    assert lib.mgemm_quant_colwise_grouped(None, 4, 64, i, 64, o, s, None, 0, None, None, None) == -1
+    assert lib.mgemm_quant_colwise_grouped(i, 4, 64, i, 60, o, s, None, 0, None, None, None) == -1
+
+
+def test_product_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "mixture_experts_grouped_gmm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), f
+                assert "oracle/" not in src, f

@@ -1,0 +1,139 @@
+"""GPU parity of the FP8 quantize kernels against oracle.quant: bytes and
+scales must match bit for bit.  Includes every finite bf16 magnitude up to 448
+through the cast at several power-of-two scales, ragged and empty groups, the
+dual form with different widths, and strided rows."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.quant import quant_colwise_grouped, quant_rowwise
+from tests.helpers import new_args, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def B():
+    from mixture_experts_grouped_gmm_gb300 import binding
+
+    return binding
+
+
+def rowwise_gpu(x, ld_out=None):
+    R, C = x.shape
+    ld_out = ld_out or ((C + 15) // 16) * 16
+    out = torch.full((R, ld_out), 0xAB, dtype=torch.uint8, device=DEV)
+    sc = torch.empty(R, dtype=torch.float32, device=DEV)
+    B().mgemm_quant_rowwise(x, out, sc)
+    torch.cuda.synchronize()
+    return out, sc
+
+
+def check_rowwise(x):
+    out, sc = rowwise_gpu(x)
+    C = x.shape[1]
+    q, s = quant_rowwise(to_np(x))
+    assert np.array_equal(to_np(out)[:, :C], q)
+    assert np.array_equal(to_np(sc), s)
+    if out.shape[1] > C:
+        assert (to_np(out)[:, C:] == 0xAB).all()      # nothing written past C
+
+
+@pytest.mark.parametrize("R,C", [(1, 8), (64, 128), (33, 1408), (7, 2048), (5, 5120), (9, 6152), (3, 8200),
+                                 (300, 256), (2, 4096)])
+def test_rowwise_shapes(R, C):
+    g = torch.Generator(device=DEV).manual_seed(R * 1000 + C)
+    x = torch.randn(R, C, generator=g, device=DEV) * torch.exp2(torch.randint(-20, 20, (R, 1), generator=g,
+                                                                               device=DEV).float())
+    x = x.to(torch.bfloat16)
+    x[0] = 0                                            # all-zero row: scale 2^48, codes 0
+    check_rowwise(x)
+
+
+def test_rowwise_strided_rows():
+    g = torch.Generator(device=DEV).manual_seed(1)
+    big = torch.randn(40, 1000, generator=g, device=DEV).to(torch.bfloat16)
+    x = big[:, :768]                                    # row stride 1000 elements
+    out = torch.full((40, 800), 0xAB, dtype=torch.uint8, device=DEV)
+    sc = torch.empty(40, dtype=torch.float32, device=DEV)
+    B().mgemm_quant_rowwise(x, out[:, :768], sc)
+    torch.cuda.synchronize()
+    q, s = quant_rowwise(to_np(x))
+    assert np.array_equal(to_np(out)[:, :768], q) and (to_np(out)[:, 768:] == 0xAB).all()
+    assert np.array_equal(to_np(sc), s)
+
+
+@pytest.mark.parametrize("anchor", [448.0, 1.0, 2.0 ** -7, 2.0 ** 20])
+def test_cast_every_bf16_magnitude(anchor):
+    # every finite bf16 value v with |v| <= anchor, one row per 255 values plus
+    # the anchor, so the row scale is pow2floor(448 / anchor) and the cast sees v * s
+    bits = torch.from_numpy(np.arange(65536, dtype=np.uint16).view(np.int16))
+    v = bits.view(torch.bfloat16).float()
+    v = v[torch.isfinite(v) & (v.abs() <= anchor)]
+    n = (v.numel() + 254) // 255
+    rows = torch.full((n * 255,), 0.0)
+    rows[: v.numel()] = v
+    x = torch.cat([rows.view(n, 255), torch.full((n, 1), anchor)], dim=1)
+    x = torch.cat([x, torch.zeros(n, 256)], dim=1).to(torch.bfloat16).to(DEV)   # C = 512
+    check_rowwise(x)
+
+
+def colwise_case(sizes, C1, C2=None, seed=0):
+    E = len(sizes)
+    M = int(np.sum(sizes))
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    a1 = (torch.randn(M, C1, generator=g, device=DEV) * 3).to(torch.bfloat16)
+    gs = torch.tensor(sizes, dtype=torch.int64, device=DEV)
+    args = new_args(E, DEV)
+    B().mgemm_fill_args(gs, E, M, args)
+    o1 = torch.full((C1 * M,), 0xAB, dtype=torch.uint8, device=DEV)
+    s1 = torch.full((E * C1,), -1.0, dtype=torch.float32, device=DEV)
+    a2 = o2 = s2 = None
+    if C2:
+        a2 = (torch.randn(M, C2, generator=g, device=DEV) * 1e-3).to(torch.bfloat16)
+        o2 = torch.full((C2 * M,), 0xAB, dtype=torch.uint8, device=DEV)
+        s2 = torch.full((E * C2,), -1.0, dtype=torch.float32, device=DEV)
+    B().mgemm_quant_colwise_grouped(args, E, M, a1, o1, s1, a2, o2, s2)
+    torch.cuda.synchronize()
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    q1, r1 = quant_colwise_grouped(to_np(a1), offs)
+    assert np.array_equal(to_np(s1), r1)
+    assert np.array_equal(to_np(o1).reshape(C1, M), q1)
+    if C2:
+        q2, r2 = quant_colwise_grouped(to_np(a2), offs)
+        assert np.array_equal(to_np(s2), r2)
+        assert np.array_equal(to_np(o2).reshape(C2, M), q2)
+
+
+@pytest.mark.parametrize("sizes,C1,C2", [
+    ([64], 64, None),
+    ([10, 0, 30, 24], 128, None),          # M = 64, empty group
+    ([7, 0, 93], 72, None),                # M = 100: not a multiple of 16 (byte stores)
+    ([1, 200, 0, 55, 0, 0, 4], 200, 136),  # dual, different widths
+    ([300, 301, 3, 0, 420], 64, 64),       # dual, same widths, groups across 128-row chunks
+    ([0, 0, 0, 16], 8, 8),
+])
+def test_colwise(sizes, C1, C2):
+    colwise_case(sizes, C1, C2, seed=len(sizes) * 7 + C1)
+
+
+def test_colwise_large_groups_deepseek_like():
+    rng = np.random.default_rng(3)
+    sizes = rng.integers(0, 2000, 16)
+    sizes[[2, 9]] = 0
+    sizes[-1] += (16 - sizes.sum() % 16) % 16
+    colwise_case(sizes.tolist(), 256, 96, seed=11)
+
+
+def test_colwise_status_blocks_writes():
+    E, M, C = 3, 48, 64
+    gs = torch.tensor([16, -1, 33], dtype=torch.int64, device=DEV)
+    args = new_args(E, DEV)
+    B().mgemm_fill_args(gs, E, M, args)
+    a = torch.randn(M, C, device=DEV).to(torch.bfloat16)
+    o = torch.full((C * M,), 0xAB, dtype=torch.uint8, device=DEV)
+    s = torch.full((E * C,), -1.0, device=DEV)
+    B().mgemm_quant_colwise_grouped(args, E, M, a, o, s)
+    torch.cuda.synchronize()
+    assert (to_np(o) == 0xAB).all() and (to_np(s) == -1.0).all()
