@@ -188,6 +188,10 @@ int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, con
 int mgemm_num_sms(void);
 /* Static string naming a MGEMM_E* or MGEMM_STATUS_* code. */
 const char *mgemm_error_string(int code);
+/* Text describing the last CUDA failure that made a call return MGEMM_ECUDA
+ * in the calling thread ("" if none); static per-thread storage, valid until
+ * the next failing call from the same thread. */
+const char *mgemm_last_error(void);
 /* Library ABI version (major * 100 + minor). */
 int mgemm_version(void);
 

@@ -53,6 +53,7 @@ _SIGS = {
     "mgemm_num_sms": (ctypes.c_int, []),
     "mgemm_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mgemm_version": (ctypes.c_int, []),
+    "mgemm_last_error": (ctypes.c_char_p, []),
 }
 
 
@@ -82,7 +83,8 @@ def _stream(t=None):
 
 def _check(rc, what):
     if rc != MGEMM_OK:
-        raise MgemmError(f"{what} failed: {rc} ({lib().mgemm_error_string(rc).decode()})")
+        detail = lib().mgemm_last_error().decode() if rc == -4 else ""
+        raise MgemmError(f"{what} failed: {rc} ({lib().mgemm_error_string(rc).decode()}) {detail}")
 
 
 def _cuda(*ts):

@@ -44,6 +44,19 @@ def _inputs():
     return files
 
 
+def source_hash():
+    """sha256 over the CUDA sources and the header (identifies a kernel build)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in sorted(_inputs()):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(f).encode())
+            with open(f, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def up_to_date():
     if not os.path.exists(LIB_PATH):
         return False

@@ -105,9 +105,20 @@ __global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict
   }
 }
 
+namespace {
+thread_local char g_last_error[192] = "";
+}
+
+void note_error(const char *where, int code) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: error %d (%s)", where, code,
+           cudaGetErrorString((cudaError_t)code));
+}
+
 }  // namespace mgemm
 
 using namespace mgemm;
+
+extern "C" const char *mgemm_last_error(void) { return g_last_error; }
 
 extern "C" size_t mgemm_args_bytes(int E) {
   if (E < 1 || E > MGEMM_MAX_EXPERTS) return 0;
@@ -139,14 +150,15 @@ extern "C" int mgemm_fill_args(const int64_t *group_sizes, int E, int64_t M, voi
     fill_args_kernel<128><<<1, 128, 0, s>>>(group_sizes, E, M, (uint8_t *)args);
   else
     fill_args_kernel<1024><<<1, 1024, 0, s>>>(group_sizes, E, M, (uint8_t *)args);
-  return cudaGetLastError() == cudaSuccess ? MGEMM_OK : MGEMM_ECUDA;
+  return cuda_rc(cudaGetLastError(), "mgemm_fill_args launch");
 }
 
 extern "C" int mgemm_num_sms(void) {
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MGEMM_ECUDA;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MGEMM_ECUDA;
-  return n;
+  int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  rc = cuda_rc(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+  return rc ? rc : n;
 }
 
 extern "C" const char *mgemm_error_string(int code) {

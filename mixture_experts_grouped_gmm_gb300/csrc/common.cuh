@@ -12,6 +12,16 @@
 
 namespace mgemm {
 
+// ---------------------------------------------------------------- host errors
+// Records a failed CUDA call for mgemm_last_error() (per thread) and maps it
+// to MGEMM_ECUDA.
+void note_error(const char *where, int code);
+inline int cuda_rc(cudaError_t e, const char *where) {
+  if (e == cudaSuccess) return MGEMM_OK;
+  note_error(where, (int)e);
+  return MGEMM_ECUDA;
+}
+
 // ---------------------------------------------------------------- args block
 struct ArgsLayout {
   size_t offsets, active, mtile_start, wgrad_order, bytes;

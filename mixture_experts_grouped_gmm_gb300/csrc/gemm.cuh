@@ -356,18 +356,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int col0 = ti.n0 + c * 32;
         float cinv = 1.f;  // lane j holds the column scale of column col0 + j
         if (C::Fp8 && col0 + lane < p.Nout) cinv = 1.f / __ldg(p.cscale + (int64_t)ti.e * p.Nout + col0 + lane);
-        if (row_ok && col0 < p.Nout) {
-          uint32_t pk[16];
+        // every lane converts (the shuffles need the whole warp); only valid rows store
+        uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float f0 = __uint_as_float(v[2 * j]), f1 = __uint_as_float(v[2 * j + 1]);
-            if (C::Fp8) {
-              f0 = f0 * rinv * __shfl_sync(0xffffffffu, cinv, 2 * j);
-              f1 = f1 * rinv * __shfl_sync(0xffffffffu, cinv, 2 * j + 1);
-            }
-            __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
-            pk[j] = *reinterpret_cast<uint32_t *>(&h);
+        for (int j = 0; j < 16; ++j) {
+          float f0 = __uint_as_float(v[2 * j]), f1 = __uint_as_float(v[2 * j + 1]);
+          if (C::Fp8) {
+            f0 = f0 * rinv * __shfl_sync(0xffffffffu, cinv, 2 * j);
+            f1 = f1 * rinv * __shfl_sync(0xffffffffu, cinv, 2 * j + 1);
           }
+          __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+          pk[j] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        if (row_ok && col0 < p.Nout) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + col0);
 #pragma unroll
           for (int j = 0; j < 4; ++j)

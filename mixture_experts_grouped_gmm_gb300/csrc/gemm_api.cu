@@ -30,16 +30,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool make_map(CUtensorMap *m, bool fp8, int rank, const void *base, const uint64_t *dims,
               const uint64_t *strides, const uint32_t *box) {
   auto enc = encode_fn();
-  if (!enc) return false;
+  if (!enc) {
+    note_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", 0);
+    return false;
+  }
   const uint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r =
       enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) {
+    note_error("cuTensorMapEncodeTiled", (int)r);
+    return false;
+  }
+  return true;
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+// cuTensorMapEncodeTiled needs a current context.  A thread that has made no
+// CUDA call yet (for example an autograd worker) has none: make the current
+// device's primary context current, once per thread.
+int ensure_context() {
+  thread_local bool done = false;
+  if (done) return MGEMM_OK;
+  int dev = 0;
+  int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  rc = cuda_rc(cudaSetDevice(dev), "cudaSetDevice");
+  if (rc) return rc;
+  done = true;
+  return MGEMM_OK;
+}
 
 int sm_count() {
   static int cached[64] = {};
@@ -79,6 +101,7 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   if (fp8 && !trans_b) return MGEMM_ENOTSUP;
   if (fp8 && (!sx || !sw)) return MGEMM_EINVAL;
   if (M == 0) return MGEMM_OK;
+  if ((rc = ensure_context())) return rc;
   const uint64_t es = fp8 ? 1 : 2;
   const uint32_t bk = fp8 ? 128 : 64;
   CUtensorMap ta, tb;
@@ -125,6 +148,7 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   const bool fp8 = dtype == MGEMM_FP8_E4M3;
   if (fp8 && (!sgo || !sw)) return MGEMM_EINVAL;
   if (M == 0) return MGEMM_OK;
+  if ((rc = ensure_context())) return rc;
   const uint64_t es = fp8 ? 1 : 2;
   const uint32_t bk = fp8 ? 128 : 64;
   CUtensorMap ta, tb;
@@ -171,6 +195,7 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
   const void *xa = M > 0 ? x : grad_w;
   const void *ga = M > 0 ? grad_out : grad_w;
   const uint64_t Mm = M > 0 ? (uint64_t)M : 16;
+  if ((rc = ensure_context())) return rc;
   CUtensorMap ta, tb;
   if (fp8) {
     // column-major operands: x^T [K, M] and grad_out^T [N, M], contraction contiguous

@@ -10,15 +10,18 @@ template <class C>
 int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MGEMM_ECUDA;
+  int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 0 || dev >= 64) return MGEMM_EINVAL;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(mgemm_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::SMEM_BYTES) != cudaSuccess)
-      return MGEMM_ECUDA;
+    rc = cuda_rc(cudaFuncSetAttribute(mgemm_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)C::SMEM_BYTES),
+                 "cudaFuncSetAttribute");
+    if (rc) return rc;
     attr_done[dev] = true;
   }
   mgemm_gemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, b, p);
-  return cudaGetLastError() == cudaSuccess ? MGEMM_OK : MGEMM_ECUDA;
+  return cuda_rc(cudaGetLastError(), "grouped GEMM launch");
 }
 
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)

@@ -270,7 +270,7 @@ extern "C" int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t
   else if (nch <= 16) launch_rowwise<16>(x, R, C, ld_in, out, ld_out, scales, s);
   else if (nch <= 24) launch_rowwise<24>(x, R, C, ld_in, out, ld_out, scales, s);
   else launch_rowwise<0>(x, R, C, ld_in, out, ld_out, scales, s);
-  return cudaGetLastError() == cudaSuccess ? MGEMM_OK : MGEMM_ECUDA;
+  return cuda_rc(cudaGetLastError(), "mgemm_quant_rowwise launch");
 }
 
 extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, const void *in1, int64_t C1,
@@ -293,5 +293,5 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
   if (items >= (int64_t(1) << 31)) return MGEMM_EINVAL;
   quant_colwise_kernel<<<(unsigned)items, kColThreads, 0, (cudaStream_t)stream>>>((const uint8_t *)args, E, M,
                                                                                   t1, t2, vec_ok);
-  return cudaGetLastError() == cudaSuccess ? MGEMM_OK : MGEMM_ECUDA;
+  return cuda_rc(cudaGetLastError(), "mgemm_quant_colwise_grouped launch");
 }

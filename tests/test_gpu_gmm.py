@@ -160,29 +160,6 @@ def test_wgrad_all_groups_empty_writes_zeros():
     assert (to_np(gw) == 0).all()
 
 
-def test_autograd_gmm_matches_oracle():
-    from mixture_experts_grouped_gmm_gb300 import gmm
-
-    sizes, K, N = [0, 300, 1, 129, 250], 320, 520
-    M, E = int(np.sum(sizes)), len(sizes)
-    gs = torch.tensor(sizes, dtype=torch.int64, device=DEV)
-    for trans_b in (False, True):
-        x = rand_bf16((M, K), 11, "normal").requires_grad_(True)
-        w = rand_bf16((E, N, K) if trans_b else (E, K, N), 12, "normal").requires_grad_(True)
-        out = gmm(x, w, gs, trans_b=trans_b)
-        G = rand_bf16((M, N), 13, "normal")
-        out.backward(G)
-        torch.cuda.synchronize()
-        xs, ws, Gs = to_np(x), to_np(w), to_np(G)
-        wk = ws.transpose(0, 2, 1) if trans_b else ws            # [E, K, N]
-        assert_close(to_np(out), og.gmm_fwd(xs, wk, sizes), BF16_TOL, "autograd fwd")
-        assert_close(to_np(x.grad), og.gmm_dgrad(Gs, wk, sizes), BF16_TOL, "autograd dgrad")
-        gw = og.gmm_wgrad(xs, Gs, sizes)
-        if trans_b:
-            gw = gw.transpose(0, 2, 1)
-        assert_close(to_np(w.grad), gw, BF16_TOL, "autograd wgrad")
-
-
 # ----------------------------------------------------------------- FP8 path
 def quant_rows_gpu(t):
     R, C = t.shape
@@ -195,7 +172,7 @@ def quant_rows_gpu(t):
 FP8_CASES = [
     ([15, 16, 19, 14], 128, 256),
     ([5, 0, 37, 100, 2], 256, 272),           # M = 144; group starts off 16-row boundaries
-    ([0, 300, 1, 129, 250, 0, 0, 16], 320, 528),
+    ([0, 300, 1, 129, 250, 0, 0, 24], 320, 528),
     ([48], 512, 256),
 ]
 
@@ -248,3 +225,4 @@ def test_fp8_fwd_dgrad_wgrad(sizes, K, N):
     assert_close(got_w, ref_w, FP8_TOL, "fp8 wgrad")
     # the FP8 result also tracks the unquantized bf16 product (quantization error only)
     assert_close(to_np(out[:M]), og.gmm_fwd(xs, to_np(w_nk), sizes, trans_b=True), 0.1, "fp8 vs bf16 fwd")
+
