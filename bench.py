@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true", help="headline step only")
+    p.add_argument("--workload", choices=["all", "sparse", "deepseek", "mixtral"], default="all",
+                   help="'all': headline line with every block; otherwise run only that block (profiling)")
+    p.add_argument("--tokens", type=int, default=16384, help="DeepSeek-shaped block: tokens (x top-6 rows)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return p.parse_args()
 
@@ -218,10 +221,10 @@ def sparse_m_extra(torch, B, dev, pk):
     return res
 
 
-def deepseek_extra(torch, B, dev, pk):
+def deepseek_extra(torch, B, dev, pk, tokens=16384, reps=10):
     from mixture_experts_grouped_gmm_gb300 import workloads
 
-    d = workloads.deepseek(device=dev)
+    d = workloads.deepseek(device=dev, T=tokens)
     M, K, N, E = d["M"], d["K"], d["N"], d["E"]
     u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
     w_kn = d["w"]
@@ -252,10 +255,9 @@ def deepseek_extra(torch, B, dev, pk):
         mark(7); B.mgemm_wgrad(T["args"], 1, T["xqt"], T["sxc"], T["goqt"], T["sgoc"], T["gw"], M, K, N, E)
         mark(8)
 
-    for _ in range(3):
+    for _ in range(min(3, reps)):
         step()
     torch.cuda.synchronize()
-    reps = 10
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(reps)]
     for r in range(reps):
         step(evs[r])
@@ -341,6 +343,26 @@ def cpu_baseline_grin(seconds=10.0):
     return {"value": round(flops / dt / 1e12, 5), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
             "sample": f"{n} x (fwd+dgrad+wgrad) of one 128-row expert group (1/8 of the step), float64 numpy",
             "seconds": round(dt, 2)}
+
+
+def run_block(a):
+    """One secondary block alone (used for profiling a workload's kernels)."""
+    import torch
+
+    from mixture_experts_grouped_gmm_gb300 import binding as B
+    from mixture_experts_grouped_gmm_gb300 import build as _build
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    pk, _ = peaks()
+    if a.workload == "sparse":
+        out = sparse_m_extra(torch, B, dev, pk)
+    elif a.workload == "deepseek":
+        out = deepseek_extra(torch, B, dev, pk, tokens=a.tokens, reps=max(1, a.steps))
+    else:
+        out = mixtral_extra(torch, B, dev, pk)
+    print(json.dumps({"workload": a.workload, a.workload: out}), flush=True)
 
 
 def run_ours(a):
@@ -546,6 +568,8 @@ def main():
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.workload != "all":
+        run_block(a)
     else:
         run_ours(a)
 

@@ -2,33 +2,39 @@
 //
 // Computes, over the tile schedule that mgemm_fill_args wrote:
 //   kRows mode (forward, dgrad):   out[r, n] = sum_k A[r, k] B_e(r)[n, k]
-//       one tile = 128 token rows of one non-empty group x 256 output
-//       columns; tiles of empty groups do not exist ("F8I4 Grouped Gemm
-//       Optimization for Sparse M", Summary).
+//       one tile = 128 token rows of one non-empty group x BN output columns;
+//       tiles of empty groups do not exist ("F8I4 Grouped Gemm Optimization
+//       for Sparse M", Summary).
 //   kExperts mode (wgrad):         out_e[k, n] = sum_{r in group e} A[r, k] G[r, n]
-//       one tile = 128 rows of K x 256 columns of N of expert e, contracting
+//       one tile = 128 rows of K x BN columns of N of expert e, contracting
 //       over the rows of group e ("dynamic k"); experts are visited in the
 //       order sorted by group size, largest first, and empty experts get a
 //       zero tile with no main loop ("Support GPU-resident batch sizes",
 //       review of csrc/fill_arguments.cuh and ZeroOutK0Outputs).
+// BN (64, 128 or 256) is chosen per launch on the host to balance the tile
+// count against the number of SMs.
 //
 // CTA layout (192 threads, one CTA per SM, grid = number of SMs, tiles
 // strided by gridDim.x):
 //   warp 0      TMA producer: one thread fills a 4-stage ring of
-//               (A 128 x 128 B, B 256 x 128 B) shared-memory tiles, 128-byte
-//               swizzled, each stage guarded by a full/empty mbarrier pair.
+//               (A 128 rows x 128 B, B BN rows x 128 B) shared-memory tiles,
+//               128-byte swizzled, each stage guarded by a full/empty mbarrier.
 //   warp 1      TMEM owner and MMA issuer: allocates 512 TMEM columns (two
 //               128 x 256 fp32 accumulators), one thread issues
-//               tcgen05.mma (M=128, N=256, K=16 bf16 / 32 e4m3) per 32-byte
-//               K step and commits stage release / accumulator-ready events.
-//               On a tile whose contraction range does not cover the whole
-//               block (wgrad group edges), the warp first zeroes the
-//               out-of-group rows in shared memory.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane =
-//               one output row per thread), optional FP8 scale division,
-//               bf16 rounding, row/column-predicated global stores.  The
-//               second accumulator lets the next tile's main loop run during
-//               this tile's epilogue.
+//               tcgen05.mma (M=128, N=BN, K=16 bf16 / 32 e4m3) per 32-byte
+//               K step and commits stage-release / accumulator-ready events.
+//               On a wgrad tile whose contraction range does not cover the
+//               whole block (group edges) the warp first zeroes the
+//               out-of-group positions in shared memory.
+//   warps 2-5   epilogue, one TMEM lane quarter (32 output rows) each:
+//               tcgen05.ld, optional FP8 scale division, bf16 rounding, then
+//               a 128-byte-swizzled shared-memory staging buffer (two per
+//               warp) and a TMA store of each 32-row x 64-column block.  A
+//               warp whose 32 rows are not all valid (group edge) stores
+//               those rows directly instead, so nothing outside the tile's
+//               rows is ever written.  The accumulator is released right
+//               after its last tcgen05.ld, so the next tile's main loop
+//               overlaps the stores.
 // Every mbarrier wait is bounded (about 1 s); on expiry the kernel records
 // MGEMM_STATUS_TIMEOUT in the args block, lets the other roles leave their
 // loops, drains its own outstanding copies and MMAs, frees TMEM and returns.
@@ -46,26 +52,28 @@ struct GemmCfg {
   static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
   static constexpr bool BMn = kBMn;
   static constexpr int Mode = kMode;
-  static constexpr int BM = 128, BN = 256;
+  static constexpr int BM = 128, BN_MAX = 256;
   static constexpr int ESIZE = kFp8 ? 1 : 2;
   static constexpr int BK = 128 / ESIZE;  // contraction elements per stage (one 128-byte row)
   static constexpr int UK = 32 / ESIZE;   // contraction elements per MMA
   static constexpr int KSTEPS = BK / UK;  // 4
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_BYTES = BN_MAX * 128;
   static constexpr int STAGES = 4;
   static constexpr int CHUNK = 64 * 128;  // MN-major: one 64-element x BK-row block (8 KB)
-  static constexpr uint32_t IDESC = make_idesc(kFp8 ? 0u : 1u, kAMn, kBMn, BM, BN);
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = 2 * BN_MAX;
   static constexpr int THREADS = 192;
-  static constexpr size_t SMEM_BYTES =
-      1024 /*align slack*/ + (size_t)STAGES * (A_BYTES + B_BYTES) + 256 /*barriers, flags*/;
+  static constexpr int OUT_BUF = 32 * 128;  // 32 rows x 64 bf16 columns
+  static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * (A_BYTES + B_BYTES) +
+                                       4 * 2 * OUT_BUF /*epilogue staging*/ + 256 /*barriers, flags*/;
 };
 
 struct GemmParams {
   const uint8_t *args;
   int E;
-  int n_tiles;      // ceil(Nout / BN)
+  int bn;           // output tile width: 64, 128 or 256
+  uint32_t idesc;   // tcgen05 instruction descriptor for M=128, N=bn
+  int n_tiles;      // ceil(Nout / bn)
   int mt_k;         // kExperts: ceil(Kout / BM)
   int Kc;           // kRows: contraction length
   int Nout;         // output columns
@@ -92,7 +100,7 @@ template <class C>
 __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, const ArgsView &av) {
   TileInfo ti;
   const int nt = t % p.n_tiles;
-  ti.n0 = nt * C::BN;
+  ti.n0 = nt * p.bn;
   if (C::Mode == kModeRows) {
     const int gm = t / p.n_tiles;
     int lo = 0, hi = *av.n_active - 1;
@@ -128,10 +136,10 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
 // Zero the contraction positions outside [lo, hi) of one stage (positions are
 // relative to the block start).  Executed by all 32 lanes of the MMA warp.
 template <class C>
-__device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int lo, int hi, int lane) {
+__device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int bn, int lo, int hi, int lane) {
   if (C::AMn) {
     // MN-major: contraction positions are rows of 128 bytes in each 64-wide chunk
-    const int nA = C::BM / 64, nB = C::BN / 64;
+    const int nA = C::BM / 64, nB = bn / 64;
     const int nrows = C::BK;
     for (int idx = lane; idx < (nA + nB) * nrows; idx += 32) {
       const int ch = idx / nrows, p = idx % nrows;
@@ -145,7 +153,7 @@ __device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int lo, int
     // K-major, 128-byte swizzle: row r holds 8 16-byte chunks, physical chunk
     // pc carries logical contraction chunk pc ^ (r & 7).
     constexpr int EPC = 16 / C::ESIZE;  // elements per 16-byte chunk
-    const int rows = C::BM + C::BN;
+    const int rows = C::BM + bn;
     for (int idx = lane; idx < rows * 8; idx += 32) {
       const int r = idx >> 3, pc = idx & 7;
       const int lc = pc ^ (r & 7);
@@ -166,15 +174,21 @@ __device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int lo, int
   }
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     mgemm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const GemmParams p) {
+                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_BYTES);
+  uint8_t *sOut = sB + C::STAGES * C::B_BYTES;  // [4 warps][2 buffers][32 x 128 B]
+  uint64_t *full = reinterpret_cast<uint64_t *>(sOut + 4 * 2 * C::OUT_BUF);
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
@@ -202,6 +216,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -212,6 +227,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   volatile int *vabort = abort_flag;
+  const int bn = p.bn;
 
   // Producer bookkeeping kept for the drain after an abort.
   uint32_t issued = 0;
@@ -220,6 +236,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      const uint32_t tx = C::A_BYTES + bn * 128;
       for (int t = blockIdx.x; t < total && !*vabort; t += gridDim.x) {
         const TileInfo ti = decode_tile<C>(t, p, av);
         for (int kb = 0; kb < ti.kb_count; ++kb) {
@@ -230,13 +247,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           uint8_t *a = sA + stage * C::A_BYTES;
           uint8_t *b = sB + stage * C::B_BYTES;
-          mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
+          mbar_arrive_expect_tx(&full[stage], tx);
           ++issued;
           if (C::Mode == kModeRows) {
             tma_load_2d(a, &tmA, &full[stage], kb * C::BK, ti.a_row);
             if (C::BMn) {
-#pragma unroll
-              for (int j = 0; j < C::BN / 64; ++j)
+              for (int j = 0; j < bn / 64; ++j)
                 tma_load_3d(b + j * C::CHUNK, &tmB, &full[stage], ti.n0 + 64 * j, kb * C::BK, ti.e);
             } else {
               tma_load_3d(b, &tmB, &full[stage], kb * C::BK, ti.n0, ti.e);
@@ -245,9 +261,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int xr = ti.x0 + kb * C::BK;
             if (C::AMn) {
 #pragma unroll
-              for (int j = 0; j < C::BM / 64; ++j) tma_load_2d(a + j * C::CHUNK, &tmA, &full[stage], ti.a_row + 64 * j, xr);
-#pragma unroll
-              for (int j = 0; j < C::BN / 64; ++j) tma_load_2d(b + j * C::CHUNK, &tmB, &full[stage], ti.n0 + 64 * j, xr);
+              for (int j = 0; j < C::BM / 64; ++j)
+                tma_load_2d(a + j * C::CHUNK, &tmA, &full[stage], ti.a_row + 64 * j, xr);
+              for (int j = 0; j < bn / 64; ++j)
+                tma_load_2d(b + j * C::CHUNK, &tmB, &full[stage], ti.n0 + 64 * j, xr);
             } else {
               tma_load_2d(a, &tmA, &full[stage], xr, ti.a_row);
               tma_load_2d(b, &tmB, &full[stage], xr, ti.n0);
@@ -269,7 +286,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (ti.kb_count == 0) continue;
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1, vabort)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * C::BN;
+      const uint32_t d_tmem = tmem_base + acc * C::BN_MAX;
       for (int kb = 0; kb < ti.kb_count; ++kb) {
         if (!mbar_wait(&full[stage], phase, vabort)) { ok = false; break; }
         tc_fence_after();
@@ -278,7 +295,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (C::Mode == kModeExperts) {
           const int lo = ti.lo - kb * C::BK, hi = ti.hi - kb * C::BK;
           if (lo > 0 || hi < C::BK) {
-            mask_stage<C>(a, b, lo, hi, lane);
+            mask_stage<C>(a, b, bn, lo, hi, lane);
             fence_proxy_async_smem();
             __syncwarp();
           }
@@ -292,9 +309,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint64_t bd = C::BMn ? smem_desc_sw128(bbase + k * C::UK * 128, C::CHUNK, 1024)
                                        : smem_desc_sw128(bbase + k * 32, 16, 1024);
             if (C::Fp8)
-              mma_f8(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+              mma_f8(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
             else
-              mma_f16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+              mma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
           }
           mma_commit(&empty[stage]);
         }
@@ -323,65 +340,101 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     __syncwarp();
   } else {
-    // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
+    // epilogue warps 2..5 -> TMEM lane quarter q = warp % 4 -> tile rows 32q..32q+31
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    uint8_t *my_buf = sOut + (size_t)q * 2 * C::OUT_BUF;
+    int last_buf = -1;  // staging buffer read by this warp's most recent TMA store group
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_tile<C>(t, p, av);
+      const bool has_acc = ti.kb_count > 0;
       const bool row_ok = r < ti.out_rows;
+      const bool warp_full = q * 32 + 32 <= ti.out_rows;
       __nv_bfloat16 *orow = p.out + (int64_t)(ti.out_row0 + r) * p.Nout;
-      if (ti.kb_count == 0) {
-        if (row_ok) {
-          for (int c = ti.n0; c < ti.n0 + C::BN && c < p.Nout; c += 8)
-            *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0, 0, 0, 0);
-        }
-        continue;
-      }
       float rinv = 1.f;
-      if (C::Fp8 && row_ok) rinv = 1.f / __ldg(p.rscale + ti.out_row0 + r);
-      if (!mbar_wait(&tfull[acc], acc_phase, vabort)) {
-        set_status(av.status, MGEMM_STATUS_TIMEOUT);
-        *vabort = 1;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::BN;
-#pragma unroll 1
-      for (int c = 0; c < C::BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, v);
-        tmem_ld_wait();
-        const int col0 = ti.n0 + c * 32;
-        float cinv = 1.f;  // lane j holds the column scale of column col0 + j
-        if (C::Fp8 && col0 + lane < p.Nout) cinv = 1.f / __ldg(p.cscale + (int64_t)ti.e * p.Nout + col0 + lane);
-        // every lane converts (the shuffles need the whole warp); only valid rows store
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float f0 = __uint_as_float(v[2 * j]), f1 = __uint_as_float(v[2 * j + 1]);
-          if (C::Fp8) {
-            f0 = f0 * rinv * __shfl_sync(0xffffffffu, cinv, 2 * j);
-            f1 = f1 * rinv * __shfl_sync(0xffffffffu, cinv, 2 * j + 1);
-          }
-          __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
-          pk[j] = *reinterpret_cast<uint32_t *>(&h);
+      if (C::Fp8 && row_ok && has_acc) rinv = 1.f / __ldg(p.rscale + ti.out_row0 + r);
+      if (has_acc) {
+        if (!mbar_wait(&tfull[acc], acc_phase, vabort)) {
+          set_status(av.status, MGEMM_STATUS_TIMEOUT);
+          *vabort = 1;
+          break;
         }
-        if (row_ok && col0 < p.Nout) {
+        tc_fence_after();
+      }
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::BN_MAX;
+      const int nchunks = bn / 64;
+#pragma unroll 1
+      for (int c = 0; c < nchunks; ++c) {
+        const int col0 = ti.n0 + c * 64;
+        uint32_t pk[32];
+        if (has_acc) {
+          uint32_t v[32], w[32];
+          tmem_ld_32x32b_x32(taddr + c * 64, v);
+          tmem_ld_32x32b_x32(taddr + c * 64 + 32, w);
+          tmem_ld_wait();
+          if (c == nchunks - 1) {  // accumulator fully read: hand it back to the MMA warp
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+          float cinv0 = 1.f, cinv1 = 1.f;  // lane j: scales of columns col0 + j and col0 + 32 + j
+          if (C::Fp8) {
+            if (col0 + lane < p.Nout) cinv0 = 1.f / __ldg(p.cscale + (int64_t)ti.e * p.Nout + col0 + lane);
+            if (col0 + 32 + lane < p.Nout)
+              cinv1 = 1.f / __ldg(p.cscale + (int64_t)ti.e * p.Nout + col0 + 32 + lane);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float f0 = __uint_as_float(v[2 * j]), f1 = __uint_as_float(v[2 * j + 1]);
+            float g0 = __uint_as_float(w[2 * j]), g1 = __uint_as_float(w[2 * j + 1]);
+            if (C::Fp8) {  // every lane takes part in the shuffles
+              f0 *= rinv * __shfl_sync(0xffffffffu, cinv0, 2 * j);
+              f1 *= rinv * __shfl_sync(0xffffffffu, cinv0, 2 * j + 1);
+              g0 *= rinv * __shfl_sync(0xffffffffu, cinv1, 2 * j);
+              g1 *= rinv * __shfl_sync(0xffffffffu, cinv1, 2 * j + 1);
+            }
+            pk[j] = pack_bf16x2(f0, f1);
+            pk[16 + j] = pack_bf16x2(g0, g1);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = 0u;
+        }
+        if (col0 >= p.Nout) continue;
+        if (warp_full) {
+          const int b = c & 1;
+          uint8_t *buf = my_buf + b * C::OUT_BUF;
+          if (lane == 0) {
+            if (last_buf == b) bulk_wait_read<0>(); else bulk_wait_read<1>();
+          }
+          __syncwarp();
+          uint8_t *rowp = buf + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4 *>(rowp + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmOut, buf, col0, ti.out_row0 + q * 32);
+            bulk_commit();
+          }
+          last_buf = b;
+        } else if (row_ok) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + col0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < 8; ++j)
             if (col0 + 8 * j < p.Nout) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
+      if (has_acc && ++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
       }
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // teardown: every role has left its loop

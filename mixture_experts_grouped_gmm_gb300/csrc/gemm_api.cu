@@ -89,6 +89,43 @@ int grid_for(int64_t tiles_upper) {
   return (int)(tiles_upper < sms ? tiles_upper : sms);
 }
 
+// Output tile width: the candidate with the fewest waves x (width + per-tile
+// overhead), where waves = ceil(estimated tiles / SMs); ties go to the wider
+// tile (better operand reuse in shared memory).  m_tiles_est is the host's
+// estimate of 128-row tiles (the exact count lives on the device).
+int choose_bn(int64_t m_tiles_est, int64_t n_cols) {
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  int best = 256;
+  int64_t best_cost = -1;
+  for (int bn : {256, 128, 64}) {
+    const int64_t tiles = m_tiles_est * ((n_cols + bn - 1) / bn);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const int64_t cost = waves * (bn + 64);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+// Rows-mode estimate of 128-row tiles: dense groups give about M/128, sparse
+// routing about one tile per touched group (at most min(M, E)).
+int64_t rows_tiles_estimate(int64_t M, int E) {
+  const int64_t dense = (M + 127) / 128;
+  const int64_t sparse = M < E ? M : E;
+  return dense > sparse ? dense : sparse;
+}
+
+// Map for the epilogue's TMA stores: the output viewed [rows, cols] bf16,
+// boxes of 32 rows x 64 columns, 128-byte swizzle.
+bool make_out_map(CUtensorMap *m, void *out, int64_t rows, int64_t cols) {
+  const uint64_t d[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint64_t st[1] = {(uint64_t)cols * 2};
+  const uint32_t box[2] = {64, 32};
+  return make_map(m, false, 2, out, d, st, box);
+}
+
 }  // namespace
 
 extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
@@ -111,10 +148,11 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
     const uint32_t box[2] = {bk, 128};
     if (!make_map(&ta, fp8, 2, x, d, st, box)) return MGEMM_ECUDA;
   }
+  const int bn = choose_bn(rows_tiles_estimate(M, E), N);
   if (trans_b) {  // w [E, N, K]
     const uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
     const uint64_t st[2] = {(uint64_t)K * es, (uint64_t)N * K * es};
-    const uint32_t box[3] = {bk, 256, 1};
+    const uint32_t box[3] = {bk, (uint32_t)bn, 1};
     if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
   } else {  // w [E, K, N], loaded as 64-column MN-major chunks
     const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
@@ -122,10 +160,14 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
     const uint32_t box[3] = {64, bk, 1};
     if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
   }
+  CUtensorMap to;
+  if (!make_out_map(&to, out, M, N)) return MGEMM_ECUDA;
   GemmParams p{};
   p.args = (const uint8_t *)args;
   p.E = E;
-  p.n_tiles = (N + 255) / 256;
+  p.bn = bn;
+  p.idesc = make_idesc(fp8 ? 0u : 1u, false, !trans_b, 128, bn);
+  p.n_tiles = (N + bn - 1) / bn;
   p.Kc = K;
   p.Nout = N;
   p.out = (__nv_bfloat16 *)out;
@@ -135,8 +177,8 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
   cudaStream_t s = (cudaStream_t)stream;
-  if (fp8) return gemm_fp8_rows(ta, tb, p, grid, s);
-  return trans_b ? gemm_bf16_rows_bk(ta, tb, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, p, grid, s);
+  if (fp8) return gemm_fp8_rows(ta, tb, to, p, grid, s);
+  return trans_b ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, to, p, grid, s);
 }
 
 extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,
@@ -158,16 +200,21 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
     const uint32_t box[2] = {bk, 128};
     if (!make_map(&ta, fp8, 2, grad_out, d, st, box)) return MGEMM_ECUDA;
   }
+  const int bn = choose_bn(rows_tiles_estimate(M, E), K);
   {  // w [E, K, N]: output column k, contraction n contiguous
     const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
     const uint64_t st[2] = {(uint64_t)N * es, (uint64_t)K * N * es};
-    const uint32_t box[3] = {bk, 256, 1};
+    const uint32_t box[3] = {bk, (uint32_t)bn, 1};
     if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
   }
+  CUtensorMap to;
+  if (!make_out_map(&to, grad_x, M, K)) return MGEMM_ECUDA;
   GemmParams p{};
   p.args = (const uint8_t *)args;
   p.E = E;
-  p.n_tiles = (K + 255) / 256;
+  p.bn = bn;
+  p.idesc = make_idesc(fp8 ? 0u : 1u, false, false, 128, bn);
+  p.n_tiles = (K + bn - 1) / bn;
   p.Kc = N;
   p.Nout = K;
   p.out = (__nv_bfloat16 *)grad_x;
@@ -177,7 +224,7 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
   cudaStream_t s = (cudaStream_t)stream;
-  return fp8 ? gemm_fp8_rows(ta, tb, p, grid, s) : gemm_bf16_rows_bk(ta, tb, p, grid, s);
+  return fp8 ? gemm_fp8_rows(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk(ta, tb, to, p, grid, s);
 }
 
 extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, const void *grad_out,
@@ -196,12 +243,14 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
   const void *ga = M > 0 ? grad_out : grad_w;
   const uint64_t Mm = M > 0 ? (uint64_t)M : 16;
   if ((rc = ensure_context())) return rc;
+  const int mt_k = (K + 127) / 128;
+  const int bn = choose_bn((int64_t)E * mt_k, N);
   CUtensorMap ta, tb;
   if (fp8) {
     // column-major operands: x^T [K, M] and grad_out^T [N, M], contraction contiguous
     const uint64_t da[2] = {Mm, (uint64_t)K}, db[2] = {Mm, (uint64_t)N};
     const uint64_t st[1] = {Mm};
-    const uint32_t boxa[2] = {128, 128}, boxb[2] = {128, 256};
+    const uint32_t boxa[2] = {128, 128}, boxb[2] = {128, (uint32_t)bn};
     if (!make_map(&ta, true, 2, xa, da, st, boxa)) return MGEMM_ECUDA;
     if (!make_map(&tb, true, 2, ga, db, st, boxb)) return MGEMM_ECUDA;
   } else {
@@ -212,11 +261,15 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
     if (!make_map(&ta, false, 2, xa, da, sta, box)) return MGEMM_ECUDA;
     if (!make_map(&tb, false, 2, ga, db, stb, box)) return MGEMM_ECUDA;
   }
+  CUtensorMap to;
+  if (!make_out_map(&to, grad_w, (int64_t)E * K, N)) return MGEMM_ECUDA;
   GemmParams p{};
   p.args = (const uint8_t *)args;
   p.E = E;
-  p.n_tiles = (N + 255) / 256;
-  p.mt_k = (K + 127) / 128;
+  p.bn = bn;
+  p.idesc = make_idesc(fp8 ? 0u : 1u, !fp8, !fp8, 128, bn);
+  p.n_tiles = (N + bn - 1) / bn;
+  p.mt_k = mt_k;
   p.Nout = N;
   p.Kout = K;
   p.out = (__nv_bfloat16 *)grad_w;
@@ -227,5 +280,5 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
   cudaStream_t s = (cudaStream_t)stream;
-  return fp8 ? gemm_fp8_experts(ta, tb, p, grid, s) : gemm_bf16_experts(ta, tb, p, grid, s);
+  return fp8 ? gemm_fp8_experts(ta, tb, to, p, grid, s) : gemm_bf16_experts(ta, tb, to, p, grid, s);
 }

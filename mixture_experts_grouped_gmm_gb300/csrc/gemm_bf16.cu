@@ -3,14 +3,17 @@
 
 namespace mgemm {
 
-int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
-  return launch_gemm<GemmCfg<false, false, true, kModeRows>>(a, b, p, grid, s);
+int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, true, kModeRows>>(a, b, o, p, grid, s);
 }
-int gemm_bf16_rows_bk(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
-  return launch_gemm<GemmCfg<false, false, false, kModeRows>>(a, b, p, grid, s);
+int gemm_bf16_rows_bk(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows>>(a, b, o, p, grid, s);
 }
-int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
-  return launch_gemm<GemmCfg<false, true, true, kModeExperts>>(a, b, p, grid, s);
+int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, true, true, kModeExperts>>(a, b, o, p, grid, s);
 }
 
 }  // namespace mgemm

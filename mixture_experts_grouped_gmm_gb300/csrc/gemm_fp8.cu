@@ -4,11 +4,13 @@
 
 namespace mgemm {
 
-int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
-  return launch_gemm<GemmCfg<true, false, false, kModeRows>>(a, b, p, grid, s);
+int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows>>(a, b, o, p, grid, s);
 }
-int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
-  return launch_gemm<GemmCfg<true, false, false, kModeExperts>>(a, b, p, grid, s);
+int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeExperts>>(a, b, o, p, grid, s);
 }
 
 }  // namespace mgemm

@@ -7,7 +7,8 @@
 namespace mgemm {
 
 template <class C>
-int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s) {
+int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
@@ -20,19 +21,24 @@ int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p,
     if (rc) return rc;
     attr_done[dev] = true;
   }
-  mgemm_gemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, b, p);
+  mgemm_gemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, b, o, p);
   return cuda_rc(cudaGetLastError(), "grouped GEMM launch");
 }
 
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)
-int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s);
 // bf16: A K-major rows, B K-major ([E, N, K] weights, or dgrad on [E, K, N])
-int gemm_bf16_rows_bk(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+int gemm_bf16_rows_bk(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s);
 // bf16 wgrad: both operands MN-major (row-major x and grad_out)
-int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s);
 // fp8 forward / dgrad: both K-major, scaled epilogue
-int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s);
 // fp8 wgrad: column-major quantized operands (K-major), scaled epilogue
-int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s);
+int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s);
 
 }  // namespace mgemm

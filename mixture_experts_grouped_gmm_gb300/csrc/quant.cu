@@ -11,12 +11,12 @@
 //   rowwise: one warp per row; a row of up to 24*256 elements stays in
 //            registers between the amax and the cast, so it is read once.
 //            Longer rows take a second pass (served by L2).
-//   colwise: one CTA per (tensor, group, 64-column block); pass 1 reduces the
-//            column amax over the group's rows, pass 2 re-reads (L2), casts,
-//            transposes 128-row chunks in shared memory and writes each
-//            column's bytes contiguously (16-byte stores inside the group,
-//            byte stores on the ragged group edges).  CTAs are ordered by
-//            group size, largest first, so the long groups start early.
+//   colwise: one 512-thread CTA per (tensor, group, 64-column block); pass 1
+//            reduces the column amax over the group's rows, pass 2 re-reads
+//            (from L2), casts, transposes 256-row chunks in shared memory and
+//            writes each column's bytes contiguously (16-byte stores inside
+//            the group, byte stores on the ragged group edges).  CTAs are
+//            ordered by group size, largest first, so long groups start early.
 #include "common.cuh"
 
 namespace mgemm {
@@ -43,6 +43,16 @@ __device__ __forceinline__ uint2 cast8(const uint4 &v, float s) {
         ((uint32_t)cvt_e4m3x2(bf16_lo(v.y) * s, bf16_hi(v.y) * s) << 16);
   o.y = (uint32_t)cvt_e4m3x2(bf16_lo(v.z) * s, bf16_hi(v.z) * s) |
         ((uint32_t)cvt_e4m3x2(bf16_lo(v.w) * s, bf16_hi(v.w) * s) << 16);
+  return o;
+}
+
+// 8 bf16 -> 8 e4m3 bytes with one power-of-two scale per column
+__device__ __forceinline__ uint2 cast8_scaled(const uint4 &v, const float (&s)[8]) {
+  uint2 o;
+  o.x = (uint32_t)cvt_e4m3x2(bf16_lo(v.x) * s[0], bf16_hi(v.x) * s[1]) |
+        ((uint32_t)cvt_e4m3x2(bf16_lo(v.y) * s[2], bf16_hi(v.y) * s[3]) << 16);
+  o.y = (uint32_t)cvt_e4m3x2(bf16_lo(v.z) * s[4], bf16_hi(v.z) * s[5]) |
+        ((uint32_t)cvt_e4m3x2(bf16_lo(v.w) * s[6], bf16_hi(v.w) * s[7]) << 16);
   return o;
 }
 
@@ -103,10 +113,17 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 }
 
 // ------------------------------------------------------------------ colwise
-constexpr int kColBlock = 64;      // columns per CTA (128 bytes of bf16 per row)
-constexpr int kRowChunk = 128;     // rows per transpose chunk
-constexpr int kColThreads = 256;
-constexpr int kTPitch = kRowChunk + 16;  // bytes per transposed column row in smem
+// One CTA of 512 threads per (tensor, group, 64-column block).  Warp w owns
+// columns 8*(w % 8) .. +7 and, per 256-row chunk, rows 128*(w / 8) + 4*lane
+// .. +3: each lane loads four 16-byte row pieces (the CTA keeps 64 KB of loads
+// in flight), and in pass 2 writes each column's four codes with one 32-bit
+// shared-memory store (consecutive lanes -> consecutive words, no bank
+// conflicts).  Few, fat CTAs keep the set of group column blocks being read
+// small enough that pass 2 re-reads them from L2.
+constexpr int kColBlock = 64;                 // columns per CTA (128 bytes of bf16 per row)
+constexpr int kColThreads = 512;
+constexpr int kRowChunk = 256;                // rows per pass-2 transpose chunk
+constexpr int kTPitch = kRowChunk + 16;       // bytes per transposed column in smem
 
 struct ColTensor {
   const __nv_bfloat16 *in;
@@ -116,10 +133,21 @@ struct ColTensor {
   int ncb;  // column blocks
 };
 
+__device__ __forceinline__ void amax8_into(float (&a)[8], const uint4 &v) {
+  a[0] = fmaxf(a[0], fabsf(bf16_lo(v.x)));
+  a[1] = fmaxf(a[1], fabsf(bf16_hi(v.x)));
+  a[2] = fmaxf(a[2], fabsf(bf16_lo(v.y)));
+  a[3] = fmaxf(a[3], fabsf(bf16_hi(v.y)));
+  a[4] = fmaxf(a[4], fabsf(bf16_lo(v.z)));
+  a[5] = fmaxf(a[5], fabsf(bf16_hi(v.z)));
+  a[6] = fmaxf(a[6], fabsf(bf16_lo(v.w)));
+  a[7] = fmaxf(a[7], fabsf(bf16_hi(v.w)));
+}
+
 __global__ void __launch_bounds__(kColThreads) quant_colwise_kernel(const uint8_t *__restrict__ args, int E,
                                                                     int64_t M, ColTensor t1, ColTensor t2,
                                                                     int vec_ok) {
-  __shared__ float red[kColThreads / 8][kColBlock + 1];
+  __shared__ float red[2][kColBlock];
   __shared__ float s_scale[kColBlock];
   __shared__ __align__(16) uint8_t tile[kColBlock][kTPitch];
 
@@ -133,54 +161,37 @@ __global__ void __launch_bounds__(kColThreads) quant_colwise_kernel(const uint8_
   if (cb >= t1.ncb) cb -= t1.ncb;
   const int64_t rs = av.offsets[g], re = av.offsets[g + 1];
   const int64_t col0 = (int64_t)cb * kColBlock;
-  const int tid = threadIdx.x;
-  const int cchunk = tid & 7;  // 8 columns each
-  const int rlane = tid >> 3;  // 0..31
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cchunk = warp & 7;          // 8 columns each
+  const int rhalf = warp >> 3;          // 0..1
   const int64_t mycol = col0 + cchunk * 8;
   const bool col_ok = mycol < T.C;
+  const __nv_bfloat16 *src = T.in + mycol;
 
-  // pass 1: column amax over the group's rows
+  // pass 1: column amax over the group's rows (each lane: 4-row quads)
   float a[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) a[j] = 0.f;
   if (col_ok) {
-    int64_t r = rs + rlane;
-    for (; r + 96 < re; r += 128) {
+    for (int64_t r0 = rs + rhalf * 128 + lane * 4; r0 < re; r0 += 256) {
       uint4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = ldg_nc_v4(T.in + (r + 32 * u) * T.C + mycol);
+      for (int i = 0; i < 4; ++i)
+        if (r0 + i < re) v[i] = ldg_nc_v4(src + (r0 + i) * T.C);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        a[0] = fmaxf(a[0], fabsf(bf16_lo(v[u].x)));
-        a[1] = fmaxf(a[1], fabsf(bf16_hi(v[u].x)));
-        a[2] = fmaxf(a[2], fabsf(bf16_lo(v[u].y)));
-        a[3] = fmaxf(a[3], fabsf(bf16_hi(v[u].y)));
-        a[4] = fmaxf(a[4], fabsf(bf16_lo(v[u].z)));
-        a[5] = fmaxf(a[5], fabsf(bf16_hi(v[u].z)));
-        a[6] = fmaxf(a[6], fabsf(bf16_lo(v[u].w)));
-        a[7] = fmaxf(a[7], fabsf(bf16_hi(v[u].w)));
-      }
-    }
-    for (; r < re; r += 32) {
-      const uint4 v = ldg_nc_v4(T.in + r * T.C + mycol);
-      a[0] = fmaxf(a[0], fabsf(bf16_lo(v.x)));
-      a[1] = fmaxf(a[1], fabsf(bf16_hi(v.x)));
-      a[2] = fmaxf(a[2], fabsf(bf16_lo(v.y)));
-      a[3] = fmaxf(a[3], fabsf(bf16_hi(v.y)));
-      a[4] = fmaxf(a[4], fabsf(bf16_lo(v.z)));
-      a[5] = fmaxf(a[5], fabsf(bf16_hi(v.z)));
-      a[6] = fmaxf(a[6], fabsf(bf16_lo(v.w)));
-      a[7] = fmaxf(a[7], fabsf(bf16_hi(v.w)));
+      for (int i = 0; i < 4; ++i)
+        if (r0 + i < re) amax8_into(a, v[i]);
     }
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) red[rlane][cchunk * 8 + j] = a[j];
+  for (int j = 0; j < 8; ++j) a[j] = warp_max(a[j]);
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) red[rhalf][cchunk * 8 + j] = a[j];
+  }
   __syncthreads();
   if (tid < kColBlock) {
-    float m = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < kColThreads / 8; ++i) m = fmaxf(m, red[i][tid]);
-    const float s = pow2_scale_from_amax(m);
+    const float s = pow2_scale_from_amax(fmaxf(red[0][tid], red[1][tid]));
     s_scale[tid] = s;
     if (col0 + tid < T.C) T.sc[(int64_t)g * T.C + col0 + tid] = s;
   }
@@ -195,27 +206,34 @@ __global__ void __launch_bounds__(kColThreads) quant_colwise_kernel(const uint8_
   // Chunks start on 16-row boundaries of the whole tensor so that interior
   // 16-byte segments of every column are aligned.
   const int64_t base0 = rs & ~(int64_t)15;
+  const int lr0 = rhalf * 128 + lane * 4;  // this lane's first row within the chunk
   for (int64_t cr = base0; cr < re; cr += kRowChunk) {
+    uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < kRowChunk / 32; ++u) {
-      const int lr = rlane + 32 * u;
-      const int64_t r = cr + lr;
-      uint2 o = make_uint2(0, 0);
-      if (col_ok && r >= rs && r < re) {
-        const uint4 v = ldg_nc_v4(T.in + r * T.C + mycol);
-        o.x = (uint32_t)cvt_e4m3x2(bf16_lo(v.x) * sc[0], bf16_hi(v.x) * sc[1]) |
-              ((uint32_t)cvt_e4m3x2(bf16_lo(v.y) * sc[2], bf16_hi(v.y) * sc[3]) << 16);
-        o.y = (uint32_t)cvt_e4m3x2(bf16_lo(v.z) * sc[4], bf16_hi(v.z) * sc[5]) |
-              ((uint32_t)cvt_e4m3x2(bf16_lo(v.w) * sc[6], bf16_hi(v.w) * sc[7]) << 16);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tile[cchunk * 8 + j][lr] = (uint8_t)(o.x >> (8 * j));
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tile[cchunk * 8 + 4 + j][lr] = (uint8_t)(o.y >> (8 * j));
+    for (int i = 0; i < 4; ++i) {
+      const int64_t r = cr + lr0 + i;
+      v[i] = (col_ok && r >= rs && r < re) ? ldg_nc_v4(src + r * T.C) : make_uint4(0, 0, 0, 0);
     }
+    // codes of column j for rows lr0..lr0+3, one byte per row
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 o = cast8_scaled(v[i], sc);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        w[j] |= ((o.x >> (8 * j)) & 0xFFu) << (8 * i);
+        w[4 + j] |= ((o.y >> (8 * j)) & 0xFFu) << (8 * i);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint32_t *>(&tile[cchunk * 8 + j][lr0]) = w[j];
     __syncthreads();
-    // 64 columns x 8 segments of 16 rows
-    for (int idx = tid; idx < kColBlock * (kRowChunk / 16); idx += kColThreads) {
+    // 64 columns x 16 segments of 16 rows
+#pragma unroll
+    for (int k = 0; k < (kColBlock * (kRowChunk / 16)) / kColThreads; ++k) {
+      const int idx = tid + k * kColThreads;
       const int c = idx / (kRowChunk / 16);
       const int seg = idx % (kRowChunk / 16);
       const int64_t col = col0 + c;
