@@ -122,7 +122,9 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
     const int mk = (t % per_e) / p.n_tiles;
     ti.e = __ldg(av.wgrad_order + i);
     const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
-    ti.x0 = C::Fp8 ? (int)(rs & ~(int64_t)15) : (int)rs;  // fp8: TMA inner coordinate on 16 bytes
+    // fp8 operands are column-major, so the group's first row is the TMA inner
+    // coordinate: start the box on a 128-byte boundary and mask the head
+    ti.x0 = C::Fp8 ? (int)(rs & ~(int64_t)127) : (int)rs;
     ti.lo = (int)(rs - ti.x0);
     ti.hi = (int)(re - ti.x0);
     ti.kb_count = re > rs ? (ti.hi + C::BK - 1) / C::BK : 0;
@@ -135,10 +137,14 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
 
 // Zero the contraction positions outside [lo, hi) of one stage (positions are
 // relative to the block start).  Executed by all 32 lanes of the MMA warp.
+// bf16 (MN-major operands): whole 128-byte rows of A and B are cleared, so a
+// non-finite value in a neighbouring group cannot leak in.  FP8 (K-major
+// operands, codes written by the colwise quantizer and therefore finite): only
+// A is cleared -- a zero in A zeroes the product -- one row per lane, 16-byte
+// chunks, with a masked read-modify-write on the two boundary chunks.
 template <class C>
 __device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int bn, int lo, int hi, int lane) {
   if (C::AMn) {
-    // MN-major: contraction positions are rows of 128 bytes in each 64-wide chunk
     const int nA = C::BM / 64, nB = bn / 64;
     const int nrows = C::BK;
     for (int idx = lane; idx < (nA + nB) * nrows; idx += 32) {
@@ -150,27 +156,40 @@ __device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int bn, int
       for (int j = 0; j < 8; ++j) row[j] = make_uint4(0, 0, 0, 0);
     }
   } else {
-    // K-major, 128-byte swizzle: row r holds 8 16-byte chunks, physical chunk
-    // pc carries logical contraction chunk pc ^ (r & 7).
-    constexpr int EPC = 16 / C::ESIZE;  // elements per 16-byte chunk
-    const int rows = C::BM + bn;
-    for (int idx = lane; idx < rows * 8; idx += 32) {
-      const int r = idx >> 3, pc = idx & 7;
-      const int lc = pc ^ (r & 7);
-      const int p0 = lc * EPC, p1 = p0 + EPC;
-      if (p0 >= lo && p1 <= hi) continue;
-      uint8_t *rowp = r < C::BM ? sa + r * 128 : sb + (r - C::BM) * 128;
-      uint8_t *ck = rowp + pc * 16;
-      if (p1 <= lo || p0 >= hi) {
-        *reinterpret_cast<uint4 *>(ck) = make_uint4(0, 0, 0, 0);
-      } else {
-        for (int j = 0; j < EPC; ++j) {
-          const int p = p0 + j;
-          if (p < lo || p >= hi)
-            for (int b = 0; b < C::ESIZE; ++b) ck[j * C::ESIZE + b] = 0;
+    // valid byte range of every 128-byte row; row r stores logical 16-byte
+    // chunk lc at physical chunk lc ^ (r & 7) (128-byte swizzle)
+    const int blo = max(lo, 0) * C::ESIZE, bhi = min(hi, C::BK) * C::ESIZE;
+    for (int r = lane; r < C::BM; r += 32) {
+      uint8_t *rowp = sa + r * 128;
+#pragma unroll
+      for (int lc = 0; lc < 8; ++lc) {
+        const int b0 = lc * 16, b1 = b0 + 16;
+        if (b0 >= blo && b1 <= bhi) continue;
+        uint4 *ck = reinterpret_cast<uint4 *>(rowp + ((lc ^ (r & 7)) << 4));
+        if (b1 <= blo || b0 >= bhi) {
+          *ck = make_uint4(0, 0, 0, 0);
+          continue;
         }
+        // keep bytes [max(b0, blo), min(b1, bhi)) of this chunk
+        const int s0 = max(blo - b0, 0), s1 = min(bhi - b0, 16);
+        const uint32_t keep16 = ((1u << s1) - 1u) & ~((1u << s0) - 1u);
+        uint32_t wm[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t bits = (keep16 >> (4 * w)) & 0xFu;
+          wm[w] = ((bits & 1u) ? 0x000000FFu : 0u) | ((bits & 2u) ? 0x0000FF00u : 0u) |
+                  ((bits & 4u) ? 0x00FF0000u : 0u) | ((bits & 8u) ? 0xFF000000u : 0u);
+        }
+        uint4 v = *ck;
+        v.x &= wm[0];
+        v.y &= wm[1];
+        v.z &= wm[2];
+        v.w &= wm[3];
+        *ck = v;
       }
     }
+    (void)sb;
+    (void)bn;
   }
 }
 

@@ -168,19 +168,22 @@ __global__ void __launch_bounds__(kColThreads) quant_colwise_kernel(const uint8_
   const bool col_ok = mycol < T.C;
   const __nv_bfloat16 *src = T.in + mycol;
 
-  // pass 1: column amax over the group's rows (each lane: 4-row quads)
+  // pass 1: column amax over the group's rows (each lane: two 4-row quads, 8
+  // loads in flight)
   float a[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) a[j] = 0.f;
   if (col_ok) {
-    for (int64_t r0 = rs + rhalf * 128 + lane * 4; r0 < re; r0 += 256) {
-      uint4 v[4];
+    for (int64_t r0 = rs + rhalf * 128 + lane * 4; r0 < re; r0 += 512) {
+      uint4 v[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (r0 + i < re) v[i] = ldg_nc_v4(src + (r0 + i) * T.C);
+      for (int i = 0; i < 8; ++i) {
+        const int64_t r = r0 + (i & 3) + (i >> 2) * 256;
+        if (r < re) v[i] = ldg_nc_v4(src + r * T.C);
+      }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (r0 + i < re) amax8_into(a, v[i]);
+      for (int i = 0; i < 8; ++i)
+        if (r0 + (i & 3) + (i >> 2) * 256 < re) amax8_into(a, v[i]);
     }
   }
 #pragma unroll
@@ -207,13 +210,16 @@ __global__ void __launch_bounds__(kColThreads) quant_colwise_kernel(const uint8_
   // 16-byte segments of every column are aligned.
   const int64_t base0 = rs & ~(int64_t)15;
   const int lr0 = rhalf * 128 + lane * 4;  // this lane's first row within the chunk
-  for (int64_t cr = base0; cr < re; cr += kRowChunk) {
-    uint4 v[4];
+  auto load_chunk = [&](uint4 (&v)[4], int64_t cr) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t r = cr + lr0 + i;
       v[i] = (col_ok && r >= rs && r < re) ? ldg_nc_v4(src + r * T.C) : make_uint4(0, 0, 0, 0);
     }
+  };
+  uint4 v[4];
+  load_chunk(v, base0);
+  for (int64_t cr = base0; cr < re; cr += kRowChunk) {
     // codes of column j for rows lr0..lr0+3, one byte per row
     uint32_t w[8];
 #pragma unroll
@@ -227,6 +233,8 @@ __global__ void __launch_bounds__(kColThreads) quant_colwise_kernel(const uint8_
         w[4 + j] |= ((o.y >> (8 * j)) & 0xFFu) << (8 * i);
       }
     }
+    // next chunk's loads are in flight while this one is transposed and stored
+    if (cr + kRowChunk < re) load_chunk(v, cr + kRowChunk);
 #pragma unroll
     for (int j = 0; j < 8; ++j) *reinterpret_cast<uint32_t *>(&tile[cchunk * 8 + j][lr0]) = w[j];
     __syncthreads();
