@@ -51,6 +51,7 @@ def parse():
     p.add_argument("--workload", choices=["all", "sparse", "deepseek", "mixtral"], default="all",
                    help="'all': headline line with every block; otherwise run only that block (profiling)")
     p.add_argument("--tokens", type=int, default=16384, help="DeepSeek-shaped block: tokens (x top-6 rows)")
+    p.add_argument("--experts", type=int, default=128, help="sparse-M block: number of experts")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return p.parse_args()
 
@@ -160,17 +161,17 @@ def time_events(torch, fn, reps, scrub=None):
             "mean_us": sum(ts) / len(ts)}
 
 
-def sparse_m_extra(torch, B, dev, pk):
+def sparse_m_extra(torch, B, dev, pk, E=128, reps=30):
     from mixture_experts_grouped_gmm_gb300 import workloads
 
-    E, K, N = 128, 5120, 8192
+    K, N = 5120, 8192
     w = workloads.sparse_m(1, E=E, K=K, N=N, device=dev)["w_nk"]
     wq = torch.empty(E * N, K, dtype=torch.uint8, device=dev)
     sw = torch.empty(E * N, dtype=torch.float32, device=dev)
     B.mgemm_quant_rowwise(w.view(E * N, K), wq, sw)
     del w
     scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    res = {"shape": "E=128 K=5120 N=8192 fp8 e4m3, rowwise scales; cold L2 (256 MB scrub between reps)",
+    res = {"shape": f"E={E} K=5120 N=8192 fp8 e4m3, rowwise scales; cold L2 (256 MB scrub between reps)",
            "points": []}
     for tm in (1, 2, 4, 16, 64, 256):
         d = workloads.sparse_m(tm, E=E, K=K, N=N, device=dev, with_weights=False)
@@ -191,8 +192,8 @@ def sparse_m_extra(torch, B, dev, pk):
         def fwd_only():
             B.mgemm_fwd(args, B.MGEMM_FP8_E4M3, 1, xq, sx, wq, sw, out, tm, K, N, E)
 
-        t_full = time_events(torch, full, 30, scrub)
-        t_fwd = time_events(torch, fwd_only, 30, scrub)
+        t_full = time_events(torch, full, reps, scrub)
+        t_fwd = time_events(torch, fwd_only, reps, scrub)
         byts = n_touched * K * N + n_touched * N * 4 + tm * (K + 4 + 2 * N)
         res["points"].append({"total_M": tm, "experts_touched": n_touched,
                               "p50_us_fill_quant_fwd": round(t_full["p50_us"], 2),
@@ -201,7 +202,7 @@ def sparse_m_extra(torch, B, dev, pk):
     # flat in E: one token, E experts (a prefix of the same weights)
     sweep = []
     d = workloads.sparse_m(1, E=8, K=K, N=N, device=dev, with_weights=False)
-    for Ee in (8, 16, 32, 64, 128):
+    for Ee in [e for e in (8, 16, 32, 64, 128) if e <= E]:
         gs = torch.zeros(Ee, dtype=torch.int64, device=dev)
         gs[Ee // 2] = 1
         args = torch.empty(B.mgemm_args_bytes(Ee), dtype=torch.uint8, device=dev)
@@ -215,7 +216,7 @@ def sparse_m_extra(torch, B, dev, pk):
             B.mgemm_fwd(args, B.MGEMM_FP8_E4M3, 1, xq, sx, wq, sw, out, 1, K, N, Ee)
 
         full()
-        sweep.append({"E": Ee, "p50_us_fill_quant_fwd": round(time_events(torch, full, 30, scrub)["p50_us"], 2)})
+        sweep.append({"E": Ee, "p50_us_fill_quant_fwd": round(time_events(torch, full, reps, scrub)["p50_us"], 2)})
     res["E_sweep_total_M_1"] = sweep
     del wq, scrub
     return res
@@ -357,7 +358,7 @@ def run_block(a):
     _build.build()
     pk, _ = peaks()
     if a.workload == "sparse":
-        out = sparse_m_extra(torch, B, dev, pk)
+        out = sparse_m_extra(torch, B, dev, pk, E=a.experts, reps=max(1, a.steps))
     elif a.workload == "deepseek":
         out = deepseek_extra(torch, B, dev, pk, tokens=a.tokens, reps=max(1, a.steps))
     else:

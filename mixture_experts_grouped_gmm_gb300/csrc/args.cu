@@ -12,7 +12,10 @@
 // deterministic and needs no temporary storage.  The block size is bucketed by
 // E (32, 128, 1024 threads) since the cost of a single-CTA kernel grows with
 // its thread count.
+#include <cudaTypedefs.h>
 #include <stdio.h>
+
+#include <mutex>
 
 #include "common.cuh"
 
@@ -107,6 +110,61 @@ __global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict
 
 namespace {
 thread_local char g_last_error[192] = "";
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+bool make_tensor_map(CUtensorMap *m, bool byte_elems, int rank, const void *base, const uint64_t *dims,
+                     const uint64_t *strides, const uint32_t *box) {
+  auto enc = encode_fn();
+  if (!enc) {
+    note_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", 0);
+    return false;
+  }
+  const uint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r =
+      enc(m, byte_elems ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    note_error("cuTensorMapEncodeTiled", (int)r);
+    return false;
+  }
+  return true;
+}
+
+int ensure_context() {
+  thread_local bool done = false;
+  if (done) return MGEMM_OK;
+  int dev = 0;
+  int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  rc = cuda_rc(cudaSetDevice(dev), "cudaSetDevice");
+  if (rc) return rc;
+  done = true;
+  return MGEMM_OK;
+}
+
+int sm_count_cached() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (!cached[dev]) cached[dev] = mgemm_num_sms();
+  return cached[dev];
 }
 
 void note_error(const char *where, int code) {

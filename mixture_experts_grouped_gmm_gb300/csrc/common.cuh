@@ -22,6 +22,17 @@ inline int cuda_rc(cudaError_t e, const char *where) {
   return MGEMM_ECUDA;
 }
 
+// Tiled tensor map with 128-byte swizzle and zero fill outside the tensor
+// (dims[0] contiguous; strides in bytes for dims 1..rank-1).
+bool make_tensor_map(CUtensorMap *m, bool byte_elems, int rank, const void *base, const uint64_t *dims,
+                     const uint64_t *strides, const uint32_t *box);
+// cuTensorMapEncodeTiled needs a current context; a thread that has made no
+// CUDA call yet (an autograd worker, say) has none.  Makes the current
+// device's primary context current, once per thread.
+int ensure_context();
+// Number of SMs of the current device (cached per device), or < 0 on error.
+int sm_count_cached();
+
 // ---------------------------------------------------------------- args block
 struct ArgsLayout {
   size_t offsets, active, mtile_start, wgrad_order, bytes;
@@ -112,6 +123,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
       if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
   }
+}
+
+// mbar_wait for a whole converged warp: every lane waits, and all lanes get
+// the same answer (a timeout seen by any lane counts for the warp), so the
+// code after it never diverges into warp-collective instructions.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const volatile int *abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------- TMA

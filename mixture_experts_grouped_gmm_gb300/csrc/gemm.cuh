@@ -16,11 +16,11 @@
 //
 // CTA layout (192 threads, one CTA per SM, grid = number of SMs, tiles
 // strided by gridDim.x):
-//   warp 0      TMA producer: one thread fills a 4-stage ring of
+//   warp 0      TMA producer: one thread fills a ring (4 stages wide, 8 narrow) of
 //               (A 128 rows x 128 B, B BN rows x 128 B) shared-memory tiles,
 //               128-byte swizzled, each stage guarded by a full/empty mbarrier.
-//   warp 1      TMEM owner and MMA issuer: allocates 512 TMEM columns (two
-//               128 x 256 fp32 accumulators), one thread issues
+//   warp 1      TMEM owner and MMA issuer: allocates two 128 x BN_MAX fp32
+//               accumulators in TMEM, one thread issues
 //               tcgen05.mma (M=128, N=BN, K=16 bf16 / 32 e4m3) per 32-byte
 //               K step and commits stage-release / accumulator-ready events.
 //               On a wgrad tile whose contraction range does not cover the
@@ -46,22 +46,26 @@ namespace mgemm {
 
 enum { kModeRows = 0, kModeExperts = 1 };
 
-template <bool kFp8, bool kAMn, bool kBMn, int kMode>
+// kBnMax / kStages: the widest output tile this instantiation serves and its
+// ring depth.  The wide form (256, 4 stages) serves dense problems; the narrow
+// form (64, 8 stages) serves weight-streaming launches with few token rows,
+// where a deeper ring keeps more HBM reads in flight per SM.
+template <bool kFp8, bool kAMn, bool kBMn, int kMode, int kBnMax = 256, int kStages = 4>
 struct GemmCfg {
   static constexpr bool Fp8 = kFp8;
   static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
   static constexpr bool BMn = kBMn;
   static constexpr int Mode = kMode;
-  static constexpr int BM = 128, BN_MAX = 256;
+  static constexpr int BM = 128, BN_MAX = kBnMax;
   static constexpr int ESIZE = kFp8 ? 1 : 2;
   static constexpr int BK = 128 / ESIZE;  // contraction elements per stage (one 128-byte row)
   static constexpr int UK = 32 / ESIZE;   // contraction elements per MMA
   static constexpr int KSTEPS = BK / UK;  // 4
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN_MAX * 128;
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = kStages;
   static constexpr int CHUNK = 64 * 128;  // MN-major: one 64-element x BK-row block (8 KB)
-  static constexpr int TMEM_COLS = 2 * BN_MAX;
+  static constexpr int TMEM_COLS = 2 * BN_MAX;  // a power of two >= 32
   static constexpr int THREADS = 192;
   static constexpr int OUT_BUF = 32 * 128;  // 32 rows x 64 bf16 columns
   static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * (A_BYTES + B_BYTES) +
@@ -72,6 +76,7 @@ struct GemmParams {
   const uint8_t *args;
   int E;
   int bn;           // output tile width: 64, 128 or 256
+  int a_rows;       // rows mode: rows of each A box (128, or fewer when M itself is smaller)
   uint32_t idesc;   // tcgen05 instruction descriptor for M=128, N=bn
   int n_tiles;      // ceil(Nout / bn)
   int mt_k;         // kExperts: ceil(Kout / BM)
@@ -99,9 +104,10 @@ __device__ __forceinline__ int total_tiles(const GemmParams &p, const ArgsView &
 template <class C>
 __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, const ArgsView &av) {
   TileInfo ti;
-  const int nt = t % p.n_tiles;
-  ti.n0 = nt * p.bn;
   if (C::Mode == kModeRows) {
+    // Group a owns tiles [mtile_start[a] * n_tiles, mtile_start[a+1] * n_tiles).
+    // Inside a group the row tile varies fastest, so CTAs running together
+    // share one weight tile through L2 instead of each streaming its own.
     const int gm = t / p.n_tiles;
     int lo = 0, hi = *av.n_active - 1;
     while (lo < hi) {
@@ -109,14 +115,20 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
       if (__ldg(av.mtile_start + mid) <= gm) lo = mid; else hi = mid - 1;
     }
     ti.e = __ldg(av.active + lo);
+    const int m_first = __ldg(av.mtile_start + lo);
+    const int mt_g = __ldg(av.mtile_start + lo + 1) - m_first;
+    const int local = t - m_first * p.n_tiles;
+    const int mt = local % mt_g;
+    ti.n0 = (local / mt_g) * p.bn;
     const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
-    const int row0 = (int)rs + (gm - __ldg(av.mtile_start + lo)) * C::BM;
+    const int row0 = (int)rs + mt * C::BM;
     ti.kb_count = (p.Kc + C::BK - 1) / C::BK;
     ti.a_row = row0;
     ti.out_row0 = row0;
     ti.out_rows = (int)min((int64_t)C::BM, re - row0);
     ti.x0 = 0; ti.lo = 0; ti.hi = 0;
   } else {
+    ti.n0 = (t % p.n_tiles) * p.bn;
     const int per_e = p.mt_k * p.n_tiles;
     const int i = t / per_e;
     const int mk = (t % per_e) / p.n_tiles;
@@ -255,7 +267,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      const uint32_t tx = C::A_BYTES + bn * 128;
+      // with fewer than 128 token rows the A box is cut to them (rounded up to 8);
+      // the MMA's remaining A rows hold stale data and only feed output rows
+      // that are never stored
+      const uint32_t tx = (C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128;
       for (int t = blockIdx.x; t < total && !*vabort; t += gridDim.x) {
         const TileInfo ti = decode_tile<C>(t, p, av);
         for (int kb = 0; kb < ti.kb_count; ++kb) {
@@ -303,11 +318,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const TileInfo ti = decode_tile<C>(t, p, av);
       if (ti.kb_count == 0) continue;
-      if (!mbar_wait(&tempty[acc], acc_phase ^ 1, vabort)) { ok = false; break; }
+      if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1, vabort)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * C::BN_MAX;
       for (int kb = 0; kb < ti.kb_count; ++kb) {
-        if (!mbar_wait(&full[stage], phase, vabort)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
         tc_fence_after();
         uint8_t *a = sA + stage * C::A_BYTES;
         uint8_t *b = sB + stage * C::B_BYTES;
@@ -375,7 +390,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       float rinv = 1.f;
       if (C::Fp8 && row_ok && has_acc) rinv = 1.f / __ldg(p.rscale + ti.out_row0 + r);
       if (has_acc) {
-        if (!mbar_wait(&tfull[acc], acc_phase, vabort)) {
+        if (!mbar_wait_warp(&tfull[acc], acc_phase, vabort)) {
           set_status(av.status, MGEMM_STATUS_TIMEOUT);
           *vabort = 1;
           break;

@@ -1,75 +1,20 @@
 // Entry points mgemm_fwd / mgemm_dgrad / mgemm_wgrad: argument checks,
 // tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry
 // point, so the library needs no link-time libcuda), grid sizing and dispatch.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "gemm_launch.cuh"
 
 using namespace mgemm;
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// Tiled map with 128-byte swizzle and zero fill outside the tensor.
-// dims[0] is the contiguous dimension; strides are in bytes for dims 1..rank-1.
 bool make_map(CUtensorMap *m, bool fp8, int rank, const void *base, const uint64_t *dims,
               const uint64_t *strides, const uint32_t *box) {
-  auto enc = encode_fn();
-  if (!enc) {
-    note_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", 0);
-    return false;
-  }
-  const uint32_t estr[5] = {1, 1, 1, 1, 1};
-  const CUresult r =
-      enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
-          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    note_error("cuTensorMapEncodeTiled", (int)r);
-    return false;
-  }
-  return true;
+  return make_tensor_map(m, fp8, rank, base, dims, strides, box);
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
-// cuTensorMapEncodeTiled needs a current context.  A thread that has made no
-// CUDA call yet (for example an autograd worker) has none: make the current
-// device's primary context current, once per thread.
-int ensure_context() {
-  thread_local bool done = false;
-  if (done) return MGEMM_OK;
-  int dev = 0;
-  int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
-  if (rc) return rc;
-  rc = cuda_rc(cudaSetDevice(dev), "cudaSetDevice");
-  if (rc) return rc;
-  done = true;
-  return MGEMM_OK;
-}
-
-int sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
-  if (!cached[dev]) cached[dev] = mgemm_num_sms();
-  return cached[dev];
-}
+int sm_count() { return sm_count_cached(); }
 
 int common_checks(const void *args, int dtype, int64_t M, int K, int N, int E) {
   if (!args) return MGEMM_EINVAL;
@@ -142,10 +87,11 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   const uint64_t es = fp8 ? 1 : 2;
   const uint32_t bk = fp8 ? 128 : 64;
   CUtensorMap ta, tb;
+  const uint32_t a_rows = M < 128 ? (uint32_t)((M + 7) / 8 * 8) : 128u;
   {
     const uint64_t d[2] = {(uint64_t)K, (uint64_t)M};
     const uint64_t st[1] = {(uint64_t)K * es};
-    const uint32_t box[2] = {bk, 128};
+    const uint32_t box[2] = {bk, a_rows};
     if (!make_map(&ta, fp8, 2, x, d, st, box)) return MGEMM_ECUDA;
   }
   const int bn = choose_bn(rows_tiles_estimate(M, E), N);
@@ -167,6 +113,7 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   p.E = E;
   p.bn = bn;
   p.idesc = make_idesc(fp8 ? 0u : 1u, false, !trans_b, 128, bn);
+  p.a_rows = (int)a_rows;
   p.n_tiles = (N + bn - 1) / bn;
   p.Kc = K;
   p.Nout = N;
@@ -177,6 +124,11 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
   cudaStream_t s = (cudaStream_t)stream;
+  if (bn <= 64) {
+    if (fp8) return gemm_fp8_rows_narrow(ta, tb, to, p, grid, s);
+    return trans_b ? gemm_bf16_rows_bk_narrow(ta, tb, to, p, grid, s)
+                   : gemm_bf16_rows_bmn_narrow(ta, tb, to, p, grid, s);
+  }
   if (fp8) return gemm_fp8_rows(ta, tb, to, p, grid, s);
   return trans_b ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, to, p, grid, s);
 }
@@ -194,10 +146,11 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   const uint64_t es = fp8 ? 1 : 2;
   const uint32_t bk = fp8 ? 128 : 64;
   CUtensorMap ta, tb;
+  const uint32_t a_rows = M < 128 ? (uint32_t)((M + 7) / 8 * 8) : 128u;
   {  // grad_out [M, N], contraction over N
     const uint64_t d[2] = {(uint64_t)N, (uint64_t)M};
     const uint64_t st[1] = {(uint64_t)N * es};
-    const uint32_t box[2] = {bk, 128};
+    const uint32_t box[2] = {bk, a_rows};
     if (!make_map(&ta, fp8, 2, grad_out, d, st, box)) return MGEMM_ECUDA;
   }
   const int bn = choose_bn(rows_tiles_estimate(M, E), K);
@@ -214,6 +167,7 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   p.E = E;
   p.bn = bn;
   p.idesc = make_idesc(fp8 ? 0u : 1u, false, false, 128, bn);
+  p.a_rows = (int)a_rows;
   p.n_tiles = (K + bn - 1) / bn;
   p.Kc = N;
   p.Nout = K;
@@ -224,6 +178,7 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
   cudaStream_t s = (cudaStream_t)stream;
+  if (bn <= 64) return fp8 ? gemm_fp8_rows_narrow(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk_narrow(ta, tb, to, p, grid, s);
   return fp8 ? gemm_fp8_rows(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk(ta, tb, to, p, grid, s);
 }
 

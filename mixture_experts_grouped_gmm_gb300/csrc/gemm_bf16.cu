@@ -15,5 +15,13 @@ int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensor
                        cudaStream_t s) {
   return launch_gemm<GemmCfg<false, true, true, kModeExperts>>(a, b, o, p, grid, s);
 }
+int gemm_bf16_rows_bmn_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                              int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, true, kModeRows, 64, 8>>(a, b, o, p, grid, s);
+}
+int gemm_bf16_rows_bk_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                             int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 64, 8>>(a, b, o, p, grid, s);
+}
 
 }  // namespace mgemm

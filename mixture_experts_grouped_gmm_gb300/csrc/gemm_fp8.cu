@@ -12,5 +12,9 @@ int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorM
                        cudaStream_t s) {
   return launch_gemm<GemmCfg<true, false, false, kModeExperts>>(a, b, o, p, grid, s);
 }
+int gemm_fp8_rows_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                         int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows, 64, 8>>(a, b, o, p, grid, s);
+}
 
 }  // namespace mgemm

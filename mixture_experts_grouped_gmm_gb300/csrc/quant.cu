@@ -11,12 +11,14 @@
 //   rowwise: one warp per row; a row of up to 24*256 elements stays in
 //            registers between the amax and the cast, so it is read once.
 //            Longer rows take a second pass (served by L2).
-//   colwise: one 512-thread CTA per (tensor, group, 64-column block); pass 1
-//            reduces the column amax over the group's rows, pass 2 re-reads
-//            (from L2), casts, transposes 256-row chunks in shared memory and
-//            writes each column's bytes contiguously (16-byte stores inside
-//            the group, byte stores on the ragged group edges).  CTAs are
-//            ordered by group size, largest first, so long groups start early.
+//   colwise: persistent CTAs (one per SM) fed by TMA through a 5-stage ring
+//            of 256-row x 64-column boxes, over (group, tensor, column-block)
+//            items in order of decreasing group size; 16 consumer warps read
+//            the boxes with transposing ldmatrix, reduce the column magnitude
+//            max (pass 1), then convert two rows of one column per e4m3x2
+//            conversion so the codes come out column-major (pass 2), stage
+//            256-row chunks in shared memory and write each column's bytes
+//            contiguously.
 #include "common.cuh"
 
 namespace mgemm {
@@ -43,16 +45,6 @@ __device__ __forceinline__ uint2 cast8(const uint4 &v, float s) {
         ((uint32_t)cvt_e4m3x2(bf16_lo(v.y) * s, bf16_hi(v.y) * s) << 16);
   o.y = (uint32_t)cvt_e4m3x2(bf16_lo(v.z) * s, bf16_hi(v.z) * s) |
         ((uint32_t)cvt_e4m3x2(bf16_lo(v.w) * s, bf16_hi(v.w) * s) << 16);
-  return o;
-}
-
-// 8 bf16 -> 8 e4m3 bytes with one power-of-two scale per column
-__device__ __forceinline__ uint2 cast8_scaled(const uint4 &v, const float (&s)[8]) {
-  uint2 o;
-  o.x = (uint32_t)cvt_e4m3x2(bf16_lo(v.x) * s[0], bf16_hi(v.x) * s[1]) |
-        ((uint32_t)cvt_e4m3x2(bf16_lo(v.y) * s[2], bf16_hi(v.y) * s[3]) << 16);
-  o.y = (uint32_t)cvt_e4m3x2(bf16_lo(v.z) * s[4], bf16_hi(v.z) * s[5]) |
-        ((uint32_t)cvt_e4m3x2(bf16_lo(v.w) * s[6], bf16_hi(v.w) * s[7]) << 16);
   return o;
 }
 
@@ -113,152 +105,291 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 }
 
 // ------------------------------------------------------------------ colwise
-// One CTA of 512 threads per (tensor, group, 64-column block).  Warp w owns
-// columns 8*(w % 8) .. +7 and, per 256-row chunk, rows 128*(w / 8) + 4*lane
-// .. +3: each lane loads four 16-byte row pieces (the CTA keeps 64 KB of loads
-// in flight), and in pass 2 writes each column's four codes with one 32-bit
-// shared-memory store (consecutive lanes -> consecutive words, no bank
-// conflicts).  Few, fat CTAs keep the set of group column blocks being read
-// small enough that pass 2 re-reads them from L2.
-constexpr int kColBlock = 64;                 // columns per CTA (128 bytes of bf16 per row)
-constexpr int kColThreads = 512;
-constexpr int kRowChunk = 256;                // rows per pass-2 transpose chunk
-constexpr int kTPitch = kRowChunk + 16;       // bytes per transposed column in smem
+// Persistent, TMA-fed.  Work item = (group, tensor, 64-column block), items
+// in order of decreasing group size; CTA b takes items b, b + grid, ...
+//   warp 16 (one thread): streams boxes of 256 rows x 64 columns (32 KB,
+//            128-byte swizzle) of the item's column block through a 5-stage
+//            ring (160 KB of loads in flight per SM), running ahead across
+//            items.  Rows count from the group's first row rounded down to
+//            16, so the 16-row output segments of every column are aligned.
+//   warps 0-15: warp w owns columns 8*(w % 8) .. +7 and rows 128*(w / 8) ..
+//            +127 of each box.  ldmatrix.x4.trans reads 32 rows x 8 columns
+//            (conflict-free under the swizzle) and hands lane t, in each of
+//            its 4 registers, two consecutive rows of column t / 4.  Pass 1
+//            keeps a packed bf16x2 running max of magnitudes; pass 2 scales
+//            each register with one packed fp32 multiply and converts it to an
+//            e4m3 pair that is already in column-major order, stores it as 16
+//            bits into one of two [64 columns][256 rows] tiles, and the CTA
+//            writes that tile out as 16-byte column-contiguous stores (byte
+//            stores on ragged group edges) while the next box is converted
+//            into the other tile.  A group spanning at most 5 boxes stays in
+//            the ring between the passes instead of being reloaded.
+// Consumer warps synchronize through an mbarrier with bounded waits; every
+// pipeline wait gives up after about 1 s with MGEMM_STATUS_TIMEOUT.
+constexpr int kCwRows = 256;
+constexpr int kCwStages = 5;
+constexpr int kCwConsumers = 16;
+constexpr int kCwThreads = (kCwConsumers + 1) * 32;
+constexpr int kCwBox = kCwRows * 128;   // 32 KB
+constexpr int kCwPitch = kCwRows + 16;  // transposed tile: bytes per column
+constexpr size_t kCwSmem = 1024 + (size_t)kCwStages * kCwBox + 2 * 64 * kCwPitch + 2 * 64 * 4 + 128;
 
 struct ColTensor {
-  const __nv_bfloat16 *in;
   uint8_t *out;
   float *sc;
   int64_t C;
-  int ncb;  // column blocks
+  int ncb;  // 64-column blocks
 };
 
-__device__ __forceinline__ void amax8_into(float (&a)[8], const uint4 &v) {
-  a[0] = fmaxf(a[0], fabsf(bf16_lo(v.x)));
-  a[1] = fmaxf(a[1], fabsf(bf16_hi(v.x)));
-  a[2] = fmaxf(a[2], fabsf(bf16_lo(v.y)));
-  a[3] = fmaxf(a[3], fabsf(bf16_hi(v.y)));
-  a[4] = fmaxf(a[4], fabsf(bf16_lo(v.z)));
-  a[5] = fmaxf(a[5], fabsf(bf16_hi(v.z)));
-  a[6] = fmaxf(a[6], fabsf(bf16_lo(v.w)));
-  a[7] = fmaxf(a[7], fabsf(bf16_hi(v.w)));
+struct CwItem {
+  int tensor, g, cb, nck;
+  int64_t rs, re, base;
+};
+
+__device__ __forceinline__ CwItem cw_decode(int item, const ArgsView &av, const ColTensor &t1,
+                                            const ColTensor &t2) {
+  CwItem it;
+  const int per_group = t1.ncb + t2.ncb;
+  it.g = av.wgrad_order[item / per_group];
+  const int cb = item % per_group;
+  it.tensor = cb < t1.ncb ? 0 : 1;
+  it.cb = it.tensor == 0 ? cb : cb - t1.ncb;
+  it.rs = av.offsets[it.g];
+  it.re = av.offsets[it.g + 1];
+  it.base = it.rs & ~(int64_t)15;
+  it.nck = it.re > it.rs ? (int)((it.re - it.base + kCwRows - 1) / kCwRows) : 0;
+  return it;
 }
 
-__global__ void __launch_bounds__(kColThreads) quant_colwise_kernel(const uint8_t *__restrict__ args, int E,
-                                                                    int64_t M, ColTensor t1, ColTensor t2,
-                                                                    int vec_ok) {
-  __shared__ float red[2][kColBlock];
-  __shared__ float s_scale[kColBlock];
-  __shared__ __align__(16) uint8_t tile[kColBlock][kTPitch];
+// Packed running max of magnitudes: each half of the result has magnitude
+// max(|acc|, |v|) (its sign is meaningless; clear it before use).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t v) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(v));
+  return r;
+}
+
+// Two bf16 values (one register) times a power-of-two scale (packed as {s, s})
+// -> two e4m3 codes (round to nearest even, saturating), low element in the
+// low byte.  One packed fp32 multiply serves both elements.
+__device__ __forceinline__ uint16_t bf16x2_scaled_e4m3x2(uint32_t x, uint64_t s2) {
+  uint16_t r;
+  asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 p;\n\t"
+      "shl.b32 lo, %1, 16;\n\t"
+      "and.b32 hi, %1, 0xFFFF0000;\n\t"
+      "mov.b64 p, {lo, hi};\n\t"
+      "mul.rn.f32x2 p, p, %2;\n\t"
+      "mov.b64 {lo, hi}, p;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 %0, hi, lo;\n\t}"
+      : "=h"(r)
+      : "r"(x), "l"(s2));
+  return r;
+}
+
+// Four 8x8 b16 matrices (rows given by lanes 0-31), transposed on the way out.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__global__ void __launch_bounds__(kCwThreads, 1)
+    quant_colwise_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm2,
+                         const uint8_t *__restrict__ args, int E, int64_t M, ColTensor t1, ColTensor t2, int vec_ok,
+                         int items) {
+  extern __shared__ uint8_t cw_smem_raw[];
+  uint8_t *smem =
+      reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(cw_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *ring = smem;
+  uint8_t *tiles = ring + kCwStages * kCwBox;                         // 2 x [64][kCwPitch]
+  float *red = reinterpret_cast<float *>(tiles + 2 * 64 * kCwPitch);  // [2][64]
+  uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * 64);
+  uint64_t *empty = full + kCwStages;
+  uint64_t *csync = empty + kCwStages;
+  int *abort_flag = reinterpret_cast<int *>(csync + 1);
 
   const ArgsView av(args, E);
   if (*av.status != 0) return;
-  const int per_group = t1.ncb + t2.ncb;
-  const int item = blockIdx.x;
-  const int g = av.wgrad_order[item / per_group];  // largest groups first
-  int cb = item % per_group;
-  const ColTensor &T = cb < t1.ncb ? t1 : t2;
-  if (cb >= t1.ncb) cb -= t1.ncb;
-  const int64_t rs = av.offsets[g], re = av.offsets[g + 1];
-  const int64_t col0 = (int64_t)cb * kColBlock;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cchunk = warp & 7;          // 8 columns each
-  const int rhalf = warp >> 3;          // 0..1
-  const int64_t mycol = col0 + cchunk * 8;
-  const bool col_ok = mycol < T.C;
-  const __nv_bfloat16 *src = T.in + mycol;
-
-  // pass 1: column amax over the group's rows (each lane: two 4-row quads, 8
-  // loads in flight)
-  float a[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) a[j] = 0.f;
-  if (col_ok) {
-    for (int64_t r0 = rs + rhalf * 128 + lane * 4; r0 < re; r0 += 512) {
-      uint4 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int64_t r = r0 + (i & 3) + (i >> 2) * 256;
-        if (r < re) v[i] = ldg_nc_v4(src + r * T.C);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (r0 + (i & 3) + (i >> 2) * 256 < re) amax8_into(a, v[i]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kCwStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kCwConsumers);
     }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) a[j] = warp_max(a[j]);
-  if (lane == 0) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) red[rhalf][cchunk * 8 + j] = a[j];
+    mbar_init(csync, kCwConsumers);
+    *abort_flag = 0;
+    fence_barrier_init();
   }
   __syncthreads();
-  if (tid < kColBlock) {
-    const float s = pow2_scale_from_amax(fmaxf(red[0][tid], red[1][tid]));
-    s_scale[tid] = s;
-    if (col0 + tid < T.C) T.sc[(int64_t)g * T.C + col0 + tid] = s;
-  }
-  __syncthreads();
-  if (re <= rs) return;
+  volatile int *vabort = abort_flag;
+  uint32_t issued = 0;
 
-  float sc[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) sc[j] = s_scale[cchunk * 8 + j];
-
-  // pass 2: cast, transpose through shared memory, column-contiguous stores.
-  // Chunks start on 16-row boundaries of the whole tensor so that interior
-  // 16-byte segments of every column are aligned.
-  const int64_t base0 = rs & ~(int64_t)15;
-  const int lr0 = rhalf * 128 + lane * 4;  // this lane's first row within the chunk
-  auto load_chunk = [&](uint4 (&v)[4], int64_t cr) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = cr + lr0 + i;
-      v[i] = (col_ok && r >= rs && r < re) ? ldg_nc_v4(src + r * T.C) : make_uint4(0, 0, 0, 0);
-    }
-  };
-  uint4 v[4];
-  load_chunk(v, base0);
-  for (int64_t cr = base0; cr < re; cr += kRowChunk) {
-    // codes of column j for rows lr0..lr0+3, one byte per row
-    uint32_t w[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) w[j] = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint2 o = cast8_scaled(v[i], sc);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        w[j] |= ((o.x >> (8 * j)) & 0xFFu) << (8 * i);
-        w[4 + j] |= ((o.y >> (8 * j)) & 0xFFu) << (8 * i);
-      }
-    }
-    // next chunk's loads are in flight while this one is transposed and stored
-    if (cr + kRowChunk < re) load_chunk(v, cr + kRowChunk);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint32_t *>(&tile[cchunk * 8 + j][lr0]) = w[j];
-    __syncthreads();
-    // 64 columns x 16 segments of 16 rows
-#pragma unroll
-    for (int k = 0; k < (kColBlock * (kRowChunk / 16)) / kColThreads; ++k) {
-      const int idx = tid + k * kColThreads;
-      const int c = idx / (kRowChunk / 16);
-      const int seg = idx % (kRowChunk / 16);
-      const int64_t col = col0 + c;
-      const int64_t r0 = cr + seg * 16;
-      if (col >= T.C || r0 >= re || r0 + 16 <= rs) continue;
-      uint8_t *dst = T.out + col * M + r0;
-      const uint8_t *srcb = &tile[c][seg * 16];
-      if (vec_ok && r0 >= rs && r0 + 16 <= re) {
-        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(srcb);
-      } else {
-        for (int j = 0; j < 16; ++j) {
-          const int64_t r = r0 + j;
-          if (r >= rs && r < re) dst[j] = srcb[j];
+  if (warp == kCwConsumers) {
+    // ---- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm1);
+      tma_prefetch_desc(&tm2);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int item = blockIdx.x; item < items && !*vabort; item += gridDim.x) {
+        const CwItem it = cw_decode(item, av, t1, t2);
+        const CUtensorMap *tm = it.tensor == 0 ? &tm1 : &tm2;
+        const int passes = it.nck <= kCwStages ? 1 : 2;
+        for (int pass = 0; pass < passes && !*vabort; ++pass) {
+          for (int k = 0; k < it.nck; ++k) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, vabort)) {
+              set_status(av.status, MGEMM_STATUS_TIMEOUT);
+              *vabort = 1;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], kCwBox);
+            ++issued;
+            tma_load_2d(ring + stage * kCwBox, tm, &full[stage], it.cb * 64, (int)(it.base + (int64_t)k * kCwRows));
+            if (++stage == kCwStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
         }
       }
     }
-    __syncthreads();
+  } else {
+    // ---- consumers
+    const int cc = warp & 7, rhalf = warp >> 3;
+    const int lcol = cc * 8 + (lane >> 2);  // this lane's column within the block
+    const int rpair = 2 * (lane & 3);       // row offset of its pair inside each 8-row matrix
+    const int st_c = threadIdx.x >> 4;      // store phase: columns st_c, st_c + 32
+    const int st_seg = threadIdx.x & 15;    //              16-row segment
+    int stage = 0;
+    uint32_t phase = 0, cphase = 0;
+    bool ok = true;
+    auto cons_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(csync);
+      const bool r = mbar_wait_warp(csync, cphase, vabort);
+      cphase ^= 1;
+      return r;
+    };
+    // ldmatrix row address of this lane for 32-row block j of the warp's half of a box
+    auto row_addr = [&](const uint8_t *box, int j) -> uint32_t {
+      const int r = rhalf * 128 + j * 32 + lane;
+      return smem_u32(box + r * 128 + ((cc ^ (r & 7)) << 4));
+    };
+    for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+      const CwItem it = cw_decode(item, av, t1, t2);
+      const ColTensor &T = it.tensor == 0 ? t1 : t2;
+      const int64_t col0 = (int64_t)it.cb * 64;
+      if (it.nck == 0) {  // empty group: amax 0 -> scale 2^48, no data
+        if (rhalf == 0 && (lane & 3) == 0 && col0 + lcol < T.C)
+          T.sc[(int64_t)it.g * T.C + col0 + lcol] = pow2_scale_from_amax(0.f);
+        continue;
+      }
+      const bool resident = it.nck <= kCwStages;
+      const int s0 = stage;
+      const uint32_t p0 = phase;
+      // pass 1: magnitude max of column lcol over this warp's rows; only the
+      // boxes at the group's two ends hold rows of other groups
+      uint32_t am = 0u;
+      for (int k = 0; k < it.nck; ++k) {
+        if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        const uint8_t *box = ring + stage * kCwBox;
+        const int64_t r0 = it.base + (int64_t)k * kCwRows + rhalf * 128;
+        const bool edge = (k == 0) || (k == it.nck - 1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[4];
+          ldsm_x4_trans(row_addr(box, j), v);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint32_t x = v[m];
+            if (edge) {
+              const int64_t gr = r0 + j * 32 + m * 8 + rpair;  // rows gr (low half), gr + 1 (high half)
+              if (gr < it.rs || gr >= it.re) x &= 0xFFFF0000u;
+              if (gr + 1 < it.rs || gr + 1 >= it.re) x &= 0x0000FFFFu;
+            }
+            am = bf16x2_absmax(am, x);
+          }
+        }
+        __syncwarp();
+        if (!resident && lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == kCwStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      am = bf16x2_absmax(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = bf16x2_absmax(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      am &= 0x7FFF7FFFu;
+      if ((lane & 3) == 0) red[rhalf * 64 + lcol] = fmaxf(bf16_lo(am), bf16_hi(am));
+      if (!cons_sync()) { ok = false; break; }
+      const float sc = pow2_scale_from_amax(fmaxf(red[lcol], red[64 + lcol]));
+      if (rhalf == 0 && (lane & 3) == 0 && col0 + lcol < T.C) T.sc[(int64_t)it.g * T.C + col0 + lcol] = sc;
+      const uint64_t sc2 = ((uint64_t)__float_as_uint(sc) << 32) | __float_as_uint(sc);
+      // pass 2: box k is converted into tile k % 2 while the stores of box k - 1
+      // drain from the other tile; one consumer sync per box
+      if (resident) {
+        stage = s0;
+        phase = p0;
+      }
+      for (int k = 0; k < it.nck; ++k) {
+        if (!resident && !mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        const uint8_t *box = ring + stage * kCwBox;
+        uint8_t *tile = tiles + (k & 1) * (64 * kCwPitch);
+        uint8_t *tcol = tile + lcol * kCwPitch + rhalf * 128 + rpair;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[4];
+          ldsm_x4_trans(row_addr(box, j), v);
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<uint16_t *>(tcol + j * 32 + m * 8) = bf16x2_scaled_e4m3x2(v[m], sc2);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);  // box consumed; the codes live in the tile
+        if (++stage == kCwStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        // every warp has finished this tile, and the stores of box k - 2 (which
+        // used it before) were issued before those warps got here
+        if (!cons_sync()) { ok = false; break; }
+        // 64 columns x 16 segments of 16 rows, 512 consumer threads: this
+        // thread stores segment st_seg of columns st_c and st_c + 32
+        const int64_t q0 = it.base + (int64_t)k * kCwRows + st_seg * 16;
+        const bool inner = vec_ok && q0 >= it.rs && q0 + 16 <= it.re;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int c = st_c + 32 * u;
+          const int64_t col = col0 + c;
+          if (col >= T.C || q0 >= it.re || q0 + 16 <= it.rs) continue;
+          uint8_t *dst = T.out + col * M + q0;
+          const uint8_t *srcb = tile + c * kCwPitch + st_seg * 16;
+          if (inner) {
+            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(srcb);
+          } else {
+            for (int jj = 0; jj < 16; ++jj) {
+              const int64_t rr = q0 + jj;
+              if (rr >= it.rs && rr < it.re) dst[jj] = srcb[jj];
+            }
+          }
+        }
+      }
+      // the next item's pass-1 writes to red and to the tiles start after every
+      // warp is done with this item
+      if (ok && !cons_sync()) { ok = false; break; }
+    }
+    if (!ok) {
+      if (lane == 0) set_status(av.status, MGEMM_STATUS_TIMEOUT);
+      *vabort = 1;
+    }
+  }
+  __syncthreads();
+  if (*vabort && warp == kCwConsumers && lane == 0) {
+    for (int s = 0; s < kCwStages; ++s) {  // wait for this CTA's copies in flight, bounded
+      const uint32_t armed = issued / kCwStages + ((uint32_t)s < issued % kCwStages ? 1u : 0u);
+      if (armed) mbar_wait(&full[s], (armed - 1) & 1, nullptr);
+    }
   }
 }
 
@@ -307,17 +438,48 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
   if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
   if (M < 0 || M >= (int64_t(1) << 31) || C1 <= 0 || C1 % 8) return MGEMM_EINVAL;
   if (((uintptr_t)args & 15) || ((uintptr_t)in1 & 15)) return MGEMM_EALIGN;
-  ColTensor t1{(const __nv_bfloat16 *)in1, out1, sc1, C1, (int)((C1 + kColBlock - 1) / kColBlock)};
-  ColTensor t2{nullptr, nullptr, nullptr, 0, 0};
   if (in2) {
     if (!out2 || !sc2 || C2 <= 0 || C2 % 8) return MGEMM_EINVAL;
     if ((uintptr_t)in2 & 15) return MGEMM_EALIGN;
-    t2 = ColTensor{(const __nv_bfloat16 *)in2, out2, sc2, C2, (int)((C2 + kColBlock - 1) / kColBlock)};
   }
+  int rc = ensure_context();
+  if (rc) return rc;
+  // rows of a zero-row tensor are never loaded; the map only needs valid dims
+  const uint64_t Mm = M > 0 ? (uint64_t)M : 1;
+  CUtensorMap tm1, tm2;
+  {
+    const uint64_t d[2] = {(uint64_t)C1, Mm};
+    const uint64_t st[1] = {(uint64_t)C1 * 2};
+    const uint32_t box[2] = {64, kCwRows};
+    if (!make_tensor_map(&tm1, false, 2, in1, d, st, box)) return MGEMM_ECUDA;
+  }
+  if (in2) {
+    const uint64_t d[2] = {(uint64_t)C2, Mm};
+    const uint64_t st[1] = {(uint64_t)C2 * 2};
+    const uint32_t box[2] = {64, kCwRows};
+    if (!make_tensor_map(&tm2, false, 2, in2, d, st, box)) return MGEMM_ECUDA;
+  } else {
+    tm2 = tm1;
+  }
+  ColTensor t1{out1, sc1, C1, (int)((C1 + 63) / 64)};
+  ColTensor t2{out2, sc2, in2 ? C2 : 0, in2 ? (int)((C2 + 63) / 64) : 0};
   const int vec_ok = (M % 16 == 0) && (((uintptr_t)out1 & 15) == 0) && (!in2 || (((uintptr_t)out2 & 15) == 0));
   const int64_t items = (int64_t)E * (t1.ncb + t2.ncb);
   if (items >= (int64_t(1) << 31)) return MGEMM_EINVAL;
-  quant_colwise_kernel<<<(unsigned)items, kColThreads, 0, (cudaStream_t)stream>>>((const uint8_t *)args, E, M,
-                                                                                  t1, t2, vec_ok);
+  const int sms = sm_count_cached();
+  if (sms <= 0) return MGEMM_ECUDA;
+  const int grid = (int)(items < sms ? items : sms);
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if ((rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if ((rc = cuda_rc(cudaFuncSetAttribute(quant_colwise_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kCwSmem),
+                      "cudaFuncSetAttribute")))
+      return rc;
+    attr_done[dev] = true;
+  }
+  quant_colwise_kernel<<<grid, kCwThreads, kCwSmem, (cudaStream_t)stream>>>(tm1, tm2, (const uint8_t *)args, E, M,
+                                                                           t1, t2, vec_ok, (int)items);
   return cuda_rc(cudaGetLastError(), "mgemm_quant_colwise_grouped launch");
 }
