@@ -77,7 +77,9 @@ typedef struct CUstream_st *mgemm_stream_t;
  *   [0]   int32  status        MGEMM_STATUS_*
  *   [4]   int32  n_active      number of non-empty groups (<= min(M, E))
  *   [8]   int32  E
- *   [12]  int32  reserved (0)
+ *   [12]  int32  work counter: mgemm_fill_args writes 0; mgemm_quant_colwise_grouped
+ *                hands out its work items from it and leaves it at 0 again when it
+ *                completes (calls that share an args block must not overlap on the GPU)
  *   [16]  int64  M
  *   [24]  int64  offsets[E+1]  exclusive prefix sum of group_sizes
  *   [A]   int32  active[E]     ids of the non-empty groups, ascending (first n_active valid)

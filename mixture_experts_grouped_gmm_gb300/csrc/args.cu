@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict
     hdr[0] = st;
     hdr[1] = n_active_sh;
     hdr[2] = E;
-    hdr[3] = 0;
+    hdr[3] = 0;  // work counter of the colwise quantizer
     *(int64_t *)(args + 16) = M;
   }
 }

@@ -50,6 +50,7 @@ __host__ __device__ inline ArgsLayout args_layout(int E) {
 
 struct ArgsView {
   int *status;
+  int *work;  // header word 3: work counter, 0 between launches
   const int *n_active;
   const int64_t *offsets;
   const int *active;
@@ -59,6 +60,7 @@ struct ArgsView {
     uint8_t *b = (uint8_t *)base;
     ArgsLayout L = args_layout(E);
     status = (int *)b;
+    work = (int *)(b + 12);
     n_active = (const int *)(b + 4);
     offsets = (const int64_t *)(b + L.offsets);
     active = (const int *)(b + L.active);
@@ -257,12 +259,17 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, bool a_mn,
 }
 
 // ---------------------------------------------------------------- numerics
-// Power-of-two scale 2^floor(log2(fp32(448 / max(amax, 1e-12)))), the
-// division done in float64 and rounded once to fp32, the floor taken from the
-// exponent bits (exact).
+// Power-of-two scale 2^floor(log2(fp32(448 / max(amax, 1e-12)))), with the
+// floor taken from the exponent bits (exact).  The quotient is defined as the
+// float64 quotient rounded once to fp32; a correctly rounded fp32 division
+// gives the same fp32 value, because rounding first to 53 bits and then to 24
+// cannot change a 24-bit quotient (53 >= 2 * 24 + 2).  The fp32 constant 1e-12f
+// differs from the float64 one only in an interval that holds no bf16 value,
+// and for amax below it the quotient (~4.48e14) sits far from a power-of-two
+// boundary, so the power-of-two result is identical for every bf16 amax.
+// (This GPU's float64 throughput is low; one fp32 division per value is cheap.)
 __device__ __forceinline__ float pow2_scale_from_amax(float amax) {
-  const double q = 448.0 / fmax((double)amax, 1e-12);
-  const float s = __double2float_rn(q);
+  const float s = __fdiv_rn(448.0f, fmaxf(amax, 1e-12f));
   return __uint_as_float(__float_as_uint(s) & 0x7F800000u);
 }
 

@@ -106,7 +106,9 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 
 // ------------------------------------------------------------------ colwise
 // Persistent, TMA-fed.  Work item = (group, tensor, 64-column block), items
-// in order of decreasing group size; CTA b takes items b, b + grid, ...
+// in order of decreasing group size, handed out one at a time from a counter
+// in the args block (dynamic scheduling keeps the CTAs balanced when group
+// sizes are skewed).
 //   warp 16 (one thread): streams boxes of 256 rows x 64 columns (32 KB,
 //            128-byte swizzle) of the item's column block through a 5-stage
 //            ring (160 KB of loads in flight per SM), running ahead across
@@ -124,15 +126,20 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 //            stores on ragged group edges) while the next box is converted
 //            into the other tile.  A group spanning at most 5 boxes stays in
 //            the ring between the passes instead of being reloaded.
-// Consumer warps synchronize through an mbarrier with bounded waits; every
-// pipeline wait gives up after about 1 s with MGEMM_STATUS_TIMEOUT.
+// The CTA first copies the group offsets and the size order into shared
+// memory.  Consumer warps synchronize with a hardware barrier (see
+// cw_consumer_barrier_any); every pipeline wait is bounded and gives up after about
+// 1 s with MGEMM_STATUS_TIMEOUT.
 constexpr int kCwRows = 256;
 constexpr int kCwStages = 5;
 constexpr int kCwConsumers = 16;
 constexpr int kCwThreads = (kCwConsumers + 1) * 32;
 constexpr int kCwBox = kCwRows * 128;   // 32 KB
 constexpr int kCwPitch = kCwRows + 16;  // transposed tile: bytes per column
-constexpr size_t kCwSmem = 1024 + (size_t)kCwStages * kCwBox + 2 * 64 * kCwPitch + 2 * 64 * 4 + 128;
+constexpr int kCwQueue = 4;  // item ids handed from the producer to the consumers
+constexpr size_t kCwSmemFixed = 1024 + (size_t)kCwStages * kCwBox + 2 * 64 * kCwPitch + 2 * 2 * 64 * 4 + 256;
+// plus a copy of the group offsets and the size order: 8 (E + 1) + 4 E bytes
+__host__ __device__ constexpr size_t cw_smem_bytes(int E) { return kCwSmemFixed + 8 * (size_t)(E + 1) + 4 * (size_t)E + 16; }
 
 struct ColTensor {
   uint8_t *out;
@@ -146,16 +153,16 @@ struct CwItem {
   int64_t rs, re, base;
 };
 
-__device__ __forceinline__ CwItem cw_decode(int item, const ArgsView &av, const ColTensor &t1,
+__device__ __forceinline__ CwItem cw_decode(int item, const int64_t *off, const int *order, const ColTensor &t1,
                                             const ColTensor &t2) {
   CwItem it;
   const int per_group = t1.ncb + t2.ncb;
-  it.g = av.wgrad_order[item / per_group];
+  it.g = order[item / per_group];
   const int cb = item % per_group;
   it.tensor = cb < t1.ncb ? 0 : 1;
   it.cb = it.tensor == 0 ? cb : cb - t1.ncb;
-  it.rs = av.offsets[it.g];
-  it.re = av.offsets[it.g + 1];
+  it.rs = off[it.g];
+  it.re = off[it.g + 1];
   it.base = it.rs & ~(int64_t)15;
   it.nck = it.re > it.rs ? (int)((it.re - it.base + kCwRows - 1) / kCwRows) : 0;
   return it;
@@ -193,6 +200,25 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
+// Hardware barrier among the 16 consumer warps only (the producer warp never
+// takes part), returning the OR of `flag` over all of them.  Every consumer warp
+// executes every barrier: a warp whose bounded data wait gives up raises the
+// abort flag and keeps going through the same steps; the decision to leave is
+// taken by this barrier, so all consumer warps get the same answer and leave
+// together.
+__device__ __forceinline__ bool cw_consumer_barrier_any(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, p;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)flag), "n"(kCwConsumers * 32)
+      : "memory");
+  return r != 0;
+}
+
 __global__ void __launch_bounds__(kCwThreads, 1)
     quant_colwise_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm2,
                          const uint8_t *__restrict__ args, int E, int64_t M, ColTensor t1, ColTensor t2, int vec_ok,
@@ -202,21 +228,30 @@ __global__ void __launch_bounds__(kCwThreads, 1)
       reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(cw_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *ring = smem;
   uint8_t *tiles = ring + kCwStages * kCwBox;                         // 2 x [64][kCwPitch]
-  float *red = reinterpret_cast<float *>(tiles + 2 * 64 * kCwPitch);  // [2][64]
-  uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * 64);
+  float *red = reinterpret_cast<float *>(tiles + 2 * 64 * kCwPitch);  // [2 items][2 halves][64]
+  uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * 2 * 64);
   uint64_t *empty = full + kCwStages;
-  uint64_t *csync = empty + kCwStages;
-  int *abort_flag = reinterpret_cast<int *>(csync + 1);
+  uint64_t *qfull = empty + kCwStages;
+  uint64_t *qempty = qfull + kCwQueue;
+  int *abort_flag = reinterpret_cast<int *>(qempty + kCwQueue);
+  int *s_item = abort_flag + 1;  // [kCwQueue]
+  int64_t *s_off = reinterpret_cast<int64_t *>(smem + (kCwSmemFixed - 1024));  // [E + 1]
+  int *s_order = reinterpret_cast<int *>(s_off + E + 1);                      // [E]
 
   const ArgsView av(args, E);
   if (*av.status != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = av.offsets[i];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_order[i] = av.wgrad_order[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kCwStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kCwConsumers);
     }
-    mbar_init(csync, kCwConsumers);
+    for (int q = 0; q < kCwQueue; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], kCwConsumers);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -229,10 +264,29 @@ __global__ void __launch_bounds__(kCwThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm1);
       tma_prefetch_desc(&tm2);
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int item = blockIdx.x; item < items && !*vabort; item += gridDim.x) {
-        const CwItem it = cw_decode(item, av, t1, t2);
+      int stage = 0, q = 0;
+      uint32_t phase = 0, qphase = 0;
+      // Items are taken from the args block's work counter in order of
+      // decreasing group size, so every CTA stays busy until the end.  Each
+      // CTA's last take returns a value >= items; the CTA whose last take is
+      // the launch's final one (items + grid - 1) sets the counter back to 0:
+      // no other CTA touches it after its own last take.
+      while (true) {
+        int item = atomicAdd(av.work, 1);
+        const bool done = item >= items || *vabort;
+        if (item == items + (int)gridDim.x - 1) atomicExch(av.work, 0);
+        if (!mbar_wait(&qempty[q], qphase ^ 1, vabort)) {
+          set_status(av.status, MGEMM_STATUS_TIMEOUT);
+          *vabort = 1;
+        }
+        s_item[q] = done ? -1 : item;
+        mbar_arrive(&qfull[q]);
+        if (++q == kCwQueue) {
+          q = 0;
+          qphase ^= 1;
+        }
+        if (done) break;
+        const CwItem it = cw_decode(item, s_off, s_order, t1, t2);
         const CUtensorMap *tm = it.tensor == 0 ? &tm1 : &tm2;
         const int passes = it.nck <= kCwStages ? 1 : 2;
         for (int pass = 0; pass < passes && !*vabort; ++pass) {
@@ -260,23 +314,35 @@ __global__ void __launch_bounds__(kCwThreads, 1)
     const int rpair = 2 * (lane & 3);       // row offset of its pair inside each 8-row matrix
     const int st_c = threadIdx.x >> 4;      // store phase: columns st_c, st_c + 32
     const int st_seg = threadIdx.x & 15;    //              16-row segment
-    int stage = 0;
-    uint32_t phase = 0, cphase = 0;
-    bool ok = true;
-    auto cons_sync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(csync);
-      const bool r = mbar_wait_warp(csync, cphase, vabort);
-      cphase ^= 1;
-      return r;
+    int stage = 0, q = 0;
+    uint32_t phase = 0, qphase = 0;
+    uint32_t tile_par = 0;  // alternates with every pass-2 box, across items
+    uint32_t item_par = 0;  // alternates with every item that has rows
+    // a data wait that gives up marks the kernel aborted but does not leave the
+    // step sequence, so barrier participation stays identical in every warp
+    auto wait_full = [&]() {
+      if (!mbar_wait_warp(&full[stage], phase, vabort) && lane == 0) {
+        set_status(av.status, MGEMM_STATUS_TIMEOUT);
+        *vabort = 1;
+      }
     };
     // ldmatrix row address of this lane for 32-row block j of the warp's half of a box
     auto row_addr = [&](const uint8_t *box, int j) -> uint32_t {
       const int r = rhalf * 128 + j * 32 + lane;
       return smem_u32(box + r * 128 + ((cc ^ (r & 7)) << 4));
     };
-    for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
-      const CwItem it = cw_decode(item, av, t1, t2);
+    while (true) {
+      // next item id from the producer (-1: no more work)
+      int item = -1;
+      if (mbar_wait_warp(&qfull[q], qphase, vabort)) item = s_item[q];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty[q]);
+      if (++q == kCwQueue) {
+        q = 0;
+        qphase ^= 1;
+      }
+      if (cw_consumer_barrier_any(item < 0 || *vabort != 0)) break;
+      const CwItem it = cw_decode(item, s_off, s_order, t1, t2);
       const ColTensor &T = it.tensor == 0 ? t1 : t2;
       const int64_t col0 = (int64_t)it.cb * 64;
       if (it.nck == 0) {  // empty group: amax 0 -> scale 2^48, no data
@@ -287,11 +353,13 @@ __global__ void __launch_bounds__(kCwThreads, 1)
       const bool resident = it.nck <= kCwStages;
       const int s0 = stage;
       const uint32_t p0 = phase;
+      float *red_i = red + item_par * 128;
+      item_par ^= 1;
       // pass 1: magnitude max of column lcol over this warp's rows; only the
       // boxes at the group's two ends hold rows of other groups
       uint32_t am = 0u;
       for (int k = 0; k < it.nck; ++k) {
-        if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        wait_full();
         const uint8_t *box = ring + stage * kCwBox;
         const int64_t r0 = it.base + (int64_t)k * kCwRows + rhalf * 128;
         const bool edge = (k == 0) || (k == it.nck - 1);
@@ -317,25 +385,26 @@ __global__ void __launch_bounds__(kCwThreads, 1)
           phase ^= 1;
         }
       }
-      if (!ok) break;
       am = bf16x2_absmax(am, __shfl_xor_sync(0xffffffffu, am, 1));
       am = bf16x2_absmax(am, __shfl_xor_sync(0xffffffffu, am, 2));
       am &= 0x7FFF7FFFu;
-      if ((lane & 3) == 0) red[rhalf * 64 + lcol] = fmaxf(bf16_lo(am), bf16_hi(am));
-      if (!cons_sync()) { ok = false; break; }
-      const float sc = pow2_scale_from_amax(fmaxf(red[lcol], red[64 + lcol]));
+      if ((lane & 3) == 0) red_i[rhalf * 64 + lcol] = fmaxf(bf16_lo(am), bf16_hi(am));
+      if (cw_consumer_barrier_any(*vabort != 0)) break;
+      const float sc = pow2_scale_from_amax(fmaxf(red_i[lcol], red_i[64 + lcol]));
       if (rhalf == 0 && (lane & 3) == 0 && col0 + lcol < T.C) T.sc[(int64_t)it.g * T.C + col0 + lcol] = sc;
       const uint64_t sc2 = ((uint64_t)__float_as_uint(sc) << 32) | __float_as_uint(sc);
-      // pass 2: box k is converted into tile k % 2 while the stores of box k - 1
-      // drain from the other tile; one consumer sync per box
+      // pass 2: box k is converted into one tile while the stores of the
+      // previous box drain from the other; one consumer barrier per box
       if (resident) {
         stage = s0;
         phase = p0;
       }
+      bool aborted = false;
       for (int k = 0; k < it.nck; ++k) {
-        if (!resident && !mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        if (!resident) wait_full();
         const uint8_t *box = ring + stage * kCwBox;
-        uint8_t *tile = tiles + (k & 1) * (64 * kCwPitch);
+        uint8_t *tile = tiles + tile_par * (64 * kCwPitch);
+        tile_par ^= 1;
         uint8_t *tcol = tile + lcol * kCwPitch + rhalf * 128 + rpair;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -351,9 +420,12 @@ __global__ void __launch_bounds__(kCwThreads, 1)
           stage = 0;
           phase ^= 1;
         }
-        // every warp has finished this tile, and the stores of box k - 2 (which
-        // used it before) were issued before those warps got here
-        if (!cons_sync()) { ok = false; break; }
+        // every warp has finished this tile; the stores that used it before
+        // (two boxes ago) were issued before those warps reached this barrier
+        if (cw_consumer_barrier_any(*vabort != 0)) {
+          aborted = true;
+          break;
+        }
         // 64 columns x 16 segments of 16 rows, 512 consumer threads: this
         // thread stores segment st_seg of columns st_c and st_c + 32
         const int64_t q0 = it.base + (int64_t)k * kCwRows + st_seg * 16;
@@ -375,13 +447,7 @@ __global__ void __launch_bounds__(kCwThreads, 1)
           }
         }
       }
-      // the next item's pass-1 writes to red and to the tiles start after every
-      // warp is done with this item
-      if (ok && !cons_sync()) { ok = false; break; }
-    }
-    if (!ok) {
-      if (lane == 0) set_status(av.status, MGEMM_STATUS_TIMEOUT);
-      *vabort = 1;
+      if (aborted) break;
     }
   }
   __syncthreads();
@@ -474,12 +540,12 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
   if ((rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     if ((rc = cuda_rc(cudaFuncSetAttribute(quant_colwise_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kCwSmem),
+                                           (int)cw_smem_bytes(MGEMM_MAX_EXPERTS)),
                       "cudaFuncSetAttribute")))
       return rc;
     attr_done[dev] = true;
   }
-  quant_colwise_kernel<<<grid, kCwThreads, kCwSmem, (cudaStream_t)stream>>>(tm1, tm2, (const uint8_t *)args, E, M,
-                                                                           t1, t2, vec_ok, (int)items);
+  quant_colwise_kernel<<<grid, kCwThreads, cw_smem_bytes(E), (cudaStream_t)stream>>>(
+      tm1, tm2, (const uint8_t *)args, E, M, t1, t2, vec_ok, (int)items);
   return cuda_rc(cudaGetLastError(), "mgemm_quant_colwise_grouped launch");
 }

@@ -137,3 +137,23 @@ def test_colwise_status_blocks_writes():
     B().mgemm_quant_colwise_grouped(args, E, M, a, o, s)
     torch.cuda.synchronize()
     assert (to_np(o) == 0xAB).all() and (to_np(s) == -1.0).all()
+
+
+def test_colwise_repeated_on_one_args_block():
+    # the work counter in the args header is handed back at 0, so a second call
+    # with the same args block sees every item again
+    sizes = [300, 0, 77, 1000, 5, 130]
+    E, M = len(sizes), int(np.sum(sizes))
+    gs = torch.tensor(sizes, dtype=torch.int64, device=DEV)
+    args = new_args(E, DEV)
+    B().mgemm_fill_args(gs, E, M, args)
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    for rep in range(3):
+        a = (torch.randn(M, 136, generator=torch.Generator(device=DEV).manual_seed(rep), device=DEV)).to(torch.bfloat16)
+        o = torch.full((136 * M,), 0xAB, dtype=torch.uint8, device=DEV)
+        s = torch.full((E * 136,), -1.0, dtype=torch.float32, device=DEV)
+        B().mgemm_quant_colwise_grouped(args, E, M, a, o, s)
+        torch.cuda.synchronize()
+        q, r = quant_colwise_grouped(to_np(a), offs)
+        assert np.array_equal(to_np(o).reshape(136, M), q) and np.array_equal(to_np(s), r)
+        assert int(args[12:16].view(torch.int32).item()) == 0
