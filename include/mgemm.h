@@ -186,6 +186,30 @@ int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *
 int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, const void *grad_out,
                 const float *sgo, void *grad_w, int64_t M, int K, int N, int E, mgemm_stream_t stream);
 
+/*
+ * mgemm_fwd_noalloc -- mgemm_fwd for callers that cannot allocate device memory.
+ * The source pages have no counterpart to this call; it exists for callers
+ * that may not call cudaMalloc (or any allocator) at the point where they run
+ * the forward pass -- for example code inside another framework's launch
+ * callback that has no allocator of its own, loops where an allocation could
+ * synchronize the device, or runtimes that only provide a fixed workspace
+ * chosen in advance.  Instead of a caller-provided args block it uses one held
+ * in a static device array of this library, sized for MGEMM_NOALLOC_MAX_EXPERTS
+ * experts (about 20 KB, kept on every GPU that loads the library until exit).
+ *   group_sizes  int64[E], device (as for mgemm_fill_args)
+ *   the other arguments are those of mgemm_fwd.
+ * Runs mgemm_fill_args into the static array, then mgemm_fwd.  Allocates
+ * nothing.  E > MGEMM_NOALLOC_MAX_EXPERTS returns MGEMM_ETOOMANY.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the array: calls whose work overlaps on the GPU race on it.
+ * Device-side errors go to the status word of the static args block, which the
+ * caller cannot read; check the group sizes beforehand when that matters.
+ */
+#define MGEMM_NOALLOC_MAX_EXPERTS 1024
+int mgemm_fwd_noalloc(const int64_t *group_sizes, int E, int dtype, int trans_b, const void *x, const float *sx,
+                      const void *w, const float *sw, void *out, int64_t M, int K, int N, mgemm_stream_t stream);
+
 /* Number of SMs of the current device (the persistent GEMM grid size), or < 0 on error. */
 int mgemm_num_sms(void);
 /* Static string naming a MGEMM_E* or MGEMM_STATUS_* code. */

@@ -50,6 +50,9 @@ _SIGS = {
     "mgemm_wgrad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "mgemm_fwd_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "mgemm_num_sms": (ctypes.c_int, []),
     "mgemm_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mgemm_version": (ctypes.c_int, []),
@@ -139,6 +142,15 @@ def mgemm_wgrad(args, dtype, x, sx, grad_out, sgo, grad_w, M, K, N, E):
     _cuda(args, x, sx, grad_out, sgo, grad_w)
     _check(lib().mgemm_wgrad(_p(args), int(dtype), _p(x), _p(sx), _p(grad_out), _p(sgo), _p(grad_w), int(M),
                              int(K), int(N), int(E), _stream(grad_w)), "mgemm_wgrad")
+
+
+def mgemm_fwd_noalloc(group_sizes, dtype, trans_b, x, sx, w, sw, out, M, K, N, E):
+    """Forward pass without a caller-provided args block (for callers that
+    cannot allocate device memory; the library keeps the block in a static
+    device array shared by all calls)."""
+    _cuda(group_sizes, x, sx, w, sw, out)
+    _check(lib().mgemm_fwd_noalloc(_p(group_sizes), int(E), int(dtype), int(trans_b), _p(x), _p(sx), _p(w), _p(sw),
+                                   _p(out), int(M), int(K), int(N), _stream(out)), "mgemm_fwd_noalloc")
 
 
 def mgemm_num_sms():

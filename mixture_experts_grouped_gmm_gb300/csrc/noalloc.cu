@@ -1,0 +1,73 @@
+// mgemm_fwd_noalloc: the grouped forward GEMM for callers that cannot
+// allocate device memory.
+//
+// The forward pass needs an args block (the tile schedule that
+// mgemm_fill_args derives from the group sizes) besides its inputs and
+// output.  Most callers allocate it themselves.  Some cannot: code that runs
+// inside another framework's launch callback with no allocator of its own,
+// code that must not call cudaMalloc because that can synchronize the device
+// in a latency-critical loop, or runtimes that only hand out a fixed
+// workspace decided ahead of time.  For them this entry point keeps the args
+// block in a statically sized device array that lives in this library.
+//
+// The array holds an args block for up to MGEMM_NOALLOC_MAX_EXPERTS experts
+// (about 20 KB); every GPU that loads the library keeps it until the process
+// exits.  All calls share it, so calls whose work overlaps on the GPU (for
+// example on two streams) race on it.  Each call rewrites every part of it
+// that the forward kernel reads (mgemm_fill_args writes the whole header,
+// the offsets, the active-group list and the tile prefix), so nothing from
+// an earlier call leaks into the next.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr size_t noalloc_args_bytes() {
+  // same layout as mgemm_args_layout(E) with E = MGEMM_NOALLOC_MAX_EXPERTS
+  return (24 + 8 * (size_t)(MGEMM_NOALLOC_MAX_EXPERTS + 1) + 4 * (size_t)MGEMM_NOALLOC_MAX_EXPERTS +
+          4 * (size_t)(MGEMM_NOALLOC_MAX_EXPERTS + 1) + 4 * (size_t)MGEMM_NOALLOC_MAX_EXPERTS + 15) &
+         ~(size_t)15;
+}
+
+static __device__ __align__(256) uint8_t g_noalloc_args[noalloc_args_bytes()];
+
+// Device address of g_noalloc_args, looked up once per device with that
+// device current (in host code the symbol is only a stand-in, not an address
+// the GPU can use).
+void *noalloc_args_ptr(int *rc) {
+  static void *ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  *rc = mgemm::cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
+  if (*rc) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *rc = MGEMM_EINVAL;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    *rc = mgemm::cuda_rc(cudaGetSymbolAddress(&p, g_noalloc_args), "cudaGetSymbolAddress");
+    if (*rc) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" int mgemm_fwd_noalloc(const int64_t *group_sizes, int E, int dtype, int trans_b, const void *x,
+                                 const float *sx, const void *w, const float *sw, void *out, int64_t M, int K, int N,
+                                 mgemm_stream_t stream) {
+  if (!group_sizes) return MGEMM_EINVAL;
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_NOALLOC_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  if (mgemm::args_layout(E).bytes > sizeof(g_noalloc_args)) return MGEMM_ETOOMANY;
+  int rc = MGEMM_OK;
+  void *args = noalloc_args_ptr(&rc);
+  if (rc) return rc;
+  rc = mgemm_fill_args(group_sizes, E, M, args, stream);
+  if (rc) return rc;
+  return mgemm_fwd(args, dtype, trans_b, x, sx, w, sw, out, M, K, N, E, stream);
+}
