@@ -16,7 +16,7 @@
 //
 // CTA layout (192 threads, one CTA per SM, grid = number of SMs, tiles
 // strided by gridDim.x):
-//   warp 0      TMA producer: one thread fills a ring (4 stages wide, 8 narrow) of
+//   warp 0      TMA producer: one thread fills a ring (4, 6 or 8 stages) of
 //               (A 128 rows x 128 B, B BN rows x 128 B) shared-memory tiles,
 //               128-byte swizzled, each stage guarded by a full/empty mbarrier.
 //   warp 1      TMEM owner and MMA issuer: allocates two 128 x BN_MAX fp32
@@ -28,8 +28,9 @@
 //               out-of-group positions in shared memory.
 //   warps 2-5   epilogue, one TMEM lane quarter (32 output rows) each:
 //               tcgen05.ld, optional FP8 scale division, bf16 rounding, then
-//               a 128-byte-swizzled shared-memory staging buffer (two per
-//               warp) and a TMA store of each 32-row x 64-column block.  A
+//               128-byte-swizzled shared-memory staging buffers (2 per warp,
+//               4 for wgrad, whose short main loops leave the stores as the
+//               critical path) and a TMA store of each 32-row x 64-column block.  A
 //               warp whose 32 rows are not all valid (group edge) stores
 //               those rows directly instead, so nothing outside the tile's
 //               rows is ever written.  The accumulator is released right
@@ -47,10 +48,10 @@ namespace mgemm {
 enum { kModeRows = 0, kModeExperts = 1 };
 
 // kBnMax / kStages: the widest output tile this instantiation serves and its
-// ring depth.  The wide form (256, 4 stages) serves dense problems; the narrow
-// form (64, 8 stages) serves weight-streaming launches with few token rows,
-// where a deeper ring keeps more HBM reads in flight per SM.
-template <bool kFp8, bool kAMn, bool kBMn, int kMode, int kBnMax = 256, int kStages = 4>
+// ring depth.  Wide (256, 4 stages), mid (128, 6) and narrow (64, 8) forms
+// fill the same shared memory; the narrower forms serve weight-streaming
+// launches, where a deeper ring keeps more HBM reads in flight per SM.
+template <bool kFp8, bool kAMn, bool kBMn, int kMode, int kBnMax = 256, int kStages = 4, int kOutBufs = 2>
 struct GemmCfg {
   static constexpr bool Fp8 = kFp8;
   static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
@@ -68,8 +69,10 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = 2 * BN_MAX;  // a power of two >= 32
   static constexpr int THREADS = 192;
   static constexpr int OUT_BUF = 32 * 128;  // 32 rows x 64 bf16 columns
+  static constexpr int NBUF = kOutBufs;      // staging buffers per epilogue warp
   static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * (A_BYTES + B_BYTES) +
-                                       4 * 2 * OUT_BUF /*epilogue staging*/ + 256 /*barriers, flags*/;
+                                       4 * NBUF * OUT_BUF /*epilogue staging*/ + 4 * 64 * 4 /*column scales*/ +
+                                       256 /*barriers, flags*/;
 };
 
 struct GemmParams {
@@ -205,6 +208,9 @@ __device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int bn, int
   }
 }
 
+// 1 / s for a power of two s in [2^-126, 2^126] (exact: the exponent is negated)
+__device__ __forceinline__ float pow2_recip(float s) { return __uint_as_float(0x7F000000u - __float_as_uint(s)); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -218,8 +224,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + C::STAGES * C::A_BYTES;
-  uint8_t *sOut = sB + C::STAGES * C::B_BYTES;  // [4 warps][2 buffers][32 x 128 B]
-  uint64_t *full = reinterpret_cast<uint64_t *>(sOut + 4 * 2 * C::OUT_BUF);
+  uint8_t *sOut = sB + C::STAGES * C::B_BYTES;  // [4 warps][NBUF buffers][32 x 128 B]
+  float *s_csc = reinterpret_cast<float *>(sOut + 4 * C::NBUF * C::OUT_BUF);  // [4 warps][64]
+  uint64_t *full = reinterpret_cast<uint64_t *>(s_csc + 4 * 64);
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
@@ -377,8 +384,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // epilogue warps 2..5 -> TMEM lane quarter q = warp % 4 -> tile rows 32q..32q+31
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    uint8_t *my_buf = sOut + (size_t)q * 2 * C::OUT_BUF;
-    int last_buf = -1;  // staging buffer read by this warp's most recent TMA store group
+    uint8_t *my_buf = sOut + (size_t)q * C::NBUF * C::OUT_BUF;
+    uint32_t nstored = 0;  // TMA-stored chunks so far; buffers rotate with it
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -388,7 +395,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const bool warp_full = q * 32 + 32 <= ti.out_rows;
       __nv_bfloat16 *orow = p.out + (int64_t)(ti.out_row0 + r) * p.Nout;
       float rinv = 1.f;
-      if (C::Fp8 && row_ok && has_acc) rinv = 1.f / __ldg(p.rscale + ti.out_row0 + r);
+      if (C::Fp8 && row_ok && has_acc) rinv = pow2_recip(__ldg(p.rscale + ti.out_row0 + r));
       if (has_acc) {
         if (!mbar_wait_warp(&tfull[acc], acc_phase, vabort)) {
           set_status(av.status, MGEMM_STATUS_TIMEOUT);
@@ -399,37 +406,57 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::BN_MAX;
       const int nchunks = bn / 64;
-#pragma unroll 1
-      for (int c = 0; c < nchunks; ++c) {
+      // TMEM -> registers runs one chunk ahead: chunk c + 1 is loading while
+      // chunk c is converted and stored (the loop is unrolled so both register
+      // sets keep fixed names)
+      uint32_t va[2][32], vb[2][32];
+      if (has_acc) {
+        tmem_ld_32x32b_x32(taddr, va[0]);
+        tmem_ld_32x32b_x32(taddr + 32, vb[0]);
+      }
+#pragma unroll
+      for (int c = 0; c < C::BN_MAX / 64; ++c) {
+        if (c >= nchunks) break;
+        const int cur = c & 1;
         const int col0 = ti.n0 + c * 64;
         uint32_t pk[32];
         if (has_acc) {
-          uint32_t v[32], w[32];
-          tmem_ld_32x32b_x32(taddr + c * 64, v);
-          tmem_ld_32x32b_x32(taddr + c * 64 + 32, w);
           tmem_ld_wait();
-          if (c == nchunks - 1) {  // accumulator fully read: hand it back to the MMA warp
+          if (c + 1 < nchunks) {
+            tmem_ld_32x32b_x32(taddr + (c + 1) * 64, va[cur ^ 1]);
+            tmem_ld_32x32b_x32(taddr + (c + 1) * 64 + 32, vb[cur ^ 1]);
+          } else {  // accumulator fully read: hand it back to the MMA warp
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
           }
-          float cinv0 = 1.f, cinv1 = 1.f;  // lane j: scales of columns col0 + j and col0 + 32 + j
           if (C::Fp8) {
-            if (col0 + lane < p.Nout) cinv0 = 1.f / __ldg(p.cscale + (int64_t)ti.e * p.Nout + col0 + lane);
-            if (col0 + 32 + lane < p.Nout)
-              cinv1 = 1.f / __ldg(p.cscale + (int64_t)ti.e * p.Nout + col0 + 32 + lane);
-          }
+            // column-scale reciprocals of this chunk, staged per warp and read as
+            // broadcasts (scales are powers of two: the reciprocal is exact)
+            float *cs = s_csc + q * 64;
+            const int64_t cb = (int64_t)ti.e * p.Nout + col0;
+            cs[lane] = col0 + lane < p.Nout ? pow2_recip(__ldg(p.cscale + cb + lane)) : 0.f;
+            cs[lane + 32] = col0 + 32 + lane < p.Nout ? pow2_recip(__ldg(p.cscale + cb + 32 + lane)) : 0.f;
+            __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float f0 = __uint_as_float(v[2 * j]), f1 = __uint_as_float(v[2 * j + 1]);
-            float g0 = __uint_as_float(w[2 * j]), g1 = __uint_as_float(w[2 * j + 1]);
-            if (C::Fp8) {  // every lane takes part in the shuffles
-              f0 *= rinv * __shfl_sync(0xffffffffu, cinv0, 2 * j);
-              f1 *= rinv * __shfl_sync(0xffffffffu, cinv0, 2 * j + 1);
-              g0 *= rinv * __shfl_sync(0xffffffffu, cinv1, 2 * j);
-              g1 *= rinv * __shfl_sync(0xffffffffu, cinv1, 2 * j + 1);
+            for (int j = 0; j < 8; ++j) {
+              const float4 c0 = *reinterpret_cast<const float4 *>(cs + 4 * j);
+              const float4 c1 = *reinterpret_cast<const float4 *>(cs + 32 + 4 * j);
+              pk[2 * j] = pack_bf16x2(__uint_as_float(va[cur][4 * j]) * rinv * c0.x,
+                                      __uint_as_float(va[cur][4 * j + 1]) * rinv * c0.y);
+              pk[2 * j + 1] = pack_bf16x2(__uint_as_float(va[cur][4 * j + 2]) * rinv * c0.z,
+                                          __uint_as_float(va[cur][4 * j + 3]) * rinv * c0.w);
+              pk[16 + 2 * j] = pack_bf16x2(__uint_as_float(vb[cur][4 * j]) * rinv * c1.x,
+                                           __uint_as_float(vb[cur][4 * j + 1]) * rinv * c1.y);
+              pk[16 + 2 * j + 1] = pack_bf16x2(__uint_as_float(vb[cur][4 * j + 2]) * rinv * c1.z,
+                                               __uint_as_float(vb[cur][4 * j + 3]) * rinv * c1.w);
             }
-            pk[j] = pack_bf16x2(f0, f1);
-            pk[16 + j] = pack_bf16x2(g0, g1);
+            __syncwarp();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              pk[j] = pack_bf16x2(__uint_as_float(va[cur][2 * j]), __uint_as_float(va[cur][2 * j + 1]));
+              pk[16 + j] = pack_bf16x2(__uint_as_float(vb[cur][2 * j]), __uint_as_float(vb[cur][2 * j + 1]));
+            }
           }
         } else {
 #pragma unroll
@@ -437,11 +464,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (col0 >= p.Nout) continue;
         if (warp_full) {
-          const int b = c & 1;
-          uint8_t *buf = my_buf + b * C::OUT_BUF;
-          if (lane == 0) {
-            if (last_buf == b) bulk_wait_read<0>(); else bulk_wait_read<1>();
-          }
+          // one store group per chunk, committed in rotation order: the group
+          // that last read this buffer is NBUF groups back
+          uint8_t *buf = my_buf + (nstored % C::NBUF) * C::OUT_BUF;
+          if (lane == 0) bulk_wait_read<C::NBUF - 1>();
           __syncwarp();
           uint8_t *rowp = buf + lane * 128;
 #pragma unroll
@@ -454,7 +480,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tma_store_2d(&tmOut, buf, col0, ti.out_row0 + q * 32);
             bulk_commit();
           }
-          last_buf = b;
+          ++nstored;
         } else if (row_ok) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + col0);
 #pragma unroll

@@ -129,6 +129,10 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
     return trans_b ? gemm_bf16_rows_bk_narrow(ta, tb, to, p, grid, s)
                    : gemm_bf16_rows_bmn_narrow(ta, tb, to, p, grid, s);
   }
+  if (bn <= 128) {
+    if (fp8) return gemm_fp8_rows_mid(ta, tb, to, p, grid, s);
+    return trans_b ? gemm_bf16_rows_bk_mid(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn_mid(ta, tb, to, p, grid, s);
+  }
   if (fp8) return gemm_fp8_rows(ta, tb, to, p, grid, s);
   return trans_b ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, to, p, grid, s);
 }
@@ -179,6 +183,7 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   if (grid < 0) return MGEMM_ECUDA;
   cudaStream_t s = (cudaStream_t)stream;
   if (bn <= 64) return fp8 ? gemm_fp8_rows_narrow(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk_narrow(ta, tb, to, p, grid, s);
+  if (bn <= 128) return fp8 ? gemm_fp8_rows_mid(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk_mid(ta, tb, to, p, grid, s);
   return fp8 ? gemm_fp8_rows(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk(ta, tb, to, p, grid, s);
 }
 

@@ -13,7 +13,7 @@ int gemm_bf16_rows_bk(const CUtensorMap &a, const CUtensorMap &b, const CUtensor
 }
 int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s) {
-  return launch_gemm<GemmCfg<false, true, true, kModeExperts>>(a, b, o, p, grid, s);
+  return launch_gemm<GemmCfg<false, true, true, kModeExperts, 256, 3, 4>>(a, b, o, p, grid, s);
 }
 int gemm_bf16_rows_bmn_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                               int grid, cudaStream_t s) {
@@ -22,6 +22,14 @@ int gemm_bf16_rows_bmn_narrow(const CUtensorMap &a, const CUtensorMap &b, const 
 int gemm_bf16_rows_bk_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                              int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<false, false, false, kModeRows, 64, 8>>(a, b, o, p, grid, s);
+}
+int gemm_bf16_rows_bmn_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                           int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, true, kModeRows, 128, 6>>(a, b, o, p, grid, s);
+}
+int gemm_bf16_rows_bk_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                          int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 128, 6>>(a, b, o, p, grid, s);
 }
 
 }  // namespace mgemm

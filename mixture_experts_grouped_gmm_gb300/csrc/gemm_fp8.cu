@@ -16,5 +16,9 @@ int gemm_fp8_rows_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUten
                          int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<true, false, false, kModeRows, 64, 8>>(a, b, o, p, grid, s);
 }
+int gemm_fp8_rows_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                      int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows, 128, 6>>(a, b, o, p, grid, s);
+}
 
 }  // namespace mgemm
