@@ -396,6 +396,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       __nv_bfloat16 *orow = p.out + (int64_t)(ti.out_row0 + r) * p.Nout;
       float rinv = 1.f;
       if (C::Fp8 && row_ok && has_acc) rinv = pow2_recip(__ldg(p.rscale + ti.out_row0 + r));
+      // FP8: this tile's column-scale reciprocals, fetched before the accumulator
+      // wait so no global load sits between a TMEM read and its stores; lane l
+      // holds columns n0 + 32 i + l (scales are powers of two: exact reciprocals)
+      float csr[C::BN_MAX / 32];
+      if (C::Fp8) {
+#pragma unroll
+        for (int i = 0; i < C::BN_MAX / 32; ++i) {
+          const int col = ti.n0 + 32 * i + lane;
+          csr[i] = has_acc && 32 * i < bn && col < p.Nout ? pow2_recip(__ldg(p.cscale + (int64_t)ti.e * p.Nout + col))
+                                                          : 0.f;
+        }
+      }
       if (has_acc) {
         if (!mbar_wait_warp(&tfull[acc], acc_phase, vabort)) {
           set_status(av.status, MGEMM_STATUS_TIMEOUT);
@@ -430,12 +442,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_arrive(&tempty[acc]);
           }
           if (C::Fp8) {
-            // column-scale reciprocals of this chunk, staged per warp and read as
-            // broadcasts (scales are powers of two: the reciprocal is exact)
+            // this chunk's column-scale reciprocals, staged per warp and read as broadcasts
             float *cs = s_csc + q * 64;
-            const int64_t cb = (int64_t)ti.e * p.Nout + col0;
-            cs[lane] = col0 + lane < p.Nout ? pow2_recip(__ldg(p.cscale + cb + lane)) : 0.f;
-            cs[lane + 32] = col0 + 32 + lane < p.Nout ? pow2_recip(__ldg(p.cscale + cb + 32 + lane)) : 0.f;
+            cs[lane] = csr[2 * c];
+            cs[lane + 32] = csr[2 * c + 1];
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
