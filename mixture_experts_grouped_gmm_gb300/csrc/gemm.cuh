@@ -23,9 +23,9 @@
 //               accumulators in TMEM, one thread issues
 //               tcgen05.mma (M=128, N=BN, K=16 bf16 / 32 e4m3) per 32-byte
 //               K step and commits stage-release / accumulator-ready events.
-//               On a wgrad tile whose contraction range does not cover the
-//               whole block (group edges) the warp first zeroes the
-//               out-of-group positions in shared memory.
+//               On a wgrad block at a group edge the warp issues only the
+//               k-steps that hold group rows and first zeroes the few
+//               out-of-group positions inside the partial step at each end.
 //   warps 2-5   epilogue, one TMEM lane quarter (32 output rows) each:
 //               tcgen05.ld, optional FP8 scale division, bf16 rounding, then
 //               128-byte-swizzled shared-memory staging buffers (2 per warp,
@@ -150,56 +150,46 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
   return ti;
 }
 
-// Zero the contraction positions outside [lo, hi) of one stage (positions are
-// relative to the block start).  Executed by all 32 lanes of the MMA warp.
-// bf16 (MN-major operands): whole 128-byte rows of A and B are cleared, so a
-// non-finite value in a neighbouring group cannot leak in.  FP8 (K-major
-// operands, codes written by the colwise quantizer and therefore finite): only
-// A is cleared -- a zero in A zeroes the product -- one row per lane, 16-byte
-// chunks, with a masked read-modify-write on the two boundary chunks.
+// Zero contraction positions [zlo, zhi) of one stage (positions relative to
+// the block start, all inside one MMA k-step).  Executed by all 32 lanes of
+// the MMA warp.  Positions of a block that fall in no group row are either in
+// k-steps the MMA skips altogether or in the one partial k-step at each end of
+// the group's range; only those few positions are cleared.
+// bf16 (MN-major operands): the rows of those positions are cleared in A and
+// B, so a non-finite value in a neighbouring group cannot leak in.  FP8
+// (K-major operands, codes written by the colwise quantizer and therefore
+// finite): only A is cleared -- a zero in A zeroes the product -- with a
+// masked read-modify-write of the (at most two) 16-byte chunks of each row.
 template <class C>
-__device__ __forceinline__ void mask_stage(uint8_t *sa, uint8_t *sb, int bn, int lo, int hi, int lane) {
+__device__ __forceinline__ void mask_positions(uint8_t *sa, uint8_t *sb, int bn, int zlo, int zhi, int lane) {
   if (C::AMn) {
-    const int nA = C::BM / 64, nB = bn / 64;
-    const int nrows = C::BK;
-    for (int idx = lane; idx < (nA + nB) * nrows; idx += 32) {
-      const int ch = idx / nrows, p = idx % nrows;
-      if (p >= lo && p < hi) continue;
+    const int nA = C::BM / 64, nch = nA + bn / 64;
+    const int nrows = zhi - zlo;
+    for (int idx = lane; idx < nch * nrows * 8; idx += 32) {  // 16-byte granules
+      const int g = idx & 7, rr = idx >> 3;
+      const int ch = rr / nrows, pos = zlo + rr % nrows;
       uint8_t *base = ch < nA ? sa + ch * C::CHUNK : sb + (ch - nA) * C::CHUNK;
-      uint4 *row = reinterpret_cast<uint4 *>(base + p * 128);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) row[j] = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(base + pos * 128 + g * 16) = make_uint4(0, 0, 0, 0);
     }
   } else {
-    // valid byte range of every 128-byte row; row r stores logical 16-byte
-    // chunk lc at physical chunk lc ^ (r & 7) (128-byte swizzle)
-    const int blo = max(lo, 0) * C::ESIZE, bhi = min(hi, C::BK) * C::ESIZE;
+    // row r stores logical 16-byte chunk lc at physical chunk lc ^ (r & 7) (128-byte swizzle)
+    const int blo = zlo * C::ESIZE, bhi = zhi * C::ESIZE;
     for (int r = lane; r < C::BM; r += 32) {
       uint8_t *rowp = sa + r * 128;
-#pragma unroll
-      for (int lc = 0; lc < 8; ++lc) {
-        const int b0 = lc * 16, b1 = b0 + 16;
-        if (b0 >= blo && b1 <= bhi) continue;
+      for (int lc = blo >> 4; lc * 16 < bhi; ++lc) {
+        const int b0 = lc * 16;
+        const int s0 = max(blo - b0, 0), s1 = min(bhi - b0, 16);  // bytes [s0, s1) of this chunk are cleared
+        const uint32_t clear16 = ((1u << s1) - 1u) & ~((1u << s0) - 1u);
         uint4 *ck = reinterpret_cast<uint4 *>(rowp + ((lc ^ (r & 7)) << 4));
-        if (b1 <= blo || b0 >= bhi) {
-          *ck = make_uint4(0, 0, 0, 0);
-          continue;
-        }
-        // keep bytes [max(b0, blo), min(b1, bhi)) of this chunk
-        const int s0 = max(blo - b0, 0), s1 = min(bhi - b0, 16);
-        const uint32_t keep16 = ((1u << s1) - 1u) & ~((1u << s0) - 1u);
-        uint32_t wm[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t bits = (keep16 >> (4 * w)) & 0xFu;
-          wm[w] = ((bits & 1u) ? 0x000000FFu : 0u) | ((bits & 2u) ? 0x0000FF00u : 0u) |
-                  ((bits & 4u) ? 0x00FF0000u : 0u) | ((bits & 8u) ? 0xFF000000u : 0u);
-        }
         uint4 v = *ck;
-        v.x &= wm[0];
-        v.y &= wm[1];
-        v.z &= wm[2];
-        v.w &= wm[3];
+        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t bits = (clear16 >> (4 * q)) & 0xFu;
+          const uint32_t m = ((bits & 1u) ? 0x000000FFu : 0u) | ((bits & 2u) ? 0x0000FF00u : 0u) |
+                             ((bits & 4u) ? 0x00FF0000u : 0u) | ((bits & 8u) ? 0xFF000000u : 0u);
+          w[q] &= ~m;
+        }
         *ck = v;
       }
     }
@@ -333,26 +323,50 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
         uint8_t *a = sA + stage * C::A_BYTES;
         uint8_t *b = sB + stage * C::B_BYTES;
-        if (C::Mode == kModeExperts) {
-          const int lo = ti.lo - kb * C::BK, hi = ti.hi - kb * C::BK;
-          if (lo > 0 || hi < C::BK) {
-            mask_stage<C>(a, b, bn, lo, hi, lane);
+        // wgrad: at a group's first and last block only the MMA k-steps
+        // [k_first, k_last] hold group rows; the others are skipped, and the
+        // out-of-group positions inside the partial steps are cleared
+        const bool edge = C::Mode == kModeExperts && (ti.lo - kb * C::BK > 0 || ti.hi - kb * C::BK < C::BK);
+        int k_first = 0, k_last = C::KSTEPS - 1;
+        if (edge) {
+          const int lo = max(ti.lo - kb * C::BK, 0), hi = min(ti.hi - kb * C::BK, C::BK);
+          k_first = lo / C::UK;
+          k_last = (hi - 1) / C::UK;
+          const bool head = lo > k_first * C::UK, tail = hi < (k_last + 1) * C::UK;
+          if (head) mask_positions<C>(a, b, bn, k_first * C::UK, lo, lane);
+          if (tail) mask_positions<C>(a, b, bn, hi, (k_last + 1) * C::UK, lane);
+          if (head || tail) {
             fence_proxy_async_smem();
             __syncwarp();
           }
         }
         if (lane == 0) {
           const uint32_t abase = smem_u32(a), bbase = smem_u32(b);
+          if (!edge) {
 #pragma unroll
-          for (int k = 0; k < C::KSTEPS; ++k) {
-            const uint64_t ad = C::AMn ? smem_desc_sw128(abase + k * C::UK * 128, C::CHUNK, 1024)
-                                       : smem_desc_sw128(abase + k * 32, 16, 1024);
-            const uint64_t bd = C::BMn ? smem_desc_sw128(bbase + k * C::UK * 128, C::CHUNK, 1024)
-                                       : smem_desc_sw128(bbase + k * 32, 16, 1024);
-            if (C::Fp8)
-              mma_f8(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
-            else
-              mma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+            for (int k = 0; k < C::KSTEPS; ++k) {
+              const uint64_t ad = C::AMn ? smem_desc_sw128(abase + k * C::UK * 128, C::CHUNK, 1024)
+                                         : smem_desc_sw128(abase + k * 32, 16, 1024);
+              const uint64_t bd = C::BMn ? smem_desc_sw128(bbase + k * C::UK * 128, C::CHUNK, 1024)
+                                         : smem_desc_sw128(bbase + k * 32, 16, 1024);
+              // the tile's first MMA overwrites the accumulator
+              if (C::Fp8)
+                mma_f8(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+              else
+                mma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+            }
+          } else {
+            for (int k = k_first; k <= k_last; ++k) {
+              const uint64_t ad = C::AMn ? smem_desc_sw128(abase + k * C::UK * 128, C::CHUNK, 1024)
+                                         : smem_desc_sw128(abase + k * 32, 16, 1024);
+              const uint64_t bd = C::BMn ? smem_desc_sw128(bbase + k * C::UK * 128, C::CHUNK, 1024)
+                                         : smem_desc_sw128(bbase + k * 32, 16, 1024);
+              const bool acc_on = kb > 0 || k > k_first;
+              if (C::Fp8)
+                mma_f8(d_tmem, ad, bd, p.idesc, acc_on);
+              else
+                mma_f16(d_tmem, ad, bd, p.idesc, acc_on);
+            }
           }
           mma_commit(&empty[stage]);
         }
