@@ -230,13 +230,14 @@ def deepseek_extra(torch, B, dev, pk, tokens=16384, reps=10):
     u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
     w_kn = d["w"]
     w_nk = w_kn.transpose(1, 2).contiguous()
+    ld = B.mgemm_colwise_ld(M, E)  # padded column-major FP8 layout of the colwise outputs
     T = dict(args=torch.empty(B.mgemm_args_bytes(E), dtype=u8, device=dev),
              xq=torch.empty(M, K, dtype=u8, device=dev), sx=torch.empty(M, dtype=f32, device=dev),
              goq=torch.empty(M, N, dtype=u8, device=dev), sgo=torch.empty(M, dtype=f32, device=dev),
              wq=torch.empty(E * N, K, dtype=u8, device=dev), sw=torch.empty(E * N, dtype=f32, device=dev),
              wdq=torch.empty(E * K, N, dtype=u8, device=dev), swd=torch.empty(E * K, dtype=f32, device=dev),
-             xqt=torch.empty(K * M, dtype=u8, device=dev), sxc=torch.empty(E * K, dtype=f32, device=dev),
-             goqt=torch.empty(N * M, dtype=u8, device=dev), sgoc=torch.empty(E * N, dtype=f32, device=dev),
+             xqt=torch.empty(K * ld, dtype=u8, device=dev), sxc=torch.empty(E * K, dtype=f32, device=dev),
+             goqt=torch.empty(N * ld, dtype=u8, device=dev), sgoc=torch.empty(E * N, dtype=f32, device=dev),
              out=torch.empty(M, N, dtype=bf, device=dev), gx=torch.empty(M, K, dtype=bf, device=dev),
              gw=torch.empty(E, K, N, dtype=bf, device=dev))
     x, go = d["x"], d["grad_out"]

@@ -69,6 +69,8 @@ typedef struct CUstream_st *mgemm_stream_t;
 #define MGEMM_MAX_EXPERTS 1024
 /* Rows per output tile; the fill kernel's tile prefix counts tiles of this height. */
 #define MGEMM_TILE_M 128
+/* Row padding of each group in the column-major FP8 layout (see mgemm_colwise_ld). */
+#define MGEMM_COL_PAD 128
 
 /*
  * Args block: a device buffer of mgemm_args_bytes(E) bytes, 16-byte aligned,
@@ -85,7 +87,11 @@ typedef struct CUstream_st *mgemm_stream_t;
  *   [A]   int32  active[E]     ids of the non-empty groups, ascending (first n_active valid)
  *   [T]   int32  mtile_start[E+1]  prefix over active groups of ceil(m_e / MGEMM_TILE_M)
  *   [W]   int32  wgrad_order[E]    all experts by m_e descending, ties by ascending id
- * with A = 24 + 8(E+1), T = A + 4E, W = T + 4(E+1); mgemm_args_layout returns them.
+ *   [P]   int64  poffsets[E+1] exclusive prefix sum of group_sizes each rounded up to
+ *                MGEMM_COL_PAD: where group e starts in the padded column-major
+ *                FP8 layout of mgemm_quant_colwise_grouped / mgemm_wgrad
+ * with A = 24 + 8(E+1), T = A + 4E, W = T + 4(E+1), P = W + 4E rounded up to a
+ * multiple of 8; mgemm_args_layout returns A, T and W.
  */
 size_t mgemm_args_bytes(int E);
 int mgemm_args_layout(int E, size_t *off_offsets, size_t *off_active, size_t *off_mtile_start,
@@ -123,24 +129,40 @@ int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t ld_in, uin
                         float *scales, mgemm_stream_t stream);
 
 /*
+ * mgemm_colwise_ld -- the smallest leading dimension (bytes per column) of the
+ * padded column-major FP8 layout for M rows in E groups: M plus the padding of
+ * up to min(M, E) non-empty groups, rounded up to MGEMM_COL_PAD.  Known on the
+ * host without the group sizes.  Returns -1 for M < 0 or E outside 1..MGEMM_MAX_EXPERTS.
+ * (Implementation choice, not in the paper: it sizes the layout below.)
+ */
+int64_t mgemm_colwise_ld(int64_t M, int E);
+
+/*
  * mgemm_quant_colwise_grouped -- per-group, per-column scale and e4m3 cast,
  * column-major output; optionally two tensors in one launch (dual form).
  * [FP8 _colwise_kernel]: for group g (rows offsets[g]..offsets[g+1]) and
  * column c, amax over the group's rows, the same power-of-two scale rule, the
  * scale stored at index c + C * g, the cast clamp(x * s) -> e4m3;
- * [FP8 run_experiment]: the output is column-major (strides (1, M));
+ * [FP8 run_experiment]: the output is column-major;
  * [FP8 commit message]: the dual kernel quantizes grad_output and A together.
  *   args        args block from mgemm_fill_args (group offsets, status)
  *   E, M        experts and rows (must match the args block)
  *   in1         bf16 [M, C1] row-major
- *   out1        fp8 column-major: out1[c * M + r] holds row r, column c  (C1 * M bytes)
+ *   out1        fp8, padded column-major: column c of group g occupies bytes
+ *               out1[c * ld + poffsets[g] ...], m_g codes followed by zeros up
+ *               to the next multiple of MGEMM_COL_PAD (C1 * ld bytes; bytes past
+ *               poffsets[E] in a column are not written)
  *   sc1         float32 [E * C1], sc1[c + C1 * g]
  *   in2/out2/sc2/C2  the second tensor; in2 == NULL selects the single form
- * C1, C2 % 8 == 0.  Empty groups get scale 2^48 (amax 0) and no data.
+ *   ld          bytes per output column: >= mgemm_colwise_ld(M, E), % 16 == 0
+ * C1, C2 % 8 == 0; out1, out2 16-byte aligned.  Empty groups get scale 2^48
+ * (amax 0) and no data.  The padding keeps every group's codes aligned and
+ * lets mgemm_wgrad contract whole 128-row blocks without masking (an
+ * implementation choice; the paper's layout is unpadded, strides (1, M)).
  */
 int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, const void *in1, int64_t C1,
                                 uint8_t *out1, float *sc1, const void *in2, int64_t C2, uint8_t *out2,
-                                float *sc2, mgemm_stream_t stream);
+                                float *sc2, int64_t ld, mgemm_stream_t stream);
 
 /*
  * mgemm_fwd -- out[r, :] = x[r, :] . w[e(r)] for every row r of every non-empty group.
@@ -178,13 +200,16 @@ int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *
  * [GRB review, ZeroOutK0Outputs]: k = 0 problems produce zeros;
  * [FP8 commit message]: grad_B uses per-group colwise scales of grad_output and A.
  *   dtype == MGEMM_BF16: x bf16 [M, K], grad_out bf16 [M, N] (row-major).
- *   dtype == MGEMM_FP8_E4M3: x fp8 column-major (x[c * M + r]) + sx float32
- *     [E * K]; grad_out fp8 column-major + sgo float32 [E * N] (the outputs of
- *     mgemm_quant_colwise_grouped); M % 16 == 0.
+ *   dtype == MGEMM_FP8_E4M3: x fp8 [K, ld] and grad_out fp8 [N, ld] in the
+ *     padded column-major layout of mgemm_quant_colwise_grouped (rows of group
+ *     e at poffsets[e], zero padding after them), sx float32 [E * K] and sgo
+ *     float32 [E * N] its scales; ld as passed to it.
+ *   ld        FP8: bytes per column of x and grad_out (% 16 == 0,
+ *             >= mgemm_colwise_ld(M, E)); ignored for MGEMM_BF16.
  *   grad_w    bf16 [E, K, N]; every element is written.
  */
 int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, const void *grad_out,
-                const float *sgo, void *grad_w, int64_t M, int K, int N, int E, mgemm_stream_t stream);
+                const float *sgo, void *grad_w, int64_t M, int K, int N, int E, int64_t ld, mgemm_stream_t stream);
 
 /*
  * mgemm_fwd_noalloc -- mgemm_fwd for callers that cannot allocate device memory.

@@ -21,6 +21,7 @@ MGEMM_BF16 = 0
 MGEMM_FP8_E4M3 = 1
 MGEMM_MAX_EXPERTS = 1024
 MGEMM_TILE_M = 128
+MGEMM_COL_PAD = 128
 STATUS = {0: "ok", 1: "negative group size", 2: "group sizes do not sum to M", 4: "pipeline wait timed out"}
 
 _lib = None
@@ -40,7 +41,9 @@ _SIGS = {
     "mgemm_quant_colwise_grouped": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                                    ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                   ctypes.c_void_p]),
+    "mgemm_colwise_ld": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int]),
     "mgemm_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
@@ -49,7 +52,7 @@ _SIGS = {
                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "mgemm_wgrad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
-                                   ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p]),
     "mgemm_fwd_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
@@ -118,11 +121,20 @@ def mgemm_quant_rowwise(inp, out, scales):
                                      _stream(inp)), "mgemm_quant_rowwise")
 
 
-def mgemm_quant_colwise_grouped(args, E, M, in1, out1, sc1, in2=None, out2=None, sc2=None):
+def mgemm_colwise_ld(M, E):
+    """Bytes per column of the padded column-major FP8 layout (a multiple of 128)."""
+    return int(lib().mgemm_colwise_ld(int(M), int(E)))
+
+
+def mgemm_quant_colwise_grouped(args, E, M, in1, out1, sc1, in2=None, out2=None, sc2=None, ld=None):
+    """out1 / out2: C * ld bytes (ld defaults to their size / C), padded column-major."""
     _cuda(args, in1, out1, sc1, in2, out2, sc2)
+    C1 = in1.shape[1]
     C2 = in2.shape[1] if in2 is not None else 0
-    _check(lib().mgemm_quant_colwise_grouped(_p(args), int(E), int(M), _p(in1), in1.shape[1], _p(out1), _p(sc1),
-                                             _p(in2), C2, _p(out2), _p(sc2), _stream(in1)),
+    if ld is None:
+        ld = out1.numel() // C1
+    _check(lib().mgemm_quant_colwise_grouped(_p(args), int(E), int(M), _p(in1), C1, _p(out1), _p(sc1),
+                                             _p(in2), C2, _p(out2), _p(sc2), int(ld), _stream(in1)),
            "mgemm_quant_colwise_grouped")
 
 
@@ -138,10 +150,13 @@ def mgemm_dgrad(args, dtype, grad_out, sgo, w, sw, grad_x, M, K, N, E):
                              int(K), int(N), int(E), _stream(grad_x)), "mgemm_dgrad")
 
 
-def mgemm_wgrad(args, dtype, x, sx, grad_out, sgo, grad_w, M, K, N, E):
+def mgemm_wgrad(args, dtype, x, sx, grad_out, sgo, grad_w, M, K, N, E, ld=None):
+    """FP8: x [K, ld] and grad_out [N, ld] padded column-major (ld defaults to x's size / K)."""
     _cuda(args, x, sx, grad_out, sgo, grad_w)
+    if ld is None:
+        ld = x.numel() // K if dtype == MGEMM_FP8_E4M3 and x is not None else 0
     _check(lib().mgemm_wgrad(_p(args), int(dtype), _p(x), _p(sx), _p(grad_out), _p(sgo), _p(grad_w), int(M),
-                             int(K), int(N), int(E), _stream(grad_w)), "mgemm_wgrad")
+                             int(K), int(N), int(E), int(ld), _stream(grad_w)), "mgemm_wgrad")
 
 
 def mgemm_fwd_noalloc(group_sizes, dtype, trans_b, x, sx, w, sw, out, M, K, N, E):

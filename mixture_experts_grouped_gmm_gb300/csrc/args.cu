@@ -68,6 +68,13 @@ __global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict
   __shared__ int64_t total_sh;
   if (t == E - 1) total_sh = incl;
 
+  // padded offsets: every group rounded up to kColPad rows
+  const int64_t padded = (m > 0 ? (m + kColPad - 1) / kColPad : 0) * kColPad;
+  const int64_t pincl = block_inclusive_scan<int64_t, NT>(padded, tot64);
+  int64_t *poffsets = (int64_t *)(args + L.poffsets);
+  if (t == 0) poffsets[0] = 0;
+  if (t < E) poffsets[t + 1] = pincl;
+
   // compaction of non-empty groups and their row-tile prefix
   const int flag = (t < E && m > 0) ? 1 : 0;
   const int pos = block_inclusive_scan<int, NT>(flag, tot32);
@@ -177,6 +184,13 @@ void note_error(const char *where, int code) {
 using namespace mgemm;
 
 extern "C" const char *mgemm_last_error(void) { return g_last_error; }
+
+extern "C" int64_t mgemm_colwise_ld(int64_t M, int E) {
+  if (M < 0 || E < 1 || E > MGEMM_MAX_EXPERTS) return -1;
+  const int64_t groups = M < E ? M : E;  // at most this many non-empty groups, each padded by < kColPad rows
+  const int64_t rows = M + (int64_t)(kColPad - 1) * groups;
+  return (rows + kColPad - 1) / kColPad * kColPad;
+}
 
 extern "C" size_t mgemm_args_bytes(int E) {
   if (E < 1 || E > MGEMM_MAX_EXPERTS) return 0;

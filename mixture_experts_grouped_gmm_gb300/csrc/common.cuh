@@ -34,8 +34,12 @@ int ensure_context();
 int sm_count_cached();
 
 // ---------------------------------------------------------------- args block
+// Rows of each group in the padded column-major FP8 layout are rounded up to this.
+constexpr int kColPad = MGEMM_COL_PAD;
+static_assert(kColPad % 16 == 0, "padded groups keep 16-byte alignment");
+
 struct ArgsLayout {
-  size_t offsets, active, mtile_start, wgrad_order, bytes;
+  size_t offsets, active, mtile_start, wgrad_order, poffsets, bytes;
 };
 
 __host__ __device__ inline ArgsLayout args_layout(int E) {
@@ -44,7 +48,8 @@ __host__ __device__ inline ArgsLayout args_layout(int E) {
   L.active = L.offsets + 8 * (size_t)(E + 1);
   L.mtile_start = L.active + 4 * (size_t)E;
   L.wgrad_order = L.mtile_start + 4 * (size_t)(E + 1);
-  L.bytes = (L.wgrad_order + 4 * (size_t)E + 15) & ~(size_t)15;
+  L.poffsets = (L.wgrad_order + 4 * (size_t)E + 7) & ~(size_t)7;
+  L.bytes = (L.poffsets + 8 * (size_t)(E + 1) + 15) & ~(size_t)15;
   return L;
 }
 
@@ -56,6 +61,7 @@ struct ArgsView {
   const int *active;
   const int *mtile_start;
   const int *wgrad_order;
+  const int64_t *poffsets;  // padded column-major layout: group e starts at poffsets[e]
   __device__ ArgsView(const void *base, int E) {
     uint8_t *b = (uint8_t *)base;
     ArgsLayout L = args_layout(E);
@@ -66,6 +72,7 @@ struct ArgsView {
     active = (const int *)(b + L.active);
     mtile_start = (const int *)(b + L.mtile_start);
     wgrad_order = (const int *)(b + L.wgrad_order);
+    poffsets = (const int64_t *)(b + L.poffsets);
   }
 };
 

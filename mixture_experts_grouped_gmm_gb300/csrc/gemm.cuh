@@ -23,9 +23,10 @@
 //               accumulators in TMEM, one thread issues
 //               tcgen05.mma (M=128, N=BN, K=16 bf16 / 32 e4m3) per 32-byte
 //               K step and commits stage-release / accumulator-ready events.
-//               On a wgrad block at a group edge the warp issues only the
-//               k-steps that hold group rows and first zeroes the few
-//               out-of-group positions inside the partial step at each end.
+//               On the partial last block of a group in bf16 wgrad the warp
+//               issues only the k-steps that hold group rows and first zeroes
+//               the few out-of-group positions inside the partial step (FP8
+//               wgrad reads the padded layout, whose blocks are whole).
 //   warps 2-5   epilogue, one TMEM lane quarter (32 output rows) each:
 //               tcgen05.ld, optional FP8 scale division, bf16 rounding, then
 //               128-byte-swizzled shared-memory staging buffers (2 per warp,
@@ -136,13 +137,23 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
     const int i = t / per_e;
     const int mk = (t % per_e) / p.n_tiles;
     ti.e = __ldg(av.wgrad_order + i);
-    const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
-    // fp8 operands are column-major, so the group's first row is the TMA inner
-    // coordinate: start the box on a 128-byte boundary and mask the head
-    ti.x0 = C::Fp8 ? (int)(rs & ~(int64_t)127) : (int)rs;
-    ti.lo = (int)(rs - ti.x0);
-    ti.hi = (int)(re - ti.x0);
-    ti.kb_count = re > rs ? (ti.hi + C::BK - 1) / C::BK : 0;
+    if (C::Fp8) {
+      // padded column-major operands: the group's rows start 128-aligned at
+      // poffsets[e] and are followed by zeros up to a multiple of 128, so
+      // every block is whole and nothing is masked
+      const int64_t ps = __ldg(av.poffsets + ti.e), pe = __ldg(av.poffsets + ti.e + 1);
+      ti.x0 = (int)ps;
+      ti.lo = 0;
+      ti.hi = (int)(pe - ps);
+      ti.kb_count = ti.hi / C::BK;
+    } else {
+      // row-major operands: the group's rows are the TMA outer coordinate
+      const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
+      ti.x0 = (int)rs;
+      ti.lo = 0;
+      ti.hi = (int)(re - rs);
+      ti.kb_count = re > rs ? (ti.hi + C::BK - 1) / C::BK : 0;
+    }
     ti.a_row = mk * C::BM;
     ti.out_row0 = ti.e * p.Kout + mk * C::BM;
     ti.out_rows = min(C::BM, p.Kout - mk * C::BM);
@@ -152,49 +163,21 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
 
 // Zero contraction positions [zlo, zhi) of one stage (positions relative to
 // the block start, all inside one MMA k-step).  Executed by all 32 lanes of
-// the MMA warp.  Positions of a block that fall in no group row are either in
-// k-steps the MMA skips altogether or in the one partial k-step at each end of
-// the group's range; only those few positions are cleared.
-// bf16 (MN-major operands): the rows of those positions are cleared in A and
-// B, so a non-finite value in a neighbouring group cannot leak in.  FP8
-// (K-major operands, codes written by the colwise quantizer and therefore
-// finite): only A is cleared -- a zero in A zeroes the product -- with a
-// masked read-modify-write of the (at most two) 16-byte chunks of each row.
+// the MMA warp.  Only bf16 wgrad has partial blocks (the tail of a group's
+// rows; its operands are the row-major activations, MN-major in shared
+// memory): the rows of those positions are cleared in A and B, so a
+// non-finite value in the next group cannot leak in.  FP8 wgrad reads the
+// padded column-major layout, whose blocks are always whole.
 template <class C>
 __device__ __forceinline__ void mask_positions(uint8_t *sa, uint8_t *sb, int bn, int zlo, int zhi, int lane) {
-  if (C::AMn) {
-    const int nA = C::BM / 64, nch = nA + bn / 64;
-    const int nrows = zhi - zlo;
-    for (int idx = lane; idx < nch * nrows * 8; idx += 32) {  // 16-byte granules
-      const int g = idx & 7, rr = idx >> 3;
-      const int ch = rr / nrows, pos = zlo + rr % nrows;
-      uint8_t *base = ch < nA ? sa + ch * C::CHUNK : sb + (ch - nA) * C::CHUNK;
-      *reinterpret_cast<uint4 *>(base + pos * 128 + g * 16) = make_uint4(0, 0, 0, 0);
-    }
-  } else {
-    // row r stores logical 16-byte chunk lc at physical chunk lc ^ (r & 7) (128-byte swizzle)
-    const int blo = zlo * C::ESIZE, bhi = zhi * C::ESIZE;
-    for (int r = lane; r < C::BM; r += 32) {
-      uint8_t *rowp = sa + r * 128;
-      for (int lc = blo >> 4; lc * 16 < bhi; ++lc) {
-        const int b0 = lc * 16;
-        const int s0 = max(blo - b0, 0), s1 = min(bhi - b0, 16);  // bytes [s0, s1) of this chunk are cleared
-        const uint32_t clear16 = ((1u << s1) - 1u) & ~((1u << s0) - 1u);
-        uint4 *ck = reinterpret_cast<uint4 *>(rowp + ((lc ^ (r & 7)) << 4));
-        uint4 v = *ck;
-        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t bits = (clear16 >> (4 * q)) & 0xFu;
-          const uint32_t m = ((bits & 1u) ? 0x000000FFu : 0u) | ((bits & 2u) ? 0x0000FF00u : 0u) |
-                             ((bits & 4u) ? 0x00FF0000u : 0u) | ((bits & 8u) ? 0xFF000000u : 0u);
-          w[q] &= ~m;
-        }
-        *ck = v;
-      }
-    }
-    (void)sb;
-    (void)bn;
+  static_assert(!C::Fp8 && C::AMn && C::BMn, "only MN-major bf16 operands have partial blocks");
+  const int nA = C::BM / 64, nch = nA + bn / 64;
+  const int nrows = zhi - zlo;
+  for (int idx = lane; idx < nch * nrows * 8; idx += 32) {  // 16-byte granules
+    const int g = idx & 7, rr = idx >> 3;
+    const int ch = rr / nrows, pos = zlo + rr % nrows;
+    uint8_t *base = ch < nA ? sa + ch * C::CHUNK : sb + (ch - nA) * C::CHUNK;
+    *reinterpret_cast<uint4 *>(base + pos * 128 + g * 16) = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -323,18 +306,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
         uint8_t *a = sA + stage * C::A_BYTES;
         uint8_t *b = sB + stage * C::B_BYTES;
-        // wgrad: at a group's first and last block only the MMA k-steps
-        // [k_first, k_last] hold group rows; the others are skipped, and the
-        // out-of-group positions inside the partial steps are cleared
-        const bool edge = C::Mode == kModeExperts && (ti.lo - kb * C::BK > 0 || ti.hi - kb * C::BK < C::BK);
+        // bf16 wgrad: at the partial last block of a group only the MMA
+        // k-steps [k_first, k_last] hold group rows; the others are skipped,
+        // and the out-of-group positions inside the partial step are cleared
+        constexpr bool kPartial = C::Mode == kModeExperts && !C::Fp8;
+        const bool edge = kPartial && (ti.lo - kb * C::BK > 0 || ti.hi - kb * C::BK < C::BK);
         int k_first = 0, k_last = C::KSTEPS - 1;
         if (edge) {
           const int lo = max(ti.lo - kb * C::BK, 0), hi = min(ti.hi - kb * C::BK, C::BK);
           k_first = lo / C::UK;
           k_last = (hi - 1) / C::UK;
           const bool head = lo > k_first * C::UK, tail = hi < (k_last + 1) * C::UK;
-          if (head) mask_positions<C>(a, b, bn, k_first * C::UK, lo, lane);
-          if (tail) mask_positions<C>(a, b, bn, hi, (k_last + 1) * C::UK, lane);
+          if constexpr (kPartial) {
+            if (head) mask_positions<C>(a, b, bn, k_first * C::UK, lo, lane);
+            if (tail) mask_positions<C>(a, b, bn, hi, (k_last + 1) * C::UK, lane);
+          }
           if (head || tail) {
             fence_proxy_async_smem();
             __syncwarp();

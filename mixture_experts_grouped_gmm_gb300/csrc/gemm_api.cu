@@ -188,7 +188,8 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
 }
 
 extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, const void *grad_out,
-                           const float *sgo, void *grad_w, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
+                           const float *sgo, void *grad_w, int64_t M, int K, int N, int E, int64_t ld,
+                           mgemm_stream_t stream) {
   int rc = common_checks(args, dtype, M, K, N, E);
   if (rc) return rc;
   if (!grad_w) return MGEMM_EINVAL;
@@ -196,20 +197,22 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
   if (!aligned16(grad_w) || (M > 0 && (!aligned16(x) || !aligned16(grad_out)))) return MGEMM_EALIGN;
   const bool fp8 = dtype == MGEMM_FP8_E4M3;
   if (fp8 && (!sx || !sgo)) return MGEMM_EINVAL;
-  if (fp8 && M % 16) return MGEMM_EALIGN;
+  if (fp8 && (ld < mgemm_colwise_ld(M, E) || ld >= (int64_t(1) << 31))) return MGEMM_EINVAL;
+  if (fp8 && ld % 16) return MGEMM_EALIGN;
   // With M == 0 every expert is empty: the kernel only writes zeros and never
   // loads, so the maps just need a valid description of some memory.
   const void *xa = M > 0 ? x : grad_w;
   const void *ga = M > 0 ? grad_out : grad_w;
   const uint64_t Mm = M > 0 ? (uint64_t)M : 16;
+  const uint64_t Lm = fp8 && ld > 0 ? (uint64_t)ld : 16;
   if ((rc = ensure_context())) return rc;
   const int mt_k = (K + 127) / 128;
   const int bn = choose_bn((int64_t)E * mt_k, N);
   CUtensorMap ta, tb;
   if (fp8) {
-    // column-major operands: x^T [K, M] and grad_out^T [N, M], contraction contiguous
-    const uint64_t da[2] = {Mm, (uint64_t)K}, db[2] = {Mm, (uint64_t)N};
-    const uint64_t st[1] = {Mm};
+    // padded column-major operands: x^T [K, ld] and grad_out^T [N, ld], contraction contiguous
+    const uint64_t da[2] = {Lm, (uint64_t)K}, db[2] = {Lm, (uint64_t)N};
+    const uint64_t st[1] = {Lm};
     const uint32_t boxa[2] = {128, 128}, boxb[2] = {128, (uint32_t)bn};
     if (!make_map(&ta, true, 2, xa, da, st, boxa)) return MGEMM_ECUDA;
     if (!make_map(&tb, true, 2, ga, db, st, boxb)) return MGEMM_ECUDA;

@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 //   warp 16 (one thread): streams boxes of 256 rows x 64 columns (32 KB,
 //            128-byte swizzle) of the item's column block through a 5-stage
 //            ring (160 KB of loads in flight per SM), running ahead across
-//            items.  Rows count from the group's first row rounded down to
-//            16, so the 16-row output segments of every column are aligned.
+//            items.  Boxes start at the group's first row and cover its rows
+//            rounded up to kColPad (the padded length of its output column).
 //   warps 0-15: warp w owns columns 8*(w % 8) .. +7 and rows 128*(w / 8) ..
 //            +127 of each box.  ldmatrix.x4.trans reads 32 rows x 8 columns
 //            (conflict-free under the swizzle) and hands lane t, in each of
@@ -122,12 +122,18 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 //            each register with one packed fp32 multiply and converts it to an
 //            e4m3 pair that is already in column-major order, stores it as 16
 //            bits into one of two [64 columns][256 rows] tiles, and the CTA
-//            writes that tile out as 16-byte column-contiguous stores (byte
-//            stores on ragged group edges) while the next box is converted
-//            into the other tile.  A group spanning at most 5 boxes stays in
-//            the ring between the passes instead of being reloaded.
-// The CTA first copies the group offsets and the size order into shared
-// memory.  Consumer warps synchronize with a hardware barrier (see
+//            writes that tile out as 16-byte column-contiguous stores while
+//            the next box is converted into the other tile.  Rows past the
+//            group are cleared before the cast, so the padding of every
+//            column is written as zero codes.  A group spanning at most 5
+//            boxes stays in the ring between the passes instead of being
+//            reloaded.
+// Output: the padded column-major layout -- column c of group g starts at
+// out[c * ld + poffsets[g]] (poffsets from the args block), m_g codes then
+// zeros up to a multiple of kColPad; every start is 128-byte aligned, so the
+// FP8 wgrad reads whole, aligned 128-row blocks of every group.
+// The CTA first copies the group offsets, padded offsets and the size order
+// into shared memory.  Consumer warps synchronize with a hardware barrier (see
 // cw_consumer_barrier_any); every pipeline wait is bounded and gives up after about
 // 1 s with MGEMM_STATUS_TIMEOUT.
 constexpr int kCwRows = 256;
@@ -138,8 +144,10 @@ constexpr int kCwBox = kCwRows * 128;   // 32 KB
 constexpr int kCwPitch = kCwRows + 16;  // transposed tile: bytes per column
 constexpr int kCwQueue = 4;  // item ids handed from the producer to the consumers
 constexpr size_t kCwSmemFixed = 1024 + (size_t)kCwStages * kCwBox + 2 * 64 * kCwPitch + 2 * 2 * 64 * 4 + 256;
-// plus a copy of the group offsets and the size order: 8 (E + 1) + 4 E bytes
-__host__ __device__ constexpr size_t cw_smem_bytes(int E) { return kCwSmemFixed + 8 * (size_t)(E + 1) + 4 * (size_t)E + 16; }
+// plus a copy of the group offsets, the padded offsets and the size order: 16 (E + 1) + 4 E bytes
+__host__ __device__ constexpr size_t cw_smem_bytes(int E) {
+  return kCwSmemFixed + 16 * (size_t)(E + 1) + 4 * (size_t)E + 16;
+}
 
 struct ColTensor {
   uint8_t *out;
@@ -150,11 +158,13 @@ struct ColTensor {
 
 struct CwItem {
   int tensor, g, cb, nck;
-  int64_t rs, re, base;
+  int64_t rs, re;  // the group's rows
+  int64_t plen;    // its padded length (rows rounded up to kColPad)
+  int64_t pos;     // where its rows start in each output column
 };
 
-__device__ __forceinline__ CwItem cw_decode(int item, const int64_t *off, const int *order, const ColTensor &t1,
-                                            const ColTensor &t2) {
+__device__ __forceinline__ CwItem cw_decode(int item, const int64_t *off, const int64_t *poff, const int *order,
+                                            const ColTensor &t1, const ColTensor &t2) {
   CwItem it;
   const int per_group = t1.ncb + t2.ncb;
   it.g = order[item / per_group];
@@ -163,8 +173,9 @@ __device__ __forceinline__ CwItem cw_decode(int item, const int64_t *off, const 
   it.cb = it.tensor == 0 ? cb : cb - t1.ncb;
   it.rs = off[it.g];
   it.re = off[it.g + 1];
-  it.base = it.rs & ~(int64_t)15;
-  it.nck = it.re > it.rs ? (int)((it.re - it.base + kCwRows - 1) / kCwRows) : 0;
+  it.plen = (it.re - it.rs + kColPad - 1) / kColPad * kColPad;
+  it.pos = poff[it.g];
+  it.nck = (int)((it.plen + kCwRows - 1) / kCwRows);
   return it;
 }
 
@@ -221,7 +232,7 @@ __device__ __forceinline__ bool cw_consumer_barrier_any(bool flag) {
 
 __global__ void __launch_bounds__(kCwThreads, 1)
     quant_colwise_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm2,
-                         const uint8_t *__restrict__ args, int E, int64_t M, ColTensor t1, ColTensor t2, int vec_ok,
+                         const uint8_t *__restrict__ args, int E, int64_t ld, ColTensor t1, ColTensor t2,
                          int items) {
   extern __shared__ uint8_t cw_smem_raw[];
   uint8_t *smem =
@@ -236,12 +247,16 @@ __global__ void __launch_bounds__(kCwThreads, 1)
   int *abort_flag = reinterpret_cast<int *>(qempty + kCwQueue);
   int *s_item = abort_flag + 1;  // [kCwQueue]
   int64_t *s_off = reinterpret_cast<int64_t *>(smem + (kCwSmemFixed - 1024));  // [E + 1]
-  int *s_order = reinterpret_cast<int *>(s_off + E + 1);                      // [E]
+  int64_t *s_poff = s_off + E + 1;                                              // [E + 1]
+  int *s_order = reinterpret_cast<int *>(s_poff + E + 1);                     // [E]
 
   const ArgsView av(args, E);
   if (*av.status != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = av.offsets[i];
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    s_off[i] = av.offsets[i];
+    s_poff[i] = av.poffsets[i];
+  }
   for (int i = threadIdx.x; i < E; i += blockDim.x) s_order[i] = av.wgrad_order[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kCwStages; ++s) {
@@ -286,7 +301,7 @@ __global__ void __launch_bounds__(kCwThreads, 1)
           qphase ^= 1;
         }
         if (done) break;
-        const CwItem it = cw_decode(item, s_off, s_order, t1, t2);
+        const CwItem it = cw_decode(item, s_off, s_poff, s_order, t1, t2);
         const CUtensorMap *tm = it.tensor == 0 ? &tm1 : &tm2;
         const int passes = it.nck <= kCwStages ? 1 : 2;
         for (int pass = 0; pass < passes && !*vabort; ++pass) {
@@ -298,7 +313,7 @@ __global__ void __launch_bounds__(kCwThreads, 1)
             }
             mbar_arrive_expect_tx(&full[stage], kCwBox);
             ++issued;
-            tma_load_2d(ring + stage * kCwBox, tm, &full[stage], it.cb * 64, (int)(it.base + (int64_t)k * kCwRows));
+            tma_load_2d(ring + stage * kCwBox, tm, &full[stage], it.cb * 64, (int)(it.rs + (int64_t)k * kCwRows));
             if (++stage == kCwStages) {
               stage = 0;
               phase ^= 1;
@@ -342,7 +357,7 @@ __global__ void __launch_bounds__(kCwThreads, 1)
         qphase ^= 1;
       }
       if (cw_consumer_barrier_any(item < 0 || *vabort != 0)) break;
-      const CwItem it = cw_decode(item, s_off, s_order, t1, t2);
+      const CwItem it = cw_decode(item, s_off, s_poff, s_order, t1, t2);
       const ColTensor &T = it.tensor == 0 ? t1 : t2;
       const int64_t col0 = (int64_t)it.cb * 64;
       if (it.nck == 0) {  // empty group: amax 0 -> scale 2^48, no data
@@ -361,8 +376,8 @@ __global__ void __launch_bounds__(kCwThreads, 1)
       for (int k = 0; k < it.nck; ++k) {
         wait_full();
         const uint8_t *box = ring + stage * kCwBox;
-        const int64_t r0 = it.base + (int64_t)k * kCwRows + rhalf * 128;
-        const bool edge = (k == 0) || (k == it.nck - 1);
+        const int64_t r0 = it.rs + (int64_t)k * kCwRows + rhalf * 128;
+        const bool edge = it.rs + (int64_t)(k + 1) * kCwRows > it.re;  // the box runs past the group
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t v[4];
@@ -372,8 +387,8 @@ __global__ void __launch_bounds__(kCwThreads, 1)
             uint32_t x = v[m];
             if (edge) {
               const int64_t gr = r0 + j * 32 + m * 8 + rpair;  // rows gr (low half), gr + 1 (high half)
-              if (gr < it.rs || gr >= it.re) x &= 0xFFFF0000u;
-              if (gr + 1 < it.rs || gr + 1 >= it.re) x &= 0x0000FFFFu;
+              if (gr >= it.re) x &= 0xFFFF0000u;
+              if (gr + 1 >= it.re) x &= 0x0000FFFFu;
             }
             am = bf16x2_absmax(am, x);
           }
@@ -406,13 +421,23 @@ __global__ void __launch_bounds__(kCwThreads, 1)
         uint8_t *tile = tiles + tile_par * (64 * kCwPitch);
         tile_par ^= 1;
         uint8_t *tcol = tile + lcol * kCwPitch + rhalf * 128 + rpair;
+        // rows past the group become zero codes: the padding of the column
+        const int64_t r0 = it.rs + (int64_t)k * kCwRows + rhalf * 128;
+        const bool edge = it.rs + (int64_t)(k + 1) * kCwRows > it.re;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t v[4];
           ldsm_x4_trans(row_addr(box, j), v);
 #pragma unroll
-          for (int m = 0; m < 4; ++m)
-            *reinterpret_cast<uint16_t *>(tcol + j * 32 + m * 8) = bf16x2_scaled_e4m3x2(v[m], sc2);
+          for (int m = 0; m < 4; ++m) {
+            uint32_t x = v[m];
+            if (edge) {
+              const int64_t gr = r0 + j * 32 + m * 8 + rpair;
+              if (gr >= it.re) x &= 0xFFFF0000u;
+              if (gr + 1 >= it.re) x &= 0x0000FFFFu;
+            }
+            *reinterpret_cast<uint16_t *>(tcol + j * 32 + m * 8) = bf16x2_scaled_e4m3x2(x, sc2);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);  // box consumed; the codes live in the tile
@@ -427,24 +452,16 @@ __global__ void __launch_bounds__(kCwThreads, 1)
           break;
         }
         // 64 columns x 16 segments of 16 rows, 512 consumer threads: this
-        // thread stores segment st_seg of columns st_c and st_c + 32
-        const int64_t q0 = it.base + (int64_t)k * kCwRows + st_seg * 16;
-        const bool inner = vec_ok && q0 >= it.rs && q0 + 16 <= it.re;
+        // thread stores segment st_seg of columns st_c and st_c + 32 (whole
+        // 16-byte segments: the group's padded rows are a multiple of 16)
+        const int64_t q0 = (int64_t)k * kCwRows + st_seg * 16;  // offset inside the group's padded rows
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int c = st_c + 32 * u;
           const int64_t col = col0 + c;
-          if (col >= T.C || q0 >= it.re || q0 + 16 <= it.rs) continue;
-          uint8_t *dst = T.out + col * M + q0;
-          const uint8_t *srcb = tile + c * kCwPitch + st_seg * 16;
-          if (inner) {
-            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(srcb);
-          } else {
-            for (int jj = 0; jj < 16; ++jj) {
-              const int64_t rr = q0 + jj;
-              if (rr >= it.rs && rr < it.re) dst[jj] = srcb[jj];
-            }
-          }
+          if (col >= T.C || q0 >= it.plen) continue;
+          *reinterpret_cast<uint4 *>(T.out + col * ld + it.pos + q0) =
+              *reinterpret_cast<const uint4 *>(tile + c * kCwPitch + st_seg * 16);
         }
       }
       if (aborted) break;
@@ -498,15 +515,16 @@ extern "C" int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t
 
 extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, const void *in1, int64_t C1,
                                            uint8_t *out1, float *sc1, const void *in2, int64_t C2,
-                                           uint8_t *out2, float *sc2, mgemm_stream_t stream) {
+                                           uint8_t *out2, float *sc2, int64_t ld, mgemm_stream_t stream) {
   if (!args || !in1 || !out1 || !sc1) return MGEMM_EINVAL;
   if (E < 1) return MGEMM_EINVAL;
   if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
   if (M < 0 || M >= (int64_t(1) << 31) || C1 <= 0 || C1 % 8) return MGEMM_EINVAL;
-  if (((uintptr_t)args & 15) || ((uintptr_t)in1 & 15)) return MGEMM_EALIGN;
+  if (ld < mgemm_colwise_ld(M, E)) return MGEMM_EINVAL;
+  if (((uintptr_t)args & 15) || ((uintptr_t)in1 & 15) || ((uintptr_t)out1 & 15) || ld % 16) return MGEMM_EALIGN;
   if (in2) {
     if (!out2 || !sc2 || C2 <= 0 || C2 % 8) return MGEMM_EINVAL;
-    if ((uintptr_t)in2 & 15) return MGEMM_EALIGN;
+    if (((uintptr_t)in2 & 15) || ((uintptr_t)out2 & 15)) return MGEMM_EALIGN;
   }
   int rc = ensure_context();
   if (rc) return rc;
@@ -529,7 +547,6 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
   }
   ColTensor t1{out1, sc1, C1, (int)((C1 + 63) / 64)};
   ColTensor t2{out2, sc2, in2 ? C2 : 0, in2 ? (int)((C2 + 63) / 64) : 0};
-  const int vec_ok = (M % 16 == 0) && (((uintptr_t)out1 & 15) == 0) && (!in2 || (((uintptr_t)out2 & 15) == 0));
   const int64_t items = (int64_t)E * (t1.ncb + t2.ncb);
   if (items >= (int64_t(1) << 31)) return MGEMM_EINVAL;
   const int sms = sm_count_cached();
@@ -546,6 +563,6 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
     attr_done[dev] = true;
   }
   quant_colwise_kernel<<<grid, kCwThreads, cw_smem_bytes(E), (cudaStream_t)stream>>>(
-      tm1, tm2, (const uint8_t *)args, E, M, t1, t2, vec_ok, (int)items);
+      tm1, tm2, (const uint8_t *)args, E, ld, t1, t2, (int)items);
   return cuda_rc(cudaGetLastError(), "mgemm_quant_colwise_grouped launch");
 }

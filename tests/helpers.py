@@ -41,7 +41,37 @@ def parse_args(args, E):
     out["mtile_start"] = np.frombuffer(raw[lay["mtile_start"]:lay["mtile_start"] + 4 * (E + 1)],
                                        dtype=np.int32).tolist()
     out["wgrad_order"] = np.frombuffer(raw[lay["wgrad_order"]:lay["wgrad_order"] + 4 * E], dtype=np.int32).tolist()
+    P = (lay["wgrad_order"] + 4 * E + 7) // 8 * 8           # header: W + 4E rounded up to 8
+    out["poffsets"] = np.frombuffer(raw[P:P + 8 * (E + 1)], dtype=np.int64).tolist()
     return out
+
+
+COL_PAD = 128  # MGEMM_COL_PAD
+
+
+def padded_offsets(sizes, pad=COL_PAD):
+    """Where each group starts in the padded column-major FP8 layout (the header's
+    poffsets): the prefix sum of the group sizes, each rounded up to pad."""
+    p = [0]
+    for m in sizes:
+        p.append(p[-1] + -(-int(m) // pad) * pad)
+    return p
+
+
+def unpad_colwise(buf, C, ld, sizes):
+    """[C, ld] padded column-major codes -> [C, M] (the groups' rows only)."""
+    a = np.asarray(buf).reshape(C, ld)
+    po = padded_offsets(sizes)
+    parts = [a[:, po[g]:po[g] + int(m)] for g, m in enumerate(sizes)]
+    return np.concatenate(parts, axis=1) if parts else a[:, :0]
+
+
+def colwise_padding(buf, C, ld, sizes):
+    """The padding bytes of every group and column (must all be zero codes)."""
+    a = np.asarray(buf).reshape(C, ld)
+    po = padded_offsets(sizes)
+    parts = [a[:, po[g] + int(m):po[g + 1]] for g, m in enumerate(sizes)]
+    return np.concatenate(parts, axis=1) if parts else a[:, :0]
 
 
 def new_args(E, device):

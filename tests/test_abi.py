@@ -86,8 +86,9 @@ def test_host_checks_gemms(lib):
     assert lib.mgemm_fwd(a, 0, 0, x, None, w, None, o, 64, 128, 256, 2000, None) == -3
     assert lib.mgemm_fwd(a, 0, 0, x, None, w, None, o, 0, 128, 256, 4, None) == 0          # M = 0: nothing to do
     assert lib.mgemm_dgrad(a, 0, x, None, w, None, None, 64, 128, 256, 4, None) == -1
-    assert lib.mgemm_wgrad(a, 1, x, s, w, s, o, 72, 128, 256, 4, None) == -2               # fp8 wgrad M % 16
-    assert lib.mgemm_wgrad(a, 0, x, None, w, None, None, 64, 128, 256, 4, None) == -1
+    assert lib.mgemm_wgrad(a, 1, x, s, w, s, o, 64, 128, 256, 4, 64, None) == -1           # fp8 ld < colwise_ld
+    assert lib.mgemm_wgrad(a, 1, x, s, w, s, o, 64, 128, 256, 4, 648, None) == -2          # fp8 ld % 16
+    assert lib.mgemm_wgrad(a, 0, x, None, w, None, None, 64, 128, 256, 4, 0, None) == -1
 
 
 def test_host_checks_quant(lib):
@@ -95,8 +96,26 @@ def test_host_checks_quant(lib):
     assert lib.mgemm_quant_rowwise(i, 4, 12, 12, o, 16, s, None) == -1                    # C % 8
     assert lib.mgemm_quant_rowwise(i, 4, 16, 16, o, 24, s, None) == -2                    # ld_out % 16
     assert lib.mgemm_quant_rowwise(i, 0, 16, 16, o, 16, s, None) == 0                     # empty: no launch
-    assert lib.mgemm_quant_colwise_grouped(None, 4, 64, i, 64, o, s, None, 0, None, None, None) == -1
-    assert lib.mgemm_quant_colwise_grouped(i, 4, 64, i, 60, o, s, None, 0, None, None, None) == -1
+    assert lib.mgemm_quant_colwise_grouped(None, 4, 64, i, 64, o, s, None, 0, None, None, 640, None) == -1
+    assert lib.mgemm_quant_colwise_grouped(i, 4, 64, i, 60, o, s, None, 0, None, None, 640, None) == -1  # C % 8
+    assert lib.mgemm_quant_colwise_grouped(i, 4, 64, i, 64, o, s, None, 0, None, None, 512, None) == -1  # ld small
+    assert lib.mgemm_quant_colwise_grouped(i, 4, 64, i, 64, o, s, None, 0, None, None, 648, None) == -2  # ld % 16
+
+
+def test_colwise_ld_bounds_the_padded_layout():
+    # M rows in at most min(M, E) non-empty groups, each padded by fewer than
+    # MGEMM_COL_PAD rows, rounded up to MGEMM_COL_PAD
+    from mixture_experts_grouped_gmm_gb300 import binding as B
+
+    pad = B.MGEMM_COL_PAD
+    for M, E in ((64, 4), (0, 4), (1, 1), (1, 128), (98304, 64), (1000, 1024), (5, 3)):
+        want = -(-(M + (pad - 1) * min(M, E)) // pad) * pad
+        assert B.mgemm_colwise_ld(M, E) == want, (M, E)
+        # enough for the worst split: min(M, E) groups of one row each, the rest in one group
+        g = min(M, E)
+        worst = (g - 1) * pad + (-(-(M - g + 1) // pad) * pad if M else 0) if g else 0
+        assert B.mgemm_colwise_ld(M, E) >= worst
+    assert B.mgemm_colwise_ld(-1, 4) == -1 and B.mgemm_colwise_ld(10, 0) == -1 and B.mgemm_colwise_ld(10, 1025) == -1
 
 
 def test_product_never_imports_the_oracle():

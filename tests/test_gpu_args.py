@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from oracle.args import fill_args
-from tests.helpers import new_args, parse_args
+from tests.helpers import new_args, padded_offsets, parse_args
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -36,6 +36,7 @@ def compare(sizes):
     assert got["active"][:na] == ref["active"]
     assert got["mtile_start"][:na + 1] == ref["mtile_start"]
     assert got["wgrad_order"] == ref["wgrad_order"]
+    assert got["poffsets"] == padded_offsets(sizes)
 
 
 @pytest.mark.parametrize("E", [1, 2, 4, 8, 31, 32, 33, 64, 128, 129, 500, 1000, 1024])

@@ -13,7 +13,8 @@ import pytest
 import torch
 
 from oracle import formats, gmm as og, quant as oq
-from tests.helpers import BF16_TOL, FP8_TOL, assert_close, is_sentinel, new_args, sentinel_bf16, to_np
+from tests.helpers import (BF16_TOL, FP8_TOL, assert_close, colwise_padding, is_sentinel, new_args, sentinel_bf16,
+                           to_np, unpad_colwise)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -174,13 +175,13 @@ FP8_CASES = [
     ([5, 0, 37, 100, 2], 256, 272),           # M = 144; group starts off 16-row boundaries
     ([0, 300, 1, 129, 250, 0, 0, 24], 320, 528),
     ([48], 512, 256),
+    ([7, 0, 93, 33], 128, 144),               # M = 133: wgrad reads the padded layout, any M
 ]
 
 
 @pytest.mark.parametrize("sizes,K,N", FP8_CASES)
 def test_fp8_fwd_dgrad_wgrad(sizes, K, N):
     M, E = int(np.sum(sizes)), len(sizes)
-    assert M % 16 == 0
     args = fill(sizes)
     x = rand_bf16((M, K), 21, "normal")
     go = rand_bf16((M, N), 22, "normal")
@@ -191,31 +192,34 @@ def test_fp8_fwd_dgrad_wgrad(sizes, K, N):
     goq, sgo = quant_rows_gpu(go)
     wq, sw = quant_rows_gpu(w_nk.view(E * N, K))
     wdq, swd = quant_rows_gpu(w_kn.view(E * K, N))
-    xqt = torch.empty(K * M, dtype=torch.uint8, device=DEV)
-    goqt = torch.empty(N * M, dtype=torch.uint8, device=DEV)
+    ld = B().mgemm_colwise_ld(M, E)
+    xqt = torch.empty(K * ld, dtype=torch.uint8, device=DEV)
+    goqt = torch.empty(N * ld, dtype=torch.uint8, device=DEV)
     sxc = torch.empty(E * K, dtype=torch.float32, device=DEV)
     sgoc = torch.empty(E * N, dtype=torch.float32, device=DEV)
-    B().mgemm_quant_colwise_grouped(args, E, M, go, goqt, sgoc, x, xqt, sxc)
+    B().mgemm_quant_colwise_grouped(args, E, M, go, goqt, sgoc, x, xqt, sxc, ld=ld)
     torch.cuda.synchronize()
+    xqt_u, goqt_u = unpad_colwise(to_np(xqt), K, ld, sizes), unpad_colwise(to_np(goqt), N, ld, sizes)
+    assert (colwise_padding(to_np(xqt), K, ld, sizes) == 0).all()
     xs, gos = to_np(x), to_np(go)
     q_ref, s_ref = oq.quant_rowwise(xs)
     assert np.array_equal(to_np(xq), q_ref) and np.array_equal(to_np(sx), s_ref)
     offs = np.concatenate([[0], np.cumsum(sizes)])
     (gqt_ref, sgc_ref), (xqt_ref, sxc_ref) = oq.quant_colwise_grouped_dual(gos, xs, offs)
-    assert np.array_equal(to_np(goqt).reshape(N, M), gqt_ref) and np.array_equal(to_np(sgoc), sgc_ref)
-    assert np.array_equal(to_np(xqt).reshape(K, M), xqt_ref) and np.array_equal(to_np(sxc), sxc_ref)
+    assert np.array_equal(goqt_u, gqt_ref) and np.array_equal(to_np(sgoc), sgc_ref)
+    assert np.array_equal(xqt_u, xqt_ref) and np.array_equal(to_np(sxc), sxc_ref)
 
     out = sentinel_bf16((M + 8, N), DEV)
     gx = sentinel_bf16((M + 8, K), DEV)
     gw = sentinel_bf16((E + 1, K, N), DEV)
     B().mgemm_fwd(args, B().MGEMM_FP8_E4M3, 1, xq, sx, wq, sw, out, M, K, N, E)
     B().mgemm_dgrad(args, B().MGEMM_FP8_E4M3, goq, sgo, wdq, swd, gx, M, K, N, E)
-    B().mgemm_wgrad(args, B().MGEMM_FP8_E4M3, xqt, sxc, goqt, sgoc, gw, M, K, N, E)
+    B().mgemm_wgrad(args, B().MGEMM_FP8_E4M3, xqt, sxc, goqt, sgoc, gw, M, K, N, E, ld=ld)
     torch.cuda.synchronize()
     assert is_sentinel(out[M:]) and is_sentinel(gx[M:]) and is_sentinel(gw[E:])
     ref_f = og.gmm_fwd_fp8(to_np(xq), to_np(sx), to_np(wq).reshape(E, N, K), to_np(sw), sizes)
     ref_d = og.gmm_dgrad_fp8(to_np(goq), to_np(sgo), to_np(wdq).reshape(E, K, N), to_np(swd), sizes)
-    ref_w = og.gmm_wgrad_fp8(to_np(xqt).reshape(K, M), to_np(sxc), to_np(goqt).reshape(N, M), to_np(sgoc), sizes)
+    ref_w = og.gmm_wgrad_fp8(xqt_u, to_np(sxc), goqt_u, to_np(sgoc), sizes)
     assert_close(to_np(out[:M]), ref_f, FP8_TOL, "fp8 fwd")
     assert_close(to_np(gx[:M]), ref_d, FP8_TOL, "fp8 dgrad")
     got_w = to_np(gw[:E])

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from oracle.quant import quant_colwise_grouped, quant_rowwise
-from tests.helpers import new_args, to_np
+from tests.helpers import colwise_padding, new_args, padded_offsets, to_np, unpad_colwise
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -87,29 +87,34 @@ def colwise_case(sizes, C1, C2=None, seed=0):
     gs = torch.tensor(sizes, dtype=torch.int64, device=DEV)
     args = new_args(E, DEV)
     B().mgemm_fill_args(gs, E, M, args)
-    o1 = torch.full((C1 * M,), 0xAB, dtype=torch.uint8, device=DEV)
+    ld = B().mgemm_colwise_ld(M, E)
+    o1 = torch.full((C1 * ld,), 0xAB, dtype=torch.uint8, device=DEV)
     s1 = torch.full((E * C1,), -1.0, dtype=torch.float32, device=DEV)
     a2 = o2 = s2 = None
     if C2:
         a2 = (torch.randn(M, C2, generator=g, device=DEV) * 1e-3).to(torch.bfloat16)
-        o2 = torch.full((C2 * M,), 0xAB, dtype=torch.uint8, device=DEV)
+        o2 = torch.full((C2 * ld,), 0xAB, dtype=torch.uint8, device=DEV)
         s2 = torch.full((E * C2,), -1.0, dtype=torch.float32, device=DEV)
-    B().mgemm_quant_colwise_grouped(args, E, M, a1, o1, s1, a2, o2, s2)
+    B().mgemm_quant_colwise_grouped(args, E, M, a1, o1, s1, a2, o2, s2, ld=ld)
     torch.cuda.synchronize()
     offs = np.concatenate([[0], np.cumsum(sizes)])
+    used = padded_offsets(sizes)[-1]
     q1, r1 = quant_colwise_grouped(to_np(a1), offs)
     assert np.array_equal(to_np(s1), r1)
-    assert np.array_equal(to_np(o1).reshape(C1, M), q1)
+    assert np.array_equal(unpad_colwise(to_np(o1), C1, ld, sizes), q1)
+    assert (colwise_padding(to_np(o1), C1, ld, sizes) == 0).all(), "padding must hold zero codes"
+    assert (to_np(o1).reshape(C1, ld)[:, used:] == 0xAB).all(), "bytes past the last group are not written"
     if C2:
         q2, r2 = quant_colwise_grouped(to_np(a2), offs)
         assert np.array_equal(to_np(s2), r2)
-        assert np.array_equal(to_np(o2).reshape(C2, M), q2)
+        assert np.array_equal(unpad_colwise(to_np(o2), C2, ld, sizes), q2)
+        assert (colwise_padding(to_np(o2), C2, ld, sizes) == 0).all()
 
 
 @pytest.mark.parametrize("sizes,C1,C2", [
     ([64], 64, None),
     ([10, 0, 30, 24], 128, None),          # M = 64, empty group
-    ([7, 0, 93], 72, None),                # M = 100: not a multiple of 16 (byte stores)
+    ([7, 0, 93], 72, None),                # M = 100: not a multiple of 16
     ([1, 200, 0, 55, 0, 0, 4], 200, 136),  # dual, different widths
     ([300, 301, 3, 0, 420], 64, 64),       # dual, same widths, groups across 128-row chunks
     ([0, 0, 0, 16], 8, 8),
@@ -126,13 +131,20 @@ def test_colwise_large_groups_deepseek_like():
     colwise_case(sizes.tolist(), 256, 96, seed=11)
 
 
+def test_colwise_group_over_many_segments():
+    # one group of 20000 rows (79 boxes of 256 rows) over 24 column blocks of
+    # two tensors, next to tiny and empty groups
+    colwise_case([20000, 3, 0, 4997], 1024, 512, seed=5)
+
+
 def test_colwise_status_blocks_writes():
     E, M, C = 3, 48, 64
     gs = torch.tensor([16, -1, 33], dtype=torch.int64, device=DEV)
     args = new_args(E, DEV)
     B().mgemm_fill_args(gs, E, M, args)
     a = torch.randn(M, C, device=DEV).to(torch.bfloat16)
-    o = torch.full((C * M,), 0xAB, dtype=torch.uint8, device=DEV)
+    ld = B().mgemm_colwise_ld(M, E)
+    o = torch.full((C * ld,), 0xAB, dtype=torch.uint8, device=DEV)
     s = torch.full((E * C,), -1.0, device=DEV)
     B().mgemm_quant_colwise_grouped(args, E, M, a, o, s)
     torch.cuda.synchronize()
@@ -150,10 +162,11 @@ def test_colwise_repeated_on_one_args_block():
     offs = np.concatenate([[0], np.cumsum(sizes)])
     for rep in range(3):
         a = (torch.randn(M, 136, generator=torch.Generator(device=DEV).manual_seed(rep), device=DEV)).to(torch.bfloat16)
-        o = torch.full((136 * M,), 0xAB, dtype=torch.uint8, device=DEV)
+        ld = B().mgemm_colwise_ld(M, E)
+        o = torch.full((136 * ld,), 0xAB, dtype=torch.uint8, device=DEV)
         s = torch.full((E * 136,), -1.0, dtype=torch.float32, device=DEV)
         B().mgemm_quant_colwise_grouped(args, E, M, a, o, s)
         torch.cuda.synchronize()
         q, r = quant_colwise_grouped(to_np(a), offs)
-        assert np.array_equal(to_np(o).reshape(136, M), q) and np.array_equal(to_np(s), r)
+        assert np.array_equal(unpad_colwise(to_np(o), 136, ld, sizes), q) and np.array_equal(to_np(s), r)
         assert int(args[12:16].view(torch.int32).item()) == 0
