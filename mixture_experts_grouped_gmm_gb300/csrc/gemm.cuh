@@ -14,8 +14,8 @@
 // BN (64, 128 or 256) is chosen per launch on the host to balance the tile
 // count against the number of SMs.
 //
-// CTA layout (192 threads, one CTA per SM, grid = number of SMs, tiles
-// strided by gridDim.x):
+// CTA layout (64 + 32 x EPI threads, one CTA per SM, grid = number of SMs,
+// tiles strided by the grid; with CTA pairs, tiles strided by the clusters):
 //   warp 0      TMA producer: one thread fills a ring (4, 6 or 8 stages) of
 //               (A 128 rows x 128 B, B BN rows x 128 B) shared-memory tiles,
 //               128-byte swizzled, each stage guarded by a full/empty mbarrier.
@@ -27,16 +27,25 @@
 //               issues only the k-steps that hold group rows and first zeroes
 //               the few out-of-group positions inside the partial step (FP8
 //               wgrad reads the padded layout, whose blocks are whole).
-//   warps 2-5   epilogue, one TMEM lane quarter (32 output rows) each:
-//               tcgen05.ld, optional FP8 scale division, bf16 rounding, then
-//               128-byte-swizzled shared-memory staging buffers (2 per warp,
-//               4 for wgrad, whose short main loops leave the stores as the
-//               critical path) and a TMA store of each 32-row x 64-column block.  A
-//               warp whose 32 rows are not all valid (group edge) stores
-//               those rows directly instead, so nothing outside the tile's
-//               rows is ever written.  The accumulator is released right
-//               after its last tcgen05.ld, so the next tile's main loop
+//   warps 2..   epilogue, EPI = 4 warps (one per TMEM lane quarter, 32 output
+//               rows each) or 8 (two per quarter, each taking every other
+//               64-column chunk): tcgen05.ld, optional FP8 scale division
+//               (packed fp32x2 multiplies by power-of-two reciprocals fetched
+//               one tile ahead), bf16 rounding, then 128-byte-swizzled
+//               shared-memory staging buffers and a TMA store of each 32-row x
+//               64-column block.  A warp whose 32 rows are not all valid (group
+//               edge) stores those rows directly instead, so nothing outside
+//               the tile's rows is ever written.  The accumulator is released
+//               right after its last tcgen05.ld, so the next tile's main loop
 //               overlaps the stores.
+// CTA pairs (FP8 wgrad): a cluster of two CTAs computes one 256-row tile with
+// cta_group::2 MMAs issued by the even CTA.  Each CTA copies its 128 rows of A
+// and half of B's columns; the odd CTA's copies complete on the even CTA's
+// full barrier (which expects both CTAs' bytes), MMA commits free the stage
+// and publish the accumulator in both CTAs (multicast), and both CTAs'
+// epilogue warps hand the accumulator back on the even CTA's barrier.  Per SM
+// that is 32 KB of operands per contraction block instead of 48 KB, and six
+// ring stages instead of four.
 // Every mbarrier wait is bounded (about 1 s); on expiry the kernel records
 // MGEMM_STATUS_TIMEOUT in the args block, lets the other roles leave their
 // loops, drains its own outstanding copies and MMAs, frees TMEM and returns.
@@ -52,7 +61,13 @@ enum { kModeRows = 0, kModeExperts = 1 };
 // ring depth.  Wide (256, 4 stages), mid (128, 6) and narrow (64, 8) forms
 // fill the same shared memory; the narrower forms serve weight-streaming
 // launches, where a deeper ring keeps more HBM reads in flight per SM.
-template <bool kFp8, bool kAMn, bool kBMn, int kMode, int kBnMax = 256, int kStages = 4, int kOutBufs = 2>
+// kPair: a cluster of two CTAs computes one 256-row tile with cta_group::2
+// MMAs (each CTA loads its 128 rows of A and half of B's columns), so every SM
+// reads half of the B tile it would otherwise read.
+// kEpiWarps: epilogue warps, 4 (one per TMEM lane quarter) or 8 (two per
+// quarter, splitting the tile's 64-column chunks between them).
+template <bool kFp8, bool kAMn, bool kBMn, int kMode, int kBnMax = 256, int kStages = 4, int kOutBufs = 2,
+          bool kPair = false, int kEpiWarps = 4>
 struct GemmCfg {
   static constexpr bool Fp8 = kFp8;
   static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
@@ -63,17 +78,20 @@ struct GemmCfg {
   static constexpr int BK = 128 / ESIZE;  // contraction elements per stage (one 128-byte row)
   static constexpr int UK = 32 / ESIZE;   // contraction elements per MMA
   static constexpr int KSTEPS = BK / UK;  // 4
+  static constexpr bool Pair = kPair;
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN_MAX * 128;
+  static constexpr int B_BYTES = (kPair ? BN_MAX / 2 : BN_MAX) * 128;
   static constexpr int STAGES = kStages;
   static constexpr int CHUNK = 64 * 128;  // MN-major: one 64-element x BK-row block (8 KB)
   static constexpr int TMEM_COLS = 2 * BN_MAX;  // a power of two >= 32
-  static constexpr int THREADS = 192;
+  static constexpr int EPI = kEpiWarps;
+  static_assert(EPI == 4 || EPI == 8, "one or two epilogue warps per TMEM lane quarter");
+  static constexpr int HN = EPI / 4;         // epilogue warps per lane quarter
+  static constexpr int THREADS = 64 + 32 * EPI;
   static constexpr int OUT_BUF = 32 * 128;  // 32 rows x 64 bf16 columns
   static constexpr int NBUF = kOutBufs;      // staging buffers per epilogue warp
   static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * (A_BYTES + B_BYTES) +
-                                       4 * NBUF * OUT_BUF /*epilogue staging*/ + 4 * 64 * 4 /*column scales*/ +
-                                       256 /*barriers, flags*/;
+                                       (size_t)EPI * NBUF * OUT_BUF /*epilogue staging*/ + 256 /*barriers, flags*/;
 };
 
 struct GemmParams {
@@ -93,7 +111,7 @@ struct GemmParams {
 };
 
 struct TileInfo {
-  int e, kb_count, a_row, n0, x0, lo, hi, out_row0, out_rows;
+  int e, kb_count, a_row, b_row, n0, x0, lo, hi, out_row0, out_rows;
 };
 
 template <class C>
@@ -106,7 +124,7 @@ __device__ __forceinline__ int total_tiles(const GemmParams &p, const ArgsView &
 }
 
 template <class C>
-__device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, const ArgsView &av) {
+__device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, const ArgsView &av, uint32_t rank) {
   TileInfo ti;
   if (C::Mode == kModeRows) {
     // Group a owns tiles [mtile_start[a] * n_tiles, mtile_start[a+1] * n_tiles).
@@ -130,6 +148,7 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
     ti.a_row = row0;
     ti.out_row0 = row0;
     ti.out_rows = (int)min((int64_t)C::BM, re - row0);
+    ti.b_row = ti.n0;
     ti.x0 = 0; ti.lo = 0; ti.hi = 0;
   } else {
     ti.n0 = (t % p.n_tiles) * p.bn;
@@ -154,9 +173,12 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
       ti.hi = (int)(re - rs);
       ti.kb_count = re > rs ? (ti.hi + C::BK - 1) / C::BK : 0;
     }
-    ti.a_row = mk * C::BM;
-    ti.out_row0 = ti.e * p.Kout + mk * C::BM;
-    ti.out_rows = min(C::BM, p.Kout - mk * C::BM);
+    // a CTA pair's tile is 256 rows of K: rank r takes rows 128 r .. 128 r + 127
+    // and columns n0 + r bn / 2 .. of B
+    ti.a_row = C::Pair ? mk * 2 * C::BM + (int)rank * C::BM : mk * C::BM;
+    ti.b_row = C::Pair ? ti.n0 + (int)rank * (p.bn / 2) : ti.n0;
+    ti.out_row0 = ti.e * p.Kout + ti.a_row;
+    ti.out_rows = max(0, min(C::BM, p.Kout - ti.a_row));
   }
   return ti;
 }
@@ -184,6 +206,22 @@ __device__ __forceinline__ void mask_positions(uint8_t *sa, uint8_t *sb, int bn,
 // 1 / s for a power of two s in [2^-126, 2^126] (exact: the exponent is negated)
 __device__ __forceinline__ float pow2_recip(float s) { return __uint_as_float(0x7F000000u - __float_as_uint(s)); }
 
+// (a0, a1) * (b0, b1) elementwise, round to nearest (one packed fp32 multiply)
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  return f32x2(__float_as_uint(lo), __float_as_uint(hi));
+}
+// two packed fp32 values -> bf16x2 (round to nearest even), low element in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2_u64(uint64_t v) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -197,9 +235,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + C::STAGES * C::A_BYTES;
-  uint8_t *sOut = sB + C::STAGES * C::B_BYTES;  // [4 warps][NBUF buffers][32 x 128 B]
-  float *s_csc = reinterpret_cast<float *>(sOut + 4 * C::NBUF * C::OUT_BUF);  // [4 warps][64]
-  uint64_t *full = reinterpret_cast<uint64_t *>(s_csc + 4 * 64);
+  uint8_t *sOut = sB + C::STAGES * C::B_BYTES;  // [EPI warps][NBUF buffers][32 x 128 B]
+  uint64_t *full = reinterpret_cast<uint64_t *>(sOut + C::EPI * C::NBUF * C::OUT_BUF);
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
@@ -211,7 +248,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const ArgsView av(p.args, p.E);
   if (*av.status != 0) return;
   const int total = total_tiles<C>(p, av);
-  if ((int)blockIdx.x >= total) return;
+  // CTA pairs walk the tiles per cluster: both CTAs of a pair see the same
+  // sequence and leave (or stay) together
+  const uint32_t rank = C::Pair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int t_first = C::Pair ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int t_step = C::Pair ? (int)ncluster_x() : (int)gridDim.x;
+  if (t_first >= total) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -220,7 +263,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      // one arrival per thread of the four epilogue warps, or per warp with
+      // eight of them (pair: per warp of each CTA, on the leader's barrier)
+      mbar_init(&tempty[a], C::Pair ? 2 * C::EPI : (C::EPI == 4 ? 128 : C::EPI));
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -230,15 +275,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (C::Pair) {
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (C::Pair)
+    cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   volatile int *vabort = abort_flag;
   const int bn = p.bn;
+  // an abort in one CTA of a pair is raised in the other as well
+  auto raise_abort = [&]() {
+    *vabort = 1;
+    if constexpr (C::Pair) st_cluster_u32(cluster_addr(abort_flag, rank ^ 1u), 1u);
+  };
 
   // Producer bookkeeping kept for the drain after an abort.
   uint32_t issued = 0;
@@ -250,17 +308,39 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // with fewer than 128 token rows the A box is cut to them (rounded up to 8);
       // the MMA's remaining A rows hold stale data and only feed output rows
       // that are never stored
-      const uint32_t tx = (C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128;
-      for (int t = blockIdx.x; t < total && !*vabort; t += gridDim.x) {
-        const TileInfo ti = decode_tile<C>(t, p, av);
+      // pair: the leader's full barrier counts the bytes of both CTAs
+      const uint32_t tx = C::Pair ? 2u * (uint32_t)(C::A_BYTES + (bn / 2) * 128)
+                                  : (C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128;
+      for (int t = t_first; t < total && !*vabort; t += t_step) {
+        const TileInfo ti = decode_tile<C>(t, p, av, rank);
         for (int kb = 0; kb < ti.kb_count; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, vabort)) {
             set_status(av.status, MGEMM_STATUS_TIMEOUT);
-            *vabort = 1;
+            raise_abort();
             break;
           }
           uint8_t *a = sA + stage * C::A_BYTES;
           uint8_t *b = sB + stage * C::B_BYTES;
+          if constexpr (C::Pair) {
+            static_assert(C::Pair ? (C::Mode == kModeExperts && C::Fp8) : true, "CTA pairs serve FP8 wgrad");
+            // each CTA copies its own halves; the peer's copies complete on the leader's barrier
+            const int xr = ti.x0 + kb * C::BK;
+            if (leader) {
+              mbar_arrive_expect_tx(&full[stage], tx);
+              ++issued;
+              tma_load_2d(a, &tmA, &full[stage], xr, ti.a_row);
+              tma_load_2d(b, &tmB, &full[stage], xr, ti.b_row);
+            } else {
+              const uint32_t lbar = cluster_addr(&full[stage], 0);
+              tma_load_2d_pair(a, &tmA, lbar, xr, ti.a_row);
+              tma_load_2d_pair(b, &tmB, lbar, xr, ti.b_row);
+            }
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(&full[stage], tx);
           ++issued;
           if (C::Mode == kModeRows) {
@@ -295,8 +375,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C>(t, p, av);
+    // pair: only the leader issues MMAs (for both CTAs); the peer's warp 1 only owns its TMEM
+    const int t_mma = (!C::Pair || leader) ? t_first : total;
+    for (int t = t_mma; t < total && ok; t += t_step) {
+      const TileInfo ti = decode_tile<C>(t, p, av, rank);
       if (ti.kb_count == 0) continue;
       if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1, vabort)) { ok = false; break; }
       tc_fence_after();
@@ -336,7 +418,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               const uint64_t bd = C::BMn ? smem_desc_sw128(bbase + k * C::UK * 128, C::CHUNK, 1024)
                                          : smem_desc_sw128(bbase + k * 32, 16, 1024);
               // the tile's first MMA overwrites the accumulator
-              if (C::Fp8)
+              if constexpr (C::Pair)
+                mma_f8_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+              else if (C::Fp8)
                 mma_f8(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
               else
                 mma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
@@ -354,7 +438,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 mma_f16(d_tmem, ad, bd, p.idesc, acc_on);
             }
           }
-          mma_commit(&empty[stage]);
+          if constexpr (C::Pair)
+            mma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
+          else
+            mma_commit(&empty[stage]);
         }
         __syncwarp();
         if (++stage == C::STAGES) {
@@ -363,7 +450,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(&tfull[acc]);
+      if (lane == 0) {
+        if constexpr (C::Pair)
+          mma_commit_pair(&tfull[acc], 0x3);  // both CTAs' accumulators are ready
+        else
+          mma_commit(&tfull[acc]);
+      }
       __syncwarp();
       if (++acc == 2) {
         acc = 0;
@@ -372,93 +464,147 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     if (!ok) {
       if (lane == 0) set_status(av.status, MGEMM_STATUS_TIMEOUT);
-      *vabort = 1;
+      raise_abort();
     }
     // all MMAs this thread issued have completed before TMEM is released
-    if (lane == 0) {
-      mma_commit(drain);
+    if (lane == 0 && (!C::Pair || leader)) {
+      if constexpr (C::Pair)
+        mma_commit_pair(drain, 0x1);
+      else
+        mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
     __syncwarp();
   } else {
-    // epilogue warps 2..5 -> TMEM lane quarter q = warp % 4 -> tile rows 32q..32q+31
+    // epilogue warps 2 .. EPI + 1: warp w reads TMEM lane quarter q = w % 4 (tile
+    // rows 32q .. 32q + 31) and, with two warps per quarter, every other
+    // 64-column chunk of the tile (h = its place among the quarter's warps)
+    const int ew = warp - 2;
     const int q = warp & 3;
+    const int h = ew / 4;
     const int r = q * 32 + lane;
-    uint8_t *my_buf = sOut + (size_t)q * C::NBUF * C::OUT_BUF;
+    constexpr int kCpw = (C::BN_MAX / 64 + C::HN - 1) / C::HN;  // chunks per warp, at most
+    uint8_t *my_buf = sOut + (size_t)ew * C::NBUF * C::OUT_BUF;
     uint32_t nstored = 0;  // TMA-stored chunks so far; buffers rotate with it
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C>(t, p, av);
+    // FP8: the row-scale reciprocal of this thread's row and the column-scale
+    // reciprocals of the warp's chunks of one tile (lane l: columns col0 + l
+    // and col0 + 32 + l of each chunk), loaded one tile ahead so their latency
+    // never sits between an accumulator and its stores (scales are powers of
+    // two: the reciprocals are exact)
+    float rinv_next = 1.f, csr_next[2 * kCpw] = {};
+    auto load_scales = [&](int tn) {
+      if (!C::Fp8 || tn >= total) return;
+      const TileInfo tj = decode_tile<C>(tn, p, av, rank);
+      const bool live = tj.kb_count > 0;
+      rinv_next = live && r < tj.out_rows ? pow2_recip(__ldg(p.rscale + tj.out_row0 + r)) : 1.f;
+#pragma unroll
+      for (int i = 0; i < 2 * kCpw; ++i) {
+        const int c = h + C::HN * (i >> 1);
+        const int col = tj.n0 + c * 64 + 32 * (i & 1) + lane;
+        csr_next[i] = live && c * 64 < bn && col < p.Nout ? pow2_recip(__ldg(p.cscale + (int64_t)tj.e * p.Nout + col))
+                                                           : 0.f;
+      }
+    };
+    // hand the accumulator back to the MMA warp (one arrival per warp)
+    auto release = [&](int a) {
+      tc_fence_before();
+      if constexpr (!C::Pair && C::EPI == 4) {
+        mbar_arrive(&tempty[a]);  // every thread arrives
+      } else {
+        __syncwarp();
+        if (lane == 0) {
+          if (!C::Pair || leader)
+            mbar_arrive(&tempty[a]);
+          else
+            mbar_arrive_cluster(cluster_addr(&tempty[a], 0));
+        }
+      }
+    };
+    load_scales(t_first);
+    for (int t = t_first; t < total; t += t_step) {
+      const TileInfo ti = decode_tile<C>(t, p, av, rank);
       const bool has_acc = ti.kb_count > 0;
       const bool row_ok = r < ti.out_rows;
       const bool warp_full = q * 32 + 32 <= ti.out_rows;
       __nv_bfloat16 *orow = p.out + (int64_t)(ti.out_row0 + r) * p.Nout;
-      float rinv = 1.f;
-      if (C::Fp8 && row_ok && has_acc) rinv = pow2_recip(__ldg(p.rscale + ti.out_row0 + r));
-      // FP8: this tile's column-scale reciprocals, fetched before the accumulator
-      // wait so no global load sits between a TMEM read and its stores; lane l
-      // holds columns n0 + 32 i + l (scales are powers of two: exact reciprocals)
-      float csr[C::BN_MAX / 32];
-      if (C::Fp8) {
+      float rinv = 1.f, csr[2 * kCpw];
+      if constexpr (C::Fp8) {
+        rinv = rinv_next;
 #pragma unroll
-        for (int i = 0; i < C::BN_MAX / 32; ++i) {
-          const int col = ti.n0 + 32 * i + lane;
-          csr[i] = has_acc && 32 * i < bn && col < p.Nout ? pow2_recip(__ldg(p.cscale + (int64_t)ti.e * p.Nout + col))
-                                                          : 0.f;
-        }
+        for (int i = 0; i < 2 * kCpw; ++i) csr[i] = csr_next[i];
+        load_scales(t + t_step);
       }
       if (has_acc) {
         if (!mbar_wait_warp(&tfull[acc], acc_phase, vabort)) {
           set_status(av.status, MGEMM_STATUS_TIMEOUT);
-          *vabort = 1;
+          raise_abort();
           break;
         }
         tc_fence_after();
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::BN_MAX;
       const int nchunks = bn / 64;
-      // TMEM -> registers runs one chunk ahead: chunk c + 1 is loading while
-      // chunk c is converted and stored (the loop is unrolled so both register
-      // sets keep fixed names)
-      uint32_t va[2][32], vb[2][32];
-      if (has_acc) {
-        tmem_ld_32x32b_x32(taddr, va[0]);
-        tmem_ld_32x32b_x32(taddr + 32, vb[0]);
+      bool released = false;
+      // with one warp per quarter, TMEM -> registers runs one chunk ahead (chunk
+      // c + 1 loads while chunk c is converted and stored; the loop is unrolled
+      // so both register sets keep fixed names); with two, the other warp of the
+      // quarter hides the load latency and registers stay within the budget
+      constexpr int kNb = C::HN == 1 ? 2 : 1;
+      uint32_t va[kNb][32], vb[kNb][32];
+      if (kNb == 2 && has_acc && h < nchunks) {
+        tmem_ld_32x32b_x32(taddr + h * 64, va[0]);
+        tmem_ld_32x32b_x32(taddr + h * 64 + 32, vb[0]);
       }
 #pragma unroll
-      for (int c = 0; c < C::BN_MAX / 64; ++c) {
+      for (int ci = 0; ci < kCpw; ++ci) {
+        const int c = h + C::HN * ci;
         if (c >= nchunks) break;
-        const int cur = c & 1;
+        const int cur = kNb == 2 ? (ci & 1) : 0;
         const int col0 = ti.n0 + c * 64;
+        // the staging buffer of this chunk; the store group that last read it is
+        // NBUF groups back (FP8 parks the chunk's column scales in it first, so
+        // it waits for the buffer before the math; bf16 only before its stores)
+        uint8_t *buf = my_buf + (nstored % C::NBUF) * C::OUT_BUF;
+        if constexpr (C::Fp8) {
+          if (lane == 0) bulk_wait_read<C::NBUF - 1>();
+          __syncwarp();
+        }
         uint32_t pk[32];
         if (has_acc) {
+          if (kNb == 1) {
+            tmem_ld_32x32b_x32(taddr + c * 64, va[0]);
+            tmem_ld_32x32b_x32(taddr + c * 64 + 32, vb[0]);
+          }
           tmem_ld_wait();
-          if (c + 1 < nchunks) {
-            tmem_ld_32x32b_x32(taddr + (c + 1) * 64, va[cur ^ 1]);
-            tmem_ld_32x32b_x32(taddr + (c + 1) * 64 + 32, vb[cur ^ 1]);
-          } else {  // accumulator fully read: hand it back to the MMA warp
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+          if (c + C::HN >= nchunks) {  // the warp's last chunk: the accumulator is read
+            release(acc);
+            released = true;
+          } else if (kNb == 2) {
+            tmem_ld_32x32b_x32(taddr + (c + C::HN) * 64, va[cur ^ (kNb - 1)]);
+            tmem_ld_32x32b_x32(taddr + (c + C::HN) * 64 + 32, vb[cur ^ (kNb - 1)]);
           }
           if (C::Fp8) {
-            // this chunk's column-scale reciprocals, staged per warp and read as broadcasts
-            float *cs = s_csc + q * 64;
-            cs[lane] = csr[2 * c];
-            cs[lane + 32] = csr[2 * c + 1];
+            // the chunk's column-scale reciprocals, staged in the (free) staging
+            // buffer and read as broadcasts before the codes overwrite them
+            float *cs = reinterpret_cast<float *>(buf);
+            cs[lane] = csr[2 * ci];
+            cs[lane + 32] = csr[2 * ci + 1];
             __syncwarp();
+            // two packed multiplies per pair of elements: by the row's, then the columns' reciprocals
+            const uint64_t r2 = f32x2(rinv, rinv);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float4 c0 = *reinterpret_cast<const float4 *>(cs + 4 * j);
               const float4 c1 = *reinterpret_cast<const float4 *>(cs + 32 + 4 * j);
-              pk[2 * j] = pack_bf16x2(__uint_as_float(va[cur][4 * j]) * rinv * c0.x,
-                                      __uint_as_float(va[cur][4 * j + 1]) * rinv * c0.y);
-              pk[2 * j + 1] = pack_bf16x2(__uint_as_float(va[cur][4 * j + 2]) * rinv * c0.z,
-                                          __uint_as_float(va[cur][4 * j + 3]) * rinv * c0.w);
-              pk[16 + 2 * j] = pack_bf16x2(__uint_as_float(vb[cur][4 * j]) * rinv * c1.x,
-                                           __uint_as_float(vb[cur][4 * j + 1]) * rinv * c1.y);
-              pk[16 + 2 * j + 1] = pack_bf16x2(__uint_as_float(vb[cur][4 * j + 2]) * rinv * c1.z,
-                                               __uint_as_float(vb[cur][4 * j + 3]) * rinv * c1.w);
+              pk[2 * j] = pack_bf16x2_u64(mul_f32x2(mul_f32x2(f32x2(va[cur][4 * j], va[cur][4 * j + 1]), r2), f32x2(c0.x, c0.y)));
+              pk[2 * j + 1] =
+                  pack_bf16x2_u64(mul_f32x2(mul_f32x2(f32x2(va[cur][4 * j + 2], va[cur][4 * j + 3]), r2), f32x2(c0.z, c0.w)));
+              pk[16 + 2 * j] =
+                  pack_bf16x2_u64(mul_f32x2(mul_f32x2(f32x2(vb[cur][4 * j], vb[cur][4 * j + 1]), r2), f32x2(c1.x, c1.y)));
+              pk[16 + 2 * j + 1] =
+                  pack_bf16x2_u64(mul_f32x2(mul_f32x2(f32x2(vb[cur][4 * j + 2], vb[cur][4 * j + 3]), r2), f32x2(c1.z, c1.w)));
             }
             __syncwarp();
           } else {
@@ -474,11 +620,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (col0 >= p.Nout) continue;
         if (warp_full) {
-          // one store group per chunk, committed in rotation order: the group
-          // that last read this buffer is NBUF groups back
-          uint8_t *buf = my_buf + (nstored % C::NBUF) * C::OUT_BUF;
-          if (lane == 0) bulk_wait_read<C::NBUF - 1>();
-          __syncwarp();
+          if constexpr (!C::Fp8) {
+            if (lane == 0) bulk_wait_read<C::NBUF - 1>();
+            __syncwarp();
+          }
           uint8_t *rowp = buf + lane * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
@@ -498,9 +643,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (col0 + 8 * j < p.Nout) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
-      if (has_acc && ++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
+      if (has_acc) {
+        if (!released) release(acc);  // a warp with no chunk of this tile (narrow tiles)
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -511,17 +659,30 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (*vabort && warp == 0 && lane == 0) {
-    // wait for the TMA copies this CTA issued, bounded
+    // wait for the TMA copies this CTA armed, bounded
     for (int s = 0; s < C::STAGES; ++s) {
       const uint32_t armed = issued / C::STAGES + ((uint32_t)s < issued % C::STAGES ? 1u : 0u);
       if (armed) mbar_wait(&full[s], (armed - 1) & 1, nullptr);
     }
+    // pair: copies a peer issued for stages its leader never armed are not
+    // counted anywhere; give them far longer than a copy takes to land
+    if constexpr (C::Pair) {
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 100000ull) __nanosleep(1000);
+    }
   }
-  __syncthreads();
+  if constexpr (C::Pair)
+    cluster_sync();  // every MMA into either CTA's TMEM and every remote arrival is done
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (C::Pair)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  if constexpr (C::Pair) cluster_sync();  // neither CTA leaves while the other may still address it
 }
 
 }  // namespace mgemm

@@ -38,8 +38,8 @@ int grid_for(int64_t tiles_upper) {
 // overhead), where waves = ceil(estimated tiles / SMs); ties go to the wider
 // tile (better operand reuse in shared memory).  m_tiles_est is the host's
 // estimate of 128-row tiles (the exact count lives on the device).
-int choose_bn(int64_t m_tiles_est, int64_t n_cols) {
-  const int sms = sm_count() > 0 ? sm_count() : 148;
+int choose_bn_units(int64_t m_tiles_est, int64_t n_cols, int units) {
+  const int sms = units > 0 ? units : 1;
   int best = 256;
   int64_t best_cost = -1;
   for (int bn : {256, 128, 64}) {
@@ -52,6 +52,10 @@ int choose_bn(int64_t m_tiles_est, int64_t n_cols) {
     }
   }
   return best;
+}
+
+int choose_bn(int64_t m_tiles_est, int64_t n_cols) {
+  return choose_bn_units(m_tiles_est, n_cols, sm_count() > 0 ? sm_count() : 148);
 }
 
 // Rows-mode estimate of 128-row tiles: dense groups give about M/128, sparse
@@ -206,14 +210,18 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
   const uint64_t Mm = M > 0 ? (uint64_t)M : 16;
   const uint64_t Lm = fp8 && ld > 0 ? (uint64_t)ld : 16;
   if ((rc = ensure_context())) return rc;
-  const int mt_k = (K + 127) / 128;
-  const int bn = choose_bn((int64_t)E * mt_k, N);
+  // FP8 runs on CTA pairs: one tile is 256 rows of K (each CTA 128) by bn columns
+  const int mt_k = fp8 ? (K + 255) / 256 : (K + 127) / 128;
+  const int sms = sm_count();
+  if (sms <= 1) return MGEMM_ECUDA;
+  const int bn = fp8 ? choose_bn_units((int64_t)E * mt_k, N, sms / 2) : choose_bn((int64_t)E * mt_k, N);
   CUtensorMap ta, tb;
   if (fp8) {
-    // padded column-major operands: x^T [K, ld] and grad_out^T [N, ld], contraction contiguous
+    // padded column-major operands: x^T [K, ld] and grad_out^T [N, ld], contraction
+    // contiguous; each CTA of a pair loads 128 rows of x^T and bn / 2 rows of grad_out^T
     const uint64_t da[2] = {Lm, (uint64_t)K}, db[2] = {Lm, (uint64_t)N};
     const uint64_t st[1] = {Lm};
-    const uint32_t boxa[2] = {128, 128}, boxb[2] = {128, (uint32_t)bn};
+    const uint32_t boxa[2] = {128, 128}, boxb[2] = {128, (uint32_t)bn / 2};
     if (!make_map(&ta, true, 2, xa, da, st, boxa)) return MGEMM_ECUDA;
     if (!make_map(&tb, true, 2, ga, db, st, boxb)) return MGEMM_ECUDA;
   } else {
@@ -230,7 +238,7 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
   p.args = (const uint8_t *)args;
   p.E = E;
   p.bn = bn;
-  p.idesc = make_idesc(fp8 ? 0u : 1u, !fp8, !fp8, 128, bn);
+  p.idesc = make_idesc(fp8 ? 0u : 1u, !fp8, !fp8, fp8 ? 256 : 128, bn);
   p.n_tiles = (N + bn - 1) / bn;
   p.mt_k = mt_k;
   p.Nout = N;
@@ -240,8 +248,12 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
   p.cscale = sgo;
   const int64_t upper = (int64_t)E * p.mt_k * p.n_tiles;
   if (upper >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (fp8) {
+    const int pairs = (int)(upper < sms / 2 ? upper : sms / 2);
+    return gemm_fp8_experts_pair(ta, tb, to, p, 2 * pairs, s);
+  }
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
-  cudaStream_t s = (cudaStream_t)stream;
-  return fp8 ? gemm_fp8_experts(ta, tb, to, p, grid, s) : gemm_bf16_experts(ta, tb, to, p, grid, s);
+  return gemm_bf16_experts(ta, tb, to, p, grid, s);
 }

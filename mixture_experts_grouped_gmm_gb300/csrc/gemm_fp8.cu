@@ -10,11 +10,15 @@ int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap 
 }
 int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s) {
-  return launch_gemm<GemmCfg<true, false, false, kModeExperts>>(a, b, o, p, grid, s);
+  return launch_gemm<GemmCfg<true, false, false, kModeExperts, 256, 4, 1, false, 8>>(a, b, o, p, grid, s);
+}
+int gemm_fp8_experts_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                          int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeExperts, 256, 6, 1, true, 8>>(a, b, o, p, grid, s);
 }
 int gemm_fp8_rows_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                          int grid, cudaStream_t s) {
-  return launch_gemm<GemmCfg<true, false, false, kModeRows, 64, 8>>(a, b, o, p, grid, s);
+  return launch_gemm<GemmCfg<true, false, false, kModeRows, 64, 8, 1, false, 8>>(a, b, o, p, grid, s);
 }
 int gemm_fp8_rows_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                       int grid, cudaStream_t s) {

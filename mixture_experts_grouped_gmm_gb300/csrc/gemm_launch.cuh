@@ -21,8 +21,25 @@ int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o
     if (rc) return rc;
     attr_done[dev] = true;
   }
-  mgemm_gemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, b, o, p);
-  return cuda_rc(cudaGetLastError(), "grouped GEMM launch");
+  if constexpr (C::Pair) {
+    // clusters of two CTAs (grid is even); every CTA of the grid is resident
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_rc(cudaLaunchKernelEx(&cfg, mgemm_gemm_kernel<C>, a, b, o, p), "grouped GEMM launch (CTA pairs)");
+  } else {
+    mgemm_gemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, b, o, p);
+    return cuda_rc(cudaGetLastError(), "grouped GEMM launch");
+  }
 }
 
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)
@@ -53,5 +70,8 @@ int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap 
 // fp8 wgrad: column-major quantized operands (K-major), scaled epilogue
 int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s);
+// the same on CTA pairs (256-row tiles of K, cta_group::2; grid even)
+int gemm_fp8_experts_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                          int grid, cudaStream_t s);
 
 }  // namespace mgemm
