@@ -440,11 +440,11 @@ def run_ours(a):
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         try:
-            from mixture_experts_grouped_gmm_gb300.build import source_hash
+            from mixture_experts_grouped_gmm_gb300.build import gemm_source_hash
 
             tj = json.load(open(tpath))
             ent = tj.get(dom)
-            if ent and ent.get("source_hash") == source_hash():
+            if ent and ent.get("gemm_source_hash") == gemm_source_hash():
                 traffic = ent.get("dram_bytes_per_launch")
         except Exception:
             traffic = None

@@ -57,6 +57,25 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
+# the files that make up the grouped GEMM kernels (a change to any of them
+# invalidates counters taken from an earlier build of those kernels)
+GEMM_FILES = ["common.cuh", "gemm.cuh", "gemm_launch.cuh", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_api.cu"]
+
+
+def gemm_source_hash():
+    """sha256 over the grouped GEMM's sources and the header."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in GEMM_FILES:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    with open(os.path.join(INCLUDE, "mgemm.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def up_to_date():
     if not os.path.exists(LIB_PATH):
         return False
