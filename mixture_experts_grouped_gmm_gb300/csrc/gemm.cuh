@@ -98,6 +98,7 @@ struct GemmParams {
   const uint8_t *args;
   int E;
   int bn;           // output tile width: 64, 128 or 256
+  int b_one_box;    // rows mode, MN-major B: the whole BN-column tile is one 4-d box (N % 64 == 0)
   int a_rows;       // rows mode: rows of each A box (128, or fewer when M itself is smaller)
   uint32_t idesc;   // tcgen05 instruction descriptor for M=128, N=bn
   int n_tiles;      // ceil(Nout / bn)
@@ -346,8 +347,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (C::Mode == kModeRows) {
             tma_load_2d(a, &tmA, &full[stage], kb * C::BK, ti.a_row);
             if (C::BMn) {
-              for (int j = 0; j < bn / 64; ++j)
-                tma_load_3d(b + j * C::CHUNK, &tmB, &full[stage], ti.n0 + 64 * j, kb * C::BK, ti.e);
+              if (p.b_one_box) {  // [chunk][row][64 columns] in one copy: the layout the MMA reads
+                tma_load_4d(b, &tmB, &full[stage], 0, kb * C::BK, ti.n0 / 64, ti.e);
+              } else {
+                for (int j = 0; j < bn / 64; ++j)
+                  tma_load_3d(b + j * C::CHUNK, &tmB, &full[stage], ti.n0 + 64 * j, kb * C::BK, ti.e);
+              }
             } else {
               tma_load_3d(b, &tmB, &full[stage], kb * C::BK, ti.n0, ti.e);
             }

@@ -99,16 +99,29 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
     if (!make_map(&ta, fp8, 2, x, d, st, box)) return MGEMM_ECUDA;
   }
   const int bn = choose_bn(rows_tiles_estimate(M, E), N);
+  bool b_one_box = false;
   if (trans_b) {  // w [E, N, K]
     const uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
     const uint64_t st[2] = {(uint64_t)K * es, (uint64_t)N * K * es};
     const uint32_t box[3] = {bk, (uint32_t)bn, 1};
     if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
   } else {  // w [E, K, N], loaded as 64-column MN-major chunks
-    const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
-    const uint64_t st[2] = {(uint64_t)N * es, (uint64_t)K * N * es};
-    const uint32_t box[3] = {64, bk, 1};
-    if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
+    // with N % 64 == 0, w is viewed as [E][N / 64 chunks][K rows][64 columns] (chunk stride 128 B)
+    // so one box brings the tile's bn / 64 chunks at once; every box row stays inside w
+    bool one = N % 64 == 0;
+    if (one) {
+      const uint64_t d[4] = {64, (uint64_t)K, (uint64_t)N / 64, (uint64_t)E};
+      const uint64_t st[3] = {(uint64_t)N * es, 64 * es, (uint64_t)K * N * es};
+      const uint32_t box[4] = {64, bk, (uint32_t)bn / 64, 1};
+      one = make_map(&tb, fp8, 4, w, d, st, box);
+    }
+    if (!one) {
+      const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
+      const uint64_t st[2] = {(uint64_t)N * es, (uint64_t)K * N * es};
+      const uint32_t box[3] = {64, bk, 1};
+      if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
+    }
+    b_one_box = one;
   }
   CUtensorMap to;
   if (!make_out_map(&to, out, M, N)) return MGEMM_ECUDA;
@@ -116,6 +129,7 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   p.args = (const uint8_t *)args;
   p.E = E;
   p.bn = bn;
+  p.b_one_box = b_one_box ? 1 : 0;
   p.idesc = make_idesc(fp8 ? 0u : 1u, false, !trans_b, 128, bn);
   p.a_rows = (int)a_rows;
   p.n_tiles = (N + bn - 1) / bn;
