@@ -66,8 +66,17 @@ enum { kModeRows = 0, kModeExperts = 1 };
 // reads half of the B tile it would otherwise read.
 // kEpiWarps: epilogue warps, 4 (one per TMEM lane quarter) or 8 (two per
 // quarter, splitting the tile's 64-column chunks between them).
+// kDynRing: the ring's stages are [A slot of a_rows x 128 B][B slot of BN x
+// 128 B] and their number is chosen per launch (kStages is then the most
+// there can be): with few token rows (sparse routing) the A slot shrinks to
+// those rows and the weight stream gets the rest of shared memory.
+// kKc: contraction blocks per ring stage (run-time rings only).  With kKc > 1
+// each operand comes in one box of kKc consecutive 128-byte k-chunks (a 3-d /
+// 4-d view of the K-major tensor, chunk stride 128 B), landing as kKc
+// consecutive MMA tiles: fewer, larger copies, which is what latency-bound
+// launches with few rows need.
 template <bool kFp8, bool kAMn, bool kBMn, int kMode, int kBnMax = 256, int kStages = 4, int kOutBufs = 2,
-          bool kPair = false, int kEpiWarps = 4>
+          bool kPair = false, int kEpiWarps = 4, bool kDynRing = false, int kKc = 1>
 struct GemmCfg {
   static constexpr bool Fp8 = kFp8;
   static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
@@ -79,6 +88,10 @@ struct GemmCfg {
   static constexpr int UK = 32 / ESIZE;   // contraction elements per MMA
   static constexpr int KSTEPS = BK / UK;  // 4
   static constexpr bool Pair = kPair;
+  static constexpr bool DynRing = kDynRing;
+  static constexpr int KC = kKc;
+  static_assert(kKc == 1 || (kDynRing && !kAMn && !kBMn), "multi-block stages: run-time rings of K-major operands");
+  static_assert(!kDynRing || (kMode == kModeRows && !kPair), "run-time rings serve the rows schedule");
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = (kPair ? BN_MAX / 2 : BN_MAX) * 128;
   static constexpr int STAGES = kStages;
@@ -90,8 +103,12 @@ struct GemmCfg {
   static constexpr int THREADS = 64 + 32 * EPI;
   static constexpr int OUT_BUF = 32 * 128;  // 32 rows x 64 bf16 columns
   static constexpr int NBUF = kOutBufs;      // staging buffers per epilogue warp
-  static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * (A_BYTES + B_BYTES) +
-                                       (size_t)EPI * NBUF * OUT_BUF /*epilogue staging*/ + 256 /*barriers, flags*/;
+  static constexpr size_t TAIL_BYTES = 16 * STAGES + 256;  // barriers, flags
+  static constexpr size_t FIXED_BYTES = 1024 /*align slack*/ + (size_t)EPI * NBUF * OUT_BUF /*epilogue staging*/ +
+                                        TAIL_BYTES;
+  // a run-time ring takes what the launch needs, up to the per-CTA limit
+  static constexpr size_t SMEM_BYTES =
+      kDynRing ? (size_t)227 * 1024 : FIXED_BYTES + (size_t)STAGES * (A_BYTES + B_BYTES);
 };
 
 struct GemmParams {
@@ -99,6 +116,8 @@ struct GemmParams {
   int E;
   int bn;           // output tile width: 64, 128 or 256
   int b_one_box;    // rows mode, MN-major B: the whole BN-column tile is one 4-d box (N % 64 == 0)
+  int stages;       // run-time ring: stages, and bytes per stage ((a_rows + bn) x 128)
+  int stage_bytes;
   int a_rows;       // rows mode: rows of each A box (128, or fewer when M itself is smaller)
   uint32_t idesc;   // tcgen05 instruction descriptor for M=128, N=bn
   int n_tiles;      // ceil(Nout / bn)
@@ -145,7 +164,7 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
     ti.n0 = (local / mt_g) * p.bn;
     const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
     const int row0 = (int)rs + mt * C::BM;
-    ti.kb_count = (p.Kc + C::BK - 1) / C::BK;
+    ti.kb_count = (p.Kc + C::BK * C::KC - 1) / (C::BK * C::KC);
     ti.a_row = row0;
     ti.out_row0 = row0;
     ti.out_rows = (int)min((int64_t)C::BM, re - row0);
@@ -234,9 +253,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                       const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // ring stages, then the epilogue staging [EPI warps][NBUF buffers][32 x 128 B], then barriers
+  const int nst = C::DynRing ? p.stages : C::STAGES;
   uint8_t *sA = smem;
   uint8_t *sB = smem + C::STAGES * C::A_BYTES;
-  uint8_t *sOut = sB + C::STAGES * C::B_BYTES;  // [EPI warps][NBUF buffers][32 x 128 B]
+  uint8_t *sOut = C::DynRing ? smem + (size_t)nst * p.stage_bytes : sB + C::STAGES * C::B_BYTES;
+  auto stage_a = [&](int st) -> uint8_t * { return C::DynRing ? smem + (size_t)st * p.stage_bytes : sA + st * C::A_BYTES; };
+  auto stage_b = [&](int st) -> uint8_t * {
+    return C::DynRing ? smem + (size_t)st * p.stage_bytes + C::KC * p.a_rows * 128 : sB + st * C::B_BYTES;
+  };
   uint64_t *full = reinterpret_cast<uint64_t *>(sOut + C::EPI * C::NBUF * C::OUT_BUF);
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
@@ -258,7 +283,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (t_first >= total) return;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -311,7 +336,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // that are never stored
       // pair: the leader's full barrier counts the bytes of both CTAs
       const uint32_t tx = C::Pair ? 2u * (uint32_t)(C::A_BYTES + (bn / 2) * 128)
-                                  : (C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128;
+                                  : C::KC * ((C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128);
       for (int t = t_first; t < total && !*vabort; t += t_step) {
         const TileInfo ti = decode_tile<C>(t, p, av, rank);
         for (int kb = 0; kb < ti.kb_count; ++kb) {
@@ -320,8 +345,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             raise_abort();
             break;
           }
-          uint8_t *a = sA + stage * C::A_BYTES;
-          uint8_t *b = sB + stage * C::B_BYTES;
+          uint8_t *a = stage_a(stage);
+          uint8_t *b = stage_b(stage);
           if constexpr (C::Pair) {
             static_assert(C::Pair ? (C::Mode == kModeExperts && C::Fp8) : true, "CTA pairs serve FP8 wgrad");
             // each CTA copies its own halves; the peer's copies complete on the leader's barrier
@@ -336,7 +361,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               tma_load_2d_pair(a, &tmA, lbar, xr, ti.a_row);
               tma_load_2d_pair(b, &tmB, lbar, xr, ti.b_row);
             }
-            if (++stage == C::STAGES) {
+            if (++stage == nst) {
               stage = 0;
               phase ^= 1;
             }
@@ -344,7 +369,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           mbar_arrive_expect_tx(&full[stage], tx);
           ++issued;
-          if (C::Mode == kModeRows) {
+          if (C::Mode == kModeRows && C::KC > 1) {
+            // [KC chunks][a_rows][128 B] and [KC chunks][bn][128 B] in one copy each
+            tma_load_3d(a, &tmA, &full[stage], 0, ti.a_row, kb * C::KC);
+            tma_load_4d(b, &tmB, &full[stage], 0, ti.b_row, kb * C::KC, ti.e);
+          } else if (C::Mode == kModeRows) {
             tma_load_2d(a, &tmA, &full[stage], kb * C::BK, ti.a_row);
             if (C::BMn) {
               if (p.b_one_box) {  // [chunk][row][64 columns] in one copy: the layout the MMA reads
@@ -369,7 +398,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               tma_load_2d(b, &tmB, &full[stage], xr, ti.n0);
             }
           }
-          if (++stage == C::STAGES) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1;
           }
@@ -391,8 +420,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       for (int kb = 0; kb < ti.kb_count; ++kb) {
         if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
         tc_fence_after();
-        uint8_t *a = sA + stage * C::A_BYTES;
-        uint8_t *b = sB + stage * C::B_BYTES;
+        uint8_t *a = stage_a(stage);
+        uint8_t *b = stage_b(stage);
         // bf16 wgrad: at the partial last block of a group only the MMA
         // k-steps [k_first, k_last] hold group rows; the others are skipped,
         // and the out-of-group positions inside the partial step are cleared
@@ -417,18 +446,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const uint32_t abase = smem_u32(a), bbase = smem_u32(b);
           if (!edge) {
 #pragma unroll
-            for (int k = 0; k < C::KSTEPS; ++k) {
-              const uint64_t ad = C::AMn ? smem_desc_sw128(abase + k * C::UK * 128, C::CHUNK, 1024)
-                                         : smem_desc_sw128(abase + k * 32, 16, 1024);
-              const uint64_t bd = C::BMn ? smem_desc_sw128(bbase + k * C::UK * 128, C::CHUNK, 1024)
-                                         : smem_desc_sw128(bbase + k * 32, 16, 1024);
-              // the tile's first MMA overwrites the accumulator
-              if constexpr (C::Pair)
-                mma_f8_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
-              else if (C::Fp8)
-                mma_f8(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
-              else
-                mma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+            for (int j = 0; j < C::KC; ++j) {  // the stage's contraction blocks (one unless KC > 1)
+              const uint32_t aj = abase + j * p.a_rows * 128, bj = bbase + j * bn * 128;
+#pragma unroll
+              for (int k = 0; k < C::KSTEPS; ++k) {
+                const uint64_t ad = C::AMn ? smem_desc_sw128(aj + k * C::UK * 128, C::CHUNK, 1024)
+                                           : smem_desc_sw128(aj + k * 32, 16, 1024);
+                const uint64_t bd = C::BMn ? smem_desc_sw128(bj + k * C::UK * 128, C::CHUNK, 1024)
+                                           : smem_desc_sw128(bj + k * 32, 16, 1024);
+                // the tile's first MMA overwrites the accumulator
+                const bool acc_on = (kb | j | k) != 0;
+                if constexpr (C::Pair)
+                  mma_f8_pair(d_tmem, ad, bd, p.idesc, acc_on);
+                else if (C::Fp8)
+                  mma_f8(d_tmem, ad, bd, p.idesc, acc_on);
+                else
+                  mma_f16(d_tmem, ad, bd, p.idesc, acc_on);
+              }
             }
           } else {
             for (int k = k_first; k <= k_last; ++k) {
@@ -449,7 +483,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mma_commit(&empty[stage]);
         }
         __syncwarp();
-        if (++stage == C::STAGES) {
+        if (++stage == nst) {
           stage = 0;
           phase ^= 1;
         }
@@ -665,8 +699,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __syncthreads();
   if (*vabort && warp == 0 && lane == 0) {
     // wait for the TMA copies this CTA armed, bounded
-    for (int s = 0; s < C::STAGES; ++s) {
-      const uint32_t armed = issued / C::STAGES + ((uint32_t)s < issued % C::STAGES ? 1u : 0u);
+    for (int s = 0; s < nst; ++s) {
+      const uint32_t armed = issued / nst + ((uint32_t)s < issued % nst ? 1u : 0u);
       if (armed) mbar_wait(&full[s], (armed - 1) & 1, nullptr);
     }
     // pair: copies a peer issued for stages its leader never armed are not

@@ -66,6 +66,26 @@ int64_t rows_tiles_estimate(int64_t M, int E) {
   return dense > sparse ? dense : sparse;
 }
 
+// FP8 with few token rows: the operands viewed as 128-byte k-chunks so that one
+// box brings kc consecutive contraction blocks (the run-time-ring kernels with
+// kc blocks per stage).  A [M, Kc] as {128, M, Kc / 128}; B [E, Nrows, Kc] as
+// {128, Nrows, Kc / 128, E} (chunk stride 128 B; Kc % 128 == 0 keeps every box
+// row inside its row).
+bool few_maps(CUtensorMap *ta, CUtensorMap *tb, const void *a, int64_t M, int Kc, uint32_t a_rows, const void *b,
+              int Nrows, int E, int bn, uint32_t kc) {
+  const uint64_t da[3] = {128, (uint64_t)M, (uint64_t)Kc / 128};
+  const uint64_t sa[2] = {(uint64_t)Kc, 128};
+  const uint32_t ba[3] = {128, a_rows, kc};
+  const uint64_t db[4] = {128, (uint64_t)Nrows, (uint64_t)Kc / 128, (uint64_t)E};
+  const uint64_t sb[3] = {(uint64_t)Kc, 128, (uint64_t)Nrows * Kc};
+  const uint32_t bb[4] = {128, (uint32_t)bn, kc, 1};
+  CUtensorMap ma, mb;  // the caller's maps stay intact unless both views encode
+  if (!make_map(&ma, true, 3, a, da, sa, ba) || !make_map(&mb, true, 4, b, db, sb, bb)) return false;
+  *ta = ma;
+  *tb = mb;
+  return true;
+}
+
 // Map for the epilogue's TMA stores: the output viewed [rows, cols] bf16,
 // boxes of 32 rows x 64 columns, 128-byte swizzle.
 bool make_out_map(CUtensorMap *m, void *out, int64_t rows, int64_t cols) {
@@ -142,6 +162,15 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
   cudaStream_t s = (cudaStream_t)stream;
+  if (fp8 && a_rows < 128 && K % 128 == 0) {
+    // few token rows: the weight stream gets the shared memory the A slots leave
+    // (4 / 2 / 1 contraction blocks per stage for BN 64 / 128 / 256)
+    if (bn <= 64 && few_maps(&ta, &tb, x, M, K, a_rows, w, N, E, bn, 4))
+      return gemm_fp8_rows_few_narrow(ta, tb, to, p, grid, s);
+    if (bn > 64 && bn <= 128 && few_maps(&ta, &tb, x, M, K, a_rows, w, N, E, bn, 2))
+      return gemm_fp8_rows_few_mid(ta, tb, to, p, grid, s);
+    if (bn > 128) return gemm_fp8_rows_few(ta, tb, to, p, grid, s);
+  }
   if (bn <= 64) {
     if (fp8) return gemm_fp8_rows_narrow(ta, tb, to, p, grid, s);
     return trans_b ? gemm_bf16_rows_bk_narrow(ta, tb, to, p, grid, s)
@@ -200,6 +229,13 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
   cudaStream_t s = (cudaStream_t)stream;
+  if (fp8 && a_rows < 128 && N % 128 == 0) {
+    if (bn <= 64 && few_maps(&ta, &tb, grad_out, M, N, a_rows, w, K, E, bn, 4))
+      return gemm_fp8_rows_few_narrow(ta, tb, to, p, grid, s);
+    if (bn > 64 && bn <= 128 && few_maps(&ta, &tb, grad_out, M, N, a_rows, w, K, E, bn, 2))
+      return gemm_fp8_rows_few_mid(ta, tb, to, p, grid, s);
+    if (bn > 128) return gemm_fp8_rows_few(ta, tb, to, p, grid, s);
+  }
   if (bn <= 64) return fp8 ? gemm_fp8_rows_narrow(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk_narrow(ta, tb, to, p, grid, s);
   if (bn <= 128) return fp8 ? gemm_fp8_rows_mid(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk_mid(ta, tb, to, p, grid, s);
   return fp8 ? gemm_fp8_rows(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk(ta, tb, to, p, grid, s);

@@ -16,6 +16,18 @@ int gemm_fp8_experts_pair(const CUtensorMap &a, const CUtensorMap &b, const CUte
                           int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<true, false, false, kModeExperts, 256, 6, 1, true, 8>>(a, b, o, p, grid, s);
 }
+int gemm_fp8_rows_few(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                      cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows, 256, 24, 1, false, 8, true, 1>>(a, b, o, p, grid, s);
+}
+int gemm_fp8_rows_few_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                          int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows, 128, 24, 1, false, 8, true, 2>>(a, b, o, p, grid, s);
+}
+int gemm_fp8_rows_few_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                             int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows, 64, 24, 1, false, 8, true, 4>>(a, b, o, p, grid, s);
+}
 int gemm_fp8_rows_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                          int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<true, false, false, kModeRows, 64, 8, 1, false, 8>>(a, b, o, p, grid, s);

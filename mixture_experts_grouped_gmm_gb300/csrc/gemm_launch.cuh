@@ -7,8 +7,19 @@
 namespace mgemm {
 
 template <class C>
-int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p_in, int grid,
                 cudaStream_t s) {
+  GemmParams p = p_in;
+  size_t smem = C::SMEM_BYTES;
+  if constexpr (C::DynRing) {
+    // as many [A slot | B slot] stages as fit next to the staging buffers and barriers
+    p.stage_bytes = C::KC * (p.a_rows + p.bn) * 128;
+    const size_t room = (size_t)227 * 1024 - C::FIXED_BYTES;
+    const int fit = (int)(room / (size_t)p.stage_bytes);
+    p.stages = fit < C::STAGES ? fit : C::STAGES;
+    if (p.a_rows % 8 || p.stages < 2) return MGEMM_EINVAL;
+    smem = C::FIXED_BYTES + (size_t)p.stages * p.stage_bytes;
+  }
   static bool attr_done[64] = {};
   int dev = 0;
   int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
@@ -26,7 +37,7 @@ int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -37,7 +48,7 @@ int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o
     cfg.numAttrs = 1;
     return cuda_rc(cudaLaunchKernelEx(&cfg, mgemm_gemm_kernel<C>, a, b, o, p), "grouped GEMM launch (CTA pairs)");
   } else {
-    mgemm_gemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, b, o, p);
+    mgemm_gemm_kernel<C><<<grid, C::THREADS, smem, s>>>(a, b, o, p);
     return cuda_rc(cudaGetLastError(), "grouped GEMM launch");
   }
 }
@@ -67,6 +78,13 @@ int gemm_fp8_rows_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUten
 // fp8 forward / dgrad: both K-major, scaled epilogue
 int gemm_fp8_rows(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s);
+// the same with a run-time ring sized to the launch's token rows (fewer than 128), by tile width
+int gemm_fp8_rows_few(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                      cudaStream_t s);
+int gemm_fp8_rows_few_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                          int grid, cudaStream_t s);
+int gemm_fp8_rows_few_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                             int grid, cudaStream_t s);
 // fp8 wgrad: column-major quantized operands (K-major), scaled epilogue
 int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s);
