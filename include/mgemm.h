@@ -90,8 +90,10 @@ typedef struct CUstream_st *mgemm_stream_t;
  *   [P]   int64  poffsets[E+1] exclusive prefix sum of group_sizes each rounded up to
  *                MGEMM_COL_PAD: where group e starts in the padded column-major
  *                FP8 layout of mgemm_quant_colwise_grouped / mgemm_wgrad
+ *   [Q]   int32  ptile_start[E+1]  prefix over active groups of ceil(m_e / (2 MGEMM_TILE_M))
+ *                (the row-tile pairs of the FP8 GEMMs that run on CTA pairs)
  * with A = 24 + 8(E+1), T = A + 4E, W = T + 4(E+1), P = W + 4E rounded up to a
- * multiple of 8; mgemm_args_layout returns A, T and W.
+ * multiple of 8, Q = P + 8(E+1); mgemm_args_layout returns A, T and W.
  */
 size_t mgemm_args_bytes(int E);
 int mgemm_args_layout(int E, size_t *off_offsets, size_t *off_active, size_t *off_mtile_start,

@@ -80,12 +80,19 @@ __global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict
   const int pos = block_inclusive_scan<int, NT>(flag, tot32);
   const int tiles = flag ? (int)((m + MGEMM_TILE_M - 1) / MGEMM_TILE_M) : 0;
   const int tile_incl = block_inclusive_scan<int, NT>(tiles, tot32);
+  const int pairs = (tiles + 1) / 2;  // 256-row tiles of a CTA pair
+  const int pair_incl = block_inclusive_scan<int, NT>(pairs, tot32);
   int *active = (int *)(args + L.active);
   int *mtile_start = (int *)(args + L.mtile_start);
-  if (t == 0) mtile_start[0] = 0;
+  int *ptile_start = (int *)(args + L.ptile_start);
+  if (t == 0) {
+    mtile_start[0] = 0;
+    ptile_start[0] = 0;
+  }
   if (flag) {
     active[pos - 1] = t;
     mtile_start[pos] = tile_incl;
+    ptile_start[pos] = pair_incl;
   }
   __shared__ int n_active_sh;
   if (t == E - 1) n_active_sh = pos;

@@ -39,7 +39,7 @@ constexpr int kColPad = MGEMM_COL_PAD;
 static_assert(kColPad % 16 == 0, "padded groups keep 16-byte alignment");
 
 struct ArgsLayout {
-  size_t offsets, active, mtile_start, wgrad_order, poffsets, bytes;
+  size_t offsets, active, mtile_start, wgrad_order, poffsets, ptile_start, bytes;
 };
 
 __host__ __device__ inline ArgsLayout args_layout(int E) {
@@ -49,7 +49,8 @@ __host__ __device__ inline ArgsLayout args_layout(int E) {
   L.mtile_start = L.active + 4 * (size_t)E;
   L.wgrad_order = L.mtile_start + 4 * (size_t)(E + 1);
   L.poffsets = (L.wgrad_order + 4 * (size_t)E + 7) & ~(size_t)7;
-  L.bytes = (L.poffsets + 8 * (size_t)(E + 1) + 15) & ~(size_t)15;
+  L.ptile_start = L.poffsets + 8 * (size_t)(E + 1);
+  L.bytes = (L.ptile_start + 4 * (size_t)(E + 1) + 15) & ~(size_t)15;
   return L;
 }
 
@@ -62,6 +63,7 @@ struct ArgsView {
   const int *mtile_start;
   const int *wgrad_order;
   const int64_t *poffsets;  // padded column-major layout: group e starts at poffsets[e]
+  const int *ptile_start;   // prefix over active groups of ceil(m / 256): row-tile pairs of CTA pairs
   __device__ ArgsView(const void *base, int E) {
     uint8_t *b = (uint8_t *)base;
     ArgsLayout L = args_layout(E);
@@ -73,6 +75,7 @@ struct ArgsView {
     mtile_start = (const int *)(b + L.mtile_start);
     wgrad_order = (const int *)(b + L.wgrad_order);
     poffsets = (const int64_t *)(b + L.poffsets);
+    ptile_start = (const int *)(b + L.ptile_start);
   }
 };
 
@@ -280,6 +283,14 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *m, uint32_t cluster_bar, int c0,
+                                                 int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {

@@ -138,7 +138,7 @@ template <class C>
 __device__ __forceinline__ int total_tiles(const GemmParams &p, const ArgsView &av) {
   if (C::Mode == kModeRows) {
     const int na = *av.n_active;
-    return av.mtile_start[na] * p.n_tiles;
+    return (C::Pair ? av.ptile_start[na] : av.mtile_start[na]) * p.n_tiles;
   }
   return p.E * p.mt_k * p.n_tiles;
 }
@@ -147,28 +147,33 @@ template <class C>
 __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, const ArgsView &av, uint32_t rank) {
   TileInfo ti;
   if (C::Mode == kModeRows) {
-    // Group a owns tiles [mtile_start[a] * n_tiles, mtile_start[a+1] * n_tiles).
+    // Group a owns tiles [start[a] * n_tiles, start[a+1] * n_tiles), start being
+    // the 128-row tile prefix (or, for CTA pairs, the 256-row pair prefix).
     // Inside a group the row tile varies fastest, so CTAs running together
     // share one weight tile through L2 instead of each streaming its own.
+    const int *start = C::Pair ? av.ptile_start : av.mtile_start;
     const int gm = t / p.n_tiles;
     int lo = 0, hi = *av.n_active - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(av.mtile_start + mid) <= gm) lo = mid; else hi = mid - 1;
+      if (__ldg(start + mid) <= gm) lo = mid; else hi = mid - 1;
     }
     ti.e = __ldg(av.active + lo);
-    const int m_first = __ldg(av.mtile_start + lo);
-    const int mt_g = __ldg(av.mtile_start + lo + 1) - m_first;
+    const int m_first = __ldg(start + lo);
+    const int mt_g = __ldg(start + lo + 1) - m_first;
     const int local = t - m_first * p.n_tiles;
     const int mt = local % mt_g;
     ti.n0 = (local / mt_g) * p.bn;
     const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
-    const int row0 = (int)rs + mt * C::BM;
+    // a CTA pair's tile is 256 rows: rank r takes rows 128 r .. 128 r + 127 (the
+    // odd CTA's half may lie past the group: loaded, never stored) and columns
+    // n0 + r bn / 2 .. of B
+    const int row0 = (int)rs + (C::Pair ? mt * 2 * C::BM + (int)rank * C::BM : mt * C::BM);
     ti.kb_count = (p.Kc + C::BK * C::KC - 1) / (C::BK * C::KC);
     ti.a_row = row0;
     ti.out_row0 = row0;
-    ti.out_rows = (int)min((int64_t)C::BM, re - row0);
-    ti.b_row = ti.n0;
+    ti.out_rows = (int)max((int64_t)0, min((int64_t)C::BM, re - row0));
+    ti.b_row = C::Pair ? ti.n0 + (int)rank * (p.bn / 2) : ti.n0;
     ti.x0 = 0; ti.lo = 0; ti.hi = 0;
   } else {
     ti.n0 = (t % p.n_tiles) * p.bn;
@@ -348,18 +353,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           uint8_t *a = stage_a(stage);
           uint8_t *b = stage_b(stage);
           if constexpr (C::Pair) {
-            static_assert(C::Pair ? (C::Mode == kModeExperts && C::Fp8) : true, "CTA pairs serve FP8 wgrad");
+            static_assert(C::Pair ? (C::Fp8 && !C::AMn && !C::BMn) : true, "CTA pairs serve K-major FP8 operands");
             // each CTA copies its own halves; the peer's copies complete on the leader's barrier
-            const int xr = ti.x0 + kb * C::BK;
+            // (wgrad: column-major operands, contraction inner; rows: x [M, K], w [E, N, K])
+            const int xr = C::Mode == kModeExperts ? ti.x0 + kb * C::BK : kb * C::BK;
             if (leader) {
               mbar_arrive_expect_tx(&full[stage], tx);
               ++issued;
               tma_load_2d(a, &tmA, &full[stage], xr, ti.a_row);
-              tma_load_2d(b, &tmB, &full[stage], xr, ti.b_row);
+              if (C::Mode == kModeExperts)
+                tma_load_2d(b, &tmB, &full[stage], xr, ti.b_row);
+              else
+                tma_load_3d(b, &tmB, &full[stage], xr, ti.b_row, ti.e);
             } else {
               const uint32_t lbar = cluster_addr(&full[stage], 0);
               tma_load_2d_pair(a, &tmA, lbar, xr, ti.a_row);
-              tma_load_2d_pair(b, &tmB, lbar, xr, ti.b_row);
+              if (C::Mode == kModeExperts)
+                tma_load_2d_pair(b, &tmB, lbar, xr, ti.b_row);
+              else
+                tma_load_3d_pair(b, &tmB, lbar, xr, ti.b_row, ti.e);
             }
             if (++stage == nst) {
               stage = 0;

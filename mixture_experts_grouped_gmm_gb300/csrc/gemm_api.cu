@@ -86,6 +86,22 @@ bool few_maps(CUtensorMap *ta, CUtensorMap *tb, const void *a, int64_t M, int Kc
   return true;
 }
 
+// CTA pairs pay where a pair's 256-row tile is mostly real rows: groups that
+// average at least 256 rows.  With fewer rows per group (sparse routing) the
+// odd CTA's half of most tiles would be empty and the pair only couples two
+// epilogues.
+bool pairs_pay(int64_t M, int E) {
+  const int64_t groups = M < E ? M : E;
+  return groups > 0 && M / groups >= 256;
+}
+
+// Rows-mode estimate of 256-row pair tiles (CTA pairs).
+int64_t pair_tiles_estimate(int64_t M, int E) {
+  const int64_t dense = (M + 255) / 256;
+  const int64_t sparse = M < E ? M : E;
+  return dense > sparse ? dense : sparse;
+}
+
 // Map for the epilogue's TMA stores: the output viewed [rows, cols] bf16,
 // boxes of 32 rows x 64 columns, 128-byte swizzle.
 bool make_out_map(CUtensorMap *m, void *out, int64_t rows, int64_t cols) {
@@ -118,12 +134,17 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
     const uint32_t box[2] = {bk, a_rows};
     if (!make_map(&ta, fp8, 2, x, d, st, box)) return MGEMM_ECUDA;
   }
-  const int bn = choose_bn(rows_tiles_estimate(M, E), N);
+  // FP8 with at least 128 token rows runs on CTA pairs: 256-row tiles, each CTA
+  // copying bn / 2 rows of the weight tile
+  const int sms = sm_count();
+  if (sms <= 1) return MGEMM_ECUDA;
+  const bool pair = fp8 && a_rows == 128 && pairs_pay(M, E);
+  const int bn = pair ? choose_bn_units(pair_tiles_estimate(M, E), N, sms / 2) : choose_bn(rows_tiles_estimate(M, E), N);
   bool b_one_box = false;
   if (trans_b) {  // w [E, N, K]
     const uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
     const uint64_t st[2] = {(uint64_t)K * es, (uint64_t)N * K * es};
-    const uint32_t box[3] = {bk, (uint32_t)bn, 1};
+    const uint32_t box[3] = {bk, (uint32_t)(pair ? bn / 2 : bn), 1};
     if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
   } else {  // w [E, K, N], loaded as 64-column MN-major chunks
     // with N % 64 == 0, w is viewed as [E][N / 64 chunks][K rows][64 columns] (chunk stride 128 B)
@@ -150,7 +171,7 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   p.E = E;
   p.bn = bn;
   p.b_one_box = b_one_box ? 1 : 0;
-  p.idesc = make_idesc(fp8 ? 0u : 1u, false, !trans_b, 128, bn);
+  p.idesc = make_idesc(fp8 ? 0u : 1u, false, !trans_b, pair ? 256 : 128, bn);
   p.a_rows = (int)a_rows;
   p.n_tiles = (N + bn - 1) / bn;
   p.Kc = K;
@@ -158,10 +179,15 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   p.out = (__nv_bfloat16 *)out;
   p.rscale = sx;
   p.cscale = sw;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (pair) {
+    const int64_t pupper = pair_tiles_estimate(M, E) * p.n_tiles + (M < E ? M : E) * p.n_tiles;
+    const int pairs = (int)(pupper < sms / 2 ? pupper : sms / 2);
+    return gemm_fp8_rows_pair(ta, tb, to, p, 2 * pairs, s);
+  }
   const int64_t upper = ((M + 127) / 128 + (M < E ? M : E)) * p.n_tiles;
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
-  cudaStream_t s = (cudaStream_t)stream;
   if (fp8 && a_rows < 128 && K % 128 == 0) {
     // few token rows: the weight stream gets the shared memory the A slots leave
     // (4 / 2 / 1 contraction blocks per stage for BN 64 / 128 / 256)
@@ -204,11 +230,14 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
     const uint32_t box[2] = {bk, a_rows};
     if (!make_map(&ta, fp8, 2, grad_out, d, st, box)) return MGEMM_ECUDA;
   }
-  const int bn = choose_bn(rows_tiles_estimate(M, E), K);
+  const int sms = sm_count();
+  if (sms <= 1) return MGEMM_ECUDA;
+  const bool pair = fp8 && a_rows == 128 && pairs_pay(M, E);  // CTA pairs, as in mgemm_fwd
+  const int bn = pair ? choose_bn_units(pair_tiles_estimate(M, E), K, sms / 2) : choose_bn(rows_tiles_estimate(M, E), K);
   {  // w [E, K, N]: output column k, contraction n contiguous
     const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
     const uint64_t st[2] = {(uint64_t)N * es, (uint64_t)K * N * es};
-    const uint32_t box[3] = {bk, (uint32_t)bn, 1};
+    const uint32_t box[3] = {bk, (uint32_t)(pair ? bn / 2 : bn), 1};
     if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
   }
   CUtensorMap to;
@@ -217,7 +246,7 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   p.args = (const uint8_t *)args;
   p.E = E;
   p.bn = bn;
-  p.idesc = make_idesc(fp8 ? 0u : 1u, false, false, 128, bn);
+  p.idesc = make_idesc(fp8 ? 0u : 1u, false, false, pair ? 256 : 128, bn);
   p.a_rows = (int)a_rows;
   p.n_tiles = (K + bn - 1) / bn;
   p.Kc = N;
@@ -225,10 +254,15 @@ extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, co
   p.out = (__nv_bfloat16 *)grad_x;
   p.rscale = sgo;
   p.cscale = sw;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (pair) {
+    const int64_t pupper = pair_tiles_estimate(M, E) * p.n_tiles + (M < E ? M : E) * p.n_tiles;
+    const int pairs = (int)(pupper < sms / 2 ? pupper : sms / 2);
+    return gemm_fp8_rows_pair(ta, tb, to, p, 2 * pairs, s);
+  }
   const int64_t upper = ((M + 127) / 128 + (M < E ? M : E)) * p.n_tiles;
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
-  cudaStream_t s = (cudaStream_t)stream;
   if (fp8 && a_rows < 128 && N % 128 == 0) {
     if (bn <= 64 && few_maps(&ta, &tb, grad_out, M, N, a_rows, w, K, E, bn, 4))
       return gemm_fp8_rows_few_narrow(ta, tb, to, p, grid, s);

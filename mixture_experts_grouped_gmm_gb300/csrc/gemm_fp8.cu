@@ -12,6 +12,10 @@ int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorM
                        cudaStream_t s) {
   return launch_gemm<GemmCfg<true, false, false, kModeExperts, 256, 4, 1, false, 8>>(a, b, o, p, grid, s);
 }
+int gemm_fp8_rows_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows, 256, 6, 1, true, 8>>(a, b, o, p, grid, s);
+}
 int gemm_fp8_experts_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                           int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<true, false, false, kModeExperts, 256, 6, 1, true, 8>>(a, b, o, p, grid, s);

@@ -88,6 +88,9 @@ int gemm_fp8_rows_few_narrow(const CUtensorMap &a, const CUtensorMap &b, const C
 // fp8 wgrad: column-major quantized operands (K-major), scaled epilogue
 int gemm_fp8_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s);
+// fp8 forward / dgrad with at least 128 token rows on CTA pairs (256-row tiles inside a group; grid even)
+int gemm_fp8_rows_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
+                       cudaStream_t s);
 // the same on CTA pairs (256-row tiles of K, cta_group::2; grid even)
 int gemm_fp8_experts_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                           int grid, cudaStream_t s);

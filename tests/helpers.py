@@ -43,6 +43,8 @@ def parse_args(args, E):
     out["wgrad_order"] = np.frombuffer(raw[lay["wgrad_order"]:lay["wgrad_order"] + 4 * E], dtype=np.int32).tolist()
     P = (lay["wgrad_order"] + 4 * E + 7) // 8 * 8           # header: W + 4E rounded up to 8
     out["poffsets"] = np.frombuffer(raw[P:P + 8 * (E + 1)], dtype=np.int64).tolist()
+    Q = P + 8 * (E + 1)
+    out["ptile_start"] = np.frombuffer(raw[Q:Q + 4 * (E + 1)], dtype=np.int32).tolist()
     return out
 
 

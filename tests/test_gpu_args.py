@@ -37,6 +37,12 @@ def compare(sizes):
     assert got["mtile_start"][:na + 1] == ref["mtile_start"]
     assert got["wgrad_order"] == ref["wgrad_order"]
     assert got["poffsets"] == padded_offsets(sizes)
+    # row-tile pairs (256 rows) of the active groups, prefix summed (header: ptile_start)
+    pairs = [0]
+    for m in sizes:
+        if m > 0:
+            pairs.append(pairs[-1] + (-(-int(m) // 128) + 1) // 2)
+    assert got["ptile_start"][:na + 1] == pairs
 
 
 @pytest.mark.parametrize("E", [1, 2, 4, 8, 31, 32, 33, 64, 128, 129, 500, 1000, 1024])
