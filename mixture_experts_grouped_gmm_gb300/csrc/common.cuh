@@ -42,8 +42,8 @@ struct ArgsLayout {
   size_t offsets, active, mtile_start, wgrad_order, poffsets, ptile_start, bytes;
 };
 
-__host__ __device__ inline ArgsLayout args_layout(int E) {
-  ArgsLayout L;
+__host__ __device__ constexpr ArgsLayout args_layout(int E) {
+  ArgsLayout L{};
   L.offsets = 24;
   L.active = L.offsets + 8 * (size_t)(E + 1);
   L.mtile_start = L.active + 4 * (size_t)E;

@@ -11,7 +11,7 @@
 // block in a statically sized device array that lives in this library.
 //
 // The array holds an args block for up to MGEMM_NOALLOC_MAX_EXPERTS experts
-// (about 20 KB); every GPU that loads the library keeps it until the process
+// (about 33 KB); every GPU that loads the library keeps it until the process
 // exits.  All calls share it, so calls whose work overlaps on the GPU (for
 // example on two streams) race on it.  Each call rewrites every part of it
 // that the forward kernel reads (mgemm_fill_args writes the whole header,
@@ -23,12 +23,7 @@
 
 namespace {
 
-constexpr size_t noalloc_args_bytes() {
-  // same layout as mgemm_args_layout(E) with E = MGEMM_NOALLOC_MAX_EXPERTS
-  return (24 + 8 * (size_t)(MGEMM_NOALLOC_MAX_EXPERTS + 1) + 4 * (size_t)MGEMM_NOALLOC_MAX_EXPERTS +
-          4 * (size_t)(MGEMM_NOALLOC_MAX_EXPERTS + 1) + 4 * (size_t)MGEMM_NOALLOC_MAX_EXPERTS + 15) &
-         ~(size_t)15;
-}
+constexpr size_t noalloc_args_bytes() { return mgemm::args_layout(MGEMM_NOALLOC_MAX_EXPERTS).bytes; }
 
 static __device__ __align__(256) uint8_t g_noalloc_args[noalloc_args_bytes()];
 

@@ -73,3 +73,6 @@ def test_noalloc_rejects_too_many_experts():
     too_many = 1025
     assert lib.mgemm_fwd_noalloc(p, too_many, 0, 0, p, None, p, None, p, 64, 128, 256, None) == -3
     assert lib.mgemm_fwd_noalloc(None, 8, 0, 0, p, None, p, None, p, 64, 128, 256, None) == -1
+    # the stated maximum fits the library's array: E = 1024 passes the size check (and then,
+    # without a GPU here, fails at the first CUDA call rather than as too many experts)
+    assert lib.mgemm_fwd_noalloc(p, 1024, 0, 0, p, None, p, None, p, 64, 128, 256, None) not in (-1, -3)
