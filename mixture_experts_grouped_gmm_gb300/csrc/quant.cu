@@ -17,8 +17,8 @@
 //            the boxes with transposing ldmatrix, reduce the column magnitude
 //            max (pass 1), then convert two rows of one column per e4m3x2
 //            conversion so the codes come out column-major (pass 2), stage
-//            256-row chunks in shared memory and write each column's bytes
-//            contiguously.
+//            them in shared memory, and write them with TMA tensor stores,
+//            each column's bytes contiguous.
 #include "common.cuh"
 
 namespace mgemm {
@@ -121,9 +121,10 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 //            keeps a packed bf16x2 running max of magnitudes; pass 2 scales
 //            each register with one packed fp32 multiply and converts it to an
 //            e4m3 pair that is already in column-major order, stores it as 16
-//            bits into one of two [64 columns][256 rows] tiles, and the CTA
-//            writes that tile out as 16-byte column-contiguous stores while
-//            the next box is converted into the other tile.  Rows past the
+//            bits into one of two tiles (two [64 columns][128 rows] halves,
+//            16-byte chunks swizzled by the column), and one thread writes
+//            that tile out with TMA tensor stores while the next box is
+//            converted into the other tile.  Rows past the
 //            group are cleared before the cast, so the padding of every
 //            column is written as zero codes.  A group spanning at most 5
 //            boxes stays in the ring between the passes instead of being
@@ -141,9 +142,9 @@ constexpr int kCwStages = 5;
 constexpr int kCwConsumers = 16;
 constexpr int kCwThreads = (kCwConsumers + 1) * 32;
 constexpr int kCwBox = kCwRows * 128;   // 32 KB
-constexpr int kCwPitch = kCwRows + 16;  // transposed tile: bytes per column
+constexpr int kCwTile = 64 * kCwRows;   // transposed tile: 2 halves of [64 columns][128 rows] codes
 constexpr int kCwQueue = 4;  // item ids handed from the producer to the consumers
-constexpr size_t kCwSmemFixed = 1024 + (size_t)kCwStages * kCwBox + 2 * 64 * kCwPitch + 2 * 2 * 64 * 4 + 256;
+constexpr size_t kCwSmemFixed = 1024 + (size_t)kCwStages * kCwBox + 2 * kCwTile + 2 * 2 * 64 * 4 + 256;
 // plus a copy of the group offsets, the padded offsets and the size order: 16 (E + 1) + 4 E bytes
 __host__ __device__ constexpr size_t cw_smem_bytes(int E) {
   return kCwSmemFixed + 16 * (size_t)(E + 1) + 4 * (size_t)E + 16;
@@ -232,14 +233,15 @@ __device__ __forceinline__ bool cw_consumer_barrier_any(bool flag) {
 
 __global__ void __launch_bounds__(kCwThreads, 1)
     quant_colwise_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm2,
+                         const __grid_constant__ CUtensorMap tmo1, const __grid_constant__ CUtensorMap tmo2,
                          const uint8_t *__restrict__ args, int E, int64_t ld, ColTensor t1, ColTensor t2,
                          int items) {
   extern __shared__ uint8_t cw_smem_raw[];
   uint8_t *smem =
       reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(cw_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *ring = smem;
-  uint8_t *tiles = ring + kCwStages * kCwBox;                         // 2 x [64][kCwPitch]
-  float *red = reinterpret_cast<float *>(tiles + 2 * 64 * kCwPitch);  // [2 items][2 halves][64]
+  uint8_t *tiles = ring + kCwStages * kCwBox;                  // 2 x kCwTile
+  float *red = reinterpret_cast<float *>(tiles + 2 * kCwTile);  // [2 items][2 halves][64]
   uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * 2 * 64);
   uint64_t *empty = full + kCwStages;
   uint64_t *qfull = empty + kCwStages;
@@ -279,6 +281,8 @@ __global__ void __launch_bounds__(kCwThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm1);
       tma_prefetch_desc(&tm2);
+      tma_prefetch_desc(&tmo1);
+      tma_prefetch_desc(&tmo2);
       int stage = 0, q = 0;
       uint32_t phase = 0, qphase = 0;
       // Items are taken from the args block's work counter in order of
@@ -327,8 +331,10 @@ __global__ void __launch_bounds__(kCwThreads, 1)
     const int cc = warp & 7, rhalf = warp >> 3;
     const int lcol = cc * 8 + (lane >> 2);  // this lane's column within the block
     const int rpair = 2 * (lane & 3);       // row offset of its pair inside each 8-row matrix
-    const int st_c = threadIdx.x >> 4;      // store phase: columns st_c, st_c + 32
-    const int st_seg = threadIdx.x & 15;    //              16-row segment
+    // this lane's column in a transposed half-tile: 128 bytes (rows) per
+    // column, 16-byte chunks swizzled by the column (the 128-byte pattern the
+    // output tensor maps store with)
+    const uint32_t tsw = (uint32_t)(lcol & 7);
     int stage = 0, q = 0;
     uint32_t phase = 0, qphase = 0;
     uint32_t tile_par = 0;  // alternates with every pass-2 box, across items
@@ -418,9 +424,9 @@ __global__ void __launch_bounds__(kCwThreads, 1)
       for (int k = 0; k < it.nck; ++k) {
         if (!resident) wait_full();
         const uint8_t *box = ring + stage * kCwBox;
-        uint8_t *tile = tiles + tile_par * (64 * kCwPitch);
+        uint8_t *tile = tiles + tile_par * kCwTile;
         tile_par ^= 1;
-        uint8_t *tcol = tile + lcol * kCwPitch + rhalf * 128 + rpair;
+        uint8_t *tcol = tile + rhalf * (kCwTile / 2) + lcol * 128 + rpair;
         // rows past the group become zero codes: the padding of the column
         const int64_t r0 = it.rs + (int64_t)k * kCwRows + rhalf * 128;
         const bool edge = it.rs + (int64_t)(k + 1) * kCwRows > it.re;
@@ -436,36 +442,42 @@ __global__ void __launch_bounds__(kCwThreads, 1)
               if (gr >= it.re) x &= 0xFFFF0000u;
               if (gr + 1 >= it.re) x &= 0x0000FFFFu;
             }
-            *reinterpret_cast<uint16_t *>(tcol + j * 32 + m * 8) = bf16x2_scaled_e4m3x2(x, sc2);
+            // rows j*32 + m*8 + rpair, +1 of the half: chunk 2j + m/2, byte 8 (m & 1) + rpair
+            const uint32_t chunk = (uint32_t)(2 * j + (m >> 1)) ^ tsw;
+            *reinterpret_cast<uint16_t *>(tcol + chunk * 16 + (m & 1) * 8) = bf16x2_scaled_e4m3x2(x, sc2);
           }
         }
+        fence_proxy_async_smem();  // the codes are read by the tensor store below
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);  // box consumed; the codes live in the tile
         if (++stage == kCwStages) {
           stage = 0;
           phase ^= 1;
         }
-        // every warp has finished this tile; the stores that used it before
-        // (two boxes ago) were issued before those warps reached this barrier
+        // The tile written next was last stored two boxes ago: its store has
+        // finished reading before any warp passes this barrier.
+        if (threadIdx.x == 0) bulk_wait_read<0>();
         if (cw_consumer_barrier_any(*vabort != 0)) {
           aborted = true;
           break;
         }
-        // 64 columns x 16 segments of 16 rows, 512 consumer threads: this
-        // thread stores segment st_seg of columns st_c and st_c + 32 (whole
-        // 16-byte segments: the group's padded rows are a multiple of 16)
-        const int64_t q0 = (int64_t)k * kCwRows + st_seg * 16;  // offset inside the group's padded rows
+        // one thread stores the box's halves that hold rows of the group's
+        // padded length (a multiple of 128): [64 columns][128 rows] each, to
+        // rows pos + 256 k + 128 h of columns col0 .. col0 + 63 (the map clips
+        // the columns past C)
+        if (threadIdx.x == 0) {
+          const CUtensorMap *tmo = it.tensor == 0 ? &tmo1 : &tmo2;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = st_c + 32 * u;
-          const int64_t col = col0 + c;
-          if (col >= T.C || q0 >= it.plen) continue;
-          *reinterpret_cast<uint4 *>(T.out + col * ld + it.pos + q0) =
-              *reinterpret_cast<const uint4 *>(tile + c * kCwPitch + st_seg * 16);
+          for (int h = 0; h < 2; ++h) {
+            const int64_t q = (int64_t)k * kCwRows + h * 128;
+            if (q < it.plen) tma_store_2d(tmo, tile + h * (kCwTile / 2), (int)(it.pos + q), (int)col0);
+          }
+          bulk_commit();
         }
       }
       if (aborted) break;
     }
+    if (threadIdx.x == 0) bulk_wait_all();  // the tensor stores are complete before the CTA leaves
   }
   __syncthreads();
   if (*vabort && warp == kCwConsumers && lane == 0) {
@@ -545,6 +557,23 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
   } else {
     tm2 = tm1;
   }
+  // the outputs: column c of the padded layout is row c of a [C][ld] byte
+  // matrix; boxes of 64 columns x 128 rows (bytes)
+  CUtensorMap tmo1, tmo2;
+  {
+    const uint64_t d[2] = {(uint64_t)ld, (uint64_t)C1};
+    const uint64_t st[1] = {(uint64_t)ld};
+    const uint32_t box[2] = {128, 64};
+    if (!make_tensor_map(&tmo1, true, 2, out1, d, st, box)) return MGEMM_ECUDA;
+  }
+  if (in2) {
+    const uint64_t d[2] = {(uint64_t)ld, (uint64_t)C2};
+    const uint64_t st[1] = {(uint64_t)ld};
+    const uint32_t box[2] = {128, 64};
+    if (!make_tensor_map(&tmo2, true, 2, out2, d, st, box)) return MGEMM_ECUDA;
+  } else {
+    tmo2 = tmo1;
+  }
   ColTensor t1{out1, sc1, C1, (int)((C1 + 63) / 64)};
   ColTensor t2{out2, sc2, in2 ? C2 : 0, in2 ? (int)((C2 + 63) / 64) : 0};
   const int64_t items = (int64_t)E * (t1.ncb + t2.ncb);
@@ -563,6 +592,6 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
     attr_done[dev] = true;
   }
   quant_colwise_kernel<<<grid, kCwThreads, cw_smem_bytes(E), (cudaStream_t)stream>>>(
-      tm1, tm2, (const uint8_t *)args, E, ld, t1, t2, (int)items);
+      tm1, tm2, tmo1, tmo2, (const uint8_t *)args, E, ld, t1, t2, (int)items);
   return cuda_rc(cudaGetLastError(), "mgemm_quant_colwise_grouped launch");
 }

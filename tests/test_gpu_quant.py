@@ -137,6 +137,14 @@ def test_colwise_group_over_many_segments():
     colwise_case([20000, 3, 0, 4997], 1024, 512, seed=5)
 
 
+def test_colwise_split_groups_every_chunk_shape():
+    # Groups of more than 5 boxes (1280 rows) are split across the CTAs of a
+    # cluster: 6 boxes over 8 CTAs (some CTAs read none), 9, 12 (every chunk
+    # stays in the ring), 47 (chunks of 5 and 6 boxes: some are read twice),
+    # next to small and empty groups, over two tensors of different widths.
+    colwise_case([1281, 12000, 0, 2100, 1300, 3000, 17, 250], 200, 136, seed=21)
+
+
 def test_colwise_status_blocks_writes():
     E, M, C = 3, 48, 64
     gs = torch.tensor([16, -1, 33], dtype=torch.int64, device=DEV)
@@ -151,10 +159,11 @@ def test_colwise_status_blocks_writes():
     assert (to_np(o) == 0xAB).all() and (to_np(s) == -1.0).all()
 
 
-def test_colwise_repeated_on_one_args_block():
+@pytest.mark.parametrize("sizes", [[300, 0, 77, 1000, 5, 130], [300, 0, 77, 3000, 5, 1500]])
+def test_colwise_repeated_on_one_args_block(sizes):
     # the work counter in the args header is handed back at 0, so a second call
-    # with the same args block sees every item again
-    sizes = [300, 0, 77, 1000, 5, 130]
+    # with the same args block sees every item again (with and without groups
+    # split across CTAs)
     E, M = len(sizes), int(np.sum(sizes))
     gs = torch.tensor(sizes, dtype=torch.int64, device=DEV)
     args = new_args(E, DEV)
