@@ -11,7 +11,7 @@
 //       order sorted by group size, largest first, and empty experts get a
 //       zero tile with no main loop ("Support GPU-resident batch sizes",
 //       review of csrc/fill_arguments.cuh and ZeroOutK0Outputs).
-// BN (64, 128 or 256) is chosen per launch on the host to balance the tile
+// BN (64, 128, 192 or 256) is chosen per launch on the host to balance the tile
 // count against the number of SMs.
 //
 // CTA layout (64 + 32 x EPI threads, one CTA per SM, grid = number of SMs,
@@ -58,9 +58,11 @@ namespace mgemm {
 enum { kModeRows = 0, kModeExperts = 1 };
 
 // kBnMax / kStages: the widest output tile this instantiation serves and its
-// ring depth.  Wide (256, 4 stages), mid (128, 6) and narrow (64, 8) forms
-// fill the same shared memory; the narrower forms serve weight-streaming
-// launches, where a deeper ring keeps more HBM reads in flight per SM.
+// ring depth.  Wide (256, 4 stages), 192-wide (5), mid (128, 6) and narrow
+// (64, 8) forms fill the same shared memory; the narrower forms serve
+// weight-streaming launches, where a deeper ring keeps more HBM reads in
+// flight per SM, and the 192-wide one gives the weight tile the largest share
+// of the ring (the A tile, re-read from L2, is the same 16 KB in every form).
 // kPair: a cluster of two CTAs computes one 256-row tile with cta_group::2
 // MMAs (each CTA loads its 128 rows of A and half of B's columns), so every SM
 // reads half of the B tile it would otherwise read.
@@ -96,7 +98,13 @@ struct GemmCfg {
   static constexpr int B_BYTES = (kPair ? BN_MAX / 2 : BN_MAX) * 128;
   static constexpr int STAGES = kStages;
   static constexpr int CHUNK = 64 * 128;  // MN-major: one 64-element x BK-row block (8 KB)
-  static constexpr int TMEM_COLS = 2 * BN_MAX;  // a power of two >= 32
+  // two accumulators of BN_MAX columns, allocated as a power of two >= 32
+  static constexpr int TMEM_COLS = 2 * BN_MAX <= 32    ? 32
+                                   : 2 * BN_MAX <= 64  ? 64
+                                   : 2 * BN_MAX <= 128 ? 128
+                                   : 2 * BN_MAX <= 256 ? 256
+                                                       : 512;
+  static_assert(2 * BN_MAX <= 512, "two accumulators fit in TMEM");
   static constexpr int EPI = kEpiWarps;
   static_assert(EPI == 4 || EPI == 8, "one or two epilogue warps per TMEM lane quarter");
   static constexpr int HN = EPI / 4;         // epilogue warps per lane quarter

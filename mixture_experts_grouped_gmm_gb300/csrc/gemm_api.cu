@@ -38,11 +38,12 @@ int grid_for(int64_t tiles_upper) {
 // overhead), where waves = ceil(estimated tiles / SMs); ties go to the wider
 // tile (better operand reuse in shared memory).  m_tiles_est is the host's
 // estimate of 128-row tiles (the exact count lives on the device).
-int choose_bn_units(int64_t m_tiles_est, int64_t n_cols, int units) {
+int choose_bn_units(int64_t m_tiles_est, int64_t n_cols, int units, bool allow192 = false) {
   const int sms = units > 0 ? units : 1;
   int best = 256;
   int64_t best_cost = -1;
-  for (int bn : {256, 128, 64}) {
+  for (int bn : {256, 192, 128, 64}) {
+    if (bn == 192 && !allow192) continue;
     const int64_t tiles = m_tiles_est * ((n_cols + bn - 1) / bn);
     const int64_t waves = (tiles + sms - 1) / sms;
     const int64_t cost = waves * (bn + 64);
@@ -54,8 +55,8 @@ int choose_bn_units(int64_t m_tiles_est, int64_t n_cols, int units) {
   return best;
 }
 
-int choose_bn(int64_t m_tiles_est, int64_t n_cols) {
-  return choose_bn_units(m_tiles_est, n_cols, sm_count() > 0 ? sm_count() : 148);
+int choose_bn(int64_t m_tiles_est, int64_t n_cols, bool allow192 = false) {
+  return choose_bn_units(m_tiles_est, n_cols, sm_count() > 0 ? sm_count() : 148, allow192);
 }
 
 // Rows-mode estimate of 128-row tiles: dense groups give about M/128, sparse
@@ -139,7 +140,12 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   const int sms = sm_count();
   if (sms <= 1) return MGEMM_ECUDA;
   const bool pair = fp8 && a_rows == 128 && pairs_pay(M, E);
-  const int bn = pair ? choose_bn_units(pair_tiles_estimate(M, E), N, sms / 2) : choose_bn(rows_tiles_estimate(M, E), N);
+  // 192-wide tiles (a 5-stage ring whose weight tiles are 24 KB of each 40 KB
+  // stage): bf16 with w [E, K, N] in one box per stage, when the weights
+  // stream (at most 256 rows per expert on average, so HBM bounds the launch)
+  const bool allow192 = !fp8 && !trans_b && N % 64 == 0 && M <= 256 * (int64_t)E;
+  const int bn = pair ? choose_bn_units(pair_tiles_estimate(M, E), N, sms / 2)
+                      : choose_bn(rows_tiles_estimate(M, E), N, allow192);
   bool b_one_box = false;
   if (trans_b) {  // w [E, N, K]
     const uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
@@ -206,6 +212,7 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
     if (fp8) return gemm_fp8_rows_mid(ta, tb, to, p, grid, s);
     return trans_b ? gemm_bf16_rows_bk_mid(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn_mid(ta, tb, to, p, grid, s);
   }
+  if (bn == 192 && b_one_box) return gemm_bf16_rows_bmn_w192(ta, tb, to, p, grid, s);
   if (fp8) return gemm_fp8_rows(ta, tb, to, p, grid, s);
   return trans_b ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, to, p, grid, s);
 }

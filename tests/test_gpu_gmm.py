@@ -75,6 +75,26 @@ def test_fwd_bf16(sizes, K, N, trans_b):
     assert_close(to_np(out), ref, BF16_TOL, "fwd")
 
 
+@pytest.mark.parametrize("sizes,K,N,kind", [
+    ([128] * 8, 256, 3072, "uniform"),
+    ([128, 0, 300, 7, 128, 256, 64, 141], 192, 3008, "normal"),  # last tile 128 of 192 columns
+    ([128, 0, 300, 7, 128, 256, 64, 141], 192, 3008, "int"),
+])
+def test_fwd_bf16_weight_streaming_192_wide(sizes, K, N, kind):
+    # 8 row tiles at most 256 rows per expert and w [E, K, N]: 192-wide tiles
+    # take one wave (16 x 8 tiles) where 128-wide ones take two, so these
+    # launches run the 192-wide, 5-stage form
+    M, E = int(np.sum(sizes)), len(sizes)
+    x = rand_bf16((M, K), 21, kind)
+    w = rand_bf16((E, K, N), 22, kind)
+    out = bf16_fwd(sizes, K, N, x, w, 0)
+    ref = og.gmm_fwd(to_np(x), to_np(w), sizes, trans_b=False)
+    if kind == "int":
+        assert np.array_equal(to_np(out), formats.round_bf16(ref)), "integer inputs: exact"
+    else:
+        assert_close(to_np(out), ref, BF16_TOL, "fwd 192-wide")
+
+
 @pytest.mark.parametrize("sizes,K,N", CASES)
 def test_dgrad_bf16(sizes, K, N):
     M, E = int(np.sum(sizes)), len(sizes)
