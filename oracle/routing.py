@@ -1,0 +1,75 @@
+"""Routing-side steps of the fused MoE layer, restated as plain Python (oracle;
+test infrastructure only).
+
+Source: pytorch-labs/applied-ai issue 24 (the column-major fused MoE script,
+built on vLLM's fused_moe.py): the docstring of ``moe_align_block_size`` and
+its worked example, the docstring and body of ``fused_moe_kernel``, and
+``fused_moe``.
+
+What ``moe_align_block_size`` computes (docstring): the flat list of
+(token, slot) entries of ``topk_ids`` (row-major, so entry i belongs to token
+i // top_k) is grouped by expert; each expert's entries are padded with the
+id ``numel`` up to a multiple of ``block_size``; ``expert_ids`` names the expert
+of every block and ``num_tokens_post_padded`` is the padded total.
+
+Readings (where the page is silent or garbled):
+* Order inside an expert: ascending flat index (stable); the worked example
+  shows exactly that.
+* The worked example names experts 1..4 under ``num_experts = 4``; read as
+  0-based expert ids with five experts, expert 0 receiving no entries.  An
+  expert with no entries gets no block (padding rounds 0 up to 0).
+* Experts appear in ascending id.
+* Buffer sizes are the page's: ``sorted_token_ids`` holds
+  ``numel + num_experts * (block_size - 1)`` entries, pre-filled with ``numel``
+  (so every position past the padded total also reads ``numel``).
+  ``expert_ids`` is sized here to the largest possible block count,
+  ``(numel + num_experts * (block_size - 1)) // block_size``; the page leaves
+  the unused tail uninitialized, here it holds -1.
+* Entries outside [0, num_experts) are not placed anywhere (the page does not
+  say; vLLM would index out of bounds).
+* ``group_sizes`` (not on the page) is each expert's padded count, the row
+  count the grouped GEMM of this library takes per expert.
+"""
+
+
+def buffer_sizes(numel, num_experts, block_size):
+    """(entries of sorted_token_ids, entries of expert_ids)."""
+    cap = numel + num_experts * (block_size - 1)
+    return cap, cap // block_size
+
+
+def moe_align_block_size(topk_ids, block_size, num_experts):
+    """topk_ids: nested list / array of expert ids, any shape (flattened
+    row-major).  Returns (sorted_token_ids, expert_ids, num_tokens_post_padded,
+    group_sizes) as Python lists / int."""
+    flat = [int(v) for v in _flatten(topk_ids)]
+    numel = len(flat)
+    cap, max_blocks = buffer_sizes(numel, num_experts, block_size)
+    per_expert = [[] for _ in range(num_experts)]
+    for i, e in enumerate(flat):
+        if 0 <= e < num_experts:
+            per_expert[e].append(i)
+    sorted_ids = []
+    expert_ids = []
+    group_sizes = []
+    for e in range(num_experts):
+        ids = per_expert[e]
+        padded = -(-len(ids) // block_size) * block_size
+        sorted_ids += ids + [numel] * (padded - len(ids))
+        expert_ids += [e] * (padded // block_size)
+        group_sizes.append(padded)
+    total = len(sorted_ids)
+    sorted_ids += [numel] * (cap - total)
+    expert_ids += [-1] * (max_blocks - len(expert_ids))
+    return sorted_ids, expert_ids, total, group_sizes
+
+
+def _flatten(x):
+    if hasattr(x, "tolist"):
+        x = x.tolist()
+    if isinstance(x, (list, tuple)):
+        out = []
+        for v in x:
+            out += _flatten(v)
+        return out
+    return [x]

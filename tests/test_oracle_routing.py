@@ -1,0 +1,105 @@
+"""Pins for oracle.routing.moe_align_block_size.
+
+* The worked example printed in the docstring of moe_align_block_size
+  (pytorch-labs/applied-ai issue 24, column-major fused MoE script), stored in
+  tests/golden/moe_align_example.json.
+* An independent construction: numpy's stable argsort of the flat expert ids
+  gives the same within-expert order, then padding by arithmetic; compared on
+  random inputs and exhaustively on tiny ones.
+* Invariants the docstring fixes: every entry placed once, blocks of one
+  expert each, padded total divisible by block_size, pad id = numel."""
+
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle.routing import buffer_sizes, moe_align_block_size
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "moe_align_example.json")
+
+
+def test_worked_example():
+    g = json.load(open(GOLDEN))
+    flat = [v for row in g["topk_ids"] for v in row]
+    assert flat == g["flattened"]
+    sid, eid, total, gs = moe_align_block_size(g["topk_ids"], g["block_size"], g["num_experts"])
+    n = len(flat)
+    assert n == g["padding_id"]
+    assert total == g["num_tokens_post_padded"]
+    assert sid[:total] == g["sorted_token_ids_prefix"]
+    cap, max_blocks = buffer_sizes(n, g["num_experts"], g["block_size"])
+    assert len(sid) == cap and all(v == n for v in sid[total:])
+    assert eid[: total // g["block_size"]] == [1, 2, 3, 4]
+    assert len(eid) == max_blocks and all(v == -1 for v in eid[total // g["block_size"]:])
+    assert gs == [0, 4, 4, 4, 4]
+
+
+def by_argsort(flat, block, E):
+    """Same result from numpy's stable argsort (invalid ids sort last and are dropped)."""
+    flat = np.asarray(flat, dtype=np.int64).ravel()
+    n = flat.size
+    valid = (flat >= 0) & (flat < E)
+    key = np.where(valid, flat, E)
+    order = np.argsort(key, kind="stable")
+    sid, eid, gs = [], [], []
+    for e in range(E):
+        ids = order[key[order] == e].tolist()
+        p = (len(ids) + block - 1) // block * block
+        sid += ids + [n] * (p - len(ids))
+        eid += [e] * (p // block)
+        gs.append(p)
+    return sid, eid, gs
+
+
+def check(flat, block, E):
+    sid, eid, total, gs = moe_align_block_size(flat, block, E)
+    s2, e2, g2 = by_argsort(flat, block, E)
+    assert sid[:total] == s2 and eid[: total // block] == e2 and gs == g2
+    n = len(np.asarray(flat).ravel())
+    flat_l = np.asarray(flat).ravel().tolist()
+    # invariants
+    assert total % block == 0 and total == sum(gs)
+    placed = [v for v in sid[:total] if v != n]
+    assert sorted(placed) == [i for i, v in enumerate(flat_l) if 0 <= v < E]
+    for b in range(total // block):
+        blk = sid[b * block:(b + 1) * block]
+        real = [v for v in blk if v != n]
+        assert real == sorted(real)
+        assert all(flat_l[v] == eid[b] for v in real)
+        assert blk == real + [n] * (block - len(real))  # padding only at an expert's end
+    assert eid[: total // block] == sorted(eid[: total // block])
+
+
+@pytest.mark.parametrize("T,k,E,block,seed", [
+    (64, 2, 8, 16, 0), (100, 6, 64, 128, 1), (7, 3, 5, 4, 2), (1, 1, 128, 128, 3), (333, 4, 16, 1, 4),
+    (50, 2, 1024, 8, 5),
+])
+def test_random_against_argsort(T, k, E, block, seed):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, E, size=(T, k))
+    check(ids, block, E)
+
+
+def test_invalid_ids_are_not_placed():
+    ids = [[0, 5, -1], [2, 2, 9], [4, 0, 1]]
+    check(ids, 2, 5)
+    sid, eid, total, gs = moe_align_block_size(ids, 2, 5)
+    # entries 1, 2 and 5 carry the out-of-range ids 5, -1 and 9
+    assert all(i not in sid[:total] for i in (1, 2, 5))
+    assert gs == [2, 2, 2, 0, 2]
+
+
+def test_no_entries():
+    sid, eid, total, gs = moe_align_block_size([], 4, 3)
+    assert total == 0 and sid == [0] * 9 and eid == [-1] * 2 and gs == [0, 0, 0]
+
+
+def test_exhaustive_tiny():
+    for E in (1, 2, 3):
+        for n in range(0, 5):
+            for flat in itertools.product(range(-1, E + 1), repeat=n):
+                for block in (1, 2, 3):
+                    check(list(flat), block, E)
