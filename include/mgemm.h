@@ -14,6 +14,9 @@
  *   [FP8]  "[moe training] Optimize FP8 MoE backward pass: fused colwise
  *          kernel + AMD tuning" (pytorch/ao commit 34322b5): commit message and
  *          bench_colwise_block_configs.py (_colwise_kernel, run_experiment).
+ *   [CMM]  pytorch-labs/applied-ai issue 24, the column-major fused MoE script
+ *          (built on vLLM's fused_moe.py): moe_align_block_size (docstring and
+ *          worked example), fused_moe_kernel, fused_moe.
  *
  * Conventions (all entry points):
  *   - Every pointer argument is a DEVICE pointer owned by the caller; the
@@ -222,7 +225,7 @@ int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, con
  * synchronize the device, or runtimes that only provide a fixed workspace
  * chosen in advance.  Instead of a caller-provided args block it uses one held
  * in a static device array of this library, sized for MGEMM_NOALLOC_MAX_EXPERTS
- * experts (about 20 KB, kept on every GPU that loads the library until exit).
+ * experts (about 33 KB, kept on every GPU that loads the library until exit).
  *   group_sizes  int64[E], device (as for mgemm_fill_args)
  *   the other arguments are those of mgemm_fwd.
  * Runs mgemm_fill_args into the static array, then mgemm_fwd.  Allocates
@@ -236,6 +239,37 @@ int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, con
 #define MGEMM_NOALLOC_MAX_EXPERTS 1024
 int mgemm_fwd_noalloc(const int64_t *group_sizes, int E, int dtype, int trans_b, const void *x, const float *sx,
                       const void *w, const float *sw, void *out, int64_t M, int K, int N, mgemm_stream_t stream);
+
+/*
+ * mgemm_moe_align -- moe_align_block_size on the device [CMM]: the flat
+ * (token, slot) entries of topk_ids are grouped by expert, each expert's list
+ * padded up to a multiple of block_size, so that every block of the sorted list
+ * belongs to one expert.
+ *   topk_ids      int32 [numel]: expert of flat entry i (token i / top_k when
+ *                 topk_ids is [T, top_k] row-major).  Entries outside [0, E)
+ *                 are not placed.
+ *   sorted_ids    int32 [numel + E * (block_size - 1)]: expert by expert in
+ *                 ascending id, the expert's flat indices in ascending order,
+ *                 then the pad id numel up to the expert's padded count; every
+ *                 position from num_post_padded to the end also holds numel.
+ *   expert_ids    int32 [(numel + E * (block_size - 1)) / block_size]: the
+ *                 expert of each block of block_size positions; -1 past the
+ *                 last block.
+ *   num_post_padded  int32 [1]: the padded total (a multiple of block_size).
+ *   group_sizes   int64 [E] or NULL: each expert's padded count (the group
+ *                 sizes for mgemm_fill_args over the sorted, padded rows).
+ *   workspace     mgemm_moe_align_workspace_bytes(numel, E) bytes, 16-byte
+ *                 aligned, scratch for the duration of the call's kernels.
+ * Limits: 1 <= E <= MGEMM_MAX_EXPERTS, 1 <= block_size <= 4096,
+ * numel + E * (block_size - 1) < 2^31.  The result is unique (stable order), so
+ * it is bit-for-bit reproducible.  Three kernels: per-chunk counts, one CTA
+ * that turns them into positions and writes the padding and block experts,
+ * and the stable placement.
+ */
+int64_t mgemm_moe_align_workspace_bytes(int64_t numel, int E);
+int mgemm_moe_align(const int32_t *topk_ids, int64_t numel, int E, int block_size, int32_t *sorted_ids,
+                    int32_t *expert_ids, int32_t *num_post_padded, int64_t *group_sizes, void *workspace,
+                    mgemm_stream_t stream);
 
 /* Number of SMs of the current device (the persistent GEMM grid size), or < 0 on error. */
 int mgemm_num_sms(void);

@@ -56,6 +56,10 @@ _SIGS = {
     "mgemm_fwd_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "mgemm_moe_align_workspace_bytes": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int]),
+    "mgemm_moe_align": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p]),
     "mgemm_num_sms": (ctypes.c_int, []),
     "mgemm_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mgemm_version": (ctypes.c_int, []),
@@ -166,6 +170,25 @@ def mgemm_fwd_noalloc(group_sizes, dtype, trans_b, x, sx, w, sw, out, M, K, N, E
     _cuda(group_sizes, x, sx, w, sw, out)
     _check(lib().mgemm_fwd_noalloc(_p(group_sizes), int(E), int(dtype), int(trans_b), _p(x), _p(sx), _p(w), _p(sw),
                                    _p(out), int(M), int(K), int(N), _stream(out)), "mgemm_fwd_noalloc")
+
+
+def mgemm_moe_align_workspace_bytes(numel, E):
+    return int(lib().mgemm_moe_align_workspace_bytes(int(numel), int(E)))
+
+
+def moe_align_buffer_sizes(numel, E, block_size):
+    """(entries of sorted_ids, entries of expert_ids) for mgemm_moe_align."""
+    cap = int(numel) + int(E) * (int(block_size) - 1)
+    return cap, cap // int(block_size)
+
+
+def mgemm_moe_align(topk_ids, E, block_size, sorted_ids, expert_ids, num_post_padded, workspace, group_sizes=None):
+    """moe_align_block_size on the device: topk_ids int32 (any shape, flattened
+    row-major); outputs as laid out in mgemm.h."""
+    _cuda(topk_ids, sorted_ids, expert_ids, num_post_padded, workspace, group_sizes)
+    _check(lib().mgemm_moe_align(_p(topk_ids), int(topk_ids.numel()), int(E), int(block_size), _p(sorted_ids),
+                                 _p(expert_ids), _p(num_post_padded), _p(group_sizes), _p(workspace),
+                                 _stream(sorted_ids)), "mgemm_moe_align")
 
 
 def mgemm_num_sms():

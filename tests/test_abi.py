@@ -102,6 +102,23 @@ def test_host_checks_quant(lib):
     assert lib.mgemm_quant_colwise_grouped(i, 4, 64, i, 64, o, s, None, 0, None, None, 648, None) == -2  # ld % 16
 
 
+def test_host_checks_moe_align(lib):
+    # rejected on the host before any CUDA call, so these run without a GPU
+    p = ctypes.c_void_p(0x10000)
+    f = lib.mgemm_moe_align
+    assert f(p, 12, 0, 4, p, p, p, None, p, None) == -1          # E < 1
+    assert f(p, 12, 1025, 4, p, p, p, None, p, None) == -3       # E > MGEMM_MAX_EXPERTS
+    assert f(p, 12, 4, 0, p, p, p, None, p, None) == -1          # block_size < 1
+    assert f(p, -1, 4, 4, p, p, p, None, p, None) == -1          # numel < 0
+    assert f(p, (1 << 31) - 10, 4, 4, p, p, p, None, p, None) == -1  # numel + E (block - 1) >= 2^31
+    assert f(None, 12, 4, 4, p, p, p, None, p, None) == -1       # no topk_ids
+    assert f(p, 12, 4, 4, None, p, p, None, p, None) == -1       # no sorted_ids
+    assert f(p, 12, 4, 4, p, p, p, None, ctypes.c_void_p(0x10008), None) == -2  # workspace not 16-aligned
+    assert f(p, 12, 4, 4, p, p, p, ctypes.c_void_p(0x10004), p, None) == -2      # group_sizes not 8-aligned
+    ws = lib.mgemm_moe_align_workspace_bytes
+    assert ws(0, 4) == 16 and ws(2048, 4) == 16 and ws(2049, 64) == 2 * 64 * 4 and ws(10, 0) == -1
+
+
 def test_colwise_ld_bounds_the_padded_layout():
     # M rows in at most min(M, E) non-empty groups, each padded by fewer than
     # MGEMM_COL_PAD rows, rounded up to MGEMM_COL_PAD
