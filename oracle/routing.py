@@ -73,3 +73,54 @@ def _flatten(x):
             out += _flatten(v)
         return out
     return [x]
+
+
+def fused_moe_gemm(A, B, sorted_ids, expert_ids, num_post, numel, top_k, block_size, topk_weights=None):
+    """One launch of fused_moe_kernel, in float64: for every position s below
+    num_post whose id = sorted_ids[s] is a real entry (id < numel), row id of
+    the output is A[id // top_k] . B[e]^T with e = expert_ids[s // block_size],
+    times topk_weights[id] when weights are given (MUL_ROUTED_WEIGHT).
+    A [rows, K], B [E, N, K] (the kernel's b_ptr strides: expert, n, k).
+    Returns [numel, N] with NaN in rows no position writes."""
+    import numpy as np
+
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    N = B.shape[1]
+    out = np.full((numel, N), np.nan)
+    for s in range(int(num_post)):
+        i = int(sorted_ids[s])
+        if i >= numel:
+            continue  # padding: masked loads and stores
+        e = int(expert_ids[s // block_size])
+        row = A[i // top_k] @ B[e].T
+        if topk_weights is not None:
+            row = row * float(topk_weights[i])
+        out[i] = row
+    return out
+
+
+def silu_and_mul(x):
+    """vLLM's silu_and_mul as fused_moe uses it: for [rows, 2F] input,
+    silu(x[:, :F]) * x[:, F:] with silu(v) = v / (1 + exp(-v)), in float64."""
+    import numpy as np
+
+    x = np.asarray(x, dtype=np.float64)
+    F = x.shape[1] // 2
+    g, u = x[:, :F], x[:, F:]
+    return g / (1.0 + np.exp(-g)) * u
+
+
+def gather_rows(src, sorted_ids, num_post, numel, top_k):
+    """Row s of the result is src[sorted_ids[s] // top_k] for the real entries
+    below num_post, zero for padding (the rows fused_moe_kernel's masked loads
+    see)."""
+    import numpy as np
+
+    src = np.asarray(src)
+    out = np.zeros((int(num_post), src.shape[1]), dtype=np.float64)
+    for s in range(int(num_post)):
+        i = int(sorted_ids[s])
+        if i < numel:
+            out[s] = src[i // top_k]
+    return out

@@ -103,3 +103,61 @@ def test_exhaustive_tiny():
             for flat in itertools.product(range(-1, E + 1), repeat=n):
                 for block in (1, 2, 3):
                     check(list(flat), block, E)
+
+
+def test_fused_moe_gemm_hand_example():
+    # tokens 0..2 with top-2 experts [[0,1],[1,2],[0,2]], block 2: worked by hand
+    from oracle.routing import fused_moe_gemm
+    sid, eid, tot, _ = moe_align_block_size([[0, 1], [1, 2], [0, 2]], 2, 3)
+    A = np.arange(6, dtype=float).reshape(3, 2)
+    Bw = np.arange(24, dtype=float).reshape(3, 4, 2)
+    out = fused_moe_gemm(A, Bw, sid, eid, tot, 6, 2, 2)
+    assert out[0].tolist() == [1, 3, 5, 7]          # token 0 . expert 0
+    assert out[4].tolist() == [5, 23, 41, 59]       # token 2 . expert 0
+    assert out[5].tolist() == [149, 167, 185, 203]  # token 2 . expert 2
+    w = np.array([0.5, 2, 1, 1, 1, 4])
+    outw = fused_moe_gemm(A, Bw, sid, eid, tot, 6, 2, 2, topk_weights=w)
+    assert np.array_equal(outw, out * w[:, None])
+
+
+def test_fused_moe_gemm_against_einsum():
+    # every entry against a dense per-entry matmul (numpy einsum), padding and
+    # out-of-range ids leave NaN rows
+    from oracle.routing import fused_moe_gemm
+    rng = np.random.default_rng(7)
+    T, k, E, K, N, block = 50, 3, 6, 16, 12, 8
+    ids = rng.integers(-1, E, size=(T, k))
+    sid, eid, tot, _ = moe_align_block_size(ids, block, E)
+    A = rng.standard_normal((T, K))
+    Bw = rng.standard_normal((E, N, K))
+    wts = rng.random(T * k)
+    out = fused_moe_gemm(A, Bw, sid, eid, tot, T * k, k, block, topk_weights=wts)
+    flat = ids.ravel()
+    for i in range(T * k):
+        if 0 <= flat[i] < E:
+            ref = np.einsum("k,nk->n", A[i // k], Bw[flat[i]]) * wts[i]
+            assert np.allclose(out[i], ref, rtol=1e-13, atol=1e-12)
+        else:
+            assert np.isnan(out[i]).all()
+
+
+def test_silu_and_mul_closed_forms():
+    from scipy.special import expit
+
+    from oracle.routing import silu_and_mul
+    x = np.array([[0.0, 1.0, 3.0, -2.0], [50.0, -50.0, 1.0, 1.0]])
+    h = silu_and_mul(x)
+    assert h.shape == (2, 2)
+    assert h[0, 0] == 0.0                                   # silu(0) = 0
+    assert np.isclose(h[0, 1], 1.0 * expit(1.0) * -2.0)    # silu(v) = v * sigmoid(v)
+    assert np.isclose(h[1, 0], 50.0, rtol=1e-15)            # silu(v) -> v for large v
+    assert abs(h[1, 1]) < 1e-19                             # silu(v) -> 0 for very negative v
+
+
+def test_gather_rows_pads_with_zeros():
+    from oracle.routing import gather_rows
+    sid, eid, tot, _ = moe_align_block_size([[1, 0], [0, 0]], 4, 2)
+    src = np.array([[1.0, 2.0], [3.0, 4.0]])
+    g = gather_rows(src, sid, tot, 4, 2)
+    # expert 0: entries 1, 2, 3 (tokens 0, 1, 1) + 1 pad; expert 1: entry 0 (token 0) + 3 pads
+    assert g.tolist() == [[1, 2], [3, 4], [3, 4], [0, 0], [1, 2], [0, 0], [0, 0], [0, 0]]
