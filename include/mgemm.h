@@ -111,7 +111,10 @@ int mgemm_args_layout(int E, size_t *off_offsets, size_t *off_active, size_t *of
  * the min(total_M, groups) non-empty groups are scheduled (active, mtile_start).
  *   group_sizes  int64[E], device; group_sizes[e] rows belong to expert e
  *   E            number of experts, 1..MGEMM_MAX_EXPERTS
- *   M            total rows the caller expects (checked on the device)
+ *   M            total rows the caller expects (checked on the device), or -1:
+ *                the rows are the sum of the sizes, which only the device
+ *                knows (sizes written by another kernel, e.g. the padded
+ *                group sizes of mgemm_moe_align); status 2 if it reaches 2^31
  *   args         device buffer of mgemm_args_bytes(E) bytes (output)
  * One launch of one CTA.  Invalid sizes set status 1 or 2 (the other fields
  * are then unspecified).
@@ -270,6 +273,67 @@ int64_t mgemm_moe_align_workspace_bytes(int64_t numel, int E);
 int mgemm_moe_align(const int32_t *topk_ids, int64_t numel, int E, int block_size, int32_t *sorted_ids,
                     int32_t *expert_ids, int32_t *num_post_padded, int64_t *group_sizes, void *workspace,
                     mgemm_stream_t stream);
+
+/*
+ * The routed (fused_moe) layer [CMM], built from mgemm_moe_align and these
+ * calls: x rows are gathered into expert order, the grouped GEMM runs over the
+ * sorted rows, and its epilogue scatters each row to its flat (token, slot)
+ * entry, optionally times the routed weight -- the work of fused_moe_kernel,
+ * whose masked loads read padding entries as zero rows and whose masked stores
+ * skip them; then silu_and_mul, the second GEMM with MUL_ROUTED_WEIGHT, and the
+ * sum over the top_k slots of each token.
+ *
+ * mgemm_gather_rows -- dst row s = src row sorted_ids[s] / top_k for every s
+ * below min(*num_post_padded, dst_rows); zeros when sorted_ids[s] >= numel (a
+ * padding entry) or names a row outside src.  Rows from *num_post_padded on
+ * are not written.
+ *   src  [src_rows] rows of row_bytes bytes, src_ld_bytes apart
+ *   dst  [dst_rows] rows, dst_ld_bytes apart (row_bytes and both strides
+ *        multiples of 16; src and dst 16-byte aligned)
+ *   sorted_ids, num_post_padded, numel: as from mgemm_moe_align
+ */
+int mgemm_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes, int64_t src_ld_bytes,
+                      const int32_t *sorted_ids, const int32_t *num_post_padded, int64_t numel, int top_k,
+                      void *dst, int64_t dst_rows, int64_t dst_ld_bytes, mgemm_stream_t stream);
+
+/*
+ * mgemm_fwd_scatter -- mgemm_fwd over rows sorted by expert, with each output
+ * row stored at the row row_map names (fused_moe_kernel's c_ptrs), optionally
+ * multiplied by its routed weight (MUL_ROUTED_WEIGHT: the fp32 accumulator row
+ * times the weight, then one rounding to bf16).
+ *   args        args block of the sorted rows: mgemm_fill_args over the padded
+ *               group sizes of mgemm_moe_align, with M = -1
+ *   x           bf16 [M, K]: the sorted rows (mgemm_gather_rows); M >= the
+ *               padded total (e.g. the sorted_ids capacity)
+ *   w           bf16 [E, N, K] (trans_b = 1, the layout of fused_moe) or [E, K, N]
+ *   out         bf16 [map_limit, N]
+ *   row_map     int32 [M]: output row of sorted row i (sorted_ids: flat entry
+ *               ids); a row with row_map[i] < 0 or >= map_limit (padding) is
+ *               not stored
+ *   map_limit   rows of out (numel of topk_ids)
+ *   row_weight  float32 [map_limit] or NULL
+ * bf16 only (fp8 returns MGEMM_ENOTSUP).  Output rows no sorted row names are
+ * left as they were.
+ */
+int mgemm_fwd_scatter(const void *args, int dtype, int trans_b, const void *x, const void *w, void *out,
+                      const int32_t *row_map, int64_t map_limit, const float *row_weight, int64_t M, int K, int N,
+                      int E, mgemm_stream_t stream);
+
+/*
+ * mgemm_silu_and_mul -- out[r, j] = silu(in[r, j]) * in[r, F + j] for in bf16
+ * [R, 2F] and out bf16 [R, F] (vLLM's silu_and_mul as fused_moe applies it to
+ * the first GEMM's output), silu(v) = v / (1 + exp(-v)), computed in fp32 and
+ * rounded to bf16 once.  F % 8 == 0; pointers 16-byte aligned.
+ */
+int mgemm_silu_and_mul(const void *in, int64_t R, int64_t F, void *out, mgemm_stream_t stream);
+
+/*
+ * mgemm_topk_sum -- out[t, :] = sum_j in[t * top_k + j, :] for in bf16
+ * [T * top_k, H] and out bf16 [T, H] (fused_moe's final sum over the top_k
+ * slots), accumulated in fp32 in ascending j and rounded to bf16 once.
+ * H % 8 == 0; pointers 16-byte aligned.
+ */
+int mgemm_topk_sum(const void *in, int64_t T, int top_k, int64_t H, void *out, mgemm_stream_t stream);
 
 /* Number of SMs of the current device (the persistent GEMM grid size), or < 0 on error. */
 int mgemm_num_sms(void);

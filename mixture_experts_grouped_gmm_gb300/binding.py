@@ -60,6 +60,17 @@ _SIGS = {
     "mgemm_moe_align": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p]),
+    "mgemm_gather_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
+    "mgemm_fwd_scatter": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p]),
+    "mgemm_silu_and_mul": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                          ctypes.c_void_p]),
+    "mgemm_topk_sum": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_void_p]),
     "mgemm_num_sms": (ctypes.c_int, []),
     "mgemm_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mgemm_version": (ctypes.c_int, []),
@@ -189,6 +200,34 @@ def mgemm_moe_align(topk_ids, E, block_size, sorted_ids, expert_ids, num_post_pa
     _check(lib().mgemm_moe_align(_p(topk_ids), int(topk_ids.numel()), int(E), int(block_size), _p(sorted_ids),
                                  _p(expert_ids), _p(num_post_padded), _p(group_sizes), _p(workspace),
                                  _stream(sorted_ids)), "mgemm_moe_align")
+
+
+def mgemm_gather_rows(src, sorted_ids, num_post_padded, numel, top_k, dst):
+    """dst row s = src row sorted_ids[s] // top_k (zeros for padding entries), s < *num_post_padded."""
+    _cuda(src, sorted_ids, num_post_padded, dst)
+    rb = src.shape[1] * src.element_size()
+    _check(lib().mgemm_gather_rows(_p(src), src.shape[0], rb, src.stride(0) * src.element_size(), _p(sorted_ids),
+                                   _p(num_post_padded), int(numel), int(top_k), _p(dst), dst.shape[0],
+                                   dst.stride(0) * dst.element_size(), _stream(dst)), "mgemm_gather_rows")
+
+
+def mgemm_fwd_scatter(args, dtype, trans_b, x, w, out, row_map, map_limit, row_weight, M, K, N, E):
+    _cuda(args, x, w, out, row_map, row_weight)
+    _check(lib().mgemm_fwd_scatter(_p(args), int(dtype), int(trans_b), _p(x), _p(w), _p(out), _p(row_map),
+                                   int(map_limit), _p(row_weight), int(M), int(K), int(N), int(E), _stream(out)),
+           "mgemm_fwd_scatter")
+
+
+def mgemm_silu_and_mul(inp, out):
+    _cuda(inp, out)
+    R, F2 = inp.shape
+    _check(lib().mgemm_silu_and_mul(_p(inp), R, F2 // 2, _p(out), _stream(out)), "mgemm_silu_and_mul")
+
+
+def mgemm_topk_sum(inp, T, top_k, out):
+    _cuda(inp, out)
+    _check(lib().mgemm_topk_sum(_p(inp), int(T), int(top_k), inp.shape[-1], _p(out), _stream(out)),
+           "mgemm_topk_sum")
 
 
 def mgemm_num_sms():

@@ -109,16 +109,18 @@ __global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict
   }
   if (t == 0) {
     int st = MGEMM_STATUS_OK;
+    // M = -1: the rows are whatever the sizes add up to (below 2^31)
+    const bool check = M >= 0;
     if (any_neg)
       st = MGEMM_STATUS_NEGATIVE_SIZE;
-    else if (total_sh != M)
+    else if (check ? total_sh != M : total_sh >= (int64_t(1) << 31))
       st = MGEMM_STATUS_SUM_MISMATCH;
     int *hdr = (int *)args;
     hdr[0] = st;
     hdr[1] = n_active_sh;
     hdr[2] = E;
     hdr[3] = 0;  // work counter of the colwise quantizer
-    *(int64_t *)(args + 16) = M;
+    *(int64_t *)(args + 16) = check ? M : total_sh;
   }
 }
 
@@ -220,7 +222,7 @@ extern "C" int mgemm_fill_args(const int64_t *group_sizes, int E, int64_t M, voi
   if (!group_sizes || !args) return MGEMM_EINVAL;
   if (E < 1) return MGEMM_EINVAL;
   if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
-  if (M < 0 || M >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  if (M < -1 || M >= (int64_t(1) << 31)) return MGEMM_EINVAL;
   if (((uintptr_t)args & 15) || ((uintptr_t)group_sizes & 7)) return MGEMM_EALIGN;
   cudaStream_t s = (cudaStream_t)stream;
   if (E <= 32)

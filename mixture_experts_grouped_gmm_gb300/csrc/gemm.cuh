@@ -136,6 +136,13 @@ struct GemmParams {
   __nv_bfloat16 *out;
   const float *rscale;  // FP8: per output row (indexed by out_row0 + r)
   const float *cscale;  // FP8: per (expert, column): cscale[e * Nout + col]
+  // bf16 rows mode, scattered output (routed layers): row i of the row-sorted
+  // result goes to output row row_map[i] when 0 <= row_map[i] < map_limit and
+  // nowhere otherwise; with row_weight, the fp32 accumulator row is first
+  // multiplied by row_weight[row_map[i]] (one rounding to bf16 after it)
+  const int32_t *row_map;
+  int64_t map_limit;
+  const float *row_weight;
 };
 
 struct TileInfo {
@@ -585,9 +592,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int t = t_first; t < total; t += t_step) {
       const TileInfo ti = decode_tile<C>(t, p, av, rank);
       const bool has_acc = ti.kb_count > 0;
-      const bool row_ok = r < ti.out_rows;
-      const bool warp_full = q * 32 + 32 <= ti.out_rows;
-      __nv_bfloat16 *orow = p.out + (int64_t)(ti.out_row0 + r) * p.Nout;
+      bool row_ok = r < ti.out_rows;
+      bool warp_full = q * 32 + 32 <= ti.out_rows;
+      int64_t out_row = (int64_t)ti.out_row0 + r;
+      float wgt = 1.f;
+      if constexpr (C::Mode == kModeRows && !C::Fp8) {
+        if (p.row_map) {  // scattered rows: plain per-row stores
+          const int32_t d = row_ok ? __ldg(p.row_map + ti.out_row0 + r) : -1;
+          row_ok = d >= 0 && d < p.map_limit;
+          out_row = row_ok ? d : 0;
+          warp_full = false;
+          if (row_ok && p.row_weight) wgt = __ldg(p.row_weight + d);
+        }
+      }
+      __nv_bfloat16 *orow = p.out + out_row * p.Nout;
       float rinv = 1.f, csr[2 * kCpw];
       if constexpr (C::Fp8) {
         rinv = rinv_next;
@@ -666,6 +684,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                   pack_bf16x2_u64(mul_f32x2(mul_f32x2(f32x2(vb[cur][4 * j + 2], vb[cur][4 * j + 3]), r2), f32x2(c1.z, c1.w)));
             }
             __syncwarp();
+          } else if (C::Mode == kModeRows && p.row_weight) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              pk[j] = pack_bf16x2(__uint_as_float(va[cur][2 * j]) * wgt, __uint_as_float(va[cur][2 * j + 1]) * wgt);
+              pk[16 + j] =
+                  pack_bf16x2(__uint_as_float(vb[cur][2 * j]) * wgt, __uint_as_float(vb[cur][2 * j + 1]) * wgt);
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {

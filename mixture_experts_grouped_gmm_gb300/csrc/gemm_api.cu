@@ -114,8 +114,10 @@ bool make_out_map(CUtensorMap *m, void *out, int64_t rows, int64_t cols) {
 
 }  // namespace
 
-extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
-                         const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
+// mgemm_fwd, and mgemm_fwd_scatter when row_map is given (bf16 only)
+static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
+                    const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream,
+                    const int32_t *row_map, int64_t map_limit, const float *row_weight) {
   int rc = common_checks(args, dtype, M, K, N, E);
   if (rc) return rc;
   if (!x || !w || !out) return MGEMM_EINVAL;
@@ -170,13 +172,16 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
     }
     b_one_box = one;
   }
-  CUtensorMap to;
-  if (!make_out_map(&to, out, M, N)) return MGEMM_ECUDA;
+  CUtensorMap to;  // (scattered rows are stored row by row; the map then goes unused)
+  if (!make_out_map(&to, out, row_map ? (map_limit > 0 ? map_limit : 1) : M, N)) return MGEMM_ECUDA;
   GemmParams p{};
   p.args = (const uint8_t *)args;
   p.E = E;
   p.bn = bn;
   p.b_one_box = b_one_box ? 1 : 0;
+  p.row_map = row_map;
+  p.map_limit = map_limit;
+  p.row_weight = row_weight;
   p.idesc = make_idesc(fp8 ? 0u : 1u, false, !trans_b, pair ? 256 : 128, bn);
   p.a_rows = (int)a_rows;
   p.n_tiles = (N + bn - 1) / bn;
@@ -215,6 +220,22 @@ extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x
   if (bn == 192 && b_one_box) return gemm_bf16_rows_bmn_w192(ta, tb, to, p, grid, s);
   if (fp8) return gemm_fp8_rows(ta, tb, to, p, grid, s);
   return trans_b ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, to, p, grid, s);
+}
+
+extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
+                         const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
+  return fwd_impl(args, dtype, trans_b, x, sx, w, sw, out, M, K, N, E, stream, nullptr, 0, nullptr);
+}
+
+extern "C" int mgemm_fwd_scatter(const void *args, int dtype, int trans_b, const void *x, const void *w, void *out,
+                                 const int32_t *row_map, int64_t map_limit, const float *row_weight, int64_t M,
+                                 int K, int N, int E, mgemm_stream_t stream) {
+  if (dtype != MGEMM_BF16 && dtype != MGEMM_FP8_E4M3) return MGEMM_EINVAL;
+  if (dtype != MGEMM_BF16) return MGEMM_ENOTSUP;
+  if (!row_map || map_limit < 0 || map_limit >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  if (((uintptr_t)row_map & 3) || ((uintptr_t)row_weight & 3)) return MGEMM_EALIGN;
+  return fwd_impl(args, dtype, trans_b, x, nullptr, w, nullptr, out, M, K, N, E, stream, row_map, map_limit,
+                  row_weight);
 }
 
 extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,

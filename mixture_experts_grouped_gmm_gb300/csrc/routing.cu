@@ -138,9 +138,127 @@ __global__ void __launch_bounds__(kAlignThreads) moe_align_place_kernel(const in
   }
 }
 
+// Row s of dst (s below the padded total and dst_rows) is row ids[s] / top_k of
+// src, or zeros for a padding entry (ids[s] >= numel) -- the rows the masked
+// loads of fused_moe_kernel see.  One warp per row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restrict__ src, int64_t src_rows,
+                                                            int64_t row_chunks, int64_t src_ld, int64_t dst_ld,
+                                                            const int32_t *__restrict__ ids,
+                                                            const int32_t *__restrict__ num_post, int64_t numel,
+                                                            int top_k, uint4 *__restrict__ dst, int64_t dst_rows) {
+  const int64_t total = *num_post;
+  const int64_t rows = total < dst_rows ? total : dst_rows;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t s = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < rows; s += nwarps) {
+    const int32_t id = __ldg(ids + s);
+    const int64_t r = id >= 0 && id < numel ? id / top_k : -1;
+    const bool ok = r >= 0 && r < src_rows;
+    const uint4 *sp = src + (ok ? r : 0) * src_ld;
+    uint4 *dp = dst + s * dst_ld;
+#pragma unroll 4
+    for (int64_t c = lane; c < row_chunks; c += 32) dp[c] = ok ? __ldg(sp + c) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// out[r, j] = silu(in[r, j]) * in[r, F + j], silu(v) = v / (1 + exp(-v)),
+// in fp32 from the bf16 inputs, rounded to bf16 once; 8 columns per thread.
+__global__ void __launch_bounds__(256) silu_mul_kernel(const uint4 *__restrict__ in, int64_t R, int64_t F8,
+                                                         uint4 *__restrict__ out) {
+  const int64_t n = R * F8;
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n; c += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = c / F8, j = c - row * F8;
+    const uint4 g = __ldg(in + row * 2 * F8 + j), u = __ldg(in + row * 2 * F8 + F8 + j);
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float g0 = __uint_as_float(gw[k] << 16), g1 = __uint_as_float(gw[k] & 0xFFFF0000u);
+      const float u0 = __uint_as_float(uw[k] << 16), u1 = __uint_as_float(uw[k] & 0xFFFF0000u);
+      const float h0 = g0 / (1.f + expf(-g0)) * u0, h1 = g1 / (1.f + expf(-g1)) * u1;
+      __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+      o[k] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// out[t, :] = sum over j < top_k of in[t * top_k + j, :], in fp32 (ascending j),
+// rounded to bf16 once; 8 columns per thread.
+__global__ void __launch_bounds__(256) topk_sum_kernel(const uint4 *__restrict__ in, int64_t T, int top_k,
+                                                         int64_t H8, uint4 *__restrict__ out) {
+  const int64_t n = T * H8;
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n; c += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = c / H8, j = c - t * H8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < top_k; ++k) {
+      const uint4 v = __ldg(in + (t * top_k + k) * H8 + j);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += __uint_as_float(w[q] << 16);
+        acc[2 * q + 1] += __uint_as_float(w[q] & 0xFFFF0000u);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      o[q] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 }  // namespace mgemm
 
 using namespace mgemm;
+
+extern "C" int mgemm_topk_sum(const void *in, int64_t T, int top_k, int64_t H, void *out, mgemm_stream_t stream) {
+  if (!in || !out || T < 0 || top_k < 1 || H < 0) return MGEMM_EINVAL;
+  if (H % 8 || ((uintptr_t)in & 15) || ((uintptr_t)out & 15)) return MGEMM_EALIGN;
+  if (T == 0 || H == 0) return MGEMM_OK;
+  int sms = sm_count_cached();
+  if (sms <= 0) return MGEMM_ECUDA;
+  const int64_t n = T * (H / 8);
+  const int64_t want = (n + 255) / 256;
+  const int blocks = (int)(want < (int64_t)sms * 32 ? want : (int64_t)sms * 32);
+  topk_sum_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>((const uint4 *)in, T, top_k, H / 8, (uint4 *)out);
+  return cuda_rc(cudaGetLastError(), "mgemm_topk_sum launch");
+}
+
+extern "C" int mgemm_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes, int64_t src_ld_bytes,
+                                 const int32_t *sorted_ids, const int32_t *num_post_padded, int64_t numel, int top_k,
+                                 void *dst, int64_t dst_rows, int64_t dst_ld_bytes, mgemm_stream_t stream) {
+  if (!src || !sorted_ids || !num_post_padded || !dst) return MGEMM_EINVAL;
+  if (src_rows < 0 || dst_rows < 0 || numel < 0 || top_k < 1 || row_bytes <= 0) return MGEMM_EINVAL;
+  if (src_ld_bytes < row_bytes || dst_ld_bytes < row_bytes) return MGEMM_EINVAL;
+  if (row_bytes % 16 || src_ld_bytes % 16 || dst_ld_bytes % 16 || ((uintptr_t)src & 15) || ((uintptr_t)dst & 15) ||
+      ((uintptr_t)sorted_ids & 3) || ((uintptr_t)num_post_padded & 3))
+    return MGEMM_EALIGN;
+  if (dst_rows == 0) return MGEMM_OK;
+  int sms = sm_count_cached();
+  if (sms <= 0) return MGEMM_ECUDA;
+  const int64_t want = (dst_rows + 7) / 8;
+  const int blocks = (int)(want < (int64_t)sms * 16 ? want : (int64_t)sms * 16);
+  gather_rows_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(
+      (const uint4 *)src, src_rows, row_bytes / 16, src_ld_bytes / 16, dst_ld_bytes / 16, sorted_ids,
+      num_post_padded, numel, top_k, (uint4 *)dst, dst_rows);
+  return cuda_rc(cudaGetLastError(), "mgemm_gather_rows launch");
+}
+
+extern "C" int mgemm_silu_and_mul(const void *in, int64_t R, int64_t F, void *out, mgemm_stream_t stream) {
+  if (!in || !out || R < 0 || F < 0) return MGEMM_EINVAL;
+  if (F % 8 || ((uintptr_t)in & 15) || ((uintptr_t)out & 15)) return MGEMM_EALIGN;
+  if (R == 0 || F == 0) return MGEMM_OK;
+  int sms = sm_count_cached();
+  if (sms <= 0) return MGEMM_ECUDA;
+  const int64_t n = R * (F / 8);
+  const int64_t want = (n + 255) / 256;
+  const int blocks = (int)(want < (int64_t)sms * 32 ? want : (int64_t)sms * 32);
+  silu_mul_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>((const uint4 *)in, R, F / 8, (uint4 *)out);
+  return cuda_rc(cudaGetLastError(), "mgemm_silu_and_mul launch");
+}
 
 extern "C" int64_t mgemm_moe_align_workspace_bytes(int64_t numel, int E) {
   if (numel < 0 || E < 1 || E > MGEMM_MAX_EXPERTS) return -1;

@@ -1,0 +1,81 @@
+"""The routed MoE layer (``fused_moe``) on this library's kernels.
+
+pytorch-labs/applied-ai issue 24 (the column-major fused MoE script, built on
+vLLM's fused_moe.py), ``fused_moe``: the top-k expert ids are aligned to the
+block size (``moe_align_block_size``); the first GEMM multiplies each (token,
+slot) entry by its expert's w1 and writes row ``entry`` of a [T * top_k, 2F]
+cache; ``silu_and_mul`` gates it to [T * top_k, F]; the second GEMM multiplies
+each entry by its expert's w2, scaled by its routed weight; the top_k rows of
+each token are summed.
+
+Here the steps are:
+  mgemm_moe_align   sorted entries, block experts, padded group sizes
+  mgemm_fill_args   args block of the sorted rows (M = -1: the padded total)
+  mgemm_gather_rows the token rows in sorted order (zeros for padding)
+  mgemm_fwd_scatter grouped GEMM over the sorted rows, each row stored at its
+                    entry (second GEMM: times the routed weight)
+  mgemm_silu_and_mul, mgemm_gather_rows, mgemm_fwd_scatter, mgemm_topk_sum
+The routing itself (softmax over the gating logits, top-k, renormalization)
+is the caller's: ``topk_weights`` and ``topk_ids`` come in.  This module only
+allocates buffers with torch and calls the binding; every step runs in the
+CUDA library, and nothing waits on the host.
+"""
+
+import torch
+
+from . import binding as B
+
+BLOCK = B.MGEMM_TILE_M  # rows per block: the GEMM's row tile
+
+
+def align(topk_ids, E, block=BLOCK):
+    """mgemm_moe_align with freshly allocated outputs: (sorted_ids,
+    expert_ids, num_post_padded, group_sizes)."""
+    dev = topk_ids.device
+    ids = topk_ids.to(torch.int32).contiguous()
+    n = ids.numel()
+    cap, max_blocks = B.moe_align_buffer_sizes(n, E, block)
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(max_blocks, dtype=torch.int32, device=dev)
+    npp = torch.empty(1, dtype=torch.int32, device=dev)
+    gs = torch.empty(E, dtype=torch.int64, device=dev)
+    ws = torch.empty(B.mgemm_moe_align_workspace_bytes(n, E), dtype=torch.uint8, device=dev)
+    B.mgemm_moe_align(ids, E, block, sorted_ids, expert_ids, npp, ws, gs)
+    return sorted_ids, expert_ids, npp, gs
+
+
+def fused_moe(hidden_states, w1, w2, topk_weights, topk_ids):
+    """hidden_states bf16 [T, H]; w1 bf16 [E, 2F, H]; w2 bf16 [E, H, F];
+    topk_weights float32 [T, top_k]; topk_ids int [T, top_k], every id in
+    [0, E) (as in fused_moe, whose caches are uninitialized: an entry that is
+    not placed leaves its rows undefined).  Returns bf16 [T, H]."""
+    if hidden_states.dtype != torch.bfloat16 or w1.dtype != torch.bfloat16 or w2.dtype != torch.bfloat16:
+        raise B.MgemmError("fused_moe takes bf16 activations and weights")
+    x = hidden_states.contiguous()
+    w1 = w1.contiguous()
+    w2 = w2.contiguous()
+    T, H = x.shape
+    E, F2, _ = w1.shape
+    F = F2 // 2
+    top_k = topk_ids.shape[1]
+    n = T * top_k
+    dev = x.device
+    sorted_ids, _, npp, gs = align(topk_ids, E)
+    cap = sorted_ids.numel()
+    args = torch.empty(B.mgemm_args_bytes(E), dtype=torch.uint8, device=dev)
+    B.mgemm_fill_args(gs, E, -1, args)
+    bf = torch.bfloat16
+    a1 = torch.empty(cap, H, dtype=bf, device=dev)
+    B.mgemm_gather_rows(x, sorted_ids, npp, n, top_k, a1)
+    c1 = torch.empty(n, F2, dtype=bf, device=dev)
+    B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a1, w1, c1, sorted_ids, n, None, cap, H, F2, E)
+    c2 = torch.empty(n, F, dtype=bf, device=dev)
+    B.mgemm_silu_and_mul(c1, c2)
+    a2 = torch.empty(cap, F, dtype=bf, device=dev)
+    B.mgemm_gather_rows(c2, sorted_ids, npp, n, 1, a2)
+    c3 = torch.empty(n, H, dtype=bf, device=dev)
+    wts = topk_weights.to(torch.float32).contiguous().view(-1)
+    B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a2, w2, c3, sorted_ids, n, wts, cap, F, H, E)
+    out = torch.empty(T, H, dtype=bf, device=dev)
+    B.mgemm_topk_sum(c3, T, top_k, out)
+    return out

@@ -69,7 +69,7 @@ def test_host_checks_fill_args(lib):
     assert lib.mgemm_fill_args(None, 4, 64, good, None) == -1
     assert lib.mgemm_fill_args(good, 0, 64, good, None) == -1
     assert lib.mgemm_fill_args(good, 1025, 64, good, None) == -3
-    assert lib.mgemm_fill_args(good, 4, -1, good, None) == -1
+    assert lib.mgemm_fill_args(good, 4, -2, good, None) == -1  # M = -1 means "the sum of the sizes"
     assert lib.mgemm_fill_args(good, 4, 64, P(0x10008), None) == -2   # args must be 16-byte aligned
 
 

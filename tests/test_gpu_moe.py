@@ -1,0 +1,134 @@
+"""GPU parity of the routed layer's calls (mgemm_gather_rows,
+mgemm_fwd_scatter, mgemm_silu_and_mul, mgemm_topk_sum, mgemm_fill_args with
+M = -1) and of moe.fused_moe, against oracle.routing.
+
+Integer outputs (gather) are compared bit for bit; GEMM outputs within
+1e-2 * max|ref| (bf16 operands, fp32 accumulation, one rounding); the whole
+layer (two GEMMs with bf16 caches between them) within 2e-2 * max|ref|.
+Rows the kernels must not touch are pre-filled with a sentinel and checked."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import routing as R
+from tests.helpers import BF16_TOL, assert_close, is_sentinel, new_args, parse_args, sentinel_bf16, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF = torch.bfloat16
+
+
+def B():
+    from mixture_experts_grouped_gmm_gb300 import binding
+
+    return binding
+
+
+def routing_ids(T, k, E, seed):
+    """Top-k distinct experts per token (uniform), int32 [T, k]."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+
+
+def aligned(ids, E):
+    from mixture_experts_grouped_gmm_gb300 import moe
+
+    sid, eid, npp, gs = moe.align(ids.to(DEV), E)
+    torch.cuda.synchronize()
+    return sid, eid, npp, gs
+
+
+def test_fill_args_sum_mode_matches_explicit_M():
+    gs = torch.tensor([256, 0, 128, 384, 0, 128], dtype=torch.int64, device=DEV)
+    a1, a2 = new_args(6, DEV), new_args(6, DEV)
+    B().mgemm_fill_args(gs, 6, 896, a1)
+    B().mgemm_fill_args(gs, 6, -1, a2)
+    torch.cuda.synchronize()
+    assert torch.equal(a1, a2)
+    assert parse_args(a2, 6)["status"] == 0
+
+
+def test_gather_rows_bit_exact():
+    T, k, E, K = 300, 2, 8, 136
+    ids = routing_ids(T, k, E, 1)
+    sid, eid, npp, gs = aligned(ids, E)
+    x = torch.randn(T, K, device=DEV).to(BF)
+    cap = sid.numel()
+    dst = sentinel_bf16((cap, K), DEV)
+    B().mgemm_gather_rows(x, sid, npp, T * k, k, dst)
+    torch.cuda.synchronize()
+    tot = int(npp)
+    ref = R.gather_rows(to_np(x), sid.cpu().numpy(), tot, T * k, k)
+    assert np.array_equal(to_np(dst[:tot]), ref.astype(np.float32))
+    assert is_sentinel(dst[tot:]), "rows past the padded total must stay untouched"
+
+
+@pytest.mark.parametrize("with_weights", [False, True])
+@pytest.mark.parametrize("T,k,E,K,N", [(300, 2, 8, 256, 384), (5, 2, 16, 128, 256), (1000, 6, 64, 192, 136)])
+def test_fwd_scatter_against_oracle(T, k, E, K, N, with_weights):
+    ids = routing_ids(T, k, E, T + E)
+    sid, eid, npp, gs = aligned(ids, E)
+    n, cap = T * k, sid.numel()
+    args = new_args(E, DEV)
+    B().mgemm_fill_args(gs, E, -1, args)
+    x = torch.randn(T, K, device=DEV).to(BF)
+    w = (0.05 * torch.randn(E, N, K, device=DEV)).to(BF)
+    a = torch.empty(cap, K, dtype=BF, device=DEV)
+    B().mgemm_gather_rows(x, sid, npp, n, k, a)
+    wts = torch.rand(n, device=DEV) if with_weights else None
+    out = sentinel_bf16((n + 4, N), DEV)
+    B().mgemm_fwd_scatter(args, B().MGEMM_BF16, 1, a, w, out, sid, n, wts, cap, K, N, E)
+    torch.cuda.synchronize()
+    assert parse_args(args, E)["status"] == 0
+    assert is_sentinel(out[n:]), "wrote past the entry rows"
+    ref = R.fused_moe_gemm(to_np(x), to_np(w), sid.cpu().numpy(), eid.cpu().numpy(), int(npp), n, k, 128,
+                           None if wts is None else wts.cpu().numpy())
+    assert not np.isnan(ref).any()  # every entry is placed
+    assert_close(to_np(out[:n]), ref, BF16_TOL, "fwd_scatter")
+
+
+def test_silu_and_mul():
+    x = (3 * torch.randn(257, 2 * 136, device=DEV)).to(BF)
+    out = torch.empty(257, 136, dtype=BF, device=DEV)
+    B().mgemm_silu_and_mul(x, out)
+    torch.cuda.synchronize()
+    ref = R.silu_and_mul(to_np(x))
+    got = to_np(out).astype(np.float64)
+    # one bf16 rounding of an fp32 result: within 2^-8 relative, plus fp32 exp error
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+def test_topk_sum():
+    T, k, H = 129, 3, 264
+    c = torch.randn(T * k, H, device=DEV).to(BF)
+    out = torch.empty(T, H, dtype=BF, device=DEV)
+    B().mgemm_topk_sum(c, T, k, out)
+    torch.cuda.synchronize()
+    ref = to_np(c).astype(np.float64).reshape(T, k, H).sum(axis=1)
+    got = to_np(out).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
+
+
+@pytest.mark.parametrize("T,k,E,H,F", [(200, 2, 8, 256, 384), (3, 2, 8, 128, 128)])
+def test_fused_moe_layer(T, k, E, H, F):
+    from mixture_experts_grouped_gmm_gb300 import moe
+
+    torch.manual_seed(T)
+    x = torch.randn(T, H, device=DEV).to(BF)
+    w1 = (0.05 * torch.randn(E, 2 * F, H, device=DEV)).to(BF)
+    w2 = (0.05 * torch.randn(E, H, F, device=DEV)).to(BF)
+    logits = torch.randn(T, E, device=DEV)
+    probs = torch.softmax(logits, dim=-1)
+    tw, tid = torch.topk(probs, k, dim=-1)
+    tw = tw / tw.sum(dim=-1, keepdim=True)
+    out = moe.fused_moe(x, w1, w2, tw, tid)
+    torch.cuda.synchronize()
+    # oracle: the same steps in float64 (no bf16 caches in between)
+    sid, eid, tot, _ = R.moe_align_block_size(tid.cpu().numpy(), 128, E)
+    n = T * k
+    c1 = R.fused_moe_gemm(to_np(x), to_np(w1), sid, eid, tot, n, k, 128)
+    c2 = R.silu_and_mul(c1)
+    c3 = R.fused_moe_gemm(c2, to_np(w2), sid, eid, tot, n, 1, 128, topk_weights=tw.cpu().numpy().ravel())
+    ref = c3.reshape(T, k, H).sum(axis=1)
+    assert_close(to_np(out), ref, 2e-2, "fused_moe")
