@@ -9,12 +9,18 @@ each entry by its expert's w2, scaled by its routed weight; the top_k rows of
 each token are summed.
 
 Here the steps are:
-  mgemm_moe_align   sorted entries, block experts, padded group sizes
-  mgemm_fill_args   args block of the sorted rows (M = -1: the padded total)
-  mgemm_gather_rows the token rows in sorted order (zeros for padding)
-  mgemm_fwd_scatter grouped GEMM over the sorted rows, each row stored at its
-                    entry (second GEMM: times the routed weight)
-  mgemm_silu_and_mul, mgemm_gather_rows, mgemm_fwd_scatter, mgemm_topk_sum
+  mgemm_moe_align    sorted entries, block experts, padded group sizes
+  mgemm_fill_args    args block of the sorted rows (M = -1: the padded total)
+  mgemm_gather_rows  the token rows in sorted order (zeros for padding)
+  mgemm_fwd          first GEMM over the sorted rows, output kept in sorted order
+  mgemm_silu_and_mul gated rows, still in sorted order: exactly the rows the
+                     second GEMM reads (padding rows give zeros through both)
+  mgemm_fwd_scatter  second GEMM, each row times its routed weight and stored
+                     at its (token, slot) entry
+  mgemm_topk_sum     the sum over each token's top_k entries
+The pages' layer keeps the first cache in entry order and gathers it again
+for the second GEMM; keeping it in sorted order gives the same values per
+entry with one copy less.
 The routing itself (softmax over the gating logits, top-k, renormalization)
 is the caller's: ``topk_weights`` and ``topk_ids`` come in.  This module only
 allocates buffers with torch and calls the binding; every step runs in the
@@ -67,12 +73,10 @@ def fused_moe(hidden_states, w1, w2, topk_weights, topk_ids):
     bf = torch.bfloat16
     a1 = torch.empty(cap, H, dtype=bf, device=dev)
     B.mgemm_gather_rows(x, sorted_ids, npp, n, top_k, a1)
-    c1 = torch.empty(n, F2, dtype=bf, device=dev)
-    B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a1, w1, c1, sorted_ids, n, None, cap, H, F2, E)
-    c2 = torch.empty(n, F, dtype=bf, device=dev)
-    B.mgemm_silu_and_mul(c1, c2)
+    c1 = torch.empty(cap, F2, dtype=bf, device=dev)  # rows past the padded total are never read
+    B.mgemm_fwd(args, B.MGEMM_BF16, 1, a1, None, w1, None, c1, cap, H, F2, E)
     a2 = torch.empty(cap, F, dtype=bf, device=dev)
-    B.mgemm_gather_rows(c2, sorted_ids, npp, n, 1, a2)
+    B.mgemm_silu_and_mul(c1, a2)
     c3 = torch.empty(n, H, dtype=bf, device=dev)
     wts = topk_weights.to(torch.float32).contiguous().view(-1)
     B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a2, w2, c3, sorted_ids, n, wts, cap, F, H, E)
