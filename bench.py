@@ -311,8 +311,32 @@ def mixtral_extra(torch, B, dev, pk):
         res[n] = {"p50_us": round(t["p50_us"], 1), "tflops_padded_rows": round(tf, 1),
                   "tensor_frac": round(tf / pk["bf16_tflops"], 3),
                   "tflops_routed_rows": round(tf * real / M, 1)}
+    res["routed_layer"] = routed_layer(torch, B, dev, pk, d)
     del d
     return res
+
+
+def routed_layer(torch, B, dev, pk, d):
+    """The routed layer (moe.fused_moe: device alignment, gather, up GEMM,
+    silu_and_mul, down GEMM with routed weights scattered to the entries, top-k
+    sum) on the same routing and weights (viewed in the [E, N, K] layout of
+    fused_moe; the values do not affect the time)."""
+    from mixture_experts_grouped_gmm_gb300 import moe
+
+    T, H, F, E = d["T"], d["H"], d["F"], d["E"]
+    w1 = d["w1"].view(E, 2 * F, H)
+    w2 = d["w2"].view(E, H, F)
+    g = torch.Generator(device=dev).manual_seed(1)
+    x = torch.randn(T, H, generator=g, device=dev).to(torch.bfloat16)
+    tw = d["topk_weights"].to(dev)
+    tid = d["topk_ids"].to(dev).to(torch.int32)
+    t = time_events(torch, lambda: moe.fused_moe(x, w1, w2, tw, tid), 10)
+    routed = T * tid.shape[1]
+    flop = 2 * routed * H * 2 * F + 2 * routed * F * H
+    tf = flop / (t["p50_us"] * 1e-6) / 1e12
+    return {"what": "fused_moe(x, w1, w2, topk_weights, topk_ids), all steps on the device",
+            "p50_us": round(t["p50_us"], 1), "tflops_routed_rows": round(tf, 1),
+            "tensor_frac_routed": round(tf / pk["bf16_tflops"], 3)}
 
 
 def cpu_baseline_grin(seconds=10.0):
