@@ -124,3 +124,31 @@ def gather_rows(src, sorted_ids, num_post, numel, top_k):
         if i < numel:
             out[s] = src[i // top_k]
     return out
+
+
+def topk_softmax(gating_output, top_k, renormalize):
+    """fused_moe's routing: softmax over the experts of each token's gating
+    logits, the top_k largest probabilities (largest first) and their expert
+    ids, divided by their sum when renormalize.  float64.
+
+    Readings: the selection is made on the logits (softmax is strictly
+    increasing in each logit, so the top_k probabilities are those of the
+    top_k logits); equal logits go to the lower expert id first (the order a
+    stable descending sort gives)."""
+    import numpy as np
+
+    g = np.asarray(gating_output, dtype=np.float64)
+    T, E = g.shape
+    ids = np.empty((T, top_k), dtype=np.int64)
+    wts = np.empty((T, top_k), dtype=np.float64)
+    for t in range(T):
+        row = g[t]
+        m = row.max()
+        ex = np.exp(row - m)
+        p = ex / ex.sum()
+        order = sorted(range(E), key=lambda e: (-row[e], e))[:top_k]
+        ids[t] = order
+        wts[t] = p[order]
+        if renormalize:
+            wts[t] = wts[t] / wts[t].sum()
+    return wts, ids

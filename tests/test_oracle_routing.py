@@ -161,3 +161,23 @@ def test_gather_rows_pads_with_zeros():
     g = gather_rows(src, sid, tot, 4, 2)
     # expert 0: entries 1, 2, 3 (tokens 0, 1, 1) + 1 pad; expert 1: entry 0 (token 0) + 3 pads
     assert g.tolist() == [[1, 2], [3, 4], [3, 4], [0, 0], [1, 2], [0, 0], [0, 0], [0, 0]]
+
+
+def test_topk_softmax_against_torch_and_by_hand():
+    import torch
+
+    from oracle.routing import topk_softmax
+    rng = np.random.default_rng(3)
+    g = rng.standard_normal((64, 16)).astype(np.float32)   # distinct logits: no ties
+    w, i = topk_softmax(g, 4, False)
+    p = torch.softmax(torch.from_numpy(g).double(), dim=-1)
+    tw, ti = torch.topk(p, 4, dim=-1)
+    assert np.array_equal(i, ti.numpy()) and np.allclose(w, tw.numpy(), rtol=1e-14)
+    wr, ir = topk_softmax(g, 4, True)
+    assert np.array_equal(ir, i) and np.allclose(wr.sum(axis=1), 1.0, rtol=1e-14)
+    assert np.allclose(wr, w / w.sum(axis=1, keepdims=True), rtol=1e-14)
+    # by hand: logits [0, ln 3, ln 3, 0]: probabilities [1/8, 3/8, 3/8, 1/8]; ties -> lower id
+    h = np.array([[0.0, np.log(3.0), np.log(3.0), 0.0]])
+    w2, i2 = topk_softmax(h, 3, False)
+    assert i2.tolist() == [[1, 2, 0]]
+    assert np.allclose(w2, [[3 / 8, 3 / 8, 1 / 8]], rtol=1e-14)
