@@ -330,7 +330,7 @@ def routed_layer(torch, B, dev, pk, d):
     x = torch.randn(T, H, generator=g, device=dev).to(torch.bfloat16)
     tw = d["topk_weights"].to(dev)
     tid = d["topk_ids"].to(dev).to(torch.int32)
-    t = time_events(torch, lambda: moe.fused_moe(x, w1, w2, tw, tid), 10)
+    t = time_events(torch, lambda: moe.fused_experts(x, w1, w2, tw, tid), 10)
     routed = T * tid.shape[1]
     flop = 2 * routed * H * 2 * F + 2 * routed * F * H
     tf = flop / (t["p50_us"] * 1e-6) / 1e12

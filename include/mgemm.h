@@ -335,6 +335,22 @@ int mgemm_silu_and_mul(const void *in, int64_t R, int64_t F, void *out, mgemm_st
  */
 int mgemm_topk_sum(const void *in, int64_t T, int top_k, int64_t H, void *out, mgemm_stream_t stream);
 
+/*
+ * mgemm_topk_softmax -- fused_moe's routing [CMM] (its topk_softmax call and
+ * renormalize step): per token t, p = softmax(gating[t, :]) over the E
+ * experts; topk_ids[t, :] = the top_k experts, largest probability first;
+ * topk_weights[t, :] = their probabilities, divided by their sum when
+ * renormalize != 0.
+ *   gating        float32 [T, E], finite
+ *   topk_weights  float32 [T, top_k];  topk_ids  int32 [T, top_k]
+ * The selection compares logits (softmax is increasing in each, so the same
+ * experts, with no rounding ties); equal logits go to the lower id.  The
+ * weights are exp(l - max) / sum in fp32.  1 <= top_k <= E <= MGEMM_MAX_EXPERTS.
+ * One warp per token.
+ */
+int mgemm_topk_softmax(const float *gating, int64_t T, int E, int top_k, int renormalize, float *topk_weights,
+                       int32_t *topk_ids, mgemm_stream_t stream);
+
 /* Number of SMs of the current device (the persistent GEMM grid size), or < 0 on error. */
 int mgemm_num_sms(void);
 /* Static string naming a MGEMM_E* or MGEMM_STATUS_* code. */

@@ -71,6 +71,8 @@ _SIGS = {
                                           ctypes.c_void_p]),
     "mgemm_topk_sum": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                       ctypes.c_void_p, ctypes.c_void_p]),
+    "mgemm_topk_softmax": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "mgemm_num_sms": (ctypes.c_int, []),
     "mgemm_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mgemm_version": (ctypes.c_int, []),
@@ -228,6 +230,14 @@ def mgemm_topk_sum(inp, T, top_k, out):
     _cuda(inp, out)
     _check(lib().mgemm_topk_sum(_p(inp), int(T), int(top_k), inp.shape[-1], _p(out), _stream(out)),
            "mgemm_topk_sum")
+
+
+def mgemm_topk_softmax(gating, top_k, renormalize, topk_weights, topk_ids):
+    """gating float32 [T, E] -> topk_weights float32 [T, top_k], topk_ids int32 [T, top_k]."""
+    _cuda(gating, topk_weights, topk_ids)
+    T, E = gating.shape
+    _check(lib().mgemm_topk_softmax(_p(gating), T, E, int(top_k), int(bool(renormalize)), _p(topk_weights),
+                                    _p(topk_ids), _stream(gating)), "mgemm_topk_softmax")
 
 
 def mgemm_num_sms():

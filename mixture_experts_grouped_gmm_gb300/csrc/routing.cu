@@ -210,9 +210,111 @@ __global__ void __launch_bounds__(256) topk_sum_kernel(const uint4 *__restrict__
   }
 }
 
+// fused_moe's routing, one warp per token: softmax over the E experts of the
+// token's gating logits and the top_k largest probabilities, largest first.
+// The selection compares the logits (softmax is increasing in each of them, so
+// this picks the same experts without rounding ties), equal logits going to the
+// lower expert id; the weights are exp(l - max) / sum, in fp32 with expf, and
+// divided by their sum when renormalize.  Lane l holds experts l, l + 32, ...
+template <int NV>
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ gating, int64_t T, int E,
+                                                             int top_k, int renormalize, float *__restrict__ weights,
+                                                             int32_t *__restrict__ ids) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;  // whole warps leave together
+  const float *row = gating + t * E;
+  float v[NV];
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? __ldg(row + e) : -INFINITY;
+    m = fmaxf(m, v[j]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < NV; ++j)
+    if (lane + 32 * j < E) sum += expf(v[j] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  uint32_t taken = 0;
+  float wsel = 0.f, wsum = 0.f;  // lane r keeps the weight of pick r
+  int isel = 0;
+  for (int r = 0; r < top_k; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < bi))) {
+        bv = v[j];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);  // the owner marks it
+    const float w = expf(bv - m) / sum;
+    wsum += w;
+    if (lane == (r & 31)) {
+      wsel = w;
+      isel = bi;
+    }
+    if ((r & 31) == 31 || r == top_k - 1) {  // flush up to 32 picks
+      const int r0 = r & ~31;
+      if (lane <= r - r0) {
+        ids[t * top_k + r0 + lane] = isel;
+        weights[t * top_k + r0 + lane] = wsel;  // renormalized below
+      }
+    }
+  }
+  if (renormalize) {
+    __syncwarp();
+    for (int r = lane; r < top_k; r += 32) weights[t * top_k + r] = weights[t * top_k + r] / wsum;
+  }
+}
+
 }  // namespace mgemm
 
 using namespace mgemm;
+
+extern "C" int mgemm_topk_softmax(const float *gating, int64_t T, int E, int top_k, int renormalize,
+                                  float *topk_weights, int32_t *topk_ids, mgemm_stream_t stream) {
+  if (T < 0 || E < 1 || E > MGEMM_MAX_EXPERTS || top_k < 1 || top_k > E) return MGEMM_EINVAL;
+  if (T == 0) return MGEMM_OK;
+  if (!gating || !topk_weights || !topk_ids) return MGEMM_EINVAL;
+  if (((uintptr_t)gating & 3) || ((uintptr_t)topk_weights & 3) || ((uintptr_t)topk_ids & 3)) return MGEMM_EALIGN;
+  const int64_t blocks = (T + 7) / 8;
+  if (blocks >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int nv = (E + 31) / 32;
+#define MGEMM_TOPK_LAUNCH(NV) \
+  topk_softmax_kernel<NV><<<(unsigned)blocks, 256, 0, s>>>(gating, T, E, top_k, renormalize, topk_weights, topk_ids)
+  if (nv <= 1)
+    MGEMM_TOPK_LAUNCH(1);
+  else if (nv <= 2)
+    MGEMM_TOPK_LAUNCH(2);
+  else if (nv <= 4)
+    MGEMM_TOPK_LAUNCH(4);
+  else if (nv <= 8)
+    MGEMM_TOPK_LAUNCH(8);
+  else if (nv <= 16)
+    MGEMM_TOPK_LAUNCH(16);
+  else
+    MGEMM_TOPK_LAUNCH(32);
+#undef MGEMM_TOPK_LAUNCH
+  return cuda_rc(cudaGetLastError(), "mgemm_topk_softmax launch");
+}
 
 extern "C" int mgemm_topk_sum(const void *in, int64_t T, int top_k, int64_t H, void *out, mgemm_stream_t stream) {
   if (!in || !out || T < 0 || top_k < 1 || H < 0) return MGEMM_EINVAL;

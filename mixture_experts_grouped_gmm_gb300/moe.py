@@ -21,10 +21,12 @@ Here the steps are:
 The pages' layer keeps the first cache in entry order and gathers it again
 for the second GEMM; keeping it in sorted order gives the same values per
 entry with one copy less.
-The routing itself (softmax over the gating logits, top-k, renormalization)
-is the caller's: ``topk_weights`` and ``topk_ids`` come in.  This module only
-allocates buffers with torch and calls the binding; every step runs in the
-CUDA library, and nothing waits on the host.
+``fused_moe`` starts from the gating logits, as the page's does: the routing
+(softmax over the experts, top-k, optional renormalization) is
+``mgemm_topk_softmax``.  ``fused_experts`` starts from routing weights and ids
+the caller already has.  This module only allocates buffers with torch and
+calls the binding; every step runs in the CUDA library, and nothing waits on
+the host.
 """
 
 import torch
@@ -50,7 +52,24 @@ def align(topk_ids, E, block=BLOCK):
     return sorted_ids, expert_ids, npp, gs
 
 
-def fused_moe(hidden_states, w1, w2, topk_weights, topk_ids):
+def route(gating_output, topk, renormalize):
+    """mgemm_topk_softmax: (topk_weights float32 [T, topk], topk_ids int32 [T, topk])."""
+    g = gating_output.to(torch.float32).contiguous()
+    T = g.shape[0]
+    w = torch.empty(T, topk, dtype=torch.float32, device=g.device)
+    i = torch.empty(T, topk, dtype=torch.int32, device=g.device)
+    B.mgemm_topk_softmax(g, topk, renormalize, w, i)
+    return w, i
+
+
+def fused_moe(hidden_states, w1, w2, gating_output, topk, renormalize):
+    """The page's fused_moe: route by gating_output [T, E] (top-k of the
+    softmax, renormalized when asked), then fused_experts."""
+    topk_weights, topk_ids = route(gating_output, topk, renormalize)
+    return fused_experts(hidden_states, w1, w2, topk_weights, topk_ids)
+
+
+def fused_experts(hidden_states, w1, w2, topk_weights, topk_ids):
     """hidden_states bf16 [T, H]; w1 bf16 [E, 2F, H]; w2 bf16 [E, H, F];
     topk_weights float32 [T, top_k]; topk_ids int [T, top_k], every id in
     [0, E) (as in fused_moe, whose caches are uninitialized: an entry that is

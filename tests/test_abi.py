@@ -89,6 +89,12 @@ def test_host_checks_gemms(lib):
     assert lib.mgemm_wgrad(a, 1, x, s, w, s, o, 64, 128, 256, 4, 64, None) == -1           # fp8 ld < colwise_ld
     assert lib.mgemm_wgrad(a, 1, x, s, w, s, o, 64, 128, 256, 4, 648, None) == -2          # fp8 ld % 16
     assert lib.mgemm_wgrad(a, 0, x, None, w, None, None, 64, 128, 256, 4, 0, None) == -1
+    f = lib.mgemm_fwd_scatter
+    m = P(0x60000)
+    assert f(a, 1, 1, x, w, o, m, 64, None, 64, 128, 256, 4, None) == -5                  # fp8: not provided
+    assert f(a, 0, 1, x, w, o, None, 64, None, 64, 128, 256, 4, None) == -1               # no row map
+    assert f(a, 0, 1, x, w, o, P(0x60002), 64, None, 64, 128, 256, 4, None) == -2         # row map alignment
+    assert f(a, 0, 1, x, w, o, m, -1, None, 64, 128, 256, 4, None) == -1                  # map_limit < 0
 
 
 def test_host_checks_quant(lib):
@@ -117,6 +123,18 @@ def test_host_checks_moe_align(lib):
     assert f(p, 12, 4, 4, p, p, p, ctypes.c_void_p(0x10004), p, None) == -2      # group_sizes not 8-aligned
     ws = lib.mgemm_moe_align_workspace_bytes
     assert ws(0, 4) == 16 and ws(2048, 4) == 16 and ws(2049, 64) == 2 * 64 * 4 and ws(10, 0) == -1
+
+
+def test_host_checks_topk_softmax(lib):
+    p = ctypes.c_void_p(0x10000)
+    f = lib.mgemm_topk_softmax
+    assert f(p, 4, 0, 1, 0, p, p, None) == -1      # E < 1
+    assert f(p, 4, 1025, 1, 0, p, p, None) == -1   # E > MGEMM_MAX_EXPERTS
+    assert f(p, 4, 8, 9, 0, p, p, None) == -1      # top_k > E
+    assert f(p, 4, 8, 0, 0, p, p, None) == -1      # top_k < 1
+    assert f(None, 4, 8, 2, 0, p, p, None) == -1   # no logits
+    assert f(ctypes.c_void_p(0x10002), 4, 8, 2, 0, p, p, None) == -2  # misaligned
+    assert f(None, 0, 8, 2, 0, None, None, None) == 0   # no tokens: nothing to do
 
 
 def test_colwise_ld_bounds_the_padded_layout():

@@ -1,6 +1,7 @@
-"""GPU parity of the routed layer's calls (mgemm_gather_rows,
-mgemm_fwd_scatter, mgemm_silu_and_mul, mgemm_topk_sum, mgemm_fill_args with
-M = -1) and of moe.fused_moe, against oracle.routing.
+"""GPU parity of the routed layer's calls (mgemm_topk_softmax,
+mgemm_gather_rows, mgemm_fwd_scatter, mgemm_silu_and_mul, mgemm_topk_sum,
+mgemm_fill_args with M = -1) and of moe.fused_experts / moe.fused_moe, against
+oracle.routing.  Expert ids are compared exactly.
 
 Integer outputs (gather) are compared bit for bit; GEMM outputs within
 1e-2 * max|ref| (bf16 operands, fp32 accumulation, one rounding); the whole
@@ -122,7 +123,7 @@ def test_fused_moe_layer(T, k, E, H, F):
     probs = torch.softmax(logits, dim=-1)
     tw, tid = torch.topk(probs, k, dim=-1)
     tw = tw / tw.sum(dim=-1, keepdim=True)
-    out = moe.fused_moe(x, w1, w2, tw, tid)
+    out = moe.fused_experts(x, w1, w2, tw, tid)
     torch.cuda.synchronize()
     # oracle: the same steps in float64 (no bf16 caches in between)
     sid, eid, tot, _ = R.moe_align_block_size(tid.cpu().numpy(), 128, E)
@@ -132,3 +133,43 @@ def test_fused_moe_layer(T, k, E, H, F):
     c3 = R.fused_moe_gemm(c2, to_np(w2), sid, eid, tot, n, 1, 128, topk_weights=tw.cpu().numpy().ravel())
     ref = c3.reshape(T, k, H).sum(axis=1)
     assert_close(to_np(out), ref, 2e-2, "fused_moe")
+
+
+@pytest.mark.parametrize("T,E,k,renorm,kind", [
+    (1000, 8, 2, True, "normal"), (333, 64, 6, False, "normal"), (64, 128, 40, True, "normal"),
+    (40, 1024, 1024, False, "normal"), (200, 64, 6, True, "ties"), (17, 3, 3, True, "ties"),
+])
+def test_topk_softmax(T, E, k, renorm, kind):
+    g = torch.Generator(device=DEV).manual_seed(T + E)
+    if kind == "normal":
+        logits = torch.randn(T, E, generator=g, device=DEV)
+    else:  # few distinct values: many equal logits, ties go to the lower id
+        logits = torch.randint(-2, 3, (T, E), generator=g, device=DEV).float()
+    w = torch.empty(T, k, device=DEV)
+    i = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    B().mgemm_topk_softmax(logits, k, renorm, w, i)
+    torch.cuda.synchronize()
+    rw, ri = R.topk_softmax(logits.cpu().numpy(), k, renorm)
+    assert np.array_equal(i.cpu().numpy(), ri), "expert ids must match exactly"
+    # fp32 exp and an fp32 sum over E terms
+    assert np.allclose(w.cpu().numpy(), rw, rtol=1e-4, atol=1e-7)
+
+
+def test_fused_moe_from_gating_logits():
+    from mixture_experts_grouped_gmm_gb300 import moe
+
+    T, k, E, H, F = 150, 2, 8, 256, 256
+    torch.manual_seed(5)
+    x = torch.randn(T, H, device=DEV).to(BF)
+    w1 = (0.05 * torch.randn(E, 2 * F, H, device=DEV)).to(BF)
+    w2 = (0.05 * torch.randn(E, H, F, device=DEV)).to(BF)
+    gating = torch.randn(T, E, device=DEV)
+    out = moe.fused_moe(x, w1, w2, gating, k, True)
+    torch.cuda.synchronize()
+    tw, tid = R.topk_softmax(gating.cpu().numpy(), k, True)
+    sid, eid, tot, _ = R.moe_align_block_size(tid, 128, E)
+    n = T * k
+    c1 = R.fused_moe_gemm(to_np(x), to_np(w1), sid, eid, tot, n, k, 128)
+    c3 = R.fused_moe_gemm(R.silu_and_mul(c1), to_np(w2), sid, eid, tot, n, 1, 128, topk_weights=tw.ravel())
+    ref = c3.reshape(T, k, H).sum(axis=1)
+    assert_close(to_np(out), ref, 2e-2, "fused_moe from gating logits")
