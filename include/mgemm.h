@@ -320,6 +320,19 @@ int mgemm_fwd_scatter(const void *args, int dtype, int trans_b, const void *x, c
                       int E, mgemm_stream_t stream);
 
 /*
+ * mgemm_fwd_gated -- the first GEMM of fused_moe with silu_and_mul in its
+ * epilogue: out[r, j] = silu(g) * u with g = x[r, :] . w[e(r), j, :] and
+ * u = x[r, :] . w[e(r), F + j, :] (the gate and up halves of w1 [E, 2F, K],
+ * vLLM's silu_and_mul convention), g and u in fp32, silu(g) = g / (1 + exp(-g)),
+ * one rounding to bf16.  Each tile's weight stage holds matching gate and up
+ * rows, so both halves of an output column meet in one accumulator.
+ *   args, x [M, K], M, K, E: as for mgemm_fwd (bf16)
+ *   w    bf16 [E, 2F, K];  out  bf16 [M, F] (F % 8 == 0)
+ */
+int mgemm_fwd_gated(const void *args, const void *x, const void *w, void *out, int64_t M, int K, int F, int E,
+                    mgemm_stream_t stream);
+
+/*
  * mgemm_silu_and_mul -- out[r, j] = silu(in[r, j]) * in[r, F + j] for in bf16
  * [R, 2F] and out bf16 [R, F] (vLLM's silu_and_mul as fused_moe applies it to
  * the first GEMM's output), silu(v) = v / (1 + exp(-v)), computed in fp32 and

@@ -143,6 +143,13 @@ struct GemmParams {
   const int32_t *row_map;
   int64_t map_limit;
   const float *row_weight;
+  // bf16 rows mode, K-major B: gated output (the first GEMM of a SiLU-gated
+  // MLP).  A tile's B stage holds bn / 2 rows of the gate half of w
+  // (rows n0 ..) then the bn / 2 matching rows of the up half (rows
+  // gate_rows + n0 ..); the epilogue writes silu(gate) * up for output
+  // columns n0 .. n0 + bn / 2 - 1.
+  int gated;
+  int gate_rows;
 };
 
 struct TileInfo {
@@ -178,7 +185,7 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
     const int mt_g = __ldg(start + lo + 1) - m_first;
     const int local = t - m_first * p.n_tiles;
     const int mt = local % mt_g;
-    ti.n0 = (local / mt_g) * p.bn;
+    ti.n0 = (local / mt_g) * (p.gated ? p.bn / 2 : p.bn);
     const int64_t rs = __ldg(av.offsets + ti.e), re = __ldg(av.offsets + ti.e + 1);
     // a CTA pair's tile is 256 rows: rank r takes rows 128 r .. 128 r + 127 (the
     // odd CTA's half may lie past the group: loaded, never stored) and columns
@@ -410,7 +417,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                   tma_load_3d(b + j * C::CHUNK, &tmB, &full[stage], ti.n0 + 64 * j, kb * C::BK, ti.e);
               }
             } else {
-              tma_load_3d(b, &tmB, &full[stage], kb * C::BK, ti.n0, ti.e);
+              if (p.gated) {  // gate rows, then the matching up rows (boxes of bn / 2 rows)
+                tma_load_3d(b, &tmB, &full[stage], kb * C::BK, ti.n0, ti.e);
+                tma_load_3d(b + (bn / 2) * 128, &tmB, &full[stage], kb * C::BK, p.gate_rows + ti.n0, ti.e);
+              } else {
+                tma_load_3d(b, &tmB, &full[stage], kb * C::BK, ti.n0, ti.e);
+              }
             }
           } else {
             const int xr = ti.x0 + kb * C::BK;
@@ -622,14 +634,79 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::BN_MAX;
-      const int nchunks = bn / 64;
-      bool released = false;
       // with one warp per quarter, TMEM -> registers runs one chunk ahead (chunk
       // c + 1 loads while chunk c is converted and stored; the loop is unrolled
       // so both register sets keep fixed names); with two, the other warp of the
       // quarter hides the load latency and registers stay within the budget
       constexpr int kNb = C::HN == 1 ? 2 : 1;
       uint32_t va[kNb][32], vb[kNb][32];
+      if constexpr (C::Mode == kModeRows && !C::Fp8 && !C::BMn && C::HN == 1) {
+        if (p.gated) {
+          // accumulator columns [0, bn / 2) hold the gate, [bn / 2, bn) the up
+          // projection of the same output columns: h = silu(g) * u in fp32,
+          // silu(g) = g / (1 + exp(-g)), one rounding to bf16
+          const int half = bn / 2, nout = half / 64;
+          uint32_t(&g)[32] = va[0];  // gate columns c*64 .. +31, then +32 .. +63 in vb[0]
+          uint32_t(&u)[32] = va[1];  // up columns, likewise in vb[1]
+          for (int c = 0; c < nout; ++c) {
+            const int col0 = ti.n0 + c * 64;
+            uint32_t pk[32];
+            if (has_acc) {
+              tmem_ld_32x32b_x32(taddr + c * 64, g);
+              tmem_ld_32x32b_x32(taddr + c * 64 + 32, vb[0]);
+              tmem_ld_32x32b_x32(taddr + half + c * 64, u);
+              tmem_ld_32x32b_x32(taddr + half + c * 64 + 32, vb[1]);
+              tmem_ld_wait();
+              if (c == nout - 1) release(acc);  // the accumulator is read
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+                const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+                pk[j] = pack_bf16x2(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
+                const float g2 = __uint_as_float(vb[0][2 * j]), g3 = __uint_as_float(vb[0][2 * j + 1]);
+                const float u2 = __uint_as_float(vb[1][2 * j]), u3 = __uint_as_float(vb[1][2 * j + 1]);
+                pk[16 + j] = pack_bf16x2(g2 / (1.f + expf(-g2)) * u2, g3 / (1.f + expf(-g3)) * u3);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) pk[j] = 0u;
+            }
+            if (col0 >= p.Nout) continue;
+            if (warp_full) {
+              uint8_t *buf = my_buf + (nstored % C::NBUF) * C::OUT_BUF;
+              if (lane == 0) bulk_wait_read<C::NBUF - 1>();
+              __syncwarp();
+              uint8_t *rowp = buf + lane * 128;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(rowp + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmOut, buf, col0, ti.out_row0 + q * 32);
+                bulk_commit();
+              }
+              ++nstored;
+            } else if (row_ok) {
+              uint4 *dst = reinterpret_cast<uint4 *>(orow + col0);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (col0 + 8 * j < p.Nout) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+          }
+          if (has_acc) {
+            if (nout == 0) release(acc);
+            if (++acc == 2) {
+              acc = 0;
+              acc_phase ^= 1;
+            }
+          }
+          continue;
+        }
+      }
+      const int nchunks = bn / 64;
+      bool released = false;
       if (kNb == 2 && has_acc && h < nchunks) {
         tmem_ld_32x32b_x32(taddr + h * 64, va[0]);
         tmem_ld_32x32b_x32(taddr + h * 64 + 32, vb[0]);

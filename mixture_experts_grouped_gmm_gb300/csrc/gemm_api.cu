@@ -114,10 +114,11 @@ bool make_out_map(CUtensorMap *m, void *out, int64_t rows, int64_t cols) {
 
 }  // namespace
 
-// mgemm_fwd, and mgemm_fwd_scatter when row_map is given (bf16 only)
+// mgemm_fwd; mgemm_fwd_scatter when row_map is given; mgemm_fwd_gated when
+// gate_rows > 0 (w [E, 2 gate_rows, K], N = 2 gate_rows, output gate_rows wide)
 static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
                     const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream,
-                    const int32_t *row_map, int64_t map_limit, const float *row_weight) {
+                    const int32_t *row_map, int64_t map_limit, const float *row_weight, int gate_rows = 0) {
   int rc = common_checks(args, dtype, M, K, N, E);
   if (rc) return rc;
   if (!x || !w || !out) return MGEMM_EINVAL;
@@ -146,13 +147,17 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   // stage): bf16 with w [E, K, N] in one box per stage, when the weights
   // stream (at most 256 rows per expert on average, so HBM bounds the launch)
   const bool allow192 = !fp8 && !trans_b && N % 64 == 0 && M <= 256 * (int64_t)E;
-  const int bn = pair ? choose_bn_units(pair_tiles_estimate(M, E), N, sms / 2)
-                      : choose_bn(rows_tiles_estimate(M, E), N, allow192);
+  int bn = pair ? choose_bn_units(pair_tiles_estimate(M, E), N, sms / 2)
+                : choose_bn(rows_tiles_estimate(M, E), N, allow192);
+  const bool gated = gate_rows > 0;
+  if (gated) bn = bn > 128 ? 256 : 128;  // gate and up halves of whole 64-column chunks
+  const int out_cols = gated ? gate_rows : N;
+  const int tile_cols = gated ? bn / 2 : bn;
   bool b_one_box = false;
   if (trans_b) {  // w [E, N, K]
     const uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
     const uint64_t st[2] = {(uint64_t)K * es, (uint64_t)N * K * es};
-    const uint32_t box[3] = {bk, (uint32_t)(pair ? bn / 2 : bn), 1};
+    const uint32_t box[3] = {bk, (uint32_t)(pair || gated ? bn / 2 : bn), 1};
     if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
   } else {  // w [E, K, N], loaded as 64-column MN-major chunks
     // with N % 64 == 0, w is viewed as [E][N / 64 chunks][K rows][64 columns] (chunk stride 128 B)
@@ -173,7 +178,7 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
     b_one_box = one;
   }
   CUtensorMap to;  // (scattered rows are stored row by row; the map then goes unused)
-  if (!make_out_map(&to, out, row_map ? (map_limit > 0 ? map_limit : 1) : M, N)) return MGEMM_ECUDA;
+  if (!make_out_map(&to, out, row_map ? (map_limit > 0 ? map_limit : 1) : M, out_cols)) return MGEMM_ECUDA;
   GemmParams p{};
   p.args = (const uint8_t *)args;
   p.E = E;
@@ -182,11 +187,13 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   p.row_map = row_map;
   p.map_limit = map_limit;
   p.row_weight = row_weight;
+  p.gated = gated ? 1 : 0;
+  p.gate_rows = gate_rows;
   p.idesc = make_idesc(fp8 ? 0u : 1u, false, !trans_b, pair ? 256 : 128, bn);
   p.a_rows = (int)a_rows;
-  p.n_tiles = (N + bn - 1) / bn;
+  p.n_tiles = (out_cols + tile_cols - 1) / tile_cols;
   p.Kc = K;
-  p.Nout = N;
+  p.Nout = out_cols;
   p.out = (__nv_bfloat16 *)out;
   p.rscale = sx;
   p.cscale = sw;
@@ -217,6 +224,8 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
     if (fp8) return gemm_fp8_rows_mid(ta, tb, to, p, grid, s);
     return trans_b ? gemm_bf16_rows_bk_mid(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn_mid(ta, tb, to, p, grid, s);
   }
+  if (gated)  // bf16, w [E, 2F, K]: the wide or mid K-major form
+    return bn == 256 ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk_mid(ta, tb, to, p, grid, s);
   if (bn == 192 && b_one_box) return gemm_bf16_rows_bmn_w192(ta, tb, to, p, grid, s);
   if (fp8) return gemm_fp8_rows(ta, tb, to, p, grid, s);
   return trans_b ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, to, p, grid, s);
@@ -236,6 +245,12 @@ extern "C" int mgemm_fwd_scatter(const void *args, int dtype, int trans_b, const
   if (((uintptr_t)row_map & 3) || ((uintptr_t)row_weight & 3)) return MGEMM_EALIGN;
   return fwd_impl(args, dtype, trans_b, x, nullptr, w, nullptr, out, M, K, N, E, stream, row_map, map_limit,
                   row_weight);
+}
+
+extern "C" int mgemm_fwd_gated(const void *args, const void *x, const void *w, void *out, int64_t M, int K, int F,
+                               int E, mgemm_stream_t stream) {
+  if (F < 1 || F % 8 || F > (1 << 29)) return F % 8 ? MGEMM_EALIGN : MGEMM_EINVAL;
+  return fwd_impl(args, MGEMM_BF16, 1, x, nullptr, w, nullptr, out, M, K, 2 * F, E, stream, nullptr, 0, nullptr, F);
 }
 
 extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,

@@ -12,15 +12,17 @@ Here the steps are:
   mgemm_moe_align    sorted entries, block experts, padded group sizes
   mgemm_fill_args    args block of the sorted rows (M = -1: the padded total)
   mgemm_gather_rows  the token rows in sorted order (zeros for padding)
-  mgemm_fwd          first GEMM over the sorted rows, output kept in sorted order
-  mgemm_silu_and_mul gated rows, still in sorted order: exactly the rows the
-                     second GEMM reads (padding rows give zeros through both)
+  mgemm_fwd_gated    first GEMM over the sorted rows with silu_and_mul in its
+                     epilogue (gate and up columns of w1 in one accumulator),
+                     output kept in sorted order: exactly the rows the second
+                     GEMM reads (padding rows give zeros)
   mgemm_fwd_scatter  second GEMM, each row times its routed weight and stored
                      at its (token, slot) entry
   mgemm_topk_sum     the sum over each token's top_k entries
-The pages' layer keeps the first cache in entry order and gathers it again
-for the second GEMM; keeping it in sorted order gives the same values per
-entry with one copy less.
+The page's layer writes the first GEMM's [T * top_k, 2F] output, gates it in a
+second pass and gathers it again for the second GEMM; here the gate is applied
+before the first rounding and the gated rows stay in sorted order, so neither
+the 2F-wide cache nor the second gather exists.
 ``fused_moe`` starts from the gating logits, as the page's does: the routing
 (softmax over the experts, top-k, optional renormalization) is
 ``mgemm_topk_softmax``.  ``fused_experts`` starts from routing weights and ids
@@ -92,10 +94,8 @@ def fused_experts(hidden_states, w1, w2, topk_weights, topk_ids):
     bf = torch.bfloat16
     a1 = torch.empty(cap, H, dtype=bf, device=dev)
     B.mgemm_gather_rows(x, sorted_ids, npp, n, top_k, a1)
-    c1 = torch.empty(cap, F2, dtype=bf, device=dev)  # rows past the padded total are never read
-    B.mgemm_fwd(args, B.MGEMM_BF16, 1, a1, None, w1, None, c1, cap, H, F2, E)
-    a2 = torch.empty(cap, F, dtype=bf, device=dev)
-    B.mgemm_silu_and_mul(c1, a2)
+    a2 = torch.empty(cap, F, dtype=bf, device=dev)  # rows past the padded total are never read
+    B.mgemm_fwd_gated(args, a1, w1, a2, cap, H, F, E)
     c3 = torch.empty(n, H, dtype=bf, device=dev)
     wts = topk_weights.to(torch.float32).contiguous().view(-1)
     B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a2, w2, c3, sorted_ids, n, wts, cap, F, H, E)

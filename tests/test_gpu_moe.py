@@ -173,3 +173,21 @@ def test_fused_moe_from_gating_logits():
     c3 = R.fused_moe_gemm(R.silu_and_mul(c1), to_np(w2), sid, eid, tot, n, 1, 128, topk_weights=tw.ravel())
     ref = c3.reshape(T, k, H).sum(axis=1)
     assert_close(to_np(out), ref, 2e-2, "fused_moe from gating logits")
+
+
+@pytest.mark.parametrize("sizes,K,F", [([130, 0, 257, 64, 1], 192, 200), ([128] * 4, 256, 384), ([700], 64, 1000)])
+def test_fwd_gated_against_oracle(sizes, K, F):
+    # silu_and_mul fused into the GEMM epilogue: out = silu(x . w_gate^T) * (x . w_up^T)
+    from oracle import gmm as og
+
+    M, E = int(np.sum(sizes)), len(sizes)
+    args = new_args(E, DEV)
+    B().mgemm_fill_args(torch.tensor(sizes, dtype=torch.int64, device=DEV), E, M, args)
+    x = torch.randn(M, K, device=DEV).to(BF)
+    w = (0.1 * torch.randn(E, 2 * F, K, device=DEV)).to(BF)
+    out = sentinel_bf16((M + 8, F), DEV)
+    B().mgemm_fwd_gated(args, x, w, out, M, K, F, E)
+    torch.cuda.synchronize()
+    assert is_sentinel(out[M:]), "wrote past M rows"
+    ref = R.silu_and_mul(og.gmm_fwd(to_np(x), to_np(w), sizes, trans_b=True))
+    assert_close(to_np(out[:M]), ref, BF16_TOL, "fwd_gated")
