@@ -317,7 +317,7 @@ def mixtral_extra(torch, B, dev, pk):
 
 
 def routed_layer(torch, B, dev, pk, d):
-    """The routed layer (moe.fused_moe: device alignment, gather, up GEMM,
+    """The routed layer (moe.fused_experts: device alignment, gather, gated up GEMM,
     silu_and_mul, down GEMM with routed weights scattered to the entries, top-k
     sum) on the same routing and weights (viewed in the [E, N, K] layout of
     fused_moe; the values do not affect the time)."""
@@ -334,7 +334,7 @@ def routed_layer(torch, B, dev, pk, d):
     routed = T * tid.shape[1]
     flop = 2 * routed * H * 2 * F + 2 * routed * F * H
     tf = flop / (t["p50_us"] * 1e-6) / 1e12
-    return {"what": "fused_moe(x, w1, w2, topk_weights, topk_ids), all steps on the device",
+    return {"what": "moe.fused_experts(x, w1, w2, topk_weights, topk_ids), all steps on the device",
             "p50_us": round(t["p50_us"], 1), "tflops_routed_rows": round(tf, 1),
             "tensor_frac_routed": round(tf / pk["bf16_tflops"], 3)}
 
