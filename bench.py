@@ -317,9 +317,9 @@ def mixtral_extra(torch, B, dev, pk):
 
 
 def routed_layer(torch, B, dev, pk, d):
-    """The routed layer (moe.fused_experts: device alignment, gather, gated up GEMM,
-    silu_and_mul, down GEMM with routed weights scattered to the entries, top-k
-    sum) on the same routing and weights (viewed in the [E, N, K] layout of
+    """The routed layer (moe.fused_experts: device alignment, gather, up GEMM
+    with silu_and_mul in its epilogue, down GEMM with routed weights scattered to
+    the entries, top-k sum) on the same routing and weights (viewed in the [E, N, K] layout of
     fused_moe; the values do not affect the time)."""
     from mixture_experts_grouped_gmm_gb300 import moe
 
