@@ -152,3 +152,19 @@ def topk_softmax(gating_output, top_k, renormalize):
         if renormalize:
             wts[t] = wts[t] / wts[t].sum()
     return wts, ids
+
+
+def fused_moe_token(x_row, w1, w2, expert_ids, weights):
+    """One token's output of the fused_moe layer, float64: the sum over its
+    top-k entries (expert e, routed weight a) of
+    a * silu_and_mul(x . w1[e]^T) . w2[e]^T, with w1 [E, 2F, H] and w2 [E, H, F].
+    What fused_moe computes for that token, without the rest of the batch."""
+    import numpy as np
+
+    x = np.asarray(x_row, dtype=np.float64)
+    out = np.zeros(np.asarray(w2).shape[1])
+    for e, a in zip(expert_ids, weights):
+        up = np.asarray(w1[int(e)], dtype=np.float64) @ x
+        h = silu_and_mul(up[None, :])[0]
+        out += float(a) * (np.asarray(w2[int(e)], dtype=np.float64) @ h)
+    return out

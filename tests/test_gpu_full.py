@@ -202,3 +202,34 @@ def test_mixtral_up_down_full_size():
     assert_close(to_np(down[rt][:, c2]), og.gmm_fwd(to_np(h[rt]), to_np(d["w2"][:, :, c2]), sub), BF16_TOL,
                  "mixtral down")
     assert len(experts) == E
+
+
+def test_mixtral_routed_layer_full_size():
+    # moe.fused_experts at the benchmark's Mixtral shape and launch configuration
+    # (same routing, weights viewed as [E, 2F, H] / [E, H, F]); sampled tokens
+    # recomputed one by one in float64 by the oracle, one expert at a time
+    from mixture_experts_grouped_gmm_gb300 import moe
+    from oracle.routing import fused_moe_token
+
+    d = workloads.mixtral(device=DEV)
+    T, H, F, E = d["T"], d["H"], d["F"], d["E"]
+    w1 = d["w1"].view(E, 2 * F, H)
+    w2 = d["w2"].view(E, H, F)
+    g = torch.Generator(device=DEV).manual_seed(1)
+    x = torch.randn(T, H, generator=g, device=DEV).to(BF)
+    tw = d["topk_weights"].to(DEV)
+    tid = d["topk_ids"].to(DEV).to(torch.int32)
+    out = moe.fused_experts(x, w1, w2, tw, tid)
+    torch.cuda.synchronize()
+    toks = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(9).integers(0, T, 10)]))
+    ids, wts, xs = tid.cpu().numpy(), tw.cpu().numpy(), to_np(x)
+    ref = np.zeros((len(toks), H))
+    for e in range(E):
+        users = [(i, t, j) for i, t in enumerate(toks) for j in range(ids.shape[1]) if ids[t, j] == e]
+        if not users:
+            continue
+        w1e, w2e = {e: to_np(w1[e]).astype(np.float64)}, {e: to_np(w2[e]).astype(np.float64)}
+        for i, t, j in users:
+            ref[i] += fused_moe_token(xs[t], w1e, w2e, [e], [wts[t, j]])
+        del w1e, w2e
+    assert_close(to_np(out[torch.as_tensor(toks, device=DEV)]), ref, 2e-2, "mixtral routed layer")

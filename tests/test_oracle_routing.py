@@ -181,3 +181,22 @@ def test_topk_softmax_against_torch_and_by_hand():
     w2, i2 = topk_softmax(h, 3, False)
     assert i2.tolist() == [[1, 2, 0]]
     assert np.allclose(w2, [[3 / 8, 3 / 8, 1 / 8]], rtol=1e-14)
+
+
+def test_fused_moe_token_matches_the_composed_layer():
+    # the per-token form against align + fused_moe_gemm + silu_and_mul +
+    # fused_moe_gemm (weighted) + sum over the top-k entries
+    from oracle.routing import fused_moe_gemm, fused_moe_token, silu_and_mul
+    rng = np.random.default_rng(11)
+    T, k, E, H, F = 20, 2, 5, 12, 8
+    x = rng.standard_normal((T, H))
+    w1 = rng.standard_normal((E, 2 * F, H))
+    w2 = rng.standard_normal((E, H, F))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    wts = rng.random((T, k))
+    sid, eid, tot, _ = moe_align_block_size(ids, 4, E)
+    c1 = fused_moe_gemm(x, w1, sid, eid, tot, T * k, k, 4)
+    c3 = fused_moe_gemm(silu_and_mul(c1), w2, sid, eid, tot, T * k, 1, 4, topk_weights=wts.ravel())
+    layer = c3.reshape(T, k, H).sum(axis=1)
+    for t in range(T):
+        assert np.allclose(fused_moe_token(x[t], w1, w2, ids[t], wts[t]), layer[t], rtol=1e-12, atol=1e-12)
