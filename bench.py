@@ -334,9 +334,34 @@ def routed_layer(torch, B, dev, pk, d):
     routed = T * tid.shape[1]
     flop = 2 * routed * H * 2 * F + 2 * routed * F * H
     tf = flop / (t["p50_us"] * 1e-6) / 1e12
-    return {"what": "moe.fused_experts(x, w1, w2, topk_weights, topk_ids), all steps on the device",
-            "p50_us": round(t["p50_us"], 1), "tflops_routed_rows": round(tf, 1),
-            "tensor_frac_routed": round(tf / pk["bf16_tflops"], 3)}
+    res = {"what": "moe.fused_experts(x, w1, w2, topk_weights, topk_ids), all steps on the device",
+           "p50_us": round(t["p50_us"], 1), "tflops_routed_rows": round(tf, 1),
+           "tensor_frac_routed": round(tf / pk["bf16_tflops"], 3)}
+    # decode-size batches of the whole layer from gating logits (routing included),
+    # replayed from a CUDA graph: the weights of the touched experts against HBM
+    dec = []
+    for Td in (1, 4, 16, 64):
+        xd = torch.randn(Td, H, generator=g, device=dev).to(torch.bfloat16)
+        gd = torch.randn(Td, E, generator=g, device=dev)
+        f = lambda: moe.fused_moe(xd, w1, w2, gd, 2, True)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                f()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            f()
+        td = time_events(torch, graph.replay, 20)
+        _, tidd = moe.route(gd, 2, True)
+        touched = int((torch.bincount(tidd.view(-1).long(), minlength=E) > 0).sum())
+        wb = touched * 3 * F * H * 2
+        dec.append({"tokens": Td, "experts_touched": touched, "p50_us": round(td["p50_us"], 1),
+                    "hbm_frac": round(wb / (td["p50_us"] * 1e-6) / 1e9 / pk["hbm_gbs"], 3)})
+    res["decode_graph"] = dec
+    return res
 
 
 def cpu_baseline_grin(seconds=10.0):

@@ -147,9 +147,11 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   // stage): bf16 with w [E, K, N] in one box per stage, when the weights
   // stream (at most 256 rows per expert on average, so HBM bounds the launch)
   const bool allow192 = !fp8 && !trans_b && N % 64 == 0 && M <= 256 * (int64_t)E;
-  int bn = pair ? choose_bn_units(pair_tiles_estimate(M, E), N, sms / 2)
-                : choose_bn(rows_tiles_estimate(M, E), N, allow192);
   const bool gated = gate_rows > 0;
+  // routed rows (the gated and scattered forms) come in groups padded to 128,
+  // so M / 128 bounds their row tiles; plain groups may add one partial tile each
+  const int64_t row_tiles = gated || row_map ? (M + 127) / 128 : rows_tiles_estimate(M, E);
+  int bn = pair ? choose_bn_units(pair_tiles_estimate(M, E), N, sms / 2) : choose_bn(row_tiles, N, allow192);
   if (gated) bn = bn > 128 ? 256 : 128;  // gate and up halves of whole 64-column chunks
   const int out_cols = gated ? gate_rows : N;
   const int tile_cols = gated ? bn / 2 : bn;

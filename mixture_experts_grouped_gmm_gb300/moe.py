@@ -89,16 +89,19 @@ def fused_experts(hidden_states, w1, w2, topk_weights, topk_ids):
     dev = x.device
     sorted_ids, _, npp, gs = align(topk_ids, E)
     cap = sorted_ids.numel()
+    # rows the GEMMs may see: every entry, plus the padding of at most
+    # min(E, n) experts (a bound known on the host; it sizes their tiles)
+    rows = min(cap, n + min(E, n) * (BLOCK - 1))
     args = torch.empty(B.mgemm_args_bytes(E), dtype=torch.uint8, device=dev)
     B.mgemm_fill_args(gs, E, -1, args)
     bf = torch.bfloat16
     a1 = torch.empty(cap, H, dtype=bf, device=dev)
     B.mgemm_gather_rows(x, sorted_ids, npp, n, top_k, a1)
     a2 = torch.empty(cap, F, dtype=bf, device=dev)  # rows past the padded total are never read
-    B.mgemm_fwd_gated(args, a1, w1, a2, cap, H, F, E)
+    B.mgemm_fwd_gated(args, a1, w1, a2, rows, H, F, E)
     c3 = torch.empty(n, H, dtype=bf, device=dev)
     wts = topk_weights.to(torch.float32).contiguous().view(-1)
-    B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a2, w2, c3, sorted_ids, n, wts, cap, F, H, E)
+    B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a2, w2, c3, sorted_ids, n, wts, rows, F, H, E)
     out = torch.empty(T, H, dtype=bf, device=dev)
     B.mgemm_topk_sum(c3, T, top_k, out)
     return out

@@ -157,14 +157,16 @@ def topk_softmax(gating_output, top_k, renormalize):
 def fused_moe_token(x_row, w1, w2, expert_ids, weights):
     """One token's output of the fused_moe layer, float64: the sum over its
     top-k entries (expert e, routed weight a) of
-    a * silu_and_mul(x . w1[e]^T) . w2[e]^T, with w1 [E, 2F, H] and w2 [E, H, F].
+    a * silu_and_mul(x . w1[e]^T) . w2[e]^T, with w1[e] [2F, H] and w2[e] [H, F]
+    (w1, w2: arrays [E, ...] or mappings from expert id to its matrix).
     What fused_moe computes for that token, without the rest of the batch."""
     import numpy as np
 
     x = np.asarray(x_row, dtype=np.float64)
-    out = np.zeros(np.asarray(w2).shape[1])
+    out = None
     for e, a in zip(expert_ids, weights):
         up = np.asarray(w1[int(e)], dtype=np.float64) @ x
         h = silu_and_mul(up[None, :])[0]
-        out += float(a) * (np.asarray(w2[int(e)], dtype=np.float64) @ h)
+        y = float(a) * (np.asarray(w2[int(e)], dtype=np.float64) @ h)
+        out = y if out is None else out + y
     return out
