@@ -191,3 +191,24 @@ def test_fwd_gated_against_oracle(sizes, K, F):
     assert is_sentinel(out[M:]), "wrote past M rows"
     ref = R.silu_and_mul(og.gmm_fwd(to_np(x), to_np(w), sizes, trans_b=True))
     assert_close(to_np(out[:M]), ref, BF16_TOL, "fwd_gated")
+
+
+@pytest.mark.parametrize("T,k,E,H,F,renorm", [
+    (1, 2, 8, 128, 128, True),     # one token
+    (37, 4, 4, 128, 256, True),    # top_k = E: every token in every expert
+    (50, 1, 1, 256, 128, False),   # one expert, top-1, no renormalization
+    (9, 3, 16, 136, 200, True),    # H, F not multiples of the 64-element k-block
+])
+def test_fused_moe_edges(T, k, E, H, F, renorm):
+    from mixture_experts_grouped_gmm_gb300 import moe
+
+    torch.manual_seed(T * 7 + E)
+    x = torch.randn(T, H, device=DEV).to(BF)
+    w1 = (0.05 * torch.randn(E, 2 * F, H, device=DEV)).to(BF)
+    w2 = (0.05 * torch.randn(E, H, F, device=DEV)).to(BF)
+    gating = torch.randn(T, E, device=DEV)
+    out = moe.fused_moe(x, w1, w2, gating, k, renorm)
+    torch.cuda.synchronize()
+    tw, tid = R.topk_softmax(gating.cpu().numpy(), k, renorm)
+    ref = np.stack([R.fused_moe_token(to_np(x)[t], to_np(w1), to_np(w2), tid[t], tw[t]) for t in range(T)])
+    assert_close(to_np(out), ref, 2e-2, "fused_moe edge case")
