@@ -15,7 +15,8 @@
 //            of 256-row x 64-column boxes, over (group, tensor, column-block)
 //            items in order of decreasing group size; 16 consumer warps read
 //            the boxes with transposing ldmatrix, reduce the column magnitude
-//            max (pass 1), then convert two rows of one column per e4m3x2
+//            max (pass 1; the first 8 boxes are parked in tensor memory),
+//            then convert two rows of one column per e4m3x2
 //            conversion so the codes come out column-major (pass 2), stage
 //            them in shared memory, and write them with TMA tensor stores,
 //            each column's bytes contiguous.
@@ -126,9 +127,12 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 //            that tile out with TMA tensor stores while the next box is
 //            converted into the other tile.  Rows past the
 //            group are cleared before the cast, so the padding of every
-//            column is written as zero codes.  A group spanning at most 5
-//            boxes stays in the ring between the passes instead of being
-//            reloaded.
+//            column is written as zero codes.  Between the passes the
+//            first 8 boxes of an item wait in tensor memory (each warp parks
+//            its 16 registers per box with tcgen05.st and reads them back in
+//            pass 2), so every ring slot is freed right after pass 1 and the
+//            loads of the next item stream meanwhile; boxes past the 8th are
+//            read again, newest first.
 // Output: the padded column-major layout -- column c of group g starts at
 // out[c * ld + poffsets[g]] (poffsets from the args block), m_g codes then
 // zeros up to a multiple of kColPad; every start is 128-byte aligned, so the
@@ -144,6 +148,12 @@ constexpr int kCwThreads = (kCwConsumers + 1) * 32;
 constexpr int kCwBox = kCwRows * 128;   // 32 KB
 constexpr int kCwTile = 64 * kCwRows;   // transposed tile: 2 halves of [64 columns][128 rows] codes
 constexpr int kCwQueue = 4;  // item ids handed from the producer to the consumers
+// Between the two passes the first kCwPark boxes of an item wait in tensor
+// memory (16 columns per consumer warp per box: 8 boxes fill 512 columns), so
+// every ring slot is freed as soon as pass 1 has read it; later boxes are read
+// again.
+constexpr int kCwPark = 8;
+constexpr int kCwTmemCols = 512;
 constexpr size_t kCwSmemFixed = 1024 + (size_t)kCwStages * kCwBox + 2 * kCwTile + 2 * 2 * 64 * 4 + 256;
 // plus a copy of the group offsets, the padded offsets and the size order: 16 (E + 1) + 4 E bytes
 __host__ __device__ constexpr size_t cw_smem_bytes(int E) {
@@ -248,6 +258,7 @@ __global__ void __launch_bounds__(kCwThreads, 1)
   uint64_t *qempty = qfull + kCwQueue;
   int *abort_flag = reinterpret_cast<int *>(qempty + kCwQueue);
   int *s_item = abort_flag + 1;  // [kCwQueue]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_item + kCwQueue);
   int64_t *s_off = reinterpret_cast<int64_t *>(smem + (kCwSmemFixed - 1024));  // [E + 1]
   int64_t *s_poff = s_off + E + 1;                                              // [E + 1]
   int *s_order = reinterpret_cast<int *>(s_poff + E + 1);                     // [E]
@@ -272,7 +283,14 @@ __global__ void __launch_bounds__(kCwThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kCwTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
   volatile int *vabort = abort_flag;
   uint32_t issued = 0;
 
@@ -307,21 +325,21 @@ __global__ void __launch_bounds__(kCwThreads, 1)
         if (done) break;
         const CwItem it = cw_decode(item, s_off, s_poff, s_order, t1, t2);
         const CUtensorMap *tm = it.tensor == 0 ? &tm1 : &tm2;
-        const int passes = it.nck <= kCwStages ? 1 : 2;
-        for (int pass = 0; pass < passes && !*vabort; ++pass) {
-          for (int k = 0; k < it.nck; ++k) {
-            if (!mbar_wait(&empty[stage], phase ^ 1, vabort)) {
-              set_status(av.status, MGEMM_STATUS_TIMEOUT);
-              *vabort = 1;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[stage], kCwBox);
-            ++issued;
-            tma_load_2d(ring + stage * kCwBox, tm, &full[stage], it.cb * 64, (int)(it.rs + (int64_t)k * kCwRows));
-            if (++stage == kCwStages) {
-              stage = 0;
-              phase ^= 1;
-            }
+        // every box, then again, newest first, those not parked in tensor memory
+        const int parked = it.nck < kCwPark ? it.nck : kCwPark;
+        for (int i = 0; i < 2 * it.nck - parked && !*vabort; ++i) {
+          const int k = i < it.nck ? i : it.nck - 1 - (i - it.nck);
+          if (!mbar_wait(&empty[stage], phase ^ 1, vabort)) {
+            set_status(av.status, MGEMM_STATUS_TIMEOUT);
+            *vabort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kCwBox);
+          ++issued;
+          tma_load_2d(ring + stage * kCwBox, tm, &full[stage], it.cb * 64, (int)(it.rs + (int64_t)k * kCwRows));
+          if (++stage == kCwStages) {
+            stage = 0;
+            phase ^= 1;
           }
         }
       }
@@ -371,41 +389,55 @@ __global__ void __launch_bounds__(kCwThreads, 1)
           T.sc[(int64_t)it.g * T.C + col0 + lcol] = pow2_scale_from_amax(0.f);
         continue;
       }
-      const bool resident = it.nck <= kCwStages;
-      const int s0 = stage;
-      const uint32_t p0 = phase;
+      const int parked = it.nck < kCwPark ? it.nck : kCwPark;  // boxes 0 .. parked - 1 wait in TMEM
       float *red_i = red + item_par * 128;
       item_par ^= 1;
-      // pass 1: magnitude max of column lcol over this warp's rows; only the
-      // boxes at the group's two ends hold rows of other groups
-      uint32_t am = 0u;
-      for (int k = 0; k < it.nck; ++k) {
-        wait_full();
+      // this warp's 16 columns of TMEM slot k (its lane quarter is warp % 4)
+      auto slot_addr = [&](int k) -> uint32_t {
+        return tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(k * 64 + (warp >> 2) * 16);
+      };
+      // This lane's 16 values of box k (the ring stage at hand): ldmatrix j,
+      // matrix m give rows r0 + 32 j + 8 m + rpair (low half) and + 1 (high
+      // half) of column lcol; rows past the group are cleared (only the boxes
+      // at the group's two ends hold rows of other groups).
+      auto read_box = [&](int k, uint32_t (&v)[16]) {
         const uint8_t *box = ring + stage * kCwBox;
         const int64_t r0 = it.rs + (int64_t)k * kCwRows + rhalf * 128;
         const bool edge = it.rs + (int64_t)(k + 1) * kCwRows > it.re;  // the box runs past the group
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint32_t v[4];
-          ldsm_x4_trans(row_addr(box, j), v);
+          uint32_t w[4];
+          ldsm_x4_trans(row_addr(box, j), w);
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
-            uint32_t x = v[m];
+            uint32_t x = w[m];
             if (edge) {
-              const int64_t gr = r0 + j * 32 + m * 8 + rpair;  // rows gr (low half), gr + 1 (high half)
+              const int64_t gr = r0 + j * 32 + m * 8 + rpair;
               if (gr >= it.re) x &= 0xFFFF0000u;
               if (gr + 1 >= it.re) x &= 0x0000FFFFu;
             }
-            am = bf16x2_absmax(am, x);
+            v[4 * j + m] = x;
           }
         }
+      };
+      // pass 1: magnitude max of column lcol over this warp's rows; the first
+      // kCwPark boxes are parked in TMEM, and every ring slot is freed at once
+      uint32_t am = 0u;
+      for (int k = 0; k < it.nck; ++k) {
+        wait_full();
+        uint32_t v[16];
+        read_box(k, v);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) am = bf16x2_absmax(am, v[r]);
+        if (k < parked) tmem_st_32x32b_x16(slot_addr(k), v);
         __syncwarp();
-        if (!resident && lane == 0) mbar_arrive(&empty[stage]);
+        if (lane == 0) mbar_arrive(&empty[stage]);
         if (++stage == kCwStages) {
           stage = 0;
           phase ^= 1;
         }
       }
+      tmem_st_wait();  // this thread's parked boxes are in TMEM before pass 2 reads them
       am = bf16x2_absmax(am, __shfl_xor_sync(0xffffffffu, am, 1));
       am = bf16x2_absmax(am, __shfl_xor_sync(0xffffffffu, am, 2));
       am &= 0x7FFF7FFFu;
@@ -415,44 +447,43 @@ __global__ void __launch_bounds__(kCwThreads, 1)
       if (rhalf == 0 && (lane & 3) == 0 && col0 + lcol < T.C) T.sc[(int64_t)it.g * T.C + col0 + lcol] = sc;
       const uint64_t sc2 = ((uint64_t)__float_as_uint(sc) << 32) | __float_as_uint(sc);
       // pass 2: box k is converted into one tile while the stores of the
-      // previous box drain from the other; one consumer barrier per box
-      if (resident) {
-        stage = s0;
-        phase = p0;
-      }
+      // previous box drain from the other; one consumer barrier per box.  The
+      // parked boxes come from TMEM, the rest from the ring, newest first, in
+      // the order the producer loads them again.
       bool aborted = false;
-      for (int k = 0; k < it.nck; ++k) {
-        if (!resident) wait_full();
-        const uint8_t *box = ring + stage * kCwBox;
+      for (int i = 0; i < it.nck; ++i) {
+        const bool from_tmem = i < parked;
+        const int k = from_tmem ? i : it.nck - 1 - (i - parked);
+        uint32_t v[16];
+        if (from_tmem) {
+          tmem_ld_32x32b_x16(slot_addr(k), v);
+          tmem_ld_wait();
+        } else {
+          wait_full();
+          read_box(k, v);
+        }
         uint8_t *tile = tiles + tile_par * kCwTile;
         tile_par ^= 1;
         uint8_t *tcol = tile + rhalf * (kCwTile / 2) + lcol * 128 + rpair;
-        // rows past the group become zero codes: the padding of the column
-        const int64_t r0 = it.rs + (int64_t)k * kCwRows + rhalf * 128;
-        const bool edge = it.rs + (int64_t)(k + 1) * kCwRows > it.re;
+        // rows past the group were cleared: the padding of the column gets zero codes
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint32_t v[4];
-          ldsm_x4_trans(row_addr(box, j), v);
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
-            uint32_t x = v[m];
-            if (edge) {
-              const int64_t gr = r0 + j * 32 + m * 8 + rpair;
-              if (gr >= it.re) x &= 0xFFFF0000u;
-              if (gr + 1 >= it.re) x &= 0x0000FFFFu;
-            }
             // rows j*32 + m*8 + rpair, +1 of the half: chunk 2j + m/2, byte 8 (m & 1) + rpair
             const uint32_t chunk = (uint32_t)(2 * j + (m >> 1)) ^ tsw;
-            *reinterpret_cast<uint16_t *>(tcol + chunk * 16 + (m & 1) * 8) = bf16x2_scaled_e4m3x2(x, sc2);
+            *reinterpret_cast<uint16_t *>(tcol + chunk * 16 + (m & 1) * 8) =
+                bf16x2_scaled_e4m3x2(v[4 * j + m], sc2);
           }
         }
         fence_proxy_async_smem();  // the codes are read by the tensor store below
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);  // box consumed; the codes live in the tile
-        if (++stage == kCwStages) {
-          stage = 0;
-          phase ^= 1;
+        if (!from_tmem) {
+          if (lane == 0) mbar_arrive(&empty[stage]);  // box consumed; the codes live in the tile
+          if (++stage == kCwStages) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
         // The tile written next was last stored two boxes ago: its store has
         // finished reading before any warp passes this barrier.
@@ -477,14 +508,20 @@ __global__ void __launch_bounds__(kCwThreads, 1)
       }
       if (aborted) break;
     }
+    tmem_st_wait();
     if (threadIdx.x == 0) bulk_wait_all();  // the tensor stores are complete before the CTA leaves
   }
+  tc_fence_before();
   __syncthreads();
   if (*vabort && warp == kCwConsumers && lane == 0) {
     for (int s = 0; s < kCwStages; ++s) {  // wait for this CTA's copies in flight, bounded
       const uint32_t armed = issued / kCwStages + ((uint32_t)s < issued % kCwStages ? 1u : 0u);
       if (armed) mbar_wait(&full[s], (armed - 1) & 1, nullptr);
     }
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kCwTmemCols);
   }
 }
 
