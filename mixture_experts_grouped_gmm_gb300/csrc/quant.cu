@@ -11,7 +11,7 @@
 //   rowwise: one warp per row; a row of up to 24*256 elements stays in
 //            registers between the amax and the cast, so it is read once.
 //            Longer rows take a second pass (served by L2).
-//   colwise: persistent CTAs (one per SM) fed by TMA through a 5-stage ring
+//   colwise: persistent CTAs (one per SM) fed by TMA through a 6-stage ring
 //            of 256-row x 64-column boxes, over (group, tensor, column-block)
 //            items in order of decreasing group size; 16 consumer warps read
 //            the boxes with transposing ldmatrix, reduce the column magnitude
@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 // in the args block (dynamic scheduling keeps the CTAs balanced when group
 // sizes are skewed).
 //   warp 16 (one thread): streams boxes of 256 rows x 64 columns (32 KB,
-//            128-byte swizzle) of the item's column block through a 5-stage
-//            ring (160 KB of loads in flight per SM), running ahead across
+//            128-byte swizzle) of the item's column block through a 6-stage
+//            ring (192 KB of loads in flight per SM), running ahead across
 //            items.  Boxes start at the group's first row and cover its rows
 //            rounded up to kColPad (the padded length of its output column).
 //   warps 0-15: warp w owns columns 8*(w % 8) .. +7 and rows 128*(w / 8) ..
@@ -137,12 +137,11 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 // out[c * ld + poffsets[g]] (poffsets from the args block), m_g codes then
 // zeros up to a multiple of kColPad; every start is 128-byte aligned, so the
 // FP8 wgrad reads whole, aligned 128-row blocks of every group.
-// The CTA first copies the group offsets, padded offsets and the size order
-// into shared memory.  Consumer warps synchronize with a hardware barrier (see
+// Consumer warps synchronize with a hardware barrier (see
 // cw_consumer_barrier_any); every pipeline wait is bounded and gives up after about
 // 1 s with MGEMM_STATUS_TIMEOUT.
 constexpr int kCwRows = 256;
-constexpr int kCwStages = 5;
+constexpr int kCwStages = 6;
 constexpr int kCwConsumers = 16;
 constexpr int kCwThreads = (kCwConsumers + 1) * 32;
 constexpr int kCwBox = kCwRows * 128;   // 32 KB
@@ -155,10 +154,10 @@ constexpr int kCwQueue = 4;  // item ids handed from the producer to the consume
 constexpr int kCwPark = 8;
 constexpr int kCwTmemCols = 512;
 constexpr size_t kCwSmemFixed = 1024 + (size_t)kCwStages * kCwBox + 2 * kCwTile + 2 * 2 * 64 * 4 + 256;
-// plus a copy of the group offsets, the padded offsets and the size order: 16 (E + 1) + 4 E bytes
-__host__ __device__ constexpr size_t cw_smem_bytes(int E) {
-  return kCwSmemFixed + 16 * (size_t)(E + 1) + 4 * (size_t)E + 16;
-}
+static_assert(kCwSmemFixed <= 227 * 1024, "the ring, tiles and barriers fit one CTA's shared memory");
+// (the group offsets, padded offsets and size order are read from the args
+// block through the read-only cache, once per item)
+__host__ __device__ constexpr size_t cw_smem_bytes(int) { return kCwSmemFixed; }
 
 struct ColTensor {
   uint8_t *out;
@@ -178,14 +177,14 @@ __device__ __forceinline__ CwItem cw_decode(int item, const int64_t *off, const 
                                             const ColTensor &t1, const ColTensor &t2) {
   CwItem it;
   const int per_group = t1.ncb + t2.ncb;
-  it.g = order[item / per_group];
+  it.g = __ldg(order + item / per_group);
   const int cb = item % per_group;
   it.tensor = cb < t1.ncb ? 0 : 1;
   it.cb = it.tensor == 0 ? cb : cb - t1.ncb;
-  it.rs = off[it.g];
-  it.re = off[it.g + 1];
+  it.rs = __ldg(off + it.g);
+  it.re = __ldg(off + it.g + 1);
   it.plen = (it.re - it.rs + kColPad - 1) / kColPad * kColPad;
-  it.pos = poff[it.g];
+  it.pos = __ldg(poff + it.g);
   it.nck = (int)((it.plen + kCwRows - 1) / kCwRows);
   return it;
 }
@@ -259,18 +258,10 @@ __global__ void __launch_bounds__(kCwThreads, 1)
   int *abort_flag = reinterpret_cast<int *>(qempty + kCwQueue);
   int *s_item = abort_flag + 1;  // [kCwQueue]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_item + kCwQueue);
-  int64_t *s_off = reinterpret_cast<int64_t *>(smem + (kCwSmemFixed - 1024));  // [E + 1]
-  int64_t *s_poff = s_off + E + 1;                                              // [E + 1]
-  int *s_order = reinterpret_cast<int *>(s_poff + E + 1);                     // [E]
 
   const ArgsView av(args, E);
   if (*av.status != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
-    s_off[i] = av.offsets[i];
-    s_poff[i] = av.poffsets[i];
-  }
-  for (int i = threadIdx.x; i < E; i += blockDim.x) s_order[i] = av.wgrad_order[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kCwStages; ++s) {
       mbar_init(&full[s], 1);
@@ -323,7 +314,7 @@ __global__ void __launch_bounds__(kCwThreads, 1)
           qphase ^= 1;
         }
         if (done) break;
-        const CwItem it = cw_decode(item, s_off, s_poff, s_order, t1, t2);
+        const CwItem it = cw_decode(item, av.offsets, av.poffsets, av.wgrad_order, t1, t2);
         const CUtensorMap *tm = it.tensor == 0 ? &tm1 : &tm2;
         // every box, then again, newest first, those not parked in tensor memory
         const int parked = it.nck < kCwPark ? it.nck : kCwPark;
@@ -381,7 +372,7 @@ __global__ void __launch_bounds__(kCwThreads, 1)
         qphase ^= 1;
       }
       if (cw_consumer_barrier_any(item < 0 || *vabort != 0)) break;
-      const CwItem it = cw_decode(item, s_off, s_poff, s_order, t1, t2);
+      const CwItem it = cw_decode(item, av.offsets, av.poffsets, av.wgrad_order, t1, t2);
       const ColTensor &T = it.tensor == 0 ? t1 : t2;
       const int64_t col0 = (int64_t)it.cb * 64;
       if (it.nck == 0) {  // empty group: amax 0 -> scale 2^48, no data
