@@ -123,9 +123,10 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 //            each register with one packed fp32 multiply and converts it to an
 //            e4m3 pair that is already in column-major order, stores it as 16
 //            bits into one of two tiles (two [64 columns][128 rows] halves,
-//            16-byte chunks swizzled by the column), and one thread writes
-//            that tile out with TMA tensor stores while the next box is
-//            converted into the other tile.  Rows past the
+//            16-byte chunks swizzled by the column); each warp's 8 columns x
+//            128 rows form a 1 KB block of the tile, which the warp writes out
+//            with its own TMA tensor store while it converts the next box into
+//            the other tile -- no CTA-wide barrier per box.  Rows past the
 //            group are cleared before the cast, so the padding of every
 //            column is written as zero codes.  Between the passes the
 //            first 8 boxes of an item wait in tensor memory (each warp parks
@@ -441,7 +442,6 @@ __global__ void __launch_bounds__(kCwThreads, 1)
       // previous box drain from the other; one consumer barrier per box.  The
       // parked boxes come from TMEM, the rest from the ring, newest first, in
       // the order the producer loads them again.
-      bool aborted = false;
       for (int i = 0; i < it.nck; ++i) {
         const bool from_tmem = i < parked;
         const int k = from_tmem ? i : it.nck - 1 - (i - parked);
@@ -455,7 +455,12 @@ __global__ void __launch_bounds__(kCwThreads, 1)
         }
         uint8_t *tile = tiles + tile_par * kCwTile;
         tile_par ^= 1;
-        uint8_t *tcol = tile + rhalf * (kCwTile / 2) + lcol * 128 + rpair;
+        // this warp's block of the tile: its 8 columns x 128 rows (1 KB); the
+        // store that read it two boxes ago has finished reading it
+        uint8_t *wblk = tile + rhalf * (kCwTile / 2) + cc * 1024;
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        uint8_t *tcol = wblk + (lane >> 2) * 128 + rpair;
         // rows past the group were cleared: the padding of the column gets zero codes
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -476,31 +481,23 @@ __global__ void __launch_bounds__(kCwThreads, 1)
             phase ^= 1;
           }
         }
-        // The tile written next was last stored two boxes ago: its store has
-        // finished reading before any warp passes this barrier.
-        if (threadIdx.x == 0) bulk_wait_read<0>();
-        if (cw_consumer_barrier_any(*vabort != 0)) {
-          aborted = true;
-          break;
-        }
-        // one thread stores the box's halves that hold rows of the group's
-        // padded length (a multiple of 128): [64 columns][128 rows] each, to
-        // rows pos + 256 k + 128 h of columns col0 .. col0 + 63 (the map clips
-        // the columns past C)
-        if (threadIdx.x == 0) {
-          const CUtensorMap *tmo = it.tensor == 0 ? &tmo1 : &tmo2;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t q = (int64_t)k * kCwRows + h * 128;
-            if (q < it.plen) tma_store_2d(tmo, tile + h * (kCwTile / 2), (int)(it.pos + q), (int)col0);
-          }
+        // the warp stores its own block: [8 columns][128 rows] to rows
+        // pos + 256 k + 128 rhalf of columns col0 + 8 cc .. (only halves inside
+        // the group's padded length, a multiple of 128; the map clips columns
+        // past C).  No CTA barrier: a wait that gave up lets every warp run on
+        // to the next item's barrier, where they all leave together.
+        // (one bulk group per box, empty when there is nothing to store, so
+        // "at most one group pending" always means the store of the last box)
+        const int64_t q = (int64_t)k * kCwRows + rhalf * 128;
+        if (lane == 0) {
+          if (q < it.plen && col0 + cc * 8 < T.C)
+            tma_store_2d(it.tensor == 0 ? &tmo1 : &tmo2, wblk, (int)(it.pos + q), (int)(col0 + cc * 8));
           bulk_commit();
         }
       }
-      if (aborted) break;
     }
     tmem_st_wait();
-    if (threadIdx.x == 0) bulk_wait_all();  // the tensor stores are complete before the CTA leaves
+    if (lane == 0) bulk_wait_all();  // the warp's tensor stores are complete before the CTA leaves
   }
   tc_fence_before();
   __syncthreads();
@@ -586,18 +583,18 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
     tm2 = tm1;
   }
   // the outputs: column c of the padded layout is row c of a [C][ld] byte
-  // matrix; boxes of 64 columns x 128 rows (bytes)
+  // matrix; boxes of 8 columns x 128 rows (bytes): one consumer warp's block
   CUtensorMap tmo1, tmo2;
   {
     const uint64_t d[2] = {(uint64_t)ld, (uint64_t)C1};
     const uint64_t st[1] = {(uint64_t)ld};
-    const uint32_t box[2] = {128, 64};
+    const uint32_t box[2] = {128, 8};
     if (!make_tensor_map(&tmo1, true, 2, out1, d, st, box)) return MGEMM_ECUDA;
   }
   if (in2) {
     const uint64_t d[2] = {(uint64_t)ld, (uint64_t)C2};
     const uint64_t st[1] = {(uint64_t)ld};
-    const uint32_t box[2] = {128, 64};
+    const uint32_t box[2] = {128, 8};
     if (!make_tensor_map(&tmo2, true, 2, out2, d, st, box)) return MGEMM_ECUDA;
   } else {
     tmo2 = tmo1;
