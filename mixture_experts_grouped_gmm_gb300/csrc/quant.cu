@@ -160,8 +160,7 @@ static_assert(kCwSmemFixed <= 227 * 1024, "the ring, tiles and barriers fit one 
 // block through the read-only cache, once per item)
 __host__ __device__ constexpr size_t cw_smem_bytes(int) { return kCwSmemFixed; }
 
-struct ColTensor {
-  uint8_t *out;
+struct ColTensor {  // (the codes go out through the tensor maps)
   float *sc;
   int64_t C;
   int ncb;  // 64-column blocks
@@ -599,8 +598,8 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
   } else {
     tmo2 = tmo1;
   }
-  ColTensor t1{out1, sc1, C1, (int)((C1 + 63) / 64)};
-  ColTensor t2{out2, sc2, in2 ? C2 : 0, in2 ? (int)((C2 + 63) / 64) : 0};
+  ColTensor t1{sc1, C1, (int)((C1 + 63) / 64)};
+  ColTensor t2{sc2, in2 ? C2 : 0, in2 ? (int)((C2 + 63) / 64) : 0};
   const int64_t items = (int64_t)E * (t1.ncb + t2.ncb);
   if (items >= (int64_t(1) << 31)) return MGEMM_EINVAL;
   const int sms = sm_count_cached();
