@@ -459,11 +459,7 @@ def run_ours(a):
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier()
-    ms = t_start.elapsed_time(t_end) / a.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end) / a.steps, world, dist, dev)
     # status after the timed region (sync point outside timing)
     assert B.args_status(st.args) == 0
 
@@ -497,7 +493,7 @@ def run_ours(a):
                 traffic = ent.get("dram_bytes_per_launch")
         except Exception:
             traffic = None
-    value = world * FLOP_STEP / (ms * 1e-3) / 1e12
+    value = job_tflops(world, FLOP_STEP, ms)
 
     line = {"metric": "grouped-GEMM TFLOP/s (GRIN-MoE gmm fwd+bwd)", "value": round(value, 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
@@ -534,12 +530,8 @@ def run_ours(a):
         for _ in range(e2e_steps):
             e2e_step()
         torch.cuda.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-        if world > 1:
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
-        line["e2e"] = {"value": round(world * FLOP_STEP / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, world, dist, dev)
+        line["e2e"] = {"value": round(job_tflops(world, FLOP_STEP, e2e_ms), 2), "unit": "TFLOP/s",
                        "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                        "h2d_bytes_per_step": xh.numel() * 2 + wh.numel() * 2 + gh.numel() * 8,
                        "d2h_bytes_per_step": 4,
@@ -562,6 +554,23 @@ def run_ours(a):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def max_over_ranks(value, world, dist, device):
+    """The largest of every rank's value (the job's time is its slowest
+    rank's); the value itself with one rank."""
+    if world <= 1:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flop_per_rank_step, ms_per_step):
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return world * flop_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
 def run_reference(a):
