@@ -165,6 +165,18 @@ __device__ __forceinline__ int total_tiles(const GemmParams &p, const ArgsView &
   return p.E * p.mt_k * p.n_tiles;
 }
 
+// The j-th tile of the CTA (or pair) c of P: round j covers tiles j P ..
+// j P + P - 1.  For wgrad (tiles of an expert cost in proportion to its rows,
+// experts in decreasing size) odd rounds run backwards, so the CTA that took
+// the costliest tile of one round takes the cheapest of the next (static
+// round-robin left the DeepSeek wgrad ~10% longer than balanced; this order
+// ~2%).  Row tiles all cost the same and keep the plain order.
+template <class C>
+__device__ __forceinline__ int tile_of(int j, int c, int P) {
+  if (C::Mode == kModeExperts && (j & 1)) return j * P + (P - 1 - c);
+  return j * P + c;
+}
+
 template <class C>
 __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, const ArgsView &av, uint32_t rank) {
   TileInfo ti;
@@ -364,7 +376,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // pair: the leader's full barrier counts the bytes of both CTAs
       const uint32_t tx = C::Pair ? 2u * (uint32_t)(C::A_BYTES + (bn / 2) * 128)
                                   : C::KC * ((C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128);
-      for (int t = t_first; t < total && !*vabort; t += t_step) {
+      for (int j = 0; j * t_step < total && !*vabort; ++j) {
+        const int t = tile_of<C>(j, t_first, t_step);
+        if (t >= total) continue;
         const TileInfo ti = decode_tile<C>(t, p, av, rank);
         for (int kb = 0; kb < ti.kb_count; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, vabort)) {
@@ -449,8 +463,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
     // pair: only the leader issues MMAs (for both CTAs); the peer's warp 1 only owns its TMEM
-    const int t_mma = (!C::Pair || leader) ? t_first : total;
-    for (int t = t_mma; t < total && ok; t += t_step) {
+    const bool issues = !C::Pair || leader;
+    for (int j = 0; issues && j * t_step < total && ok; ++j) {
+      const int t = tile_of<C>(j, t_first, t_step);
+      if (t >= total) continue;
       const TileInfo ti = decode_tile<C>(t, p, av, rank);
       if (ti.kb_count == 0) continue;
       if (!mbar_wait_warp(&tempty[acc], acc_phase ^ 1, vabort)) { ok = false; break; }
@@ -601,7 +617,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
     };
     load_scales(t_first);
-    for (int t = t_first; t < total; t += t_step) {
+    for (int j = 0; j * t_step < total; ++j) {
+      const int t = tile_of<C>(j, t_first, t_step);
+      if (t >= total) continue;
       const TileInfo ti = decode_tile<C>(t, p, av, rank);
       const bool has_acc = ti.kb_count > 0;
       bool row_ok = r < ti.out_rows;
@@ -623,7 +641,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         rinv = rinv_next;
 #pragma unroll
         for (int i = 0; i < 2 * kCpw; ++i) csr[i] = csr_next[i];
-        load_scales(t + t_step);
+        load_scales(tile_of<C>(j + 1, t_first, t_step));
       }
       if (has_acc) {
         if (!mbar_wait_warp(&tfull[acc], acc_phase, vabort)) {
