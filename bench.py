@@ -462,6 +462,29 @@ def run_ours(a):
     ms = max_over_ranks(t_start.elapsed_time(t_end) / a.steps, world, dist, dev)
     # status after the timed region (sync point outside timing)
     assert B.args_status(st.args) == 0
+    # the same step captured once in a CUDA graph and replayed: no call reads
+    # anything on the host, so the replays run back to back
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        st.run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph):
+        st.run()
+    for _ in range(3):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record()
+    for _ in range(a.steps):
+        step_graph.replay()
+    g1.record()
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1) / a.steps, world, dist, dev)
+    assert B.args_status(st.args) == 0
+    del step_graph
 
     names = ["fill_args", "fwd", "dgrad", "wgrad"]
     per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(a.steps)) * 1e3
@@ -502,7 +525,9 @@ def run_ours(a):
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                          "peak_source": pk_src, "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 3),
                          "traffic": traffic, "alg_bytes_per_launch": alg_bytes[dom]},
-            "kernels": kernels, "clocks": clk}
+            "kernels": kernels, "clocks": clk,
+            "graph": {"ms_per_step": round(graph_ms, 5), "value": round(job_tflops(world, FLOP_STEP, graph_ms), 2),
+                      "unit": "TFLOP/s", "what": "the same step captured once in a CUDA graph, replayed"}}
 
     # end to end through the public op with host-resident inputs
     if rank == 0 or True:
