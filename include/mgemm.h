@@ -141,7 +141,7 @@ int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t ld_in, uin
  * padded column-major FP8 layout for M rows in E groups: M plus the padding of
  * up to min(M, E) non-empty groups, rounded up to MGEMM_COL_PAD.  Known on the
  * host without the group sizes.  Returns -1 for M < 0 or E outside 1..MGEMM_MAX_EXPERTS.
- * (Implementation choice, not in the paper: it sizes the layout below.)
+ * (An implementation choice, not in [FP8]: it sizes the layout below.)
  */
 int64_t mgemm_colwise_ld(int64_t M, int E);
 
@@ -166,7 +166,7 @@ int64_t mgemm_colwise_ld(int64_t M, int E);
  * C1, C2 % 8 == 0; out1, out2 16-byte aligned.  Empty groups get scale 2^48
  * (amax 0) and no data.  The padding keeps every group's codes aligned and
  * lets mgemm_wgrad contract whole 128-row blocks without masking (an
- * implementation choice; the paper's layout is unpadded, strides (1, M)).
+ * implementation choice; [FP8 run_experiment]'s layout is unpadded, strides (1, M)).
  */
 int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, const void *in1, int64_t C1,
                                 uint8_t *out1, float *sc1, const void *in2, int64_t C2, uint8_t *out2,
