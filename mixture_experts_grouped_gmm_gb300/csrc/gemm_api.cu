@@ -144,9 +144,12 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   if (sms <= 1) return MGEMM_ECUDA;
   const bool pair = fp8 && a_rows == 128 && pairs_pay(M, E);
   // 192-wide tiles (a 5-stage ring whose weight tiles are 24 KB of each 40 KB
-  // stage): bf16 with w [E, K, N] in one box per stage, when the weights
-  // stream (at most 256 rows per expert on average, so HBM bounds the launch)
-  const bool allow192 = !fp8 && !trans_b && N % 64 == 0 && M <= 256 * (int64_t)E;
+  // stage), bf16 with w [E, K, N] in one box per stage (N % 64 == 0) or
+  // w [E, N, K], when the weights stream (at most 256 rows per expert on
+  // average, so HBM bounds the launch).  With more rows the wider tile's
+  // operand reuse wins.
+  // (the gated form needs whole 64-column halves: 128 or 256)
+  const bool allow192 = !fp8 && gate_rows == 0 && (trans_b || N % 64 == 0) && M <= 256 * (int64_t)E;
   const bool gated = gate_rows > 0;
   // routed rows (the gated and scattered forms) come in groups padded to 128,
   // so M / 128 bounds their row tiles; plain groups may add one partial tile each
@@ -228,6 +231,7 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   }
   if (gated)  // bf16, w [E, 2F, K]: the wide or mid K-major form
     return bn == 256 ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bk_mid(ta, tb, to, p, grid, s);
+  if (bn == 192 && trans_b) return gemm_bf16_rows_bk_w192(ta, tb, to, p, grid, s);
   if (bn == 192 && b_one_box) return gemm_bf16_rows_bmn_w192(ta, tb, to, p, grid, s);
   if (fp8) return gemm_fp8_rows(ta, tb, to, p, grid, s);
   return trans_b ? gemm_bf16_rows_bk(ta, tb, to, p, grid, s) : gemm_bf16_rows_bmn(ta, tb, to, p, grid, s);

@@ -31,6 +31,10 @@ int gemm_bf16_rows_bmn_w192(const CUtensorMap &a, const CUtensorMap &b, const CU
                             int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<false, false, true, kModeRows, 192, 5, 1>>(a, b, o, p, grid, s);
 }
+int gemm_bf16_rows_bk_w192(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                           int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 192, 5, 1>>(a, b, o, p, grid, s);
+}
 int gemm_bf16_rows_bk_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                           int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<false, false, false, kModeRows, 128, 6>>(a, b, o, p, grid, s);

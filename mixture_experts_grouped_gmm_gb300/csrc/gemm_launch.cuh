@@ -67,6 +67,8 @@ int gemm_bf16_rows_bmn_mid(const CUtensorMap &a, const CUtensorMap &b, const CUt
                            int grid, cudaStream_t s);
 int gemm_bf16_rows_bmn_w192(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                             int grid, cudaStream_t s);
+int gemm_bf16_rows_bk_w192(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                           int grid, cudaStream_t s);
 int gemm_bf16_rows_bk_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                           int grid, cudaStream_t s);
 int gemm_fp8_rows_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,

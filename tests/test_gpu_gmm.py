@@ -95,6 +95,18 @@ def test_fwd_bf16_weight_streaming_192_wide(sizes, K, N, kind):
         assert_close(to_np(out), ref, BF16_TOL, "fwd 192-wide")
 
 
+@pytest.mark.parametrize("sizes,K,N", [([128] * 8, 256, 3072), ([128, 0, 300, 7, 128, 256, 64, 141], 192, 3008)])
+def test_fwd_bf16_kmajor_weight_streaming_192_wide(sizes, K, N):
+    # w [E, N, K] with the shapes of the 192-wide weight-streaming case: the
+    # K-major 192-wide form
+    M, E = int(np.sum(sizes)), len(sizes)
+    x = rand_bf16((M, K), 33, "normal")
+    w = rand_bf16((E, N, K), 34, "normal")
+    out = bf16_fwd(sizes, K, N, x, w, 1)
+    ref = og.gmm_fwd(to_np(x), to_np(w), sizes, trans_b=True)
+    assert_close(to_np(out), ref, BF16_TOL, "fwd 192-wide, K-major weights")
+
+
 @pytest.mark.parametrize("sizes,K,N", CASES)
 def test_dgrad_bf16(sizes, K, N):
     M, E = int(np.sum(sizes)), len(sizes)
