@@ -388,27 +388,32 @@ __global__ void __launch_bounds__(kCwThreads, 1)
         return tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(k * 64 + (warp >> 2) * 16);
       };
       // This lane's 16 values of box k (the ring stage at hand): ldmatrix j,
-      // matrix m give rows r0 + 32 j + 8 m + rpair (low half) and + 1 (high
-      // half) of column lcol; rows past the group are cleared (only the boxes
-      // at the group's two ends hold rows of other groups).
+      // matrix m give rows 128 rhalf + 32 j + 8 m + rpair (low half) and + 1
+      // (high half) of the box, column lcol.  Rows past the group are cleared
+      // (only the boxes at the group's two ends hold rows of other groups) in
+      // a separate pass over the registers that only such a box takes: a
+      // compare inside the load loop cost about 10% of the kernel's time.
       auto read_box = [&](int k, uint32_t (&v)[16]) {
         const uint8_t *box = ring + stage * kCwBox;
-        const int64_t r0 = it.rs + (int64_t)k * kCwRows + rhalf * 128;
         const bool edge = it.rs + (int64_t)(k + 1) * kCwRows > it.re;  // the box runs past the group
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t w[4];
           ldsm_x4_trans(row_addr(box, j), w);
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            uint32_t x = w[m];
-            if (edge) {
-              const int64_t gr = r0 + j * 32 + m * 8 + rpair;
-              if (gr >= it.re) x &= 0xFFFF0000u;
-              if (gr + 1 >= it.re) x &= 0x0000FFFFu;
+          for (int m = 0; m < 4; ++m) v[4 * j + m] = w[m];
+        }
+        if (edge) {
+          // rows of the warp's half at or past lim (relative to its pair) lie past the group
+          const int lim = (int)(it.re - (it.rs + (int64_t)k * kCwRows + rhalf * 128)) - rpair;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int gr = j * 32 + m * 8;
+              if (gr >= lim) v[4 * j + m] &= 0xFFFF0000u;
+              if (gr + 1 >= lim) v[4 * j + m] &= 0x0000FFFFu;
             }
-            v[4 * j + m] = x;
-          }
         }
       };
       // pass 1: magnitude max of column lcol over this warp's rows; the first
