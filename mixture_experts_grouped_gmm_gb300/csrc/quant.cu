@@ -364,14 +364,25 @@ __global__ void __launch_bounds__(kCwThreads, 1)
     while (true) {
       // next item id from the producer (-1: no more work)
       int item = -1;
-      if (mbar_wait_warp(&qfull[q], qphase, vabort)) item = s_item[q];
+      if (mbar_wait_warp(&qfull[q], qphase, vabort)) {
+        item = s_item[q];
+      } else if (lane == 0) {  // gave up (or the kernel was aborted): report it, leave
+        set_status(av.status, MGEMM_STATUS_TIMEOUT);
+        *vabort = 1;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty[q]);
       if (++q == kCwQueue) {
         q = 0;
         qphase ^= 1;
       }
-      if (cw_consumer_barrier_any(item < 0 || *vabort != 0)) break;
+      // No barrier per item start: the one after pass 1 combines the column
+      // maxima, and every warp leaves at a barrier too (here, or at that one
+      // when any warp gave up), so all warps run the same number of barriers.
+      if (item < 0) {  // no more work, or a wait that gave up: the exit barrier
+        cw_consumer_barrier_any(true);
+        break;
+      }
       const CwItem it = cw_decode(item, av.offsets, av.poffsets, av.wgrad_order, t1, t2);
       const ColTensor &T = it.tensor == 0 ? t1 : t2;
       const int64_t col0 = (int64_t)it.cb * 64;
