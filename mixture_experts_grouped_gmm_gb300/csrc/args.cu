@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict
   __shared__ int tot32[NT / 32 > 0 ? NT / 32 : 1];
   const ArgsLayout L = args_layout(E);
   const int t = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   const int64_t m = t < E ? sizes[t] : 0;
   s_size[t] = m;
   const int any_neg = __syncthreads_or(m < 0);
@@ -225,13 +227,11 @@ extern "C" int mgemm_fill_args(const int64_t *group_sizes, int E, int64_t M, voi
   if (M < -1 || M >= (int64_t(1) << 31)) return MGEMM_EINVAL;
   if (((uintptr_t)args & 15) || ((uintptr_t)group_sizes & 7)) return MGEMM_EALIGN;
   cudaStream_t s = (cudaStream_t)stream;
-  if (E <= 32)
-    fill_args_kernel<32><<<1, 32, 0, s>>>(group_sizes, E, M, (uint8_t *)args);
-  else if (E <= 128)
-    fill_args_kernel<128><<<1, 128, 0, s>>>(group_sizes, E, M, (uint8_t *)args);
-  else
-    fill_args_kernel<1024><<<1, 1024, 0, s>>>(group_sizes, E, M, (uint8_t *)args);
-  return cuda_rc(cudaGetLastError(), "mgemm_fill_args launch");
+  uint8_t *a = (uint8_t *)args;
+  if (E <= 32) return launch_pdl(fill_args_kernel<32>, dim3(1), dim3(32), 0, s, 1, "mgemm_fill_args launch", group_sizes, E, M, a);
+  if (E <= 128)
+    return launch_pdl(fill_args_kernel<128>, dim3(1), dim3(128), 0, s, 1, "mgemm_fill_args launch", group_sizes, E, M, a);
+  return launch_pdl(fill_args_kernel<1024>, dim3(1), dim3(1024), 0, s, 1, "mgemm_fill_args launch", group_sizes, E, M, a);
 }
 
 extern "C" int mgemm_num_sms(void) {

@@ -33,6 +33,40 @@ int ensure_context();
 // Number of SMs of the current device (cached per device), or < 0 on error.
 int sm_count_cached();
 
+// Launch with programmatic stream serialization: the kernel's CTAs may be
+// placed while the previous kernel of the stream is still finishing, which
+// hides the launch latency between the two.  Every kernel launched this way
+// calls pdl_wait() before it reads or writes global memory (the wait ends when
+// the previous grid has completed and its writes are visible, so the ordering
+// is that of a plain launch) and pdl_trigger() only after that wait: the next
+// launch can then start only once every CTA of this one is resident, so it
+// never holds an SM that a CTA of this grid still needs.  cluster_x > 1 also
+// launches clusters of that many CTAs.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, unsigned cluster_x,
+               const char *what, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cuda_rc(cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...), what);
+}
+
 // ---------------------------------------------------------------- args block
 // Rows of each group in the padded column-major FP8 layout are rounded up to this.
 constexpr int kColPad = MGEMM_COL_PAD;
@@ -81,6 +115,11 @@ struct ArgsView {
 
 // Records the first device-side error; later ones do not overwrite it.
 __device__ __forceinline__ void set_status(int *status, int code) { atomicCAS(status, 0, code); }
+
+// Programmatic dependent launch (see launch_pdl): wait for the previous grid
+// of the stream (a no-op for a plain launch), then let the next one be placed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- PTX: basics
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

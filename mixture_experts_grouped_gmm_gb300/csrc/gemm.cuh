@@ -310,6 +310,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   const ArgsView av(p.args, p.E);
   if (*av.status != 0) return;
   const int total = total_tiles<C>(p, av);

@@ -32,25 +32,9 @@ int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o
     if (rc) return rc;
     attr_done[dev] = true;
   }
-  if constexpr (C::Pair) {
-    // clusters of two CTAs (grid is even); every CTA of the grid is resident
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cuda_rc(cudaLaunchKernelEx(&cfg, mgemm_gemm_kernel<C>, a, b, o, p), "grouped GEMM launch (CTA pairs)");
-  } else {
-    mgemm_gemm_kernel<C><<<grid, C::THREADS, smem, s>>>(a, b, o, p);
-    return cuda_rc(cudaGetLastError(), "grouped GEMM launch");
-  }
+  // CTA pairs: clusters of two CTAs (grid is even); every CTA of the grid is resident
+  return launch_pdl(mgemm_gemm_kernel<C>, dim3((unsigned)grid), dim3(C::THREADS), smem, s, C::Pair ? 2u : 1u,
+                    C::Pair ? "grouped GEMM launch (CTA pairs)" : "grouped GEMM launch", a, b, o, p);
 }
 
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)

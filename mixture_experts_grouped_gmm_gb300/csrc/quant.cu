@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
                                                             int64_t C, int64_t ld_in, uint8_t *__restrict__ out,
                                                             int64_t ld_out, float *__restrict__ scales) {
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < R; row += warps_total) {
     const __nv_bfloat16 *src = in + row * ld_in;
@@ -259,6 +261,8 @@ __global__ void __launch_bounds__(kCwThreads, 1)
   int *s_item = abort_flag + 1;  // [kCwQueue]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_item + kCwQueue);
 
+  pdl_wait();
+  pdl_trigger();
   const ArgsView av(args, E);
   if (*av.status != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -533,14 +537,15 @@ __global__ void __launch_bounds__(kCwThreads, 1)
 using namespace mgemm;
 
 template <int NCH>
-static void launch_rowwise(const __nv_bfloat16 *in, int64_t R, int64_t C, int64_t ld_in, uint8_t *out,
-                           int64_t ld_out, float *scales, cudaStream_t s) {
+static int launch_rowwise(const __nv_bfloat16 *in, int64_t R, int64_t C, int64_t ld_in, uint8_t *out,
+                          int64_t ld_out, float *scales, cudaStream_t s) {
   const int64_t blocks_needed = (R + 7) / 8;
-  int sms = mgemm_num_sms();
+  int sms = sm_count_cached();
   if (sms <= 0) sms = 148;
   const int64_t cap = (int64_t)sms * 32;
   const int blocks = (int)(blocks_needed < cap ? blocks_needed : cap);
-  quant_rowwise_kernel<NCH><<<blocks, 256, 0, s>>>(in, R, C, ld_in, out, ld_out, scales);
+  return launch_pdl(quant_rowwise_kernel<NCH>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_rowwise launch", in, R, C,
+                    ld_in, out, ld_out, scales);
 }
 
 extern "C" int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t ld_in, uint8_t *out,
@@ -553,16 +558,15 @@ extern "C" int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t
   const __nv_bfloat16 *x = (const __nv_bfloat16 *)in;
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t nch = (C + 255) / 256;
-  if (nch <= 1) launch_rowwise<1>(x, R, C, ld_in, out, ld_out, scales, s);
-  else if (nch <= 2) launch_rowwise<2>(x, R, C, ld_in, out, ld_out, scales, s);
-  else if (nch <= 4) launch_rowwise<4>(x, R, C, ld_in, out, ld_out, scales, s);
-  else if (nch <= 6) launch_rowwise<6>(x, R, C, ld_in, out, ld_out, scales, s);
-  else if (nch <= 8) launch_rowwise<8>(x, R, C, ld_in, out, ld_out, scales, s);
-  else if (nch <= 12) launch_rowwise<12>(x, R, C, ld_in, out, ld_out, scales, s);
-  else if (nch <= 16) launch_rowwise<16>(x, R, C, ld_in, out, ld_out, scales, s);
-  else if (nch <= 24) launch_rowwise<24>(x, R, C, ld_in, out, ld_out, scales, s);
-  else launch_rowwise<0>(x, R, C, ld_in, out, ld_out, scales, s);
-  return cuda_rc(cudaGetLastError(), "mgemm_quant_rowwise launch");
+  if (nch <= 1) return launch_rowwise<1>(x, R, C, ld_in, out, ld_out, scales, s);
+  if (nch <= 2) return launch_rowwise<2>(x, R, C, ld_in, out, ld_out, scales, s);
+  if (nch <= 4) return launch_rowwise<4>(x, R, C, ld_in, out, ld_out, scales, s);
+  if (nch <= 6) return launch_rowwise<6>(x, R, C, ld_in, out, ld_out, scales, s);
+  if (nch <= 8) return launch_rowwise<8>(x, R, C, ld_in, out, ld_out, scales, s);
+  if (nch <= 12) return launch_rowwise<12>(x, R, C, ld_in, out, ld_out, scales, s);
+  if (nch <= 16) return launch_rowwise<16>(x, R, C, ld_in, out, ld_out, scales, s);
+  if (nch <= 24) return launch_rowwise<24>(x, R, C, ld_in, out, ld_out, scales, s);
+  return launch_rowwise<0>(x, R, C, ld_in, out, ld_out, scales, s);
 }
 
 extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, const void *in1, int64_t C1,
@@ -631,7 +635,7 @@ extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, c
       return rc;
     attr_done[dev] = true;
   }
-  quant_colwise_kernel<<<grid, kCwThreads, cw_smem_bytes(E), (cudaStream_t)stream>>>(
-      tm1, tm2, tmo1, tmo2, (const uint8_t *)args, E, ld, t1, t2, (int)items);
-  return cuda_rc(cudaGetLastError(), "mgemm_quant_colwise_grouped launch");
+  return launch_pdl(quant_colwise_kernel, dim3(grid), dim3(kCwThreads), cw_smem_bytes(E), (cudaStream_t)stream, 1,
+                    "mgemm_quant_colwise_grouped launch", tm1, tm2, tmo1, tmo2, (const uint8_t *)args, E, ld, t1,
+                    t2, (int)items);
 }
