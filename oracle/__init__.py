@@ -25,6 +25,7 @@ Modules:
   args   -- group-size scan, active-group compaction, tile prefix, wgrad order
   quant  -- power-of-two absmax scales, rowwise and per-group colwise quantize
   gmm    -- forward, dgrad and wgrad for bf16 and FP8-scaled operands
+  mx     -- MXFP8: 32-element block scales (e8m0), block quantize, block-scaled grouped GEMM
 
 Parity status: every function is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_*.py``; none is "parity unpinned".

@@ -1,0 +1,74 @@
+"""MXFP8 (block-scaled e4m3) quantize and grouped GEMM (oracle; test
+infrastructure only).
+
+Source: "[moe training] Optimize FP8 MoE backward pass: fused colwise kernel +
+AMD tuning" (pytorch/ao commit 34322b5), commit message: the MXFP8 grouped MM
+path exists beside the FP8 one and needs its token groups padded to a multiple
+of 32 rows (the FP8 path 16); its tests run on SM100-class GPUs only.  The page
+names the format and its block of 32 and prints nothing more.
+
+Readings (the page is silent on the arithmetic):
+* A block is 32 consecutive elements of one row along the contraction
+  dimension; every block has one shared scale, stored as an e8m0 byte (a bare
+  biased exponent: byte b means 2^(b - 127)).
+* The block's scale follows the same power-of-two rule as the rowwise and
+  colwise quantizers of this build (``quant.pow2_scale``: s = 2^floor(log2(
+  fp32(448 / max(amax, 1e-12))))), applied to the block's magnitude maximum;
+  codes are the saturating e4m3 cast of x * s.  The e8m0 byte stores the
+  decode factor 1 / s = 2^-log2(s), i.e. byte = 127 - log2(s); for every
+  finite bf16 input it lies in [79, 254] (amax = 0 gives s = 2^48, byte 79).
+* The grouped GEMM multiplies decoded values: operand value = e4m3 value of
+  the code times 2^(byte - 127) of its block; for group e,
+  out[r, n] = sum_k xv[r, k] * wv[e, n, k] (forward, w stored [E, N, K]);
+  dgrad is the same contraction with grad_out and w stored [E, K, N]
+  quantized along N.
+
+Arithmetic: float64 numpy, ``np.matmul`` per group as the contraction.
+"""
+
+import numpy as np
+
+from .formats import decode_e4m3, encode_e4m3
+from .quant import pow2_scale
+
+MX_BLOCK = 32
+E8M0_BIAS = 127
+
+
+def quant_mx_rows(x):
+    """x: [R, K] float64 holding bf16 values, K % 32 == 0 ->
+    (codes uint8 [R, K], e8m0 uint8 [R, K // 32])."""
+    x = np.asarray(x, dtype=np.float64)
+    R, K = x.shape
+    assert K % MX_BLOCK == 0
+    xb = x.reshape(R, K // MX_BLOCK, MX_BLOCK)
+    amax = np.max(np.abs(xb), axis=2) if K else np.zeros((R, 0))
+    s = pow2_scale(amax)                                    # [R, K/32], powers of two
+    codes = encode_e4m3(xb * s[:, :, None]).reshape(R, K)   # x * s is exact
+    _, ex = np.frexp(s)                                     # s = 0.5 * 2^ex
+    log2s = ex - 1
+    e8m0 = (E8M0_BIAS - log2s).astype(np.int64)
+    assert np.all((e8m0 >= 0) & (e8m0 <= 254))
+    return codes.astype(np.uint8), e8m0.astype(np.uint8)
+
+
+def decode_mx(codes, e8m0):
+    """codes uint8 [R, K], e8m0 uint8 [R, K // 32] -> float64 values [R, K]."""
+    v = decode_e4m3(codes)
+    R, K = v.shape
+    f = np.ldexp(1.0, np.asarray(e8m0, dtype=np.int64) - E8M0_BIAS)  # [R, K/32]
+    return (v.reshape(R, K // MX_BLOCK, MX_BLOCK) * f[:, :, None]).reshape(R, K)
+
+
+def gmm_fwd_mx(xq, xs, wq, ws, group_sizes):
+    """xq [M, K] + xs [M, K/32]; wq [E, N, K] + ws [E, N, K/32] -> out [M, N]."""
+    x = decode_mx(xq, xs)
+    E, N, K = wq.shape
+    w = decode_mx(np.asarray(wq).reshape(E * N, K), np.asarray(ws).reshape(E * N, K // MX_BLOCK)).reshape(E, N, K)
+    out = np.zeros((x.shape[0], N))
+    off = np.concatenate([[0], np.cumsum(np.asarray(group_sizes, dtype=np.int64))])
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 > r0:
+            out[r0:r1] = x[r0:r1] @ w[e].T
+    return out

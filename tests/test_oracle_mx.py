@@ -1,0 +1,109 @@
+"""Pins for oracle.mx: the MXFP8 block quantizer and the block-scaled grouped
+GEMM, checked against hand-computed codes and bytes, the reduction to the
+(separately pinned) rowwise quantizer when a row is one block, exact
+round trips, and a brute-force loop over the definition."""
+
+import numpy as np
+
+from oracle.formats import decode_e4m3
+from oracle.mx import decode_mx, gmm_fwd_mx, quant_mx_rows
+from oracle.quant import quant_rowwise
+
+
+def test_hand_example_two_blocks():
+    x = np.zeros((1, 64))
+    x[0, :4] = [1.0, -2.0, 0.5, 0.0]     # block 0: amax 2 -> 448/2 = 224 -> s = 128
+    q, e = quant_mx_rows(x)               # block 1: all zero -> s = 2^48
+    assert e.tolist() == [[127 - 7, 127 - 48]]
+    # 128 = 2^7 -> 0x70; -256 -> 0xF8; 64 -> 0x68; 0 -> 0x00
+    assert q[0, :4].tolist() == [0x70, 0xF8, 0x68, 0x00]
+    assert not q[0, 4:].any()
+
+
+def test_one_block_rows_reduce_to_rowwise():
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal((50, 32)) * np.exp2(rng.integers(-20, 20, (50, 1)))).astype(np.float32).astype(np.float64)
+    x[3] = 0.0
+    q, e = quant_mx_rows(x)
+    qr, sr = quant_rowwise(x)
+    assert np.array_equal(q, qr)
+    assert np.array_equal(np.exp2(127.0 - e[:, 0].astype(np.float64)), sr)
+
+
+def test_blocks_are_independent_rows_of_32():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal((7, 256)) * np.exp2(rng.integers(-6, 6, (7, 8)).repeat(32, axis=1))).astype(np.float32)
+    x = x.astype(np.float64)
+    q, e = quant_mx_rows(x)
+    qb, sb = quant_rowwise(x.reshape(-1, 32))
+    assert np.array_equal(q, qb.reshape(7, 256))
+    assert np.array_equal(np.exp2(127.0 - e.reshape(-1).astype(np.float64)), sb)
+    # changing one block leaves every other block's codes and byte alone
+    y = x.copy()
+    y[2, 64:96] *= 1000.0
+    q2, e2 = quant_mx_rows(y)
+    mask = np.ones_like(q, dtype=bool)
+    mask[2, 64:96] = False
+    assert np.array_equal(q[mask], q2[mask])
+    emask = np.ones_like(e, dtype=bool)
+    emask[2, 2] = False
+    assert np.array_equal(e[emask], e2[emask])
+    # 1000x is about 2^10: the decode factor of that block grows by 2^9 or 2^10
+    assert int(e2[2, 2]) - int(e[2, 2]) in (9, 10)
+
+
+def test_exact_round_trip_for_representable_blocks():
+    # every block holds e4m3 values times 2^j with one element at 448 * 2^j:
+    # the scale is exactly 2^-j and decoding gives the input back
+    rng = np.random.default_rng(2)
+    R, K = 9, 128
+    codes = rng.integers(0, 0x7E, (R, K), dtype=np.uint8) | (rng.integers(0, 2, (R, K), dtype=np.uint8) << 7)
+    codes[:, ::32] = 0x7E
+    j = rng.integers(-20, 20, (R, K // 32))
+    x = decode_e4m3(codes) * np.exp2(j).repeat(32, axis=1)
+    q, e = quant_mx_rows(x)
+    assert np.array_equal(decode_mx(q, e), x)
+    assert np.array_equal(e.astype(np.int64), 127 + j)
+
+
+def test_relative_error_bound():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((32, 512)) * 3.0).astype(np.float32).astype(np.float64)
+    q, e = quant_mx_rows(x)
+    d = decode_mx(q, e)
+    blk = np.abs(x).reshape(32, 16, 32).max(axis=2).repeat(32, axis=1)
+    # e4m3 keeps 3 mantissa bits: error <= 2^-4 of the value, or half the
+    # subnormal step (2^-10 of the scaled unit) for tiny elements
+    assert np.all(np.abs(d - x) <= np.maximum(np.abs(x) * 2.0 ** -4, blk / 448.0 * 2.0 ** -9 * 2))
+
+
+def test_gemm_hand_example():
+    xq = np.full((1, 32), 0x38, dtype=np.uint8)       # 1.0
+    xs = np.array([[127]], dtype=np.uint8)            # x 1
+    wq = np.full((1, 1, 32), 0x40, dtype=np.uint8)    # 2.0
+    ws = np.array([[[128]]], dtype=np.uint8)          # x 2
+    out = gmm_fwd_mx(xq, xs, wq, ws, [1])
+    assert out.tolist() == [[32 * 1.0 * 2.0 * 2.0]]
+
+
+def test_gemm_brute_force():
+    rng = np.random.default_rng(4)
+    E, N, K = 3, 5, 64
+    sizes = [2, 0, 3]
+    M = sum(sizes)
+    xq = rng.integers(0, 0x7F, (M, K), dtype=np.uint8) ^ (rng.integers(0, 2, (M, K), dtype=np.uint8) << 7)
+    wq = rng.integers(0, 0x7F, (E, N, K), dtype=np.uint8) ^ (rng.integers(0, 2, (E, N, K), dtype=np.uint8) << 7)
+    xs = rng.integers(110, 140, (M, K // 32), dtype=np.uint8)
+    ws = rng.integers(110, 140, (E, N, K // 32), dtype=np.uint8)
+    out = gmm_fwd_mx(xq, xs, wq, ws, sizes)
+    dv = {c: float(decode_e4m3(np.array([c], dtype=np.uint8))[0]) for c in range(256)}
+    starts = [0, 2, 2]
+    for e in range(E):
+        for r in range(starts[e], starts[e] + sizes[e]):
+            for n in range(N):
+                acc = 0.0
+                for k in range(K):
+                    a = dv[int(xq[r, k])] * 2.0 ** (int(xs[r, k // 32]) - 127)
+                    b = dv[int(wq[e, n, k])] * 2.0 ** (int(ws[e, n, k // 32]) - 127)
+                    acc += a * b
+                assert abs(out[r, n] - acc) <= 1e-12 * max(1.0, abs(acc)), (e, r, n)
