@@ -48,7 +48,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true", help="headline step only")
-    p.add_argument("--workload", choices=["all", "sparse", "deepseek", "mixtral"], default="all",
+    p.add_argument("--workload", choices=["all", "sparse", "deepseek", "mxfp8", "mixtral"], default="all",
                    help="'all': headline line with every block; otherwise run only that block (profiling)")
     p.add_argument("--tokens", type=int, default=16384, help="DeepSeek-shaped block: tokens (x top-6 rows)")
     p.add_argument("--experts", type=int, default=128, help="sparse-M block: number of experts")
@@ -300,6 +300,70 @@ def deepseek_extra(torch, B, dev, pk, tokens=16384, reps=10):
     return out
 
 
+def deepseek_mx_extra(torch, B, dev, pk, tokens=16384, reps=10):
+    """MXFP8 on the DeepSeek shapes: the block casts (one e8m0 scale per 32
+    contraction elements) of x, grad_out and both weight layouts, and the
+    block-scaled fwd and dgrad GEMMs."""
+    from mixture_experts_grouped_gmm_gb300 import workloads
+
+    d = workloads.deepseek(device=dev, T=tokens)
+    M, K, N, E = d["M"], d["K"], d["N"], d["E"]
+    u8, bf = torch.uint8, torch.bfloat16
+    w_kn = d["w"]
+    w_nk = w_kn.transpose(1, 2).contiguous()
+    x, go = d["x"], d["grad_out"]
+    lk, ln = B.mx_ld_sf(K), B.mx_ld_sf(N)
+    T = dict(args=torch.empty(B.mgemm_args_bytes(E), dtype=u8, device=dev),
+             xq=torch.empty(M, K, dtype=u8, device=dev), sx=torch.empty(M, lk, dtype=u8, device=dev),
+             goq=torch.empty(M, N, dtype=u8, device=dev), sgo=torch.empty(M, ln, dtype=u8, device=dev),
+             wq=torch.empty(E * N, K, dtype=u8, device=dev), sw=torch.empty(E * N, lk, dtype=u8, device=dev),
+             wdq=torch.empty(E * K, N, dtype=u8, device=dev), swd=torch.empty(E * K, ln, dtype=u8, device=dev),
+             out=torch.empty(M, N, dtype=bf, device=dev), gx=torch.empty(M, K, dtype=bf, device=dev))
+    names = ["quant_w", "quant_x", "fwd", "quant_go", "dgrad"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev: ev[i].record()
+        B.mgemm_fill_args(d["group_sizes"], E, M, T["args"])
+        mark(0); B.mgemm_quant_mx(w_nk.view(E * N, K), T["wq"], T["sw"])
+        B.mgemm_quant_mx(w_kn.view(E * K, N), T["wdq"], T["swd"])
+        mark(1); B.mgemm_quant_mx(x, T["xq"], T["sx"])
+        mark(2); B.mgemm_fwd_mx(T["args"], T["xq"], T["sx"], T["wq"].view(E, N, K), T["sw"], T["out"], M, K, N, E)
+        mark(3); B.mgemm_quant_mx(go, T["goq"], T["sgo"])
+        mark(4); B.mgemm_fwd_mx(T["args"], T["goq"], T["sgo"], T["wdq"].view(E, K, N), T["swd"], T["gx"], M, N, K, E)
+        mark(5)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
+    for r in range(reps):
+        step(evs[r])
+    torch.cuda.synchronize()
+    t = {n: statistics.median(evs[r][i].elapsed_time(evs[r][i + 1]) * 1e3 for r in range(reps))
+         for i, n in enumerate(names)}
+    fl = 2 * M * K * N
+    fp8_peak = 2 * pk["bf16_tflops"]
+    byts = {"quant_w": 2 * E * N * K * 3 + E * (N * lk + K * ln), "quant_x": M * K * 3 + M * lk,
+            "quant_go": M * N * 3 + M * ln}
+    kern = {}
+    for n in names:
+        k = {"us": round(t[n], 2)}
+        if n in ("fwd", "dgrad"):
+            k["tflops"] = round(fl / (t[n] * 1e-6) / 1e12, 1)
+            k["tensor_frac_fp8"] = round(fl / (t[n] * 1e-6) / 1e12 / fp8_peak, 3)
+        if n in byts:
+            gbs = byts[n] / (t[n] * 1e-6) / 1e9
+            k["gbs"] = round(gbs, 1)
+            k["hbm_frac"] = round(gbs / pk["hbm_gbs"], 3)
+        kern[n] = k
+    out = {"shape": f"M={M} K={K} N={N} E={E} (the DeepSeek step's routing), e4m3 codes, one e8m0 scale per "
+                    "32 contraction elements, bf16 outputs",
+           "fp8_peak_tflops": round(fp8_peak, 1), "kernels": kern}
+    del T, d, w_nk
+    return out
+
+
 def mixtral_extra(torch, B, dev, pk):
     from mixture_experts_grouped_gmm_gb300 import workloads
 
@@ -420,6 +484,8 @@ def run_block(a):
         out = sparse_m_extra(torch, B, dev, pk, E=a.experts, reps=max(1, a.steps))
     elif a.workload == "deepseek":
         out = deepseek_extra(torch, B, dev, pk, tokens=a.tokens, reps=max(1, a.steps))
+    elif a.workload == "mxfp8":
+        out = deepseek_mx_extra(torch, B, dev, pk, tokens=a.tokens, reps=max(1, a.steps))
     else:
         out = mixtral_extra(torch, B, dev, pk)
     print(json.dumps({"workload": a.workload, a.workload: out}), flush=True)
@@ -590,6 +656,8 @@ def run_ours(a):
         line["sparse_m_fp8"] = sparse_m_extra(torch, B, dev, pk)
         torch.cuda.empty_cache()
         line["deepseek_fp8_step"] = deepseek_extra(torch, B, dev, pk)
+        torch.cuda.empty_cache()
+        line["deepseek_mxfp8"] = deepseek_mx_extra(torch, B, dev, pk)
         torch.cuda.empty_cache()
         line["mixtral_bf16"] = mixtral_extra(torch, B, dev, pk)
     if rank == 0 and world == 1 and not a.no_cpu:

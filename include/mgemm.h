@@ -137,6 +137,24 @@ int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t ld_in, uin
                         float *scales, mgemm_stream_t stream);
 
 /*
+ * mgemm_quant_mx -- MXFP8 block quantize: e4m3 codes with one e8m0 scale per
+ * 32 consecutive elements of a row.  [FP8 commit message]: the MXFP8 grouped
+ * MM path beside the FP8 one, with its token groups padded to 32; the page
+ * prints no arithmetic.  Reading: per block b of row r (columns 32b..32b+31),
+ * amax = max |in|; s = the power-of-two rule of mgemm_quant_rowwise applied to
+ * that amax; out = e4m3_rne_sat(in * s); sf[r, b] = 127 - log2(s) (the e8m0
+ * byte of the decode factor 1/s, always in 79..254).
+ *   in   bf16 [R, C] with row stride ld_in elements (ld_in >= C, ld_in % 8 == 0)
+ *   out  e4m3 [R, C] with row stride ld_out bytes (ld_out >= C, ld_out % 16 == 0)
+ *   sf   e8m0 [R, ld_sf] bytes, ld_sf >= C / 32, ld_sf % 16 == 0 (bytes past
+ *        C / 32 in each row are not written)
+ * C % 32 == 0.  R == 0 or C == 0 launches nothing.  Errors: -1 (sizes), -2
+ * (alignment).
+ */
+int mgemm_quant_mx(const void *in, int64_t R, int64_t C, int64_t ld_in, uint8_t *out, int64_t ld_out, uint8_t *sf,
+                   int64_t ld_sf, mgemm_stream_t stream);
+
+/*
  * mgemm_colwise_ld -- the smallest leading dimension (bytes per column) of the
  * padded column-major FP8 layout for M rows in E groups: M plus the padding of
  * up to min(M, E) non-empty groups, rounded up to MGEMM_COL_PAD.  Known on the
@@ -200,6 +218,25 @@ int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x, const flo
  */
 int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,
                 const float *sw, void *grad_x, int64_t M, int K, int N, int E, mgemm_stream_t stream);
+
+/*
+ * mgemm_fwd_mx -- the MXFP8 grouped GEMM: out[r, n] = sum_k xv[r, k] wv[e(r), n, k]
+ * where xv, wv are the decoded block-scaled values (e4m3 value times
+ * 2^(sf - 127) of its 32-element block; see mgemm_quant_mx).  [FP8 commit
+ * message]: the MXFP8 grouped MM path; the block scales are applied by the
+ * tensor cores (block-scaled MMA, one e8m0 scale per 32 contraction elements
+ * of each row of either operand), accumulation in fp32, bf16 output (RNE).
+ * The same call computes the MXFP8 dgrad: pass grad_out as x (contraction N)
+ * and w stored [E, K, N] quantized along N as w.
+ *   x    e4m3 [M, K] (row stride K bytes); sx e8m0 [M, ld_sf]
+ *   w    e4m3 [E, N, K]; sw e8m0 [E * N, ld_sf]
+ *   ld_sf  bytes per scale row, >= K / 32, % 16 == 0 (as written by mgemm_quant_mx)
+ *   out  bf16 [M, N]
+ * K % 128 == 0, N % 8 == 0.  Groups of any size (the blocks run along K).
+ * Errors: -1 (sizes or NULL), -2 (alignment), -3 (E), -4 (CUDA).
+ */
+int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *sx, const uint8_t *w, const uint8_t *sw,
+                 int64_t ld_sf, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream);
 
 /*
  * mgemm_wgrad -- grad_w[e] = x_e^T . grad_out_e, contracting over the m_e rows

@@ -43,6 +43,12 @@ _SIGS = {
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                    ctypes.c_void_p]),
+    "mgemm_quant_mx": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                      ctypes.c_void_p]),
+    "mgemm_fwd_mx": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "mgemm_colwise_ld": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int]),
     "mgemm_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -138,6 +144,29 @@ def mgemm_quant_rowwise(inp, out, scales):
     R, C = inp.shape
     _check(lib().mgemm_quant_rowwise(_p(inp), R, C, inp.stride(0), _p(out), out.stride(0), _p(scales),
                                      _stream(inp)), "mgemm_quant_rowwise")
+
+
+MX_BLOCK = 32
+
+
+def mx_ld_sf(C):
+    """Bytes per scale row of mgemm_quant_mx for C columns: C / 32 rounded up to 16."""
+    return -(-(C // MX_BLOCK) // 16) * 16
+
+
+def mgemm_quant_mx(inp, out, sf):
+    """inp bf16 [R, C] -> out e4m3 [R, C] (uint8) and sf e8m0 [R, ld_sf] (uint8)."""
+    _cuda(inp, out, sf)
+    R, C = inp.shape
+    _check(lib().mgemm_quant_mx(_p(inp), R, C, inp.stride(0), _p(out), out.stride(0), _p(sf), sf.stride(0),
+                                _stream(inp)), "mgemm_quant_mx")
+
+
+def mgemm_fwd_mx(args, x, sx, w, sw, out, M, K, N, E):
+    """MXFP8 grouped GEMM: x e4m3 [M, K] + sx [M, ld_sf]; w e4m3 [E, N, K] + sw [E * N, ld_sf]."""
+    _cuda(args, x, sx, w, sw, out)
+    _check(lib().mgemm_fwd_mx(_p(args), _p(x), _p(sx), _p(w), _p(sw), sx.stride(0), _p(out), int(M), int(K), int(N),
+                              int(E), _stream(out)), "mgemm_fwd_mx")
 
 
 def mgemm_colwise_ld(M, E):

@@ -147,7 +147,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 bool make_tensor_map(CUtensorMap *m, bool byte_elems, int rank, const void *base, const uint64_t *dims,
-                     const uint64_t *strides, const uint32_t *box) {
+                     const uint64_t *strides, const uint32_t *box, bool swizzle128) {
   auto enc = encode_fn();
   if (!enc) {
     note_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", 0);
@@ -157,7 +157,8 @@ bool make_tensor_map(CUtensorMap *m, bool byte_elems, int rank, const void *base
   const CUresult r =
       enc(m, byte_elems ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     note_error("cuTensorMapEncodeTiled", (int)r);
     return false;

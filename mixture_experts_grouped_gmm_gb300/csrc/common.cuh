@@ -22,10 +22,10 @@ inline int cuda_rc(cudaError_t e, const char *where) {
   return MGEMM_ECUDA;
 }
 
-// Tiled tensor map with 128-byte swizzle and zero fill outside the tensor
-// (dims[0] contiguous; strides in bytes for dims 1..rank-1).
+// Tiled tensor map with 128-byte swizzle (or none) and zero fill outside the
+// tensor (dims[0] contiguous; strides in bytes for dims 1..rank-1).
 bool make_tensor_map(CUtensorMap *m, bool byte_elems, int rank, const void *base, const uint64_t *dims,
-                     const uint64_t *strides, const uint32_t *box);
+                     const uint64_t *strides, const uint32_t *box, bool swizzle128 = true);
 // cuTensorMapEncodeTiled needs a current context; a thread that has made no
 // CUDA call yet (an autograd worker, say) has none.  Makes the current
 // device's primary context current, once per thread.
@@ -265,6 +265,23 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 // Same for 8-bit float inputs (e4m3 here).
+// Block-scaled e4m3 MMA (one ue8m0 scale per 32 contraction elements of each
+// row of A and B, read from tensor memory at sfa / sfb).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Shared memory -> tensor memory copy of scale factors: 32 rows of 16 bytes
+// to lanes 0-31 of each lane quarter (4 columns).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
@@ -415,6 +432,18 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
 // stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+// Shared-memory descriptor of an unswizzled tile of 16-byte rows stored
+// back to back (8-row core matrices 128 bytes apart; the tile is one core
+// matrix wide, so both strides are 128 bytes).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 16;
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
@@ -427,6 +456,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Instruction descriptor: fp32 accumulator, dense, A/B format code (kind::f16:
 // 1 = bf16; kind::f8f6f4: 0 = e4m3), operand majorness (1 = MN-major), N, M.
+// Instruction descriptor of the block-scaled kind::mxf8f6f4 MMA: e4m3 A and B
+// (format 0), both K-major, fp32 accumulator, M = m, N = n; bit 23 selects
+// the scale format (1: ue8m0).  The scale-factor ids (bits 4-5 for B, 29-30
+// for A: which byte of each 32-bit tensor-memory word the MMA takes) are
+// or-ed in per MMA.
+__host__ __device__ constexpr uint32_t make_idesc_mx(int m, int n, uint32_t ue8m0) {
+  return ((uint32_t)(n >> 3) << 17) | ((ue8m0 & 1u) << 23) | ((uint32_t)(m >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, bool a_mn, bool b_mn, int m, int n) {
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);

@@ -78,9 +78,15 @@ enum { kModeRows = 0, kModeExperts = 1 };
 // consecutive MMA tiles: fewer, larger copies, which is what latency-bound
 // launches with few rows need.
 template <bool kFp8, bool kAMn, bool kBMn, int kMode, int kBnMax = 256, int kStages = 4, int kOutBufs = 2,
-          bool kPair = false, int kEpiWarps = 4, bool kDynRing = false, int kKc = 1>
+          bool kPair = false, int kEpiWarps = 4, bool kDynRing = false, int kKc = 1, bool kMx = false>
 struct GemmCfg {
   static constexpr bool Fp8 = kFp8;
+  // kMx: MXFP8 -- e4m3 operands with one e8m0 scale per 32 contraction
+  // elements of every row, applied by block-scaled MMAs (no epilogue scales)
+  static constexpr bool Mx = kMx;
+  static constexpr bool Scaled = kFp8 && !kMx;  // FP8 with row / column scales in the epilogue
+  static_assert(!kMx || (kFp8 && kMode == kModeRows && !kAMn && !kBMn && !kPair && !kDynRing && kBnMax == 128),
+                "MXFP8: rows schedule, K-major operands, 128-wide tiles");
   static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
   static constexpr bool BMn = kBMn;
   static constexpr int Mode = kMode;
@@ -99,7 +105,8 @@ struct GemmCfg {
   static constexpr int STAGES = kStages;
   static constexpr int CHUNK = 64 * 128;  // MN-major: one 64-element x BK-row block (8 KB)
   // two accumulators of BN_MAX columns, allocated as a power of two >= 32
-  static constexpr int TMEM_COLS = 2 * BN_MAX <= 32    ? 32
+  static constexpr int TMEM_COLS = kMx                ? 512  // + the scale factors of every stage
+                                   : 2 * BN_MAX <= 32  ? 32
                                    : 2 * BN_MAX <= 64  ? 64
                                    : 2 * BN_MAX <= 128 ? 128
                                    : 2 * BN_MAX <= 256 ? 256
@@ -112,8 +119,12 @@ struct GemmCfg {
   static constexpr int OUT_BUF = 32 * 128;  // 32 rows x 64 bf16 columns
   static constexpr int NBUF = kOutBufs;      // staging buffers per epilogue warp
   static constexpr size_t TAIL_BYTES = 16 * STAGES + 256;  // barriers, flags
+  // MXFP8, per stage: the scale rows of A (128 x 16 B, four contraction blocks)
+  // and of B (BN x 16 B) as loaded, and the two 512-byte tiles rearranged for
+  // the tensor-memory copy
+  static constexpr int SF_STAGE = kMx ? 128 * 16 + BN_MAX * 16 + 2 * 512 : 0;
   static constexpr size_t FIXED_BYTES = 1024 /*align slack*/ + (size_t)EPI * NBUF * OUT_BUF /*epilogue staging*/ +
-                                        TAIL_BYTES;
+                                        (size_t)STAGES * SF_STAGE + TAIL_BYTES;
   // a run-time ring takes what the launch needs, up to the per-CTA limit
   static constexpr size_t SMEM_BYTES =
       kDynRing ? (size_t)227 * 1024 : FIXED_BYTES + (size_t)STAGES * (A_BYTES + B_BYTES);
@@ -289,7 +300,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     mgemm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+                      const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmSFA,
+                      const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // ring stages, then the epilogue staging [EPI warps][NBUF buffers][32 x 128 B], then barriers
@@ -301,7 +313,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto stage_b = [&](int st) -> uint8_t * {
     return C::DynRing ? smem + (size_t)st * p.stage_bytes + C::KC * p.a_rows * 128 : sB + st * C::B_BYTES;
   };
-  uint64_t *full = reinterpret_cast<uint64_t *>(sOut + C::EPI * C::NBUF * C::OUT_BUF);
+  // MXFP8 scale rows (per stage: A as loaded, B as loaded, A and B tiles for the copy)
+  uint8_t *sSF = sOut + C::EPI * C::NBUF * C::OUT_BUF;
+  auto sfa_land = [&](int st) -> uint8_t * { return sSF + st * C::SF_STAGE; };
+  auto sfb_land = [&](int st) -> uint8_t * { return sSF + st * C::SF_STAGE + 128 * 16; };
+  auto sf_tile = [&](int st, int op) -> uint8_t * {
+    return sSF + st * C::SF_STAGE + 128 * 16 + C::BN_MAX * 16 + op * 512;
+  };
+  uint64_t *full = reinterpret_cast<uint64_t *>(sSF + C::STAGES * C::SF_STAGE);
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
@@ -340,6 +359,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmOut);
+    if constexpr (C::Mx) {
+      tma_prefetch_desc(&tmSFA);
+      tma_prefetch_desc(&tmSFB);
+    }
   }
   if (warp == 1) {
     if constexpr (C::Pair) {
@@ -377,7 +400,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // that are never stored
       // pair: the leader's full barrier counts the bytes of both CTAs
       const uint32_t tx = C::Pair ? 2u * (uint32_t)(C::A_BYTES + (bn / 2) * 128)
-                                  : C::KC * ((C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128);
+                                  : C::KC * ((C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128) +
+                                        (C::Mx ? (uint32_t)(128 * 16 + bn * 16) : 0u);
       for (int j = 0; j * t_step < total && !*vabort; ++j) {
         const int t = tile_of<C>(j, t_first, t_step);
         if (t >= total) continue;
@@ -440,6 +464,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tma_load_3d(b, &tmB, &full[stage], kb * C::BK, ti.n0, ti.e);
               }
             }
+            if constexpr (C::Mx) {
+              // the scale rows of four contraction blocks (16 bytes per row;
+              // x is a multiple of 16 bytes): A rows of the tile, and rows
+              // e N + n0 .. of B's [E N, ld_sf] scales
+              tma_load_2d(sfa_land(stage), &tmSFA, &full[stage], (kb >> 2) * 16, ti.a_row);
+              tma_load_2d(sfb_land(stage), &tmSFB, &full[stage], (kb >> 2) * 16, ti.e * p.Nout + ti.n0);
+            }
           } else {
             const int xr = ti.x0 + kb * C::BK;
             if (C::AMn) {
@@ -499,7 +530,44 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             __syncwarp();
           }
         }
-        if (lane == 0) {
+        if constexpr (C::Mx) {
+          // MXFP8.  The stage's scale rows cover four contraction blocks of 128
+          // (16 bytes per row); word j = kb % 4 of each row holds this block's
+          // four 32-element scales.  Tensor memory takes them as a 512-byte
+          // tile per operand, row l holding rows l, l + 32, l + 64, l + 96 of
+          // the tile (byte 4 m + s: sub-block s of row l + 32 m), copied into
+          // each lane quarter; the MMA of sub-block s reads byte s (the
+          // scale-factor ids of the instruction descriptor).  Lane l of the
+          // MMA warp builds row l of both tiles.
+          const int j = kb & 3;
+          const uint32_t *la = reinterpret_cast<const uint32_t *>(sfa_land(stage));
+          const uint32_t *lb = reinterpret_cast<const uint32_t *>(sfb_land(stage));
+          const uint4 va = make_uint4(la[lane * 4 + j], la[(lane + 32) * 4 + j], la[(lane + 64) * 4 + j],
+                                      la[(lane + 96) * 4 + j]);
+          const uint4 vb = make_uint4(lb[lane * 4 + j], lb[(lane + 32) * 4 + j], lb[(lane + 64) * 4 + j],
+                                      lb[(lane + 96) * 4 + j]);
+          reinterpret_cast<uint4 *>(sf_tile(stage, 0))[lane] = va;
+          reinterpret_cast<uint4 *>(sf_tile(stage, 1))[lane] = vb;
+          fence_proxy_async_smem();  // the tiles are read by tcgen05.cp
+          __syncwarp();
+          if (lane == 0) {
+            // per stage, columns 2 BN_MAX + 8 stage (A) and + 4 (B): the
+            // stage's empty barrier, armed by the commit below, also orders the
+            // copies before the next use of these columns
+            const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * 8, sfb_t = sfa_t + 4;
+            tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(smem_u32(sf_tile(stage, 0))));
+            tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(smem_u32(sf_tile(stage, 1))));
+            const uint32_t abase = smem_u32(a), bbase = smem_u32(b);
+#pragma unroll
+            for (int k = 0; k < C::KSTEPS; ++k) {
+              const uint64_t ad = smem_desc_sw128(abase + k * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(bbase + k * 32, 16, 1024);
+              const uint32_t idk = p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29);
+              mma_mx(d_tmem, ad, bd, idk, sfa_t, sfb_t, (kb | k) != 0);
+            }
+            mma_commit(&empty[stage]);
+          }
+        } else if (lane == 0) {
           const uint32_t abase = smem_u32(a), bbase = smem_u32(b);
           if (!edge) {
 #pragma unroll
@@ -591,7 +659,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // two: the reciprocals are exact)
     float rinv_next = 1.f, csr_next[2 * kCpw] = {};
     auto load_scales = [&](int tn) {
-      if (!C::Fp8 || tn >= total) return;
+      if (!C::Scaled || tn >= total) return;
       const TileInfo tj = decode_tile<C>(tn, p, av, rank);
       const bool live = tj.kb_count > 0;
       rinv_next = live && r < tj.out_rows ? pow2_recip(__ldg(p.rscale + tj.out_row0 + r)) : 1.f;
@@ -639,7 +707,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       __nv_bfloat16 *orow = p.out + out_row * p.Nout;
       float rinv = 1.f, csr[2 * kCpw];
-      if constexpr (C::Fp8) {
+      if constexpr (C::Scaled) {
         rinv = rinv_next;
 #pragma unroll
         for (int i = 0; i < 2 * kCpw; ++i) csr[i] = csr_next[i];
@@ -741,7 +809,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // NBUF groups back (FP8 parks the chunk's column scales in it first, so
         // it waits for the buffer before the math; bf16 only before its stores)
         uint8_t *buf = my_buf + (nstored % C::NBUF) * C::OUT_BUF;
-        if constexpr (C::Fp8) {
+        if constexpr (C::Scaled) {
           if (lane == 0) bulk_wait_read<C::NBUF - 1>();
           __syncwarp();
         }
@@ -759,7 +827,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tmem_ld_32x32b_x32(taddr + (c + C::HN) * 64, va[cur ^ (kNb - 1)]);
             tmem_ld_32x32b_x32(taddr + (c + C::HN) * 64 + 32, vb[cur ^ (kNb - 1)]);
           }
-          if (C::Fp8) {
+          if (C::Scaled) {
             // the chunk's column-scale reciprocals, staged in the (free) staging
             // buffer and read as broadcasts before the codes overwrite them
             float *cs = reinterpret_cast<float *>(buf);
@@ -801,7 +869,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (col0 >= p.Nout) continue;
         if (warp_full) {
-          if constexpr (!C::Fp8) {
+          if constexpr (!C::Scaled) {
             if (lane == 0) bulk_wait_read<C::NBUF - 1>();
             __syncwarp();
           }

@@ -259,6 +259,66 @@ extern "C" int mgemm_fwd_gated(const void *args, const void *x, const void *w, v
   return fwd_impl(args, MGEMM_BF16, 1, x, nullptr, w, nullptr, out, M, K, 2 * F, E, stream, nullptr, 0, nullptr, F);
 }
 
+extern "C" int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *sx, const uint8_t *w, const uint8_t *sw,
+                            int64_t ld_sf, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
+  if (!args || !x || !sx || !w || !sw || !out) return MGEMM_EINVAL;
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  if (M < 0 || M >= (int64_t(1) << 31) || K <= 0 || N <= 0 || ld_sf < K / 32) return MGEMM_EINVAL;
+  if ((int64_t)E * N >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  if (K % 128 || N % 8) return MGEMM_EINVAL;
+  if (!aligned16(args) || !aligned16(x) || !aligned16(sx) || !aligned16(w) || !aligned16(sw) || !aligned16(out) ||
+      ld_sf % 16)
+    return MGEMM_EALIGN;
+  if (M == 0) return MGEMM_OK;
+  int rc = ensure_context();
+  if (rc) return rc;
+  const int sms = sm_count();
+  if (sms <= 0) return MGEMM_ECUDA;
+  const int bn = 128;
+  CUtensorMap ta, tb, to, tsa, tsb;
+  {
+    const uint64_t d[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t st[1] = {(uint64_t)K};
+    const uint32_t box[2] = {128, 128};
+    if (!make_map(&ta, true, 2, x, d, st, box)) return MGEMM_ECUDA;
+  }
+  {
+    const uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
+    const uint64_t st[2] = {(uint64_t)K, (uint64_t)N * K};
+    const uint32_t box[3] = {128, (uint32_t)bn, 1};
+    if (!make_map(&tb, true, 3, w, d, st, box)) return MGEMM_ECUDA;
+  }
+  // scale rows: 16-byte boxes (four contraction blocks of 128) of 128 / bn rows, unswizzled
+  {
+    const uint64_t d[2] = {(uint64_t)ld_sf, (uint64_t)M};
+    const uint64_t st[1] = {(uint64_t)ld_sf};
+    const uint32_t box[2] = {16, 128};
+    if (!make_tensor_map(&tsa, true, 2, sx, d, st, box, false)) return MGEMM_ECUDA;
+  }
+  {
+    const uint64_t d[2] = {(uint64_t)ld_sf, (uint64_t)E * N};
+    const uint64_t st[1] = {(uint64_t)ld_sf};
+    const uint32_t box[2] = {16, (uint32_t)bn};
+    if (!make_tensor_map(&tsb, true, 2, sw, d, st, box, false)) return MGEMM_ECUDA;
+  }
+  if (!make_out_map(&to, out, M, N)) return MGEMM_ECUDA;
+  GemmParams p{};
+  p.args = (const uint8_t *)args;
+  p.E = E;
+  p.bn = bn;
+  p.a_rows = 128;
+  p.idesc = make_idesc_mx(128, bn, 1);  // ue8m0 scales
+  p.n_tiles = (N + bn - 1) / bn;
+  p.Kc = K;
+  p.Nout = N;
+  p.out = (__nv_bfloat16 *)out;
+  const int64_t upper = ((M + 127) / 128 + (M < E ? M : E)) * p.n_tiles;
+  const int grid = grid_for(upper);
+  if (grid < 0) return MGEMM_ECUDA;
+  return gemm_fp8_rows_mx(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
+}
+
 extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,
                            const float *sw, void *grad_x, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
   int rc = common_checks(args, dtype, M, K, N, E);

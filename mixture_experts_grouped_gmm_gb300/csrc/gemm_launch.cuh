@@ -8,7 +8,7 @@ namespace mgemm {
 
 template <class C>
 int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p_in, int grid,
-                cudaStream_t s) {
+                cudaStream_t s, const CUtensorMap *sfa = nullptr, const CUtensorMap *sfb = nullptr) {
   GemmParams p = p_in;
   size_t smem = C::SMEM_BYTES;
   if constexpr (C::DynRing) {
@@ -34,9 +34,13 @@ int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o
   }
   // CTA pairs: clusters of two CTAs (grid is even); every CTA of the grid is resident
   return launch_pdl(mgemm_gemm_kernel<C>, dim3((unsigned)grid), dim3(C::THREADS), smem, s, C::Pair ? 2u : 1u,
-                    C::Pair ? "grouped GEMM launch (CTA pairs)" : "grouped GEMM launch", a, b, o, p);
+                    C::Pair ? "grouped GEMM launch (CTA pairs)" : "grouped GEMM launch", a, b, o, sfa ? *sfa : a,
+                    sfb ? *sfb : a, p);
 }
 
+// MXFP8: e4m3 x [M, K] and w [E, N, K] with e8m0 scale rows (maps sfa, sfb), 128-wide tiles
+int gemm_fp8_rows_mx(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
+                     const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)
 int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s);

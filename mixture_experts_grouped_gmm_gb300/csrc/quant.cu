@@ -107,6 +107,39 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
   }
 }
 
+// ------------------------------------------------------------------ MX blocks
+// One warp per row, 8 elements (16 bytes) per lane and chunk of 256: lanes
+// 4j .. 4j + 3 hold block j of the chunk, whose magnitude maximum two
+// shuffles combine.  The scale is the rowwise rule applied per block; the
+// e8m0 byte 127 - log2(s) is 254 minus s's biased exponent (s is a power of
+// two, always normal).
+__global__ void __launch_bounds__(256) quant_mx_kernel(const __nv_bfloat16 *__restrict__ in, int64_t R, int64_t C,
+                                                       int64_t ld_in, uint8_t *__restrict__ out, int64_t ld_out,
+                                                       uint8_t *__restrict__ sf, int64_t ld_sf) {
+  const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < R; row += warps_total) {
+    const __nv_bfloat16 *src = in + row * ld_in;
+    uint8_t *dst = out + row * ld_out;
+    for (int64_t c0 = 0; c0 < C; c0 += 256) {
+      const int64_t c = c0 + lane * 8;
+      const bool live = c < C;  // C % 32 == 0: a block's four lanes agree
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (live) v = ldg_nc_v4(src + c);
+      float a = amax8(v, 0.f);
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+      const float s = pow2_scale_from_amax(a);
+      if (live) {
+        *reinterpret_cast<uint2 *>(dst + c) = cast8(v, s);
+        if ((lane & 3) == 0) sf[row * ld_sf + c / 32] = (uint8_t)(254u - (__float_as_uint(s) >> 23));
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ colwise
 // Persistent, TMA-fed.  Work item = (group, tensor, 64-column block), items
 // in order of decreasing group size, handed out one at a time from a counter
@@ -567,6 +600,24 @@ extern "C" int mgemm_quant_rowwise(const void *in, int64_t R, int64_t C, int64_t
   if (nch <= 16) return launch_rowwise<16>(x, R, C, ld_in, out, ld_out, scales, s);
   if (nch <= 24) return launch_rowwise<24>(x, R, C, ld_in, out, ld_out, scales, s);
   return launch_rowwise<0>(x, R, C, ld_in, out, ld_out, scales, s);
+}
+
+extern "C" int mgemm_quant_mx(const void *in, int64_t R, int64_t C, int64_t ld_in, uint8_t *out, int64_t ld_out,
+                              uint8_t *sf, int64_t ld_sf, mgemm_stream_t stream) {
+  if (R < 0 || C < 0) return MGEMM_EINVAL;
+  if (R == 0 || C == 0) return MGEMM_OK;
+  if (!in || !out || !sf) return MGEMM_EINVAL;
+  if (C % 32 || ld_in < C || ld_out < C || ld_sf < C / 32) return MGEMM_EINVAL;
+  if (((uintptr_t)in & 15) || ((uintptr_t)out & 15) || ((uintptr_t)sf & 15) || (ld_in % 8) || (ld_out % 16) ||
+      (ld_sf % 16))
+    return MGEMM_EALIGN;
+  const int64_t blocks_needed = (R + 7) / 8;
+  int sms = sm_count_cached();
+  if (sms <= 0) sms = 148;
+  const int64_t cap = (int64_t)sms * 32;
+  const int blocks = (int)(blocks_needed < cap ? blocks_needed : cap);
+  return launch_pdl(quant_mx_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, 1, "mgemm_quant_mx launch",
+                    (const __nv_bfloat16 *)in, R, C, ld_in, out, ld_out, sf, ld_sf);
 }
 
 extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, const void *in1, int64_t C1,

@@ -110,6 +110,24 @@ def test_host_checks_quant(lib):
     assert lib.mgemm_quant_colwise_grouped(i, 4, 64, i, 64, o, s, None, 0, None, None, 648, None) == -2  # ld % 16
 
 
+def test_host_checks_mx(lib):
+    i, o, s, a = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    q = lib.mgemm_quant_mx
+    assert q(i, 4, 48, 48, o, 48, s, 16, None) == -1           # C % 32
+    assert q(i, 4, 64, 64, o, 64, s, 8, None) == -2            # ld_sf % 16
+    assert q(i, 4, 64, 64, o, 64, s, 0, None) == -1            # ld_sf < C / 32
+    assert q(i, 0, 64, 64, o, 64, s, 16, None) == 0            # empty: no launch
+    assert q(P(0x10008), 4, 64, 64, o, 64, s, 16, None) == -2  # input alignment
+    f = lib.mgemm_fwd_mx
+    assert f(a, i, s, i, s, 16, o, 64, 192, 256, 4, None) == -1     # K % 128
+    assert f(a, i, s, i, s, 16, o, 64, 1024, 256, 4, None) == -1    # ld_sf < K / 32
+    assert f(a, i, s, i, s, 24, o, 64, 512, 256, 4, None) == -2     # ld_sf % 16
+    assert f(a, i, s, i, s, 16, o, 64, 512, 252, 4, None) == -1     # N % 8
+    assert f(a, i, s, i, s, 16, o, 64, 512, 256, 1025, None) == -3  # E
+    assert f(a, None, s, i, s, 16, o, 64, 512, 256, 4, None) == -1  # no x
+    assert f(a, i, s, i, s, 16, o, 0, 512, 256, 4, None) == 0       # M = 0: nothing to do
+
+
 def test_host_checks_moe_align(lib):
     # rejected on the host before any CUDA call, so these run without a GPU
     p = ctypes.c_void_p(0x10000)
