@@ -115,7 +115,7 @@ struct GemmCfg {
   static constexpr int EPI = kEpiWarps;
   static_assert(EPI == 4 || EPI == 8, "one or two epilogue warps per TMEM lane quarter");
   static constexpr int HN = EPI / 4;         // epilogue warps per lane quarter
-  static constexpr int THREADS = 64 + 32 * EPI;
+  static constexpr int THREADS = 64 + 32 * EPI + (kMx ? 32 : 0);  // MXFP8: + the scale warp
   static constexpr int OUT_BUF = 32 * 128;  // 32 rows x 64 bf16 columns
   static constexpr int NBUF = kOutBufs;      // staging buffers per epilogue warp
   static constexpr size_t TAIL_BYTES = 16 * STAGES + 256;  // barriers, flags
@@ -124,7 +124,7 @@ struct GemmCfg {
   // the tensor-memory copy
   static constexpr int SF_STAGE = kMx ? 128 * 16 + BN_MAX * 16 + 2 * 512 : 0;
   static constexpr size_t FIXED_BYTES = 1024 /*align slack*/ + (size_t)EPI * NBUF * OUT_BUF /*epilogue staging*/ +
-                                        (size_t)STAGES * SF_STAGE + TAIL_BYTES;
+                                        (size_t)STAGES * SF_STAGE + (kMx ? 8 * (STAGES + 1) : 0) + TAIL_BYTES;
   // a run-time ring takes what the launch needs, up to the per-CTA limit
   static constexpr size_t SMEM_BYTES =
       kDynRing ? (size_t)227 * 1024 : FIXED_BYTES + (size_t)STAGES * (A_BYTES + B_BYTES);
@@ -320,7 +320,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto sf_tile = [&](int st, int op) -> uint8_t * {
     return sSF + st * C::SF_STAGE + 128 * 16 + C::BN_MAX * 16 + op * 512;
   };
-  uint64_t *full = reinterpret_cast<uint64_t *>(sSF + C::STAGES * C::SF_STAGE);
+  // MXFP8: a stage's scales are in tensor memory (per stage), and the scale
+  // warp's copies have drained (one)
+  uint64_t *sfready = reinterpret_cast<uint64_t *>(sSF + C::STAGES * C::SF_STAGE);
+  uint64_t *sfdrain = sfready + C::STAGES;
+  uint64_t *full = sfready + (C::Mx ? C::STAGES + 1 : 0);
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
@@ -354,6 +358,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&tempty[a], C::Pair ? 2 * C::EPI : (C::EPI == 4 ? 128 : C::EPI));
     }
     mbar_init(drain, 1);
+    if constexpr (C::Mx) {
+      for (int s = 0; s < nst; ++s) mbar_init(&sfready[s], 1);
+      mbar_init(sfdrain, 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -506,7 +514,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * C::BN_MAX;
       for (int kb = 0; kb < ti.kb_count; ++kb) {
-        if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        // MXFP8: the scale warp's barrier (its copies into tensor memory are
+        // done, and it had waited for the stage's data)
+        if (!mbar_wait_warp(C::Mx ? &sfready[stage] : &full[stage], phase, vabort)) { ok = false; break; }
         tc_fence_after();
         uint8_t *a = stage_a(stage);
         uint8_t *b = stage_b(stage);
@@ -531,32 +541,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         }
         if constexpr (C::Mx) {
-          // MXFP8.  The stage's scale rows cover four contraction blocks of 128
-          // (16 bytes per row); word j = kb % 4 of each row holds this block's
-          // four 32-element scales.  Tensor memory takes them as a 512-byte
-          // tile per operand, row l holding rows l, l + 32, l + 64, l + 96 of
-          // the tile (byte 4 m + s: sub-block s of row l + 32 m), copied into
-          // each lane quarter; the MMA of sub-block s reads byte s (the
-          // scale-factor ids of the instruction descriptor).  Lane l of the
-          // MMA warp builds row l of both tiles.
-          const int j = kb & 3;
-          const uint32_t *la = reinterpret_cast<const uint32_t *>(sfa_land(stage));
-          const uint32_t *lb = reinterpret_cast<const uint32_t *>(sfb_land(stage));
-          const uint4 va = make_uint4(la[lane * 4 + j], la[(lane + 32) * 4 + j], la[(lane + 64) * 4 + j],
-                                      la[(lane + 96) * 4 + j]);
-          const uint4 vb = make_uint4(lb[lane * 4 + j], lb[(lane + 32) * 4 + j], lb[(lane + 64) * 4 + j],
-                                      lb[(lane + 96) * 4 + j]);
-          reinterpret_cast<uint4 *>(sf_tile(stage, 0))[lane] = va;
-          reinterpret_cast<uint4 *>(sf_tile(stage, 1))[lane] = vb;
-          fence_proxy_async_smem();  // the tiles are read by tcgen05.cp
-          __syncwarp();
+          // MXFP8: sub-block k of the stage reads byte k of the scale words
+          // (the scale-factor ids of the instruction descriptor)
           if (lane == 0) {
-            // per stage, columns 2 BN_MAX + 8 stage (A) and + 4 (B): the
-            // stage's empty barrier, armed by the commit below, also orders the
-            // copies before the next use of these columns
             const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * 8, sfb_t = sfa_t + 4;
-            tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(smem_u32(sf_tile(stage, 0))));
-            tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(smem_u32(sf_tile(stage, 1))));
             const uint32_t abase = smem_u32(a), bbase = smem_u32(b);
 #pragma unroll
             for (int k = 0; k < C::KSTEPS; ++k) {
@@ -637,6 +625,60 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       else
         mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
+    }
+    __syncwarp();
+  } else if (C::Mx && warp == 2 + C::EPI) {
+    // MXFP8 scale warp.  A stage's scale rows cover four contraction blocks of
+    // 128 (16 bytes per row); word j = kb % 4 of each row holds this block's
+    // four 32-element scales.  Tensor memory takes them as a 512-byte tile per
+    // operand, row l holding rows l, l + 32, l + 64, l + 96 of the tile (byte
+    // 4 m + s: sub-block s of row l + 32 m), copied into each lane quarter at
+    // columns 2 BN_MAX + 8 stage (A) and + 4 (B).  Lane l builds row l of both
+    // tiles; the copies' commit arms the stage's sfready barrier, which the MMA
+    // warp waits for.  The columns are written again only after the stage was
+    // refilled, i.e. after the MMAs that read them.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int j = 0; j * t_step < total && ok; ++j) {
+      const int t = tile_of<C>(j, t_first, t_step);
+      if (t >= total) continue;
+      const TileInfo ti = decode_tile<C>(t, p, av, rank);
+      if (ti.kb_count == 0) continue;
+      for (int kb = 0; kb < ti.kb_count; ++kb) {
+        if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        const int w = kb & 3;
+        const uint32_t *la = reinterpret_cast<const uint32_t *>(sfa_land(stage));
+        const uint32_t *lb = reinterpret_cast<const uint32_t *>(sfb_land(stage));
+        const uint4 va = make_uint4(la[lane * 4 + w], la[(lane + 32) * 4 + w], la[(lane + 64) * 4 + w],
+                                    la[(lane + 96) * 4 + w]);
+        const uint4 vb = make_uint4(lb[lane * 4 + w], lb[(lane + 32) * 4 + w], lb[(lane + 64) * 4 + w],
+                                    lb[(lane + 96) * 4 + w]);
+        reinterpret_cast<uint4 *>(sf_tile(stage, 0))[lane] = va;
+        reinterpret_cast<uint4 *>(sf_tile(stage, 1))[lane] = vb;
+        fence_proxy_async_smem();  // the tiles are read by tcgen05.cp
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * 8, sfb_t = sfa_t + 4;
+          tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(smem_u32(sf_tile(stage, 0))));
+          tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(smem_u32(sf_tile(stage, 1))));
+          mma_commit(&sfready[stage]);
+        }
+        __syncwarp();
+        if (++stage == nst) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) set_status(av.status, MGEMM_STATUS_TIMEOUT);
+      raise_abort();
+    }
+    // every copy this warp issued has landed before tensor memory is freed
+    if (lane == 0) {
+      mma_commit(sfdrain);
+      mbar_wait(sfdrain, 0, nullptr);
     }
     __syncwarp();
   } else {

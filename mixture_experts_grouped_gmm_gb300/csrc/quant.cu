@@ -123,18 +123,26 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(const __nv_bfloat16 *__re
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < R; row += warps_total) {
     const __nv_bfloat16 *src = in + row * ld_in;
     uint8_t *dst = out + row * ld_out;
-    for (int64_t c0 = 0; c0 < C; c0 += 256) {
-      const int64_t c = c0 + lane * 8;
-      const bool live = c < C;  // C % 32 == 0: a block's four lanes agree
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (live) v = ldg_nc_v4(src + c);
-      float a = amax8(v, 0.f);
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-      const float s = pow2_scale_from_amax(a);
-      if (live) {
-        *reinterpret_cast<uint2 *>(dst + c) = cast8(v, s);
-        if ((lane & 3) == 0) sf[row * ld_sf + c / 32] = (uint8_t)(254u - (__float_as_uint(s) >> 23));
+    // four chunks per round, their loads issued first (16 bytes x 4 in flight per lane)
+    for (int64_t c0 = 0; c0 < C; c0 += 1024) {
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t c = c0 + i * 256 + lane * 8;
+        v[i] = c < C ? ldg_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t c = c0 + i * 256 + lane * 8;
+        const bool live = c < C;  // C % 32 == 0: a block's four lanes agree
+        float a = amax8(v[i], 0.f);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const float s = pow2_scale_from_amax(a);
+        if (live) {
+          *reinterpret_cast<uint2 *>(dst + c) = cast8(v[i], s);
+          if ((lane & 3) == 0) sf[row * ld_sf + c / 32] = (uint8_t)(254u - (__float_as_uint(s) >> 23));
+        }
       }
     }
   }
