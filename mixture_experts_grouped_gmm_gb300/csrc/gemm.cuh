@@ -119,12 +119,17 @@ struct GemmCfg {
   static constexpr int OUT_BUF = 32 * 128;  // 32 rows x 64 bf16 columns
   static constexpr int NBUF = kOutBufs;      // staging buffers per epilogue warp
   static constexpr size_t TAIL_BYTES = 16 * STAGES + 256;  // barriers, flags
-  // MXFP8, per stage: the scale rows of A (128 x 16 B, four contraction blocks)
-  // and of B (BN x 16 B) as loaded, and the two 512-byte tiles rearranged for
-  // the tensor-memory copy
-  static constexpr int SF_STAGE = kMx ? 128 * 16 + BN_MAX * 16 + 2 * 512 : 0;
+  // MXFP8: per stage, the two 512-byte scale tiles rearranged for the
+  // tensor-memory copy; and a ring of SF_SLOTS slots holding the scale rows
+  // of A (128 x 16 B) and B (BN x 16 B) as loaded, one slot per four
+  // contraction blocks
+  static constexpr int SF_STAGE = kMx ? 2 * 512 : 0;
+  static constexpr int SF_SLOTS = 2;
+  static constexpr int SF_SLOT = kMx ? 128 * 16 + BN_MAX * 16 : 0;
+  static constexpr size_t SF_BYTES = (size_t)STAGES * SF_STAGE + (size_t)SF_SLOTS * SF_SLOT;
+  static constexpr size_t SF_BARS = kMx ? 8 * (STAGES + 1 + 2 * SF_SLOTS) : 0;
   static constexpr size_t FIXED_BYTES = 1024 /*align slack*/ + (size_t)EPI * NBUF * OUT_BUF /*epilogue staging*/ +
-                                        (size_t)STAGES * SF_STAGE + (kMx ? 8 * (STAGES + 1) : 0) + TAIL_BYTES;
+                                        SF_BYTES + SF_BARS + TAIL_BYTES;
   // a run-time ring takes what the launch needs, up to the per-CTA limit
   static constexpr size_t SMEM_BYTES =
       kDynRing ? (size_t)227 * 1024 : FIXED_BYTES + (size_t)STAGES * (A_BYTES + B_BYTES);
@@ -313,18 +318,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto stage_b = [&](int st) -> uint8_t * {
     return C::DynRing ? smem + (size_t)st * p.stage_bytes + C::KC * p.a_rows * 128 : sB + st * C::B_BYTES;
   };
-  // MXFP8 scale rows (per stage: A as loaded, B as loaded, A and B tiles for the copy)
+  // MXFP8 scales: per stage the A and B tiles for the copy, then the slots of loaded scale rows
   uint8_t *sSF = sOut + C::EPI * C::NBUF * C::OUT_BUF;
-  auto sfa_land = [&](int st) -> uint8_t * { return sSF + st * C::SF_STAGE; };
-  auto sfb_land = [&](int st) -> uint8_t * { return sSF + st * C::SF_STAGE + 128 * 16; };
-  auto sf_tile = [&](int st, int op) -> uint8_t * {
-    return sSF + st * C::SF_STAGE + 128 * 16 + C::BN_MAX * 16 + op * 512;
-  };
-  // MXFP8: a stage's scales are in tensor memory (per stage), and the scale
-  // warp's copies have drained (one)
-  uint64_t *sfready = reinterpret_cast<uint64_t *>(sSF + C::STAGES * C::SF_STAGE);
+  auto sf_tile = [&](int st, int op) -> uint8_t * { return sSF + st * C::SF_STAGE + op * 512; };
+  auto sfa_slot = [&](int q) -> uint8_t * { return sSF + C::STAGES * C::SF_STAGE + q * C::SF_SLOT; };
+  auto sfb_slot = [&](int q) -> uint8_t * { return sSF + C::STAGES * C::SF_STAGE + q * C::SF_SLOT + 128 * 16; };
+  // MXFP8 barriers: a stage's scales are in tensor memory; the scale warp's
+  // copies have drained; a slot of scale rows has landed / is free again
+  uint64_t *sfready = reinterpret_cast<uint64_t *>(sSF + C::SF_BYTES);
   uint64_t *sfdrain = sfready + C::STAGES;
-  uint64_t *full = sfready + (C::Mx ? C::STAGES + 1 : 0);
+  uint64_t *sf_full = sfdrain + 1;
+  uint64_t *sf_empty = sf_full + C::SF_SLOTS;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sSF + C::SF_BYTES + C::SF_BARS);
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
@@ -361,6 +366,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if constexpr (C::Mx) {
       for (int s = 0; s < nst; ++s) mbar_init(&sfready[s], 1);
       mbar_init(sfdrain, 1);
+      for (int q = 0; q < C::SF_SLOTS; ++q) {
+        mbar_init(&sf_full[q], 1);
+        mbar_init(&sf_empty[q], 1);
+      }
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   };
 
   // Producer bookkeeping kept for the drain after an abort.
-  uint32_t issued = 0;
+  uint32_t issued = 0, sf_issued = 0;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -408,8 +417,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // that are never stored
       // pair: the leader's full barrier counts the bytes of both CTAs
       const uint32_t tx = C::Pair ? 2u * (uint32_t)(C::A_BYTES + (bn / 2) * 128)
-                                  : C::KC * ((C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128) +
-                                        (C::Mx ? (uint32_t)(128 * 16 + bn * 16) : 0u);
+                                  : C::KC * ((C::Mode == kModeRows ? p.a_rows * 128 : C::A_BYTES) + bn * 128);
+      int qslot = 0;
+      uint32_t qphase = 0;
       for (int j = 0; j * t_step < total && !*vabort; ++j) {
         const int t = tile_of<C>(j, t_first, t_step);
         if (t >= total) continue;
@@ -422,6 +432,26 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           uint8_t *a = stage_a(stage);
           uint8_t *b = stage_b(stage);
+          if constexpr (C::Mx) {
+            if ((kb & 3) == 0) {
+              // the scale rows of this and the next three contraction blocks
+              // (16 bytes per row; x is a multiple of 16 bytes): A rows of the
+              // tile, and rows e N + n0 .. of B's [E N, ld_sf] scales
+              if (!mbar_wait(&sf_empty[qslot], qphase ^ 1, vabort)) {
+                set_status(av.status, MGEMM_STATUS_TIMEOUT);
+                raise_abort();
+                break;
+              }
+              mbar_arrive_expect_tx(&sf_full[qslot], (uint32_t)(128 * 16 + bn * 16));
+              ++sf_issued;
+              tma_load_2d(sfa_slot(qslot), &tmSFA, &sf_full[qslot], (kb >> 2) * 16, ti.a_row);
+              tma_load_2d(sfb_slot(qslot), &tmSFB, &sf_full[qslot], (kb >> 2) * 16, ti.e * p.Nout + ti.n0);
+              if (++qslot == C::SF_SLOTS) {
+                qslot = 0;
+                qphase ^= 1;
+              }
+            }
+          }
           if constexpr (C::Pair) {
             static_assert(C::Pair ? (C::Fp8 && !C::AMn && !C::BMn) : true, "CTA pairs serve K-major FP8 operands");
             // each CTA copies its own halves; the peer's copies complete on the leader's barrier
@@ -472,13 +502,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tma_load_3d(b, &tmB, &full[stage], kb * C::BK, ti.n0, ti.e);
               }
             }
-            if constexpr (C::Mx) {
-              // the scale rows of four contraction blocks (16 bytes per row;
-              // x is a multiple of 16 bytes): A rows of the tile, and rows
-              // e N + n0 .. of B's [E N, ld_sf] scales
-              tma_load_2d(sfa_land(stage), &tmSFA, &full[stage], (kb >> 2) * 16, ti.a_row);
-              tma_load_2d(sfb_land(stage), &tmSFB, &full[stage], (kb >> 2) * 16, ti.e * p.Nout + ti.n0);
-            }
           } else {
             const int xr = ti.x0 + kb * C::BK;
             if (C::AMn) {
@@ -514,9 +537,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * C::BN_MAX;
       for (int kb = 0; kb < ti.kb_count; ++kb) {
-        // MXFP8: the scale warp's barrier (its copies into tensor memory are
-        // done, and it had waited for the stage's data)
-        if (!mbar_wait_warp(C::Mx ? &sfready[stage] : &full[stage], phase, vabort)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        // MXFP8: and the stage's scales are in tensor memory
+        if (C::Mx && !mbar_wait_warp(&sfready[stage], phase, vabort)) { ok = false; break; }
         tc_fence_after();
         uint8_t *a = stage_a(stage);
         uint8_t *b = stage_b(stage);
@@ -628,17 +651,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     __syncwarp();
   } else if (C::Mx && warp == 2 + C::EPI) {
-    // MXFP8 scale warp.  A stage's scale rows cover four contraction blocks of
-    // 128 (16 bytes per row); word j = kb % 4 of each row holds this block's
-    // four 32-element scales.  Tensor memory takes them as a 512-byte tile per
-    // operand, row l holding rows l, l + 32, l + 64, l + 96 of the tile (byte
-    // 4 m + s: sub-block s of row l + 32 m), copied into each lane quarter at
-    // columns 2 BN_MAX + 8 stage (A) and + 4 (B).  Lane l builds row l of both
-    // tiles; the copies' commit arms the stage's sfready barrier, which the MMA
-    // warp waits for.  The columns are written again only after the stage was
-    // refilled, i.e. after the MMAs that read them.
-    int stage = 0;
-    uint32_t phase = 0;
+    // MXFP8 scale warp.  A slot holds the scale rows of four contraction
+    // blocks of 128 (16 bytes per row); word w = kb % 4 of each row holds
+    // block kb's four 32-element scales.  Tensor memory takes them as a
+    // 512-byte tile per operand, row l holding rows l, l + 32, l + 64, l + 96
+    // of the tile (byte 4 m + s: sub-block s of row l + 32 m), copied into
+    // each lane quarter at columns 2 BN_MAX + 8 stage (A) and + 4 (B).  Lane
+    // l builds row l of both tiles.  A stage's tiles and columns are reused
+    // once its previous MMAs are done (its empty barrier, which the producer
+    // waits for too); the copies' commit arms the stage's sfready barrier,
+    // which the MMA warp waits for; a slot is released after its fourth block
+    // (or the tile's last).
+    int stage = 0, qslot = 0;
+    uint32_t phase = 0, qphase = 0;
     bool ok = true;
     for (int j = 0; j * t_step < total && ok; ++j) {
       const int t = tile_of<C>(j, t_first, t_step);
@@ -646,10 +671,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const TileInfo ti = decode_tile<C>(t, p, av, rank);
       if (ti.kb_count == 0) continue;
       for (int kb = 0; kb < ti.kb_count; ++kb) {
-        if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1, vabort)) { ok = false; break; }
+        if ((kb & 3) == 0 && !mbar_wait_warp(&sf_full[qslot], qphase, vabort)) { ok = false; break; }
         const int w = kb & 3;
-        const uint32_t *la = reinterpret_cast<const uint32_t *>(sfa_land(stage));
-        const uint32_t *lb = reinterpret_cast<const uint32_t *>(sfb_land(stage));
+        const uint32_t *la = reinterpret_cast<const uint32_t *>(sfa_slot(qslot));
+        const uint32_t *lb = reinterpret_cast<const uint32_t *>(sfb_slot(qslot));
         const uint4 va = make_uint4(la[lane * 4 + w], la[(lane + 32) * 4 + w], la[(lane + 64) * 4 + w],
                                     la[(lane + 96) * 4 + w]);
         const uint4 vb = make_uint4(lb[lane * 4 + w], lb[(lane + 32) * 4 + w], lb[(lane + 64) * 4 + w],
@@ -663,8 +689,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(smem_u32(sf_tile(stage, 0))));
           tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(smem_u32(sf_tile(stage, 1))));
           mma_commit(&sfready[stage]);
+          if (w == 3 || kb == ti.kb_count - 1) mbar_arrive(&sf_empty[qslot]);  // the slot's rows are read
         }
         __syncwarp();
+        if (w == 3 || kb == ti.kb_count - 1) {
+          if (++qslot == C::SF_SLOTS) {
+            qslot = 0;
+            qphase ^= 1;
+          }
+        }
         if (++stage == nst) {
           stage = 0;
           phase ^= 1;
@@ -954,6 +987,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int s = 0; s < nst; ++s) {
       const uint32_t armed = issued / nst + ((uint32_t)s < issued % nst ? 1u : 0u);
       if (armed) mbar_wait(&full[s], (armed - 1) & 1, nullptr);
+    }
+    if constexpr (C::Mx) {  // and the scale-row copies
+      for (int q = 0; q < C::SF_SLOTS; ++q) {
+        const uint32_t armed = sf_issued / C::SF_SLOTS + ((uint32_t)q < sf_issued % C::SF_SLOTS ? 1u : 0u);
+        if (armed) mbar_wait(&sf_full[q], (armed - 1) & 1, nullptr);
+      }
     }
     // pair: copies a peer issued for stages its leader never armed are not
     // counted anywhere; give them far longer than a copy takes to land
