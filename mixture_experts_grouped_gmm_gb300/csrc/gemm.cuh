@@ -85,8 +85,9 @@ struct GemmCfg {
   // elements of every row, applied by block-scaled MMAs (no epilogue scales)
   static constexpr bool Mx = kMx;
   static constexpr bool Scaled = kFp8 && !kMx;  // FP8 with row / column scales in the epilogue
-  static_assert(!kMx || (kFp8 && kMode == kModeRows && !kAMn && !kBMn && !kPair && !kDynRing && kBnMax == 128),
-                "MXFP8: rows schedule, K-major operands, 128-wide tiles");
+  static_assert(!kMx || (kFp8 && kMode == kModeRows && !kAMn && !kBMn && !kPair && !kDynRing &&
+                          (kBnMax == 128 || kBnMax == 192)),
+                "MXFP8: rows schedule, K-major operands, 128- or 192-wide tiles");
   static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
   static constexpr bool BMn = kBMn;
   static constexpr int Mode = kMode;
@@ -123,7 +124,9 @@ struct GemmCfg {
   // tensor-memory copy; and a ring of SF_SLOTS slots holding the scale rows
   // of A (128 x 16 B) and B (BN x 16 B) as loaded, one slot per four
   // contraction blocks
-  static constexpr int SF_STAGE = kMx ? 2 * 512 : 0;
+  static constexpr int SF_TILES_B = BN_MAX > 128 ? 2 : 1;  // B scale tiles per stage (128 columns each)
+  static constexpr int SF_STAGE = kMx ? (1 + SF_TILES_B) * 512 : 0;
+  static constexpr int SF_COLS = 4 + 4 * SF_TILES_B;        // tensor-memory columns of a stage's scales
   static constexpr int SF_SLOTS = 2;
   static constexpr int SF_SLOT = kMx ? 128 * 16 + BN_MAX * 16 : 0;
   static constexpr size_t SF_BYTES = (size_t)STAGES * SF_STAGE + (size_t)SF_SLOTS * SF_SLOT;
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // MXFP8: sub-block k of the stage reads byte k of the scale words
           // (the scale-factor ids of the instruction descriptor)
           if (lane == 0) {
-            const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * 8, sfb_t = sfa_t + 4;
+            const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * C::SF_COLS, sfb_t = sfa_t + 4;
             const uint32_t abase = smem_u32(a), bbase = smem_u32(b);
 #pragma unroll
             for (int k = 0; k < C::KSTEPS; ++k) {
@@ -656,7 +659,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // block kb's four 32-element scales.  Tensor memory takes them as a
     // 512-byte tile per operand, row l holding rows l, l + 32, l + 64, l + 96
     // of the tile (byte 4 m + s: sub-block s of row l + 32 m), copied into
-    // each lane quarter at columns 2 BN_MAX + 8 stage (A) and + 4 (B).  Lane
+    // each lane quarter at columns 2 BN_MAX + SF_COLS stage (A) and + 4 (B).  Lane
     // l builds row l of both tiles.  A stage's tiles and columns are reused
     // once its previous MMAs are done (its empty barrier, which the producer
     // waits for too); the copies' commit arms the stage's sfready barrier,
@@ -682,12 +685,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                     lb[(lane + 96) * 4 + w]);
         reinterpret_cast<uint4 *>(sf_tile(stage, 0))[lane] = va;
         reinterpret_cast<uint4 *>(sf_tile(stage, 1))[lane] = vb;
+        if constexpr (C::SF_TILES_B > 1) {
+          // B columns 128 .. BN_MAX - 1 (the slot has BN_MAX rows; the rest are zero)
+          const uint4 vc = make_uint4(lb[(lane + 128) * 4 + w], lb[(lane + 160) * 4 + w],
+                                      C::BN_MAX > 192 ? lb[(lane + 192) * 4 + w] : 0u,
+                                      C::BN_MAX > 224 ? lb[(lane + 224) * 4 + w] : 0u);
+          reinterpret_cast<uint4 *>(sf_tile(stage, 2))[lane] = vc;
+        }
         fence_proxy_async_smem();  // the tiles are read by tcgen05.cp
         __syncwarp();
         if (lane == 0) {
-          const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * 8, sfb_t = sfa_t + 4;
+          // column n of B reads the word at column sfb_t + n / 32: the second
+          // B tile (columns 128 ..) sits 4 columns after the first
+          const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * C::SF_COLS, sfb_t = sfa_t + 4;
           tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(smem_u32(sf_tile(stage, 0))));
           tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(smem_u32(sf_tile(stage, 1))));
+          if constexpr (C::SF_TILES_B > 1)
+            tmem_cp_32x128b_warpx4(sfb_t + 4, smem_desc_rows16(smem_u32(sf_tile(stage, 2))));
           mma_commit(&sfready[stage]);
           if (w == 3 || kb == ti.kb_count - 1) mbar_arrive(&sf_empty[qslot]);  // the slot's rows are read
         }

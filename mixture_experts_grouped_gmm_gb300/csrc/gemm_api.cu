@@ -275,7 +275,8 @@ extern "C" int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *s
   if (rc) return rc;
   const int sms = sm_count();
   if (sms <= 0) return MGEMM_ECUDA;
-  const int bn = 128;
+  // 192-wide tiles (less operand traffic per FLOP) unless N fits one 128-wide tile
+  const int bn = N > 128 ? 192 : 128;
   CUtensorMap ta, tb, to, tsa, tsb;
   {
     const uint64_t d[2] = {(uint64_t)K, (uint64_t)M};
@@ -316,7 +317,8 @@ extern "C" int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *s
   const int64_t upper = ((M + 127) / 128 + (M < E ? M : E)) * p.n_tiles;
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
-  return gemm_fp8_rows_mx(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
+  return bn == 192 ? gemm_fp8_rows_mx192(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream)
+                   : gemm_fp8_rows_mx(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
 }
 
 extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,

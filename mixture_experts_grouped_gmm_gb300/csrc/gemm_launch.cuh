@@ -41,6 +41,8 @@ int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o
 // MXFP8: e4m3 x [M, K] and w [E, N, K] with e8m0 scale rows (maps sfa, sfb), 128-wide tiles
 int gemm_fp8_rows_mx(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
                      const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
+int gemm_fp8_rows_mx192(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
+                        const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)
 int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s);
