@@ -22,6 +22,10 @@ Readings (the page is silent on the arithmetic):
   out[r, n] = sum_k xv[r, k] * wv[e, n, k] (forward, w stored [E, N, K]);
   dgrad is the same contraction with grad_out and w stored [E, K, N]
   quantized along N.
+* wgrad contracts over the token rows of a group, so its blocks run down the
+  columns: 32 consecutive rows of one column counted from the group's first
+  row (the page's 32-row padding of the groups makes every block whole; here
+  a group's last block may be short and its missing rows count as zeros).
 
 Arithmetic: float64 numpy, ``np.matmul`` per group as the contraction.
 """
@@ -71,4 +75,50 @@ def gmm_fwd_mx(xq, xs, wq, ws, group_sizes):
         r0, r1 = int(off[e]), int(off[e + 1])
         if r1 > r0:
             out[r0:r1] = x[r0:r1] @ w[e].T
+    return out
+
+
+def quant_mx_colwise_grouped(x, offsets):
+    """Per-group colwise MX quantize (the wgrad operands): in each group g
+    (rows offsets[g] .. offsets[g+1]) and column c, blocks of 32 consecutive
+    rows counted from the group's first row; the last block of a group may be
+    short (its missing rows count as zeros, which do not change the maximum).
+
+    x: [M, C] float64 holding bf16 values; offsets: G + 1 exclusive offsets.
+    Returns (codes_t uint8 [C, M], e8m0: list over groups of uint8
+    [C, ceil(m_g / 32)]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    M, C = x.shape
+    codes_t = np.zeros((C, M), dtype=np.uint8)
+    scales = []
+    for g in range(len(offsets) - 1):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        nb = -(-(r1 - r0) // MX_BLOCK)
+        blk = np.zeros((nb * MX_BLOCK, C))
+        blk[:r1 - r0] = x[r0:r1]
+        q, e = quant_mx_rows(blk.T.copy())          # rows = columns of x, blocks along the group's rows
+        codes_t[:, r0:r1] = q[:, :r1 - r0]
+        scales.append(e)
+    return codes_t, scales
+
+
+def gmm_wgrad_mx(xq_t, xs, goq_t, gos, group_sizes):
+    """grad_w[e] = sum over the rows of group e of x_r^T go_r on decoded MX
+    values.  xq_t [K, M], goq_t [N, M] (column-major codes); xs, gos: per-group
+    lists of [K or N, ceil(m_e / 32)] e8m0 bytes (blocks along the group's
+    rows) -> [E, K, N]; zero for an empty group."""
+    K, N = xq_t.shape[0], goq_t.shape[0]
+    E = len(group_sizes)
+    out = np.zeros((E, K, N))
+    off = np.concatenate([[0], np.cumsum(np.asarray(group_sizes, dtype=np.int64))])
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        nb = xs[e].shape[1]
+        pad = nb * MX_BLOCK - (r1 - r0)
+        xa = np.concatenate([xq_t[:, r0:r1], np.zeros((K, pad), dtype=np.uint8)], axis=1)
+        ga = np.concatenate([goq_t[:, r0:r1], np.zeros((N, pad), dtype=np.uint8)], axis=1)
+        out[e] = decode_mx(xa, xs[e]) @ decode_mx(ga, gos[e]).T
     return out

@@ -107,3 +107,62 @@ def test_gemm_brute_force():
                     b = dv[int(wq[e, n, k])] * 2.0 ** (int(ws[e, n, k // 32]) - 127)
                     acc += a * b
                 assert abs(out[r, n] - acc) <= 1e-12 * max(1.0, abs(acc)), (e, r, n)
+
+
+def test_colwise_one_block_groups_reduce_to_fp8_colwise():
+    # groups of at most 32 rows hold one block per column: the MX colwise codes
+    # equal the per-group colwise FP8 codes, and 2^(127 - byte) its scales
+    from oracle.mx import quant_mx_colwise_grouped
+    from oracle.quant import quant_colwise_grouped
+
+    rng = np.random.default_rng(5)
+    sizes = [32, 0, 7, 19]
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    x = (rng.standard_normal((off[-1], 24)) * np.exp2(rng.integers(-9, 9, (1, 24)))).astype(np.float32)
+    x = x.astype(np.float64)
+    q, e = quant_mx_colwise_grouped(x, off)
+    qf, sf = quant_colwise_grouped(x, off)
+    assert np.array_equal(q, qf)
+    for g, m in enumerate(sizes):
+        if m:
+            assert np.array_equal(np.exp2(127.0 - e[g][:, 0].astype(np.float64)), sf[g * 24:(g + 1) * 24])
+        else:
+            assert e[g].shape == (24, 0)
+
+
+def test_colwise_blocks_start_at_each_group():
+    from oracle.mx import quant_mx_colwise_grouped
+
+    x = np.zeros((70, 2))
+    x[:40, 0] = 1.0           # group 0: rows 0..39 -> blocks [0, 32), [32, 40)
+    x[39, 0] = 100.0          # only the second block of group 0 sees 100
+    x[40:70, 0] = 2.0         # group 1: rows 40..69 -> one block
+    q, e = quant_mx_colwise_grouped(x, [0, 40, 70])
+    # amax 1 -> s 256 (byte 119); amax 100 -> 448/100 -> s 4 (byte 125); amax 2 -> s 128 (byte 120)
+    assert e[0][0].tolist() == [119, 125] and e[1][0].tolist() == [120]
+    assert e[0][1].tolist() == [127 - 48, 127 - 48] and e[1][1].tolist() == [127 - 48]
+
+
+def test_wgrad_brute_force():
+    from oracle.mx import gmm_wgrad_mx, quant_mx_colwise_grouped
+
+    rng = np.random.default_rng(6)
+    sizes = [5, 0, 40]
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    M, K, N = off[-1], 3, 4
+    x = rng.standard_normal((M, K)).astype(np.float32).astype(np.float64)
+    go = rng.standard_normal((M, N)).astype(np.float32).astype(np.float64)
+    xq, xs = quant_mx_colwise_grouped(x, off)
+    gq, gs = quant_mx_colwise_grouped(go, off)
+    out = gmm_wgrad_mx(xq, xs, gq, gs, sizes)
+    dv = {c: float(decode_e4m3(np.array([c], dtype=np.uint8))[0]) for c in range(256)}
+    for e in range(3):
+        for k in range(K):
+            for n in range(N):
+                acc = 0.0
+                for r in range(off[e], off[e + 1]):
+                    b = (r - off[e]) // 32
+                    acc += dv[int(xq[k, r])] * 2.0 ** (int(xs[e][k, b]) - 127) * \
+                        dv[int(gq[n, r])] * 2.0 ** (int(gs[e][n, b]) - 127)
+                assert abs(out[e, k, n] - acc) <= 1e-12 * max(1.0, abs(acc))
+    assert not out[1].any()
