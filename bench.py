@@ -319,7 +319,11 @@ def deepseek_mx_extra(torch, B, dev, pk, tokens=16384, reps=10):
              wq=torch.empty(E * N, K, dtype=u8, device=dev), sw=torch.empty(E * N, lk, dtype=u8, device=dev),
              wdq=torch.empty(E * K, N, dtype=u8, device=dev), swd=torch.empty(E * K, ln, dtype=u8, device=dev),
              out=torch.empty(M, N, dtype=bf, device=dev), gx=torch.empty(M, K, dtype=bf, device=dev))
-    names = ["quant_w", "quant_x", "fwd", "quant_go", "dgrad"]
+    ld = B.mgemm_colwise_ld(M, E)  # padded column-major layout of the wgrad operands
+    T.update(xqt=torch.empty(K * ld, dtype=u8, device=dev), sxc=torch.empty(ld // 128 * K * 4, dtype=u8, device=dev),
+             gqt=torch.empty(N * ld, dtype=u8, device=dev), sgc=torch.empty(ld // 128 * N * 4, dtype=u8, device=dev),
+             gw=torch.empty(E, K, N, dtype=bf, device=dev))
+    names = ["quant_w", "quant_x", "fwd", "quant_go", "dgrad", "colwise_dual", "wgrad"]
 
     def step(ev=None):
         def mark(i):
@@ -331,25 +335,34 @@ def deepseek_mx_extra(torch, B, dev, pk, tokens=16384, reps=10):
         mark(2); B.mgemm_fwd_mx(T["args"], T["xq"], T["sx"], T["wq"].view(E, N, K), T["sw"], T["out"], M, K, N, E)
         mark(3); B.mgemm_quant_mx(go, T["goq"], T["sgo"])
         mark(4); B.mgemm_fwd_mx(T["args"], T["goq"], T["sgo"], T["wdq"].view(E, K, N), T["swd"], T["gx"], M, N, K, E)
-        mark(5)
+        mark(5); B.mgemm_quant_colwise_mx(T["args"], E, M, go, T["gqt"], T["sgc"], x, T["xqt"], T["sxc"], ld)
+        mark(6); B.mgemm_wgrad_mx(T["args"], T["xqt"], T["sxc"], T["gqt"], T["sgc"], T["gw"], M, K, N, E, ld)
+        mark(7)
 
     for _ in range(3):
         step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(reps)]
     for r in range(reps):
         step(evs[r])
     torch.cuda.synchronize()
     t = {n: statistics.median(evs[r][i].elapsed_time(evs[r][i + 1]) * 1e3 for r in range(reps))
          for i, n in enumerate(names)}
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for r in range(reps):
+        step()
+    s1.record()
+    torch.cuda.synchronize()
+    step_us = s0.elapsed_time(s1) * 1e3 / reps
     fl = 2 * M * K * N
     fp8_peak = 2 * pk["bf16_tflops"]
     byts = {"quant_w": 2 * E * N * K * 3 + E * (N * lk + K * ln), "quant_x": M * K * 3 + M * lk,
-            "quant_go": M * N * 3 + M * ln}
+            "quant_go": M * N * 3 + M * ln, "colwise_dual": M * (K + N) * 3 + M // 32 * (K + N)}
     kern = {}
     for n in names:
         k = {"us": round(t[n], 2)}
-        if n in ("fwd", "dgrad"):
+        if n in ("fwd", "dgrad", "wgrad"):
             k["tflops"] = round(fl / (t[n] * 1e-6) / 1e12, 1)
             k["tensor_frac_fp8"] = round(fl / (t[n] * 1e-6) / 1e12 / fp8_peak, 3)
         if n in byts:
@@ -359,6 +372,8 @@ def deepseek_mx_extra(torch, B, dev, pk, tokens=16384, reps=10):
         kern[n] = k
     out = {"shape": f"M={M} K={K} N={N} E={E} (the DeepSeek step's routing), e4m3 codes, one e8m0 scale per "
                     "32 contraction elements, bf16 outputs",
+           "step_us": round(step_us, 1), "gemm_tflops": round(3 * fl / (sum(t[n] for n in ("fwd", "dgrad", "wgrad"))
+                                                                    * 1e-6) / 1e12, 1),
            "fp8_peak_tflops": round(fp8_peak, 1), "kernels": kern}
     del T, d, w_nk
     return out

@@ -239,6 +239,43 @@ int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *sx, const ui
                  int64_t ld_sf, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream);
 
 /*
+ * mgemm_quant_colwise_mx -- per-group colwise MX blocks, the MXFP8 wgrad
+ * operands (one or two tensors per launch).  Reading of [FP8]'s MXFP8 path
+ * (groups padded to 32 rows): in group g and column c, blocks of 32
+ * consecutive rows counted from the group's first row (a group's last block
+ * may be short; its missing rows count as zeros); each block's scale and codes
+ * follow mgemm_quant_mx.
+ *   in1   bf16 [M, C1] row-major (C1 % 8 == 0); optionally in2 [M, C2] (dual)
+ *   out1  e4m3 [C1, ld]: the padded column-major layout of
+ *         mgemm_quant_colwise_grouped (group g's codes at column offset
+ *         poffsets[g], zeros after them up to a multiple of MGEMM_COL_PAD)
+ *   sf1   e8m0 [ld / 128][C1][4]: for padded row block j (rows 128 j .. 128 j +
+ *         127) and column c, the 4 bytes of its four 32-row blocks
+ *         ((ld / 128) * C1 * 4 bytes, 16-byte aligned)
+ *   ld    bytes per column: >= mgemm_colwise_ld(M, E), % 128 == 0
+ * Only bytes inside the padded total (poffsets[E]) are written.
+ * Errors: -1 (sizes, NULL), -2 (alignment), -3 (E).
+ */
+int mgemm_quant_colwise_mx(const void *args, int E, int64_t M, const void *in1, int64_t C1, uint8_t *out1,
+                           uint8_t *sf1, const void *in2, int64_t C2, uint8_t *out2, uint8_t *sf2, int64_t ld,
+                           mgemm_stream_t stream);
+
+/*
+ * mgemm_wgrad_mx -- the MXFP8 wgrad: grad_w[e] = sum over the rows r of group e
+ * of xv[r, :]^T gov[r, :], with the decoded block-scaled values of
+ * mgemm_quant_colwise_mx (blocks of 32 rows of a group); zero for an empty
+ * group.  Block-scaled tensor-core MMAs, fp32 accumulation, bf16 output.
+ *   x, sx    x's codes [K, ld] and scale rows [ld / 128][K][4] (mgemm_quant_colwise_mx)
+ *   grad_out, sgo   likewise [N, ld] and [ld / 128][N][4]
+ *   grad_w   bf16 [E, K, N]; every element is written
+ *   ld       as passed to mgemm_quant_colwise_mx
+ * K % 16 == 0, N % 16 == 0.  Errors: -1, -2, -3, -4 as mgemm_wgrad.
+ */
+int mgemm_wgrad_mx(const void *args, const uint8_t *x, const uint8_t *sx, const uint8_t *grad_out,
+                   const uint8_t *sgo, void *grad_w, int64_t M, int K, int N, int E, int64_t ld,
+                   mgemm_stream_t stream);
+
+/*
  * mgemm_wgrad -- grad_w[e] = x_e^T . grad_out_e, contracting over the m_e rows
  * of group e ("dynamic k"); grad_w[e] = 0 when m_e = 0.
  * [GRB review, fill_arguments.cuh]: problems sorted by k descending;

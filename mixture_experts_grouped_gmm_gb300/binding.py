@@ -49,6 +49,13 @@ _SIGS = {
     "mgemm_fwd_mx": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "mgemm_quant_colwise_mx": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                                              ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                              ctypes.c_void_p]),
+    "mgemm_wgrad_mx": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int64, ctypes.c_void_p]),
     "mgemm_colwise_ld": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int]),
     "mgemm_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -167,6 +174,25 @@ def mgemm_fwd_mx(args, x, sx, w, sw, out, M, K, N, E):
     _cuda(args, x, sx, w, sw, out)
     _check(lib().mgemm_fwd_mx(_p(args), _p(x), _p(sx), _p(w), _p(sw), sx.stride(0), _p(out), int(M), int(K), int(N),
                               int(E), _stream(out)), "mgemm_fwd_mx")
+
+
+def mgemm_quant_colwise_mx(args, E, M, x1, out1, sf1, x2=None, out2=None, sf2=None, ld=None):
+    """Per-group colwise MX blocks of x1 [M, C1] (and x2 [M, C2]) into the padded
+    column-major codes out1 [C1 * ld] and scale rows sf1 [ld / 128 * C1 * 4]."""
+    _cuda(args, x1, out1, sf1, x2, out2, sf2)
+    ld = ld or mgemm_colwise_ld(M, E)
+    C2 = x2.shape[1] if x2 is not None else 0
+    _check(lib().mgemm_quant_colwise_mx(_p(args), int(E), int(M), _p(x1), x1.shape[1], _p(out1), _p(sf1), _p(x2),
+                                        int(C2), _p(out2), _p(sf2), int(ld), _stream(x1)),
+           "mgemm_quant_colwise_mx")
+
+
+def mgemm_wgrad_mx(args, x, sx, go, sgo, grad_w, M, K, N, E, ld=None):
+    """MXFP8 wgrad on the outputs of mgemm_quant_colwise_mx -> grad_w bf16 [E, K, N]."""
+    _cuda(args, x, sx, go, sgo, grad_w)
+    ld = ld or mgemm_colwise_ld(M, E)
+    _check(lib().mgemm_wgrad_mx(_p(args), _p(x), _p(sx), _p(go), _p(sgo), _p(grad_w), int(M), int(K), int(N), int(E),
+                                int(ld), _stream(grad_w)), "mgemm_wgrad_mx")
 
 
 def mgemm_colwise_ld(M, E):

@@ -85,9 +85,12 @@ struct GemmCfg {
   // elements of every row, applied by block-scaled MMAs (no epilogue scales)
   static constexpr bool Mx = kMx;
   static constexpr bool Scaled = kFp8 && !kMx;  // FP8 with row / column scales in the epilogue
-  static_assert(!kMx || (kFp8 && kMode == kModeRows && !kAMn && !kBMn && !kPair && !kDynRing &&
-                          (kBnMax == 128 || kBnMax == 192)),
-                "MXFP8: rows schedule, K-major operands, 128- or 192-wide tiles");
+  static_assert(!kMx || (kFp8 && !kAMn && !kBMn && !kPair && !kDynRing && (kBnMax == 128 || kBnMax == 192)),
+                "MXFP8: K-major operands, 128- or 192-wide tiles");
+  // MXFP8 scale rows per contraction block: the rows schedule's scale rows
+  // are [rows][ld_sf] (16 bytes = four blocks per row); the experts schedule's
+  // (wgrad) are k-block-major [blocks][rows][4 B] (one block per load)
+  static constexpr int KPS = kMode == kModeRows ? 4 : 1;
   static constexpr bool AMn = kAMn;  // A stored MN-major (contraction is the strided dim)
   static constexpr bool BMn = kBMn;
   static constexpr int Mode = kMode;
@@ -436,19 +439,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           uint8_t *a = stage_a(stage);
           uint8_t *b = stage_b(stage);
           if constexpr (C::Mx) {
-            if ((kb & 3) == 0) {
-              // the scale rows of this and the next three contraction blocks
-              // (16 bytes per row; x is a multiple of 16 bytes): A rows of the
-              // tile, and rows e N + n0 .. of B's [E N, ld_sf] scales
+            if (kb % C::KPS == 0) {
               if (!mbar_wait(&sf_empty[qslot], qphase ^ 1, vabort)) {
                 set_status(av.status, MGEMM_STATUS_TIMEOUT);
                 raise_abort();
                 break;
               }
-              mbar_arrive_expect_tx(&sf_full[qslot], (uint32_t)(128 * 16 + bn * 16));
+              if constexpr (C::Mode == kModeRows) {
+                // the scale rows of this and the next three contraction blocks
+                // (16 bytes per row; x is a multiple of 16 bytes): A rows of the
+                // tile, and rows e N + n0 .. of B's [E N, ld_sf] scales
+                mbar_arrive_expect_tx(&sf_full[qslot], (uint32_t)(128 * 16 + bn * 16));
+                tma_load_2d(sfa_slot(qslot), &tmSFA, &sf_full[qslot], (kb >> 2) * 16, ti.a_row);
+                tma_load_2d(sfb_slot(qslot), &tmSFB, &sf_full[qslot], (kb >> 2) * 16, ti.e * p.Nout + ti.n0);
+              } else {
+                // one contraction block of the padded layout (its block index is
+                // x0 / 128 + kb): 4 bytes per row, rows viewed in fours (16 bytes)
+                mbar_arrive_expect_tx(&sf_full[qslot], (uint32_t)(128 * 4 + bn * 4));
+                tma_load_3d(sfa_slot(qslot), &tmSFA, &sf_full[qslot], 0, ti.a_row / 4, ti.x0 / C::BK + kb);
+                tma_load_3d(sfb_slot(qslot), &tmSFB, &sf_full[qslot], 0, ti.n0 / 4, ti.x0 / C::BK + kb);
+              }
               ++sf_issued;
-              tma_load_2d(sfa_slot(qslot), &tmSFA, &sf_full[qslot], (kb >> 2) * 16, ti.a_row);
-              tma_load_2d(sfb_slot(qslot), &tmSFB, &sf_full[qslot], (kb >> 2) * 16, ti.e * p.Nout + ti.n0);
               if (++qslot == C::SF_SLOTS) {
                 qslot = 0;
                 qphase ^= 1;
@@ -654,9 +665,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     __syncwarp();
   } else if (C::Mx && warp == 2 + C::EPI) {
-    // MXFP8 scale warp.  A slot holds the scale rows of four contraction
-    // blocks of 128 (16 bytes per row); word w = kb % 4 of each row holds
-    // block kb's four 32-element scales.  Tensor memory takes them as a
+    // MXFP8 scale warp.  A slot holds the scale rows of KPS contraction
+    // blocks of 128 (rows schedule: 16 bytes per row, four blocks; experts
+    // schedule: 4 bytes per row, one block); word w = kb % KPS of each row
+    // holds block kb's four 32-element scales.  Tensor memory takes them as a
     // 512-byte tile per operand, row l holding rows l, l + 32, l + 64, l + 96
     // of the tile (byte 4 m + s: sub-block s of row l + 32 m), copied into
     // each lane quarter at columns 2 BN_MAX + SF_COLS stage (A) and + 4 (B).  Lane
@@ -675,21 +687,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (ti.kb_count == 0) continue;
       for (int kb = 0; kb < ti.kb_count; ++kb) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1, vabort)) { ok = false; break; }
-        if ((kb & 3) == 0 && !mbar_wait_warp(&sf_full[qslot], qphase, vabort)) { ok = false; break; }
-        const int w = kb & 3;
+        if (kb % C::KPS == 0 && !mbar_wait_warp(&sf_full[qslot], qphase, vabort)) { ok = false; break; }
+        const int w = kb % C::KPS;
         const uint32_t *la = reinterpret_cast<const uint32_t *>(sfa_slot(qslot));
         const uint32_t *lb = reinterpret_cast<const uint32_t *>(sfb_slot(qslot));
-        const uint4 va = make_uint4(la[lane * 4 + w], la[(lane + 32) * 4 + w], la[(lane + 64) * 4 + w],
-                                    la[(lane + 96) * 4 + w]);
-        const uint4 vb = make_uint4(lb[lane * 4 + w], lb[(lane + 32) * 4 + w], lb[(lane + 64) * 4 + w],
-                                    lb[(lane + 96) * 4 + w]);
+        constexpr int S = C::KPS;  // words per row of a slot
+        const uint4 va = make_uint4(la[lane * S + w], la[(lane + 32) * S + w], la[(lane + 64) * S + w],
+                                    la[(lane + 96) * S + w]);
+        const uint4 vb = make_uint4(lb[lane * S + w], lb[(lane + 32) * S + w], lb[(lane + 64) * S + w],
+                                    lb[(lane + 96) * S + w]);
         reinterpret_cast<uint4 *>(sf_tile(stage, 0))[lane] = va;
         reinterpret_cast<uint4 *>(sf_tile(stage, 1))[lane] = vb;
         if constexpr (C::SF_TILES_B > 1) {
           // B columns 128 .. BN_MAX - 1 (the slot has BN_MAX rows; the rest are zero)
-          const uint4 vc = make_uint4(lb[(lane + 128) * 4 + w], lb[(lane + 160) * 4 + w],
-                                      C::BN_MAX > 192 ? lb[(lane + 192) * 4 + w] : 0u,
-                                      C::BN_MAX > 224 ? lb[(lane + 224) * 4 + w] : 0u);
+          const uint4 vc = make_uint4(lb[(lane + 128) * S + w], lb[(lane + 160) * S + w],
+                                      C::BN_MAX > 192 ? lb[(lane + 192) * S + w] : 0u,
+                                      C::BN_MAX > 224 ? lb[(lane + 224) * S + w] : 0u);
           reinterpret_cast<uint4 *>(sf_tile(stage, 2))[lane] = vc;
         }
         fence_proxy_async_smem();  // the tiles are read by tcgen05.cp
@@ -703,10 +716,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if constexpr (C::SF_TILES_B > 1)
             tmem_cp_32x128b_warpx4(sfb_t + 4, smem_desc_rows16(smem_u32(sf_tile(stage, 2))));
           mma_commit(&sfready[stage]);
-          if (w == 3 || kb == ti.kb_count - 1) mbar_arrive(&sf_empty[qslot]);  // the slot's rows are read
+          if (w == C::KPS - 1 || kb == ti.kb_count - 1) mbar_arrive(&sf_empty[qslot]);  // the slot's rows are read
         }
         __syncwarp();
-        if (w == 3 || kb == ti.kb_count - 1) {
+        if (w == C::KPS - 1 || kb == ti.kb_count - 1) {
           if (++qslot == C::SF_SLOTS) {
             qslot = 0;
             qphase ^= 1;

@@ -321,6 +321,65 @@ extern "C" int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *s
                    : gemm_fp8_rows_mx(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
 }
 
+extern "C" int mgemm_wgrad_mx(const void *args, const uint8_t *x, const uint8_t *sx, const uint8_t *grad_out,
+                              const uint8_t *sgo, void *grad_w, int64_t M, int K, int N, int E, int64_t ld,
+                              mgemm_stream_t stream) {
+  if (!args || !grad_w) return MGEMM_EINVAL;
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  if (M < 0 || M >= (int64_t(1) << 31) || K <= 0 || N <= 0 || K % 16 || N % 16) return MGEMM_EINVAL;
+  if (M > 0 && (!x || !sx || !grad_out || !sgo)) return MGEMM_EINVAL;
+  if (ld < mgemm_colwise_ld(M, E) || ld >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  if (!aligned16(args) || !aligned16(grad_w) || ld % 128) return MGEMM_EALIGN;
+  if (M > 0 && (!aligned16(x) || !aligned16(sx) || !aligned16(grad_out) || !aligned16(sgo))) return MGEMM_EALIGN;
+  int rc = ensure_context();
+  if (rc) return rc;
+  const int sms = sm_count();
+  if (sms <= 0) return MGEMM_ECUDA;
+  // with M == 0 every expert is empty: nothing is loaded, the maps only need valid memory
+  const void *xa = M > 0 ? (const void *)x : grad_w, *ga = M > 0 ? (const void *)grad_out : grad_w;
+  const void *sxa = M > 0 ? (const void *)sx : grad_w, *sga = M > 0 ? (const void *)sgo : grad_w;
+  const uint64_t L = M > 0 ? (uint64_t)ld : 128;
+  const int bn = 192;
+  CUtensorMap ta, tb, to, tsa, tsb;
+  {
+    const uint64_t da[2] = {L, (uint64_t)K}, db[2] = {L, (uint64_t)N};
+    const uint64_t st[1] = {L};
+    const uint32_t boxa[2] = {128, 128}, boxb[2] = {128, (uint32_t)bn};
+    if (!make_map(&ta, true, 2, xa, da, st, boxa)) return MGEMM_ECUDA;
+    if (!make_map(&tb, true, 2, ga, db, st, boxb)) return MGEMM_ECUDA;
+  }
+  // scale rows [ld / 128][rows][4 B], rows viewed in fours: boxes of one block
+  {
+    const uint64_t d[3] = {16, (uint64_t)K / 4, L / 128};
+    const uint64_t st[2] = {16, (uint64_t)K * 4};
+    const uint32_t box[3] = {16, 32, 1};
+    if (!make_tensor_map(&tsa, true, 3, sxa, d, st, box, false)) return MGEMM_ECUDA;
+  }
+  {
+    const uint64_t d[3] = {16, (uint64_t)N / 4, L / 128};
+    const uint64_t st[2] = {16, (uint64_t)N * 4};
+    const uint32_t box[3] = {16, (uint32_t)bn / 4, 1};
+    if (!make_tensor_map(&tsb, true, 3, sga, d, st, box, false)) return MGEMM_ECUDA;
+  }
+  if (!make_out_map(&to, grad_w, (int64_t)E * K, N)) return MGEMM_ECUDA;
+  GemmParams p{};
+  p.args = (const uint8_t *)args;
+  p.E = E;
+  p.bn = bn;
+  p.idesc = make_idesc_mx(128, bn, 1);  // ue8m0 scales
+  p.n_tiles = (N + bn - 1) / bn;
+  p.mt_k = (K + 127) / 128;
+  p.Nout = N;
+  p.Kout = K;
+  p.out = (__nv_bfloat16 *)grad_w;
+  const int64_t upper = (int64_t)E * p.mt_k * p.n_tiles;
+  if (upper >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  const int grid = grid_for(upper);
+  if (grid < 0) return MGEMM_ECUDA;
+  return gemm_fp8_experts_mx(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
+}
+
 extern "C" int mgemm_dgrad(const void *args, int dtype, const void *grad_out, const float *sgo, const void *w,
                            const float *sw, void *grad_x, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
   int rc = common_checks(args, dtype, M, K, N, E);

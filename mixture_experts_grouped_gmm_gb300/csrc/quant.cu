@@ -148,6 +148,81 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(const __nv_bfloat16 *__re
   }
 }
 
+// ------------------------------------------------------------ MX colwise
+// Per-group colwise MX blocks (the wgrad operands).  CTA (j, column block):
+// rows 128 j .. 128 j + 127 of the padded column-major layout, which lie in
+// one group g (every group spans a multiple of 128 padded rows), and 64
+// columns of one tensor.  The bf16 tile is staged in shared memory ([128
+// rows][64 columns], loaded 16 bytes per thread, rows past the group as
+// zeros); thread (s, c) then takes column c's 32-row sub-block s: its
+// magnitude maximum, the scale, 32 codes written as two 16-byte stores into
+// the column, and one e8m0 byte at sf[(j C + c) 4 + s].
+struct MxColTensor {
+  const __nv_bfloat16 *in;
+  uint8_t *out;
+  uint8_t *sf;
+  int64_t C;
+  int ncb;  // 64-column blocks
+};
+
+__global__ void __launch_bounds__(256) quant_colwise_mx_kernel(const uint8_t *__restrict__ args, int E, int64_t ld,
+                                                               MxColTensor t1, MxColTensor t2) {
+  __shared__ __align__(16) __nv_bfloat16 tile[128][64];
+  pdl_wait();
+  pdl_trigger();
+  const ArgsView av(args, E);
+  if (*av.status != 0) return;
+  const int64_t r0p = (int64_t)blockIdx.x * 128;  // first padded row of the block
+  if (r0p >= __ldg(av.poffsets + E)) return;
+  const bool second = (int)blockIdx.y >= t1.ncb;
+  const MxColTensor &T = second ? t2 : t1;
+  const int64_t col0 = (int64_t)(second ? blockIdx.y - t1.ncb : blockIdx.y) * 64;
+  // the group holding padded row r0p
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(av.poffsets + mid) <= r0p) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int64_t lr0 = r0p - __ldg(av.poffsets + g);                        // row of the group
+  const int64_t m = __ldg(av.offsets + g + 1) - __ldg(av.offsets + g);     // its rows
+  const int64_t gr0 = __ldg(av.offsets + g) + lr0;                         // first input row
+  const int t = threadIdx.x;
+  // load: thread t covers columns 8 (t % 8) .. + 7 of rows t / 8 + 32 i
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = t / 8 + 32 * i;
+    const int64_t c = col0 + 8 * (t % 8);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (lr0 + r < m && c < T.C) v = ldg_nc_v4(T.in + (gr0 + r) * T.C + c);
+    *reinterpret_cast<uint4 *>(&tile[r][8 * (t % 8)]) = v;
+  }
+  __syncthreads();
+  // convert: warp w takes sub-block s = w / 2 of columns 32 (w % 2) .. + 31
+  const int w = t >> 5, lane = t & 31;
+  const int sblk = w >> 1, cc = 32 * (w & 1) + lane;
+  const int64_t col = col0 + cc;
+  float a = 0.f;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __bfloat162float(tile[32 * sblk + i][cc]);
+    a = fmaxf(a, fabsf(v[i]));
+  }
+  const float sc = pow2_scale_from_amax(a);
+  if (col < T.C) {
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      q[i] = (uint32_t)cvt_e4m3x2(v[4 * i] * sc, v[4 * i + 1] * sc) |
+             ((uint32_t)cvt_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc) << 16);
+    uint4 *dst = reinterpret_cast<uint4 *>(T.out + col * ld + r0p + 32 * sblk);
+    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    T.sf[((int64_t)blockIdx.x * T.C + col) * 4 + sblk] = (uint8_t)(254u - (__float_as_uint(sc) >> 23));
+  }
+}
+
 // ------------------------------------------------------------------ colwise
 // Persistent, TMA-fed.  Work item = (group, tensor, 64-column block), items
 // in order of decreasing group size, handed out one at a time from a counter
@@ -626,6 +701,28 @@ extern "C" int mgemm_quant_mx(const void *in, int64_t R, int64_t C, int64_t ld_i
   const int blocks = (int)(blocks_needed < cap ? blocks_needed : cap);
   return launch_pdl(quant_mx_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, 1, "mgemm_quant_mx launch",
                     (const __nv_bfloat16 *)in, R, C, ld_in, out, ld_out, sf, ld_sf);
+}
+
+extern "C" int mgemm_quant_colwise_mx(const void *args, int E, int64_t M, const void *in1, int64_t C1, uint8_t *out1,
+                                      uint8_t *sf1, const void *in2, int64_t C2, uint8_t *out2, uint8_t *sf2,
+                                      int64_t ld, mgemm_stream_t stream) {
+  if (!args || !in1 || !out1 || !sf1) return MGEMM_EINVAL;
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  if (M < 0 || M >= (int64_t(1) << 31) || C1 <= 0 || C1 % 8) return MGEMM_EINVAL;
+  if (ld < mgemm_colwise_ld(M, E)) return MGEMM_EINVAL;
+  if (((uintptr_t)args & 15) || ((uintptr_t)in1 & 15) || ((uintptr_t)out1 & 15) || ((uintptr_t)sf1 & 15) || ld % 128)
+    return MGEMM_EALIGN;
+  if (in2) {
+    if (!out2 || !sf2 || C2 <= 0 || C2 % 8) return MGEMM_EINVAL;
+    if (((uintptr_t)in2 & 15) || ((uintptr_t)out2 & 15) || ((uintptr_t)sf2 & 15)) return MGEMM_EALIGN;
+  }
+  if (M == 0) return MGEMM_OK;
+  MxColTensor t1{(const __nv_bfloat16 *)in1, out1, sf1, C1, (int)((C1 + 63) / 64)};
+  MxColTensor t2{(const __nv_bfloat16 *)in2, out2, sf2, in2 ? C2 : 0, in2 ? (int)((C2 + 63) / 64) : 0};
+  const dim3 grid((unsigned)(ld / 128), (unsigned)(t1.ncb + t2.ncb));
+  return launch_pdl(quant_colwise_mx_kernel, grid, dim3(256), 0, (cudaStream_t)stream, 1,
+                    "mgemm_quant_colwise_mx launch", (const uint8_t *)args, E, ld, t1, t2);
 }
 
 extern "C" int mgemm_quant_colwise_grouped(const void *args, int E, int64_t M, const void *in1, int64_t C1,

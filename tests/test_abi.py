@@ -126,6 +126,16 @@ def test_host_checks_mx(lib):
     assert f(a, i, s, i, s, 16, o, 64, 512, 256, 1025, None) == -3  # E
     assert f(a, None, s, i, s, 16, o, 64, 512, 256, 4, None) == -1  # no x
     assert f(a, i, s, i, s, 16, o, 0, 512, 256, 4, None) == 0       # M = 0: nothing to do
+    c = lib.mgemm_quant_colwise_mx
+    assert c(a, 4, 64, i, 60, o, s, None, 0, None, None, 640, None) == -1   # C % 8
+    assert c(a, 4, 64, i, 64, o, s, None, 0, None, None, 512, None) == -1   # ld < colwise_ld
+    assert c(a, 4, 64, i, 64, o, s, None, 0, None, None, 656, None) == -2   # ld % 128
+    assert c(a, 0, 64, i, 64, o, s, None, 0, None, None, 640, None) == -1   # E < 1
+    wg = lib.mgemm_wgrad_mx
+    assert wg(a, i, s, i, s, o, 64, 120, 256, 4, 640, None) == -1           # K % 16
+    assert wg(a, i, s, i, s, o, 64, 128, 256, 4, 512, None) == -1           # ld < colwise_ld
+    assert wg(a, i, s, i, s, o, 64, 128, 256, 4, 656, None) == -2           # ld % 128
+    assert wg(a, None, s, i, s, o, 64, 128, 256, 4, 640, None) == -1        # no x
 
 
 def test_host_checks_moe_align(lib):

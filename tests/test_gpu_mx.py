@@ -14,8 +14,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.mx import decode_mx, gmm_fwd_mx, quant_mx_rows
-from tests.helpers import new_args, to_np
+from oracle.mx import decode_mx, gmm_fwd_mx, gmm_wgrad_mx, quant_mx_colwise_grouped, quant_mx_rows
+from tests.helpers import colwise_padding, new_args, padded_offsets, to_np, unpad_colwise
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -73,6 +73,8 @@ def test_quant_mx_extremes_and_strided_rows():
 
 
 def gemm_case(sizes, K, N, seed):
+    # GPU: quantize + GEMM on the device; reference: the oracle's quantize of
+    # the same bf16 inputs, then its GEMM (the codes agree bit for bit)
     E, M = len(sizes), sum(sizes)
     x = blocky(M, K, seed)
     w = blocky(E * N, K, seed + 1)
@@ -84,8 +86,10 @@ def gemm_case(sizes, K, N, seed):
     out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
     B().mgemm_fwd_mx(args, xq, sx, wq.view(E, N, K), sw, out, M, K, N, E)
     torch.cuda.synchronize()
-    ref = gmm_fwd_mx(to_np(xq), to_np(sx)[:, :K // 32], to_np(wq).reshape(E, N, K),
-                     to_np(sw)[:, :K // 32].reshape(E, N, K // 32), sizes)
+    qx, ex = quant_mx_rows(to_np(x))
+    qw, ew = quant_mx_rows(to_np(w))
+    assert np.array_equal(to_np(xq), qx) and np.array_equal(to_np(wq), qw)
+    ref = gmm_fwd_mx(qx, ex, qw.reshape(E, N, K), ew.reshape(E, N, K // 32), sizes)
     return to_np(out), ref
 
 
@@ -122,8 +126,9 @@ def test_dgrad_mx_through_fwd():
     gx = torch.empty(M, K, dtype=torch.bfloat16, device=DEV)
     B().mgemm_fwd_mx(args, goq, sgo, wq.view(E, K, N), sw, gx, M, N, K, E)
     torch.cuda.synchronize()
-    ref = gmm_fwd_mx(to_np(goq), to_np(sgo)[:, :N // 32], to_np(wq).reshape(E, K, N),
-                     to_np(sw)[:, :N // 32].reshape(E, K, N // 32), sizes)
+    qg, eg = quant_mx_rows(to_np(go))
+    qw, ew = quant_mx_rows(to_np(w_kn))
+    ref = gmm_fwd_mx(qg, eg, qw.reshape(E, K, N), ew.reshape(E, K, N // 32), sizes)
     assert_mx_close(to_np(gx), ref, "dgrad")
 
 
@@ -145,11 +150,11 @@ def test_fwd_mx_deepseek_size_sampled_rows():
     off = np.concatenate([[0], np.cumsum(sizes)])
     rng = np.random.default_rng(0)
     rows = np.unique(np.concatenate([rng.integers(0, M, 48), off[1:-1][sizes[1:] > 0], [M - 1]]))
-    xs = decode_mx(to_np(xq[rows]), to_np(sx[rows])[:, :K // 32])
+    xs = decode_mx(*quant_mx_rows(to_np(x[rows])))
     got = to_np(out[rows])
     experts = np.searchsorted(off, rows, side="right") - 1
     for e in np.unique(experts):
-        we = decode_mx(to_np(wq[e * N:(e + 1) * N]), to_np(sw[e * N:(e + 1) * N])[:, :K // 32])
+        we = decode_mx(*quant_mx_rows(to_np(w[e * N:(e + 1) * N])))
         sel = experts == e
         assert_mx_close(got[sel], xs[sel] @ we.T, f"rows {rows[sel][:4]} (expert {e})")
 
@@ -184,6 +189,109 @@ def test_fwd_mx_graph_replays_with_new_sizes():
         gs.copy_(torch.tensor(sizes))
         graph.replay()
         torch.cuda.synchronize()
-        ref = gmm_fwd_mx(to_np(xq), to_np(sx)[:, :K // 32], to_np(wq).reshape(E, N, K),
-                         to_np(sw)[:, :K // 32].reshape(E, N, K // 32), sizes)
+        qx, ex = quant_mx_rows(to_np(x))
+        qw, ew = quant_mx_rows(to_np(w))
+        ref = gmm_fwd_mx(qx, ex, qw.reshape(E, N, K), ew.reshape(E, N, K // 32), sizes)
         assert_mx_close(to_np(out), ref, f"replay {sizes}")
+
+
+def rowblocky(M, C, seed, lo=-10, hi=10):
+    """bf16 [M, C] on the device whose 32-row runs of each column span 2^lo .. 2^hi."""
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    base = torch.randn(M, C, generator=g, device=DEV)
+    sc = torch.exp2(torch.randint(lo, hi, (M // 32 + 1, C), generator=g, device=DEV).float())
+    return (base * sc.repeat_interleave(32, dim=0)[:M]).to(torch.bfloat16)
+
+
+def colwise_mx_gpu(xs, sizes):
+    E, M = len(sizes), sum(sizes)
+    args = new_args(E, DEV)
+    B().mgemm_fill_args(torch.tensor(sizes, dtype=torch.int64, device=DEV), E, M, args)
+    ld = B().mgemm_colwise_ld(M, E)
+    outs = [torch.full((x.shape[1] * ld,), 0xAB, dtype=torch.uint8, device=DEV) for x in xs]
+    sfs = [torch.full((ld // 128 * x.shape[1] * 4,), 0xCD, dtype=torch.uint8, device=DEV) for x in xs]
+    if len(xs) == 2:
+        B().mgemm_quant_colwise_mx(args, E, M, xs[0], outs[0], sfs[0], xs[1], outs[1], sfs[1], ld)
+    else:
+        B().mgemm_quant_colwise_mx(args, E, M, xs[0], outs[0], sfs[0], ld=ld)
+    torch.cuda.synchronize()
+    return args, ld, outs, sfs
+
+
+def check_colwise_mx(x, sizes, out, sf, ld):
+    C = x.shape[1]
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    qo, so = quant_mx_colwise_grouped(to_np(x), off)
+    assert np.array_equal(unpad_colwise(to_np(out), C, ld, sizes), qo)
+    assert not colwise_padding(to_np(out), C, ld, sizes).any()          # padding holds zero codes
+    sfv = to_np(sf).reshape(ld // 128, C, 4)
+    po = padded_offsets(sizes)
+    for g, m in enumerate(sizes):
+        for b in range(so[g].shape[1]):
+            r = po[g] + 32 * b
+            assert np.array_equal(sfv[r // 128, :, (r % 128) // 32], so[g][:, b]), (g, b)
+
+
+@pytest.mark.parametrize("sizes,C1,C2", [
+    ([100, 0, 300, 57], 64, 0),
+    ([1, 2, 3, 250, 0, 129], 136, 200),
+    ([0, 0, 70], 2048, 1408),
+    ([32] * 9, 8, 24),
+])
+def test_quant_colwise_mx(sizes, C1, C2):
+    M = sum(sizes)
+    xs = [rowblocky(M, C1, C1 + M)] + ([rowblocky(M, C2, C2 + M + 1)] if C2 else [])
+    _, ld, outs, sfs = colwise_mx_gpu(xs, sizes)
+    for x, o, f in zip(xs, outs, sfs):
+        check_colwise_mx(x, sizes, o, f, ld)
+
+
+@pytest.mark.parametrize("sizes,K,N", [
+    ([100, 0, 300, 57], 128, 192),
+    ([1, 2, 3, 250, 0, 129], 256, 400),
+    ([0, 0, 700], 384, 64),
+    ([33] * 12, 144, 208),
+])
+def test_wgrad_mx_parity(sizes, K, N):
+    E, M = len(sizes), sum(sizes)
+    x = rowblocky(M, K, 31 + K)
+    go = rowblocky(M, N, 32 + N)
+    args, ld, (xq, gq), (sx, sg) = colwise_mx_gpu([x, go], sizes)
+    gw = torch.full((E, K, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    B().mgemm_wgrad_mx(args, xq, sx, gq, sg, gw, M, K, N, E, ld)
+    torch.cuda.synchronize()
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    qx, ex = quant_mx_colwise_grouped(to_np(x), off)
+    qg, eg = quant_mx_colwise_grouped(to_np(go), off)
+    ref = gmm_wgrad_mx(qx, ex, qg, eg, sizes)
+    got = to_np(gw)
+    for e in range(E):
+        assert_mx_close(got[e], ref[e], f"expert {e} (m = {sizes[e]})")
+
+
+def test_mx_step_deepseek_size_sampled():
+    # the MXFP8 backward on the DeepSeek routing: dual colwise MX of (grad_out,
+    # x) and the wgrad; checked on sampled columns of every group
+    from mixture_experts_grouped_gmm_gb300 import workloads
+
+    d = workloads.deepseek(device=DEV, T=16384, with_weights=False)
+    M, K, N, E = d["M"], d["K"], d["N"], d["E"]
+    sizes = d["group_sizes"].cpu().numpy().tolist()
+    x, go = d["x"], d["grad_out"]
+    args, ld, (gq, xq), (sg, sx) = colwise_mx_gpu([go, x], sizes)
+    gw = torch.empty(E, K, N, dtype=torch.bfloat16, device=DEV)
+    B().mgemm_wgrad_mx(args, xq, sx, gq, sg, gw, M, K, N, E, ld)
+    torch.cuda.synchronize()
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    rng = np.random.default_rng(1)
+    kc = np.sort(rng.choice(K, 12, replace=False))
+    nc = np.sort(rng.choice(N, 12, replace=False))
+    qx, ex = quant_mx_colwise_grouped(to_np(x[:, kc]), off)
+    qg, eg = quant_mx_colwise_grouped(to_np(go[:, nc]), off)
+    # the GPU's codes of the sampled columns, bit for bit
+    assert np.array_equal(unpad_colwise(to_np(xq), K, ld, sizes)[kc], qx)
+    assert np.array_equal(unpad_colwise(to_np(gq), N, ld, sizes)[nc], qg)
+    ref = gmm_wgrad_mx(qx, ex, qg, eg, sizes)
+    got = to_np(gw[:, torch.as_tensor(kc, device=DEV)][:, :, torch.as_tensor(nc, device=DEV)])
+    for e in range(E):
+        assert_mx_close(got[e], ref[e], f"expert {e}")
