@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(const __nv_bfloat16 *__re
 }
 
 // ------------------------------------------------------------ MX colwise
-// Per-group colwise MX blocks (the wgrad operands).  CTA (j, column block):
+// Per-group colwise MX blocks (the wgrad operands).  CTA (column block, j):
 // rows 128 j .. 128 j + 127 of the padded column-major layout, which lie in
 // one group g (every group spans a multiple of 128 padded rows), and 64
 // columns of one tensor.  The bf16 tile is staged in shared memory ([128
@@ -168,15 +168,21 @@ struct MxColTensor {
 __global__ void __launch_bounds__(256) quant_colwise_mx_kernel(const uint8_t *__restrict__ args, int E, int64_t ld,
                                                                MxColTensor t1, MxColTensor t2) {
   __shared__ __align__(16) __nv_bfloat16 tile[128][64];
+  __shared__ __align__(16) uint8_t codes[64][144];  // [column][128 rows] + 16 bytes of padding (banks)
   pdl_wait();
   pdl_trigger();
   const ArgsView av(args, E);
   if (*av.status != 0) return;
-  const int64_t r0p = (int64_t)blockIdx.x * 128;  // first padded row of the block
+  // CTA b: column block b % ncb (of both tensors), row block b / ncb, so that
+  // CTAs running together read whole rows
+  const int ncb = t1.ncb + t2.ncb;
+  const int cb = (int)(blockIdx.x % (unsigned)ncb);
+  const int64_t jb = (int64_t)(blockIdx.x / (unsigned)ncb);
+  const int64_t r0p = jb * 128;  // first padded row of the block
   if (r0p >= __ldg(av.poffsets + E)) return;
-  const bool second = (int)blockIdx.y >= t1.ncb;
+  const bool second = cb >= t1.ncb;
   const MxColTensor &T = second ? t2 : t1;
-  const int64_t col0 = (int64_t)(second ? blockIdx.y - t1.ncb : blockIdx.y) * 64;
+  const int64_t col0 = (int64_t)(second ? cb - t1.ncb : cb) * 64;
   // the group holding padded row r0p
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -210,16 +216,24 @@ __global__ void __launch_bounds__(256) quant_colwise_mx_kernel(const uint8_t *__
     a = fmaxf(a, fabsf(v[i]));
   }
   const float sc = pow2_scale_from_amax(a);
-  if (col < T.C) {
-    uint32_t q[8];
+  uint32_t q[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      q[i] = (uint32_t)cvt_e4m3x2(v[4 * i] * sc, v[4 * i + 1] * sc) |
-             ((uint32_t)cvt_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc) << 16);
-    uint4 *dst = reinterpret_cast<uint4 *>(T.out + col * ld + r0p + 32 * sblk);
-    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-    T.sf[((int64_t)blockIdx.x * T.C + col) * 4 + sblk] = (uint8_t)(254u - (__float_as_uint(sc) >> 23));
+  for (int i = 0; i < 8; ++i)
+    q[i] = (uint32_t)cvt_e4m3x2(v[4 * i] * sc, v[4 * i + 1] * sc) |
+           ((uint32_t)cvt_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc) << 16);
+  uint4 *cdst = reinterpret_cast<uint4 *>(&codes[cc][32 * sblk]);
+  cdst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+  cdst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  if (col < T.C) T.sf[(jb * T.C + col) * 4 + sblk] = (uint8_t)(254u - (__float_as_uint(sc) >> 23));
+  __syncthreads();
+  // store: 16-byte piece p of column c (chunk t + 256 i = 8 c + p), so a warp
+  // writes four whole 128-byte column segments
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int id = t + 256 * i, c = id >> 3, part = id & 7;
+    if (col0 + c < T.C)
+      *reinterpret_cast<uint4 *>(T.out + (col0 + c) * ld + r0p + 16 * part) =
+          *reinterpret_cast<const uint4 *>(&codes[c][16 * part]);
   }
 }
 
@@ -720,7 +734,9 @@ extern "C" int mgemm_quant_colwise_mx(const void *args, int E, int64_t M, const 
   if (M == 0) return MGEMM_OK;
   MxColTensor t1{(const __nv_bfloat16 *)in1, out1, sf1, C1, (int)((C1 + 63) / 64)};
   MxColTensor t2{(const __nv_bfloat16 *)in2, out2, sf2, in2 ? C2 : 0, in2 ? (int)((C2 + 63) / 64) : 0};
-  const dim3 grid((unsigned)(ld / 128), (unsigned)(t1.ncb + t2.ncb));
+  const int64_t nblk = ld / 128 * (t1.ncb + t2.ncb);
+  if (nblk >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  const dim3 grid((unsigned)nblk);
   return launch_pdl(quant_colwise_mx_kernel, grid, dim3(256), 0, (cudaStream_t)stream, 1,
                     "mgemm_quant_colwise_mx launch", (const uint8_t *)args, E, ld, t1, t2);
 }
