@@ -190,7 +190,7 @@ def mgemm_quant_colwise_mx(args, E, M, x1, out1, sf1, x2=None, out2=None, sf2=No
 def mgemm_wgrad_mx(args, x, sx, go, sgo, grad_w, M, K, N, E, ld=None):
     """MXFP8 wgrad on the outputs of mgemm_quant_colwise_mx -> grad_w bf16 [E, K, N]."""
     _cuda(args, x, sx, go, sgo, grad_w)
-    ld = ld or mgemm_colwise_ld(M, E)
+    ld = mgemm_colwise_ld(M, E) if ld is None else ld
     _check(lib().mgemm_wgrad_mx(_p(args), _p(x), _p(sx), _p(go), _p(sgo), _p(grad_w), int(M), int(K), int(N), int(E),
                                 int(ld), _stream(grad_w)), "mgemm_wgrad_mx")
 

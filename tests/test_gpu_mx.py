@@ -295,3 +295,48 @@ def test_mx_step_deepseek_size_sampled():
     got = to_np(gw[:, torch.as_tensor(kc, device=DEV)][:, :, torch.as_tensor(nc, device=DEV)])
     for e in range(E):
         assert_mx_close(got[e], ref[e], f"expert {e}")
+
+
+@pytest.mark.parametrize("sizes,K,N", [
+    ([5], 128, 8),                               # one tile, N = 8 (one 128-wide tile, mostly outside N)
+    ([3, 0, 1, 2] * 64, 256, 136),               # 256 experts with one to three rows or none
+    ([0, 0, 0, 513], 640, 64),
+])
+def test_fwd_mx_edges(sizes, K, N):
+    got, ref = gemm_case(sizes, K, N, seed=len(sizes) + K + N)
+    assert_mx_close(got, ref, f"sizes={sizes[:6]}.. K={K} N={N}")
+
+
+@pytest.mark.parametrize("sizes,K,N", [
+    ([7, 0, 33], 16, 16),                        # the smallest K and N
+    ([1, 2, 3, 0] * 64, 32, 48),                 # 256 experts, tiny groups
+    ([0, 0, 0, 0, 97], 128, 192),                # a single non-empty expert
+])
+def test_wgrad_mx_edges(sizes, K, N):
+    E, M = len(sizes), sum(sizes)
+    x = rowblocky(M, K, 41 + K)
+    go = rowblocky(M, N, 42 + N)
+    args, ld, (xq, gq), (sx, sg) = colwise_mx_gpu([x, go], sizes)
+    gw = torch.full((E, K, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    B().mgemm_wgrad_mx(args, xq, sx, gq, sg, gw, M, K, N, E, ld)
+    torch.cuda.synchronize()
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    qx, ex = quant_mx_colwise_grouped(to_np(x), off)
+    qg, eg = quant_mx_colwise_grouped(to_np(go), off)
+    ref = gmm_wgrad_mx(qx, ex, qg, eg, sizes)
+    got = to_np(gw)
+    for e in range(E):
+        if sizes[e] == 0:
+            assert not got[e].any(), f"expert {e}: empty group must give zeros"
+        else:
+            assert_mx_close(got[e], ref[e], f"expert {e}")
+
+
+def test_wgrad_mx_no_rows_writes_zeros():
+    E, K, N = 3, 128, 192
+    args = new_args(E, DEV)
+    B().mgemm_fill_args(torch.zeros(E, dtype=torch.int64, device=DEV), E, 0, args)
+    gw = torch.full((E, K, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    B().mgemm_wgrad_mx(args, None, None, None, None, gw, 0, K, N, E, 0)
+    torch.cuda.synchronize()
+    assert not gw.float().any()
