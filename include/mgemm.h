@@ -387,7 +387,9 @@ int mgemm_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes, int6
  *   map_limit   rows of out (numel of topk_ids)
  *   row_weight  float32 [map_limit] or NULL
  * bf16 only (fp8 returns MGEMM_ENOTSUP).  Output rows no sorted row names are
- * left as they were.
+ * left as they were.  With map_limit < 128 (decode-size batches: a group has
+ * at most map_limit routed rows, at the start of its block) only those rows of
+ * each block are loaded.
  */
 int mgemm_fwd_scatter(const void *args, int dtype, int trans_b, const void *x, const void *w, void *out,
                       const int32_t *row_map, int64_t map_limit, const float *row_weight, int64_t M, int K, int N,
@@ -402,9 +404,14 @@ int mgemm_fwd_scatter(const void *args, int dtype, int trans_b, const void *x, c
  * rows, so both halves of an output column meet in one accumulator.
  *   args, x [M, K], M, K, E: as for mgemm_fwd (bf16)
  *   w    bf16 [E, 2F, K];  out  bf16 [M, F] (F % 8 == 0)
+ *   group_rows_max  an upper bound on the rows of any group that are not
+ *        padding (the routed entries; they come first in each 128-row block,
+ *        as mgemm_moe_align places them), or 0 if unknown.  Below 128 (decode-
+ *        size batches) only those rows of each block are loaded and stored:
+ *        the padding rows of out are then left as they were.
  */
 int mgemm_fwd_gated(const void *args, const void *x, const void *w, void *out, int64_t M, int K, int F, int E,
-                    mgemm_stream_t stream);
+                    int64_t group_rows_max, mgemm_stream_t stream);
 
 /*
  * mgemm_silu_and_mul -- out[r, j] = silu(in[r, j]) * in[r, F + j] for in bf16

@@ -81,7 +81,8 @@ _SIGS = {
                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p]),
     "mgemm_fwd_gated": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                       ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+                                       ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                       ctypes.c_void_p]),
     "mgemm_silu_and_mul": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                           ctypes.c_void_p]),
     "mgemm_topk_sum": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
@@ -277,10 +278,11 @@ def mgemm_fwd_scatter(args, dtype, trans_b, x, w, out, row_map, map_limit, row_w
            "mgemm_fwd_scatter")
 
 
-def mgemm_fwd_gated(args, x, w, out, M, K, F, E):
+def mgemm_fwd_gated(args, x, w, out, M, K, F, E, group_rows_max=0):
     """out [M, F] = silu(x . w_gate^T) * (x . w_up^T), w [E, 2F, K] bf16."""
     _cuda(args, x, w, out)
-    _check(lib().mgemm_fwd_gated(_p(args), _p(x), _p(w), _p(out), int(M), int(K), int(F), int(E), _stream(out)),
+    _check(lib().mgemm_fwd_gated(_p(args), _p(x), _p(w), _p(out), int(M), int(K), int(F), int(E),
+                                 int(group_rows_max), _stream(out)),
            "mgemm_fwd_gated")
 
 

@@ -229,6 +229,9 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
     ti.a_row = row0;
     ti.out_row0 = row0;
     ti.out_rows = (int)max((int64_t)0, min((int64_t)C::BM, re - row0));
+    // a run-time ring's A slot holds a_rows rows: the MMA rows past them read
+    // stale shared memory and are not stored (they are padding rows there)
+    if (C::DynRing && ti.out_rows > p.a_rows) ti.out_rows = p.a_rows;
     ti.b_row = C::Pair ? ti.n0 + (int)rank * (p.bn / 2) : ti.n0;
     ti.x0 = 0; ti.lo = 0; ti.hi = 0;
   } else {

@@ -118,7 +118,8 @@ bool make_out_map(CUtensorMap *m, void *out, int64_t rows, int64_t cols) {
 // gate_rows > 0 (w [E, 2 gate_rows, K], N = 2 gate_rows, output gate_rows wide)
 static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
                     const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream,
-                    const int32_t *row_map, int64_t map_limit, const float *row_weight, int gate_rows = 0) {
+                    const int32_t *row_map, int64_t map_limit, const float *row_weight, int gate_rows = 0,
+                    int64_t group_rows_max = 0) {
   int rc = common_checks(args, dtype, M, K, N, E);
   if (rc) return rc;
   if (!x || !w || !out) return MGEMM_EINVAL;
@@ -131,7 +132,17 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   const uint64_t es = fp8 ? 1 : 2;
   const uint32_t bk = fp8 ? 128 : 64;
   CUtensorMap ta, tb;
-  const uint32_t a_rows = M < 128 ? (uint32_t)((M + 7) / 8 * 8) : 128u;
+  uint32_t a_rows = M < 128 ? (uint32_t)((M + 7) / 8 * 8) : 128u;
+  // Routed rows (gated and scattered forms, bf16, w [E, N, K]): each group's
+  // rows sit at the start of its 128-row blocks, followed by padding.  With at
+  // most rb < 128 rows in a group (decode-size batches), the A box holds only
+  // those rows (rounded up to 8) and the run-time ring gives the weight stream
+  // the rest of shared memory; the padding rows' outputs are not stored.
+  int64_t rb = 128;
+  if (row_map && map_limit < rb) rb = map_limit;  // a group holds at most map_limit entries
+  if (gate_rows > 0 && group_rows_max > 0 && group_rows_max < rb) rb = group_rows_max;
+  const bool routed_few = !fp8 && trans_b && (row_map || gate_rows > 0) && rb < 128 && M >= 128;
+  if (routed_few) a_rows = (uint32_t)((rb > 0 ? rb : 1) + 7) / 8 * 8;
   {
     const uint64_t d[2] = {(uint64_t)K, (uint64_t)M};
     const uint64_t st[1] = {(uint64_t)K * es};
@@ -149,7 +160,7 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   // average, so HBM bounds the launch).  With more rows the wider tile's
   // operand reuse wins.
   // (the gated form needs whole 64-column halves: 128 or 256)
-  const bool allow192 = !fp8 && gate_rows == 0 && (trans_b || N % 64 == 0) && M <= 256 * (int64_t)E;
+  const bool allow192 = !fp8 && gate_rows == 0 && !routed_few && (trans_b || N % 64 == 0) && M <= 256 * (int64_t)E;
   const bool gated = gate_rows > 0;
   // routed rows (the gated and scattered forms) come in groups padded to 128,
   // so M / 128 bounds their row tiles; plain groups may add one partial tile each
@@ -211,6 +222,11 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   const int64_t upper = ((M + 127) / 128 + (M < E ? M : E)) * p.n_tiles;
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
+  if (routed_few) {  // bf16 routed rows, few per group: run-time rings
+    if (bn <= 64) return gemm_bf16_rows_few_narrow(ta, tb, to, p, grid, s);
+    if (bn <= 128) return gemm_bf16_rows_few_mid(ta, tb, to, p, grid, s);
+    return gemm_bf16_rows_few_wide(ta, tb, to, p, grid, s);
+  }
   if (fp8 && a_rows < 128 && K % 128 == 0) {
     // few token rows: the weight stream gets the shared memory the A slots leave
     // (4 / 2 / 1 contraction blocks per stage for BN 64 / 128 / 256)
@@ -254,9 +270,11 @@ extern "C" int mgemm_fwd_scatter(const void *args, int dtype, int trans_b, const
 }
 
 extern "C" int mgemm_fwd_gated(const void *args, const void *x, const void *w, void *out, int64_t M, int K, int F,
-                               int E, mgemm_stream_t stream) {
+                               int E, int64_t group_rows_max, mgemm_stream_t stream) {
   if (F < 1 || F % 8 || F > (1 << 29)) return F % 8 ? MGEMM_EALIGN : MGEMM_EINVAL;
-  return fwd_impl(args, MGEMM_BF16, 1, x, nullptr, w, nullptr, out, M, K, 2 * F, E, stream, nullptr, 0, nullptr, F);
+  if (group_rows_max < 0) return MGEMM_EINVAL;
+  return fwd_impl(args, MGEMM_BF16, 1, x, nullptr, w, nullptr, out, M, K, 2 * F, E, stream, nullptr, 0, nullptr, F,
+                  group_rows_max);
 }
 
 extern "C" int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *sx, const uint8_t *w, const uint8_t *sw,

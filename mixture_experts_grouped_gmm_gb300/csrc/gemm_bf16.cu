@@ -40,4 +40,20 @@ int gemm_bf16_rows_bk_mid(const CUtensorMap &a, const CUtensorMap &b, const CUte
   return launch_gemm<GemmCfg<false, false, false, kModeRows, 128, 6>>(a, b, o, p, grid, s);
 }
 
+// routed rows with few per group (decode-size batches): run-time rings whose A
+// slot holds only those rows, K-major w, four epilogue warps (the gated and
+// scattered epilogues)
+int gemm_bf16_rows_few_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                              int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 64, 24, 1, false, 4, true, 1>>(a, b, o, p, grid, s);
+}
+int gemm_bf16_rows_few_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                           int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 128, 24, 1, false, 4, true, 1>>(a, b, o, p, grid, s);
+}
+int gemm_bf16_rows_few_wide(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                            int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 256, 24, 1, false, 4, true, 1>>(a, b, o, p, grid, s);
+}
+
 }  // namespace mgemm

@@ -46,6 +46,13 @@ int gemm_fp8_rows_mx192(const CUtensorMap &a, const CUtensorMap &b, const CUtens
 // MXFP8 wgrad: padded column-major x^T [K, ld] and grad_out^T [N, ld] with k-block-major scale rows
 int gemm_fp8_experts_mx(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
                         const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
+// bf16 routed rows with few per group: run-time rings (A slot of a_rows rows), K-major w
+int gemm_bf16_rows_few_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                              int grid, cudaStream_t s);
+int gemm_bf16_rows_few_mid(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                           int grid, cudaStream_t s);
+int gemm_bf16_rows_few_wide(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                            int grid, cudaStream_t s);
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)
 int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s);

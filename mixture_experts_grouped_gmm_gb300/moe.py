@@ -98,7 +98,8 @@ def fused_experts(hidden_states, w1, w2, topk_weights, topk_ids):
     a1 = torch.empty(cap, H, dtype=bf, device=dev)
     B.mgemm_gather_rows(x, sorted_ids, npp, n, top_k, a1)
     a2 = torch.empty(cap, F, dtype=bf, device=dev)  # rows past the padded total are never read
-    B.mgemm_fwd_gated(args, a1, w1, a2, rows, H, F, E)
+    # every group holds at most n routed rows (decode-size batches: n < 128)
+    B.mgemm_fwd_gated(args, a1, w1, a2, rows, H, F, E, n)
     c3 = torch.empty(n, H, dtype=bf, device=dev)
     wts = topk_weights.to(torch.float32).contiguous().view(-1)
     B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a2, w2, c3, sorted_ids, n, wts, rows, F, H, E)

@@ -95,8 +95,9 @@ def test_host_checks_gemms(lib):
     assert f(a, 0, 1, x, w, o, None, 64, None, 64, 128, 256, 4, None) == -1               # no row map
     assert f(a, 0, 1, x, w, o, P(0x60002), 64, None, 64, 128, 256, 4, None) == -2         # row map alignment
     assert f(a, 0, 1, x, w, o, m, -1, None, 64, 128, 256, 4, None) == -1                  # map_limit < 0
-    assert lib.mgemm_fwd_gated(a, x, w, o, 64, 128, 100, 4, None) == -2                  # F % 8
-    assert lib.mgemm_fwd_gated(a, x, w, o, 64, 128, 0, 4, None) == -1                    # F < 1
+    assert lib.mgemm_fwd_gated(a, x, w, o, 64, 128, 100, 4, 0, None) == -2               # F % 8
+    assert lib.mgemm_fwd_gated(a, x, w, o, 64, 128, 0, 4, 0, None) == -1                 # F < 1
+    assert lib.mgemm_fwd_gated(a, x, w, o, 64, 128, 64, 4, -1, None) == -1               # group_rows_max < 0
 
 
 def test_host_checks_quant(lib):
