@@ -25,7 +25,8 @@ Modules:
   args   -- group-size scan, active-group compaction, tile prefix, wgrad order
   quant  -- power-of-two absmax scales, rowwise and per-group colwise quantize
   gmm    -- forward, dgrad and wgrad for bf16 and FP8-scaled operands
-  mx     -- MXFP8: 32-element block scales (e8m0), block quantize, block-scaled grouped GEMM
+  mx     -- MXFP8: 32-element block scales (e8m0), row and per-group column block quantize, block-scaled fwd and wgrad
+  routing -- moe_align_block_size, gather, topk_softmax, silu_and_mul and the fused_moe layer of the routed path
 
 Parity status: every function is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_*.py``; none is "parity unpinned".
