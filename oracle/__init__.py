@@ -17,8 +17,12 @@ cites the passage of the source pages it restates:
   Summary -- run only over the non-empty groups.
 * "[moe training] Optimize FP8 MoE backward pass: fused colwise kernel + AMD
   tuning" (pytorch/ao commit 34322b5) -- the commit message (rowwise 3-op
-  sequence, dual colwise kernel) and bench_colwise_block_configs.py
-  (_colwise_kernel, run_experiment).
+  sequence, dual colwise kernel; the MXFP8 path and its 32-row group
+  padding) and bench_colwise_block_configs.py (_colwise_kernel,
+  run_experiment).
+* pytorch-labs/applied-ai issue 24 (the column-major fused MoE script on
+  vLLM's fused_moe.py) -- moe_align_block_size and its worked example,
+  fused_moe_kernel, silu_and_mul, topk_softmax, the fused_moe layer.
 
 Modules:
   formats -- FP8 e4m3fn decode / saturating round-to-nearest-even encode, bf16 rounding
@@ -32,4 +36,4 @@ Parity status: every function is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_*.py``; none is "parity unpinned".
 """
 
-from . import args, formats, gmm, quant  # noqa: F401
+from . import args, formats, gmm, mx, quant, routing  # noqa: F401
