@@ -108,11 +108,15 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
 }
 
 // ------------------------------------------------------------------ MX blocks
-// One warp per row, 8 elements (16 bytes) per lane and chunk of 256: lanes
+// One warp per row, 8 elements (16 bytes) per lane and chunk of 256 (NCH chunks'
+// loads in flight per round, sized to the row on the host): lanes
 // 4j .. 4j + 3 hold block j of the chunk, whose magnitude maximum two
 // shuffles combine.  The scale is the rowwise rule applied per block; the
 // e8m0 byte 127 - log2(s) is 254 minus s's biased exponent (s is a power of
 // two, always normal).
+// NCH chunks of 256 elements per round, their loads issued first (a row of up
+// to NCH * 256 elements in one round).
+template <int NCH>
 __global__ void __launch_bounds__(256) quant_mx_kernel(const __nv_bfloat16 *__restrict__ in, int64_t R, int64_t C,
                                                        int64_t ld_in, uint8_t *__restrict__ out, int64_t ld_out,
                                                        uint8_t *__restrict__ sf, int64_t ld_sf) {
@@ -123,16 +127,15 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(const __nv_bfloat16 *__re
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < R; row += warps_total) {
     const __nv_bfloat16 *src = in + row * ld_in;
     uint8_t *dst = out + row * ld_out;
-    // four chunks per round, their loads issued first (16 bytes x 4 in flight per lane)
-    for (int64_t c0 = 0; c0 < C; c0 += 1024) {
-      uint4 v[4];
+    for (int64_t c0 = 0; c0 < C; c0 += NCH * 256) {
+      uint4 v[NCH];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < NCH; ++i) {
         const int64_t c = c0 + i * 256 + lane * 8;
         v[i] = c < C ? ldg_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < NCH; ++i) {
         const int64_t c = c0 + i * 256 + lane * 8;
         const bool live = c < C;  // C % 32 == 0: a block's four lanes agree
         float a = amax8(v[i], 0.f);
@@ -713,8 +716,20 @@ extern "C" int mgemm_quant_mx(const void *in, int64_t R, int64_t C, int64_t ld_i
   if (sms <= 0) sms = 148;
   const int64_t cap = (int64_t)sms * 32;
   const int blocks = (int)(blocks_needed < cap ? blocks_needed : cap);
-  return launch_pdl(quant_mx_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, 1, "mgemm_quant_mx launch",
-                    (const __nv_bfloat16 *)in, R, C, ld_in, out, ld_out, sf, ld_sf);
+  const __nv_bfloat16 *x = (const __nv_bfloat16 *)in;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t nch = (C + 255) / 256;
+  if (nch <= 2)
+    return launch_pdl(quant_mx_kernel<2>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_mx launch", x, R, C, ld_in,
+                      out, ld_out, sf, ld_sf);
+  if (nch <= 4)
+    return launch_pdl(quant_mx_kernel<4>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_mx launch", x, R, C, ld_in,
+                      out, ld_out, sf, ld_sf);
+  if (nch <= 6)
+    return launch_pdl(quant_mx_kernel<6>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_mx launch", x, R, C, ld_in,
+                      out, ld_out, sf, ld_sf);
+  return launch_pdl(quant_mx_kernel<8>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_mx launch", x, R, C, ld_in, out,
+                    ld_out, sf, ld_sf);
 }
 
 extern "C" int mgemm_quant_colwise_mx(const void *args, int E, int64_t M, const void *in1, int64_t C1, uint8_t *out1,
