@@ -31,6 +31,8 @@ static_assert(kAlignRounds < 0xFFFF, "round tags fit 16 bits");
 
 __global__ void __launch_bounds__(kAlignThreads) moe_align_count_kernel(const int32_t *__restrict__ ids, int64_t n,
                                                                           int E, int32_t *__restrict__ counts) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int hist[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(1024) moe_align_scan_kernel(int32_t *__restric
                                                                 int32_t *__restrict__ expert_ids,
                                                                 int32_t *__restrict__ num_post,
                                                                 int64_t *__restrict__ group_sizes) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_sum[32];
   __shared__ int total_sh;
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
@@ -102,6 +106,8 @@ __global__ void __launch_bounds__(1024) moe_align_scan_kernel(int32_t *__restric
 __global__ void __launch_bounds__(kAlignThreads) moe_align_place_kernel(const int32_t *__restrict__ ids, int64_t n,
                                                                           int E, const int32_t *__restrict__ first,
                                                                           int32_t *__restrict__ sorted_ids) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sm[];
   int *run = sm;                                          // [E]: entries of e placed by earlier rounds
   uint32_t *wcnt = reinterpret_cast<uint32_t *>(sm + E);  // [8 warps][E]: (round << 16) | count
@@ -146,6 +152,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restric
                                                             const int32_t *__restrict__ ids,
                                                             const int32_t *__restrict__ num_post, int64_t numel,
                                                             int top_k, uint4 *__restrict__ dst, int64_t dst_rows) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = *num_post;
   const int64_t rows = total < dst_rows ? total : dst_rows;
   const int lane = threadIdx.x & 31;
@@ -165,6 +173,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restric
 // in fp32 from the bf16 inputs, rounded to bf16 once; 8 columns per thread.
 __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4 *__restrict__ in, int64_t R, int64_t F8,
                                                          uint4 *__restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t n = R * F8;
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n; c += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = c / F8, j = c - row * F8;
@@ -187,6 +197,8 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4 *__restrict__
 // rounded to bf16 once; 8 columns per thread.
 __global__ void __launch_bounds__(256) topk_sum_kernel(const uint4 *__restrict__ in, int64_t T, int top_k,
                                                          int64_t H8, uint4 *__restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t n = T * H8;
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n; c += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = c / H8, j = c - t * H8;
@@ -220,6 +232,8 @@ template <int NV>
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ gating, int64_t T, int E,
                                                              int top_k, int renormalize, float *__restrict__ weights,
                                                              int32_t *__restrict__ ids) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;  // whole warps leave together
@@ -298,22 +312,16 @@ extern "C" int mgemm_topk_softmax(const float *gating, int64_t T, int E, int top
   if (blocks >= (int64_t(1) << 31)) return MGEMM_EINVAL;
   cudaStream_t s = (cudaStream_t)stream;
   const int nv = (E + 31) / 32;
-#define MGEMM_TOPK_LAUNCH(NV) \
-  topk_softmax_kernel<NV><<<(unsigned)blocks, 256, 0, s>>>(gating, T, E, top_k, renormalize, topk_weights, topk_ids)
-  if (nv <= 1)
-    MGEMM_TOPK_LAUNCH(1);
-  else if (nv <= 2)
-    MGEMM_TOPK_LAUNCH(2);
-  else if (nv <= 4)
-    MGEMM_TOPK_LAUNCH(4);
-  else if (nv <= 8)
-    MGEMM_TOPK_LAUNCH(8);
-  else if (nv <= 16)
-    MGEMM_TOPK_LAUNCH(16);
-  else
-    MGEMM_TOPK_LAUNCH(32);
+#define MGEMM_TOPK_LAUNCH(NV)                                                                                 \
+  return launch_pdl(topk_softmax_kernel<NV>, dim3((unsigned)blocks), dim3(256), 0, s, 1, "mgemm_topk_softmax launch", \
+                    gating, T, E, top_k, renormalize, topk_weights, topk_ids)
+  if (nv <= 1) MGEMM_TOPK_LAUNCH(1);
+  if (nv <= 2) MGEMM_TOPK_LAUNCH(2);
+  if (nv <= 4) MGEMM_TOPK_LAUNCH(4);
+  if (nv <= 8) MGEMM_TOPK_LAUNCH(8);
+  if (nv <= 16) MGEMM_TOPK_LAUNCH(16);
+  MGEMM_TOPK_LAUNCH(32);
 #undef MGEMM_TOPK_LAUNCH
-  return cuda_rc(cudaGetLastError(), "mgemm_topk_softmax launch");
 }
 
 extern "C" int mgemm_topk_sum(const void *in, int64_t T, int top_k, int64_t H, void *out, mgemm_stream_t stream) {
@@ -325,8 +333,8 @@ extern "C" int mgemm_topk_sum(const void *in, int64_t T, int top_k, int64_t H, v
   const int64_t n = T * (H / 8);
   const int64_t want = (n + 255) / 256;
   const int blocks = (int)(want < (int64_t)sms * 32 ? want : (int64_t)sms * 32);
-  topk_sum_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>((const uint4 *)in, T, top_k, H / 8, (uint4 *)out);
-  return cuda_rc(cudaGetLastError(), "mgemm_topk_sum launch");
+  return launch_pdl(topk_sum_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, 1, "mgemm_topk_sum launch",
+                    (const uint4 *)in, T, top_k, H / 8, (uint4 *)out);
 }
 
 extern "C" int mgemm_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes, int64_t src_ld_bytes,
@@ -343,10 +351,9 @@ extern "C" int mgemm_gather_rows(const void *src, int64_t src_rows, int64_t row_
   if (sms <= 0) return MGEMM_ECUDA;
   const int64_t want = (dst_rows + 7) / 8;
   const int blocks = (int)(want < (int64_t)sms * 16 ? want : (int64_t)sms * 16);
-  gather_rows_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(
-      (const uint4 *)src, src_rows, row_bytes / 16, src_ld_bytes / 16, dst_ld_bytes / 16, sorted_ids,
-      num_post_padded, numel, top_k, (uint4 *)dst, dst_rows);
-  return cuda_rc(cudaGetLastError(), "mgemm_gather_rows launch");
+  return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, 1, "mgemm_gather_rows launch",
+                    (const uint4 *)src, src_rows, row_bytes / 16, src_ld_bytes / 16, dst_ld_bytes / 16, sorted_ids,
+                    num_post_padded, numel, top_k, (uint4 *)dst, dst_rows);
 }
 
 extern "C" int mgemm_silu_and_mul(const void *in, int64_t R, int64_t F, void *out, mgemm_stream_t stream) {
@@ -358,8 +365,8 @@ extern "C" int mgemm_silu_and_mul(const void *in, int64_t R, int64_t F, void *ou
   const int64_t n = R * (F / 8);
   const int64_t want = (n + 255) / 256;
   const int blocks = (int)(want < (int64_t)sms * 32 ? want : (int64_t)sms * 32);
-  silu_mul_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>((const uint4 *)in, R, F / 8, (uint4 *)out);
-  return cuda_rc(cudaGetLastError(), "mgemm_silu_and_mul launch");
+  return launch_pdl(silu_mul_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, 1, "mgemm_silu_and_mul launch",
+                    (const uint4 *)in, R, F / 8, (uint4 *)out);
 }
 
 extern "C" int64_t mgemm_moe_align_workspace_bytes(int64_t numel, int E) {
@@ -386,18 +393,17 @@ extern "C" int mgemm_moe_align(const int32_t *topk_ids, int64_t numel, int E, in
   int32_t *counts = static_cast<int32_t *>(workspace);
   cudaStream_t s = (cudaStream_t)stream;
   if (nch > 0) {
-    moe_align_count_kernel<<<nch, kAlignThreads, (size_t)E * 4, s>>>(topk_ids, numel, E, counts);
-    int rc = cuda_rc(cudaGetLastError(), "moe_align count launch");
+    int rc = launch_pdl(moe_align_count_kernel, dim3(nch), dim3(kAlignThreads), (size_t)E * 4, s, 1,
+                        "moe_align count launch", topk_ids, numel, E, counts);
     if (rc) return rc;
   }
-  moe_align_scan_kernel<<<1, 1024, 0, s>>>(counts, nch, E, block_size, numel, cap, max_blocks, sorted_ids,
-                                           expert_ids, num_post_padded, group_sizes);
-  int rc = cuda_rc(cudaGetLastError(), "moe_align scan launch");
+  int rc = launch_pdl(moe_align_scan_kernel, dim3(1), dim3(1024), 0, s, 1, "moe_align scan launch", counts, nch, E,
+                      block_size, numel, cap, max_blocks, sorted_ids, expert_ids, num_post_padded, group_sizes);
   if (rc) return rc;
   if (nch > 0) {
     const size_t smem = (size_t)E * 4 * 9;  // run[E] + 8 warps x E counts: at most 36 KB
-    moe_align_place_kernel<<<nch, kAlignThreads, smem, s>>>(topk_ids, numel, E, counts, sorted_ids);
-    rc = cuda_rc(cudaGetLastError(), "moe_align place launch");
+    rc = launch_pdl(moe_align_place_kernel, dim3(nch), dim3(kAlignThreads), smem, s, 1, "moe_align place launch",
+                    topk_ids, numel, E, (const int32_t *)counts, sorted_ids);
   }
   return rc;
 }
