@@ -166,3 +166,44 @@ def test_wgrad_brute_force():
                         dv[int(gq[n, r])] * 2.0 ** (int(gs[e][n, b]) - 127)
                 assert abs(out[e, k, n] - acc) <= 1e-12 * max(1.0, abs(acc))
     assert not out[1].any()
+
+
+def test_fwd_equals_rowwise_fp8_when_a_row_shares_one_scale():
+    # every block of a row (and of a weight row) with the same e8m0 byte: the MX
+    # product is the rowwise-scaled FP8 product with scale 2^(127 - byte)
+    from oracle.gmm import gmm_fwd_fp8
+
+    rng = np.random.default_rng(7)
+    sizes, K, N = [3, 0, 5], 96, 7
+    E, M = len(sizes), sum(sizes)
+    xq = rng.integers(0, 0x7F, (M, K), dtype=np.uint8) ^ (rng.integers(0, 2, (M, K), dtype=np.uint8) << 7)
+    wq = rng.integers(0, 0x7F, (E, N, K), dtype=np.uint8) ^ (rng.integers(0, 2, (E, N, K), dtype=np.uint8) << 7)
+    bx = rng.integers(100, 150, M).astype(np.uint8)
+    bw = rng.integers(100, 150, (E, N)).astype(np.uint8)
+    xs = np.repeat(bx[:, None], K // 32, axis=1)
+    ws = np.repeat(bw[:, :, None], K // 32, axis=2)
+    mx = gmm_fwd_mx(xq, xs, wq, ws, sizes)
+    fp8 = gmm_fwd_fp8(xq, np.exp2(127.0 - bx), wq, np.exp2(127.0 - bw.astype(np.float64)).ravel(), sizes)
+    assert np.allclose(mx, fp8, rtol=1e-12, atol=0)
+
+
+def test_wgrad_equals_fp8_colwise_when_groups_hold_one_block():
+    # groups of at most 32 rows: one MX block per column and group, whose scale is
+    # the FP8 per-group colwise scale, so the two wgrads agree
+    from oracle.gmm import gmm_wgrad_fp8
+    from oracle.mx import gmm_wgrad_mx, quant_mx_colwise_grouped
+    from oracle.quant import quant_colwise_grouped
+
+    rng = np.random.default_rng(8)
+    sizes = [17, 0, 32, 5]
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    M, K, N = off[-1], 6, 5
+    x = (rng.standard_normal((M, K)) * 3).astype(np.float32).astype(np.float64)
+    go = rng.standard_normal((M, N)).astype(np.float32).astype(np.float64)
+    qx, ex = quant_mx_colwise_grouped(x, off)
+    qg, eg = quant_mx_colwise_grouped(go, off)
+    mx = gmm_wgrad_mx(qx, ex, qg, eg, sizes)
+    fx, sx = quant_colwise_grouped(x, off)
+    fg, sg = quant_colwise_grouped(go, off)
+    fp8 = gmm_wgrad_fp8(fx, sx, fg, sg, sizes)
+    assert np.allclose(mx, fp8, rtol=1e-12, atol=0)
