@@ -192,3 +192,12 @@ def test_product_never_imports_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), f
                 assert "oracle/" not in src, f
+
+
+def test_mx_scale_row_bytes():
+    # C / 32 scale bytes per row, rounded up to a multiple of 16 (the TMA stride rule)
+    from mixture_experts_grouped_gmm_gb300 import binding as B
+
+    for C, want in ((32, 16), (512, 16), (544, 32), (1408, 48), (2048, 64), (5120, 160), (96, 16)):
+        assert B.mx_ld_sf(C) == want, C
+        assert B.mx_ld_sf(C) >= C // 32 and B.mx_ld_sf(C) % 16 == 0
