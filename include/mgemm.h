@@ -305,10 +305,15 @@ int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, con
  * experts (about 33 KB, kept on every GPU that loads the library until exit).
  *   group_sizes  int64[E], device (as for mgemm_fill_args)
  *   the other arguments are those of mgemm_fwd.
- * Runs mgemm_fill_args into the static array, then mgemm_fwd.  Allocates
- * nothing.  E > MGEMM_NOALLOC_MAX_EXPERTS returns MGEMM_ETOOMANY.
+ * Makes every host check of mgemm_fill_args and mgemm_fwd first (same codes;
+ * a rejected call launches nothing and leaves the array untouched; M must be
+ * >= 0, and M == 0 returns MGEMM_OK at once), then runs mgemm_fill_args into
+ * the static array and mgemm_fwd.  Allocates nothing.
+ * E > MGEMM_NOALLOC_MAX_EXPERTS returns MGEMM_ETOOMANY.
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * that device current); make that first call before any stream capture.  The
+ * address is kept for the life of the process: do not use this call on a
+ * device after cudaDeviceReset.
  * All calls share the array: calls whose work overlaps on the GPU race on it.
  * Device-side errors go to the status word of the static args block, which the
  * caller cannot read; check the group sizes beforehand when that matters.

@@ -87,11 +87,30 @@ def build(force=False, verbose=False, extra_flags=()):
     """Compile and link; returns the library path.  Raises on a compiler error."""
     if not force and up_to_date():
         return LIB_PATH
+    return _build_into(LIB_PATH, BUILD_DIR, verbose, extra_flags)
+
+
+def build_variant(name, defines, force=False):
+    """A separately named copy of the library (``lib<name>.so`` beside the
+    product's), compiled from the same sources with extra preprocessor
+    definitions.  Only tests load such a copy (for example one whose pipeline
+    waits give up at once, to exercise the timeout path); the binding never
+    does."""
+    path = os.path.join(PKG, f"lib{name}.so")
+    if not force and os.path.exists(path):
+        t = os.path.getmtime(path)
+        if all(os.path.getmtime(f) <= t for f in _inputs()):
+            return path
+    flags = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    return _build_into(path, os.path.join(PKG, "_build_" + name), False, flags)
+
+
+def _build_into(lib_path, build_dir, verbose, extra_flags):
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -102,13 +121,13 @@ def build(force=False, verbose=False, extra_flags=()):
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

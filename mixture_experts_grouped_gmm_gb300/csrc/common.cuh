@@ -158,12 +158,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// Non-blocking: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) after kWaitLimitNs of wall time or when *abort_flag becomes non-zero,
-// so no kernel of this library can spin forever.
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// so no kernel of this library can spin forever.  A build with
+// MGEMM_WAIT_LIMIT_NS=0 (used only to test the give-up path) makes every
+// pipeline wait a single non-blocking test: a phase that is not already
+// complete counts as a timeout.
+#ifndef MGEMM_WAIT_LIMIT_NS
+#define MGEMM_WAIT_LIMIT_NS 1000000000ull  // 1 s
+#endif
+constexpr uint64_t kWaitLimitNs = MGEMM_WAIT_LIMIT_NS;
+// The drain after a give-up (copies and MMAs already issued must land before
+// shared and tensor memory are released) always waits up to 1 s: those
+// operations complete on their own within microseconds.
+constexpr uint64_t kDrainLimitNs = 1000ull * 1000ull * 1000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort_flag) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, const volatile int *abort_flag,
+                                              uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -171,9 +195,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 255u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort_flag) {
+  if constexpr (kWaitLimitNs == 0) return mbar_test_wait(smem_u32(bar), parity);
+  return mbar_wait_for(bar, parity, abort_flag, kWaitLimitNs);
+}
+
+// The drain's wait (see kDrainLimitNs); false if it gave up.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, nullptr, kDrainLimitNs);
 }
 
 // mbar_wait for a whole converged warp: every lane waits, and all lanes get

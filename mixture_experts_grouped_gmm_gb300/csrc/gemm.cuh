@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mma_commit_pair(drain, 0x1);
       else
         mma_commit(drain);
-      mbar_wait(drain, 0, nullptr);
+      mbar_wait_drain(drain, 0);
     }
     __syncwarp();
   } else if (C::Mx && warp == 2 + C::EPI) {
@@ -741,7 +741,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // every copy this warp issued has landed before tensor memory is freed
     if (lane == 0) {
       mma_commit(sfdrain);
-      mbar_wait(sfdrain, 0, nullptr);
+      mbar_wait_drain(sfdrain, 0);
     }
     __syncwarp();
   } else {
@@ -1016,12 +1016,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // wait for the TMA copies this CTA armed, bounded
     for (int s = 0; s < nst; ++s) {
       const uint32_t armed = issued / nst + ((uint32_t)s < issued % nst ? 1u : 0u);
-      if (armed) mbar_wait(&full[s], (armed - 1) & 1, nullptr);
+      if (armed) mbar_wait_drain(&full[s], (armed - 1) & 1);
     }
     if constexpr (C::Mx) {  // and the scale-row copies
       for (int q = 0; q < C::SF_SLOTS; ++q) {
         const uint32_t armed = sf_issued / C::SF_SLOTS + ((uint32_t)q < sf_issued % C::SF_SLOTS ? 1u : 0u);
-        if (armed) mbar_wait(&sf_full[q], (armed - 1) & 1, nullptr);
+        if (armed) mbar_wait_drain(&sf_full[q], (armed - 1) & 1);
       }
     }
     // pair: copies a peer issued for stages its leader never armed are not

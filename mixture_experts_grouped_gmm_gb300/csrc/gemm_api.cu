@@ -16,12 +16,19 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
 int sm_count() { return sm_count_cached(); }
 
-int common_checks(const void *args, int dtype, int64_t M, int K, int N, int E) {
-  if (!args) return MGEMM_EINVAL;
+// dtype, expert count and sizes (the checks that need no pointer)
+int size_checks(int dtype, int64_t M, int K, int N, int E) {
   if (dtype != MGEMM_BF16 && dtype != MGEMM_FP8_E4M3) return MGEMM_EINVAL;
   if (E < 1) return MGEMM_EINVAL;
   if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
   if (M < 0 || M >= (int64_t(1) << 31) || K <= 0 || N <= 0) return MGEMM_EINVAL;
+  return MGEMM_OK;
+}
+
+int common_checks(const void *args, int dtype, int64_t M, int K, int N, int E) {
+  if (!args) return MGEMM_EINVAL;
+  int rc = size_checks(dtype, M, K, N, E);
+  if (rc) return rc;
   if (!aligned16(args)) return MGEMM_EALIGN;
   const int kmul = dtype == MGEMM_FP8_E4M3 ? 16 : 8;
   if (K % kmul || N % kmul) return MGEMM_EALIGN;
@@ -114,6 +121,22 @@ bool make_out_map(CUtensorMap *m, void *out, int64_t rows, int64_t cols) {
 
 }  // namespace
 
+// Every host-side check of mgemm_fwd (the args block aside): the same codes,
+// returned before any CUDA call.
+int mgemm::fwd_checks(int dtype, int trans_b, const void *x, const float *sx, const void *w, const float *sw,
+                      const void *out, int64_t M, int K, int N, int E) {
+  int rc = size_checks(dtype, M, K, N, E);
+  if (rc) return rc;
+  const int kmul = dtype == MGEMM_FP8_E4M3 ? 16 : 8;
+  if (K % kmul || N % kmul) return MGEMM_EALIGN;
+  if (!x || !w || !out) return MGEMM_EINVAL;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(out)) return MGEMM_EALIGN;
+  const bool fp8 = dtype == MGEMM_FP8_E4M3;
+  if (fp8 && !trans_b) return MGEMM_ENOTSUP;
+  if (fp8 && (!sx || !sw)) return MGEMM_EINVAL;
+  return MGEMM_OK;
+}
+
 // mgemm_fwd; mgemm_fwd_scatter when row_map is given; mgemm_fwd_gated when
 // gate_rows > 0 (w [E, 2 gate_rows, K], N = 2 gate_rows, output gate_rows wide)
 static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
@@ -122,11 +145,8 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
                     int64_t group_rows_max = 0) {
   int rc = common_checks(args, dtype, M, K, N, E);
   if (rc) return rc;
-  if (!x || !w || !out) return MGEMM_EINVAL;
-  if (!aligned16(x) || !aligned16(w) || !aligned16(out)) return MGEMM_EALIGN;
+  if ((rc = fwd_checks(dtype, trans_b, x, sx, w, sw, out, M, K, N, E))) return rc;
   const bool fp8 = dtype == MGEMM_FP8_E4M3;
-  if (fp8 && !trans_b) return MGEMM_ENOTSUP;
-  if (fp8 && (!sx || !sw)) return MGEMM_EINVAL;
   if (M == 0) return MGEMM_OK;
   if ((rc = ensure_context())) return rc;
   const uint64_t es = fp8 ? 1 : 2;

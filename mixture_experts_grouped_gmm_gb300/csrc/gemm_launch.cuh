@@ -6,6 +6,12 @@
 
 namespace mgemm {
 
+// The host-side argument checks of mgemm_fwd other than those of the args
+// block (pointers, alignment, dtype and layout, sizes); MGEMM_OK or the code
+// mgemm_fwd would return.  Makes no CUDA call.
+int fwd_checks(int dtype, int trans_b, const void *x, const float *sx, const void *w, const float *sw,
+               const void *out, int64_t M, int K, int N, int E);
+
 template <class C>
 int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p_in, int grid,
                 cudaStream_t s, const CUtensorMap *sfa = nullptr, const CUtensorMap *sfb = nullptr) {

@@ -19,7 +19,7 @@
 // an earlier call leaks into the next.
 #include <mutex>
 
-#include "common.cuh"
+#include "gemm_launch.cuh"
 
 namespace {
 
@@ -27,9 +27,16 @@ constexpr size_t noalloc_args_bytes() { return mgemm::args_layout(MGEMM_NOALLOC_
 
 static __device__ __align__(256) uint8_t g_noalloc_args[noalloc_args_bytes()];
 
+// the args block of every E up to the stated maximum fits the array (the
+// layout grows with E)
+static_assert(mgemm::args_layout(MGEMM_NOALLOC_MAX_EXPERTS).bytes <= sizeof(g_noalloc_args),
+              "the static args block holds MGEMM_NOALLOC_MAX_EXPERTS experts");
+static_assert(MGEMM_NOALLOC_MAX_EXPERTS <= MGEMM_MAX_EXPERTS, "the fill kernel serves every E the array holds");
+
 // Device address of g_noalloc_args, looked up once per device with that
 // device current (in host code the symbol is only a stand-in, not an address
-// the GPU can use).
+// the GPU can use).  The address is cached for the life of the process, so
+// the library must not be used across a cudaDeviceReset of that device.
 void *noalloc_args_ptr(int *rc) {
   static void *ptrs[64] = {};
   static std::mutex mu;
@@ -55,11 +62,16 @@ void *noalloc_args_ptr(int *rc) {
 extern "C" int mgemm_fwd_noalloc(const int64_t *group_sizes, int E, int dtype, int trans_b, const void *x,
                                  const float *sx, const void *w, const float *sw, void *out, int64_t M, int K, int N,
                                  mgemm_stream_t stream) {
+  // Every check of mgemm_fill_args and mgemm_fwd comes first: a call that is
+  // rejected launches nothing and leaves the shared array as it was.
   if (!group_sizes) return MGEMM_EINVAL;
   if (E < 1) return MGEMM_EINVAL;
   if (E > MGEMM_NOALLOC_MAX_EXPERTS) return MGEMM_ETOOMANY;
-  if (mgemm::args_layout(E).bytes > sizeof(g_noalloc_args)) return MGEMM_ETOOMANY;
-  int rc = MGEMM_OK;
+  if (M < 0) return MGEMM_EINVAL;  // (mgemm_fill_args' M = -1 form has no use here)
+  if ((uintptr_t)group_sizes & 7) return MGEMM_EALIGN;
+  int rc = mgemm::fwd_checks(dtype, trans_b, x, sx, w, sw, out, M, K, N, E);
+  if (rc) return rc;
+  if (M == 0) return MGEMM_OK;  // no rows: nothing to schedule or compute
   void *args = noalloc_args_ptr(&rc);
   if (rc) return rc;
   rc = mgemm_fill_args(group_sizes, E, M, args, stream);

@@ -656,7 +656,7 @@ __global__ void __launch_bounds__(kCwThreads, 1)
   if (*vabort && warp == kCwConsumers && lane == 0) {
     for (int s = 0; s < kCwStages; ++s) {  // wait for this CTA's copies in flight, bounded
       const uint32_t armed = issued / kCwStages + ((uint32_t)s < issued % kCwStages ? 1u : 0u);
-      if (armed) mbar_wait(&full[s], (armed - 1) & 1, nullptr);
+      if (armed) mbar_wait_drain(&full[s], (armed - 1) & 1);
     }
   }
   if (warp == 0) {

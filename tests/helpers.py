@@ -25,7 +25,8 @@ def rel_err(got, ref):
 def assert_close(got, ref, tol, what=""):
     err, scale = rel_err(got, ref)
     assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), f"{what}: non-finite output"
-    assert err <= tol * scale + 1e-30, f"{what}: max|err| {err:.4g} > {tol} * max|ref| {scale:.4g}"
+    assert err <= tol * scale + 1e-30, (f"{what}: max|err| {err:.4g} > {tol} * max|ref| {scale:.4g} "
+                                        f"(ratio {err / max(scale, 1e-300):.3g})")
 
 
 def parse_args(args, E):

@@ -3,9 +3,12 @@ mgemm_gather_rows, mgemm_fwd_scatter, mgemm_silu_and_mul, mgemm_topk_sum,
 mgemm_fill_args with M = -1) and of moe.fused_experts / moe.fused_moe, against
 oracle.routing.  Expert ids are compared exactly.
 
-Integer outputs (gather) are compared bit for bit; GEMM outputs within
-1e-2 * max|ref| (bf16 operands, fp32 accumulation, one rounding); the whole
-layer (two GEMMs with bf16 caches between them) within 2e-2 * max|ref|.
+Integer outputs (gather) are compared bit for bit; GEMM outputs, and the
+whole layer, within 1e-2 * max|ref|.  The layer rounds to bf16 three times
+where the float64 oracle does not (the gated rows, the scattered entries and
+the final sum), each a relative error of at most 2^-9 of the value rounded;
+the gated rows' errors enter the second GEMM's sums with both signs, so the
+layer's max|err| stays a small multiple of 2^-9 * max|ref| (< 1e-2).
 Rows the kernels must not touch are pre-filled with a sentinel and checked."""
 
 import numpy as np
@@ -132,7 +135,7 @@ def test_fused_moe_layer(T, k, E, H, F):
     c2 = R.silu_and_mul(c1)
     c3 = R.fused_moe_gemm(c2, to_np(w2), sid, eid, tot, n, 1, 128, topk_weights=tw.cpu().numpy().ravel())
     ref = c3.reshape(T, k, H).sum(axis=1)
-    assert_close(to_np(out), ref, 2e-2, "fused_moe")
+    assert_close(to_np(out), ref, BF16_TOL, "fused_moe")
 
 
 @pytest.mark.parametrize("T,E,k,renorm,kind", [
@@ -172,7 +175,7 @@ def test_fused_moe_from_gating_logits():
     c1 = R.fused_moe_gemm(to_np(x), to_np(w1), sid, eid, tot, n, k, 128)
     c3 = R.fused_moe_gemm(R.silu_and_mul(c1), to_np(w2), sid, eid, tot, n, 1, 128, topk_weights=tw.ravel())
     ref = c3.reshape(T, k, H).sum(axis=1)
-    assert_close(to_np(out), ref, 2e-2, "fused_moe from gating logits")
+    assert_close(to_np(out), ref, BF16_TOL, "fused_moe from gating logits")
 
 
 @pytest.mark.parametrize("sizes,K,F", [([130, 0, 257, 64, 1], 192, 200), ([128] * 4, 256, 384), ([700], 64, 1000)])
@@ -211,4 +214,4 @@ def test_fused_moe_edges(T, k, E, H, F, renorm):
     torch.cuda.synchronize()
     tw, tid = R.topk_softmax(gating.cpu().numpy(), k, renorm)
     ref = np.stack([R.fused_moe_token(to_np(x)[t], to_np(w1), to_np(w2), tid[t], tw[t]) for t in range(T)])
-    assert_close(to_np(out), ref, 2e-2, "fused_moe edge case")
+    assert_close(to_np(out), ref, BF16_TOL, "fused_moe edge case")

@@ -4,11 +4,14 @@ mgemm_fwd_noalloc keeps the args block (the tile schedule derived from the
 group sizes) in a static device array inside the library, so a caller that may
 not call cudaMalloc -- code running inside another framework's launch callback,
 a loop where an allocation could stall the device, a runtime with a fixed
-workspace -- only passes inputs and the output.  These tests call it through
+workspace -- only passes inputs and the output.  The GPU tests call it through
 the C ABI twice in a row with different problems (the second with fewer
-experts, so stale contents of the shared array would show) and compare each
-result with the regular path: a caller-allocated args block filled by
-mgemm_fill_args and passed to mgemm_fwd.  This file is collected last."""
+experts, so stale contents of the shared array would show).  Each result must
+equal, bit for bit, the regular path on the same inputs (a caller-allocated
+args block filled by mgemm_fill_args and passed to mgemm_fwd: the same kernel
+on the same schedule), and match the oracle within the GEMM tolerance.  The
+FP8 cases reach the few-rows kernels (sparse groups) and the CTA-pair kernels
+(groups of 256 rows and more).  This file is collected last."""
 
 import ctypes
 
@@ -16,7 +19,8 @@ import numpy as np
 import pytest
 import torch
 
-from tests.helpers import BF16_TOL, assert_close, new_args, to_np
+from oracle import gmm as og
+from tests.helpers import BF16_TOL, FP8_TOL, assert_close, new_args, to_np
 
 DEV = "cuda"
 BF = torch.bfloat16
@@ -35,17 +39,25 @@ def B():
     return binding
 
 
-def rand_bf16(shape, seed):
+def rand_bf16(shape, seed, scale=1.0):
     g = torch.Generator(device=DEV).manual_seed(seed)
-    return torch.randn(shape, generator=g, device=DEV).to(BF)
+    return (torch.randn(shape, generator=g, device=DEV) * scale).to(BF)
 
 
-def regular_fwd(gs, x, w, trans_b, M, K, N, E):
+def regular_fwd(gs, dtype, x, sx, w, sw, trans_b, M, K, N, E):
     args = new_args(E, DEV)
     B().mgemm_fill_args(gs, E, M, args)
     out = torch.empty(M, N, dtype=BF, device=DEV)
-    B().mgemm_fwd(args, B().MGEMM_BF16, trans_b, x, None, w, None, out, M, K, N, E)
+    B().mgemm_fwd(args, dtype, trans_b, x, sx, w, sw, out, M, K, N, E)
     return out
+
+
+def quant_rows_gpu(t):
+    R, C = t.shape
+    q = torch.empty(R, C, dtype=torch.uint8, device=DEV)
+    s = torch.empty(R, dtype=torch.float32, device=DEV)
+    B().mgemm_quant_rowwise(t, q, s)
+    return q, s
 
 
 @pytest.mark.gpu
@@ -61,18 +73,47 @@ def test_noalloc_forward_matches_regular_path_twice():
         w = rand_bf16((E, N, K) if trans_b else (E, K, N), 20 + i)
         out = torch.full((M, N), float("nan"), dtype=BF, device=DEV)
         B().mgemm_fwd_noalloc(gs, B().MGEMM_BF16, trans_b, x, None, w, None, out, M, K, N, E)
-        ref = regular_fwd(gs, x, w, trans_b, M, K, N, E)
+        ref = regular_fwd(gs, B().MGEMM_BF16, x, None, w, None, trans_b, M, K, N, E)
         torch.cuda.synchronize()
-        assert_close(to_np(out), to_np(ref), BF16_TOL, f"no-alloc forward, call {i + 1}")
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"no-alloc bf16 call {i + 1} != mgemm_fwd"
+        want = og.gmm_fwd(to_np(x), to_np(w), sizes, trans_b=bool(trans_b))
+        assert_close(to_np(out), want, BF16_TOL, f"no-alloc bf16 call {i + 1} vs oracle")
 
 
-def test_noalloc_rejects_too_many_experts():
-    # checked on the host before any CUDA call, so this runs without a GPU
+@pytest.mark.gpu
+def test_noalloc_fp8_forward_matches_regular_path_twice():
+    cases = [
+        ([0, 700, 400, 0], 256, 272),            # E = 4, M / E >= 256 rows: CTA pairs
+        ([1, 0, 0, 2, 0, 1, 0, 0, 0, 3], 512, 256),  # E = 10, 7 rows: the few-rows kernels
+    ]
+    for i, (sizes, K, N) in enumerate(cases):
+        E, M = len(sizes), int(np.sum(sizes))
+        gs = torch.tensor(sizes, dtype=torch.int64, device=DEV)
+        xq, sx = quant_rows_gpu(rand_bf16((M, K), 30 + i))
+        wq, sw = quant_rows_gpu(rand_bf16((E * N, K), 40 + i, 0.02))
+        out = torch.full((M, N), float("nan"), dtype=BF, device=DEV)
+        B().mgemm_fwd_noalloc(gs, B().MGEMM_FP8_E4M3, 1, xq, sx, wq, sw, out, M, K, N, E)
+        ref = regular_fwd(gs, B().MGEMM_FP8_E4M3, xq, sx, wq, sw, 1, M, K, N, E)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"no-alloc fp8 call {i + 1} != mgemm_fwd"
+        want = og.gmm_fwd_fp8(to_np(xq), to_np(sx), to_np(wq).reshape(E, N, K), to_np(sw), sizes)
+        assert_close(to_np(out), want, FP8_TOL, f"no-alloc fp8 call {i + 1} vs oracle")
+
+
+def test_noalloc_host_checks_reject_before_any_launch():
+    # Each of these is rejected on the host before any CUDA call (the pointers
+    # are never dereferenced), so this runs with or without a GPU.
     lib = B().lib()
     p = ctypes.c_void_p(0x10000)
-    too_many = 1025
-    assert lib.mgemm_fwd_noalloc(p, too_many, 0, 0, p, None, p, None, p, 64, 128, 256, None) == -3
-    assert lib.mgemm_fwd_noalloc(None, 8, 0, 0, p, None, p, None, p, 64, 128, 256, None) == -1
-    # the stated maximum fits the library's array: E = 1024 passes the size check (and then,
-    # without a GPU here, fails at the first CUDA call rather than as too many experts)
-    assert lib.mgemm_fwd_noalloc(p, 1024, 0, 0, p, None, p, None, p, 64, 128, 256, None) not in (-1, -3)
+    odd = ctypes.c_void_p(0x10008)
+    f = lib.mgemm_fwd_noalloc
+    assert f(p, 1025, 0, 0, p, None, p, None, p, 64, 128, 256, None) == -3   # E over the array's maximum
+    assert f(None, 8, 0, 0, p, None, p, None, p, 64, 128, 256, None) == -1   # no group sizes
+    assert f(p, 0, 0, 0, p, None, p, None, p, 64, 128, 256, None) == -1      # E < 1
+    assert f(p, 8, 0, 0, p, None, p, None, p, -1, 128, 256, None) == -1      # M < 0
+    assert f(p, 8, 7, 0, p, None, p, None, p, 64, 128, 256, None) == -1      # unknown dtype
+    assert f(p, 8, 0, 0, None, None, p, None, p, 64, 128, 256, None) == -1   # no x
+    assert f(p, 8, 0, 0, odd, None, p, None, p, 64, 128, 256, None) == -2    # x not 16-byte aligned
+    assert f(p, 8, 0, 0, p, None, p, None, p, 64, 120, 260, None) == -2     # N % 8 != 0
+    assert f(p, 8, 1, 0, p, p, p, p, p, 64, 128, 256, None) == -5           # FP8 needs w [E, N, K]
+    assert f(p, 8, 1, 1, p, None, p, p, p, 64, 128, 256, None) == -1        # FP8 without sx
