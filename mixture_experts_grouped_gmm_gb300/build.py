@@ -38,7 +38,7 @@ def _inputs():
     files = []
     for d in (CSRC, INCLUDE):
         for f in os.listdir(d):
-            if f.endswith((".cu", ".cuh", ".h")):
+            if f.endswith((".cu", ".cuh", ".h", ".map")):
                 files.append(os.path.join(d, f))
     files.append(os.path.abspath(__file__))
     return files
@@ -122,7 +122,10 @@ def _build_into(lib_path, build_dir, verbose, extra_flags):
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = lib_path + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
+    # export only the C ABI (exports.map): no C++ symbol of the library can be
+    # bound to another copy of it in the same process
+    cmd = [nvcc, *ARCH, "-shared", "-Xlinker", "--version-script=" + os.path.join(CSRC, "exports.map"), "-o", tmp,
+           *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -20,6 +20,8 @@ cites the passage of the source pages it restates:
   sequence, dual colwise kernel; the MXFP8 path and its 32-row group
   padding) and bench_colwise_block_configs.py (_colwise_kernel,
   run_experiment).
+* "F8I4 Grouped Gemm Optimization for Sparse M" (pytorch/FBGEMM PR #3854),
+  title and Summary -- FP8 activations times INT4 weights (f8i4).
 * pytorch-labs/applied-ai issue 24 (the column-major fused MoE script on
   vLLM's fused_moe.py) -- moe_align_block_size and its worked example,
   fused_moe_kernel, silu_and_mul, topk_softmax, the fused_moe layer.
@@ -30,10 +32,11 @@ Modules:
   quant  -- power-of-two absmax scales, rowwise and per-group colwise quantize
   gmm    -- forward, dgrad and wgrad for bf16 and FP8-scaled operands
   mx     -- MXFP8: 32-element block scales (e8m0), row and per-group column block quantize, block-scaled fwd and wgrad
+  f8i4   -- FP8 x INT4: 32-element INT4 block quantize (e8m0 scales), nibble packing, the grouped forward
   routing -- moe_align_block_size, gather, topk_softmax, silu_and_mul and the fused_moe layer of the routed path
 
 Parity status: every function is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_*.py``; none is "parity unpinned".
 """
 
-from . import args, formats, gmm, mx, quant, routing  # noqa: F401
+from . import args, f8i4, formats, gmm, mx, quant, routing  # noqa: F401

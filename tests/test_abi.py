@@ -201,3 +201,20 @@ def test_mx_scale_row_bytes():
     for C, want in ((32, 16), (512, 16), (544, 32), (1408, 48), (2048, 64), (5120, 160), (96, 16)):
         assert B.mx_ld_sf(C) == want, C
         assert B.mx_ld_sf(C) >= C // 32 and B.mx_ld_sf(C) % 16 == 0
+
+
+def test_library_exports_only_the_c_abi():
+    # Only the C ABI (mgemm_*) is exported: C++ template instantiations and their
+    # function-local statics stay local, so two builds of the library in one
+    # process (the wait-probe test build and the product) share no symbol.
+    import shutil
+    import subprocess
+
+    from mixture_experts_grouped_gmm_gb300 import binding as B
+
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm (binutils) not available")
+    out = subprocess.run([nm, "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    names = [ln.split()[-1] for ln in out.splitlines() if ln.strip()]
+    assert names and all(n.startswith("mgemm_") for n in names), [n for n in names if not n.startswith("mgemm_")]

@@ -35,7 +35,7 @@ def _probe_library():
     from mixture_experts_grouped_gmm_gb300 import binding, build
 
     L = ctypes.CDLL(build.build_variant("mgemm_waitprobe", {"MGEMM_WAIT_LIMIT_NS": 0}))
-    for name in ("mgemm_fill_args", "mgemm_fwd"):
+    for name in ("mgemm_fill_args", "mgemm_fwd", "mgemm_last_error"):
         res, argt = binding._SIGS[name]
         getattr(L, name).restype = res
         getattr(L, name).argtypes = argt
@@ -58,7 +58,8 @@ def test_gemm_wait_timeout_sets_status_and_leaves_the_device_usable():
     args = new_args(E, DEV)
     out = sentinel_bf16((M, N), DEV)
     assert L.mgemm_fill_args(p(gs), E, M, p(args), stream) == 0
-    assert L.mgemm_fwd(p(args), B.MGEMM_BF16, 0, p(x), None, p(w), None, p(out), M, K, N, E, stream) == 0
+    rc = L.mgemm_fwd(p(args), B.MGEMM_BF16, 0, p(x), None, p(w), None, p(out), M, K, N, E, stream)
+    assert rc == 0, f"mgemm_fwd of the wait-probe build: {rc} ({L.mgemm_last_error().decode()})"
     torch.cuda.synchronize()  # the kernel returned
     assert parse_args(args, E)["status"] == 4, "the timed-out waits record MGEMM_STATUS_TIMEOUT"
     assert is_sentinel(out), "no tile is stored after a timeout"
