@@ -210,9 +210,15 @@ def sparse_m_extra(torch, B, dev, pk, E=128, reps=30):
     wq = torch.empty(E * N, K, dtype=torch.uint8, device=dev)
     sw = torch.empty(E * N, dtype=torch.float32, device=dev)
     B.mgemm_quant_rowwise(w.view(E * N, K), wq, sw)
+    # the same weights as INT4 blocks (the F8I4 path)
+    wp = torch.empty(E, N, K // 2, dtype=torch.uint8, device=dev)
+    wsf = torch.empty(B.int4_scale_bytes(E, N, K), dtype=torch.uint8, device=dev)
+    B.mgemm_quant_int4(w, wp, wsf)
     del w
     scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    res = {"shape": f"E={E} K=5120 N=8192 fp8 e4m3, rowwise scales; cold L2 (256 MB scrub between reps)",
+    res = {"shape": f"E={E} K=5120 N=8192 fp8 e4m3, rowwise scales; cold L2 (256 MB scrub between reps); "
+                    "f8i4: the same weights as INT4 blocks of 32 with e8m0 scales (mgemm_quant_int4), "
+                    "x rowwise FP8 (mgemm_fwd_f8i4)",
            "points": []}
     for tm in (1, 2, 4, 16, 64, 256):
         d = workloads.sparse_m(tm, E=E, K=K, N=N, device=dev, with_weights=False)
@@ -233,13 +239,30 @@ def sparse_m_extra(torch, B, dev, pk, E=128, reps=30):
         def fwd_only():
             B.mgemm_fwd(args, B.MGEMM_FP8_E4M3, 1, xq, sx, wq, sw, out, tm, K, N, E)
 
+        def f8i4_full():
+            B.mgemm_fill_args(gs, E, tm, args)
+            B.mgemm_quant_rowwise(d["x"], xq, sx)
+            B.mgemm_fwd_f8i4(args, xq, sx, wp, wsf, out, tm, K, N, E)
+
+        def f8i4_only():
+            B.mgemm_fwd_f8i4(args, xq, sx, wp, wsf, out, tm, K, N, E)
+
         t_full = time_events(torch, full, reps, scrub)
         t_fwd = time_events(torch, fwd_only, reps, scrub)
+        f8i4_full()
+        t_i4_full = time_events(torch, f8i4_full, reps, scrub)
+        t_i4 = time_events(torch, f8i4_only, reps, scrub)
         byts = n_touched * K * N + n_touched * N * 4 + tm * (K + 4 + 2 * N)
+        byts_i4 = n_touched * K * N // 2 + n_touched * N * K // 32 + tm * (K + 4 + 2 * N)
         res["points"].append({"total_M": tm, "experts_touched": n_touched,
                               "p50_us_fill_quant_fwd": round(t_full["p50_us"], 2),
                               "p50_us_fwd": round(t_fwd["p50_us"], 2),
-                              "fwd_hbm_frac": round(byts / (t_fwd["p50_us"] * 1e-6) / 1e9 / pk["hbm_gbs"], 3)})
+                              "fwd_hbm_frac": round(byts / (t_fwd["p50_us"] * 1e-6) / 1e9 / pk["hbm_gbs"], 3),
+                              "f8i4": {"p50_us_fill_quant_fwd": round(t_i4_full["p50_us"], 2),
+                                       "p50_us_fwd": round(t_i4["p50_us"], 2),
+                                       "fwd_hbm_frac": round(byts_i4 / (t_i4["p50_us"] * 1e-6) / 1e9 / pk["hbm_gbs"],
+                                                             3),
+                                       "fwd_vs_fp8": round(t_i4["p50_us"] / t_fwd["p50_us"], 3)}})
     # flat in E: one token, E experts (a prefix of the same weights)
     sweep = []
     d = workloads.sparse_m(1, E=8, K=K, N=N, device=dev, with_weights=False)
@@ -259,7 +282,7 @@ def sparse_m_extra(torch, B, dev, pk, E=128, reps=30):
         full()
         sweep.append({"E": Ee, "p50_us_fill_quant_fwd": round(time_events(torch, full, reps, scrub)["p50_us"], 2)})
     res["E_sweep_total_M_1"] = sweep
-    del wq, scrub
+    del wq, wp, wsf, scrub
     return res
 
 

@@ -294,6 +294,42 @@ int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, con
                 const float *sgo, void *grad_w, int64_t M, int K, int N, int E, int64_t ld, mgemm_stream_t stream);
 
 /*
+ * mgemm_quant_int4 -- the INT4 weights of the FP8 x INT4 grouped GEMM.
+ * "F8I4 Grouped Gemm Optimization for Sparse M" (FBGEMM PR #3854), title and
+ * Summary, names FP8 activations times INT4 weights and gives no format; this
+ * library's reading: per row (e, n) of w [E, N, K] and block of 32 consecutive
+ * k, s = 2^floor(log2(fp32(7 / max(amax, 1e-12)))) (the FP8 power-of-two rule
+ * at the INT4 range), q = clamp(round_half_even(w * s), -8, 7).
+ *   w       bf16 [E, N, K], row stride ld_in elements (>= K, % 8 == 0), device
+ *   packed  uint8 [E, N, K / 2]: two's-complement nibbles, element 2i in the low
+ *           nibble of byte i of its row (rows of K / 2 bytes, no padding)
+ *   sf      uint8, E * (K / 128) * N * 4 bytes: the e8m0 byte 127 - log2(s) of
+ *           each block (the decode factor 1 / s), contraction-block major:
+ *           block j of row (e, n) at ((e * (K / 128) + j / 4) * N + n) * 4 + j % 4
+ * K % 128 == 0.  Codes and bytes are unique (bit-exact against the oracle).
+ * Errors: -1 (sizes or NULL), -2 (alignment), -4 (CUDA).
+ */
+int mgemm_quant_int4(const void *w, int E, int N, int K, int64_t ld_in, uint8_t *packed, uint8_t *sf,
+                     mgemm_stream_t stream);
+
+/*
+ * mgemm_fwd_f8i4 -- the FP8 x INT4 grouped forward GEMM ("F8I4 Grouped Gemm
+ * Optimization for Sparse M", FBGEMM PR #3854, Summary: tiles only for the
+ * min(total_M, groups) non-empty groups):
+ *   out[r, n] = sum_k (e4m3(x[r, k]) / sx[r]) * q[e(r), n, k] * 2^(b[e, n, k / 32] - 127)
+ * in fp32 on the tensor cores (block-scaled MMA: x's row scale and the weight
+ * blocks' bytes are both applied inside it), rounded once to bf16 (RNE).
+ *   args     filled by mgemm_fill_args for these E group sizes and M
+ *   x, sx    e4m3 [M, K] and fp32 [M] row scales (mgemm_quant_rowwise)
+ *   w_packed, w_scales  as written by mgemm_quant_int4 for w [E, N, K]
+ *   out      bf16 [M, N]; rows of empty groups do not exist, nothing else is written
+ * K % 128 == 0, N % 8 == 0 (else -2).  Errors: -1 (sizes or NULL), -2
+ * (alignment), -3 (E), -4 (CUDA); device-side errors in the args status word.
+ */
+int mgemm_fwd_f8i4(const void *args, const uint8_t *x, const float *sx, const uint8_t *w_packed,
+                   const uint8_t *w_scales, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream);
+
+/*
  * mgemm_fwd_noalloc -- mgemm_fwd for callers that cannot allocate device memory.
  * The source pages have no counterpart to this call; it exists for callers
  * that may not call cudaMalloc (or any allocator) at the point where they run

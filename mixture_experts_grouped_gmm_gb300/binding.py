@@ -56,6 +56,11 @@ _SIGS = {
     "mgemm_wgrad_mx": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int64, ctypes.c_void_p]),
+    "mgemm_quant_int4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "mgemm_fwd_f8i4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_void_p]),
     "mgemm_colwise_ld": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int]),
     "mgemm_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -194,6 +199,26 @@ def mgemm_wgrad_mx(args, x, sx, go, sgo, grad_w, M, K, N, E, ld=None):
     ld = mgemm_colwise_ld(M, E) if ld is None else ld
     _check(lib().mgemm_wgrad_mx(_p(args), _p(x), _p(sx), _p(go), _p(sgo), _p(grad_w), int(M), int(K), int(N), int(E),
                                 int(ld), _stream(grad_w)), "mgemm_wgrad_mx")
+
+
+def int4_scale_bytes(E, N, K):
+    """Bytes of mgemm_quant_int4's scale array: one e8m0 byte per 32 elements."""
+    return E * (K // 128) * N * 4
+
+
+def mgemm_quant_int4(w, packed, sf):
+    """w bf16 [E, N, K] -> packed uint8 [E, N, K // 2], sf uint8 [int4_scale_bytes]."""
+    _cuda(w, packed, sf)
+    E, N, K = w.shape
+    if w.stride(2) != 1 or w.stride(0) != N * w.stride(1):
+        raise MgemmError("mgemm_quant_int4 takes w [E, N, K] with rows (e, n) at a common stride")
+    _check(lib().mgemm_quant_int4(_p(w), E, N, K, w.stride(1), _p(packed), _p(sf), _stream(w)), "mgemm_quant_int4")
+
+
+def mgemm_fwd_f8i4(args, x, sx, w_packed, w_scales, out, M, K, N, E):
+    _cuda(args, x, sx, w_packed, w_scales, out)
+    _check(lib().mgemm_fwd_f8i4(_p(args), _p(x), _p(sx), _p(w_packed), _p(w_scales), _p(out), int(M), int(K), int(N),
+                                int(E), _stream(out)), "mgemm_fwd_f8i4")
 
 
 def mgemm_colwise_ld(M, E):

@@ -151,6 +151,71 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(const __nv_bfloat16 *__re
   }
 }
 
+// ------------------------------------------------------------ INT4 blocks
+// The weights of the FP8 x INT4 grouped GEMM ("F8I4 Grouped Gemm
+// Optimization for Sparse M", FBGEMM PR #3854; the page gives no format, this
+// is the library's reading): w [E, N, K] bf16, one warp per row (e, n), 8
+// elements per lane and chunk of 256; lanes 4j .. 4j + 3 hold block j of 32.
+// Per block: s = 2^floor(log2(fp32(7 / max(amax, 1e-12)))), q = clamp(
+// round_half_even(w s), -8, 7) (w s is exact), nibbles packed two per byte
+// along K (element 2i in the low nibble of byte i), and the e8m0 byte of the
+// decode factor 1 / s (254 minus s's biased exponent) stored contraction-block
+// major: sf[((e (K / 128) + k / 128) N + n) 4 + (k % 128) / 32], so that the
+// scales of BN consecutive rows for one block of 128 are BN x 4 contiguous bytes.
+__device__ __forceinline__ float int4_scale_from_amax(float amax) {
+  const float s = __fdiv_rn(7.0f, fmaxf(amax, 1e-12f));
+  return __uint_as_float(__float_as_uint(s) & 0x7F800000u);
+}
+
+__device__ __forceinline__ uint32_t nib(float v, float s) {
+  const int q = min(7, max(-8, __float2int_rn(v * s)));
+  return (uint32_t)q & 15u;
+}
+
+// 8 bf16 -> 8 packed nibbles (element 0 in bits 0-3)
+__device__ __forceinline__ uint32_t pack8_int4(const uint4 &v, float s) {
+  return nib(bf16_lo(v.x), s) | nib(bf16_hi(v.x), s) << 4 | nib(bf16_lo(v.y), s) << 8 | nib(bf16_hi(v.y), s) << 12 |
+         nib(bf16_lo(v.z), s) << 16 | nib(bf16_hi(v.z), s) << 20 | nib(bf16_lo(v.w), s) << 24 |
+         nib(bf16_hi(v.w), s) << 28;
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(256) quant_int4_kernel(const __nv_bfloat16 *__restrict__ in, int64_t R, int N, int K,
+                                                         int64_t ld_in, uint8_t *__restrict__ out,
+                                                         uint8_t *__restrict__ sf) {
+  const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int kblocks = K / 128;
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < R; row += warps_total) {
+    const int64_t e = row / N, n = row % N;
+    const __nv_bfloat16 *src = in + row * ld_in;
+    uint8_t *dst = out + row * (K / 2);
+    for (int c0 = 0; c0 < K; c0 += NCH * 256) {
+      uint4 v[NCH];
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int c = c0 + i * 256 + lane * 8;
+        v[i] = c < K ? ldg_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int c = c0 + i * 256 + lane * 8;
+        float a = amax8(v[i], 0.f);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const float s = int4_scale_from_amax(a);
+        if (c < K) {  // K % 128 == 0: a block's four lanes agree
+          *reinterpret_cast<uint32_t *>(dst + c / 2) = pack8_int4(v[i], s);
+          if ((lane & 3) == 0)
+            sf[((e * kblocks + c / 128) * N + n) * 4 + (c % 128) / 32] = (uint8_t)(254u - (__float_as_uint(s) >> 23));
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ MX colwise
 // Per-group colwise MX blocks (the wgrad operands).  CTA (column block, j):
 // rows 128 j .. 128 j + 127 of the padded column-major layout, which lie in
@@ -730,6 +795,31 @@ extern "C" int mgemm_quant_mx(const void *in, int64_t R, int64_t C, int64_t ld_i
                       out, ld_out, sf, ld_sf);
   return launch_pdl(quant_mx_kernel<8>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_mx launch", x, R, C, ld_in, out,
                     ld_out, sf, ld_sf);
+}
+
+extern "C" int mgemm_quant_int4(const void *w, int E, int N, int K, int64_t ld_in, uint8_t *packed, uint8_t *sf,
+                                mgemm_stream_t stream) {
+  if (E < 1 || N < 1 || K < 1 || K % 128 || ld_in < K) return MGEMM_EINVAL;
+  if ((int64_t)E * N >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  if (!w || !packed || !sf) return MGEMM_EINVAL;
+  if (((uintptr_t)w & 15) || ((uintptr_t)packed & 15) || ((uintptr_t)sf & 15) || (ld_in % 8)) return MGEMM_EALIGN;
+  const int64_t R = (int64_t)E * N;
+  const int64_t blocks_needed = (R + 7) / 8;
+  int sms = sm_count_cached();
+  if (sms <= 0) sms = 148;
+  const int64_t cap = (int64_t)sms * 32;
+  const int blocks = (int)(blocks_needed < cap ? blocks_needed : cap);
+  const __nv_bfloat16 *x = (const __nv_bfloat16 *)w;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int nch = (K + 255) / 256;
+  if (nch <= 2)
+    return launch_pdl(quant_int4_kernel<2>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_int4 launch", x, R, N, K,
+                      ld_in, packed, sf);
+  if (nch <= 4)
+    return launch_pdl(quant_int4_kernel<4>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_int4 launch", x, R, N, K,
+                      ld_in, packed, sf);
+  return launch_pdl(quant_int4_kernel<8>, dim3(blocks), dim3(256), 0, s, 1, "mgemm_quant_int4 launch", x, R, N, K, ld_in,
+                    packed, sf);
 }
 
 extern "C" int mgemm_quant_colwise_mx(const void *args, int E, int64_t M, const void *in1, int64_t C1, uint8_t *out1,
