@@ -208,6 +208,25 @@ int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x, const flo
               const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream);
 
 /*
+ * mgemm_fwd_fp8_strided -- mgemm_fwd (dtype MGEMM_FP8_E4M3, w [E, N, K]) with
+ * the e4m3 weights addressed through strides: w[e, n, k] at byte
+ * e * ld_we + n * ld_wn + k.  With the weights' master copy stored [E, K, N]
+ * (the layout of the GRIN benchmark script), the forward operand (one scale
+ * per (e, n) over K) is mgemm_quant_colwise_grouped of w viewed [E * K, N]
+ * with E groups of K rows ([FP8 commit message]: the per-group colwise
+ * kernel): its padded column-major codes hold w[e, n, k] at
+ * n * ld + e * ceil(K / 128) * 128 + k, i.e. ld_wn = ld (as passed to it),
+ * ld_we = K rounded up to 128, and its scales [E * N] are this call's sw.  No
+ * transposed copy of the weights is needed.
+ *   ld_wn  >= K, % 16 == 0;  ld_we >= K (any value when E == 1), % 16 == 0
+ *   the other arguments: as mgemm_fwd with dtype MGEMM_FP8_E4M3, trans_b = 1.
+ * Errors as mgemm_fwd.
+ */
+int mgemm_fwd_fp8_strided(const void *args, const void *x, const float *sx, const void *w, int64_t ld_wn,
+                          int64_t ld_we, const float *sw, void *out, int64_t M, int K, int N, int E,
+                          mgemm_stream_t stream);
+
+/*
  * mgemm_dgrad -- grad_x[r, :] = grad_out[r, :] . w[e(r)]^T (the backward pass
  * of gmm w.r.t. x).  [GRB benchmark script]: out.sum().backward();
  * [GRB review, grouped_gemm.cu]: the trans_b template; [FP8 commit message]:
@@ -292,6 +311,23 @@ int mgemm_wgrad_mx(const void *args, const uint8_t *x, const uint8_t *sx, const 
  */
 int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, const void *grad_out,
                 const float *sgo, void *grad_w, int64_t M, int K, int N, int E, int64_t ld, mgemm_stream_t stream);
+
+/*
+ * mgemm_fill_args_quant_rowwise -- mgemm_fill_args and mgemm_quant_rowwise of
+ * the token rows in one launch (the two independent steps before an FP8
+ * forward: "Support GPU-resident batch sizes", the argument fill; "[moe
+ * training] Optimize FP8 MoE backward pass" commit message, the fused rowwise
+ * scale + cast).  The args block is exactly mgemm_fill_args(group_sizes, E, M,
+ * args); xq and sx exactly mgemm_quant_rowwise(x [M, K]).  One CTA fills the
+ * args block while the others cast rows, so at sparse M the pair costs about
+ * one launch instead of two.
+ *   group_sizes int64[E], device; args as for mgemm_fill_args (M >= 0 here)
+ *   x     bf16 [M, K], row stride ld_x elements; xq e4m3 [M, K], row stride ld_q
+ *         bytes; sx fp32 [M]
+ * K % 8 == 0, ld_x % 8 == 0, ld_q % 8 == 0.  Errors as for the two calls.
+ */
+int mgemm_fill_args_quant_rowwise(const int64_t *group_sizes, int E, int64_t M, void *args, const void *x, int64_t K,
+                                  int64_t ld_x, uint8_t *xq, int64_t ld_q, float *sx, mgemm_stream_t stream);
 
 /*
  * mgemm_quant_int4 -- the INT4 weights of the FP8 x INT4 grouped GEMM.

@@ -7,4 +7,4 @@ synthetic inputs.
 """
 
 from . import binding  # noqa: F401
-from .gmm import gmm  # noqa: F401
+from .gmm import gmm, gmm_fp8  # noqa: F401

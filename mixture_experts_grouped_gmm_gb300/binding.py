@@ -56,6 +56,13 @@ _SIGS = {
     "mgemm_wgrad_mx": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int64, ctypes.c_void_p]),
+    "mgemm_fill_args_quant_rowwise": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                                     ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
+    "mgemm_fwd_fp8_strided": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_void_p]),
     "mgemm_quant_int4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "mgemm_fwd_f8i4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -199,6 +206,24 @@ def mgemm_wgrad_mx(args, x, sx, go, sgo, grad_w, M, K, N, E, ld=None):
     ld = mgemm_colwise_ld(M, E) if ld is None else ld
     _check(lib().mgemm_wgrad_mx(_p(args), _p(x), _p(sx), _p(go), _p(sgo), _p(grad_w), int(M), int(K), int(N), int(E),
                                 int(ld), _stream(grad_w)), "mgemm_wgrad_mx")
+
+
+def mgemm_fill_args_quant_rowwise(group_sizes, E, M, args, x, xq, sx):
+    """mgemm_fill_args(group_sizes, E, M, args) and mgemm_quant_rowwise(x, xq, sx) in one launch."""
+    _cuda(group_sizes, args, x, xq, sx)
+    R, K = x.shape
+    if R != M:
+        raise MgemmError("x must hold the M token rows")
+    _check(lib().mgemm_fill_args_quant_rowwise(_p(group_sizes), int(E), int(M), _p(args), _p(x), K, x.stride(0),
+                                               _p(xq), xq.stride(0), _p(sx), _stream(x)),
+           "mgemm_fill_args_quant_rowwise")
+
+
+def mgemm_fwd_fp8_strided(args, x, sx, w, ld_wn, ld_we, sw, out, M, K, N, E):
+    """FP8 forward with the e4m3 weights w[e, n, k] at byte e * ld_we + n * ld_wn + k of w."""
+    _cuda(args, x, sx, w, sw, out)
+    _check(lib().mgemm_fwd_fp8_strided(_p(args), _p(x), _p(sx), _p(w), int(ld_wn), int(ld_we), _p(sw), _p(out), int(M),
+                                       int(K), int(N), int(E), _stream(out)), "mgemm_fwd_fp8_strided")
 
 
 def int4_scale_bytes(E, N, K):

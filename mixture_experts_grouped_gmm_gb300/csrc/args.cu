@@ -48,16 +48,15 @@ __device__ __forceinline__ T block_inclusive_scan(T v, T *warp_tot) {
   return v;
 }
 
+// The fill of one args block by the NT threads of one CTA.
 template <int NT>
-__global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict__ sizes, int E, int64_t M,
-                                                       uint8_t *__restrict__ args) {
+__device__ __forceinline__ void fill_args_body(const int64_t *__restrict__ sizes, int E, int64_t M,
+                                               uint8_t *__restrict__ args) {
   __shared__ int64_t s_size[NT];
   __shared__ int64_t tot64[NT / 32 > 0 ? NT / 32 : 1];
   __shared__ int tot32[NT / 32 > 0 ? NT / 32 : 1];
   const ArgsLayout L = args_layout(E);
   const int t = threadIdx.x;
-  pdl_wait();
-  pdl_trigger();
   const int64_t m = t < E ? sizes[t] : 0;
   s_size[t] = m;
   const int any_neg = __syncthreads_or(m < 0);
@@ -123,6 +122,40 @@ __global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict
     hdr[2] = E;
     hdr[3] = 0;  // work counter of the colwise quantizer
     *(int64_t *)(args + 16) = check ? M : total_sh;
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) fill_args_kernel(const int64_t *__restrict__ sizes, int E, int64_t M,
+                                                       uint8_t *__restrict__ args) {
+  pdl_wait();
+  pdl_trigger();
+  fill_args_body<NT>(sizes, E, M, args);
+}
+
+// mgemm_fill_args and mgemm_quant_rowwise of the token rows in one launch: CTA
+// 0 fills the args block while the other CTAs cast rows (one warp per row,
+// two passes over the row), so the two independent steps run side by side.
+template <int NT, int NCH>
+__global__ void __launch_bounds__(NT) fill_quant_kernel(const int64_t *__restrict__ sizes, int E, int64_t M,
+                                                        uint8_t *__restrict__ args, int64_t R,
+                                                        const __nv_bfloat16 *__restrict__ x, int64_t C,
+                                                        int64_t ld_in, uint8_t *__restrict__ q, int64_t ld_out,
+                                                        float *__restrict__ scales) {
+  pdl_wait();
+  pdl_trigger();
+  if (blockIdx.x == 0) {
+    fill_args_body<NT>(sizes, E, M, args);
+    return;
+  }
+  constexpr int W = NT / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t step = (int64_t)(gridDim.x - 1) * W;
+  for (int64_t row = (int64_t)(blockIdx.x - 1) * W + (threadIdx.x >> 5); row < R; row += step) {
+    if constexpr (NCH > 0)
+      quant_row_regs<NCH>(x + row * ld_in, C, q + row * ld_out, scales + row, lane);
+    else
+      quant_row_two_pass(x + row * ld_in, C, q + row * ld_out, scales + row, lane);
   }
 }
 
@@ -233,6 +266,45 @@ extern "C" int mgemm_fill_args(const int64_t *group_sizes, int E, int64_t M, voi
   if (E <= 128)
     return launch_pdl(fill_args_kernel<128>, dim3(1), dim3(128), 0, s, 1, "mgemm_fill_args launch", group_sizes, E, M, a);
   return launch_pdl(fill_args_kernel<1024>, dim3(1), dim3(1024), 0, s, 1, "mgemm_fill_args launch", group_sizes, E, M, a);
+}
+
+extern "C" int mgemm_fill_args_quant_rowwise(const int64_t *group_sizes, int E, int64_t M, void *args, const void *x,
+                                             int64_t K, int64_t ld_x, uint8_t *xq, int64_t ld_q, float *sx,
+                                             mgemm_stream_t stream) {
+  if (!group_sizes || !args) return MGEMM_EINVAL;
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  if (M < 0 || M >= (int64_t(1) << 31) || K < 0 || ld_x < K || ld_q < K) return MGEMM_EINVAL;
+  if (M > 0 && K > 0 && (!x || !xq || !sx)) return MGEMM_EINVAL;
+  if (((uintptr_t)args & 15) || ((uintptr_t)group_sizes & 7)) return MGEMM_EALIGN;
+  if (M > 0 && K > 0 && (((uintptr_t)x & 15) || ((uintptr_t)xq & 7) || ((uintptr_t)sx & 3) || K % 8 || ld_x % 8 ||
+                         ld_q % 8))
+    return MGEMM_EALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t *a = (uint8_t *)args;
+  const __nv_bfloat16 *xb = (const __nv_bfloat16 *)x;
+  const int64_t rows = K > 0 ? M : 0;  // no columns: nothing to cast (the scales stay unwritten)
+  int sms = sm_count_cached();
+  if (sms <= 0) sms = 148;
+  auto blocks = [&](int w) -> unsigned {
+    const int64_t need = (rows + w - 1) / w, cap = (int64_t)sms * 8;
+    return 1u + (unsigned)(need < cap ? need : cap);
+  };
+  // rows of up to 24 x 256 elements stay in registers (one read) with the
+  // 32- and 128-thread blocks; the 1024-thread block reads its rows twice
+  const bool regs = K <= 24 * 256;
+  if (E <= 32)
+    return regs ? launch_pdl(fill_quant_kernel<32, 24>, dim3(blocks(1)), dim3(32), 0, s, 1,
+                             "fill + rowwise cast launch", group_sizes, E, M, a, rows, xb, K, ld_x, xq, ld_q, sx)
+                : launch_pdl(fill_quant_kernel<32, 0>, dim3(blocks(1)), dim3(32), 0, s, 1,
+                             "fill + rowwise cast launch", group_sizes, E, M, a, rows, xb, K, ld_x, xq, ld_q, sx);
+  if (E <= 128)
+    return regs ? launch_pdl(fill_quant_kernel<128, 24>, dim3(blocks(4)), dim3(128), 0, s, 1,
+                             "fill + rowwise cast launch", group_sizes, E, M, a, rows, xb, K, ld_x, xq, ld_q, sx)
+                : launch_pdl(fill_quant_kernel<128, 0>, dim3(blocks(4)), dim3(128), 0, s, 1,
+                             "fill + rowwise cast launch", group_sizes, E, M, a, rows, xb, K, ld_x, xq, ld_q, sx);
+  return launch_pdl(fill_quant_kernel<1024, 0>, dim3(blocks(32)), dim3(1024), 0, s, 1, "fill + rowwise cast launch",
+                    group_sizes, E, M, a, rows, xb, K, ld_x, xq, ld_q, sx);
 }
 
 extern "C" int mgemm_num_sms(void) {

@@ -453,6 +453,11 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -522,6 +527,104 @@ __device__ __forceinline__ float pow2_scale_from_amax(float amax) {
 // Two floats -> two e4m3 bytes (round to nearest even, saturate to +-448).
 __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// ---------------------------------------------------------------- rows of bf16
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ float amax8(const uint4 &v, float a) {
+  a = fmaxf(a, fabsf(bf16_lo(v.x)));
+  a = fmaxf(a, fabsf(bf16_hi(v.x)));
+  a = fmaxf(a, fabsf(bf16_lo(v.y)));
+  a = fmaxf(a, fabsf(bf16_hi(v.y)));
+  a = fmaxf(a, fabsf(bf16_lo(v.z)));
+  a = fmaxf(a, fabsf(bf16_hi(v.z)));
+  a = fmaxf(a, fabsf(bf16_lo(v.w)));
+  a = fmaxf(a, fabsf(bf16_hi(v.w)));
+  return a;
+}
+
+// 8 bf16 -> 8 e4m3 bytes (x * s is exact: s is a power of two)
+__device__ __forceinline__ uint2 cast8(const uint4 &v, float s) {
+  uint2 o;
+  o.x = (uint32_t)cvt_e4m3x2(bf16_lo(v.x) * s, bf16_hi(v.x) * s) |
+        ((uint32_t)cvt_e4m3x2(bf16_lo(v.y) * s, bf16_hi(v.y) * s) << 16);
+  o.y = (uint32_t)cvt_e4m3x2(bf16_lo(v.z) * s, bf16_hi(v.z) * s) |
+        ((uint32_t)cvt_e4m3x2(bf16_lo(v.w) * s, bf16_hi(v.w) * s) << 16);
+  return o;
+}
+
+__device__ __forceinline__ float warp_max(float a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  return a;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// One row of C bf16 values (C % 8 == 0) -> e4m3 codes and its power-of-two
+// scale, by one warp: the magnitude maximum in a first pass, the cast in a
+// second (served by L2).  Loads go out eight chunks of 256 elements at a time.
+__device__ __forceinline__ void quant_row_two_pass(const __nv_bfloat16 *src, int64_t C, uint8_t *dst, float *scale,
+                                                   int lane) {
+  float a = 0.f;
+  for (int64_t c0 = 0; c0 < C; c0 += 8 * 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t c = c0 + i * 256 + lane * 8;
+      v[i] = c < C ? ldg_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = amax8(v[i], a);
+  }
+  a = warp_max(a);
+  const float s = pow2_scale_from_amax(a);
+  if (lane == 0) *scale = s;
+  for (int64_t c0 = 0; c0 < C; c0 += 8 * 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t c = c0 + i * 256 + lane * 8;
+      v[i] = c < C ? *reinterpret_cast<const uint4 *>(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t c = c0 + i * 256 + lane * 8;
+      if (c < C) *reinterpret_cast<uint2 *>(dst + c) = cast8(v[i], s);
+    }
+  }
+}
+
+// The same for a row of at most NCH * 256 elements held in registers between
+// the two steps (one DRAM read).
+template <int NCH>
+__device__ __forceinline__ void quant_row_regs(const __nv_bfloat16 *src, int64_t C, uint8_t *dst, float *scale,
+                                               int lane) {
+  uint4 v[NCH];
+  float a = 0.f;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int64_t c = ((int64_t)j * 32 + lane) * 8;
+    v[j] = c < C ? ldg_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) a = amax8(v[j], a);
+  a = warp_max(a);
+  const float s = pow2_scale_from_amax(a);
+  if (lane == 0) *scale = s;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int64_t c = ((int64_t)j * 32 + lane) * 8;
+    if (c < C) *reinterpret_cast<uint2 *>(dst + c) = cast8(v[j], s);
+  }
 }
 
 }  // namespace mgemm

@@ -178,10 +178,19 @@ struct TileInfo {
   int e, kb_count, a_row, b_row, n0, x0, lo, hi, out_row0, out_rows;
 };
 
+// FP8 with fewer than 128 token rows in all (the run-time-ring kernels with an
+// A box of a_rows < 128 rows): every group has fewer than 128 rows, so every
+// active group owns exactly one row tile (mtile_start[a] = a) and a tile's
+// group is found without the prefix search.
 template <class C>
-__device__ __forceinline__ int total_tiles(const GemmParams &p, const ArgsView &av) {
+__device__ __forceinline__ bool one_tile_per_group(const GemmParams &p) {
+  return C::Mode == kModeRows && C::DynRing && C::Fp8 && p.a_rows < C::BM;
+}
+
+template <class C>
+__device__ __forceinline__ int total_tiles(const GemmParams &p, const ArgsView &av, int na) {
   if (C::Mode == kModeRows) {
-    const int na = *av.n_active;
+    if (one_tile_per_group<C>(p)) return na * p.n_tiles;
     return (C::Pair ? av.ptile_start[na] : av.mtile_start[na]) * p.n_tiles;
   }
   return p.E * p.mt_k * p.n_tiles;
@@ -209,14 +218,18 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmParams &p, cons
     // share one weight tile through L2 instead of each streaming its own.
     const int *start = C::Pair ? av.ptile_start : av.mtile_start;
     const int gm = t / p.n_tiles;
-    int lo = 0, hi = *av.n_active - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(start + mid) <= gm) lo = mid; else hi = mid - 1;
+    int lo = gm, m_first = gm, mt_g = 1;
+    if (!one_tile_per_group<C>(p)) {
+      lo = 0;
+      int hi = *av.n_active - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(start + mid) <= gm) lo = mid; else hi = mid - 1;
+      }
+      m_first = __ldg(start + lo);
+      mt_g = __ldg(start + lo + 1) - m_first;
     }
     ti.e = __ldg(av.active + lo);
-    const int m_first = __ldg(start + lo);
-    const int mt_g = __ldg(start + lo + 1) - m_first;
     const int local = t - m_first * p.n_tiles;
     const int mt = local % mt_g;
     ti.n0 = (local / mt_g) * (p.gated ? p.bn / 2 : p.bn);
@@ -347,19 +360,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait();
-  pdl_trigger();
-  const ArgsView av(p.args, p.E);
-  if (*av.status != 0) return;
-  const int total = total_tiles<C>(p, av);
   // CTA pairs walk the tiles per cluster: both CTAs of a pair see the same
   // sequence and leave (or stay) together
   const uint32_t rank = C::Pair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
   const int t_first = C::Pair ? (int)cluster_id_x() : (int)blockIdx.x;
   const int t_step = C::Pair ? (int)ncluster_x() : (int)gridDim.x;
-  if (t_first >= total) return;
 
+  // Set-up (barriers, tensor memory, descriptor prefetch) reads nothing an
+  // earlier kernel writes, so it runs before the wait for the previous grid of
+  // the stream and overlaps that grid's tail.  A CTA with no tile (or a
+  // non-zero status) runs no role loop and goes straight to the teardown.
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
@@ -406,6 +417,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+  const ArgsView av(p.args, p.E);
+  const int status0 = *av.status, n_active0 = *av.n_active;  // two independent loads
+  const int total = status0 != 0 ? 0 : total_tiles<C>(p, av, n_active0);
   volatile int *vabort = abort_flag;
   const int bn = p.bn;
   // an abort in one CTA of a pair is raised in the other as well

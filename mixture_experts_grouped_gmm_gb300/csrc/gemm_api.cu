@@ -80,12 +80,13 @@ int64_t rows_tiles_estimate(int64_t M, int E) {
 // {128, Nrows, Kc / 128, E} (chunk stride 128 B; Kc % 128 == 0 keeps every box
 // row inside its row).
 bool few_maps(CUtensorMap *ta, CUtensorMap *tb, const void *a, int64_t M, int Kc, uint32_t a_rows, const void *b,
-              int Nrows, int E, int bn, uint32_t kc) {
+              int Nrows, int E, int bn, uint32_t kc, uint64_t ld_row = 0, uint64_t ld_exp = 0) {
   const uint64_t da[3] = {128, (uint64_t)M, (uint64_t)Kc / 128};
   const uint64_t sa[2] = {(uint64_t)Kc, 128};
   const uint32_t ba[3] = {128, a_rows, kc};
   const uint64_t db[4] = {128, (uint64_t)Nrows, (uint64_t)Kc / 128, (uint64_t)E};
-  const uint64_t sb[3] = {(uint64_t)Kc, 128, (uint64_t)Nrows * Kc};
+  // B rows (e, n) at e ld_exp + n ld_row (bytes; by default [E, Nrows, Kc] contiguous)
+  const uint64_t sb[3] = {ld_row ? ld_row : (uint64_t)Kc, 128, ld_exp ? ld_exp : (uint64_t)Nrows * Kc};
   const uint32_t bb[4] = {128, (uint32_t)bn, kc, 1};
   CUtensorMap ma, mb;  // the caller's maps stay intact unless both views encode
   if (!make_map(&ma, true, 3, a, da, sa, ba) || !make_map(&mb, true, 4, b, db, sb, bb)) return false;
@@ -139,10 +140,11 @@ int mgemm::fwd_checks(int dtype, int trans_b, const void *x, const float *sx, co
 
 // mgemm_fwd; mgemm_fwd_scatter when row_map is given; mgemm_fwd_gated when
 // gate_rows > 0 (w [E, 2 gate_rows, K], N = 2 gate_rows, output gate_rows wide)
+// ld_wn, ld_we (FP8 only; 0 = contiguous [E, N, K]): w[e, n, k] at e ld_we + n ld_wn + k bytes
 static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
                     const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream,
                     const int32_t *row_map, int64_t map_limit, const float *row_weight, int gate_rows = 0,
-                    int64_t group_rows_max = 0) {
+                    int64_t group_rows_max = 0, int64_t ld_wn = 0, int64_t ld_we = 0) {
   int rc = common_checks(args, dtype, M, K, N, E);
   if (rc) return rc;
   if ((rc = fwd_checks(dtype, trans_b, x, sx, w, sw, out, M, K, N, E))) return rc;
@@ -190,9 +192,9 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   const int out_cols = gated ? gate_rows : N;
   const int tile_cols = gated ? bn / 2 : bn;
   bool b_one_box = false;
-  if (trans_b) {  // w [E, N, K]
+  if (trans_b) {  // w [E, N, K] (FP8: rows at the given strides)
     const uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
-    const uint64_t st[2] = {(uint64_t)K * es, (uint64_t)N * K * es};
+    const uint64_t st[2] = {ld_wn ? (uint64_t)ld_wn : (uint64_t)K * es, ld_we ? (uint64_t)ld_we : (uint64_t)N * K * es};
     const uint32_t box[3] = {bk, (uint32_t)(pair || gated ? bn / 2 : bn), 1};
     if (!make_map(&tb, fp8, 3, w, d, st, box)) return MGEMM_ECUDA;
   } else {  // w [E, K, N], loaded as 64-column MN-major chunks
@@ -250,9 +252,9 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   if (fp8 && a_rows < 128 && K % 128 == 0) {
     // few token rows: the weight stream gets the shared memory the A slots leave
     // (4 / 2 / 1 contraction blocks per stage for BN 64 / 128 / 256)
-    if (bn <= 64 && few_maps(&ta, &tb, x, M, K, a_rows, w, N, E, bn, 4))
+    if (bn <= 64 && few_maps(&ta, &tb, x, M, K, a_rows, w, N, E, bn, 4, ld_wn, ld_we))
       return gemm_fp8_rows_few_narrow(ta, tb, to, p, grid, s);
-    if (bn > 64 && bn <= 128 && few_maps(&ta, &tb, x, M, K, a_rows, w, N, E, bn, 2))
+    if (bn > 64 && bn <= 128 && few_maps(&ta, &tb, x, M, K, a_rows, w, N, E, bn, 2, ld_wn, ld_we))
       return gemm_fp8_rows_few_mid(ta, tb, to, p, grid, s);
     if (bn > 128) return gemm_fp8_rows_few(ta, tb, to, p, grid, s);
   }
@@ -276,6 +278,16 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
 extern "C" int mgemm_fwd(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
                          const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
   return fwd_impl(args, dtype, trans_b, x, sx, w, sw, out, M, K, N, E, stream, nullptr, 0, nullptr);
+}
+
+extern "C" int mgemm_fwd_fp8_strided(const void *args, const void *x, const float *sx, const void *w, int64_t ld_wn,
+                                     int64_t ld_we, const float *sw, void *out, int64_t M, int K, int N, int E,
+                                     mgemm_stream_t stream) {
+  if (ld_wn < K || (E > 1 && ld_we < K) || ld_we < 0) return MGEMM_EINVAL;
+  if (ld_wn % 16 || ld_we % 16) return MGEMM_EALIGN;
+  // (with one expert the expert stride is never stepped; any multiple of 16 describes it)
+  return fwd_impl(args, MGEMM_FP8_E4M3, 1, x, sx, w, sw, out, M, K, N, E, stream, nullptr, 0, nullptr, 0, 0, ld_wn,
+                  ld_we > 0 ? ld_we : (int64_t)K);
 }
 
 extern "C" int mgemm_fwd_scatter(const void *args, int dtype, int trans_b, const void *x, const void *w, void *out,

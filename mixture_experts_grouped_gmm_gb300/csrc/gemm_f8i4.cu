@@ -4,37 +4,47 @@
 //
 //   out[r, n] = sum_k (e4m3(x[r, k]) / sx[r]) * q[e, n, k] * 2^(b[e, n, k / 32] - 127)
 //
-// over the rows tile schedule of mgemm_fill_args (tiles of 128 token rows of
-// one non-empty group x BN output columns).  The weights stream from HBM as
-// packed nibbles (half the bytes of FP8), which is what bounds the latency at
-// sparse M; the tensor cores take them as e4m3 (every integer in [-8, 7] is an
-// e4m3 value) in the block-scaled kind::mxf8f6f4 MMA, with the weight blocks'
-// e8m0 bytes as B's scale factors and each token row's power-of-two FP8 scale
-// written as the e8m0 byte 127 - log2(sx[r]) on all of A's blocks of row r,
-// so both scales are applied inside the MMA and the epilogue only rounds.
+// over the rows tile schedule of mgemm_fill_args.  The weights stream from
+// HBM as packed nibbles (half the bytes of FP8), which is what bounds the
+// latency at sparse M; the tensor cores take them as e4m3 (every integer in
+// [-8, 7] is an e4m3 value) in the block-scaled kind::mxf8f6f4 MMA, with the
+// weight blocks' e8m0 bytes as one operand's scale factors and each token
+// row's power-of-two FP8 scale written as the e8m0 byte 127 - log2(sx[r]) on
+// all of the other operand's blocks of row r, so both scales are applied
+// inside the MMA and the epilogue only rounds.
 //
-// CTA (persistent, one per SM, 320 threads):
+// The operands are swapped with respect to mgemm_fwd: a tile is 128 weight
+// rows (output columns n0 .. n0 + 127, the MMA's M side) by the TB token rows
+// of one group (the N side, TB = the token rows rounded up to 16, at most
+// 128), D[n][t] = sum_k w[n, k] x[t, k].  With few token rows per group the
+// MMA then does TB / 128 of the work a 128-token-row tile would, per weight
+// byte, which keeps the tensor cores well below the rate at which the packed
+// weights arrive.
+//
+// CTA (persistent, one per SM, 448 threads):
 //   warp 0      TMA producer: a deep "raw" ring whose slot holds KC
-//               contraction blocks of 128: A rows [KC][a_rows][128 B]
-//               (swizzled), packed B [KC][BN][64 B] and B's scale words
-//               [KC][BN][4 B]; the number of slots is set per launch by the
-//               shared memory left.
-//   warp 1      TMEM owner and MMA issuer (one thread): per tile, copies the A
-//               scale tile into tensor memory; per contraction block, copies
-//               the block's B scale tile and issues four block-scaled MMAs
-//               (K = 32 each, the scale-factor ids selecting byte k of the
-//               scale words); commits free the expanded slot, then the raw
-//               slot (its A rows are read by the MMAs), then publish the
-//               accumulator.
-//   warps 2-5   converters: per tile, the A scale tile (row r's byte
-//               replicated into a word); per contraction block, the packed
-//               nibbles of BN rows expanded to e4m3 bytes in the 128-byte
-//               swizzled K-major layout the MMA reads (a shallow "expanded"
-//               ring), and the B scale tile (row l of the 512-byte tile holds
-//               the words of rows l, l + 32, l + 64, l + 96).
-//   warps 6-9   epilogue: tcgen05.ld of the accumulator (two in TMEM, so the
-//               next tile's main loop overlaps), bf16 rounding, direct stores
-//               of the tile's valid rows.
+//               contraction blocks of 128: token rows [KC][TB][128 B]
+//               (swizzled), packed weights [KC][128][64 B] and their scale
+//               words [KC][128][4 B]; the number of slots is set per launch by
+//               the shared memory left.
+//   warp 1      TMEM owner and MMA issuer (one thread): per raw slot, the
+//               4 KC block-scaled MMAs (K = 32 each; the scale-factor ids
+//               select byte k of the scale words); commits free the expanded
+//               slot and the raw slot (its token rows are read by the MMAs),
+//               and at a tile's end publish the accumulator and free the
+//               tile's token-scale columns.
+//   warps 2-9   converters, one handoff per raw slot: the packed nibbles of
+//               its KC blocks expanded to e4m3 bytes in the 128-byte swizzled
+//               K-major layout the MMA reads (a shallow "expanded" ring of
+//               whole slots); the scale factors go straight into tensor memory
+//               with tcgen05.st by one warp per lane quarter (lane l of every
+//               quarter holds the words of rows l, l + 32, l + 64, l + 96 in
+//               four columns), for the weights per block and for the tokens
+//               once per tile (token row t's byte replicated into a word).
+//   warps 10-13 epilogue: warp w reads the accumulator lanes of quarter w % 4
+//               (weight rows, i.e. output columns), tcgen05.ld of the token
+//               columns, bf16 rounding, stores out[token][column] (a warp's 32
+//               lanes write 64 contiguous bytes of one token row).
 // Every wait is bounded; on expiry the kernel records MGEMM_STATUS_TIMEOUT,
 // drains the copies and MMAs it issued, frees TMEM and returns.
 #include "gemm_launch.cuh"
@@ -42,34 +52,37 @@
 namespace mgemm {
 namespace {
 
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kI4Threads = 64 + 32 * (kConvWarps + kEpiWarps);
 
-template <int kBn, int kKc, int kXs>
+template <int kKc, int kXs>
 struct I4Cfg {
-  static constexpr int BN = kBn;   // output columns per tile (64 or 128)
+  static constexpr int BW = 128;   // weight rows (output columns) per tile: the MMA's M
+  static constexpr int TB_MAX = 128;  // token rows per tile at most: the MMA's N
   static constexpr int KC = kKc;   // contraction blocks of 128 per raw slot
-  static constexpr int XS = kXs;   // expanded slots
+  static constexpr int XS = kXs;   // expanded slots (each holds a raw slot's KC blocks)
   static constexpr int RS_MAX = 16;
-  static constexpr int XB_BYTES = BN * 128;                                // expanded B, one block
-  static constexpr int XB_SLOT = (XB_BYTES + 512 + 1023) / 1024 * 1024;    // + its scale tile
-  static constexpr int TMEM_COLS = 2 * BN + 8 + 4 * XS <= 256 ? 256 : 512;
-  static constexpr int SFA_COL = 2 * BN;       // A scale tiles (one per accumulator), 4 columns each
-  static constexpr int SFB_COL = 2 * BN + 8;   // B scale tiles (one per expanded slot)
-  static_assert(2 * BN + 8 + 4 * XS <= 512, "tensor memory");
+  static constexpr int XB_SLOT = KC * BW * 128;                            // expanded weights of KC blocks
+  static constexpr int SFT_COL = 2 * TB_MAX;   // token scale columns (4 per accumulator)
+  static constexpr int SFW_COL = 2 * TB_MAX + 8;  // weight scale columns (4 per block of each expanded slot)
+  static constexpr int COLS = 2 * TB_MAX + 8 + 4 * KC * XS;
+  static constexpr int TMEM_COLS = COLS <= 256 ? 256 : 512;
+  static_assert(COLS <= 512, "tensor memory");
+  static_assert(XB_SLOT % 1024 == 0, "swizzle atoms");
   static constexpr size_t TAIL = 8 * (2 * RS_MAX + 2 * XS + 8 + 1) + 64;
-  // a raw slot: [A KC x a_rows x 128][B packed KC x BN x 64][B scales KC x BN x 4]
-  static size_t raw_slot_bytes(int a_rows) {
-    return ((size_t)KC * ((size_t)a_rows * 128 + BN * 64 + BN * 4) + 1023) / 1024 * 1024;
+  // a raw slot: [tokens KC x TB x 128][weights packed KC x 128 x 64][weight scales KC x 128 x 4]
+  static size_t raw_slot_bytes(int tb) {
+    return ((size_t)KC * ((size_t)tb * 128 + BW * 64 + BW * 4) + 1023) / 1024 * 1024;
   }
-  static size_t fixed_bytes() { return 1024 /*align*/ + (size_t)XS * XB_SLOT + 1024 /*A scale tiles*/ + TAIL; }
+  static size_t fixed_bytes() { return 1024 /*align*/ + (size_t)XS * XB_SLOT + TAIL; }
 };
 
-// ---- the decode of a tile: the rows schedule of the grouped GEMM (one group
-// per tile; out_rows clipped to the A box's rows)
-template <int kBn, int kKc>
-using I4Decode = GemmCfg<true, false, false, kModeRows, kBn, 24, 1, false, 8, true, kKc, false>;
+// ---- the decode of a tile: the rows schedule of the grouped GEMM, a "row
+// tile" being up to 128 token rows of one group and a "column tile" 128 weight
+// rows; out_rows is clipped to the TB token rows the tile's box holds
+template <int kKc>
+using I4Decode = GemmCfg<true, false, false, kModeRows, 128, 24, 1, false, 8, true, kKc, false>;
 
 // 8 packed nibbles (element 0 in bits 0-3) -> 8 e4m3 bytes.  The low three
 // bits of each nibble select a byte of one of two 8-entry tables (prmt): the
@@ -104,39 +117,32 @@ template <class C>
 __global__ void __launch_bounds__(kI4Threads, 1)
     f8i4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmS, const I4Params P) {
-  using D = I4Decode<C::BN, C::KC>;
+  using D = I4Decode<C::KC>;
   const GemmParams &p = P.g;
+  const int TB = p.a_rows;  // token rows per tile (a multiple of 16)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int RS = P.raw_slots;
   uint8_t *sX = smem;                                     // expanded ring
-  uint8_t *sAT = sX + C::XS * C::XB_SLOT;                 // two A scale tiles
-  uint8_t *sR = sAT + 1024;                               // raw ring
-  auto raw_a = [&](int r, int j) { return sR + (size_t)r * P.raw_slot_bytes + (size_t)j * p.a_rows * 128; };
-  auto raw_b = [&](int r, int j) {
-    return sR + (size_t)r * P.raw_slot_bytes + (size_t)C::KC * p.a_rows * 128 + (size_t)j * C::BN * 64;
-  };
+  uint8_t *sR = sX + C::XS * C::XB_SLOT;                  // raw ring
+  auto raw_t = [&](int r, int j) { return sR + (size_t)r * P.raw_slot_bytes + (size_t)j * TB * 128; };
+  auto raw_w = [&](int r) { return sR + (size_t)r * P.raw_slot_bytes + (size_t)C::KC * TB * 128; };
   auto raw_s = [&](int r, int j) {
-    return sR + (size_t)r * P.raw_slot_bytes + (size_t)C::KC * (p.a_rows * 128 + C::BN * 64) + (size_t)j * C::BN * 4;
+    return sR + (size_t)r * P.raw_slot_bytes + (size_t)C::KC * (TB * 128 + C::BW * 64) + (size_t)j * C::BW * 4;
   };
-  auto xb = [&](int x) { return sX + x * C::XB_SLOT; };
-  auto xb_tile = [&](int x) { return sX + x * C::XB_SLOT + C::XB_BYTES; };
+  auto xb = [&](int x, int j) { return sX + x * C::XB_SLOT + j * C::BW * 128; };
   uint64_t *bars = reinterpret_cast<uint64_t *>(sR + (size_t)RS * P.raw_slot_bytes);
   uint64_t *raw_full = bars, *raw_empty = bars + C::RS_MAX;
   uint64_t *xb_full = raw_empty + C::RS_MAX, *xb_empty = xb_full + C::XS;
-  uint64_t *as_full = xb_empty + C::XS, *as_empty = as_full + 2;
-  uint64_t *tfull = as_empty + 2, *tempty = tfull + 2, *drain = tempty + 2;
+  uint64_t *ts_full = xb_empty + C::XS, *ts_empty = ts_full + 2;
+  uint64_t *tfull = ts_empty + 2, *tempty = tfull + 2, *drain = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait();
-  pdl_trigger();
-  const ArgsView av(p.args, p.E);
-  if (*av.status != 0) return;
-  const int total = total_tiles<D>(p, av);
   const int t_first = (int)blockIdx.x, t_step = (int)gridDim.x;
-  if (t_first >= total) return;
+  // set-up before the wait for the previous grid (it reads nothing that grid
+  // writes); a CTA without tiles runs no role loop
   if (threadIdx.x == 0) {
     for (int r = 0; r < RS; ++r) {
       mbar_init(&raw_full[r], 1);
@@ -147,8 +153,8 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       mbar_init(&xb_empty[x], 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&as_full[a], kConvWarps);
-      mbar_init(&as_empty[a], 1);
+      mbar_init(&ts_full[a], kConvWarps);
+      mbar_init(&ts_empty[a], 1);
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], kEpiWarps);
     }
@@ -167,12 +173,17 @@ __global__ void __launch_bounds__(kI4Threads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+  const ArgsView av(p.args, p.E);
+  const int status0 = *av.status, n_active0 = *av.n_active;
+  const int total = status0 != 0 ? 0 : total_tiles<D>(p, av, n_active0);
   volatile int *vabort = abort_flag;
   uint32_t issued = 0;  // raw slots armed (for the drain after an abort)
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint32_t tx = (uint32_t)C::KC * (uint32_t)(p.a_rows * 128 + C::BN * 64 + C::BN * 4);
+      const uint32_t tx = (uint32_t)C::KC * (uint32_t)(TB * 128 + C::BW * 64 + C::BW * 4);
       int r = 0;
       uint32_t ph = 0;
       for (int j = 0; j * t_step < total && !*vabort; ++j) {
@@ -187,10 +198,10 @@ __global__ void __launch_bounds__(kI4Threads, 1)
           }
           mbar_arrive_expect_tx(&raw_full[r], tx);
           ++issued;
-          // weights first (the long pole), then the scales and the token rows
-          tma_load_4d(raw_b(r, 0), &tmB, &raw_full[r], 0, ti.b_row, g * C::KC, ti.e);
-          tma_load_4d(raw_s(r, 0), &tmS, &raw_full[r], 0, ti.b_row / 4, g * C::KC, ti.e);
-          tma_load_3d(raw_a(r, 0), &tmA, &raw_full[r], 0, ti.a_row, g * C::KC);
+          // weights first (the long pole), then their scales and the token rows
+          tma_load_4d(raw_w(r), &tmB, &raw_full[r], 0, ti.n0, g * C::KC, ti.e);
+          tma_load_4d(raw_s(r, 0), &tmS, &raw_full[r], 0, ti.n0 / 4, g * C::KC, ti.e);
+          tma_load_3d(raw_t(r, 0), &tmA, &raw_full[r], 0, ti.a_row, g * C::KC);
           if (++r == RS) {
             r = 0;
             ph ^= 1;
@@ -206,52 +217,49 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       const int t = tile_of<D>(j, t_first, t_step);
       if (t >= total) continue;
       const TileInfo ti = decode_tile<D>(t, p, av, 0u);
-      if (!mbar_wait_warp(&tempty[acc], aph ^ 1, vabort) || !mbar_wait_warp(&as_full[acc], aph, vabort)) {
+      if (!mbar_wait_warp(&tempty[acc], aph ^ 1, vabort) || !mbar_wait_warp(&ts_full[acc], aph, vabort)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * C::BN;
-      const uint32_t sfa = tmem_base + C::SFA_COL + 4 * acc;
-      if (lane == 0) {
-        tmem_cp_32x128b_warpx4(sfa, smem_desc_rows16(smem_u32(sAT + acc * 512)));
-        mma_commit(&as_empty[acc]);
-      }
-      __syncwarp();
-      for (int g = 0; g < ti.kb_count && ok; ++g) {
-        if (!mbar_wait_warp(&raw_full[r], rph, vabort)) { ok = false; break; }
-        for (int jj = 0; jj < C::KC; ++jj) {
-          if (!mbar_wait_warp(&xb_full[x], xph, vabort)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sfb = tmem_base + C::SFB_COL + 4 * x;
-            tmem_cp_32x128b_warpx4(sfb, smem_desc_rows16(smem_u32(xb_tile(x))));
-            const uint32_t abase = smem_u32(raw_a(r, jj)), bbase = smem_u32(xb(x));
+      const uint32_t d_tmem = tmem_base + acc * C::TB_MAX;
+      const uint32_t sft = tmem_base + C::SFT_COL + 4 * acc;
+      for (int g = 0; g < ti.kb_count; ++g) {
+        if (!mbar_wait_warp(&raw_full[r], rph, vabort) || !mbar_wait_warp(&xb_full[x], xph, vabort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int jj = 0; jj < C::KC; ++jj) {
+            const uint32_t sfw = tmem_base + C::SFW_COL + 4 * (x * C::KC + jj);
+            const uint32_t wbase = smem_u32(xb(x, jj)), tbase = smem_u32(raw_t(r, jj));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc_sw128(abase + k * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(bbase + k * 32, 16, 1024);
+              const uint64_t ad = smem_desc_sw128(wbase + k * 32, 16, 1024);   // weights: M side
+              const uint64_t bd = smem_desc_sw128(tbase + k * 32, 16, 1024);   // tokens: N side
               const uint32_t idk = p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-              mma_mx(d_tmem, ad, bd, idk, sfa, sfb, (g | jj | k) != 0);
+              mma_mx(d_tmem, ad, bd, idk, sfw, sft, (g | jj | k) != 0);
             }
-            mma_commit(&xb_empty[x]);
           }
-          __syncwarp();
-          if (++x == C::XS) {
-            x = 0;
-            xph ^= 1;
-          }
+          mma_commit(&xb_empty[x]);
+          mma_commit(&raw_empty[r]);  // the slot's token rows are read
         }
-        if (!ok) break;
-        if (lane == 0) mma_commit(&raw_empty[r]);  // the slot's A rows are read
         __syncwarp();
+        if (++x == C::XS) {
+          x = 0;
+          xph ^= 1;
+        }
         if (++r == RS) {
           r = 0;
           rph ^= 1;
         }
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(&tfull[acc]);
+      if (lane == 0) {
+        mma_commit(&tfull[acc]);
+        mma_commit(&ts_empty[acc]);  // the tile's token-scale columns are read
+      }
       __syncwarp();
       if (++acc == 2) {
         acc = 0;
@@ -262,13 +270,16 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       if (lane == 0) set_status(av.status, MGEMM_STATUS_TIMEOUT);
       *vabort = 1;
     }
-    if (lane == 0) {  // every MMA and copy this thread issued has completed before TMEM is freed
+    if (lane == 0) {  // every MMA this thread issued has completed before TMEM is freed
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
     }
     __syncwarp();
   } else if (warp < 2 + kConvWarps) {
-    const int c = threadIdx.x - 64;  // 0 .. 127
+    constexpr int NT = 32 * kConvWarps;
+    const int c = threadIdx.x - 64;                 // 0 .. NT - 1
+    const bool sf_writer = warp < 2 + 4;            // one warp per TMEM lane quarter writes the scales
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int r = 0, x = 0, acc = 0;
     uint32_t rph = 0, xph = 0, aph = 0;
     bool ok = true;
@@ -276,54 +287,68 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       const int t = tile_of<D>(j, t_first, t_step);
       if (t >= total) continue;
       const TileInfo ti = decode_tile<D>(t, p, av, 0u);
-      // A scale tile of this tile: word of token row i = its byte 127 - log2(sx)
+      // token scales of this tile: token row i's word is its byte 127 - log2(sx)
       // (254 minus the biased exponent of the power of two sx) in all four
       // sub-blocks; rows past the tile's rows get the unit byte
-      if (!mbar_wait_warp(&as_empty[acc], aph ^ 1, vabort)) { ok = false; break; }
-      {
-        const int i = c;  // token row i of the tile: row l = i % 32, word i / 32 of the tile row
-        uint32_t wv = 0x7F7F7F7Fu;
-        if (i < ti.out_rows) {
-          const uint32_t b = 254u - (__float_as_uint(__ldg(p.rscale + ti.out_row0 + i)) >> 23);
-          wv = b * 0x01010101u;
+      if (!mbar_wait_warp(&ts_empty[acc], aph ^ 1, vabort)) { ok = false; break; }
+      if (sf_writer) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int i = lane + 32 * m;
+          wv[m] = 0x7F7F7F7Fu;
+          if (i < ti.out_rows)
+            wv[m] = (254u - (__float_as_uint(__ldg(p.rscale + ti.out_row0 + i)) >> 23)) * 0x01010101u;
         }
-        reinterpret_cast<uint32_t *>(sAT + acc * 512)[(i & 31) * 4 + (i >> 5)] = wv;
+        tmem_st_32x32b_x4(tmem_base + lane_base + C::SFT_COL + 4 * acc, wv);
+        tmem_st_wait();
       }
-      fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&as_full[acc]);
-      for (int g = 0; g < ti.kb_count && ok; ++g) {
-        if (!mbar_wait_warp(&raw_full[r], rph, vabort)) { ok = false; break; }
-        for (int jj = 0; jj < C::KC; ++jj) {
-          if (!mbar_wait_warp(&xb_empty[x], xph ^ 1, vabort)) { ok = false; break; }
-          const uint8_t *src = raw_b(r, jj);
-          uint8_t *dst = xb(x);
-#pragma unroll 2
-          for (int idx = c; idx < C::BN * 8; idx += 32 * kConvWarps) {
-            const int n = idx >> 3, ch = idx & 7;  // output chunk ch (16 elements) of row n
-            const uint2 v = *reinterpret_cast<const uint2 *>(src + n * 64 + ch * 8);
-            const uint2 lo = int4x8_to_e4m3(v.x), hi = int4x8_to_e4m3(v.y);
-            *reinterpret_cast<uint4 *>(dst + n * 128 + ((ch ^ (n & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-          }
-          if (c < 32) {  // B scale tile: row l holds the words of rows l, l + 32, l + 64, l + 96
+      if (lane == 0) mbar_arrive(&ts_full[acc]);
+      for (int g = 0; g < ti.kb_count; ++g) {
+        if (!mbar_wait_warp(&raw_full[r], rph, vabort) || !mbar_wait_warp(&xb_empty[x], xph ^ 1, vabort)) {
+          ok = false;
+          break;
+        }
+        // expand: output chunk ch (16 elements) of weight row n of block jj
+        const uint8_t *src = raw_w(r);
+        uint8_t *dst = xb(x, 0);
+        constexpr int kChunks = C::KC * C::BW * 8;
+        static_assert(kChunks % NT == 0, "whole rounds");
+#pragma unroll
+        for (int it = 0; it < kChunks / NT; ++it) {
+          const int idx = c + it * NT;
+          const int jj = idx / (C::BW * 8), rem = idx % (C::BW * 8);
+          const int n = rem >> 3, ch = rem & 7;
+          const uint2 v = *reinterpret_cast<const uint2 *>(src + (jj * C::BW + n) * 64 + ch * 8);
+          const uint2 lo = int4x8_to_e4m3(v.x), hi = int4x8_to_e4m3(v.y);
+          *reinterpret_cast<uint4 *>(dst + (jj * C::BW + n) * 128 + ((ch ^ (n & 7)) << 4)) =
+              make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
+        if (sf_writer) {  // weight scales of the slot's blocks: lane l holds rows l, l + 32, l + 64, l + 96
+#pragma unroll
+          for (int jj = 0; jj < C::KC; ++jj) {
             const uint32_t *sw = reinterpret_cast<const uint32_t *>(raw_s(r, jj));
-            const uint4 tv = make_uint4(sw[c], C::BN > 32 ? sw[c + 32] : 0u, C::BN > 64 ? sw[c + 64] : 0u,
-                                        C::BN > 96 ? sw[c + 96] : 0u);
-            reinterpret_cast<uint4 *>(xb_tile(x))[c] = tv;
+            const uint32_t wv[4] = {sw[lane], sw[lane + 32], sw[lane + 64], sw[lane + 96]};
+            tmem_st_32x32b_x4(tmem_base + lane_base + C::SFW_COL + 4 * (x * C::KC + jj), wv);
           }
-          fence_proxy_async_smem();  // generic writes -> tensor-core reads
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&xb_full[x]);
-          if (++x == C::XS) {
-            x = 0;
-            xph ^= 1;
-          }
+          tmem_st_wait();
+        }
+        fence_proxy_async_smem();  // generic writes -> tensor-core reads
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xb_full[x]);
+        if (++x == C::XS) {
+          x = 0;
+          xph ^= 1;
         }
         if (++r == RS) {
           r = 0;
           rph ^= 1;
         }
       }
+      if (!ok) break;
       if (++acc == 2) {
         acc = 0;
         aph ^= 1;
@@ -334,9 +359,9 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       *vabort = 1;
     }
   } else {
-    // epilogue: warp w reads TMEM lane quarter w % 4 (tile rows 32 q ..)
+    // epilogue: warp w reads accumulator lanes of quarter q = w % 4, i.e. output
+    // columns n0 + 32 q + lane, and the token columns 0 .. TB - 1
     const int q = warp & 3;
-    const int rr = q * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
     for (int j = 0; j * t_step < total; ++j) {
@@ -349,28 +374,23 @@ __global__ void __launch_bounds__(kI4Threads, 1)
         break;
       }
       tc_fence_after();
-      const bool row_ok = rr < ti.out_rows;
-      __nv_bfloat16 *orow = p.out + ((int64_t)ti.out_row0 + (row_ok ? rr : 0)) * p.Nout;
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::BN;
-#pragma unroll
-      for (int cc = 0; cc < C::BN / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + cc * 32, v);
+      const int col = ti.n0 + q * 32 + lane;
+      const bool col_ok = col < p.Nout;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::TB_MAX;
+      for (int c0 = 0; c0 < TB; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(taddr + c0, v);
         tmem_ld_wait();
-        if (cc == C::BN / 32 - 1) {  // the accumulator is read: hand it back
+        if (c0 + 16 >= TB) {  // the accumulator is read: hand it back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[acc]);
         }
-        const int col0 = ti.n0 + cc * 32;
-        if (row_ok && col0 < p.Nout) {
-          uint32_t pk[16];
+        if (col_ok) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + col0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (col0 + 8 * i < p.Nout) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 16; ++i)
+            if (c0 + i < ti.out_rows)
+              p.out[((int64_t)ti.out_row0 + c0 + i) * p.Nout + col] = __float2bfloat16_rn(__uint_as_float(v[i]));
         }
       }
       if (++acc == 2) {
@@ -403,7 +423,7 @@ int launch_f8i4(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &s
   const size_t room = (size_t)227 * 1024 - C::fixed_bytes();
   int rs = (int)(room / slot);
   if (rs > C::RS_MAX) rs = C::RS_MAX;
-  if (rs < 2 || P.g.a_rows % 8) return MGEMM_EINVAL;
+  if (rs < 2 || P.g.a_rows % 16) return MGEMM_EINVAL;
   P.raw_slots = rs;
   P.raw_slot_bytes = (int)slot;
   const size_t smem = C::fixed_bytes() + (size_t)rs * slot;
@@ -444,38 +464,38 @@ extern "C" int mgemm_fwd_f8i4(const void *args, const uint8_t *x, const float *s
   if (rc) return rc;
   const int sms = sm_count_cached();
   if (sms <= 0) return MGEMM_ECUDA;
-  // 64-column tiles while the weights stream (few rows per group), 128 beyond
+  // tiles of 128 weight rows (output columns) by TB token rows of one group:
+  // TB = the token rows rounded up to 16 (the MMA's N), at most 128
   const int64_t groups = M < E ? M : E;
-  const bool narrow = M / groups < 128;
-  const int bn = narrow ? 64 : 128, kc = narrow ? 4 : 2;
-  const uint32_t a_rows = M < 128 ? (uint32_t)((M + 7) / 8 * 8) : 128u;
-  CUtensorMap ta, tb, ts;
-  {  // x [M, K] e4m3 as 128-byte k-chunks: {128, M, K / 128}, boxes of kc chunks of a_rows rows
+  const uint32_t tb = M < 128 ? (uint32_t)((M + 15) / 16 * 16) : 128u;
+  const int kc = 2;
+  CUtensorMap ta, tb_map, ts;
+  {  // x [M, K] e4m3 as 128-byte k-chunks: {128, M, K / 128}, boxes of kc chunks of tb rows
     const uint64_t d[3] = {128, (uint64_t)M, (uint64_t)K / 128};
     const uint64_t st[2] = {(uint64_t)K, 128};
-    const uint32_t box[3] = {128, a_rows, (uint32_t)kc};
+    const uint32_t box[3] = {128, tb, (uint32_t)kc};
     if (!make_tensor_map(&ta, true, 3, x, d, st, box)) return MGEMM_ECUDA;
   }
   {  // packed w [E, N, K / 2] as 64-byte k-chunks: {64, N, K / 128, E}, unswizzled
     const uint64_t d[4] = {64, (uint64_t)N, (uint64_t)K / 128, (uint64_t)E};
     const uint64_t st[3] = {(uint64_t)K / 2, 64, (uint64_t)N * K / 2};
-    const uint32_t box[4] = {64, (uint32_t)bn, (uint32_t)kc, 1};
-    if (!make_tensor_map(&tb, true, 4, w_packed, d, st, box, false)) return MGEMM_ECUDA;
+    const uint32_t box[4] = {64, 128, (uint32_t)kc, 1};
+    if (!make_tensor_map(&tb_map, true, 4, w_packed, d, st, box, false)) return MGEMM_ECUDA;
   }
   {  // scales [E][K / 128][N][4 B] as 16-byte rows of four: {16, N / 4, K / 128, E}
     const uint64_t d[4] = {16, (uint64_t)N / 4, (uint64_t)K / 128, (uint64_t)E};
     const uint64_t st[3] = {16, (uint64_t)N * 4, (uint64_t)K / 128 * N * 4};
-    const uint32_t box[4] = {16, (uint32_t)bn / 4, (uint32_t)kc, 1};
+    const uint32_t box[4] = {16, 32, (uint32_t)kc, 1};
     if (!make_tensor_map(&ts, true, 4, w_scales, d, st, box, false)) return MGEMM_ECUDA;
   }
   I4Params P{};
   GemmParams &p = P.g;
   p.args = (const uint8_t *)args;
   p.E = E;
-  p.bn = bn;
-  p.a_rows = (int)a_rows;
-  p.idesc = make_idesc_mx(128, bn, 1);  // ue8m0 scale factors
-  p.n_tiles = (N + bn - 1) / bn;
+  p.bn = 128;
+  p.a_rows = (int)tb;
+  p.idesc = make_idesc_mx(128, (int)tb, 1);  // M = 128 weight rows, N = tb token rows, ue8m0 scale factors
+  p.n_tiles = (N + 127) / 128;
   p.Kc = K;
   p.Nout = N;
   p.out = (__nv_bfloat16 *)out;
@@ -483,6 +503,5 @@ extern "C" int mgemm_fwd_f8i4(const void *args, const uint8_t *x, const float *s
   const int64_t upper = ((M + 127) / 128 + groups) * p.n_tiles;
   const int grid = (int)(upper < sms ? upper : sms);
   cudaStream_t s = (cudaStream_t)stream;
-  if (narrow) return launch_f8i4<I4Cfg<64, 4, 4>>(ta, tb, ts, P, grid, s);
-  return launch_f8i4<I4Cfg<128, 2, 3>>(ta, tb, ts, P, grid, s);
+  return launch_f8i4<I4Cfg<2, 2>>(ta, tb_map, ts, P, grid, s);
 }

@@ -24,45 +24,6 @@
 
 namespace mgemm {
 
-__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
-
-__device__ __forceinline__ float amax8(const uint4 &v, float a) {
-  a = fmaxf(a, fabsf(bf16_lo(v.x)));
-  a = fmaxf(a, fabsf(bf16_hi(v.x)));
-  a = fmaxf(a, fabsf(bf16_lo(v.y)));
-  a = fmaxf(a, fabsf(bf16_hi(v.y)));
-  a = fmaxf(a, fabsf(bf16_lo(v.z)));
-  a = fmaxf(a, fabsf(bf16_hi(v.z)));
-  a = fmaxf(a, fabsf(bf16_lo(v.w)));
-  a = fmaxf(a, fabsf(bf16_hi(v.w)));
-  return a;
-}
-
-// 8 bf16 -> 8 e4m3 bytes (x * s is exact: s is a power of two)
-__device__ __forceinline__ uint2 cast8(const uint4 &v, float s) {
-  uint2 o;
-  o.x = (uint32_t)cvt_e4m3x2(bf16_lo(v.x) * s, bf16_hi(v.x) * s) |
-        ((uint32_t)cvt_e4m3x2(bf16_lo(v.y) * s, bf16_hi(v.y) * s) << 16);
-  o.y = (uint32_t)cvt_e4m3x2(bf16_lo(v.z) * s, bf16_hi(v.z) * s) |
-        ((uint32_t)cvt_e4m3x2(bf16_lo(v.w) * s, bf16_hi(v.w) * s) << 16);
-  return o;
-}
-
-__device__ __forceinline__ float warp_max(float a) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  return a;
-}
-
-__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // ------------------------------------------------------------------ rowwise
 // NCH = chunks of 8 elements per lane kept in registers (row length <= NCH*256);
 // NCH = 0 selects the two-pass loop for any length.
@@ -97,12 +58,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const __nv_bfloat16 
         if (c < C) *reinterpret_cast<uint2 *>(dst + c) = cast8(v[j], s);
       }
     } else {
-      for (int64_t c = (int64_t)lane * 8; c < C; c += 256) a = amax8(ldg_nc_v4(src + c), a);
-      a = warp_max(a);
-      const float s = pow2_scale_from_amax(a);
-      if (lane == 0) scales[row] = s;
-      for (int64_t c = (int64_t)lane * 8; c < C; c += 256)
-        *reinterpret_cast<uint2 *>(dst + c) = cast8(*reinterpret_cast<const uint4 *>(src + c), s);
+      quant_row_two_pass(src, C, dst, scales + row, lane);
     }
   }
 }

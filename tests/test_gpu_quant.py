@@ -179,3 +179,38 @@ def test_colwise_repeated_on_one_args_block(sizes):
         q, r = quant_colwise_grouped(to_np(a), offs)
         assert np.array_equal(unpad_colwise(to_np(o), 136, ld, sizes), q) and np.array_equal(to_np(s), r)
         assert int(args[12:16].view(torch.int32).item()) == 0
+
+
+@pytest.mark.parametrize("sizes,K", [([0, 1, 0, 0], 5120), ([3, 0, 2] + [0] * 125, 5120), ([40, 0, 88], 2048),
+                                     ([7] * 300, 272), ([0, 0], 128)])
+def test_fill_args_quant_rowwise_fused_equals_the_two_calls(sizes, K):
+    # one launch: the args block equals mgemm_fill_args' byte for byte, the codes
+    # and scales equal mgemm_quant_rowwise's and the oracle's
+    from oracle import quant as oq
+
+    E, M = len(sizes), int(np.sum(sizes))
+    gs = torch.tensor(sizes, dtype=torch.int64, device=DEV)
+    x = (torch.randn(max(M, 1), K, device=DEV) * 3.0).to(torch.bfloat16)[:M]
+    a1 = torch.zeros(B().mgemm_args_bytes(E), dtype=torch.uint8, device=DEV)
+    a2 = torch.full_like(a1, 0xA5)
+    q1 = torch.empty(M, K, dtype=torch.uint8, device=DEV)
+    s1 = torch.empty(M, dtype=torch.float32, device=DEV)
+    q2, s2 = torch.empty_like(q1), torch.empty_like(s1)
+    B().mgemm_fill_args(gs, E, M, a1)
+    if M:
+        B().mgemm_quant_rowwise(x, q1, s1)
+    B().mgemm_fill_args_quant_rowwise(gs, E, M, a2, x, q2, s2)
+    torch.cuda.synchronize()
+    from tests.helpers import parse_args
+
+    p1, p2 = parse_args(a1, E), parse_args(a2, E)
+    na = p1["n_active"]
+    for k in ("active",):                      # defined for the n_active non-empty groups
+        p1[k], p2[k] = p1[k][:na], p2[k][:na]
+    for k in ("mtile_start", "ptile_start"):   # and their prefix ends
+        p1[k], p2[k] = p1[k][:na + 1], p2[k][:na + 1]
+    assert p1 == p2
+    assert torch.equal(q1, q2) and torch.equal(s1, s2)
+    if M:
+        qr, sr = oq.quant_rowwise(to_np(x))
+        assert np.array_equal(to_np(q2), qr) and np.array_equal(to_np(s2), sr)
