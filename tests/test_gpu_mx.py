@@ -106,6 +106,8 @@ def assert_mx_close(got, ref, what=""):
     ([1, 2, 3, 250, 0, 129], 1408, 200),       # K % 512 != 0; a partial last column tile
     ([0, 0, 70], 2048, 1408),
     ([33] * 12, 640, 136),
+    ([300, 0, 700, 260], 512, 400),            # groups averaging >= 256 rows: CTA pairs, partial pair tiles
+    ([1024], 384, 192),                        # E = 1 on CTA pairs, one column tile
 ])
 def test_fwd_mx_parity(sizes, K, N):
     got, ref = gemm_case(sizes, K, N, seed=len(sizes) * 100 + K + N)
