@@ -63,6 +63,9 @@ _SIGS = {
                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_void_p]),
+    "mgemm_fwd_fp8_sparse": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "mgemm_quant_int4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "mgemm_fwd_f8i4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -224,6 +227,19 @@ def mgemm_fwd_fp8_strided(args, x, sx, w, ld_wn, ld_we, sw, out, M, K, N, E):
     _cuda(args, x, sx, w, sw, out)
     _check(lib().mgemm_fwd_fp8_strided(_p(args), _p(x), _p(sx), _p(w), int(ld_wn), int(ld_we), _p(sw), _p(out), int(M),
                                        int(K), int(N), int(E), _stream(out)), "mgemm_fwd_fp8_strided")
+
+
+SPARSE_MAX_ROWS = 16
+
+
+def mgemm_fwd_fp8_sparse(group_sizes, E, x, w, sw, out, status):
+    """fill + rowwise cast of x + FP8 forward in one launch, for at most 16 token rows.
+    x bf16 [M, K]; w e4m3 [E, N, K] (uint8); sw fp32 [E * N]; out bf16 [M, N]; status int32 [1]."""
+    _cuda(group_sizes, x, w, sw, out, status)
+    M, K = x.shape
+    N = out.shape[1]
+    _check(lib().mgemm_fwd_fp8_sparse(_p(group_sizes), int(E), _p(x), x.stride(0), _p(w), _p(sw), _p(out), _p(status),
+                                      int(M), int(K), int(N), _stream(out)), "mgemm_fwd_fp8_sparse")
 
 
 def int4_scale_bytes(E, N, K):

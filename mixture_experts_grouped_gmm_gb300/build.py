@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libmgemm.so")
 
-SOURCES = ["args.cu", "quant.cu", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_api.cu", "gemm_f8i4.cu", "noalloc.cu",
+SOURCES = ["args.cu", "quant.cu", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_api.cu", "gemm_f8i4.cu", "gemm_sparse.cu",
+           "noalloc.cu",
            "routing.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I" + INCLUDE]
