@@ -333,12 +333,15 @@ int mgemm_fill_args_quant_rowwise(const int64_t *group_sizes, int E, int64_t M, 
  * mgemm_fwd_fp8_sparse -- the FP8 forward for few token rows in one launch:
  * mgemm_fill_args + mgemm_quant_rowwise of x + mgemm_fwd (MGEMM_FP8_E4M3,
  * w [E, N, K]) ("F8I4 Grouped Gemm Optimization for Sparse M", Summary:
- * tiles only for the min(total_M, groups) non-empty groups; "[moe training]
+ * work only for the min(total_M, groups) non-empty groups; "[moe training]
  * Optimize FP8 MoE backward pass" commit message: the fused rowwise scale +
- * cast).  Every CTA scans the group sizes itself, casts its group's token rows
- * (the rowwise rule: power-of-two scale from the row's magnitude maximum,
- * saturating e4m3) into shared memory, and runs the GEMM; the output equals
- * that of the three calls bit for bit.
+ * cast).  Every CTA scans the group sizes itself, casts the token rows it
+ * needs (the rowwise rule: power-of-two scale from the row's magnitude
+ * maximum, saturating e4m3) into shared memory and streams its share of the
+ * touched experts' weights.  When the tiles of 128 output columns cover at
+ * most half of the SMs (one token), pairs of CTAs split each tile's
+ * contraction in two halves and add the second half's fp32 partial sums to
+ * the first's; otherwise every output equals mgemm_fwd's bit for bit.
  *   group_sizes int64[E], device, summing to M
  *   x        bf16 [M, K] token rows sorted by expert, row stride ld_x elements
  *   w, sw    e4m3 [E, N, K] and fp32 [E * N] (as for mgemm_fwd)
@@ -347,12 +350,14 @@ int mgemm_fill_args_quant_rowwise(const int64_t *group_sizes, int E, int64_t M, 
  *            MGEMM_STATUS_SUM_MISMATCH (then nothing else is written) or
  *            MGEMM_STATUS_TIMEOUT
  * 1 <= M <= 16, E <= 1024, K % 128 == 0, N % 8 == 0, ld_x % 8 == 0, and the
- * token rows must fit on chip: ceil(M / 8) * 8 * K <= 160 KiB (else -1; use
+ * token rows must fit on chip: ceil(M / 8) * 8 * K <= 150 KiB (else -1; use
  * the three calls).  Errors: -1 (sizes or NULL), -2 (alignment), -3 (E),
  * -4 (CUDA).
  */
 int mgemm_fwd_fp8_sparse(const int64_t *group_sizes, int E, const void *x, int64_t ld_x, const void *w,
                          const float *sw, void *out, int *status, int64_t M, int K, int N, mgemm_stream_t stream);
+
+
 
 /*
  * mgemm_quant_int4 -- the INT4 weights of the FP8 x INT4 grouped GEMM.

@@ -7,27 +7,46 @@
 // mgemm_fwd (dtype MGEMM_FP8_E4M3, w [E, N, K]) compute, for at most 16 token
 // rows, where those three launches cost more than the weights' stream.
 //
-// CTA (persistent, one per SM, 320 threads), each on a contiguous range of
-// tiles; a tile is one non-empty group (every group has fewer than 128 rows,
-// so one row tile) x 64 weight rows, and consecutive tiles share their group,
-// so a CTA casts a group's rows once for the whole run of its tiles:
-//   all         scan of the E group sizes in shared memory (every CTA: the
-//               active groups, their first rows and sizes; validation)
-//   warp 0      TMA producer: the weights only, KC = 4 contraction blocks of
-//               64 rows x 128 B per stage, as many stages as fit; it starts as
-//               soon as the scan is done (the weights do not depend on x)
-//   warp 1      TMEM owner and MMA issuer: kind::f8f6f4, M = 128 (the token
-//               rows of the group, the rest unused), N = 64, K = 32
-//   warps 2-9   per tile: on a change of group, the group's token rows cast
-//               to e4m3 with their power-of-two scale by all 256 threads: the
-//               rows' 16-byte units are loaded and their magnitude maxima
-//               reduced while the MMAs of the tile before still run, and the
-//               codes are written once those MMAs are done, straight into a
-//               resident A region laid out as the MMA reads it (K / 128 chunks
-//               of a_rows x 128 B, 128-byte swizzle); then the previous tile's
-//               epilogue: TMEM -> registers, times
-//               1 / sx[row] and 1 / sw[e, column] (the same packed-multiply
-//               order as mgemm_fwd's FP8 epilogue), bf16, direct stores.
+// Orientation: a tcgen05.mma costs about the same time for every shape up to
+// M = 128, N = 128 (K = 32 for e4m3), so the weights take the MMA's 128-row
+// side (4 KB of weights per instruction) and the few token rows its N side
+// (N = 16).  With the tokens on the 128-row side, as in mgemm_fwd, an
+// instruction consumes only N x 32 bytes of weights and the tensor pipe, not
+// HBM, bounds the stream.
+//
+// Work split: a tile is one non-empty group x 128 weight rows (output
+// columns) x all of K, cut into stages of KC contraction blocks.  The CTAs
+// (persistent, one per SM) take equal contiguous ranges of tiles, and
+// consecutive tiles mostly share their group, so a CTA writes a group's token
+// codes once for the whole run of them.  When there are at most half as many
+// tiles as SMs (one token: one expert's 64 tiles), CTA pairs (clusters of two)
+// take the tiles instead, each CTA one half of the contraction, so that every
+// SM streams weights: the second CTA hands its fp32 partial sums to the
+// first through the first's shared memory, and the first adds them to its own
+// before the epilogue.  Without pairs every output equals mgemm_fwd's bit for
+// bit; with them it differs by the rounding of that one addition.
+//
+// CTA roles (320 threads):
+//   all         at launch, the token rows are read and their magnitude maxima
+//               reduced (all rows when they fit one register batch, else the
+//               first group's) while every CTA scans the E group sizes in
+//               shared memory (the active groups, their first rows and sizes;
+//               validation)
+//   warp 0      TMA producer: the weights only, KC contraction blocks of
+//               128 rows x 128 B per stage, as many stages as fit; its first
+//               copy waits until the first group's token loads are out
+//   warp 1      TMEM owner; one thread issues the MMAs: kind::f8f6f4, M = 128
+//               (weight rows), N = 16 (token rows), K = 32; two accumulators
+//   warps 2-9   at a change of group, the group's token rows cast to e4m3 with
+//               their power-of-two scale into a resident B region laid out as
+//               the MMA reads it (K / 128 chunks of a_rows x 128 B, 128-byte
+//               swizzle), once the MMAs before are done; the next group's row
+//               maxima are read while the current tile's MMAs run
+//   warps 4-7   the previous tile's epilogue, one TMEM lane quarter each:
+//               lane = output column, TMEM column = token row; in a pair's
+//               second CTA, the partial sums into the first's shared memory;
+//               else (the partner's partial added first) times 1 / sx[row] and
+//               1 / sw[e, column] in mgemm_fwd's order, bf16, direct stores.
 // Every wait is bounded; on expiry the kernel records MGEMM_STATUS_TIMEOUT in
 // *status, drains the copies and MMAs it issued, frees TMEM and returns.
 #include "gemm_launch.cuh"
@@ -35,22 +54,23 @@
 namespace mgemm {
 namespace {
 
-constexpr int kSpBn = 64;        // weight rows (output columns) per tile
-constexpr int kSpKc = 4;         // contraction blocks of 128 per stage
+constexpr int kSpBw = 128;       // weight rows (output columns) per tile: the MMA's M
+constexpr int kSpTn = 16;        // the MMA's N: token rows (a group has at most 16)
 constexpr int kSpMaxRows = 16;   // token rows of the whole call at most
 constexpr int kSpThreads = 320;
-constexpr int kSpStageBytes = kSpKc * kSpBn * 128;
+constexpr int kSpChunkBytes = kSpBw * 128;  // one contraction block of 128 weight rows
 constexpr int kSpMaxStages = 12;
-constexpr int kSpKeep = 8;       // 16-byte units per cast thread held in registers between the two passes
+constexpr int kSpKeep = 8;       // 16-byte units per cast thread held in registers
+constexpr int kSpRecvBytes = kSpBw * kSpTn * 4;  // a pair's partial sums: 128 rows x 16 fp32
 
 struct SpParams {
   const int64_t *sizes;
   int E;
   int M;
   int K, N;
-  int a_rows;     // token rows rounded up to 8 (the A region's rows)
+  int a_rows;     // token rows rounded up to 8 (the B region's rows per chunk)
   int stages;
-  int n_tiles;    // ceil(N / 64)
+  int n_tiles;    // ceil(N / 128)
   const __nv_bfloat16 *x;
   int64_t ld_x;
   const float *sw;
@@ -65,10 +85,9 @@ struct SpShared {
   long long warp_tot[kSpThreads / 32];
   int warp_cnt[kSpThreads / 32];
   unsigned amax_bits[kSpMaxRows];  // magnitude maximum of every token row (bits of a float >= 0)
-  float rinv[kSpMaxRows];          // row-scale reciprocal of every token row (a row's value never changes)
-  float cinv[3][kSpBn];   // column-scale reciprocals of the last three tiles (a tile's epilogue runs
-                          // while the next tile's are written, and before the one after it starts)
-  uint64_t full[kSpMaxStages], empty[kSpMaxStages], a_full, a_empty, tfull[2], tempty[2], drain;
+  float rinv[kSpMaxRows];          // row-scale reciprocal of every token row
+  uint64_t full[kSpMaxStages], empty[kSpMaxStages], a_full, a_empty, tfull[2], tempty[2], drain, x_go;
+  uint64_t part_full, part_empty;  // pairs: the partner's partial is in recv / recv may be rewritten
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -85,16 +104,60 @@ __device__ __forceinline__ bool bar1_256_or(bool v) {
   return r != 0;
 }
 
+__device__ __forceinline__ void bar1_256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// mbar_wait_warp with acquire at cluster scope: the arrivals come from the
+// other CTA of the pair (released at cluster scope) and order its writes
+// into this CTA's shared memory before the reads that follow.
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity, const volatile int *abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  auto test = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  bool ok = test();
+  if (!ok) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (test()) {
+        ok = true;
+        break;
+      }
+      if ((i & 255u) == 0 && ((abort_flag && *abort_flag) || global_timer_ns() - t0 > kWaitLimitNs)) break;
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
+// KC: contraction blocks of 128 per stage (a stage is KC x 16 KB of weights);
+// PAIR: clusters of two CTAs, each one half of the contraction of every tile.
+template <int KC, bool PAIR>
 __global__ void __launch_bounds__(kSpThreads, 1)
-    sparse_fp8_kernel(const __grid_constant__ CUtensorMap tmB, const SpParams p) {
+    sparse_fp8_kernel(const __grid_constant__ CUtensorMap tmW, const SpParams p) {
+  constexpr int kStageBytes = KC * kSpChunkBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int kchunks = p.K / 128;
-  uint8_t *sA = smem;                                                  // [kchunks][a_rows][128 B]
-  uint8_t *sB = sA + (size_t)kchunks * p.a_rows * 128;                 // ring of weight stages
-  SpShared &S = *reinterpret_cast<SpShared *>(sB + (size_t)p.stages * kSpStageBytes);
+  uint8_t *sT = smem;                                                  // token codes [kchunks][a_rows][128 B]
+  uint8_t *sW = sT + (size_t)kchunks * p.a_rows * 128;                 // ring of weight stages
+  SpShared &S = *reinterpret_cast<SpShared *>(sW + (size_t)p.stages * kStageBytes);
+  // pairs: the partner's partial sums, [128 rows][16] fp32 (after SpShared, 16-byte aligned)
+  float *recv = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(&S + 1) + 15) & ~uintptr_t(15));
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nst = p.stages;
+  const int ct = (int)threadIdx.x - 64;  // cast thread 0 .. 255
+  const int upr = p.K >> 3;              // 16-byte units (8 elements) per token row
+  const int U_all = p.M * upr;           // unit u: row u / upr, elements 8 (u % upr) .. + 7
+  // all rows' units fit one register batch: they are read before the scan, all rows' scales at once
+  const bool all_rows = U_all <= 256 * kSpKeep;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
@@ -105,23 +168,45 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     mbar_init(&S.a_empty, 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(&S.tfull[a], 1);
-      mbar_init(&S.tempty[a], 8);
+      mbar_init(&S.tempty[a], 4);
     }
     mbar_init(&S.drain, 1);
+    mbar_init(&S.x_go, 8);
+    mbar_init(&S.part_full, 128);
+    mbar_init(&S.part_empty, 128);
     S.abort_flag = 0;
     fence_barrier_init();
-    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmW);
   }
+  if (threadIdx.x < kSpMaxRows) S.amax_bits[threadIdx.x] = 0u;
   if (warp == 1) {
-    tmem_alloc(&S.tmem_slot, 128);
+    tmem_alloc(&S.tmem_slot, 32);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the partner's barriers are initialised before any arrival on them
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_slot;
   pdl_wait();
   pdl_trigger();
+
+  // A cast thread's units: u = base + 256 j + ct (j < kSpKeep), loaded where lo <= u < hi.
+  auto load_units = [&](int base, uint4(&v)[kSpKeep], int lo, int hi) {
+#pragma unroll
+    for (int j = 0; j < kSpKeep; ++j) {
+      const int u = base + j * 256 + ct;
+      if (u >= lo && u < hi) {
+        const int r = u / upr;
+        v[j] = ldg_nc_v4(p.x + (int64_t)r * p.ld_x + (int64_t)(u - r * upr) * 8);
+      } else {
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  };
+  uint4 keep[kSpKeep];  // the current batch of units, kept between the maxima and the codes
+  int keep_base = 0;
+  if (warp >= 2 && all_rows) load_units(0, keep, 0, U_all);  // in flight during the scan
 
   // ---- scan of the group sizes: thread t holds experts 4t .. 4t + 3
   {
@@ -173,7 +258,6 @@ __global__ void __launch_bounds__(kSpThreads, 1)
       }
       s_ex += m[i];
     }
-    if (threadIdx.x < kSpMaxRows) S.amax_bits[threadIdx.x] = 0u;
     if (threadIdx.x == kSpThreads - 1) {
       long long total = 0;
       int n = 0;
@@ -187,34 +271,47 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     __syncthreads();
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = S.bad;
   }
+  const int kbc = (kchunks + KC - 1) / KC;  // stages per tile
   const int total = S.bad ? 0 : S.n_active * p.n_tiles;
-  // this CTA's tiles: [t_lo, t_hi), an even split of the tiles in order
-  const int t_lo = (int)((long long)total * blockIdx.x / gridDim.x);
-  const int t_hi = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
-  // the A region is (re)written at a tile whose group differs from the previous tile's
-  auto recast = [&](int t) { return t == t_lo || t / p.n_tiles != (t - 1) / p.n_tiles; };
+  // this CTA's (or pair's) tiles: [t_lo, t_hi), an even split in order; its stages [kb_lo, kb_hi)
+  const int slot = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int nslot = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  // (32-bit arithmetic while total x grid stays below 2^31: a 64-bit division costs ~0.2 us here)
+  auto split = [&](int b) {
+    return total < (1 << 20) ? (int)((unsigned)total * (unsigned)b / (unsigned)nslot)
+                             : (int)((long long)total * b / nslot);
+  };
+  const int t_lo = split(slot), t_hi = split(slot + 1);
+  const int kb_half = (kbc + 1) / 2;
+  const int kb_lo = PAIR && rank == 1 ? kb_half : 0, kb_hi = PAIR && rank == 0 ? kb_half : kbc;
+  // the group (active index) of a tile; the codes are (re)written when it changes
+  auto group_of = [&](int t) { return t / p.n_tiles; };
+  auto fresh_at = [&](int t) { return t == t_lo || group_of(t) != group_of(t - 1); };
   volatile int *vabort = &S.abort_flag;
   uint32_t issued = 0;
   auto timeout = [&]() {
     atomicCAS(p.status, 0, MGEMM_STATUS_TIMEOUT);
     *vabort = 1;
   };
-  const int kb_count = (kchunks + kSpKc - 1) / kSpKc;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && t_lo < t_hi) {
+      // the first token loads go out ahead of the weight stream (with all rows in one batch they
+      // were issued before the scan)
+      bool ok = all_rows || mbar_wait(&S.x_go, 0, vabort);
+      if (!ok) timeout();
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = t_lo; t < t_hi && !*vabort; ++t) {
-        const int a = t / p.n_tiles, n0 = (t % p.n_tiles) * kSpBn, e = S.act_e[a];
-        for (int kb = 0; kb < kb_count; ++kb) {
+      for (int t = t_lo; t < t_hi && ok && !*vabort; ++t) {
+        const int a = group_of(t), n0 = (t % p.n_tiles) * kSpBw, e = S.act_e[a];
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(&S.empty[stage], phase ^ 1, vabort)) {
             timeout();
             break;
           }
-          mbar_arrive_expect_tx(&S.full[stage], (uint32_t)kSpStageBytes);
+          mbar_arrive_expect_tx(&S.full[stage], (uint32_t)kStageBytes);
           ++issued;
-          tma_load_4d(sB + (size_t)stage * kSpStageBytes, &tmB, &S.full[stage], 0, n0, kb * kSpKc, e);
+          tma_load_4d(sW + (size_t)stage * kStageBytes, &tmW, &S.full[stage], 0, n0, kb * KC, e);
           if (++stage == nst) {
             stage = 0;
             phase ^= 1;
@@ -223,205 +320,224 @@ __global__ void __launch_bounds__(kSpThreads, 1)
       }
     }
   } else if (warp == 1) {
-    int stage = 0, acc = 0;
-    uint32_t phase = 0, acc_phase = 0, a_phase = 0;
-    bool ok = true;
-    for (int t = t_lo; t < t_hi && ok; ++t) {
-      // the A region changes only at a recast tile (its codes are complete when a_full flips)
-      const bool fresh = recast(t);
-      if (!mbar_wait_warp(&S.tempty[acc], acc_phase ^ 1, vabort) ||
-          (fresh && !mbar_wait_warp(&S.a_full, a_phase, vabort))) {
-        ok = false;
-        break;
-      }
-      if (fresh) a_phase ^= 1;
-      const uint32_t d_tmem = tmem_base + acc * kSpBn;
-      for (int kb = 0; kb < kb_count; ++kb) {
-        if (!mbar_wait_warp(&S.full[stage], phase, vabort)) {
+    // one thread issues every MMA (no warp-wide vote per stage)
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0, a_phase = 0;
+      bool ok = true;
+      const uint32_t idesc = p.idesc;
+      for (int t = t_lo; t < t_hi && ok; ++t) {
+        // the token codes change only with the group (they are complete when a_full flips)
+        const bool fresh = fresh_at(t);
+        if (!mbar_wait(&S.tempty[acc], acc_phase ^ 1, vabort) || (fresh && !mbar_wait(&S.a_full, a_phase, vabort))) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t bbase = smem_u32(sB + (size_t)stage * kSpStageBytes);
+        if (fresh) a_phase ^= 1;
+        const uint32_t d_tmem = tmem_base + acc * kSpTn;
+        const uint64_t t_desc = smem_desc_sw128(smem_u32(sT), 16, 1024);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+          if (!mbar_wait(&S.full[stage], phase, vabort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t w_desc = smem_desc_sw128(smem_u32(sW + (size_t)stage * kStageBytes), 16, 1024);
 #pragma unroll
-          for (int j = 0; j < kSpKc; ++j) {
-            const int chunk = kb * kSpKc + j;
-            if (chunk >= kchunks) break;  // past K: no A rows there (the weight box holds zeros)
-            const uint32_t aj = smem_u32(sA) + (uint32_t)chunk * p.a_rows * 128, bj = bbase + j * kSpBn * 128;
+          for (int j = 0; j < KC; ++j) {
+            const int chunk = kb * KC + j;
+            if (chunk >= kchunks) break;  // past K: no token codes there (the weight box holds zeros)
+            // descriptors advance by (byte offset >> 4) in their start-address field
+            const uint64_t wj = w_desc + (uint64_t)((j * kSpChunkBytes) >> 4);
+            const uint64_t tj = t_desc + (uint64_t)(((uint32_t)chunk * p.a_rows * 128) >> 4);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f8(d_tmem, smem_desc_sw128(aj + k * 32, 16, 1024), smem_desc_sw128(bj + k * 32, 16, 1024), p.idesc,
-                     (kb | j | k) != 0);
+            for (int k = 0; k < 4; ++k) mma_f8(d_tmem, wj + 2 * k, tj + 2 * k, idesc, (kb != kb_lo) | j | k);
           }
           mma_commit(&S.empty[stage]);
+          if (++stage == nst) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        __syncwarp();
-        if (++stage == nst) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-      if (!ok) break;
-      if (lane == 0) {
+        if (!ok) break;
         mma_commit(&S.tfull[acc]);
-        if (t + 1 < t_hi && recast(t + 1)) mma_commit(&S.a_empty);  // the A region is read and will be rewritten
+        if (t + 1 < t_hi && fresh_at(t + 1)) mma_commit(&S.a_empty);  // the codes are read and will be rewritten
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
-      __syncwarp();
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
-      }
-    }
-    if (!ok) {
-      if (lane == 0) timeout();
-    }
-    if (lane == 0) {
+      if (!ok) timeout();
       mma_commit(&S.drain);
       mbar_wait_drain(&S.drain, 0);
     }
     __syncwarp();
   } else {
-    // warps 2 .. 9: cast the tile's token rows, then the previous tile's epilogue
-    const int cw = warp - 2;  // 0 .. 7
-    const int q = warp & 3;   // TMEM lane quarter this warp may read
-    uint32_t e_phase = 0, acc_phase = 0;
-    int acc = 0, cb = 0;
-    int prev_t = -1, prev_acc = 0, prev_cb = 0;
-    uint32_t prev_phase = 0;
-    auto epilogue = [&](int t, int ac, uint32_t ph, int cbuf) -> bool {
-      // rows 0 .. 31 live in TMEM lane quarter 0: warps 4 and 8 read it, 32 columns each
-      if (!mbar_wait_warp(&S.tfull[ac], ph, vabort)) return false;
-      tc_fence_after();
-      const int a = t / p.n_tiles, n0 = (t % p.n_tiles) * kSpBn;
-      const int r0 = S.act_row[a], m = S.act_m[a];
-      if (q == 0) {
-        const int h = cw >> 2;  // warp 4 -> columns 0 .. 31, warp 8 -> 32 .. 63
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ac * kSpBn + h * 32, v);
-        tmem_ld_wait();
-        if (lane < m) {
-          const float ri = S.rinv[r0 + lane];
-          __nv_bfloat16 *orow = p.out + (int64_t)(r0 + lane) * p.N;
-          const uint64_t r2 = f32x2(ri, ri);
+    // ---- warps 2 .. 9: token scales and codes; warps 4 .. 7 also the epilogue
+    // magnitude maxima of the units base + 256 j + ct below hi, into S.amax_bits of their rows
+    auto reduce_units = [&](int base, const uint4(&v)[kSpKeep], int hi) {
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            const int col = n0 + h * 32 + c8 * 8;
-            uint32_t pk[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int c = h * 32 + c8 * 8 + 2 * i;
-              pk[i] = pack_bf16x2_u64(mul_f32x2(mul_f32x2(f32x2(v[c8 * 8 + 2 * i], v[c8 * 8 + 2 * i + 1]), r2),
-                                                f32x2(S.cinv[cbuf][c], S.cinv[cbuf][c + 1])));
-            }
-            if (col < p.N) *reinterpret_cast<uint4 *>(orow + col) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
+      for (int j = 0; j < kSpKeep; ++j) {
+        if (base + j * 256 >= hi) break;  // uniform over the block
+        const int u = base + j * 256 + ct;
+        const int r = u < hi ? u / upr : (hi - 1) / upr;
+        const unsigned bits = u < hi ? __float_as_uint(amax8(v[j], 0.f)) : 0u;
+        const int r_first = __shfl_sync(0xffffffffu, r, 0);
+        if (__all_sync(0xffffffffu, r == r_first)) {
+          const unsigned mx = __reduce_max_sync(0xffffffffu, bits);
+          if (lane == 0) atomicMax(&S.amax_bits[r_first], mx);
+        } else if (bits) {
+          atomicMax(&S.amax_bits[r], bits);
         }
       }
+    };
+    // rows [r_lo, r_hi): maxima of all their units (keep holds the first batch), then their scales.
+    // Every one of the eight warps calls it at the same point (it holds a barrier).
+    auto scales = [&](int r_lo, int r_hi, bool loaded) {
+      const int lo = r_lo * upr, hi = r_hi * upr;
+      if (!loaded) load_units(lo, keep, lo, hi);
+      keep_base = lo;
+      reduce_units(lo, keep, hi);
+      for (int b = lo + 256 * kSpKeep; b < hi; b += 256 * kSpKeep) {
+        uint4 v[kSpKeep];
+        load_units(b, v, lo, hi);
+        reduce_units(b, v, hi);
+      }
+      bar1_256();  // the rows' maxima are complete
+      // S.rinv is read by the epilogue warps only after a later barrier of these warps
+      if (ct < r_hi - r_lo) S.rinv[r_lo + ct] = pow2_recip(pow2_scale_from_amax(__uint_as_float(S.amax_bits[r_lo + ct])));
+    };
+    // codes of the units base + 256 j + ct in [lo, hi) (rows r0 ..) into the B region, rows relative to r0
+    auto store_units = [&](int base, const uint4(&v)[kSpKeep], int r0, int lo, int hi) {
+#pragma unroll
+      for (int j = 0; j < kSpKeep; ++j) {
+        const int u = base + j * 256 + ct;
+        if (u >= lo && u < hi) {
+          const int r = u / upr, c = (u - r * upr) * 8, i = r - r0;  // 8 code bytes at column c of row i
+          const float sc = pow2_scale_from_amax(__uint_as_float(S.amax_bits[r]));
+          const int chunk = c >> 7, b = c & 127;
+          uint8_t *dst = sT + ((size_t)chunk * p.a_rows + i) * 128 + ((((b >> 4) ^ (i & 7)) << 4) | (b & 15));
+          *reinterpret_cast<uint2 *>(dst) = cast8(v[j], sc);
+        }
+      }
+    };
+    if (t_lo < t_hi) {
+      if (all_rows) {
+        if (lane == 0) mbar_arrive(&S.x_go);
+        scales(0, p.M, true);
+      } else {
+        const int a = group_of(t_lo);
+        const int lo = S.act_row[a] * upr;
+        load_units(lo, keep, lo, lo + S.act_m[a] * upr);
+        if (lane == 0) mbar_arrive(&S.x_go);
+        scales(S.act_row[a], S.act_row[a] + S.act_m[a], true);
+      }
+    }
+    const bool epi = warp >= 4 && warp <= 7;
+    const int q = warp & 3;  // TMEM lane quarter of an epilogue warp
+    uint32_t e_phase = 0, acc_phase = 0, part_phase = 0;
+    int acc = 0;
+    int prev_t = -1, prev_acc = 0;
+    uint32_t prev_phase = 0;
+    float sw_prev = 0.f;
+    auto epilogue = [&](int t, int ac, uint32_t ph, float swv) -> bool {
+      if (!mbar_wait_warp(&S.tfull[ac], ph, vabort)) return false;
+      tc_fence_after();
+      const int a = group_of(t), row = q * 32 + lane, n = (t % p.n_tiles) * kSpBw + row;
+      const int r0 = S.act_row[a], m = S.act_m[a];
+      uint32_t v[kSpTn];
+      tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(q * 32) << 16) + ac * kSpTn, v);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.tempty[ac]);
+      if (PAIR && rank == 1) {
+        // the second half's partial sums into the first CTA's recv, once it has read the last ones
+        if (!mbar_wait_cluster_warp(&S.part_empty, part_phase ^ 1, vabort)) return false;
+        part_phase ^= 1;
+        const uint32_t dst = cluster_addr(recv + row * kSpTn, 0);
+#pragma unroll
+        for (int j = 0; j < kSpTn; j += 4)
+          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + j * 4), "r"(v[j]), "r"(v[j + 1]),
+                       "r"(v[j + 2]), "r"(v[j + 3])
+                       : "memory");
+        mbar_arrive_cluster(cluster_addr(&S.part_full, 0));
+        return true;
+      }
+      float accv[kSpTn];
+#pragma unroll
+      for (int j = 0; j < kSpTn; ++j) accv[j] = __uint_as_float(v[j]);
+      if (PAIR) {
+        // add the second half's partial sums, then hand recv back
+        if (!mbar_wait_cluster_warp(&S.part_full, part_phase, vabort)) return false;
+        part_phase ^= 1;
+        const float4 *src = reinterpret_cast<const float4 *>(recv + row * kSpTn);
+#pragma unroll
+        for (int j = 0; j < kSpTn; j += 4) {
+          const float4 f4 = src[j / 4];
+          accv[j] += f4.x;
+          accv[j + 1] += f4.y;
+          accv[j + 2] += f4.z;
+          accv[j + 3] += f4.w;
+        }
+        mbar_arrive_cluster(cluster_addr(&S.part_empty, 1));
+      }
+      if (n < p.N) {
+        const float cs = pow2_recip(swv);
+        __nv_bfloat16 *o = p.out + (int64_t)r0 * p.N + n;
+#pragma unroll
+        for (int j = 0; j < kSpTn; ++j)
+          if (j < m) o[(int64_t)j * p.N] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(accv[j], S.rinv[r0 + j]), cs));
+      }
       return true;
     };
-    // Every one of these eight warps reaches the named barrier once per tile,
-    // and the loop is left only right after it (on the abort flag, read by all
-    // of them there): a warp whose wait gave up never strands the others at it.
-    const int ct = (int)threadIdx.x - 64;  // 0 .. 255
-    const int upr = p.K >> 3;                // 16-byte units (8 elements) per row
     for (int t = t_lo; t < t_hi; ++t) {
-      const int a = t / p.n_tiles, n0 = (t % p.n_tiles) * kSpBn;
-      const int r0 = S.act_row[a], m = S.act_m[a], e = S.act_e[a];
-      const bool fresh = recast(t);
-      bool ok = true;
-      if (fresh) {
-        // unit u of the group: row u / upr, elements 8 (u % upr) .. + 7; thread ct holds u = ct + 256 j
-        const int U = m * upr;
-        auto load = [&](int j0, uint4(&v)[kSpKeep]) {
-#pragma unroll
-          for (int j = 0; j < kSpKeep; ++j) {
-            const int u = j0 + j * 256 + ct;
-            if (u < U) {
-              const int i = u / upr;
-              v[j] = ldg_nc_v4(p.x + (int64_t)(r0 + i) * p.ld_x + (int64_t)(u - i * upr) * 8);
-            } else {
-              v[j] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-        };
-        auto reduce = [&](int j0, const uint4(&v)[kSpKeep]) {
-#pragma unroll
-          for (int j = 0; j < kSpKeep; ++j) {
-            if (j0 + j * 256 >= U) break;  // uniform over the warp
-            const int u = j0 + j * 256 + ct;
-            const int i = u < U ? u / upr : m - 1;
-            const unsigned bits = u < U ? __float_as_uint(amax8(v[j], 0.f)) : 0u;
-            const int i0 = __shfl_sync(0xffffffffu, i, 0);
-            if (__all_sync(0xffffffffu, i == i0)) {
-              const unsigned r = __reduce_max_sync(0xffffffffu, bits);
-              if (lane == 0) atomicMax(&S.amax_bits[r0 + i0], r);
-            } else if (bits) {
-              atomicMax(&S.amax_bits[r0 + i], bits);
-            }
-          }
-        };
-        auto store = [&](int j0, const uint4(&v)[kSpKeep]) {
-#pragma unroll
-          for (int j = 0; j < kSpKeep; ++j) {
-            const int u = j0 + j * 256 + ct;
-            if (u < U) {
-              const int i = u / upr, c = (u - i * upr) * 8;  // 8 code bytes at column c of row i
-              const float sc = pow2_scale_from_amax(__uint_as_float(S.amax_bits[r0 + i]));
-              const int chunk = c >> 7, b = c & 127;
-              uint8_t *dst = sA + ((size_t)chunk * p.a_rows + i) * 128 + ((((b >> 4) ^ (i & 7)) << 4) | (b & 15));
-              *reinterpret_cast<uint2 *>(dst) = cast8(v[j], sc);
-            }
-          }
-        };
-        // pass 1: the row maxima (the first kSpKeep units of every thread stay in registers)
-        uint4 keep[kSpKeep];
-        load(0, keep);
-        reduce(0, keep);
-        for (int j0 = 256 * kSpKeep; j0 < U; j0 += 256 * kSpKeep) {
-          uint4 v[kSpKeep];
-          load(j0, v);
-          reduce(j0, v);
-        }
-        asm volatile("bar.sync 1, 256;" ::: "memory");  // every row maximum is complete
-        if (ct < m) S.rinv[r0 + ct] = pow2_recip(pow2_scale_from_amax(__uint_as_float(S.amax_bits[r0 + ct])));
-        // pass 2, once the MMAs of the tile before have read the A region: the codes
+      const int a = group_of(t);
+      if (fresh_at(t)) {
+        const int r0 = S.act_row[a], m = S.act_m[a];
+        const int lo = r0 * upr, hi = (r0 + m) * upr;
+        // the codes are rewritten once the MMAs before have read them
         if (!mbar_wait_warp(&S.a_empty, e_phase ^ 1, vabort)) {
           if (lane == 0) timeout();
-          ok = false;
         } else {
-          store(0, keep);
-          for (int j0 = 256 * kSpKeep; j0 < U; j0 += 256 * kSpKeep) {
+          // keep holds the batch at keep_base (all rows, or this group's first batch)
+          store_units(keep_base, keep, r0, lo, hi);
+          for (int b = keep_base + 256 * kSpKeep; b < hi; b += 256 * kSpKeep) {
+            if (b + 256 * kSpKeep <= lo) continue;  // no unit of the group in this batch
             uint4 v[kSpKeep];
-            load(j0, v);
-            store(j0, v);
+            load_units(b, v, lo, hi);
+            store_units(b, v, r0, lo, hi);
           }
         }
+        e_phase ^= 1;
+        fence_proxy_async_smem();  // the codes are read by the tensor cores
+        __syncwarp();
+        // the codes (and the group's row scales) are visible; leave together on an abort
+        if (bar1_256_or(*vabort != 0)) break;
+        if (lane == 0) mbar_arrive(&S.a_full);
       }
-      if (ok && cw == 0)  // the tile's column-scale reciprocals
-        for (int c = lane; c < kSpBn; c += 32)
-          S.cinv[cb][c] = n0 + c < p.N ? pow2_recip(__ldg(p.sw + (int64_t)e * p.N + n0 + c)) : 0.f;
-      if (fresh) e_phase ^= 1;
-      fence_proxy_async_smem();  // the codes are read by the tensor cores
-      __syncwarp();
-      // the tile's scales are visible to all eight warps; leave together on an abort
-      if (bar1_256_or(*vabort != 0)) break;
-      if (fresh && lane == 0) mbar_arrive(&S.a_full);
-      if (prev_t >= 0 && !epilogue(prev_t, prev_acc, prev_phase, prev_cb) && lane == 0) timeout();
+      // an epilogue thread's column scale for this tile, loaded ahead of its use
+      float swv = 0.f;
+      if (epi && !(PAIR && rank == 1)) {
+        const int n = (t % p.n_tiles) * kSpBw + q * 32 + lane;
+        if (n < p.N) swv = __ldg(p.sw + (int64_t)S.act_e[a] * p.N + n);
+      }
+      if (epi && prev_t >= 0 && !epilogue(prev_t, prev_acc, prev_phase, sw_prev) && lane == 0) timeout();
+      // the next group's scales while this tile's MMAs run
+      if (!all_rows && t + 1 < t_hi && fresh_at(t + 1)) {
+        const int an = group_of(t + 1);
+        scales(S.act_row[an], S.act_row[an] + S.act_m[an], false);
+      }
       prev_t = t;
       prev_acc = acc;
-      prev_cb = cb;
       prev_phase = acc_phase;
-      if (++cb == 3) cb = 0;
+      sw_prev = swv;
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
       }
     }
-    if (!*vabort && prev_t >= 0 && !epilogue(prev_t, prev_acc, prev_phase, prev_cb) && lane == 0) timeout();
+    if (epi && !*vabort && prev_t >= 0 && !epilogue(prev_t, prev_acc, prev_phase, sw_prev) && lane == 0) timeout();
   }
 
   tc_fence_before();
@@ -433,9 +549,10 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     }
   }
   __syncthreads();
+  if (PAIR) cluster_sync();  // neither CTA of a pair leaves while the other may still reach its shared memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 128);
+    tmem_dealloc(tmem_base, 32);
   }
 }
 
@@ -456,23 +573,36 @@ extern "C" int mgemm_fwd_fp8_sparse(const int64_t *group_sizes, int E, const voi
   if (((uintptr_t)group_sizes & 7) || ((uintptr_t)x & 15) || ((uintptr_t)w & 15) || ((uintptr_t)sw & 3) ||
       ((uintptr_t)out & 15) || ((uintptr_t)status & 3))
     return MGEMM_EALIGN;
-  const int a_rows = (int)((M + 7) / 8 * 8);
-  const size_t a_bytes = (size_t)K * a_rows;
-  const size_t fixed = 1024 + a_bytes + sizeof(SpShared) + 64;
-  const size_t limit = (size_t)227 * 1024;
-  if (fixed + 2 * (size_t)kSpStageBytes > limit) return MGEMM_EINVAL;  // the token rows do not fit on chip
-  int stages = (int)((limit - fixed) / kSpStageBytes);
-  if (stages > kSpMaxStages) stages = kSpMaxStages;
   int rc = ensure_context();
   if (rc) return rc;
+  const int a_rows = (int)((M + 7) / 8 * 8);
+  const size_t a_bytes = (size_t)K * a_rows;
   const int sms = sm_count_cached();
   if (sms <= 0) return MGEMM_ECUDA;
-  CUtensorMap tb;
-  {  // w [E, N, K] e4m3 as 128-byte k-chunks: {128, N, K / 128, E}, boxes of 4 chunks of 64 rows
+  const int n_tiles = (N + kSpBw - 1) / kSpBw;
+  const int64_t tiles_max = (M < E ? M : E) * (int64_t)n_tiles;  // tiles of the call at most
+  const size_t limit = (size_t)227 * 1024;
+  // stages of 64 KB (16 MMAs between waits) while three of them fit, else of 32 KB
+  auto fixed_bytes = [&](bool pr) { return 1024 + a_bytes + sizeof(SpShared) + 16 + (pr ? kSpRecvBytes : 0) + 64; };
+  auto stage_chunks = [&](size_t fx) { return fx + 3 * 4 * (size_t)kSpChunkBytes <= limit ? 4 : 2; };
+  // pairs (each CTA one half of K) when the tiles cover at most half of the SMs and a tile has two stages
+  bool pair = 2 * tiles_max <= sms && fixed_bytes(true) + 4 * (size_t)kSpChunkBytes <= limit;
+  if (pair) {
+    const int kc_pair = stage_chunks(fixed_bytes(true));
+    pair = (K / 128 + kc_pair - 1) / kc_pair >= 2;
+  }
+  const size_t fixed = fixed_bytes(pair);
+  if (fixed + 4 * (size_t)kSpChunkBytes > limit) return MGEMM_EINVAL;  // the token rows do not fit on chip
+  const int kc = stage_chunks(fixed);
+  const size_t stage_bytes = (size_t)kc * kSpChunkBytes;
+  int stages = (int)((limit - fixed) / stage_bytes);
+  if (stages > kSpMaxStages) stages = kSpMaxStages;
+  CUtensorMap tw;
+  {  // w [E, N, K] e4m3 as 128-byte k-chunks: {128, N, K / 128, E}, boxes of kc chunks of 128 rows
     const uint64_t d[4] = {128, (uint64_t)N, (uint64_t)K / 128, (uint64_t)E};
     const uint64_t st[3] = {(uint64_t)K, 128, (uint64_t)N * K};
-    const uint32_t box[4] = {128, (uint32_t)kSpBn, (uint32_t)kSpKc, 1};
-    if (!make_tensor_map(&tb, true, 4, w, d, st, box)) return MGEMM_ECUDA;
+    const uint32_t box[4] = {128, (uint32_t)kSpBw, (uint32_t)kc, 1};
+    if (!make_tensor_map(&tw, true, 4, w, d, st, box)) return MGEMM_ECUDA;
   }
   SpParams p{};
   p.sizes = group_sizes;
@@ -482,27 +612,35 @@ extern "C" int mgemm_fwd_fp8_sparse(const int64_t *group_sizes, int E, const voi
   p.N = N;
   p.a_rows = a_rows;
   p.stages = stages;
-  p.n_tiles = (N + kSpBn - 1) / kSpBn;
+  p.n_tiles = n_tiles;
   p.x = (const __nv_bfloat16 *)x;
   p.ld_x = ld_x;
   p.sw = sw;
   p.out = (__nv_bfloat16 *)out;
   p.status = status;
-  p.idesc = make_idesc(0u, false, false, 128, kSpBn);
-  const int64_t upper = (M < E ? M : E) * (int64_t)p.n_tiles;
-  const int grid = (int)(upper < sms ? upper : sms);
-  const size_t smem = fixed + (size_t)stages * kSpStageBytes;
+  p.idesc = make_idesc(0u, false, false, kSpBw, kSpTn);
+  const int grid = pair ? (int)(2 * tiles_max) : (int)(tiles_max < sms ? tiles_max : sms);
+  const size_t smem = fixed + (size_t)stages * stage_bytes;
   static bool attr_done[64] = {};
   int dev = 0;
   rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
   if (rc) return rc;
   if (dev < 0 || dev >= 64) return MGEMM_EINVAL;
   if (!attr_done[dev]) {
-    rc = cuda_rc(cudaFuncSetAttribute(sparse_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit),
-                 "cudaFuncSetAttribute");
-    if (rc) return rc;
+    const void *fns[4] = {(const void *)sparse_fp8_kernel<2, false>, (const void *)sparse_fp8_kernel<4, false>,
+                          (const void *)sparse_fp8_kernel<2, true>, (const void *)sparse_fp8_kernel<4, true>};
+    for (const void *f : fns) {
+      rc = cuda_rc(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit),
+                   "cudaFuncSetAttribute");
+      if (rc) return rc;
+    }
     attr_done[dev] = true;
   }
-  return launch_pdl(sparse_fp8_kernel, dim3((unsigned)grid), dim3(kSpThreads), smem, (cudaStream_t)stream, 1u,
-                    "sparse FP8 forward launch", tb, p);
+  const cudaStream_t st = (cudaStream_t)stream;
+  const char *what = pair ? "sparse FP8 forward launch (CTA pairs)" : "sparse FP8 forward launch";
+  if (pair)
+    return kc == 4 ? launch_pdl(sparse_fp8_kernel<4, true>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 2u, what, tw, p)
+                   : launch_pdl(sparse_fp8_kernel<2, true>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 2u, what, tw, p);
+  return kc == 4 ? launch_pdl(sparse_fp8_kernel<4, false>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 1u, what, tw, p)
+                 : launch_pdl(sparse_fp8_kernel<2, false>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 1u, what, tw, p);
 }
