@@ -14,17 +14,18 @@
 // instruction consumes only N x 32 bytes of weights and the tensor pipe, not
 // HBM, bounds the stream.
 //
-// Work split: a tile is one non-empty group x 128 weight rows (output
+// Work split: a tile is one non-empty group x tw weight rows (output
 // columns) x all of K, cut into stages of KC contraction blocks.  The CTAs
 // (persistent, one per SM) take equal contiguous ranges of tiles, and
 // consecutive tiles mostly share their group, so a CTA writes a group's token
-// codes once for the whole run of them.  When there are at most half as many
-// tiles as SMs (one token: one expert's 64 tiles), CTA pairs (clusters of two)
-// take the tiles instead, each CTA one half of the contraction, so that every
-// SM streams weights: the second CTA hands its fp32 partial sums to the
-// first through the first's shared memory, and the first adds them to its own
-// before the epilogue.  Without pairs every output equals mgemm_fwd's bit for
-// bit; with them it differs by the rounding of that one addition.
+// codes once for the whole run of them.  The host picks tw (96 to 128) so
+// that the tiles divide evenly over the SMs.  When 128-row tiles number at
+// most half the SMs (one token: one expert's 64 tiles), CTA pairs (clusters
+// of two) take them instead, each CTA one half of the contraction, so that
+// every SM streams weights: the second CTA hands its fp32 partial sums to the
+// first through the first's shared memory, and the first adds them to its
+// own before the epilogue.  Without pairs every output equals mgemm_fwd's bit
+// for bit; with them it differs by the rounding of that one addition.
 //
 // CTA roles (320 threads):
 //   all         at launch, the token rows are read and their magnitude maxima
@@ -54,11 +55,10 @@
 namespace mgemm {
 namespace {
 
-constexpr int kSpBw = 128;       // weight rows (output columns) per tile: the MMA's M
+constexpr int kSpBw = 128;       // the MMA's M: weight rows (output columns) per tile at most
 constexpr int kSpTn = 16;        // the MMA's N: token rows (a group has at most 16)
 constexpr int kSpMaxRows = 16;   // token rows of the whole call at most
 constexpr int kSpThreads = 320;
-constexpr int kSpChunkBytes = kSpBw * 128;  // one contraction block of 128 weight rows
 constexpr int kSpMaxStages = 12;
 constexpr int kSpKeep = 8;       // 16-byte units per cast thread held in registers
 constexpr int kSpRecvBytes = kSpBw * kSpTn * 4;  // a pair's partial sums: 128 rows x 16 fp32
@@ -69,8 +69,9 @@ struct SpParams {
   int M;
   int K, N;
   int a_rows;     // token rows rounded up to 8 (the B region's rows per chunk)
+  int tw;         // weight rows per tile (a multiple of 8, at most 128), chosen to balance the SMs
   int stages;
-  int n_tiles;    // ceil(N / 128)
+  int n_tiles;    // ceil(N / tw)
   const __nv_bfloat16 *x;
   int64_t ld_x;
   const float *sw;
@@ -141,13 +142,16 @@ __device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t p
 template <int KC, bool PAIR>
 __global__ void __launch_bounds__(kSpThreads, 1)
     sparse_fp8_kernel(const __grid_constant__ CUtensorMap tmW, const SpParams p) {
-  constexpr int kStageBytes = KC * kSpChunkBytes;
+  const int chunk_bytes = p.tw * 128;  // one contraction block of the tile's weight rows
+  const int stage_bytes = KC * chunk_bytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int kchunks = p.K / 128;
   uint8_t *sT = smem;                                                  // token codes [kchunks][a_rows][128 B]
   uint8_t *sW = sT + (size_t)kchunks * p.a_rows * 128;                 // ring of weight stages
-  SpShared &S = *reinterpret_cast<SpShared *>(sW + (size_t)p.stages * kStageBytes);
+  // (the MMA reads 128 rows from a block's start; past a tile of tw rows, the next block's or the
+  // following bytes, inside the allocation, feed accumulator lanes that are never read)
+  SpShared &S = *reinterpret_cast<SpShared *>(sW + (size_t)p.stages * stage_bytes);
   // pairs: the partner's partial sums, [128 rows][16] fp32 (after SpShared, 16-byte aligned)
   float *recv = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(&S + 1) + 15) & ~uintptr_t(15));
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -303,15 +307,15 @@ __global__ void __launch_bounds__(kSpThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int t = t_lo; t < t_hi && ok && !*vabort; ++t) {
-        const int a = group_of(t), n0 = (t % p.n_tiles) * kSpBw, e = S.act_e[a];
+        const int a = group_of(t), n0 = (t % p.n_tiles) * p.tw, e = S.act_e[a];
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(&S.empty[stage], phase ^ 1, vabort)) {
             timeout();
             break;
           }
-          mbar_arrive_expect_tx(&S.full[stage], (uint32_t)kStageBytes);
+          mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
           ++issued;
-          tma_load_4d(sW + (size_t)stage * kStageBytes, &tmW, &S.full[stage], 0, n0, kb * KC, e);
+          tma_load_4d(sW + (size_t)stage * stage_bytes, &tmW, &S.full[stage], 0, n0, kb * KC, e);
           if (++stage == nst) {
             stage = 0;
             phase ^= 1;
@@ -342,13 +346,13 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t w_desc = smem_desc_sw128(smem_u32(sW + (size_t)stage * kStageBytes), 16, 1024);
+          const uint64_t w_desc = smem_desc_sw128(smem_u32(sW + (size_t)stage * stage_bytes), 16, 1024);
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
             const int chunk = kb * KC + j;
             if (chunk >= kchunks) break;  // past K: no token codes there (the weight box holds zeros)
             // descriptors advance by (byte offset >> 4) in their start-address field
-            const uint64_t wj = w_desc + (uint64_t)((j * kSpChunkBytes) >> 4);
+            const uint64_t wj = w_desc + (uint64_t)((j * chunk_bytes) >> 4);
             const uint64_t tj = t_desc + (uint64_t)(((uint32_t)chunk * p.a_rows * 128) >> 4);
 #pragma unroll
             for (int k = 0; k < 4; ++k) mma_f8(d_tmem, wj + 2 * k, tj + 2 * k, idesc, (kb != kb_lo) | j | k);
@@ -443,7 +447,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     auto epilogue = [&](int t, int ac, uint32_t ph, float swv) -> bool {
       if (!mbar_wait_warp(&S.tfull[ac], ph, vabort)) return false;
       tc_fence_after();
-      const int a = group_of(t), row = q * 32 + lane, n = (t % p.n_tiles) * kSpBw + row;
+      const int a = group_of(t), row = q * 32 + lane, n = (t % p.n_tiles) * p.tw + row;
       const int r0 = S.act_row[a], m = S.act_m[a];
       uint32_t v[kSpTn];
       tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(q * 32) << 16) + ac * kSpTn, v);
@@ -482,7 +486,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         }
         mbar_arrive_cluster(cluster_addr(&S.part_empty, 1));
       }
-      if (n < p.N) {
+      if (row < p.tw && n < p.N) {
         const float cs = pow2_recip(swv);
         __nv_bfloat16 *o = p.out + (int64_t)r0 * p.N + n;
 #pragma unroll
@@ -519,8 +523,8 @@ __global__ void __launch_bounds__(kSpThreads, 1)
       // an epilogue thread's column scale for this tile, loaded ahead of its use
       float swv = 0.f;
       if (epi && !(PAIR && rank == 1)) {
-        const int n = (t % p.n_tiles) * kSpBw + q * 32 + lane;
-        if (n < p.N) swv = __ldg(p.sw + (int64_t)S.act_e[a] * p.N + n);
+        const int row = q * 32 + lane, n = (t % p.n_tiles) * p.tw + row;
+        if (row < p.tw && n < p.N) swv = __ldg(p.sw + (int64_t)S.act_e[a] * p.N + n);
       }
       if (epi && prev_t >= 0 && !epilogue(prev_t, prev_acc, prev_phase, sw_prev) && lane == 0) timeout();
       // the next group's scales while this tile's MMAs run
@@ -579,30 +583,54 @@ extern "C" int mgemm_fwd_fp8_sparse(const int64_t *group_sizes, int E, const voi
   const size_t a_bytes = (size_t)K * a_rows;
   const int sms = sm_count_cached();
   if (sms <= 0) return MGEMM_ECUDA;
-  const int n_tiles = (N + kSpBw - 1) / kSpBw;
-  const int64_t tiles_max = (M < E ? M : E) * (int64_t)n_tiles;  // tiles of the call at most
+  const int64_t groups_max = M < E ? M : E;  // non-empty groups at most
   const size_t limit = (size_t)227 * 1024;
-  // stages of 64 KB (16 MMAs between waits) while three of them fit, else of 32 KB
-  auto fixed_bytes = [&](bool pr) { return 1024 + a_bytes + sizeof(SpShared) + 16 + (pr ? kSpRecvBytes : 0) + 64; };
-  auto stage_chunks = [&](size_t fx) { return fx + 3 * 4 * (size_t)kSpChunkBytes <= limit ? 4 : 2; };
-  // pairs (each CTA one half of K) when the tiles cover at most half of the SMs and a tile has two stages
-  bool pair = 2 * tiles_max <= sms && fixed_bytes(true) + 4 * (size_t)kSpChunkBytes <= limit;
+  // Weight rows per tile: CTA pairs take 128-row tiles when 128-row tiles cover at most half of
+  // the SMs (one token); else the tile height (a multiple of 8 from 96 to 128) that minimizes the
+  // weight rows of the busiest CTA when the tiles of groups_max groups are split evenly over the
+  // SMs.  (Below 96 rows the MMA, which takes 128 rows per instruction whatever the tile holds,
+  // would consume the weights slower than an SM's share of HBM.)
+  const int64_t tiles128 = groups_max * ((N + kSpBw - 1) / kSpBw);
+  bool pair = 2 * tiles128 <= sms;
+  int tw = kSpBw;
+  if (!pair) {
+    int64_t best = -1;
+    for (int h = kSpBw; h >= 96; h -= 8) {
+      const int64_t nt = (N + h - 1) / h, per_cta = (groups_max * nt + sms - 1) / sms * h;
+      if (best < 0 || per_cta < best) {
+        best = per_cta;
+        tw = h;
+      }
+    }
+  }
+  const int n_tiles = (N + tw - 1) / tw;
+  const int64_t tiles_max = groups_max * (int64_t)n_tiles;
+  const size_t chunk_bytes = (size_t)tw * 128;
+  // past the ring: SpShared, the pair's partial sums, and the MMA's read of 128 rows from a
+  // block's start beyond a tile of fewer rows
+  auto fixed_bytes = [&](bool pr) {
+    return 1024 + a_bytes + sizeof(SpShared) + 16 + (pr ? kSpRecvBytes : 0) + (size_t)(kSpBw - tw) * 128 + 64;
+  };
+  // stages of 4 blocks (16 MMAs between waits) while three of them fit, else of 2
+  auto stage_chunks = [&](size_t fx) { return fx + 3 * 4 * chunk_bytes <= limit ? 4 : 2; };
+  // pairs need the partial-sum buffer to fit and two stages per tile
+  if (pair) pair = fixed_bytes(true) + 4 * chunk_bytes <= limit;
   if (pair) {
     const int kc_pair = stage_chunks(fixed_bytes(true));
     pair = (K / 128 + kc_pair - 1) / kc_pair >= 2;
   }
   const size_t fixed = fixed_bytes(pair);
-  if (fixed + 4 * (size_t)kSpChunkBytes > limit) return MGEMM_EINVAL;  // the token rows do not fit on chip
+  if (fixed + 4 * chunk_bytes > limit) return MGEMM_EINVAL;  // the token rows do not fit on chip
   const int kc = stage_chunks(fixed);
-  const size_t stage_bytes = (size_t)kc * kSpChunkBytes;
+  const size_t stage_bytes = (size_t)kc * chunk_bytes;
   int stages = (int)((limit - fixed) / stage_bytes);
   if (stages > kSpMaxStages) stages = kSpMaxStages;
-  CUtensorMap tw;
+  CUtensorMap tmap;
   {  // w [E, N, K] e4m3 as 128-byte k-chunks: {128, N, K / 128, E}, boxes of kc chunks of 128 rows
     const uint64_t d[4] = {128, (uint64_t)N, (uint64_t)K / 128, (uint64_t)E};
     const uint64_t st[3] = {(uint64_t)K, 128, (uint64_t)N * K};
-    const uint32_t box[4] = {128, (uint32_t)kSpBw, (uint32_t)kc, 1};
-    if (!make_tensor_map(&tw, true, 4, w, d, st, box)) return MGEMM_ECUDA;
+    const uint32_t box[4] = {128, (uint32_t)tw, (uint32_t)kc, 1};
+    if (!make_tensor_map(&tmap, true, 4, w, d, st, box)) return MGEMM_ECUDA;
   }
   SpParams p{};
   p.sizes = group_sizes;
@@ -613,6 +641,7 @@ extern "C" int mgemm_fwd_fp8_sparse(const int64_t *group_sizes, int E, const voi
   p.a_rows = a_rows;
   p.stages = stages;
   p.n_tiles = n_tiles;
+  p.tw = tw;
   p.x = (const __nv_bfloat16 *)x;
   p.ld_x = ld_x;
   p.sw = sw;
@@ -639,8 +668,8 @@ extern "C" int mgemm_fwd_fp8_sparse(const int64_t *group_sizes, int E, const voi
   const cudaStream_t st = (cudaStream_t)stream;
   const char *what = pair ? "sparse FP8 forward launch (CTA pairs)" : "sparse FP8 forward launch";
   if (pair)
-    return kc == 4 ? launch_pdl(sparse_fp8_kernel<4, true>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 2u, what, tw, p)
-                   : launch_pdl(sparse_fp8_kernel<2, true>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 2u, what, tw, p);
-  return kc == 4 ? launch_pdl(sparse_fp8_kernel<4, false>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 1u, what, tw, p)
-                 : launch_pdl(sparse_fp8_kernel<2, false>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 1u, what, tw, p);
+    return kc == 4 ? launch_pdl(sparse_fp8_kernel<4, true>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 2u, what, tmap, p)
+                   : launch_pdl(sparse_fp8_kernel<2, true>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 2u, what, tmap, p);
+  return kc == 4 ? launch_pdl(sparse_fp8_kernel<4, false>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 1u, what, tmap, p)
+                 : launch_pdl(sparse_fp8_kernel<2, false>, dim3((unsigned)grid), dim3(kSpThreads), smem, st, 1u, what, tmap, p);
 }

@@ -78,6 +78,7 @@ def three_calls(gs, E, x, wq, sw, N):
     ([16], 4096, 64),                   # four batches
     ([3, 0, 4], 384, 136),              # rows of 48 units: a warp's units straddle two rows
     ([3, 4, 5, 4], 2048, 8192),         # more tiles than SMs: CTAs whose tiles span two groups
+    ([1] * 16, 256, 1040),              # tiles of 120 weight rows (on 148+ SMs), the last of 80
 ])
 @pytest.mark.parametrize("ld_pad", [0, 40])
 def test_sparse_fwd_equals_the_three_calls(sizes, K, N, ld_pad):
