@@ -311,18 +311,27 @@ __global__ void __launch_bounds__(kI4Threads, 1)
           ok = false;
           break;
         }
-        // expand: output chunk ch (16 elements) of weight row n of block jj
+        // expand: output chunk ch (16 elements) of weight row n of block jj.  All of a
+        // thread's packed chunks are read first (the raw and expanded slots are distinct,
+        // but the compiler cannot tell), so the reads overlap instead of each waiting
+        // behind the previous chunk's conversion and store.
         const uint8_t *src = raw_w(r);
         uint8_t *dst = xb(x, 0);
         constexpr int kChunks = C::KC * C::BW * 8;
         static_assert(kChunks % NT == 0, "whole rounds");
+        constexpr int kIt = kChunks / NT;
+        uint2 v[kIt];
 #pragma unroll
-        for (int it = 0; it < kChunks / NT; ++it) {
+        for (int it = 0; it < kIt; ++it) {
+          const int idx = c + it * NT;
+          v[it] = *reinterpret_cast<const uint2 *>(src + (size_t)idx * 8);  // = (jj * BW + n) * 64 + ch * 8
+        }
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
           const int idx = c + it * NT;
           const int jj = idx / (C::BW * 8), rem = idx % (C::BW * 8);
           const int n = rem >> 3, ch = rem & 7;
-          const uint2 v = *reinterpret_cast<const uint2 *>(src + (jj * C::BW + n) * 64 + ch * 8);
-          const uint2 lo = int4x8_to_e4m3(v.x), hi = int4x8_to_e4m3(v.y);
+          const uint2 lo = int4x8_to_e4m3(v[it].x), hi = int4x8_to_e4m3(v[it].y);
           *reinterpret_cast<uint4 *>(dst + (jj * C::BW + n) * 128 + ((ch ^ (n & 7)) << 4)) =
               make_uint4(lo.x, lo.y, hi.x, hi.y);
         }
