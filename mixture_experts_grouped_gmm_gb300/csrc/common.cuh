@@ -218,6 +218,36 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, c
   return __all_sync(0xffffffffu, ok);
 }
 
+// mbar_wait_warp with acquire at cluster scope: the arrivals come from the
+// other CTA of the pair (released at cluster scope) and order its writes
+// into this CTA's shared memory before the reads that follow.
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity, const volatile int *abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  auto test = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  bool ok = test();
+  if (!ok) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (test()) {
+        ok = true;
+        break;
+      }
+      if ((i & 255u) == 0 && ((abort_flag && *abort_flag) || global_timer_ns() - t0 > kWaitLimitNs)) break;
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -27,7 +27,8 @@
 //               (swizzled), packed weights [KC][128][64 B] and their scale
 //               words [KC][128][4 B]; the number of slots is set per launch by
 //               the shared memory left.
-//   warp 1      TMEM owner and MMA issuer (one thread): per raw slot, the
+//   warp 1      TMEM owner and MMA issuer (one thread, which also does the
+//               waits): per raw slot, the
 //               4 KC block-scaled MMAs (K = 32 each; the scale-factor ids
 //               select byte k of the scale words); commits free the expanded
 //               slot and the raw slot (its token rows are read by the MMAs),
@@ -45,6 +46,12 @@
 //               (weight rows, i.e. output columns), tcgen05.ld of the token
 //               columns, bf16 rounding, stores out[token][column] (a warp's 32
 //               lanes write 64 contiguous bytes of one token row).
+// PAIR form (at most 16 token rows, and tiles for at most half of the SMs):
+// clusters of two CTAs take the tiles, each CTA one half of the contraction
+// blocks, so that every SM streams nibbles; the second CTA writes its fp32
+// partial sums into the first's shared memory (st.shared::cluster, each lane
+// arriving on the first's barrier with release at cluster scope) and the first
+// adds them before rounding.
 // Every wait is bounded; on expiry the kernel records MGEMM_STATUS_TIMEOUT,
 // drains the copies and MMAs it issued, frees TMEM and returns.
 #include "gemm_launch.cuh"
@@ -56,8 +63,9 @@ constexpr int kConvWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kI4Threads = 64 + 32 * (kConvWarps + kEpiWarps);
 
-template <int kKc, int kXs>
+template <int kKc, int kXs, bool kPair = false>
 struct I4Cfg {
+  static constexpr bool PAIR = kPair;  // CTA pairs split each tile's contraction (16 token rows)
   static constexpr int BW = 128;   // weight rows (output columns) per tile: the MMA's M
   static constexpr int TB_MAX = 128;  // token rows per tile at most: the MMA's N
   static constexpr int KC = kKc;   // contraction blocks of 128 per raw slot
@@ -70,7 +78,8 @@ struct I4Cfg {
   static constexpr int TMEM_COLS = COLS <= 256 ? 256 : 512;
   static_assert(COLS <= 512, "tensor memory");
   static_assert(XB_SLOT % 1024 == 0, "swizzle atoms");
-  static constexpr size_t TAIL = 8 * (2 * RS_MAX + 2 * XS + 8 + 1) + 64;
+  static constexpr int RECV_BYTES = 128 * 16 * 4;  // PAIR: the partner's partial sums, 128 rows x 16 fp32
+  static constexpr size_t TAIL = 8 * (2 * RS_MAX + 2 * XS + 8 + 1 + 2) + 64 + (PAIR ? 16 + RECV_BYTES : 0);
   // a raw slot: [tokens KC x TB x 128][weights packed KC x 128 x 64][weight scales KC x 128 x 4]
   static size_t raw_slot_bytes(int tb) {
     return ((size_t)KC * ((size_t)tb * 128 + BW * 64 + BW * 4) + 1023) / 1024 * 1024;
@@ -136,11 +145,21 @@ __global__ void __launch_bounds__(kI4Threads, 1)
   uint64_t *xb_full = raw_empty + C::RS_MAX, *xb_empty = xb_full + C::XS;
   uint64_t *ts_full = xb_empty + C::XS, *ts_empty = ts_full + 2;
   uint64_t *tfull = ts_empty + 2, *tempty = tfull + 2, *drain = tempty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *part_full = drain + 1, *part_empty = part_full + 1;  // PAIR: recv holds a partial / may be rewritten
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(part_empty + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+  float *recv = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(abort_flag + 1) + 15) & ~uintptr_t(15));
+  const uint32_t rank = C::PAIR ? cluster_ctarank() : 0u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t_first = (int)blockIdx.x, t_step = (int)gridDim.x;
+  const int t_first = C::PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int t_step = C::PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  // a tile's contraction blocks (raw slots) [g_lo, g_hi) of its kb_count for this CTA
+  auto g_range = [&](int kb_count, int &g_lo, int &g_hi) {
+    const int half = (kb_count + 1) / 2;
+    g_lo = C::PAIR && rank == 1 ? half : 0;
+    g_hi = C::PAIR && rank == 0 ? half : kb_count;
+  };
   // set-up before the wait for the previous grid (it reads nothing that grid
   // writes); a CTA without tiles runs no role loop
   if (threadIdx.x == 0) {
@@ -159,6 +178,8 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       mbar_init(&tempty[a], kEpiWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(part_full, 128);
+    mbar_init(part_empty, 128);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -171,6 +192,7 @@ __global__ void __launch_bounds__(kI4Threads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (C::PAIR) cluster_sync();  // the partner's barriers are initialised before any arrival on them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();
@@ -190,7 +212,9 @@ __global__ void __launch_bounds__(kI4Threads, 1)
         const int t = tile_of<D>(j, t_first, t_step);
         if (t >= total) continue;
         const TileInfo ti = decode_tile<D>(t, p, av, 0u);
-        for (int g = 0; g < ti.kb_count; ++g) {
+        int g_lo, g_hi;
+        g_range(ti.kb_count, g_lo, g_hi);
+        for (int g = g_lo; g < g_hi; ++g) {
           if (!mbar_wait(&raw_empty[r], ph ^ 1, vabort)) {
             set_status(av.status, MGEMM_STATUS_TIMEOUT);
             *vabort = 1;
@@ -210,67 +234,65 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       }
     }
   } else if (warp == 1) {
-    int r = 0, x = 0, acc = 0;
-    uint32_t rph = 0, xph = 0, aph = 0;
-    bool ok = true;
-    for (int j = 0; j * t_step < total && ok; ++j) {
-      const int t = tile_of<D>(j, t_first, t_step);
-      if (t >= total) continue;
-      const TileInfo ti = decode_tile<D>(t, p, av, 0u);
-      if (!mbar_wait_warp(&tempty[acc], aph ^ 1, vabort) || !mbar_wait_warp(&ts_full[acc], aph, vabort)) {
-        ok = false;
-        break;
-      }
-      const uint32_t d_tmem = tmem_base + acc * C::TB_MAX;
-      const uint32_t sft = tmem_base + C::SFT_COL + 4 * acc;
-      for (int g = 0; g < ti.kb_count; ++g) {
-        if (!mbar_wait_warp(&raw_full[r], rph, vabort) || !mbar_wait_warp(&xb_full[x], xph, vabort)) {
+    // one thread waits and issues (no warp-wide vote per slot)
+    if (lane == 0) {
+      int r = 0, x = 0, acc = 0;
+      uint32_t rph = 0, xph = 0, aph = 0;
+      bool ok = true;
+      for (int j = 0; j * t_step < total && ok; ++j) {
+        const int t = tile_of<D>(j, t_first, t_step);
+        if (t >= total) continue;
+        const TileInfo ti = decode_tile<D>(t, p, av, 0u);
+        if (!mbar_wait(&tempty[acc], aph ^ 1, vabort) || !mbar_wait(&ts_full[acc], aph, vabort)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (lane == 0) {
+        const uint32_t d_tmem = tmem_base + acc * C::TB_MAX;
+        const uint32_t sft = tmem_base + C::SFT_COL + 4 * acc;
+        int g_lo, g_hi;
+        g_range(ti.kb_count, g_lo, g_hi);
+        for (int g = g_lo; g < g_hi; ++g) {
+          if (!mbar_wait(&raw_full[r], rph, vabort) || !mbar_wait(&xb_full[x], xph, vabort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int jj = 0; jj < C::KC; ++jj) {
             const uint32_t sfw = tmem_base + C::SFW_COL + 4 * (x * C::KC + jj);
-            const uint32_t wbase = smem_u32(xb(x, jj)), tbase = smem_u32(raw_t(r, jj));
+            // descriptors advance by (byte offset >> 4) in their start-address field
+            const uint64_t ad = smem_desc_sw128(smem_u32(xb(x, jj)), 16, 1024);    // weights: M side
+            const uint64_t bd = smem_desc_sw128(smem_u32(raw_t(r, jj)), 16, 1024);  // tokens: N side
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc_sw128(wbase + k * 32, 16, 1024);   // weights: M side
-              const uint64_t bd = smem_desc_sw128(tbase + k * 32, 16, 1024);   // tokens: N side
               const uint32_t idk = p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-              mma_mx(d_tmem, ad, bd, idk, sfw, sft, (g | jj | k) != 0);
+              mma_mx(d_tmem, ad + 2 * k, bd + 2 * k, idk, sfw, sft, (g != g_lo) | jj | k);
             }
           }
           mma_commit(&xb_empty[x]);
           mma_commit(&raw_empty[r]);  // the slot's token rows are read
+          if (++x == C::XS) {
+            x = 0;
+            xph ^= 1;
+          }
+          if (++r == RS) {
+            r = 0;
+            rph ^= 1;
+          }
         }
-        __syncwarp();
-        if (++x == C::XS) {
-          x = 0;
-          xph ^= 1;
-        }
-        if (++r == RS) {
-          r = 0;
-          rph ^= 1;
-        }
-      }
-      if (!ok) break;
-      if (lane == 0) {
+        if (!ok) break;
         mma_commit(&tfull[acc]);
         mma_commit(&ts_empty[acc]);  // the tile's token-scale columns are read
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1;
+        }
       }
-      __syncwarp();
-      if (++acc == 2) {
-        acc = 0;
-        aph ^= 1;
+      if (!ok) {
+        set_status(av.status, MGEMM_STATUS_TIMEOUT);
+        *vabort = 1;
       }
-    }
-    if (!ok) {
-      if (lane == 0) set_status(av.status, MGEMM_STATUS_TIMEOUT);
-      *vabort = 1;
-    }
-    if (lane == 0) {  // every MMA this thread issued has completed before TMEM is freed
+      // every MMA this thread issued has completed before TMEM is freed
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
     }
@@ -306,7 +328,9 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ts_full[acc]);
-      for (int g = 0; g < ti.kb_count; ++g) {
+      int g_lo, g_hi;
+      g_range(ti.kb_count, g_lo, g_hi);
+      for (int g = g_lo; g < g_hi; ++g) {
         if (!mbar_wait_warp(&raw_full[r], rph, vabort) || !mbar_wait_warp(&xb_empty[x], xph ^ 1, vabort)) {
           ok = false;
           break;
@@ -372,7 +396,7 @@ __global__ void __launch_bounds__(kI4Threads, 1)
     // columns n0 + 32 q + lane, and the token columns 0 .. TB - 1
     const int q = warp & 3;
     int acc = 0;
-    uint32_t aph = 0;
+    uint32_t aph = 0, part_phase = 0;
     for (int j = 0; j * t_step < total; ++j) {
       const int t = tile_of<D>(j, t_first, t_step);
       if (t >= total) continue;
@@ -386,6 +410,7 @@ __global__ void __launch_bounds__(kI4Threads, 1)
       const int col = ti.n0 + q * 32 + lane;
       const bool col_ok = col < p.Nout;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::TB_MAX;
+      bool pair_ok = true;
       for (int c0 = 0; c0 < TB; c0 += 16) {
         uint32_t v[16];
         tmem_ld_32x32b_x16(taddr + c0, v);
@@ -395,12 +420,51 @@ __global__ void __launch_bounds__(kI4Threads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[acc]);
         }
+        if (C::PAIR) {  // TB == 16: one chunk
+          const int row = q * 32 + lane;
+          if (rank == 1) {
+            // the second half's partial sums into the first CTA's recv, once it has read the last ones
+            if (!mbar_wait_cluster_warp(part_empty, part_phase ^ 1, vabort)) {
+              pair_ok = false;
+              break;
+            }
+            part_phase ^= 1;
+            const uint32_t dst = cluster_addr(recv + row * 16, 0);
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + i * 4), "r"(v[i]),
+                           "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3])
+                           : "memory");
+            mbar_arrive_cluster(cluster_addr(part_full, 0));
+            continue;
+          }
+          if (!mbar_wait_cluster_warp(part_full, part_phase, vabort)) {
+            pair_ok = false;
+            break;
+          }
+          part_phase ^= 1;
+          const float4 *src = reinterpret_cast<const float4 *>(recv + row * 16);
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 f4 = src[i / 4];
+            v[i] = __float_as_uint(__uint_as_float(v[i]) + f4.x);
+            v[i + 1] = __float_as_uint(__uint_as_float(v[i + 1]) + f4.y);
+            v[i + 2] = __float_as_uint(__uint_as_float(v[i + 2]) + f4.z);
+            v[i + 3] = __float_as_uint(__uint_as_float(v[i + 3]) + f4.w);
+          }
+          mbar_arrive_cluster(cluster_addr(part_empty, 1));
+        }
         if (col_ok) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (c0 + i < ti.out_rows)
               p.out[((int64_t)ti.out_row0 + c0 + i) * p.Nout + col] = __float2bfloat16_rn(__uint_as_float(v[i]));
         }
+      }
+      if (!pair_ok) {
+        set_status(av.status, MGEMM_STATUS_TIMEOUT);
+        *vabort = 1;
+        break;
       }
       if (++acc == 2) {
         acc = 0;
@@ -419,6 +483,7 @@ __global__ void __launch_bounds__(kI4Threads, 1)
     }
   }
   __syncthreads();
+  if (C::PAIR) cluster_sync();  // neither CTA of a pair leaves while the other may still reach its shared memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -447,8 +512,8 @@ int launch_f8i4(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &s
     if (rc) return rc;
     attr_done[dev] = true;
   }
-  return launch_pdl(f8i4_gemm_kernel<C>, dim3((unsigned)grid), dim3(kI4Threads), smem, st, 1u, "F8I4 GEMM launch", a,
-                    b, s, P);
+  return launch_pdl(f8i4_gemm_kernel<C>, dim3((unsigned)grid), dim3(kI4Threads), smem, st, C::PAIR ? 2u : 1u,
+                    C::PAIR ? "F8I4 GEMM launch (CTA pairs)" : "F8I4 GEMM launch", a, b, s, P);
 }
 
 }  // namespace
@@ -510,7 +575,12 @@ extern "C" int mgemm_fwd_f8i4(const void *args, const uint8_t *x, const float *s
   p.out = (__nv_bfloat16 *)out;
   p.rscale = sx;
   const int64_t upper = ((M + 127) / 128 + groups) * p.n_tiles;
-  const int grid = (int)(upper < sms ? upper : sms);
   cudaStream_t s = (cudaStream_t)stream;
+  // pairs: 16 token rows (every group in one row tile: at most groups x n_tiles tiles), two
+  // contraction slots per tile at least, and tiles for at most half of the SMs
+  const int64_t tiles16 = groups * p.n_tiles;
+  if (tb == 16 && K >= 2 * 128 * kc && 2 * tiles16 <= sms)
+    return launch_f8i4<I4Cfg<2, 2, true>>(ta, tb_map, ts, P, (int)(2 * tiles16), s);
+  const int grid = (int)(upper < sms ? upper : sms);
   return launch_f8i4<I4Cfg<2, 2>>(ta, tb_map, ts, P, grid, s);
 }

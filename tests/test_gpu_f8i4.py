@@ -102,7 +102,8 @@ def run_f8i4(sizes, K, N, xq, sx, packed, sf, guard=8):
 
 
 F8I4_CASES = [
-    ([1, 0, 0, 2, 0, 1, 0, 0, 0, 3], 512, 256),      # 7 rows, sparse groups: 64-wide tiles
+    ([1, 0, 0, 2, 0, 1, 0, 0, 0, 3], 512, 256),      # 7 rows, sparse groups: CTA pairs, one slot each
+    ([2, 0, 5], 5120, 1024),                         # 7 rows, the sparse-M contraction: pairs, 10 slots each
     ([5, 0, 37, 30, 2], 384, 200),                   # K = 3 blocks (not a multiple of 4), N % 64 != 0
     ([0, 300, 1, 129, 250, 0, 0, 24], 256, 136),     # 128-wide tiles, group edges inside tiles
     ([700], 640, 320),                               # E = 1
@@ -123,7 +124,8 @@ def test_fwd_f8i4_against_oracle(sizes, K, N):
     assert_close(to_np(out[:M]), og.gmm_fwd(to_np(x), to_np(w), sizes, trans_b=True), 0.25, "f8i4 vs bf16")
 
 
-@pytest.mark.parametrize("sizes,K,N", [([3, 0, 4, 1], 384, 128), ([200, 140], 256, 256)])
+@pytest.mark.parametrize("sizes,K,N", [([3, 0, 4, 1], 384, 128), ([200, 140], 256, 256),
+                                       ([3, 0, 4, 1], 1024, 128)])   # 8 rows, K = 1024: CTA pairs split K
 def test_fwd_f8i4_integer_inputs_bit_exact(sizes, K, N):
     # x in {-3..3} (codes x * 128 exact), w integers in [-7, 7] with a 7 in every
     # block (scale 1): every product and partial sum is an integer below 2^24, so
