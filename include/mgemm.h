@@ -346,9 +346,11 @@ int mgemm_fill_args_quant_rowwise(const int64_t *group_sizes, int E, int64_t M, 
  *   x        bf16 [M, K] token rows sorted by expert, row stride ld_x elements
  *   w, sw    e4m3 [E, N, K] and fp32 [E * N] (as for mgemm_fwd)
  *   out      bf16 [M, N]; only the M rows are written
- *   status   int32, device: written with 0, MGEMM_STATUS_NEGATIVE_SIZE,
- *            MGEMM_STATUS_SUM_MISMATCH (then nothing else is written) or
- *            MGEMM_STATUS_TIMEOUT
+ *   status   int32, device, holding 0 or a negative value on entry (zeroed
+ *            once, it stays 0 while calls succeed): the call raises it to
+ *            MGEMM_STATUS_NEGATIVE_SIZE or MGEMM_STATUS_SUM_MISMATCH (then
+ *            nothing else is written) or MGEMM_STATUS_TIMEOUT, else to 0; a
+ *            caller that reads a nonzero status resets it before the next call
  * 1 <= M <= 16, E <= 1024, K % 128 == 0, N % 8 == 0, ld_x % 8 == 0, and the
  * token rows must fit on chip: ceil(M / 8) * 8 * K <= 150 KiB (else -1; use
  * the three calls).  Errors: -1 (sizes or NULL), -2 (alignment), -3 (E),

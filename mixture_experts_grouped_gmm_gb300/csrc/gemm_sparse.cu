@@ -48,8 +48,9 @@
 //               second CTA, the partial sums into the first's shared memory;
 //               else (the partner's partial added first) times 1 / sx[row] and
 //               1 / sw[e, column] in mgemm_fwd's order, bf16, direct stores.
-// Every wait is bounded; on expiry the kernel records MGEMM_STATUS_TIMEOUT in
-// *status, drains the copies and MMAs it issued, frees TMEM and returns.
+// Every wait is bounded; on expiry the kernel raises *status to
+// MGEMM_STATUS_TIMEOUT, drains the copies and MMAs it issued, frees TMEM and
+// returns.
 #include "gemm_launch.cuh"
 
 namespace mgemm {
@@ -243,7 +244,9 @@ __global__ void __launch_bounds__(kSpThreads, 1)
       S.bad = any_neg ? MGEMM_STATUS_NEGATIVE_SIZE : (total != p.M ? MGEMM_STATUS_SUM_MISMATCH : 0);
     }
     __syncthreads();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = S.bad;
+    // the status only rises (0 < validation codes < timeout), so this write and a timeout
+    // recorded by another CTA give the same result in either order
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicMax(p.status, S.bad);
   }
   const int kbc = (kchunks + KC - 1) / KC;  // stages per tile
   const int total = S.bad ? 0 : S.n_active * p.n_tiles;
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
   volatile int *vabort = &S.abort_flag;
   uint32_t issued = 0;
   auto timeout = [&]() {
-    atomicCAS(p.status, 0, MGEMM_STATUS_TIMEOUT);
+    atomicMax(p.status, MGEMM_STATUS_TIMEOUT);
     *vabort = 1;
   };
 
