@@ -167,3 +167,32 @@ def test_sparse_fwd_pairs_split_the_contraction(K):
         xq, sx = oq.quant_rowwise(to_np(x))
         want = og.gmm_fwd_fp8(xq, sx, to_np(wq).reshape(E, N, K), to_np(sw), [1])
         assert_close(to_np(out), want, FP8_TOL, "pairs vs oracle")
+
+
+@pytest.mark.parametrize("total_m", [1, 4])
+def test_sparse_fwd_graph_replay_follows_device_sizes(total_m):
+    # the launch reads the group sizes on the device: captured once in a CUDA graph, it follows
+    # new sizes written into the same tensor between replays (no host round trip)
+    E, K, N = 8, 1024, 512
+    wq, sw = weights(E, N, K, 9)
+    x = (torch.randn(total_m, K, generator=torch.Generator(device=DEV).manual_seed(2), device=DEV) * 2).to(BF)
+    gs = torch.zeros(E, dtype=torch.int64, device=DEV)
+    gs[0] = total_m
+    out = torch.empty(total_m, N, dtype=BF, device=DEV)
+    st = status()
+    B().mgemm_fwd_fp8_sparse(gs, E, x, wq, sw, out, st)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        B().mgemm_fwd_fp8_sparse(gs, E, x, wq, sw, out, st)
+    for sizes in ([0] * 5 + [total_m, 0, 0], [total_m - total_m // 2, 0, 0, total_m // 2, 0, 0, 0, 0]):
+        gs.copy_(torch.tensor(sizes, dtype=torch.int64))
+        st.fill_(0)
+        graph.replay()
+        ref = three_calls(gs, E, x, wq, sw, N)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        if paired(total_m, E, N):
+            assert_within_one_step(out, ref, f"replay with sizes {sizes}")
+        else:
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"replay with sizes {sizes}"
