@@ -515,9 +515,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           mbar_arrive_expect_tx(&full[stage], tx);
           ++issued;
           if (C::Mode == kModeRows && C::KC > 1) {
-            // [KC chunks][a_rows][128 B] and [KC chunks][bn][128 B] in one copy each
+            // [KC chunks][a_rows][128 B] and [KC chunks][bn][128 B] in one copy each; the gated
+            // form's B view adds a gate / up dimension, so a chunk lands as its bn / 2 gate rows
+            // followed by the matching up rows
             tma_load_3d(a, &tmA, &full[stage], 0, ti.a_row, kb * C::KC);
-            tma_load_4d(b, &tmB, &full[stage], 0, ti.b_row, kb * C::KC, ti.e);
+            if (p.gated)
+              tma_load_5d(b, &tmB, &full[stage], 0, ti.b_row, 0, kb * C::KC, ti.e);
+            else
+              tma_load_4d(b, &tmB, &full[stage], 0, ti.b_row, kb * C::KC, ti.e);
           } else if (C::Mode == kModeRows) {
             tma_load_2d(a, &tmA, &full[stage], kb * C::BK, ti.a_row);
             if (C::BMn) {

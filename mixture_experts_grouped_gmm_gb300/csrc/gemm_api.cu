@@ -245,6 +245,33 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
   if (routed_few) {  // bf16 routed rows, few per group: run-time rings
+    if (K % 64 == 0) {
+      // k-chunk views of the bf16 rows as bytes (2K per row): one box per operand and stage
+      const uint32_t kc = bn <= 64 ? 4 : 2;
+      bool maps = false;
+      if (gated) {
+        const uint64_t da[3] = {128, (uint64_t)M, (uint64_t)K * 2 / 128};
+        const uint64_t sa[2] = {(uint64_t)K * 2, 128};
+        const uint32_t ba[3] = {128, a_rows, kc};
+        // w [E, 2F, K]: {128 B, F rows of a half, gate / up, K / 64 chunks, E}
+        const uint64_t db[5] = {128, (uint64_t)gate_rows, 2, (uint64_t)K * 2 / 128, (uint64_t)E};
+        const uint64_t sb[4] = {(uint64_t)K * 2, (uint64_t)gate_rows * K * 2, 128, (uint64_t)N * K * 2};
+        const uint32_t bb[5] = {128, (uint32_t)bn / 2, 2, kc, 1};
+        CUtensorMap ma, mb;
+        maps = make_map(&ma, true, 3, x, da, sa, ba) && make_map(&mb, true, 5, w, db, sb, bb);
+        if (maps) {
+          ta = ma;
+          tb = mb;
+        }
+      } else {
+        maps = few_maps(&ta, &tb, x, M, K * 2, a_rows, w, N, E, bn, kc);
+      }
+      if (maps) {
+        if (bn <= 64) return gemm_bf16_rows_few_narrow_kc(ta, tb, to, p, grid, s);
+        if (bn <= 128) return gemm_bf16_rows_few_mid_kc(ta, tb, to, p, grid, s);
+        return gemm_bf16_rows_few_wide_kc(ta, tb, to, p, grid, s);
+      }
+    }
     if (bn <= 64) return gemm_bf16_rows_few_narrow(ta, tb, to, p, grid, s);
     if (bn <= 128) return gemm_bf16_rows_few_mid(ta, tb, to, p, grid, s);
     return gemm_bf16_rows_few_wide(ta, tb, to, p, grid, s);

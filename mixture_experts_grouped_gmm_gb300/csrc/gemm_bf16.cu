@@ -55,5 +55,19 @@ int gemm_bf16_rows_few_wide(const CUtensorMap &a, const CUtensorMap &b, const CU
                             int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<false, false, false, kModeRows, 256, 24, 1, false, 4, true, 1>>(a, b, o, p, grid, s);
 }
+// the same with K % 64 == 0: each operand's contraction blocks of a stage in one box of
+// consecutive 128-byte k-chunks (4 / 2 / 2 blocks per stage at 64 / 128 / 256 columns)
+int gemm_bf16_rows_few_narrow_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                                 const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 64, 24, 1, false, 4, true, 4>>(a, b, o, p, grid, s);
+}
+int gemm_bf16_rows_few_mid_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                              int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 128, 24, 1, false, 4, true, 2>>(a, b, o, p, grid, s);
+}
+int gemm_bf16_rows_few_wide_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                               int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 256, 24, 1, false, 4, true, 2>>(a, b, o, p, grid, s);
+}
 
 }  // namespace mgemm

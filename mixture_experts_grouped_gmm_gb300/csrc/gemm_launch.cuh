@@ -59,6 +59,13 @@ int gemm_bf16_rows_few_mid(const CUtensorMap &a, const CUtensorMap &b, const CUt
                            int grid, cudaStream_t s);
 int gemm_bf16_rows_few_wide(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                             int grid, cudaStream_t s);
+// the same in k-chunk boxes (K % 64 == 0; the gated form's B map has a gate / up dimension)
+int gemm_bf16_rows_few_narrow_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                                 const GemmParams &p, int grid, cudaStream_t s);
+int gemm_bf16_rows_few_mid_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                              int grid, cudaStream_t s);
+int gemm_bf16_rows_few_wide_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                               int grid, cudaStream_t s);
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)
 int gemm_bf16_rows_bmn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p, int grid,
                        cudaStream_t s);

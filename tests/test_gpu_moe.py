@@ -201,6 +201,7 @@ def test_fwd_gated_against_oracle(sizes, K, F):
     (37, 4, 4, 128, 256, True),    # top_k = E: every token in every expert
     (50, 1, 1, 256, 128, False),   # one expert, top-1, no renormalization
     (9, 3, 16, 136, 200, True),    # H, F not multiples of the 64-element k-block
+    (2, 2, 8, 1024, 2048, True),   # decode: k-chunk boxes (gate and up rows of a stage in one copy)
 ])
 def test_fused_moe_edges(T, k, E, H, F, renorm):
     from mixture_experts_grouped_gmm_gb300 import moe
