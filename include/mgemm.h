@@ -458,6 +458,32 @@ int mgemm_moe_align(const int32_t *topk_ids, int64_t numel, int E, int block_siz
                     mgemm_stream_t stream);
 
 /*
+ * mgemm_moe_route_align -- for decode-size batches, one launch doing the work
+ * of mgemm_topk_softmax, mgemm_moe_align and mgemm_fill_args (M = -1) in
+ * sequence [CMM]: every output is what those three calls write, bit for bit.
+ *   gating        float32 [T, E] (as for mgemm_topk_softmax), or NULL: the
+ *                 routing is skipped and topk_ids is read as the input ids
+ *                 (as for mgemm_moe_align, entries outside [0, E) are not
+ *                 placed); topk_weights is then not used
+ *   topk_weights  float32 [T, top_k], written when gating is given
+ *   topk_ids      int32 [T, top_k]: written when gating is given, read otherwise
+ *   sorted_ids, expert_ids, num_post_padded, group_sizes (may be NULL):
+ *                 as from mgemm_moe_align with numel = T * top_k
+ *   args          mgemm_args_bytes(E) bytes, 16-byte aligned: the args block of
+ *                 the padded group sizes (the sorted rows' grouped GEMMs)
+ * Limits: 1 <= E <= MGEMM_MAX_EXPERTS; 1 <= top_k (<= E when gating is given);
+ * T * top_k <= MGEMM_ROUTE_ALIGN_MAX_ENTRIES; 1 <= block_size <= 4096.  Larger
+ * batches return MGEMM_EINVAL: use the three calls, whose kernels spread over
+ * the SMs.  With T = 0 the gating, weights and ids may be NULL; the other
+ * outputs are still written (no entries: padding ids, empty groups).  One CTA
+ * of 1024 threads.
+ */
+#define MGEMM_ROUTE_ALIGN_MAX_ENTRIES 4096
+int mgemm_moe_route_align(const float *gating, int64_t T, int E, int top_k, int renormalize, int block_size,
+                          float *topk_weights, int32_t *topk_ids, int32_t *sorted_ids, int32_t *expert_ids,
+                          int32_t *num_post_padded, int64_t *group_sizes, void *args, mgemm_stream_t stream);
+
+/*
  * The routed (fused_moe) layer [CMM], built from mgemm_moe_align and these
  * calls: x rows are gathered into expert order, the grouped GEMM runs over the
  * sorted rows, and its epilogue scatters each row to its flat (token, slot)

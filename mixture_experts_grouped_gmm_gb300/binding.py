@@ -104,6 +104,10 @@ _SIGS = {
                                       ctypes.c_void_p, ctypes.c_void_p]),
     "mgemm_topk_softmax": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "mgemm_moe_route_align": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p]),
     "mgemm_num_sms": (ctypes.c_int, []),
     "mgemm_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mgemm_version": (ctypes.c_int, []),
@@ -370,6 +374,21 @@ def mgemm_topk_softmax(gating, top_k, renormalize, topk_weights, topk_ids):
     T, E = gating.shape
     _check(lib().mgemm_topk_softmax(_p(gating), T, E, int(top_k), int(bool(renormalize)), _p(topk_weights),
                                     _p(topk_ids), _stream(gating)), "mgemm_topk_softmax")
+
+
+MGEMM_ROUTE_ALIGN_MAX_ENTRIES = 4096
+
+
+def mgemm_moe_route_align(gating, T, E, top_k, renormalize, block_size, topk_weights, topk_ids, sorted_ids,
+                          expert_ids, num_post_padded, args, group_sizes=None):
+    """mgemm_topk_softmax + mgemm_moe_align + mgemm_fill_args(M = -1) in one
+    launch (T * top_k <= MGEMM_ROUTE_ALIGN_MAX_ENTRIES).  gating float32 [T, E],
+    or None: topk_ids int32 [T, top_k] is then the input."""
+    _cuda(gating, topk_weights, topk_ids, sorted_ids, expert_ids, num_post_padded, args, group_sizes)
+    _check(lib().mgemm_moe_route_align(_p(gating), int(T), int(E), int(top_k), int(bool(renormalize)),
+                                       int(block_size), _p(topk_weights), _p(topk_ids), _p(sorted_ids),
+                                       _p(expert_ids), _p(num_post_padded), _p(group_sizes), _p(args),
+                                       _stream(sorted_ids)), "mgemm_moe_route_align")
 
 
 def mgemm_num_sms():

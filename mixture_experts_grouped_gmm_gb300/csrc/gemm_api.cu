@@ -247,7 +247,8 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   if (routed_few) {  // bf16 routed rows, few per group: run-time rings
     if (K % 64 == 0) {
       // k-chunk views of the bf16 rows as bytes (2K per row): one box per operand and stage
-      const uint32_t kc = bn <= 64 ? 4 : 2;
+      // (four blocks at 64 columns, and at 128 with at most 8 rows per group; else two)
+      const uint32_t kc = bn <= 64 || (bn <= 128 && a_rows <= 8) ? 4 : 2;
       bool maps = false;
       if (gated) {
         const uint64_t da[3] = {128, (uint64_t)M, (uint64_t)K * 2 / 128};
@@ -268,7 +269,9 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
       }
       if (maps) {
         if (bn <= 64) return gemm_bf16_rows_few_narrow_kc(ta, tb, to, p, grid, s);
-        if (bn <= 128) return gemm_bf16_rows_few_mid_kc(ta, tb, to, p, grid, s);
+        if (bn <= 128)
+          return kc == 4 ? gemm_bf16_rows_few_mid_kc4(ta, tb, to, p, grid, s)
+                         : gemm_bf16_rows_few_mid_kc(ta, tb, to, p, grid, s);
         return gemm_bf16_rows_few_wide_kc(ta, tb, to, p, grid, s);
       }
     }

@@ -65,6 +65,11 @@ int gemm_bf16_rows_few_mid_kc(const CUtensorMap &a, const CUtensorMap &b, const 
                               int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<false, false, false, kModeRows, 128, 24, 1, false, 4, true, 2>>(a, b, o, p, grid, s);
 }
+// 128 columns with at most 8 rows per group: four blocks per stage (three 68 KB stages)
+int gemm_bf16_rows_few_mid_kc4(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                               const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<false, false, false, kModeRows, 128, 24, 1, false, 4, true, 4>>(a, b, o, p, grid, s);
+}
 int gemm_bf16_rows_few_wide_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                                int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<false, false, false, kModeRows, 256, 24, 1, false, 4, true, 2>>(a, b, o, p, grid, s);

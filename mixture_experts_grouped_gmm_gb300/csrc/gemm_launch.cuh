@@ -64,6 +64,8 @@ int gemm_bf16_rows_few_narrow_kc(const CUtensorMap &a, const CUtensorMap &b, con
                                  const GemmParams &p, int grid, cudaStream_t s);
 int gemm_bf16_rows_few_mid_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                               int grid, cudaStream_t s);
+int gemm_bf16_rows_few_mid_kc4(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
+                              int grid, cudaStream_t s);
 int gemm_bf16_rows_few_wide_kc(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                                int grid, cudaStream_t s);
 // bf16: A K-major rows, B MN-major ([E, K, N] weights)

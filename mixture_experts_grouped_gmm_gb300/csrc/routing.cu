@@ -21,6 +21,7 @@
 //          plus what earlier rounds placed -- the order the docstring shows,
 //          with no sort.
 #include "common.cuh"
+#include "fill_args.cuh"
 
 namespace mgemm {
 
@@ -228,15 +229,12 @@ __global__ void __launch_bounds__(256) topk_sum_kernel(const uint4 *__restrict__
 // this picks the same experts without rounding ties), equal logits going to the
 // lower expert id; the weights are exp(l - max) / sum, in fp32 with expf, and
 // divided by their sum when renormalize.  Lane l holds experts l, l + 32, ...
+// One warp routes token t; ids_sh, when given, receives the token's ids too.
 template <int NV>
-__global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ gating, int64_t T, int E,
-                                                             int top_k, int renormalize, float *__restrict__ weights,
-                                                             int32_t *__restrict__ ids) {
-  pdl_wait();
-  pdl_trigger();
+__device__ __forceinline__ void topk_softmax_token(const float *__restrict__ gating, int64_t t, int E, int top_k,
+                                                   int renormalize, float *__restrict__ weights,
+                                                   int32_t *__restrict__ ids, int32_t *ids_sh) {
   const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;  // whole warps leave together
   const float *row = gating + t * E;
   float v[NV];
   float m = -INFINITY;
@@ -288,6 +286,7 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restri
       const int r0 = r & ~31;
       if (lane <= r - r0) {
         ids[t * top_k + r0 + lane] = isel;
+        if (ids_sh) ids_sh[t * top_k + r0 + lane] = isel;
         weights[t * top_k + r0 + lane] = wsel;  // renormalized below
       }
     }
@@ -296,6 +295,156 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restri
     __syncwarp();
     for (int r = lane; r < top_k; r += 32) weights[t * top_k + r] = weights[t * top_k + r] / wsum;
   }
+}
+
+template <int NV>
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ gating, int64_t T, int E,
+                                                             int top_k, int renormalize, float *__restrict__ weights,
+                                                             int32_t *__restrict__ ids) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;  // whole warps leave together
+  topk_softmax_token<NV>(gating, t, E, top_k, renormalize, weights, ids, nullptr);
+}
+
+// mgemm_moe_route_align: the routing, the alignment and the args block of a
+// batch of at most MGEMM_ROUTE_ALIGN_MAX_ENTRIES entries in one CTA, so that a
+// decode-size batch takes one launch instead of five.  Each step computes what
+// its own kernel above computes (the same device code for the routing; the
+// same counts, scan, tail fill and round-wise stable placement for the
+// alignment; the args fill of mgemm_fill_args with M = -1), so the results are
+// the same bit for bit; the experts of the entries stay in shared memory
+// between the steps.  Thread e owns expert e in the scan (E <= NT threads);
+// the placement takes rounds of NT entries, one per thread.  NT is 128 for the
+// smallest batches (fewer threads make the many CTA barriers cheaper), else
+// 1024.
+__host__ __device__ constexpr size_t route_align_smem(int64_t n, int E, int NT) {
+  return 4 * (size_t)n + 4 * (size_t)E * (3 + NT / 32);
+}
+
+template <int NV, int NT>
+__global__ void __launch_bounds__(NT, 1)
+    route_align_kernel(const float *__restrict__ gating, int T, int E, int top_k, int renormalize, int block,
+                       int64_t cap, int max_blocks, float *__restrict__ weights, int32_t *__restrict__ ids,
+                       int32_t *__restrict__ sorted_ids, int32_t *__restrict__ expert_ids,
+                       int32_t *__restrict__ num_post, int64_t *__restrict__ group_sizes, uint8_t *__restrict__ args) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ int ra_sm[];
+  const int n = T * top_k;
+  int32_t *s_e = ra_sm;                            // [n]: expert of each entry
+  int *cnt = ra_sm + n;                            // [E]: entries of expert e
+  int *first = cnt + E;                            // [E]: first sorted position of expert e
+  int *run = first + E;                            // [E]: entries of e placed by earlier rounds
+  uint32_t *wcnt = reinterpret_cast<uint32_t *>(run + E);  // [warps][E]: (round << 16) | count
+  constexpr int kWarps = NT / 32;
+  __shared__ int warp_sum[kWarps];
+  __shared__ int total_sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += NT) {
+    cnt[e] = 0;
+    run[e] = 0;
+  }
+  for (int i = tid; i < kWarps * E; i += NT) wcnt[i] = 0xFFFFFFFFu;  // no round matches
+  // routing, one warp per token; or the caller's ids
+  if (gating) {
+    for (int t = warp; t < T; t += kWarps) topk_softmax_token<NV>(gating, t, E, top_k, renormalize, weights, ids, s_e);
+  } else {
+    for (int i = tid; i < n; i += NT) s_e[i] = ids[i];
+  }
+  __syncthreads();
+  // counts (entries outside [0, E) are not placed)
+  for (int i = tid; i < n; i += NT) {
+    const int e = s_e[i];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  // padded counts and their exclusive scan over the experts
+  const int c = tid < E ? cnt[tid] : 0;
+  const int pc = tid < E ? (c + block - 1) / block * block : 0;
+  int incl = pc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < kWarps ? warp_sum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane < kWarps) warp_sum[lane] = v;
+    if (lane == 31) total_sh = v;
+  }
+  __syncthreads();
+  const int start = incl - pc + (warp > 0 ? warp_sum[warp - 1] : 0);
+  const int total = total_sh;
+  if (tid < E) {
+    first[tid] = start;
+    for (int q = start + c; q < start + pc; ++q) sorted_ids[q] = n;  // the expert's padding
+    for (int b = start / block; b < (start + pc) / block; ++b) expert_ids[b] = tid;
+    if (group_sizes) group_sizes[tid] = pc;
+  }
+  if (tid == 0) *num_post = total;
+  for (int64_t q = total + tid; q < cap; q += NT) sorted_ids[q] = n;
+  for (int b = total / block + tid; b < max_blocks; b += NT) expert_ids[b] = -1;
+  __syncthreads();
+  // stable placement: an entry's place among its expert's entries is its rank
+  // in its warp plus the counts of earlier warps of the round plus what
+  // earlier rounds placed
+  const uint32_t below = (1u << lane) - 1u;
+  for (int r = 0; r * NT < n; ++r) {
+    const int i = r * NT + tid;
+    int e = -1;
+    if (i < n) {
+      e = s_e[i];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & below);
+    const bool leader = rank == 0;
+    if (e >= 0 && leader) wcnt[warp * E + e] = ((uint32_t)r << 16) | (uint32_t)__popc(same);
+    __syncthreads();
+    if (e >= 0) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) {
+        const uint32_t v = wcnt[w * E + e];
+        if ((v >> 16) == (uint32_t)r) before += (int)(v & 0xFFFFu);
+      }
+      sorted_ids[first[e] + run[e] + before + rank] = i;
+    }
+    __syncthreads();
+    if (e >= 0 && leader) atomicAdd(&run[e], __popc(same));
+    __syncthreads();
+  }
+  // the args block of the padded group sizes (M = -1: their sum)
+  fill_args_body<NT>((int64_t)pc, E, -1, args);
+}
+
+template <int NV, int NT>
+int launch_route_align(size_t smem, cudaStream_t s, const float *gating, int T, int E, int top_k, int renormalize,
+                       int block, int64_t cap, int max_blocks, float *weights, int32_t *ids, int32_t *sorted_ids,
+                       int32_t *expert_ids, int32_t *num_post, int64_t *group_sizes, uint8_t *args) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 0 || dev >= 64) return MGEMM_EINVAL;
+  if (!attr_done[dev]) {
+    rc = cuda_rc(cudaFuncSetAttribute(route_align_kernel<NV, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)route_align_smem(MGEMM_ROUTE_ALIGN_MAX_ENTRIES, NT, NT)),
+                 "cudaFuncSetAttribute");
+    if (rc) return rc;
+    attr_done[dev] = true;
+  }
+  return launch_pdl(route_align_kernel<NV, NT>, dim3(1), dim3(NT), smem, s, 1, "mgemm_moe_route_align launch",
+                    gating, T, E, top_k, renormalize, block, cap, max_blocks, weights, ids, sorted_ids, expert_ids,
+                    num_post, group_sizes, args);
 }
 
 }  // namespace mgemm
@@ -367,6 +516,49 @@ extern "C" int mgemm_silu_and_mul(const void *in, int64_t R, int64_t F, void *ou
   const int blocks = (int)(want < (int64_t)sms * 32 ? want : (int64_t)sms * 32);
   return launch_pdl(silu_mul_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, 1, "mgemm_silu_and_mul launch",
                     (const uint4 *)in, R, F / 8, (uint4 *)out);
+}
+
+extern "C" int mgemm_moe_route_align(const float *gating, int64_t T, int E, int top_k, int renormalize,
+                                     int block_size, float *topk_weights, int32_t *topk_ids, int32_t *sorted_ids,
+                                     int32_t *expert_ids, int32_t *num_post_padded, int64_t *group_sizes, void *args,
+                                     mgemm_stream_t stream) {
+  if (E < 1) return MGEMM_EINVAL;
+  if (E > MGEMM_MAX_EXPERTS) return MGEMM_ETOOMANY;
+  if (T < 0 || top_k < 1 || (gating && top_k > E) || block_size < 1 || block_size > 4096) return MGEMM_EINVAL;
+  if (T > MGEMM_ROUTE_ALIGN_MAX_ENTRIES || T * top_k > MGEMM_ROUTE_ALIGN_MAX_ENTRIES) return MGEMM_EINVAL;
+  const int64_t numel = T * top_k;
+  const int64_t cap = numel + (int64_t)E * (block_size - 1);
+  if (cap >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  // (no tokens: the ids and weights may be NULL)
+  if (!sorted_ids || !expert_ids || !num_post_padded || !args || (numel > 0 && !topk_ids) ||
+      (gating && numel > 0 && !topk_weights))
+    return MGEMM_EINVAL;
+  if (((uintptr_t)gating & 3) || ((uintptr_t)topk_weights & 3) || ((uintptr_t)topk_ids & 3) ||
+      ((uintptr_t)sorted_ids & 3) || ((uintptr_t)expert_ids & 3) || ((uintptr_t)num_post_padded & 3) ||
+      ((uintptr_t)group_sizes & 7) || ((uintptr_t)args & 15))
+    return MGEMM_EALIGN;
+  const int max_blocks = (int)(cap / block_size);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int nv = (E + 31) / 32;
+  uint8_t *a = static_cast<uint8_t *>(args);
+  // 128 threads for at most 8 tokens (two per warp) over at most 128 experts
+  const bool small = E <= 128 && T <= 8;
+#define MGEMM_RA_LAUNCH(NV, NT)                                                                                   \
+  return launch_route_align<NV, NT>(route_align_smem(numel, E, NT), s, gating, (int)T, E, top_k, renormalize,   \
+                                    block_size, cap, max_blocks, topk_weights, topk_ids, sorted_ids, expert_ids, \
+                                    num_post_padded, group_sizes, a)
+  if (small) {
+    if (nv <= 1) MGEMM_RA_LAUNCH(1, 128);
+    if (nv <= 2) MGEMM_RA_LAUNCH(2, 128);
+    MGEMM_RA_LAUNCH(4, 128);
+  }
+  if (nv <= 1) MGEMM_RA_LAUNCH(1, 1024);
+  if (nv <= 2) MGEMM_RA_LAUNCH(2, 1024);
+  if (nv <= 4) MGEMM_RA_LAUNCH(4, 1024);
+  if (nv <= 8) MGEMM_RA_LAUNCH(8, 1024);
+  if (nv <= 16) MGEMM_RA_LAUNCH(16, 1024);
+  MGEMM_RA_LAUNCH(32, 1024);
+#undef MGEMM_RA_LAUNCH
 }
 
 extern "C" int64_t mgemm_moe_align_workspace_bytes(int64_t numel, int E) {

@@ -26,9 +26,11 @@ the 2F-wide cache nor the second gather exists.
 ``fused_moe`` starts from the gating logits, as the page's does: the routing
 (softmax over the experts, top-k, optional renormalization) is
 ``mgemm_topk_softmax``.  ``fused_experts`` starts from routing weights and ids
-the caller already has.  This module only allocates buffers with torch and
-calls the binding; every step runs in the CUDA library, and nothing waits on
-the host.
+the caller already has.  For decode-size batches the routing, the alignment and
+the args block come from one launch (``mgemm_moe_route_align``, the same
+results bit for bit), so the layer takes five launches.  This module only
+allocates buffers with torch and calls the binding; every step runs in the
+CUDA library, and nothing waits on the host.
 """
 
 import torch
@@ -36,6 +38,10 @@ import torch
 from . import binding as B
 
 BLOCK = B.MGEMM_TILE_M  # rows per block: the GEMM's row tile
+# fused_moe routes batches of at most this many tokens in the one-CTA launch
+# (mgemm_moe_route_align, one warp per token); larger batches use the routing
+# kernel's one warp per token over many CTAs
+ROUTE_ALIGN_TOKENS = 16
 
 
 def align(topk_ids, E, block=BLOCK):
@@ -64,9 +70,52 @@ def route(gating_output, topk, renormalize):
     return w, i
 
 
+def route_align(gating_output, topk, renormalize, block=BLOCK):
+    """mgemm_moe_route_align from gating logits [T, E], with freshly allocated
+    outputs: (topk_weights, topk_ids, sorted_ids, expert_ids, num_post_padded,
+    group_sizes, args)."""
+    g = gating_output.to(torch.float32).contiguous()
+    T, E = g.shape
+    w = torch.empty(T, topk, dtype=torch.float32, device=g.device)
+    ids = torch.empty(T, topk, dtype=torch.int32, device=g.device)
+    return _route_align(g, w, ids, T, E, topk, renormalize, block)
+
+
+def align_args(topk_ids, E, block=BLOCK):
+    """mgemm_moe_route_align on given ids: (sorted_ids, expert_ids,
+    num_post_padded, group_sizes, args)."""
+    ids = topk_ids.to(torch.int32).contiguous()
+    T, topk = ids.shape
+    r = _route_align(None, None, ids, T, E, topk, False, block)
+    return r[2:]
+
+
+def _route_align(g, w, ids, T, E, topk, renormalize, block):
+    dev = ids.device
+    n = T * topk
+    cap, max_blocks = B.moe_align_buffer_sizes(n, E, block)
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(max_blocks, dtype=torch.int32, device=dev)
+    npp = torch.empty(1, dtype=torch.int32, device=dev)
+    gs = torch.empty(E, dtype=torch.int64, device=dev)
+    args = torch.empty(B.mgemm_args_bytes(E), dtype=torch.uint8, device=dev)
+    B.mgemm_moe_route_align(g, T, E, topk, renormalize, block, w, ids, sorted_ids, expert_ids, npp, args, gs)
+    return w, ids, sorted_ids, expert_ids, npp, gs, args
+
+
+def _check_layer(hidden_states, w1, w2):
+    if hidden_states.dtype != torch.bfloat16 or w1.dtype != torch.bfloat16 or w2.dtype != torch.bfloat16:
+        raise B.MgemmError("fused_moe takes bf16 activations and weights")
+
+
 def fused_moe(hidden_states, w1, w2, gating_output, topk, renormalize):
     """The page's fused_moe: route by gating_output [T, E] (top-k of the
     softmax, renormalized when asked), then fused_experts."""
+    T = gating_output.shape[0]
+    if T <= ROUTE_ALIGN_TOKENS and T * topk <= B.MGEMM_ROUTE_ALIGN_MAX_ENTRIES:
+        _check_layer(hidden_states, w1, w2)
+        tw, _, sorted_ids, _, npp, _, args = route_align(gating_output, topk, renormalize)
+        return _experts(hidden_states, w1, w2, tw, sorted_ids, npp, args, T, topk)
     topk_weights, topk_ids = route(gating_output, topk, renormalize)
     return fused_experts(hidden_states, w1, w2, topk_weights, topk_ids)
 
@@ -76,24 +125,33 @@ def fused_experts(hidden_states, w1, w2, topk_weights, topk_ids):
     topk_weights float32 [T, top_k]; topk_ids int [T, top_k], every id in
     [0, E) (as in fused_moe, whose caches are uninitialized: an entry that is
     not placed leaves its rows undefined).  Returns bf16 [T, H]."""
-    if hidden_states.dtype != torch.bfloat16 or w1.dtype != torch.bfloat16 or w2.dtype != torch.bfloat16:
-        raise B.MgemmError("fused_moe takes bf16 activations and weights")
+    _check_layer(hidden_states, w1, w2)
+    T, top_k = topk_ids.shape
+    E = w1.shape[0]
+    n = T * top_k
+    if n <= B.MGEMM_ROUTE_ALIGN_MAX_ENTRIES:
+        sorted_ids, _, npp, _, args = align_args(topk_ids, E)
+    else:
+        sorted_ids, _, npp, gs = align(topk_ids, E)
+        args = torch.empty(B.mgemm_args_bytes(E), dtype=torch.uint8, device=sorted_ids.device)
+        B.mgemm_fill_args(gs, E, -1, args)
+    return _experts(hidden_states, w1, w2, topk_weights, sorted_ids, npp, args, T, top_k)
+
+
+def _experts(hidden_states, w1, w2, topk_weights, sorted_ids, npp, args, T, top_k):
+    """The gather, the two GEMMs and the top-k sum over aligned entries."""
     x = hidden_states.contiguous()
     w1 = w1.contiguous()
     w2 = w2.contiguous()
-    T, H = x.shape
+    H = x.shape[1]
     E, F2, _ = w1.shape
     F = F2 // 2
-    top_k = topk_ids.shape[1]
     n = T * top_k
     dev = x.device
-    sorted_ids, _, npp, gs = align(topk_ids, E)
     cap = sorted_ids.numel()
     # rows the GEMMs may see: every entry, plus the padding of at most
     # min(E, n) experts (a bound known on the host; it sizes their tiles)
     rows = min(cap, n + min(E, n) * (BLOCK - 1))
-    args = torch.empty(B.mgemm_args_bytes(E), dtype=torch.uint8, device=dev)
-    B.mgemm_fill_args(gs, E, -1, args)
     bf = torch.bfloat16
     a1 = torch.empty(cap, H, dtype=bf, device=dev)
     B.mgemm_gather_rows(x, sorted_ids, npp, n, top_k, a1)

@@ -168,6 +168,28 @@ def test_host_checks_topk_softmax(lib):
     assert f(None, 0, 8, 2, 0, None, None, None) == 0   # no tokens: nothing to do
 
 
+def test_host_checks_moe_route_align(lib):
+    p = ctypes.c_void_p(0x10000)
+    f = lib.mgemm_moe_route_align
+    # (gating, T, E, top_k, renormalize, block, weights, ids, sorted, experts, npp, sizes, args, stream)
+    assert f(p, 4, 0, 1, 0, 128, p, p, p, p, p, None, p, None) == -1          # E < 1
+    assert f(p, 4, 1025, 1, 0, 128, p, p, p, p, p, None, p, None) == -3       # E > MGEMM_MAX_EXPERTS
+    assert f(p, 4, 8, 9, 0, 128, p, p, p, p, p, None, p, None) == -1         # top_k > E with logits
+    assert f(p, 4, 8, 0, 0, 128, p, p, p, p, p, None, p, None) == -1         # top_k < 1
+    assert f(p, 4, 8, 2, 0, 0, p, p, p, p, p, None, p, None) == -1           # block_size < 1
+    assert f(p, 4, 8, 2, 0, 4097, p, p, p, p, p, None, p, None) == -1        # block_size > 4096
+    assert f(p, -1, 8, 2, 0, 128, p, p, p, p, p, None, p, None) == -1        # T < 0
+    assert f(p, 2049, 8, 2, 0, 128, p, p, p, p, p, None, p, None) == -1      # T * top_k > 4096 entries
+    assert f(p, 4097, 8, 1, 0, 128, p, p, p, p, p, None, p, None) == -1      # T > 4096
+    assert f(p, 4, 8, 2, 0, 128, None, p, p, p, p, None, p, None) == -1      # logits without weights
+    assert f(p, 4, 8, 2, 0, 128, p, p, p, p, p, None, None, None) == -1      # no args block
+    assert f(None, 4, 8, 2, 0, 128, None, None, p, p, p, None, p, None) == -1  # no ids
+    assert f(p, 4, 8, 2, 0, 128, p, p, p, p, p, None, ctypes.c_void_p(0x10008), None) == -2  # args not 16-aligned
+    assert f(p, 4, 8, 2, 0, 128, p, p, p, p, p, ctypes.c_void_p(0x10004), p, None) == -2     # sizes not 8-aligned
+    # given ids (no logits): top_k may exceed E
+    assert f(None, 4, 2, 3, 0, 128, None, p, p, p, p, None, ctypes.c_void_p(0x10008), None) == -2
+
+
 def test_colwise_ld_bounds_the_padded_layout():
     # M rows in at most min(M, E) non-empty groups, each padded by fewer than
     # MGEMM_COL_PAD rows, rounded up to MGEMM_COL_PAD

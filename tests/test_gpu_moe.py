@@ -114,7 +114,8 @@ def test_topk_sum():
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
 
 
-@pytest.mark.parametrize("T,k,E,H,F", [(200, 2, 8, 256, 384), (3, 2, 8, 128, 128)])
+@pytest.mark.parametrize("T,k,E,H,F", [(200, 2, 8, 256, 384), (3, 2, 8, 128, 128),
+                                       (2100, 2, 8, 128, 128)])  # 4200 entries: the three-kernel alignment
 def test_fused_moe_layer(T, k, E, H, F):
     from mixture_experts_grouped_gmm_gb300 import moe
 
