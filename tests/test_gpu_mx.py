@@ -108,6 +108,7 @@ def assert_mx_close(got, ref, what=""):
     ([33] * 12, 640, 136),
     ([300, 0, 700, 260], 512, 400),            # groups averaging >= 256 rows: CTA pairs, partial pair tiles
     ([1024], 384, 192),                        # E = 1 on CTA pairs, one column tile
+    ([2500, 0, 2400, 4828], 256, 384),         # large groups, two 192-wide column tiles
 ])
 def test_fwd_mx_parity(sizes, K, N):
     got, ref = gemm_case(sizes, K, N, seed=len(sizes) * 100 + K + N)
