@@ -64,9 +64,10 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true", help="headline step only")
-    p.add_argument("--workload", choices=["all", "sparse", "deepseek", "mxfp8", "mixtral"], default="all",
+    p.add_argument("--workload", choices=["all", "sparse", "deepseek", "mxfp8", "mixtral", "decode"], default="all",
                    help="'all': headline line with every block; otherwise run only that block (profiling)")
-    p.add_argument("--tokens", type=int, default=16384, help="DeepSeek-shaped block: tokens (x top-6 rows)")
+    p.add_argument("--tokens", type=int, default=16384,
+                   help="DeepSeek-shaped block: tokens (x top-6 rows); decode block: tokens of the batch")
     p.add_argument("--experts", type=int, default=128, help="sparse-M block: number of experts")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return p.parse_args()
@@ -522,10 +523,21 @@ def routed_layer(torch, B, dev, pk, d):
     res = {"what": "moe.fused_experts(x, w1, w2, topk_weights, topk_ids), all steps on the device",
            "p50_us": round(t["p50_us"], 1), "tflops_routed_rows": round(tf, 1),
            "tensor_frac_routed": round(tf / pk["bf16_tflops"], 3)}
-    # decode-size batches of the whole layer from gating logits (routing included),
-    # replayed from a CUDA graph: the weights of the touched experts against HBM
+    res["decode_graph"] = decode_layer(torch, dev, pk, d, g)
+    return res
+
+
+def decode_layer(torch, dev, pk, d, g, sizes=(1, 4, 16, 64)):
+    """Decode-size batches of the whole layer from gating logits (routing
+    included), replayed from a CUDA graph: the weights of the touched experts
+    against HBM."""
+    from mixture_experts_grouped_gmm_gb300 import moe
+
+    H, F, E = d["H"], d["F"], d["E"]
+    w1 = d["w1"].view(E, 2 * F, H)
+    w2 = d["w2"].view(E, H, F)
     dec = []
-    for Td in (1, 4, 16, 64):
+    for Td in sizes:
         xd = torch.randn(Td, H, generator=g, device=dev).to(torch.bfloat16)
         gd = torch.randn(Td, E, generator=g, device=dev)
         f = lambda: moe.fused_moe(xd, w1, w2, gd, 2, True)
@@ -540,13 +552,24 @@ def routed_layer(torch, B, dev, pk, d):
         with torch.cuda.graph(graph):
             f()
         td = time_events(torch, graph.replay, 20)
+        # ten layers back to back in one graph: the steady rate of a decode loop
+        # (a replay timed alone also holds the graph's launch from the host)
+        graph10 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph10):
+            for _ in range(10):
+                f()
+        graph10.replay()
+        t10 = time_events(torch, graph10.replay, 10)
         _, tidd = moe.route(gd, 2, True)
         touched = int((torch.bincount(tidd.view(-1).long(), minlength=E) > 0).sum())
         wb = touched * 3 * F * H * 2
+        b2b = t10["mean_us"] / 10
         dec.append({"tokens": Td, "experts_touched": touched, "p50_us": round(td["p50_us"], 1),
-                    "hbm_frac": round(wb / (td["p50_us"] * 1e-6) / 1e9 / pk["hbm_gbs"], 3)})
-    res["decode_graph"] = dec
-    return res
+                    "hbm_frac": round(wb / (td["p50_us"] * 1e-6) / 1e9 / pk["hbm_gbs"], 3),
+                    "us_per_layer_back_to_back": round(b2b, 1),
+                    "hbm_frac_back_to_back": round(wb / (b2b * 1e-6) / 1e9 / pk["hbm_gbs"], 3)})
+        del graph, graph10
+    return dec
 
 
 def cpu_baseline_grin(seconds=10.0):
@@ -733,6 +756,11 @@ def run_block(a):
         out = deepseek_extra(torch, B, dev, pk, tokens=a.tokens, reps=max(1, a.steps))
     elif a.workload == "mxfp8":
         out = deepseek_mx_extra(torch, B, dev, pk, tokens=a.tokens, reps=max(1, a.steps))
+    elif a.workload == "decode":
+        from mixture_experts_grouped_gmm_gb300 import workloads
+
+        d = workloads.mixtral(device=dev)
+        out = decode_layer(torch, dev, pk, d, torch.Generator(device=dev).manual_seed(1), sizes=(a.tokens,))
     else:
         out = mixtral_extra(torch, B, dev, pk)
     print(json.dumps({"workload": a.workload, a.workload: out}), flush=True)
