@@ -549,6 +549,25 @@ int mgemm_fwd_gated(const void *args, const void *x, const void *w, void *out, i
                     int64_t group_rows_max, mgemm_stream_t stream);
 
 /*
+ * mgemm_fwd_gated_gather -- mgemm_fwd_gated whose sorted rows are read from
+ * the token rows through the sorted entry ids, as fused_moe_kernel loads A
+ * through sorted_token_ids [CMM]: sorted row i is x row sorted_ids[i] / top_k,
+ * or a row of zeros when sorted_ids[i] >= numel (padding), so the gathered
+ * copy of mgemm_gather_rows is not needed.  The outputs equal those of
+ * mgemm_gather_rows followed by mgemm_fwd_gated, bit for bit.
+ *   x           bf16 [x_rows, K] (the token rows), 16-byte aligned
+ *   sorted_ids, numel, top_k: as from mgemm_moe_align (sorted_ids holds at
+ *               least M entries)
+ *   args, w, out, M, K, F, E, group_rows_max: as for mgemm_fwd_gated
+ * For decode-size batches only: 1 <= group_rows_max <= 32 and K % 64 == 0;
+ * other shapes return MGEMM_ENOTSUP.  The GEMM's producer copies the rows
+ * itself (16-byte asynchronous copies into the swizzled operand layout).
+ */
+int mgemm_fwd_gated_gather(const void *args, const void *x, int64_t x_rows, const int32_t *sorted_ids, int64_t numel,
+                           int top_k, const void *w, void *out, int64_t M, int K, int F, int E,
+                           int64_t group_rows_max, mgemm_stream_t stream);
+
+/*
  * mgemm_silu_and_mul -- out[r, j] = silu(in[r, j]) * in[r, F + j] for in bf16
  * [R, 2F] and out bf16 [R, F] (vLLM's silu_and_mul as fused_moe applies it to
  * the first GEMM's output), silu(v) = v / (1 + exp(-v)), computed in fp32 and

@@ -98,6 +98,10 @@ _SIGS = {
     "mgemm_fwd_gated": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                        ctypes.c_void_p]),
+    "mgemm_fwd_gated_gather": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                              ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int64, ctypes.c_void_p]),
     "mgemm_silu_and_mul": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                           ctypes.c_void_p]),
     "mgemm_topk_sum": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
@@ -354,6 +358,15 @@ def mgemm_fwd_gated(args, x, w, out, M, K, F, E, group_rows_max=0):
     _check(lib().mgemm_fwd_gated(_p(args), _p(x), _p(w), _p(out), int(M), int(K), int(F), int(E),
                                  int(group_rows_max), _stream(out)),
            "mgemm_fwd_gated")
+
+
+def mgemm_fwd_gated_gather(args, x, sorted_ids, numel, top_k, w, out, M, K, F, E, group_rows_max):
+    """mgemm_fwd_gated over the token rows x [T, K] read through sorted_ids
+    (row sorted_ids[i] // top_k; ids >= numel are padding)."""
+    _cuda(args, x, sorted_ids, w, out)
+    _check(lib().mgemm_fwd_gated_gather(_p(args), _p(x), x.shape[0], _p(sorted_ids), int(numel), int(top_k), _p(w),
+                                        _p(out), int(M), int(K), int(F), int(E), int(group_rows_max), _stream(out)),
+           "mgemm_fwd_gated_gather")
 
 
 def mgemm_silu_and_mul(inp, out):

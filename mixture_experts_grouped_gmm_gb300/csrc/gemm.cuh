@@ -139,6 +139,7 @@ struct GemmCfg {
   // a run-time ring takes what the launch needs, up to the per-CTA limit
   static constexpr size_t SMEM_BYTES =
       kDynRing ? (size_t)227 * 1024 : FIXED_BYTES + (size_t)STAGES * (A_BYTES + B_BYTES);
+  static_assert(SMEM_BYTES <= (size_t)227 * 1024, "one CTA's shared memory");
 };
 
 struct GemmParams {
@@ -172,6 +173,15 @@ struct GemmParams {
   // columns n0 .. n0 + bn / 2 - 1.
   int gated;
   int gate_rows;
+  // bf16 rows mode, run-time ring with k-chunk boxes: with a_ids, row i of
+  // the sorted rows is row a_ids[i] / a_top_k of x (a_src, a_ld bytes per
+  // row; a_ids[i] >= a_numel: padding, a row of zeros)
+  const int32_t *a_ids;
+  int64_t a_numel;
+  int a_top_k;
+  const uint8_t *a_src;
+  int64_t a_ld;
+  int a_kbytes;  // 2 K: bytes of a row inside the contraction
 };
 
 struct TileInfo {
@@ -373,7 +383,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   // non-zero status) runs no role loop and goes straight to the teardown.
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], p.a_ids ? 1 + 32 : 1);  // gathered rows: + each producer lane's copies
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -434,7 +444,70 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint32_t issued = 0, sf_issued = 0;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (C::Mode == kModeRows && C::KC > 1 && !C::Pair && !C::Mx && p.a_ids) {
+      // Gathered A rows (few rows per group, a_rows <= 32): the whole warp
+      // produces.  Lane r copies sorted row r of the tile (x row a_ids[a_row +
+      // r] / a_top_k) in 16-byte asynchronous copies into the stage's
+      // [KC chunks][a_rows][128 B] layout with its 128-byte swizzle (unit u of
+      // row r at u ^ (r & 7)); padding rows and chunks past K are zeros (nothing
+      // read), as in the gathered copy.  Lane 0 also arms the full barrier with
+      // the weight bytes and loads the weight box; every lane's copies then
+      // count one arrival when they land.
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint32_t tx = C::KC * bn * 128;
+      const uint32_t a_off = (uint32_t)lane * 128u;
+      for (int j = 0; j * t_step < total && !*vabort; ++j) {
+        const int t = tile_of<C>(j, t_first, t_step);
+        if (t >= total) continue;
+        const TileInfo ti = decode_tile<C>(t, p, av, rank);
+        int xrow = -1;
+        if (lane < p.a_rows) {
+          const int32_t id = __ldg(p.a_ids + ti.a_row + lane);
+          if (id >= 0 && id < p.a_numel) xrow = id / p.a_top_k;
+        }
+        bool ok = true;
+        for (int kb = 0; kb < ti.kb_count; ++kb) {
+          if (!mbar_wait_warp(&empty[stage], phase ^ 1, vabort)) {
+            ok = false;
+            break;
+          }
+          uint8_t *b = stage_b(stage);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[stage], tx);
+            ++issued;
+            if (p.gated)
+              tma_load_5d(b, &tmB, &full[stage], 0, ti.b_row, 0, kb * C::KC, ti.e);
+            else
+              tma_load_4d(b, &tmB, &full[stage], 0, ti.b_row, kb * C::KC, ti.e);
+          }
+          if (lane < p.a_rows) {
+            const uint32_t a_s = smem_u32(stage_a(stage)) + a_off;
+#pragma unroll
+            for (int c = 0; c < C::KC; ++c) {
+              const int kx = (kb * C::KC + c) * 128;
+              const bool live = xrow >= 0 && kx < p.a_kbytes;
+              const uint8_t *src = p.a_src + (live ? (int64_t)xrow * p.a_ld + kx : 0);
+              const uint32_t dst = a_s + (uint32_t)(c * p.a_rows * 128), nb = live ? 16u : 0u;
+#pragma unroll
+              for (int u = 0; u < 8; ++u) cp_async16(dst + ((u ^ (lane & 7)) << 4), src + (live ? u * 16 : 0), nb);
+            }
+          }
+          cp_async_mbar_arrive(&full[stage]);
+          if (++stage == nst) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) {
+          if (lane == 0) {
+            set_status(av.status, MGEMM_STATUS_TIMEOUT);
+            raise_abort();
+          }
+          break;
+        }
+      }
+    } else if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       // with fewer than 128 token rows the A box is cut to them (rounded up to 8);
@@ -576,6 +649,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const uint32_t d_tmem = tmem_base + acc * C::BN_MAX;
       for (int kb = 0; kb < ti.kb_count; ++kb) {
         if (!mbar_wait_warp(&full[stage], phase, vabort)) { ok = false; break; }
+        if (C::Mode == kModeRows && C::KC > 1 && p.a_ids) fence_proxy_async_smem();  // rows written by cp.async
         // MXFP8: and the stage's scales are in tensor memory
         if (C::Mx && !mbar_wait_warp(&sfready[stage], phase, vabort)) { ok = false; break; }
         tc_fence_after();

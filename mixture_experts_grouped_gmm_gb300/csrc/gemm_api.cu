@@ -144,7 +144,8 @@ int mgemm::fwd_checks(int dtype, int trans_b, const void *x, const float *sx, co
 static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, const float *sx, const void *w,
                     const float *sw, void *out, int64_t M, int K, int N, int E, mgemm_stream_t stream,
                     const int32_t *row_map, int64_t map_limit, const float *row_weight, int gate_rows = 0,
-                    int64_t group_rows_max = 0, int64_t ld_wn = 0, int64_t ld_we = 0) {
+                    int64_t group_rows_max = 0, int64_t ld_wn = 0, int64_t ld_we = 0,
+                    const int32_t *a_ids = nullptr, int64_t a_numel = 0, int a_top_k = 1, int64_t a_src_rows = 0) {
   int rc = common_checks(args, dtype, M, K, N, E);
   if (rc) return rc;
   if ((rc = fwd_checks(dtype, trans_b, x, sx, w, sw, out, M, K, N, E))) return rc;
@@ -165,6 +166,8 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   if (gate_rows > 0 && group_rows_max > 0 && group_rows_max < rb) rb = group_rows_max;
   const bool routed_few = !fp8 && trans_b && (row_map || gate_rows > 0) && rb < 128 && M >= 128;
   if (routed_few) a_rows = (uint32_t)((rb > 0 ? rb : 1) + 7) / 8 * 8;
+  // gathered rows: the gated form with few rows per group and k-chunk boxes only
+  if (a_ids && !(routed_few && gate_rows > 0 && K % 64 == 0)) return MGEMM_ENOTSUP;
   {
     const uint64_t d[2] = {(uint64_t)K, (uint64_t)M};
     const uint64_t st[1] = {(uint64_t)K * es};
@@ -235,6 +238,12 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
   p.out = (__nv_bfloat16 *)out;
   p.rscale = sx;
   p.cscale = sw;
+  p.a_ids = a_ids;
+  p.a_numel = a_numel;
+  p.a_top_k = a_top_k;
+  p.a_src = (const uint8_t *)x;
+  p.a_ld = (int64_t)K * 2;
+  p.a_kbytes = K * 2;
   cudaStream_t s = (cudaStream_t)stream;
   if (pair) {
     const int64_t pupper = pair_tiles_estimate(M, E) * p.n_tiles + (M < E ? M : E) * p.n_tiles;
@@ -258,8 +267,10 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
         const uint64_t db[5] = {128, (uint64_t)gate_rows, 2, (uint64_t)K * 2 / 128, (uint64_t)E};
         const uint64_t sb[4] = {(uint64_t)K * 2, (uint64_t)gate_rows * K * 2, 128, (uint64_t)N * K * 2};
         const uint32_t bb[5] = {128, (uint32_t)bn / 2, 2, kc, 1};
+        // (gathered rows are copied by the producer; the A map then describes x's own rows)
+        const uint64_t dg[3] = {128, (uint64_t)(a_ids ? a_src_rows : M), (uint64_t)K * 2 / 128};
         CUtensorMap ma, mb;
-        maps = make_map(&ma, true, 3, x, da, sa, ba) && make_map(&mb, true, 5, w, db, sb, bb);
+        maps = make_map(&ma, true, 3, x, a_ids ? dg : da, sa, ba) && make_map(&mb, true, 5, w, db, sb, bb);
         if (maps) {
           ta = ma;
           tb = mb;
@@ -267,6 +278,7 @@ static int fwd_impl(const void *args, int dtype, int trans_b, const void *x, con
       } else {
         maps = few_maps(&ta, &tb, x, M, K * 2, a_rows, w, N, E, bn, kc);
       }
+      if (!maps && a_ids) return MGEMM_ECUDA;
       if (maps) {
         if (bn <= 64) return gemm_bf16_rows_few_narrow_kc(ta, tb, to, p, grid, s);
         if (bn <= 128)
@@ -337,6 +349,17 @@ extern "C" int mgemm_fwd_gated(const void *args, const void *x, const void *w, v
   if (group_rows_max < 0) return MGEMM_EINVAL;
   return fwd_impl(args, MGEMM_BF16, 1, x, nullptr, w, nullptr, out, M, K, 2 * F, E, stream, nullptr, 0, nullptr, F,
                   group_rows_max);
+}
+
+extern "C" int mgemm_fwd_gated_gather(const void *args, const void *x, int64_t x_rows, const int32_t *sorted_ids,
+                                      int64_t numel, int top_k, const void *w, void *out, int64_t M, int K, int F,
+                                      int E, int64_t group_rows_max, mgemm_stream_t stream) {
+  if (F < 1 || F % 8 || F > (1 << 29)) return F % 8 ? MGEMM_EALIGN : MGEMM_EINVAL;
+  if (!sorted_ids || x_rows < 1 || numel < 0 || top_k < 1) return MGEMM_EINVAL;
+  if ((uintptr_t)sorted_ids & 3) return MGEMM_EALIGN;
+  if (group_rows_max < 1 || group_rows_max > 32) return MGEMM_ENOTSUP;
+  return fwd_impl(args, MGEMM_BF16, 1, x, nullptr, w, nullptr, out, M, K, 2 * F, E, stream, nullptr, 0, nullptr, F,
+                  group_rows_max, 0, 0, sorted_ids, numel, top_k, x_rows);
 }
 
 extern "C" int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *sx, const uint8_t *w, const uint8_t *sw,

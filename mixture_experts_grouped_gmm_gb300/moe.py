@@ -28,7 +28,10 @@ the 2F-wide cache nor the second gather exists.
 ``mgemm_topk_softmax``.  ``fused_experts`` starts from routing weights and ids
 the caller already has.  For decode-size batches the routing, the alignment and
 the args block come from one launch (``mgemm_moe_route_align``, the same
-results bit for bit), so the layer takes five launches.  This module only
+results bit for bit), and for at most 32 entries (a hidden size that is a
+multiple of 64) the first GEMM reads the token rows through the sorted ids
+itself (``mgemm_fwd_gated_gather``), so the layer takes four launches.  This
+module only
 allocates buffers with torch and calls the binding; every step runs in the
 CUDA library, and nothing waits on the host.
 """
@@ -153,11 +156,15 @@ def _experts(hidden_states, w1, w2, topk_weights, sorted_ids, npp, args, T, top_
     # min(E, n) experts (a bound known on the host; it sizes their tiles)
     rows = min(cap, n + min(E, n) * (BLOCK - 1))
     bf = torch.bfloat16
-    a1 = torch.empty(cap, H, dtype=bf, device=dev)
-    B.mgemm_gather_rows(x, sorted_ids, npp, n, top_k, a1)
     a2 = torch.empty(cap, F, dtype=bf, device=dev)  # rows past the padded total are never read
     # every group holds at most n routed rows (decode-size batches: n < 128)
-    B.mgemm_fwd_gated(args, a1, w1, a2, rows, H, F, E, n)
+    if n <= 32 and H % 64 == 0:
+        # the first GEMM reads the token rows through the sorted ids itself
+        B.mgemm_fwd_gated_gather(args, x, sorted_ids, n, top_k, w1, a2, rows, H, F, E, n)
+    else:
+        a1 = torch.empty(cap, H, dtype=bf, device=dev)
+        B.mgemm_gather_rows(x, sorted_ids, npp, n, top_k, a1)
+        B.mgemm_fwd_gated(args, a1, w1, a2, rows, H, F, E, n)
     c3 = torch.empty(n, H, dtype=bf, device=dev)
     wts = topk_weights.to(torch.float32).contiguous().view(-1)
     B.mgemm_fwd_scatter(args, B.MGEMM_BF16, 1, a2, w2, c3, sorted_ids, n, wts, rows, F, H, E)

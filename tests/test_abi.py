@@ -190,6 +190,19 @@ def test_host_checks_moe_route_align(lib):
     assert f(None, 4, 2, 3, 0, 128, None, p, p, p, p, None, ctypes.c_void_p(0x10008), None) == -2
 
 
+def test_host_checks_fwd_gated_gather(lib):
+    p = ctypes.c_void_p(0x10000)
+    f = lib.mgemm_fwd_gated_gather
+    # (args, x, x_rows, sorted_ids, numel, top_k, w, out, M, K, F, E, group_rows_max, stream)
+    assert f(p, p, 4, None, 8, 2, p, p, 512, 256, 64, 8, 8, None) == -1     # no sorted ids
+    assert f(p, p, 0, p, 8, 2, p, p, 512, 256, 64, 8, 8, None) == -1        # no token rows
+    assert f(p, p, 4, p, 8, 0, p, p, 512, 256, 64, 8, 8, None) == -1        # top_k < 1
+    assert f(p, p, 4, ctypes.c_void_p(0x10002), 8, 2, p, p, 512, 256, 64, 8, 8, None) == -2  # ids misaligned
+    assert f(p, p, 4, p, 8, 2, p, p, 512, 256, 60, 8, 8, None) == -2        # F % 8 != 0
+    assert f(p, p, 4, p, 80, 2, p, p, 512, 256, 64, 8, 33, None) == -5      # more than 32 rows per group
+    assert f(p, p, 4, p, 8, 2, p, p, 512, 256, 64, 8, 0, None) == -5        # no bound on the rows
+
+
 def test_colwise_ld_bounds_the_padded_layout():
     # M rows in at most min(M, E) non-empty groups, each padded by fewer than
     # MGEMM_COL_PAD rows, rounded up to MGEMM_COL_PAD

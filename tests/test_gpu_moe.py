@@ -217,3 +217,56 @@ def test_fused_moe_edges(T, k, E, H, F, renorm):
     tw, tid = R.topk_softmax(gating.cpu().numpy(), k, renorm)
     ref = np.stack([R.fused_moe_token(to_np(x)[t], to_np(w1), to_np(w2), tid[t], tw[t]) for t in range(T)])
     assert_close(to_np(out), ref, BF16_TOL, "fused_moe edge case")
+
+
+@pytest.mark.parametrize("T,k,E,H,F", [
+    (1, 2, 8, 1024, 2048),     # one token: 8-row A slots, four blocks per stage
+    (4, 2, 8, 512, 384),       # a partial last column tile
+    (9, 3, 16, 256, 520),      # 27 entries: 32-row A slots, padding rows inside them
+    (12, 2, 2, 320, 256),      # 24 entries over 2 experts; K = 320: chunks past K are zeros
+    (16, 2, 64, 4096, 128),    # 32 entries over 64 experts (the largest group_rows_max, 32)
+    (5, 1, 3, 192, 1040),      # top-1, K = 192 (three of a stage's four chunks inside K)
+])
+def test_fwd_gated_gather_matches_gather_then_gated(T, k, E, H, F):
+    from mixture_experts_grouped_gmm_gb300 import moe
+
+    torch.manual_seed(T * 31 + H)
+    x = torch.randn(T, H, device=DEV).to(BF)
+    w1 = (0.05 * torch.randn(E, 2 * F, H, device=DEV)).to(BF)
+    tid = torch.stack([torch.randperm(E, device=DEV)[:k] for _ in range(T)]).to(torch.int32)
+    n = T * k
+    sid, _, npp, _, args = moe.align_args(tid, E)
+    cap = sid.numel()
+    rows = min(cap, n + min(E, n) * 127)
+    a1 = torch.empty(cap, H, dtype=BF, device=DEV)
+    B().mgemm_gather_rows(x, sid, npp, n, k, a1)
+    ref = sentinel_bf16((cap, F), DEV)
+    got = sentinel_bf16((cap, F), DEV)
+    B().mgemm_fwd_gated(args, a1, w1, ref, rows, H, F, E, n)
+    B().mgemm_fwd_gated_gather(args, x, sid, n, k, w1, got, rows, H, F, E, n)
+    torch.cuda.synchronize()
+    # the same rows in the same order (padding rows zero in both), the same MMAs: equal bits
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    # and the routed rows against the oracle
+    s = sid.cpu().numpy()
+    real = np.nonzero(s[:rows] < n)[0]
+    e_of = np.searchsorted(np.asarray(parse_args(args, E)["offsets"]), real, side="right") - 1
+    xr = to_np(x)[s[real] // k]
+    w = to_np(w1)
+    want = np.stack([R.silu_and_mul(xr[i:i + 1] @ w[e_of[i]].T)[0] for i in range(len(real))])
+    assert_close(to_np(got[torch.as_tensor(real, device=DEV)]), want, BF16_TOL, "gathered gated rows")
+
+
+def test_fwd_gated_gather_rejects_other_shapes():
+    E, F = 4, 64
+    sid = torch.zeros(512, dtype=torch.int32, device=DEV)
+    args = new_args(E, DEV)
+    out = torch.empty(512, F, dtype=BF, device=DEV)
+    x = torch.zeros(2, 136, dtype=BF, device=DEV)
+    w1 = torch.zeros(E, 2 * F, 136, dtype=BF, device=DEV)
+    with pytest.raises(B().MgemmError):   # K % 64 != 0
+        B().mgemm_fwd_gated_gather(args, x, sid, 3, 2, w1, out, 512, 136, F, E, 3)
+    x = torch.zeros(40, 256, dtype=BF, device=DEV)
+    w1 = torch.zeros(E, 2 * F, 256, dtype=BF, device=DEV)
+    with pytest.raises(B().MgemmError):   # group_rows_max > 32
+        B().mgemm_fwd_gated_gather(args, x, sid, 80, 2, w1, out, 512, 256, F, E, 33)
