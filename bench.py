@@ -909,30 +909,55 @@ def run_ours(a):
         gh = st.d["group_sizes"].cpu().pin_memory()
         e2e_steps = max(3, min(a.steps, 50))
 
-        def e2e_step():
-            x = xh.to(dev, non_blocking=True).requires_grad_(True)
-            w = wh.to(dev, non_blocking=True).requires_grad_(True)
-            g = gh.to(dev, non_blocking=True)
-            out = gmm(x, w, g)
-            loss = out.float().sum()
-            loss.backward()
-            return loss.item()
+        # Each step's inputs are copied on a copy stream into one of two device
+        # buffers while the previous step computes (a training loop's prefetch):
+        # every timed step still copies its x, w and sizes from pinned memory and
+        # reads its loss back.
+        copy_stream = torch.cuda.Stream(device=dev)
+        bufs = [tuple(torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (xh, wh, gh)) for _ in range(2)]
+        landed = [torch.cuda.Event() for _ in range(2)]
+        freed = [torch.cuda.Event() for _ in range(2)]
+        for ev in freed:
+            ev.record()
 
-        for _ in range(2):
-            e2e_step()
+        def prefetch(i):
+            b = i % 2
+            copy_stream.wait_event(freed[b])  # step i - 2 no longer reads the buffer
+            with torch.cuda.stream(copy_stream):
+                for dst, src in zip(bufs[b], (xh, wh, gh)):
+                    dst.copy_(src, non_blocking=True)
+            landed[b].record(copy_stream)
+
+        def e2e_steps_from(i0, n):
+            prefetch(i0)
+            for i in range(i0, i0 + n):
+                b = i % 2
+                torch.cuda.current_stream().wait_event(landed[b])
+                if i + 1 < i0 + n:
+                    prefetch(i + 1)
+                xb, wb, gb = bufs[b]
+                x = xb.detach().requires_grad_(True)
+                w = wb.detach().requires_grad_(True)
+                out = gmm(x, w, gb)
+                loss = out.float().sum()
+                loss.backward()
+                freed[b].record()
+                loss.item()
+
+        e2e_steps_from(0, 2)
         torch.cuda.synchronize()
         barrier()
         t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            e2e_step()
+        e2e_steps_from(2, e2e_steps)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, world, dist, dev)
         line["e2e"] = {"value": round(job_tflops(world, FLOP_STEP, e2e_ms), 2), "unit": "TFLOP/s",
                        "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                        "h2d_bytes_per_step": xh.numel() * 2 + wh.numel() * 2 + gh.numel() * 8,
                        "d2h_bytes_per_step": 4,
-                       "path": "gmm(x, w, group_sizes) autograd op; pinned host x, w, sizes copied in every step; "
-                               "loss.item() read back"}
+                       "path": "gmm(x, w, group_sizes) autograd op; pinned host x, w, sizes copied in every step "
+                               "(on a copy stream, into two device buffers in turn, each copy overlapping the "
+                               "previous step's compute); loss.item() read back every step"}
         del xh, wh
 
     if not a.no_extras:
