@@ -85,8 +85,9 @@ struct GemmCfg {
   // elements of every row, applied by block-scaled MMAs (no epilogue scales)
   static constexpr bool Mx = kMx;
   static constexpr bool Scaled = kFp8 && !kMx;  // FP8 with row / column scales in the epilogue
-  static_assert(!kMx || (kFp8 && !kAMn && !kBMn && !kPair && !kDynRing && (kBnMax == 128 || kBnMax == 192)),
-                "MXFP8: K-major operands, 128- or 192-wide tiles");
+  static_assert(!kMx || (kFp8 && !kAMn && !kBMn && !kPair && !kDynRing &&
+                          (kBnMax == 128 || kBnMax == 192 || kBnMax == 256)),
+                "MXFP8: K-major operands, 128-, 192- or 256-wide tiles");
   // MXFP8 scale rows per contraction block: the rows schedule's scale rows
   // are [rows][ld_sf] (16 bytes = four blocks per row); the experts schedule's
   // (wgrad) are k-block-major [blocks][rows][4 B] (one block per load)
@@ -116,6 +117,11 @@ struct GemmCfg {
                                    : 2 * BN_MAX <= 256 ? 256
                                                        : 512;
   static_assert(2 * BN_MAX <= 512, "two accumulators fit in TMEM");
+  // TMEM accumulators: two (the next tile's MMAs run while the epilogue
+  // drains the last), or one for 256-wide MXFP8 tiles, whose scale factors
+  // need the columns a second accumulator would take (the MMAs of the next
+  // tile then wait until the epilogue has read the accumulator)
+  static constexpr int NACC = (kMx && kBnMax == 256) ? 1 : 2;
   static constexpr int EPI = kEpiWarps;
   static_assert(EPI == 4 || EPI == 8, "one or two epilogue warps per TMEM lane quarter");
   static constexpr int HN = EPI / 4;         // epilogue warps per lane quarter
@@ -140,6 +146,7 @@ struct GemmCfg {
   static constexpr size_t SMEM_BYTES =
       kDynRing ? (size_t)227 * 1024 : FIXED_BYTES + (size_t)STAGES * (A_BYTES + B_BYTES);
   static_assert(SMEM_BYTES <= (size_t)227 * 1024, "one CTA's shared memory");
+  static_assert(!kMx || NACC * BN_MAX + STAGES * SF_COLS <= TMEM_COLS, "MXFP8: accumulators and scales fit in TMEM");
 };
 
 struct GemmParams {
@@ -679,7 +686,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // MXFP8: sub-block k of the stage reads byte k of the scale words
           // (the scale-factor ids of the instruction descriptor)
           if (lane == 0) {
-            const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * C::SF_COLS, sfb_t = sfa_t + 4;
+            const uint32_t sfa_t = tmem_base + C::NACC * C::BN_MAX + stage * C::SF_COLS, sfb_t = sfa_t + 4;
             const uint32_t abase = smem_u32(a), bbase = smem_u32(b);
 #pragma unroll
             for (int k = 0; k < C::KSTEPS; ++k) {
@@ -744,7 +751,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           mma_commit(&tfull[acc]);
       }
       __syncwarp();
-      if (++acc == 2) {
+      if (++acc == C::NACC) {
         acc = 0;
         acc_phase ^= 1;
       }
@@ -769,7 +776,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // holds block kb's four 32-element scales.  Tensor memory takes them as a
     // 512-byte tile per operand, row l holding rows l, l + 32, l + 64, l + 96
     // of the tile (byte 4 m + s: sub-block s of row l + 32 m), copied into
-    // each lane quarter at columns 2 BN_MAX + SF_COLS stage (A) and + 4 (B).  Lane
+    // each lane quarter at columns NACC BN_MAX + SF_COLS stage (A) and + 4 (B).  Lane
     // l builds row l of both tiles.  A stage's tiles and columns are reused
     // once its previous MMAs are done (its empty barrier, which the producer
     // waits for too); the copies' commit arms the stage's sfready barrier,
@@ -808,7 +815,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 0) {
           // column n of B reads the word at column sfb_t + n / 32: the second
           // B tile (columns 128 ..) sits 4 columns after the first
-          const uint32_t sfa_t = tmem_base + 2 * C::BN_MAX + stage * C::SF_COLS, sfb_t = sfa_t + 4;
+          const uint32_t sfa_t = tmem_base + C::NACC * C::BN_MAX + stage * C::SF_COLS, sfb_t = sfa_t + 4;
           tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(smem_u32(sf_tile(stage, 0))));
           tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(smem_u32(sf_tile(stage, 1))));
           if constexpr (C::SF_TILES_B > 1)
@@ -985,7 +992,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           if (has_acc) {
             if (nout == 0) release(acc);
-            if (++acc == 2) {
+            if (++acc == C::NACC) {
               acc = 0;
               acc_phase ^= 1;
             }
@@ -1094,7 +1101,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       if (has_acc) {
         if (!released) release(acc);  // a warp with no chunk of this tile (narrow tiles)
-        if (++acc == 2) {
+        if (++acc == C::NACC) {
           acc = 0;
           acc_phase ^= 1;
         }

@@ -378,8 +378,10 @@ extern "C" int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *s
   if (rc) return rc;
   const int sms = sm_count();
   if (sms <= 0) return MGEMM_ECUDA;
-  // 192-wide tiles (less operand traffic per FLOP) unless N fits one 128-wide tile
-  const int bn = N > 128 ? 192 : 128;
+  // the widest tile N needs (less operand traffic per FLOP): 256 columns (one
+  // TMEM accumulator: the scale factors take the second one's columns), else
+  // 192 or one 128-wide tile
+  const int bn = N > 192 ? 256 : N > 128 ? 192 : 128;
   CUtensorMap ta, tb, to, tsa, tsb;
   {
     const uint64_t d[2] = {(uint64_t)K, (uint64_t)M};
@@ -420,6 +422,7 @@ extern "C" int mgemm_fwd_mx(const void *args, const uint8_t *x, const uint8_t *s
   const int64_t upper = ((M + 127) / 128 + (M < E ? M : E)) * p.n_tiles;
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
+  if (bn == 256) return gemm_fp8_rows_mx256(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
   return bn == 192 ? gemm_fp8_rows_mx192(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream)
                    : gemm_fp8_rows_mx(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
 }
@@ -443,7 +446,8 @@ extern "C" int mgemm_wgrad_mx(const void *args, const uint8_t *x, const uint8_t 
   const void *xa = M > 0 ? (const void *)x : grad_w, *ga = M > 0 ? (const void *)grad_out : grad_w;
   const void *sxa = M > 0 ? (const void *)sx : grad_w, *sga = M > 0 ? (const void *)sgo : grad_w;
   const uint64_t L = M > 0 ? (uint64_t)ld : 128;
-  const int bn = 192;
+  // 256-wide tiles (one TMEM accumulator) when N needs more than 192 columns
+  const int bn = N > 192 ? 256 : 192;
   CUtensorMap ta, tb, to, tsa, tsb;
   {
     const uint64_t da[2] = {L, (uint64_t)K}, db[2] = {L, (uint64_t)N};
@@ -480,6 +484,7 @@ extern "C" int mgemm_wgrad_mx(const void *args, const uint8_t *x, const uint8_t 
   if (upper >= (int64_t(1) << 31)) return MGEMM_EINVAL;
   const int grid = grid_for(upper);
   if (grid < 0) return MGEMM_ECUDA;
+  if (bn == 256) return gemm_fp8_experts_mx256(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
   return gemm_fp8_experts_mx(ta, tb, to, tsa, tsb, p, grid, (cudaStream_t)stream);
 }
 

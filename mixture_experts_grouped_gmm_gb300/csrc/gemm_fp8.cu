@@ -53,6 +53,19 @@ int gemm_fp8_rows_mx192(const CUtensorMap &a, const CUtensorMap &b, const CUtens
                                                                                                   &sfa, &sfb);
 }
 
+// 256-wide tiles with one TMEM accumulator (three stages, eight epilogue warps)
+int gemm_fp8_rows_mx256(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
+                        const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeRows, 256, 3, 1, false, 8, false, 1, true>>(a, b, o, p, grid, s,
+                                                                                                 &sfa, &sfb);
+}
+
+int gemm_fp8_experts_mx256(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
+                           const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s) {
+  return launch_gemm<GemmCfg<true, false, false, kModeExperts, 256, 3, 1, false, 8, false, 1, true>>(
+      a, b, o, p, grid, s, &sfa, &sfb);
+}
+
 int gemm_fp8_experts_mx(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
                         const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<true, false, false, kModeExperts, 192, 4, 2, false, 4, false, 1, true>>(

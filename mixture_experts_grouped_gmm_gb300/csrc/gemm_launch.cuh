@@ -49,8 +49,12 @@ int gemm_fp8_rows_mx(const CUtensorMap &a, const CUtensorMap &b, const CUtensorM
                      const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
 int gemm_fp8_rows_mx192(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
                         const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
+int gemm_fp8_rows_mx256(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
+                        const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
 // MXFP8 wgrad: padded column-major x^T [K, ld] and grad_out^T [N, ld] with k-block-major scale rows
 int gemm_fp8_experts_mx(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
+                        const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
+int gemm_fp8_experts_mx256(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
                         const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);
 // bf16 routed rows with few per group: run-time rings (A slot of a_rows rows), K-major w
 int gemm_bf16_rows_few_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
