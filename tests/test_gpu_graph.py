@@ -117,10 +117,16 @@ def test_fp8_step_graph_replays():
             assert torch.equal(bufs[k].view(C, ld)[:, :P], b2[k].view(C, ld)[:, :P]), f"replay {rep}: {k}"
 
 
-def test_routed_layer_graph_replays_with_new_routing():
+@pytest.mark.parametrize("T,H", [
+    (40, 128),   # routing kernel, then the one-CTA alignment of the given ids
+    (1, 256),    # decode: routing + alignment + args in one launch, the first GEMM gathering its rows
+    (4, 256),
+    (16, 128),   # the largest batch of the one-launch routing and of the gathering GEMM (32 entries)
+])
+def test_routed_layer_graph_replays_with_new_routing(T, H):
     from mixture_experts_grouped_gmm_gb300 import moe
 
-    T, E, H, F, k = 40, 8, 128, 256, 2
+    E, F, k = 8, 256, 2
     x = torch.empty(T, H, dtype=BF, device=DEV)
     gating = torch.empty(T, E, device=DEV)
     w1 = (0.05 * torch.randn(E, 2 * F, H, device=DEV)).to(BF)
