@@ -312,10 +312,12 @@ def sparse_m_extra(torch, B, dev, pk, E=128, reps=100):
     return res
 
 
-def deepseek_extra(torch, B, dev, pk, tokens=16384, reps=10):
+def deepseek_extra(torch, B, dev, pk, tokens=16384, reps=10, hidden=2048, ffn=1408, down_proj=False):
+    """The DeepSeek-shaped FP8 step on the up projection (K = hidden 2048 -> N = ffn 1408), or
+    with down_proj on the down projection (K = ffn 1408 -> N = hidden 2048), same routing."""
     from mixture_experts_grouped_gmm_gb300 import workloads
 
-    d = workloads.deepseek(device=dev, T=tokens)
+    d = workloads.deepseek(device=dev, T=tokens, H=ffn if down_proj else hidden, F=hidden if down_proj else ffn)
     M, K, N, E = d["M"], d["K"], d["N"], d["E"]
     u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
     w_kn = d["w"]   # the master weights [E, K, N]: both FP8 weight operands are cast from it in the step
@@ -385,7 +387,7 @@ def deepseek_extra(torch, B, dev, pk, tokens=16384, reps=10):
         kern[n] = k
     total = sum(t.values())
     out = {"shape": f"M={M} (16384 tokens x top-6, Zipf 1.2, {int((d['group_sizes'] == 0).sum())} empty groups) "
-                    f"K={K} N={N} E={E}, e4m3 operands, bf16 outputs; both weight casts run in the timed step from "
+                    f"K={K} N={N} E={E} ({'down' if down_proj else 'up'} projection), e4m3 operands, bf16 outputs; both weight casts run in the timed step from "
                     "the one bf16 master w [E, K, N] (forward operand: per-group colwise cast of w viewed [E K, N], "
                     "read in place by mgemm_fwd_fp8_strided; dgrad operand: rowwise cast); the weight groups' args "
                     "block (E groups of K rows, constant) is filled once outside it",
@@ -966,6 +968,8 @@ def run_ours(a):
         line["sparse_m_fp8"] = sparse_m_extra(torch, B, dev, pk)
         torch.cuda.empty_cache()
         line["deepseek_fp8_step"] = deepseek_extra(torch, B, dev, pk)
+        torch.cuda.empty_cache()
+        line["deepseek_fp8_step_down_proj"] = deepseek_extra(torch, B, dev, pk, down_proj=True)
         torch.cuda.empty_cache()
         line["deepseek_mxfp8"] = deepseek_mx_extra(torch, B, dev, pk)
         torch.cuda.empty_cache()

@@ -119,8 +119,10 @@ def test_sparse_m_fp8_full_size(sparse_weights, total_m):
     assert_close(got, ref, FP8_TOL, f"sparse-M fwd total_M={total_m}")
 
 
-def test_deepseek_fp8_step_full_size():
-    d = workloads.deepseek(device=DEV)
+@pytest.mark.parametrize("proj", ["up", "down"])
+def test_deepseek_fp8_step_full_size(proj):
+    # the up projection (K = 2048 -> N = 1408) and the down projection (K = 1408 -> N = 2048)
+    d = workloads.deepseek(device=DEV, **({} if proj == "up" else {"H": 1408, "F": 2048}))
     M, K, N, E = d["M"], d["K"], d["N"], d["E"]
     sizes = d["group_sizes"].cpu().numpy()
     assert (sizes == 0).sum() >= 1
