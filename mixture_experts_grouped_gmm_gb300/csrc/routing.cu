@@ -316,9 +316,9 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restri
 // alignment; the args fill of mgemm_fill_args with M = -1), so the results are
 // the same bit for bit; the experts of the entries stay in shared memory
 // between the steps.  Thread e owns expert e in the scan (E <= NT threads);
-// the placement takes rounds of NT entries, one per thread.  NT is 128 for the
-// smallest batches (fewer threads make the many CTA barriers cheaper), else
-// 1024.
+// the placement takes rounds of NT entries, one per thread.  NT is 128 or 256
+// for the smallest batches (fewer threads make the many CTA barriers cheaper),
+// else 1024.
 __host__ __device__ constexpr size_t route_align_smem(int64_t n, int E, int NT) {
   return 4 * (size_t)n + 4 * (size_t)E * (3 + NT / 32);
 }
@@ -541,8 +541,9 @@ extern "C" int mgemm_moe_route_align(const float *gating, int64_t T, int E, int 
   cudaStream_t s = (cudaStream_t)stream;
   const int nv = (E + 31) / 32;
   uint8_t *a = static_cast<uint8_t *>(args);
-  // 128 threads for at most 8 tokens (two per warp) over at most 128 experts
-  const bool small = E <= 128 && T <= 8;
+  // 128 threads for at most 8 tokens (two per warp) over at most 128 experts, 256 for at most
+  // 8 tokens over at most 256 experts
+  const bool small = E <= 128 && T <= 8, mid = E <= 256 && T <= 8;
 #define MGEMM_RA_LAUNCH(NV, NT)                                                                                   \
   return launch_route_align<NV, NT>(route_align_smem(numel, E, NT), s, gating, (int)T, E, top_k, renormalize,   \
                                     block_size, cap, max_blocks, topk_weights, topk_ids, sorted_ids, expert_ids, \
@@ -552,6 +553,7 @@ extern "C" int mgemm_moe_route_align(const float *gating, int64_t T, int E, int 
     if (nv <= 2) MGEMM_RA_LAUNCH(2, 128);
     MGEMM_RA_LAUNCH(4, 128);
   }
+  if (mid) MGEMM_RA_LAUNCH(8, 256);
   if (nv <= 1) MGEMM_RA_LAUNCH(1, 1024);
   if (nv <= 2) MGEMM_RA_LAUNCH(2, 1024);
   if (nv <= 4) MGEMM_RA_LAUNCH(4, 1024);

@@ -201,6 +201,9 @@ def _check_route_align(gating, ids, T, E, k, renorm, block):
     (8, 128, 8, True, 128, "normal"),     # the 128-thread form's limits (8 tokens, 128 experts)
     (6, 100, 3, False, 16, "normal"),     # 128 threads, E not a multiple of 32
     (9, 128, 8, True, 128, "normal"),     # one token past it: 1024 threads
+    (8, 256, 8, True, 128, "normal"),     # the 256-thread form's limits (DeepSeek-V3-like routing)
+    (1, 160, 6, False, 64, "ties"),       # 256 threads, E not a power of two
+    (9, 256, 8, True, 128, "normal"),     # one token past it: 1024 threads
     (16, 64, 6, True, 128, "normal"),     # DeepSeek-MoE routing, decode batch
     (64, 128, 8, False, 128, "normal"),   # 512 entries over 128 experts
     (2048, 8, 2, True, 128, "normal"),    # 4096 entries: the largest batch (four placement rounds)
