@@ -313,6 +313,31 @@ int mgemm_wgrad(const void *args, int dtype, const void *x, const float *sx, con
                 const float *sgo, void *grad_w, int64_t M, int K, int N, int E, int64_t ld, mgemm_stream_t stream);
 
 /*
+ * mgemm_dgrad_wgrad -- the bf16 backward of the grouped GEMM, both gradients:
+ * grad_x exactly as mgemm_dgrad(MGEMM_BF16, grad_out, w [E, K, N]) and grad_w
+ * exactly as mgemm_wgrad(MGEMM_BF16, x, grad_out), bit for bit ("Support
+ * GPU-resident batch sizes", benchmark script: the backward of gmm after
+ * out.sum()).  Where the groups are small enough that dgrad streams the
+ * weights from HBM while wgrad is bound by its grad_w stores, both run in one
+ * launch on disjoint sets of CTAs (a host-side model of the two sizes picks
+ * the split) and overlap; otherwise the two calls run one after the other on
+ * the stream.  Same args block as both; no other device memory.
+ *   grad_out bf16 [M, N]; w bf16 [E, K, N]; x bf16 [M, K] (row-major)
+ *   grad_x   bf16 [M, K]; grad_w bf16 [E, K, N] (every element written)
+ * With M == 0 only grad_w is written (zeros) and grad_out, x, grad_x may be
+ * NULL.  Errors as for the two calls (K % 8 == 0, N % 8 == 0, 16-byte aligned
+ * pointers).
+ */
+int mgemm_dgrad_wgrad(const void *args, const void *grad_out, const void *w, const void *x, void *grad_x,
+                      void *grad_w, int64_t M, int K, int N, int E, mgemm_stream_t stream);
+
+/* The number of CTAs mgemm_dgrad_wgrad gives to dgrad in its one-launch form
+ * for these sizes (the rest of the SMs run wgrad), or 0 when it makes the two
+ * calls in turn; negative MGEMM_E* for invalid sizes.  Host-side (reads the
+ * current device's SM count once). */
+int mgemm_dgrad_wgrad_split(int64_t M, int K, int N, int E);
+
+/*
  * mgemm_fill_args_quant_rowwise -- mgemm_fill_args and mgemm_quant_rowwise of
  * the token rows in one launch (the two independent steps before an FP8
  * forward: "Support GPU-resident batch sizes", the argument fill; "[moe

@@ -81,6 +81,10 @@ _SIGS = {
     "mgemm_wgrad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p]),
+    "mgemm_dgrad_wgrad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "mgemm_dgrad_wgrad_split": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "mgemm_fwd_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
@@ -306,6 +310,22 @@ def mgemm_wgrad(args, dtype, x, sx, grad_out, sgo, grad_w, M, K, N, E, ld=None):
         ld = x.numel() // K if dtype == MGEMM_FP8_E4M3 and x is not None else 0
     _check(lib().mgemm_wgrad(_p(args), int(dtype), _p(x), _p(sx), _p(grad_out), _p(sgo), _p(grad_w), int(M),
                              int(K), int(N), int(E), int(ld), _stream(grad_w)), "mgemm_wgrad")
+
+
+def mgemm_dgrad_wgrad(args, grad_out, w, x, grad_x, grad_w, M, K, N, E):
+    """bf16 backward with w [E, K, N]: grad_x (as mgemm_dgrad) and grad_w (as mgemm_wgrad), in one launch
+    where the two share the GPU better than they take turns."""
+    _cuda(args, grad_out, w, x, grad_x, grad_w)
+    _check(lib().mgemm_dgrad_wgrad(_p(args), _p(grad_out), _p(w), _p(x), _p(grad_x), _p(grad_w), int(M), int(K),
+                                   int(N), int(E), _stream(grad_w)), "mgemm_dgrad_wgrad")
+
+
+def mgemm_dgrad_wgrad_split(M, K, N, E):
+    """CTAs mgemm_dgrad_wgrad gives dgrad in one launch (0: two launches in turn)."""
+    rc = lib().mgemm_dgrad_wgrad_split(int(M), int(K), int(N), int(E))
+    if rc < 0:
+        _check(rc, "mgemm_dgrad_wgrad_split")
+    return rc
 
 
 def mgemm_fwd_noalloc(group_sizes, dtype, trans_b, x, sx, w, sw, out, M, K, N, E):

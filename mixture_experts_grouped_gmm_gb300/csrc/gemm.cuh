@@ -341,11 +341,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// One CTA's share of a launch: CTA cta of ncta (CTA pairs: the cluster's
+// place among the clusters) takes tiles cta, cta + ncta, ...
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1)
-    mgemm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmSFA,
-                      const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+__device__ __forceinline__ void gemm_cta(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmOut,
+                                         const CUtensorMap &tmSFA, const CUtensorMap &tmSFB, const GemmParams &p,
+                                         int cta, int ncta) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // ring stages, then the epilogue staging [EPI warps][NBUF buffers][32 x 128 B], then barriers
@@ -381,8 +382,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   // sequence and leave (or stay) together
   const uint32_t rank = C::Pair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
-  const int t_first = C::Pair ? (int)cluster_id_x() : (int)blockIdx.x;
-  const int t_step = C::Pair ? (int)ncluster_x() : (int)gridDim.x;
+  const int t_first = C::Pair ? (int)cluster_id_x() : cta;
+  const int t_step = C::Pair ? (int)ncluster_x() : ncta;
 
   // Set-up (barriers, tensor memory, descriptor prefetch) reads nothing an
   // earlier kernel writes, so it runs before the wait for the previous grid of
@@ -1145,6 +1146,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
   if constexpr (C::Pair) cluster_sync();  // neither CTA leaves while the other may still address it
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    mgemm_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmSFA,
+                      const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ GemmParams p) {
+  gemm_cta<C>(tmA, tmB, tmOut, tmSFA, tmSFB, p, (int)blockIdx.x, (int)gridDim.x);
+}
+
+// Two GEMMs of one backward pass in one launch: CTAs [0, split) run the
+// first (C0, maps a0 b0 o0, params p0), the others the second.  Neither reads
+// what the other writes; a memory-bound weight stream (dgrad) and an
+// epilogue-bound one (wgrad's grad_w stores) then share the SMs and HBM
+// instead of taking turns.
+template <class C0, class C1>
+__global__ void __launch_bounds__(C0::THREADS, 1)
+    mgemm_dual_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap b0,
+                      const __grid_constant__ CUtensorMap o0, const __grid_constant__ CUtensorMap a1,
+                      const __grid_constant__ CUtensorMap b1, const __grid_constant__ CUtensorMap o1,
+                      const __grid_constant__ GemmParams p0, const __grid_constant__ GemmParams p1, int split) {
+  static_assert(C0::THREADS == C1::THREADS && !C0::Pair && !C1::Pair && !C0::Mx && !C1::Mx,
+                "both forms run the same warps, one CTA each");
+  if ((int)blockIdx.x < split)
+    gemm_cta<C0>(a0, b0, o0, a0, a0, p0, (int)blockIdx.x, split);
+  else
+    gemm_cta<C1>(a1, b1, o1, a1, a1, p1, (int)blockIdx.x - split, (int)gridDim.x - split);
 }
 
 }  // namespace mgemm

@@ -619,3 +619,118 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
   if (grid < 0) return MGEMM_ECUDA;
   return gemm_bf16_experts(ta, tb, to, p, grid, s);
 }
+
+// CTAs given to dgrad when it shares one launch with wgrad, or 0 when two
+// launches are expected to do as well.  A makespan model with rates measured
+// on GB300 for the bf16 forms: a wgrad tile's epilogue stores ~34 GB/s of
+// grad_w per SM; a dgrad CTA streams weights at up to ~60 GB/s; HBM serves
+// ~6 TB/s to both; the tensor cores give ~12 TFLOP/s per SM.  Only the
+// memory-bound regime is considered (groups of at most 256 rows on average),
+// where dgrad streams the weights from HBM and wgrad is bound by its stores:
+// two different limits, so sharing the SMs beats taking turns.
+static int dual_split(int64_t M, int K, int N, int E, int bn_d, int bn_w, int sms) {
+  if (M <= 0 || M > 256 * (int64_t)E || sms < 4) return 0;
+  const double rw = 34e9, rd = 60e9, hbm = 6e12, tc = 12e12;
+  const double tiles_d = (double)rows_tiles_estimate(M, E) * ((K + bn_d - 1) / bn_d);
+  const double tiles_w = (double)E * ((K + 127) / 128) * ((N + bn_w - 1) / bn_w);
+  const double rows_e = (double)M / E;
+  const double tile_d = fmax((double)bn_d * N * 2 / rd, 2.0 * 128 * bn_d * N / tc);
+  const double tile_w = fmax(128.0 * bn_w * 2 / rw, 2.0 * 128 * bn_w * rows_e / tc);
+  const double bytes_d = (double)(M < E ? M : E) * K * N * 2;
+  auto t_d = [&](int g, int gw) {
+    const double share = fmax(hbm - gw * rw, 0.1 * hbm);
+    return fmax(ceil(tiles_d / g) * tile_d, bytes_d / share);
+  };
+  auto t_w = [&](int g) { return ceil(tiles_w / g) * tile_w; };
+  const double seq = t_d(sms, 0) + t_w(sms);
+  int best = 0;
+  double best_t = seq;
+  for (int g = 1; g < sms; ++g) {
+    const double t = fmax(t_d(g, sms - g), t_w(sms - g));
+    if (t < best_t) {
+      best_t = t;
+      best = g;
+    }
+  }
+  return best;
+}
+
+extern "C" int mgemm_dgrad_wgrad_split(int64_t M, int K, int N, int E) {
+  int rc = size_checks(MGEMM_BF16, M, K, N, E);
+  if (rc) return rc;
+  const int sms = sm_count();
+  if (sms <= 1) return MGEMM_ECUDA;
+  const int bn_d = choose_bn(rows_tiles_estimate(M, E), K);
+  const int bn_w = choose_bn((int64_t)E * ((K + 127) / 128), N);
+  return dual_split(M, K, N, E, bn_d, bn_w, sms);
+}
+
+extern "C" int mgemm_dgrad_wgrad(const void *args, const void *grad_out, const void *w, const void *x, void *grad_x,
+                                 void *grad_w, int64_t M, int K, int N, int E, mgemm_stream_t stream) {
+  int rc = common_checks(args, MGEMM_BF16, M, K, N, E);
+  if (rc) return rc;
+  if (M == 0) return mgemm_wgrad(args, MGEMM_BF16, x, nullptr, grad_out, nullptr, grad_w, M, K, N, E, 0, stream);
+  if (!grad_out || !w || !x || !grad_x || !grad_w) return MGEMM_EINVAL;
+  if (!aligned16(grad_out) || !aligned16(w) || !aligned16(x) || !aligned16(grad_x) || !aligned16(grad_w))
+    return MGEMM_EALIGN;
+  if ((rc = ensure_context())) return rc;
+  const int sms = sm_count();
+  if (sms <= 1) return MGEMM_ECUDA;
+  const int bn_d = choose_bn(rows_tiles_estimate(M, E), K);
+  const int mt_w = (K + 127) / 128;
+  const int bn_w = choose_bn((int64_t)E * mt_w, N);
+  const int split = dual_split(M, K, N, E, bn_d, bn_w, sms);
+  if (split == 0) {
+    rc = mgemm_dgrad(args, MGEMM_BF16, grad_out, nullptr, w, nullptr, grad_x, M, K, N, E, stream);
+    if (rc) return rc;
+    return mgemm_wgrad(args, MGEMM_BF16, x, nullptr, grad_out, nullptr, grad_w, M, K, N, E, 0, stream);
+  }
+  // dgrad: grad_out [M, N] (A, contraction over N) and w [E, K, N] (B, K-major), as in mgemm_dgrad
+  CUtensorMap da, db, dout;
+  const uint32_t a_rows = M < 128 ? (uint32_t)((M + 7) / 8 * 8) : 128u;
+  {
+    const uint64_t d[2] = {(uint64_t)N, (uint64_t)M};
+    const uint64_t st[1] = {(uint64_t)N * 2};
+    const uint32_t box[2] = {64, a_rows};
+    if (!make_map(&da, false, 2, grad_out, d, st, box)) return MGEMM_ECUDA;
+  }
+  {
+    const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
+    const uint64_t st[2] = {(uint64_t)N * 2, (uint64_t)K * N * 2};
+    const uint32_t box[3] = {64, (uint32_t)bn_d, 1};
+    if (!make_map(&db, false, 3, w, d, st, box)) return MGEMM_ECUDA;
+  }
+  if (!make_out_map(&dout, grad_x, M, K)) return MGEMM_ECUDA;
+  GemmParams pd{};
+  pd.args = (const uint8_t *)args;
+  pd.E = E;
+  pd.bn = bn_d;
+  pd.idesc = make_idesc(1u, false, false, 128, bn_d);
+  pd.a_rows = (int)a_rows;
+  pd.n_tiles = (K + bn_d - 1) / bn_d;
+  pd.Kc = N;
+  pd.Nout = K;
+  pd.out = (__nv_bfloat16 *)grad_x;
+  // wgrad: x [M, K] (A) and grad_out [M, N] (B), both MN-major, as in mgemm_wgrad
+  CUtensorMap wa, wb, wout;
+  {
+    const uint64_t dx[2] = {(uint64_t)K, (uint64_t)M}, dg[2] = {(uint64_t)N, (uint64_t)M};
+    const uint64_t sx[1] = {(uint64_t)K * 2}, sg[1] = {(uint64_t)N * 2};
+    const uint32_t box[2] = {64, 64};
+    if (!make_map(&wa, false, 2, x, dx, sx, box)) return MGEMM_ECUDA;
+    if (!make_map(&wb, false, 2, grad_out, dg, sg, box)) return MGEMM_ECUDA;
+  }
+  if (!make_out_map(&wout, grad_w, (int64_t)E * K, N)) return MGEMM_ECUDA;
+  GemmParams pw{};
+  pw.args = (const uint8_t *)args;
+  pw.E = E;
+  pw.bn = bn_w;
+  pw.idesc = make_idesc(1u, true, true, 128, bn_w);
+  pw.n_tiles = (N + bn_w - 1) / bn_w;
+  pw.mt_k = mt_w;
+  pw.Nout = N;
+  pw.Kout = K;
+  pw.out = (__nv_bfloat16 *)grad_w;
+  if ((int64_t)E * mt_w * pw.n_tiles >= (int64_t(1) << 31)) return MGEMM_EINVAL;
+  return gemm_bf16_dgrad_wgrad(da, db, dout, pd, wa, wb, wout, pw, split, sms, (cudaStream_t)stream);
+}

@@ -15,6 +15,12 @@ int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensor
                        cudaStream_t s) {
   return launch_gemm<GemmCfg<false, true, true, kModeExperts, 256, 3, 4>>(a, b, o, p, grid, s);
 }
+int gemm_bf16_dgrad_wgrad(const CUtensorMap &da, const CUtensorMap &db, const CUtensorMap &dout, const GemmParams &pd,
+                          const CUtensorMap &wa, const CUtensorMap &wb, const CUtensorMap &wout, const GemmParams &pw,
+                          int split, int grid, cudaStream_t s) {
+  return launch_dual<GemmCfg<false, false, false, kModeRows>, GemmCfg<false, true, true, kModeExperts, 256, 3, 4>>(
+      da, db, dout, pd, wa, wb, wout, pw, split, grid, s);
+}
 int gemm_bf16_rows_bmn_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                               int grid, cudaStream_t s) {
   return launch_gemm<GemmCfg<false, false, true, kModeRows, 64, 8>>(a, b, o, p, grid, s);

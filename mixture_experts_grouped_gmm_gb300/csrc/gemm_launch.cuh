@@ -44,6 +44,35 @@ int launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o
                     sfb ? *sfb : a, p);
 }
 
+// Two GEMMs in one launch (mgemm_dual_kernel): split CTAs for the first, the
+// rest of grid for the second
+template <class C0, class C1>
+int launch_dual(const CUtensorMap &a0, const CUtensorMap &b0, const CUtensorMap &o0, const GemmParams &p0,
+                const CUtensorMap &a1, const CUtensorMap &b1, const CUtensorMap &o1, const GemmParams &p1, int split,
+                int grid, cudaStream_t s) {
+  static_assert(!C0::DynRing && !C1::DynRing, "fixed rings");
+  constexpr size_t smem = C0::SMEM_BYTES > C1::SMEM_BYTES ? C0::SMEM_BYTES : C1::SMEM_BYTES;
+  if (split < 1 || split >= grid) return MGEMM_EINVAL;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 0 || dev >= 64) return MGEMM_EINVAL;
+  if (!attr_done[dev]) {
+    rc = cuda_rc(cudaFuncSetAttribute(mgemm_dual_kernel<C0, C1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem),
+                 "cudaFuncSetAttribute");
+    if (rc) return rc;
+    attr_done[dev] = true;
+  }
+  return launch_pdl(mgemm_dual_kernel<C0, C1>, dim3((unsigned)grid), dim3(C0::THREADS), smem, s, 1u,
+                    "grouped GEMM launch (two GEMMs)", a0, b0, o0, a1, b1, o1, p0, p1, split);
+}
+
+// bf16 dgrad (w [E, K, N], 256-wide form) and wgrad in one launch
+int gemm_bf16_dgrad_wgrad(const CUtensorMap &da, const CUtensorMap &db, const CUtensorMap &dout, const GemmParams &pd,
+                          const CUtensorMap &wa, const CUtensorMap &wb, const CUtensorMap &wout, const GemmParams &pw,
+                          int split, int grid, cudaStream_t s);
 // MXFP8: e4m3 x [M, K] and w [E, N, K] with e8m0 scale rows (maps sfa, sfb), 128-wide tiles
 int gemm_fp8_rows_mx(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const CUtensorMap &sfa,
                      const CUtensorMap &sfb, const GemmParams &p, int grid, cudaStream_t s);

@@ -5,8 +5,10 @@ script: ``out = gmm(x, w, batch_sizes)`` followed by ``out.sum().backward()``,
 with batch_sizes resident on the GPU so nothing waits on the host.
 
 Forward: one ``mgemm_fill_args`` (the args block is kept for the backward
-pass) and one ``mgemm_fwd``.  Backward: ``mgemm_dgrad`` and ``mgemm_wgrad``
-reuse the same args block.  This module only allocates outputs with torch and
+pass) and one ``mgemm_fwd``.  Backward: ``mgemm_dgrad_wgrad`` when both
+gradients are wanted and w is [E, K, N] (one launch where the two GEMMs
+overlap), else ``mgemm_dgrad`` / ``mgemm_fwd`` and ``mgemm_wgrad``; all reuse
+the same args block.  This module only allocates outputs with torch and
 calls the binding; every step runs in the CUDA library.
 """
 
@@ -39,6 +41,11 @@ class GroupedGemm(torch.autograd.Function):
         M, K, N, E, trans_b = ctx.dims
         go = grad_out.contiguous()
         gx = gw = None
+        if ctx.needs_input_grad[0] and ctx.needs_input_grad[1] and not trans_b:
+            gx = torch.empty(M, K, dtype=torch.bfloat16, device=x.device)
+            gw = torch.empty(E, K, N, dtype=torch.bfloat16, device=x.device)
+            B.mgemm_dgrad_wgrad(args, go, w, x, gx, gw, M, K, N, E)
+            return gx, gw, None, None
         if ctx.needs_input_grad[0]:
             gx = torch.empty(M, K, dtype=torch.bfloat16, device=x.device)
             if trans_b:   # w[e] is [N, K]: grad_x = grad_out . w[e]

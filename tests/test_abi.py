@@ -89,6 +89,17 @@ def test_host_checks_gemms(lib):
     assert lib.mgemm_wgrad(a, 1, x, s, w, s, o, 64, 128, 256, 4, 64, None) == -1           # fp8 ld < colwise_ld
     assert lib.mgemm_wgrad(a, 1, x, s, w, s, o, 64, 128, 256, 4, 648, None) == -2          # fp8 ld % 16
     assert lib.mgemm_wgrad(a, 0, x, None, w, None, None, 64, 128, 256, 4, 0, None) == -1
+    dw = lib.mgemm_dgrad_wgrad
+    g, gx, gw = P(0x60000), P(0x70000), P(0x80000)
+    assert dw(None, g, w, x, gx, gw, 64, 128, 256, 4, None) == -1                           # no args block
+    assert dw(a, g, None, x, gx, gw, 64, 128, 256, 4, None) == -1                           # no weights
+    assert dw(a, g, w, x, None, gw, 64, 128, 256, 4, None) == -1                            # no grad_x
+    assert dw(a, g, w, x, gx, P(0x80008), 64, 128, 256, 4, None) == -2                      # grad_w alignment
+    assert dw(a, g, w, x, gx, gw, 64, 130, 256, 4, None) == -2                              # K % 8
+    assert dw(a, g, w, x, gx, gw, 64, 128, 256, 2000, None) == -3                           # too many experts
+    assert dw(a, None, w, None, None, None, 0, 128, 256, 4, None) == -1                     # M = 0: grad_w needed
+    sp = lib.mgemm_dgrad_wgrad_split
+    assert sp(64, 128, 256, 0) == -1 and sp(-1, 128, 256, 4) == -1 and sp(64, 128, 256, 2000) == -3
     f = lib.mgemm_fwd_scatter
     m = P(0x60000)
     assert f(a, 1, 1, x, w, o, m, 64, None, 64, 128, 256, 4, None) == -5                  # fp8: not provided

@@ -2,7 +2,8 @@
 host: each pipeline is captured once, then replayed after new inputs --
 including new group sizes and new routing -- are written into the captured
 buffers, and each replay must equal (bit for bit) the same calls run eagerly
-on those inputs.  Covers the bf16 training step (fill, fwd, dgrad, wgrad), the
+on those inputs.  Covers the bf16 training step (fill, fwd, dgrad, wgrad; and
+with the one-launch backward mgemm_dgrad_wgrad), the
 FP8 step (rowwise and dual colwise quantize, fwd, dgrad, wgrad; the colwise
 work counter must come back to 0 between replays) and the routed layer from
 gating logits (routing, alignment, gather, gated GEMM, scattered GEMM, top-k
@@ -66,6 +67,43 @@ def test_bf16_step_graph_replays_with_new_sizes():
         a2 = new_args(E, DEV)
         o2, gx2, gw2 = torch.empty_like(out), torch.empty_like(gx), torch.empty_like(gw)
         step(a2, o2, gx2, gw2)
+        torch.cuda.synchronize()
+        assert torch.equal(out, o2) and torch.equal(gx, gx2) and torch.equal(gw, gw2), f"replay {rep}"
+
+
+def test_bf16_step_one_launch_backward_graph_replays_with_new_sizes():
+    # the same step with mgemm_dgrad_wgrad (its one-launch form at these sizes):
+    # each replay equals the separate calls run eagerly, bit for bit
+    E, M, K, N = 6, 700, 192, 264
+    assert B().mgemm_dgrad_wgrad_split(M, K, N, E) > 0
+    gs = torch.zeros(E, dtype=torch.int64, device=DEV)
+    x = torch.empty(M, K, dtype=BF, device=DEV)
+    w = torch.empty(E, K, N, dtype=BF, device=DEV)
+    go = torch.empty(M, N, dtype=BF, device=DEV)
+    args = new_args(E, DEV)
+    out = torch.empty(M, N, dtype=BF, device=DEV)
+    gx = torch.empty(M, K, dtype=BF, device=DEV)
+    gw = torch.empty(E, K, N, dtype=BF, device=DEV)
+
+    def step():
+        B().mgemm_fill_args(gs, E, M, args)
+        B().mgemm_fwd(args, 0, 0, x, None, w, None, out, M, K, N, E)
+        B().mgemm_dgrad_wgrad(args, go, w, x, gx, gw, M, K, N, E)
+
+    graph = capture(step)
+    for rep, sizes in enumerate(([100, 0, 250, 50, 300, 0], [0, 700, 0, 0, 0, 0], [117, 117, 117, 117, 116, 116])):
+        gs.copy_(torch.tensor(sizes, dtype=torch.int64))
+        x.copy_(torch.randn(M, K, device=DEV).to(BF))
+        w.copy_(torch.randn(E, K, N, device=DEV).to(BF))
+        go.copy_(torch.randn(M, N, device=DEV).to(BF))
+        graph.replay()
+        torch.cuda.synchronize()
+        a2 = new_args(E, DEV)
+        o2, gx2, gw2 = torch.empty_like(out), torch.empty_like(gx), torch.empty_like(gw)
+        B().mgemm_fill_args(gs, E, M, a2)
+        B().mgemm_fwd(a2, 0, 0, x, None, w, None, o2, M, K, N, E)
+        B().mgemm_dgrad(a2, 0, go, None, w, None, gx2, M, K, N, E)
+        B().mgemm_wgrad(a2, 0, x, None, go, None, gw2, M, K, N, E)
         torch.cuda.synchronize()
         assert torch.equal(out, o2) and torch.equal(gx, gx2) and torch.equal(gw, gw2), f"replay {rep}"
 
