@@ -621,7 +621,7 @@ extern "C" int mgemm_wgrad(const void *args, int dtype, const void *x, const flo
 }
 
 // CTAs given to dgrad when it shares one launch with wgrad, or 0 when two
-// launches are expected to do as well.  A makespan model with rates measured
+// launches are expected to do about as well.  A makespan model with rates measured
 // on GB300 for the bf16 forms: a wgrad tile's epilogue stores ~34 GB/s of
 // grad_w per SM; a dgrad CTA streams weights at up to ~60 GB/s; HBM serves
 // ~6 TB/s to both; the tensor cores give ~12 TFLOP/s per SM.  Only the
@@ -652,7 +652,9 @@ static int dual_split(int64_t M, int K, int N, int E, int bn_d, int bn_w, int sm
       best = g;
     }
   }
-  return best;
+  // the model's ratio of the two forms was off by up to ~6% on a sweep of
+  // shapes: take the one-launch form only for a larger predicted gain
+  return best_t < 0.94 * seq ? best : 0;
 }
 
 extern "C" int mgemm_dgrad_wgrad_split(int64_t M, int K, int N, int E) {

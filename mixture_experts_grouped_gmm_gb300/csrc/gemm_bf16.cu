@@ -18,8 +18,16 @@ int gemm_bf16_experts(const CUtensorMap &a, const CUtensorMap &b, const CUtensor
 int gemm_bf16_dgrad_wgrad(const CUtensorMap &da, const CUtensorMap &db, const CUtensorMap &dout, const GemmParams &pd,
                           const CUtensorMap &wa, const CUtensorMap &wb, const CUtensorMap &wout, const GemmParams &pw,
                           int split, int grid, cudaStream_t s) {
-  return launch_dual<GemmCfg<false, false, false, kModeRows>, GemmCfg<false, true, true, kModeExperts, 256, 3, 4>>(
-      da, db, dout, pd, wa, wb, wout, pw, split, grid, s);
+  // the dgrad half takes the form mgemm_dgrad would launch for its tile width
+  // (a deeper ring for narrower tiles: more weight bytes in flight per SM)
+  using W = GemmCfg<false, true, true, kModeExperts, 256, 3, 4>;
+  if (pd.bn <= 64)
+    return launch_dual<GemmCfg<false, false, false, kModeRows, 64, 8>, W>(da, db, dout, pd, wa, wb, wout, pw, split,
+                                                                          grid, s);
+  if (pd.bn <= 128)
+    return launch_dual<GemmCfg<false, false, false, kModeRows, 128, 6>, W>(da, db, dout, pd, wa, wb, wout, pw, split,
+                                                                           grid, s);
+  return launch_dual<GemmCfg<false, false, false, kModeRows>, W>(da, db, dout, pd, wa, wb, wout, pw, split, grid, s);
 }
 int gemm_bf16_rows_bmn_narrow(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const GemmParams &p,
                               int grid, cudaStream_t s) {

@@ -69,7 +69,7 @@ int launch_dual(const CUtensorMap &a0, const CUtensorMap &b0, const CUtensorMap 
                     "grouped GEMM launch (two GEMMs)", a0, b0, o0, a1, b1, o1, p0, p1, split);
 }
 
-// bf16 dgrad (w [E, K, N], 256-wide form) and wgrad in one launch
+// bf16 dgrad (w [E, K, N]; the 64-, 128- or 256-wide form by pd.bn) and wgrad in one launch
 int gemm_bf16_dgrad_wgrad(const CUtensorMap &da, const CUtensorMap &db, const CUtensorMap &dout, const GemmParams &pd,
                           const CUtensorMap &wa, const CUtensorMap &wb, const CUtensorMap &wout, const GemmParams &pw,
                           int split, int grid, cudaStream_t s);

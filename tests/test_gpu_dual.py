@@ -108,6 +108,9 @@ def test_dgrad_wgrad_split_at_grin_size():
     # GRIN-MoE gmm (M = 1024, K = 4096, N = 6400, E = 8): 128 dgrad tiles, two per dgrad CTA
     split = B().mgemm_dgrad_wgrad_split(1024, 4096, 6400, 8)
     assert split == 64, split
+    # predicted gains below 6% take the two calls (measured there: the one launch 6% / 1% slower)
+    assert B().mgemm_dgrad_wgrad_split(1024, 1024, 6400, 8) == 0
+    assert B().mgemm_dgrad_wgrad_split(4096, 2048, 1536, 16) == 0
 
 
 def test_dgrad_wgrad_bad_status_writes_nothing():
