@@ -1156,11 +1156,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   gemm_cta<C>(tmA, tmB, tmOut, tmSFA, tmSFB, p, (int)blockIdx.x, (int)gridDim.x);
 }
 
-// Two GEMMs of one backward pass in one launch: CTAs [0, split) run the
-// first (C0, maps a0 b0 o0, params p0), the others the second.  Neither reads
-// what the other writes; a memory-bound weight stream (dgrad) and an
+// Two GEMMs of one backward pass in one launch: split of the grid's CTAs run
+// the first (C0, maps a0 b0 o0, params p0), the others the second.  Neither
+// reads what the other writes; a memory-bound weight stream (dgrad) and an
 // epilogue-bound one (wgrad's grad_w stores) then share the SMs and HBM
-// instead of taking turns.
+// instead of taking turns.  The first GEMM's CTAs are spread evenly over the
+// block indices (CTA b is one of them when floor((b + 1) split / grid) >
+// floor(b split / grid); its index among them is floor(b split / grid)), so
+// neither half is packed onto a few GPCs whatever order the CTAs are placed
+// in.
 template <class C0, class C1>
 __global__ void __launch_bounds__(C0::THREADS, 1)
     mgemm_dual_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap b0,
@@ -1169,10 +1173,12 @@ __global__ void __launch_bounds__(C0::THREADS, 1)
                       const __grid_constant__ GemmParams p0, const __grid_constant__ GemmParams p1, int split) {
   static_assert(C0::THREADS == C1::THREADS && !C0::Pair && !C1::Pair && !C0::Mx && !C1::Mx,
                 "both forms run the same warps, one CTA each");
-  if ((int)blockIdx.x < split)
-    gemm_cta<C0>(a0, b0, o0, a0, a0, p0, (int)blockIdx.x, split);
+  const int b = (int)blockIdx.x, g = (int)gridDim.x;
+  const int lo = (int)((int64_t)b * split / g), hi = (int)((int64_t)(b + 1) * split / g);
+  if (hi > lo)
+    gemm_cta<C0>(a0, b0, o0, a0, a0, p0, lo, split);
   else
-    gemm_cta<C1>(a1, b1, o1, a1, a1, p1, (int)blockIdx.x - split, (int)gridDim.x - split);
+    gemm_cta<C1>(a1, b1, o1, a1, a1, p1, b - lo, g - split);
 }
 
 }  // namespace mgemm
