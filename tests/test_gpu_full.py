@@ -51,10 +51,18 @@ def test_grin_fwd_bwd_full_size():
     gx = torch.empty(M, K, dtype=BF, device=DEV)
     gw = torch.empty(E, K, N, dtype=BF, device=DEV)
     go = torch.ones(M, N, dtype=BF, device=DEV)          # loss = out.sum()
+    # the bench's launches: fill, fwd, and the backward in one launch
+    assert B().mgemm_dgrad_wgrad_split(M, K, N, E) > 0
     B().mgemm_fwd(args, 0, 0, d["x"], None, d["w"], None, out, M, K, N, E)
-    B().mgemm_dgrad(args, 0, go, None, d["w"], None, gx, M, K, N, E)
-    B().mgemm_wgrad(args, 0, d["x"], None, go, None, gw, M, K, N, E)
+    B().mgemm_dgrad_wgrad(args, go, d["w"], d["x"], gx, gw, M, K, N, E)
     torch.cuda.synchronize()
+    # bit for bit the two separate calls
+    gx2, gw2 = torch.empty_like(gx), torch.empty_like(gw)
+    B().mgemm_dgrad(args, 0, go, None, d["w"], None, gx2, M, K, N, E)
+    B().mgemm_wgrad(args, 0, d["x"], None, go, None, gw2, M, K, N, E)
+    torch.cuda.synchronize()
+    assert torch.equal(gx, gx2) and torch.equal(gw, gw2)
+    del gx2, gw2
     rows = sample_rows(sizes, 4)
     rt = torch.as_tensor(rows, device=DEV)
     sub = rows_by_expert(sizes, rows)
